@@ -1,0 +1,149 @@
+"""Float64 CPU oracle for the selective scan (S6) — TEST INFRASTRUCTURE ONLY.
+
+Only `tests/`, `__graft_entry__.smoke()` and the benchmark's CPU-baseline leg
+may import this package. The product path (the CUDA library and its binding)
+never imports, links or runs it.
+
+The arithmetic lives in `ss_oracle.c` (plain sequential float64 loops, see its
+header for the definition and the passages it follows); this module only
+marshals host tensors into that library. Inputs are the exact stored values
+(fp32, or bf16 bit patterns widened exactly to float64 inside the C code).
+
+Every function here is pinned by the `-m "not gpu"` tests in
+tests/test_oracle_pins.py (brute-force unrolled sum, LTI convolution checked
+directly and by FFT, delta->0, large delta, chunk associativity, geometric
+closed form, hand-computed L=1, zero/linearity/independence properties,
+decode-equals-scan).
+"""
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIBS = {}
+
+_I64 = ctypes.c_int64
+_P = ctypes.c_void_p
+
+
+def load(path: str = None) -> ctypes.CDLL:
+    """Load (building if needed) the oracle library; `path` selects another build."""
+    path = path or _build.build()
+    if path not in _LIBS:
+        lib = ctypes.CDLL(path)
+        lib.ss_oracle_scan.restype = ctypes.c_int
+        lib.ss_oracle_scan.argtypes = [_I64, _I64, _I64, _I64, ctypes.c_int,
+                                       _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _I64, _P, _P, ctypes.c_int]
+        lib.ss_oracle_state_update.restype = ctypes.c_int
+        lib.ss_oracle_state_update.argtypes = [_I64, _I64, _I64, ctypes.c_int, _P,
+                                               _P, _P, _P, _P, _P, _P, _P, _P,
+                                               _P, _I64, _P]
+        _LIBS[path] = lib
+    return _LIBS[path]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"oracle inputs must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    assert t.device.type == "cpu" and t.is_contiguous()
+    return t.data_ptr()
+
+
+def _f32(t):
+    if t is None:
+        return None
+    assert t.dtype == torch.float32
+    return t.contiguous()
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def scan(x: dict, channels=None, nthreads: int = None, lib_path: str = None):
+    """Selective scan in float64 on the host.
+
+    x: dict of CPU tensors u, delta_raw, z (or None) [Bt, L, D]; B, C [Bt, L, N]
+       (all float32 or all bfloat16); A [D, N], D [D] or None, delta_bias [D] or
+       None, h0 [Bt, D, N] or None (float32).
+    channels: None for every (b, d), or an int array [n, 2] of (b, d) pairs.
+    Returns (y, h_last) as float64 numpy arrays: y [Bt, L, D] and h [Bt, D, N]
+    for the full problem, else y [n, L] and h [n, N] for the listed channels.
+    """
+    lib = load(lib_path)
+    u, dr, z, B, C = x["u"], x["delta_raw"], x.get("z"), x["B"], x["C"]
+    Bt, L, Dm = u.shape
+    N = B.shape[-1]
+    code = _dtype_code(u)
+    for t in (dr, z, B, C):
+        if t is not None and _dtype_code(t) != code:
+            raise TypeError("u, delta_raw, z, B, C must share one dtype")
+    A = _f32(x["A"])
+    Dk = _f32(x.get("D"))
+    bias = _f32(x.get("delta_bias"))
+    h0 = _f32(x.get("h0"))
+    full = channels is None
+    if full:
+        bb, dd = np.meshgrid(np.arange(Bt), np.arange(Dm), indexing="ij")
+        chans = np.stack([bb.ravel(), dd.ravel()], axis=1).astype(np.int64)
+    else:
+        chans = np.ascontiguousarray(np.asarray(channels, dtype=np.int64).reshape(-1, 2))
+    n = chans.shape[0]
+    y = np.zeros((n, L), dtype=np.float64)
+    h = np.zeros((n, N), dtype=np.float64)
+    rc = lib.ss_oracle_scan(Bt, L, Dm, N, code, _ptr(u), _ptr(dr), _ptr(z), _ptr(B), _ptr(C),
+                            _ptr(A), _ptr(Dk), _ptr(bias), _ptr(h0),
+                            chans.ctypes.data, n, y.ctypes.data, h.ctypes.data,
+                            nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle scan rejected its arguments")
+    if full:
+        return y.reshape(Bt, Dm, L).transpose(0, 2, 1).copy(), h.reshape(Bt, Dm, N)
+    return y, h
+
+
+def state_update(h: np.ndarray, x: dict, channels=None, lib_path: str = None):
+    """One decode step in float64, state updated in place.
+
+    h: float64 numpy array [S, D, N] (modified); x: dict of CPU tensors u,
+    delta_raw, z (or None) [S, D]; B, C [S, N]; A [D, N], D, delta_bias [D].
+    Returns y as float64 [S, D] (full) or [n] for listed (b, d) channels.
+    """
+    lib = load(lib_path)
+    u, dr, z, B, C = x["u"], x["delta_raw"], x.get("z"), x["B"], x["C"]
+    S, Dm = u.shape
+    N = B.shape[-1]
+    code = _dtype_code(u)
+    assert h.dtype == np.float64 and h.flags.c_contiguous and h.shape == (S, Dm, N)
+    full = channels is None
+    if full:
+        bb, dd = np.meshgrid(np.arange(S), np.arange(Dm), indexing="ij")
+        chans = np.stack([bb.ravel(), dd.ravel()], axis=1).astype(np.int64)
+    else:
+        chans = np.ascontiguousarray(np.asarray(channels, dtype=np.int64).reshape(-1, 2))
+    n = chans.shape[0]
+    y = np.zeros(n, dtype=np.float64)
+    rc = lib.ss_oracle_state_update(S, Dm, N, code, h.ctypes.data, _ptr(u), _ptr(dr), _ptr(z),
+                                    _ptr(B), _ptr(C), _ptr(_f32(x["A"])), _ptr(_f32(x.get("D"))),
+                                    _ptr(_f32(x.get("delta_bias"))), chans.ctypes.data, n,
+                                    y.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle state_update rejected its arguments")
+    return y.reshape(S, Dm) if full else y

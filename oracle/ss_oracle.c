@@ -1,0 +1,188 @@
+/*
+ * CPU oracle for the selective state-space scan (S6) — TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, sequential float64 restatement of what the selective scan
+ * computes. Only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg may load this library; the product path never does.
+ *
+ * Definition followed (float64 throughout, inputs widened exactly):
+ *   for each batch b and channel d, with h_n <- h0[b,d,n] (0 when absent),
+ *   for t = 0 .. L-1:
+ *     delta = softplus(delta_raw[b,t,d] + bias[d])
+ *     for each state n:
+ *       h_n = exp(delta * A[d,n]) * h_n + delta * B[b,t,n] * u[b,t,d]
+ *     y   = sum_n C[b,t,n] * h_n + D[d] * u[b,t,d]
+ *     out[b,t,d] = y * z / (1 + exp(-z))        (z = z[b,t,d], when z is given)
+ *   h_last[b,d,n] = h_n after the last step.
+ *
+ * Sources (page titles and sections):
+ *  - discretised recurrence h_t = Abar h_{t-1} + Bbar x_t, y_t = C h_t + D x_t:
+ *    "Transformer时代终结？Mamba的状态空间革命重塑AI底层架构", section 二.1
+ *    (continuous system and its discretisation);
+ *  - Abar = exp(delta*A) (zero-order hold) and the first-order Bbar ~= delta*B:
+ *    "外文文献精读：Mamba - 线性时间序列建模与结构化状态空间模型", section 1.2,
+ *    and the mlqm.cn SSM tutorial (untitled in the capture), section 3.2
+ *    (discretisation) and the section 9.2 step sketch, which computes
+ *    dA = exp(dt*A), dB = dt*B and y = (h*C).sum + D*x;
+ *  - delta, B, C as functions of the input, B and C shared by all channels:
+ *    mlqm.cn tutorial, sections 5.2 and 9.2 (Bk, Ck have shape (d_state,));
+ *  - A = -exp(A_log): "外文文献精读" page, section 4.1 (stability);
+ *  - SiLU output gate: review page ("Mamba: Linear-Time Sequence Modeling with
+ *    Selective State Spaces"), method step 3, and mlqm.cn tutorial section 7.1;
+ *  - softplus for delta: not printed on the pages; taken as
+ *    softplus(x) = log(1 + e^x), evaluated without overflow;
+ *  - single-token decode = the same step with L = 1 and h carried in place:
+ *    "AI 推理系列（十四）：Mamba 的 Selective State Space", section
+ *    "Selective Scan 如何兼顾训练与 Decode".
+ *
+ * Parity pins live in the tests (brute-force unrolled sum, LTI convolution,
+ * delta->0, large delta, chunk associativity, closed forms).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* dtype codes of the raw input arrays */
+#define ORC_F32 0
+#define ORC_BF16 1
+
+static double widen(const void *p, int dtype, int64_t i) {
+  if (dtype == ORC_F32) return (double)((const float *)p)[i];
+  /* bfloat16: the upper 16 bits of an IEEE binary32 value */
+  uint32_t bits = (uint32_t)((const uint16_t *)p)[i] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+static double softplus(double x) {
+  /* log(1 + e^x) without overflow: for x > 0 use x + log(1 + e^-x) */
+  if (x > 0) return x + log1p(exp(-x));
+  return log1p(exp(x));
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+typedef struct {
+  int64_t batch, seqlen, dim, dstate;
+  int in_dtype;
+  const void *u, *delta_raw, *z, *B, *C;
+  const float *A, *Dskip, *bias, *h0;
+  const int64_t *chans; /* (b, d) pairs, 2 per channel */
+  int64_t n_chan;
+  double *y;      /* [n_chan][seqlen] */
+  double *h_last; /* [n_chan][dstate] */
+  int64_t next;   /* work counter */
+  pthread_mutex_t mu;
+} scan_job;
+
+static void scan_one(const scan_job *j, int64_t c) {
+  const int64_t L = j->seqlen, Dm = j->dim, N = j->dstate;
+  const int64_t b = j->chans[2 * c], d = j->chans[2 * c + 1];
+  double *h = (double *)malloc(sizeof(double) * (size_t)N);
+  for (int64_t n = 0; n < N; n++) h[n] = j->h0 ? (double)j->h0[(b * Dm + d) * N + n] : 0.0;
+  const double bias = j->bias ? (double)j->bias[d] : 0.0;
+  const double dsk = j->Dskip ? (double)j->Dskip[d] : 0.0;
+  for (int64_t t = 0; t < L; t++) {
+    const int64_t i = (b * L + t) * Dm + d;     /* [b][t][d] */
+    const int64_t r = (b * L + t) * N;          /* [b][t][n] row */
+    const double delta = softplus(widen(j->delta_raw, j->in_dtype, i) + bias);
+    const double x = widen(j->u, j->in_dtype, i);
+    double y = 0.0;
+    for (int64_t n = 0; n < N; n++) {
+      const double abar = exp(delta * (double)j->A[d * N + n]);
+      const double bbar_x = delta * widen(j->B, j->in_dtype, r + n) * x;
+      h[n] = abar * h[n] + bbar_x;
+      y += widen(j->C, j->in_dtype, r + n) * h[n];
+    }
+    y += dsk * x;
+    if (j->z) y *= silu(widen(j->z, j->in_dtype, i));
+    j->y[c * L + t] = y;
+  }
+  for (int64_t n = 0; n < N; n++) j->h_last[c * N + n] = h[n];
+  free(h);
+}
+
+static void *scan_worker(void *arg) {
+  scan_job *j = (scan_job *)arg;
+  for (;;) {
+    pthread_mutex_lock(&j->mu);
+    int64_t c = j->next++;
+    pthread_mutex_unlock(&j->mu);
+    if (c >= j->n_chan) break;
+    scan_one(j, c);
+  }
+  return NULL;
+}
+
+/*
+ * Selective scan over the channels listed in `chans` ((b, d) pairs).
+ * u, delta_raw, z: [batch][seqlen][dim]; B, C: [batch][seqlen][dstate] in
+ * in_dtype; A: [dim][dstate]; Dskip, bias: [dim] or NULL; h0:
+ * [batch][dim][dstate] or NULL; z NULL means no gate.
+ * Writes y[c][t] and h_last[c][n] for listed channel c. Returns 0, or -1 on
+ * a bad argument.
+ */
+int ss_oracle_scan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int in_dtype,
+                   const void *u, const void *delta_raw, const void *z, const void *B,
+                   const void *C, const float *A, const float *Dskip, const float *bias,
+                   const float *h0, const int64_t *chans, int64_t n_chan, double *y,
+                   double *h_last, int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0 || n_chan < 0) return -1;
+  if (in_dtype != ORC_F32 && in_dtype != ORC_BF16) return -1;
+  if (!u || !delta_raw || !B || !C || !A || !chans || !y || !h_last) return -1;
+  for (int64_t c = 0; c < n_chan; c++)
+    if (chans[2 * c] < 0 || chans[2 * c] >= batch || chans[2 * c + 1] < 0 || chans[2 * c + 1] >= dim)
+      return -1;
+  scan_job j;
+  memset(&j, 0, sizeof j);
+  j.batch = batch; j.seqlen = seqlen; j.dim = dim; j.dstate = dstate; j.in_dtype = in_dtype;
+  j.u = u; j.delta_raw = delta_raw; j.z = z; j.B = B; j.C = C;
+  j.A = A; j.Dskip = Dskip; j.bias = bias; j.h0 = h0;
+  j.chans = chans; j.n_chan = n_chan; j.y = y; j.h_last = h_last; j.next = 0;
+  pthread_mutex_init(&j.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int started = 0;
+  for (int k = 1; k < nthreads; k++)
+    if (pthread_create(&th[started], NULL, scan_worker, &j) == 0) started++;
+  scan_worker(&j);
+  for (int k = 0; k < started; k++) pthread_join(th[k], NULL);
+  pthread_mutex_destroy(&j.mu);
+  return 0;
+}
+
+/*
+ * One decode step for the listed channels, state carried in place:
+ * h: [batch][dim][dstate] float64, updated; u, delta_raw, z: [batch][dim];
+ * B, C: [batch][dstate]; writes y[c] for listed channel c.
+ */
+int ss_oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, int in_dtype, double *h,
+                           const void *u, const void *delta_raw, const void *z, const void *B,
+                           const void *C, const float *A, const float *Dskip, const float *bias,
+                           const int64_t *chans, int64_t n_chan, double *y) {
+  if (batch < 0 || dim < 0 || dstate <= 0 || n_chan < 0) return -1;
+  if (in_dtype != ORC_F32 && in_dtype != ORC_BF16) return -1;
+  if (!h || !u || !delta_raw || !B || !C || !A || !chans || !y) return -1;
+  for (int64_t c = 0; c < n_chan; c++) {
+    const int64_t b = chans[2 * c], d = chans[2 * c + 1];
+    if (b < 0 || b >= batch || d < 0 || d >= dim) return -1;
+    const int64_t i = b * dim + d;
+    const double delta = softplus(widen(delta_raw, in_dtype, i) + (bias ? (double)bias[d] : 0.0));
+    const double x = widen(u, in_dtype, i);
+    double *hs = h + i * dstate;
+    double acc = 0.0;
+    for (int64_t n = 0; n < dstate; n++) {
+      hs[n] = exp(delta * (double)A[d * dstate + n]) * hs[n] +
+              delta * widen(B, in_dtype, b * dstate + n) * x;
+      acc += widen(C, in_dtype, b * dstate + n) * hs[n];
+    }
+    acc += (Dskip ? (double)Dskip[d] : 0.0) * x;
+    if (z) acc *= silu(widen(z, in_dtype, i));
+    y[c] = acc;
+  }
+  return 0;
+}

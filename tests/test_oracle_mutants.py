@@ -1,0 +1,62 @@
+"""Planted mistakes in the oracle (on the CPU): every plausible slip in the
+recurrence must make at least one pin fail. Each mutant is a textual edit of a
+temporary copy of oracle/ss_oracle.c, compiled separately; the committed
+oracle is never modified."""
+
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import pins
+from oracle import build as obuild
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(os.path.dirname(HERE), "oracle", "ss_oracle.c")
+
+MUTANTS = {
+    "exp_sign": ("exp(delta * (double)j->A[d * N + n])", "exp(-delta * (double)j->A[d * N + n])"),
+    "drop_skip": ("y += dsk * x;", "y += 0.0 * dsk * x;"),
+    "readout_uses_B": ("y += widen(j->C, j->in_dtype, r + n) * h[n];", "y += widen(j->B, j->in_dtype, r + n) * h[n];"),
+    "gate_without_sigmoid": ("if (j->z) y *= silu(", "if (j->z) y *= (1.0 + 0.0 * "),
+    "drop_bias": ("softplus(widen(j->delta_raw, j->in_dtype, i) + bias)", "softplus(widen(j->delta_raw, j->in_dtype, i))"),
+    "A_transposed": ("(double)j->A[d * N + n]", "(double)j->A[(n * Dm + d) % (Dm * N)]"),
+    "softplus_is_exp": ("return log1p(exp(x));", "return exp(x);"),
+    "h0_ignored": ("h[n] = j->h0 ? (double)j->h0[(b * Dm + d) * N + n] : 0.0;", "h[n] = 0.0;"),
+    "bbar_without_delta": ("const double bbar_x = delta * widen(j->B", "const double bbar_x = 1.0 * widen(j->B"),
+    "B_time_lag": ("const int64_t r = (b * L + t) * N;", "const int64_t r = (b * L + (t > 0 ? t - 1 : 0)) * N;"),
+    "readout_before_update": ("h[n] = abar * h[n] + bbar_x;\n      y += widen(j->C, j->in_dtype, r + n) * h[n];",
+                              "y += widen(j->C, j->in_dtype, r + n) * h[n];\n      h[n] = abar * h[n] + bbar_x;"),
+    "skip_outside_gate": ("    y += dsk * x;\n    if (j->z) y *= silu(widen(j->z, j->in_dtype, i));",
+                          "    if (j->z) y *= silu(widen(j->z, j->in_dtype, i));\n    y += dsk * x;"),
+    "batch_stride_B": ("const int64_t r = (b * L + t) * N;", "const int64_t r = (t) * N;"),
+    "decode_exp_sign": ("hs[n] = exp(delta * (double)A[d * dstate + n]) * hs[n] +",
+                        "hs[n] = exp(-delta * (double)A[d * dstate + n]) * hs[n] +"),
+}
+
+
+@pytest.fixture(scope="module")
+def tmpdir_mod():
+    d = tempfile.mkdtemp(prefix="ss_oracle_mut_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmpdir_mod):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    csrc = os.path.join(tmpdir_mod, f"{name}.c")
+    with open(csrc, "w") as f:
+        f.write(mutated)
+    lib = obuild.build(csrc, os.path.join(tmpdir_mod, f"lib_{name}.so"), extra=("-Wno-unused",))
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"

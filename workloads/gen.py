@@ -1,0 +1,142 @@
+"""Seeded generation of host (CPU) input tensors.
+
+Every tensor is drawn from torch's CPU generator in fixed-size blocks; block k
+of stream s under seed `seed` uses its own generator seeded from (seed, s, k),
+so the values do not depend on the thread count and any block can be drawn on
+its own. Values are drawn in float64/float32 and rounded once to the storage
+dtype (bf16 by round-to-nearest-even via torch). Both the oracle and the GPU
+path receive exactly these stored values.
+"""
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import torch
+
+from .configs import ScanWorkload, DecodeWorkload
+
+BLOCK = 1 << 22
+
+# stream ids (one per drawn tensor)
+S_DT, S_ALOG, S_U, S_DRAW, S_Z, S_B, S_C, S_SYM, S_EMB = range(9)
+
+
+def _block_seed(seed: int, stream: int, block: int) -> int:
+    return (seed * 1_000_003 + stream * 10_007 + block * 7_919 + 12_345) % (1 << 62)
+
+
+def randn_blocks(numel: int, seed: int, stream: int, threads: int = 0) -> torch.Tensor:
+    """numel standard-normal float32 values, drawn block by block."""
+    out = torch.empty(numel, dtype=torch.float32)
+    nblk = (numel + BLOCK - 1) // BLOCK
+
+    def fill(k):
+        g = torch.Generator().manual_seed(_block_seed(seed, stream, k))
+        lo, hi = k * BLOCK, min(numel, (k + 1) * BLOCK)
+        out[lo:hi] = torch.randn(hi - lo, generator=g, dtype=torch.float32)
+
+    if nblk <= 1:
+        for k in range(nblk):
+            fill(k)
+    else:
+        n = threads or min(32, os.cpu_count() or 1)
+        with ThreadPoolExecutor(n) as ex:
+            list(ex.map(fill, range(nblk)))
+    return out
+
+
+def _store(x: torch.Tensor, dtype: str) -> torch.Tensor:
+    if dtype == "bf16":
+        return x.to(torch.bfloat16)
+    if dtype == "f32":
+        return x.to(torch.float32)
+    raise ValueError(dtype)
+
+
+def make_params(w: ScanWorkload):
+    """Per-layer fp32 parameters A [D,N], D_skip [D], delta_bias [D].
+
+    dt_d is log-uniform in [dt_min, dt_max]; delta_bias = softplus^{-1}(dt_d)
+    = log(expm1(dt_d)); A_log[d, n] = log(n+1) (+ jitter); A = -exp(A_log),
+    rounded once to fp32.
+    """
+    D, N = w.dim, w.dstate
+    g = torch.Generator().manual_seed(_block_seed(w.seed, S_DT, 0))
+    r = torch.rand(D, generator=g, dtype=torch.float64)
+    dt = torch.exp(math.log(w.dt_min) + r * (math.log(w.dt_max) - math.log(w.dt_min)))
+    bias = torch.log(torch.expm1(dt)).to(torch.float32)
+    a_log = torch.log(torch.arange(1, N + 1, dtype=torch.float64)).expand(D, N).clone()
+    if w.a_log_jitter:
+        g2 = torch.Generator().manual_seed(_block_seed(w.seed, S_ALOG, 0))
+        a_log += w.a_log_jitter * torch.randn(D, N, generator=g2, dtype=torch.float64)
+    A = (-torch.exp(a_log)).to(torch.float32).contiguous()
+    Dskip = torch.ones(D, dtype=torch.float32)
+    return A, Dskip, bias
+
+
+def make_scan_inputs(w: ScanWorkload, seed: int = None) -> dict:
+    """Host tensors for one ss_scan_fwd call (contiguous, row-major):
+    u, delta_raw, z: [Bt, L, D]; B, C: [Bt, L, N] in w.in_dtype;
+    A: [D, N], D: [D], delta_bias: [D] float32."""
+    s = w.seed if seed is None else seed
+    Bt, L, D, N = w.batch, w.seqlen, w.dim, w.dstate
+    A, Dskip, bias = make_params(w)
+    n_td = Bt * L * D
+    if w.u_kind == "normal":
+        u = randn_blocks(n_td, s, S_U).view(Bt, L, D)
+    elif w.u_kind == "alphabet4":
+        g = torch.Generator().manual_seed(_block_seed(s, S_EMB, 0))
+        emb = torch.randn(4, D, generator=g, dtype=torch.float32)
+        g2 = torch.Generator().manual_seed(_block_seed(s, S_SYM, 0))
+        sym = torch.randint(0, 4, (Bt, L), generator=g2)
+        u = emb[sym]  # [Bt, L, D]
+    else:
+        raise ValueError(w.u_kind)
+    out = {
+        "u": _store(u, w.in_dtype).contiguous(),
+        "delta_raw": _store(w.delta_raw_scale * randn_blocks(n_td, s, S_DRAW).view(Bt, L, D),
+                            w.in_dtype).contiguous(),
+        "z": _store(randn_blocks(n_td, s, S_Z).view(Bt, L, D), w.in_dtype).contiguous() if w.has_z else None,
+        "B": _store(randn_blocks(Bt * L * N, s, S_B).view(Bt, L, N), w.in_dtype).contiguous(),
+        "C": _store(randn_blocks(Bt * L * N, s, S_C).view(Bt, L, N), w.in_dtype).contiguous(),
+        "A": A,
+        "D": Dskip if w.has_d else None,
+        "delta_bias": bias,
+    }
+    return out
+
+
+def make_decode_steps(w: DecodeWorkload, first: int, count: int) -> dict:
+    """Inputs of decode steps [first, first+count): u, delta_raw, z [count, S, D],
+    B, C [count, S, N] in w.in_dtype. Step k draws from its own streams, so any
+    range of steps can be generated alone."""
+    S, D, N = w.streams, w.dim, w.dstate
+    us, ds, zs, bs, cs = [], [], [], [], []
+    for k in range(first, first + count):
+        sk = w.seed * 100_003 + k
+        us.append(_store(randn_blocks(S * D, sk, S_U).view(S, D), w.in_dtype))
+        ds.append(_store(w.delta_raw_scale * randn_blocks(S * D, sk, S_DRAW).view(S, D), w.in_dtype))
+        zs.append(_store(randn_blocks(S * D, sk, S_Z).view(S, D), w.in_dtype))
+        bs.append(_store(randn_blocks(S * N, sk, S_B).view(S, N), w.in_dtype))
+        cs.append(_store(randn_blocks(S * N, sk, S_C).view(S, N), w.in_dtype))
+    return {
+        "u": torch.stack(us).contiguous(),
+        "delta_raw": torch.stack(ds).contiguous(),
+        "z": torch.stack(zs).contiguous(),
+        "B": torch.stack(bs).contiguous(),
+        "C": torch.stack(cs).contiguous(),
+    }
+
+
+def random_scan_inputs(batch, seqlen, dim, dstate, in_dtype="f32", seed=0, delta_raw_scale=0.5,
+                       a_log_jitter=0.0, has_z=True, has_d=True, with_h0=False):
+    """Small ad-hoc problems (edge shapes for tests) with the c0 recipe."""
+    w = ScanWorkload("adhoc", batch, seqlen, dim, dstate, in_dtype, seed, delta_raw_scale,
+                     a_log_jitter, has_z=has_z, has_d=has_d)
+    x = make_scan_inputs(w)
+    if with_h0:
+        x["h0"] = randn_blocks(batch * dim * dstate, seed, 99).view(batch, dim, dstate).contiguous()
+    else:
+        x["h0"] = None
+    return x
