@@ -1,0 +1,495 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 selective-scan (S6) hot path.
+
+One step = one ss_scan_fwd pass over the Mamba-2.8B-shaped layer workload
+(batch 4, L 2048, d_inner 5120, d_state 16, bf16 inputs and output, fp32
+state), inputs resident in HBM. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (launched by torch.distributed.run): every rank processes its own
+copy of the workload (independent batches, no data-path collective; weak
+scaling); the timed region is bracketed by barriers and the slowest rank's
+time is taken.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import configs, gen  # noqa: E402
+
+METRIC = "selective-scan HBM GB/s (% of B300 peak) & channel-tokens/s; decode steps/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "sm_max_mhz": 2032.0}
+KERNEL_SOURCES = ["selective_state_space_130_b300/csrc/ss_scan_fwd.cu",
+                  "selective_state_space_130_b300/csrc/ss_device.cuh",
+                  "selective_state_space_130_b300/csrc/ss_internal.h"]
+SCAN_PROFILE = "profiles/ss_scan_fwd_mamba2p8b_layer.md"
+# Issue-bound compute roof of the state update: each (t, d, n) needs at least
+# 4 fp32 pipe ops (delta*A, (delta*u)*B, the h FMA, the C.h FMA) and one MUFU
+# ex2, each one issue slot; an SM issues 4 warp-instructions (128 lane-ops)
+# per clock, so at most 128 / 5 = 25.6 state updates per clock per SM.
+STATE_UPDATES_PER_CLK_SM = 128.0 / 5.0
+SMS = 148
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ setup
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, local):
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region (read-only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def sources_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, SCAN_PROFILE)
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != sources_sha():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ our arm
+def to_dev(x, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def scan_call(ss, d, y, h, ws):
+    ss.ss_scan_fwd(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], None,
+                   y=y, h_last=h, workspace=ws)
+
+
+def bench_scan(ss, w, x, steps, warmup, out_dtype, dev, nsets=None):
+    """Device-resident timing. Input sets rotate so consecutive steps never
+    find their inputs in L2 (each set is larger than L2 or sets are cycled
+    until the cycle is). Returns per-launch and total times in ms."""
+    set_bytes = w.algorithmic_bytes("bf16")
+    if nsets is None:
+        nsets = max(2, math.ceil(3 * 126e6 / set_bytes) + 1)
+    base = to_dev(x, dev)
+    sets = [base] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in base.items()}
+                     for _ in range(nsets - 1)]
+    Bt, L, Dm = w.batch, w.seqlen, w.dim
+    ys = [torch.empty((Bt, L, Dm), dtype=out_dtype, device=dev) for _ in range(nsets)]
+    hs = [torch.empty((Bt, Dm, 16), dtype=torch.float32, device=dev) for _ in range(nsets)]
+    ws_bytes = ss.ss_scan_fwd_workspace_size(Bt, L, Dm)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        k = i % nsets
+        scan_call(ss, sets[k], ys[k], hs[k], ws)
+    torch.cuda.synchronize()
+    ss.ss_scan_status(ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    return dict(sets=sets, ys=ys, hs=hs, ws=ws, ev=ev, t0=t0, t1=t1, nsets=nsets, stream=stream,
+                launches_per_step=(2 if ws_bytes else 1))
+
+
+def run_timed(ss, st, steps):
+    st["t0"].record()
+    for i in range(steps):
+        k = i % st["nsets"]
+        st["ev"][i][0].record()
+        scan_call(ss, st["sets"][k], st["ys"][k], st["hs"][k], st["ws"])
+        st["ev"][i][1].record()
+    st["t1"].record()
+
+
+def timed_results(st, steps):
+    total = st["t0"].elapsed_time(st["t1"])
+    per = [a.elapsed_time(b) for a, b in st["ev"]]
+    return total, per
+
+
+def bench_e2e(ss, w, x, steps, warmup, out_dtype, dev):
+    """Through the public call with HOST buffers: every step copies its inputs
+    from pinned host memory, runs the scan and copies y and h_last back."""
+    keys = ("u", "delta_raw", "z", "B", "C")
+    host = {k: x[k].pin_memory() for k in keys}
+    params = to_dev({k: x[k] for k in ("A", "D", "delta_bias")}, dev)
+    dbuf = {k: torch.empty_like(host[k], device=dev) for k in keys}
+    Bt, L, Dm = w.batch, w.seqlen, w.dim
+    y = torch.empty((Bt, L, Dm), dtype=out_dtype, device=dev)
+    h = torch.empty((Bt, Dm, 16), dtype=torch.float32, device=dev)
+    y_host = torch.empty(y.shape, dtype=out_dtype).pin_memory()
+    h_host = torch.empty(h.shape, dtype=torch.float32).pin_memory()
+    ws_bytes = ss.ss_scan_fwd_workspace_size(Bt, L, Dm)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y.numel() * y.element_size() + h.numel() * 4
+
+    def one():
+        for k in keys:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        d = dict(dbuf, **params)
+        scan_call(ss, d, y, h, ws)
+        y_host.copy_(y, non_blocking=True)
+        h_host.copy_(h, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def bench_decode(ss, w, dev, timed_steps=64, warmup=8):
+    """Decode steps of the 256-stream workload. Cold: an L2 flush (write of a
+    buffer larger than L2) before every timed step, each step timed alone.
+    Warm: back-to-back steps (the 84 MB state may stay in the 126 MB L2)."""
+    S, Dm = w.streams, w.dim
+    A, Dk, bias = gen.make_params(w.prefix)
+    nin = 16
+    steps = gen.make_decode_steps(w, 0, nin)
+    su = {k: v.to(dev) for k, v in steps.items()}
+    A, Dk, bias = A.to(dev), Dk.to(dev), bias.to(dev)
+    g = torch.Generator(device=dev).manual_seed(4)
+    h = 0.1 * torch.randn((S, Dm, 16), generator=g, device=dev, dtype=torch.float32)
+    y = torch.empty((S, Dm), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(k):
+        ss.ss_state_update(h, su["u"][k], su["delta_raw"][k], A, su["B"][k], su["C"][k], Dk, su["z"][k], bias, y=y)
+
+    for k in range(warmup):
+        step(k % nin)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(timed_steps)]
+    for i in range(timed_steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        step(i % nin)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    cold = [a.elapsed_time(b) for a, b in ev]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nwarm = 1000
+    a.record()
+    for i in range(nwarm):
+        step(i % nin)
+    b.record()
+    torch.cuda.synchronize()
+    warm_ms = a.elapsed_time(b) / nwarm
+    cold_ms = statistics.mean(cold)
+    bytes_step = w.algorithmic_bytes_per_step("bf16")
+    return {"workload": f"{w.name}: {S} streams x d_inner {Dm} x d_state 16, bf16 inputs/y, fp32 state",
+            "steps_per_s": 1e3 / cold_ms, "ms_per_step": cold_ms, "hbm_gbs": bytes_step / (cold_ms * 1e-3) / 1e9,
+            "tokens_per_s": S * 1e3 / cold_ms, "l2": "flushed before every timed step",
+            "warm_steps_per_s": 1e3 / warm_ms, "warm_note": "1000 back-to-back steps, state may stay in L2"}
+
+
+def cpu_baseline_scan(w, x, target_s=12.0):
+    """The float64 oracle as it stands, on the host cores, over channels of the
+    same workload; scaled to algorithmic GB/s of the sample."""
+    import oracle
+
+    nthreads = oracle.default_threads()
+    per_ch_bytes = w.algorithmic_bytes("bf16") / (w.batch * w.dim)
+    rng = np.random.default_rng(0)
+    n = min(w.batch * w.dim, 256)
+    total_ch, total_t = 0, 0.0
+    while True:
+        ch = np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.dim, n)], axis=1)
+        t = time.perf_counter()
+        oracle.scan(x, channels=ch, nthreads=nthreads)
+        dt = time.perf_counter() - t
+        total_ch += n
+        total_t += dt
+        if total_t >= target_s or total_ch >= w.batch * w.dim:
+            break
+        n = int(min(w.batch * w.dim - total_ch, max(n, n * (target_s - total_t) / max(dt, 1e-3))))
+        n = max(n, 1)
+    gbs = per_ch_bytes * total_ch / total_t / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{total_ch} of {w.batch * w.dim} channels x {w.seqlen} tokens of {w.name}, "
+                      f"{total_t:.1f} s wall", "channel_tokens_per_s": total_ch * w.seqlen / total_t}
+
+
+def run_ours(args, world, rank, local):
+    import selective_state_space_130_b300 as ss
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = configs.get_config(args.workload)
+    out_dtype = torch.bfloat16
+    peaks, peak_kind = load_peaks()
+    x = gen.make_scan_inputs(w, seed=w.seed + 1000 * rank)
+
+    st = bench_scan(ss, w, x, args.steps, args.warmup, out_dtype, dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    run_timed(ss, st, args.steps)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ss.ss_scan_status(st["ws"])
+    total_ms, per = timed_results(st, args.steps)
+    ms_step = max_over_ranks(world, total_ms / args.steps)
+    per_launch_ms = statistics.mean(per)
+
+    bytes_step = w.algorithmic_bytes("bf16")
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    achieved = bytes_step / (per_launch_ms * 1e-3) / 1e9
+    hbm_peak = float(peaks["hbm_gbs"])
+    clock_mhz = clk.get("sm_mhz") or float(peaks.get("sm_max_mhz", 2032.0))
+    states = w.channel_tokens * w.dstate
+    alu_peak = STATE_UPDATES_PER_CLK_SM * SMS * clock_mhz * 1e6
+    alu_achieved = states / (per_launch_ms * 1e-3)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: batch {w.batch}, L {w.seqlen}, d_inner {w.dim}, d_state {w.dstate}, "
+                               "bf16 u/delta_raw/z/B/C and y, fp32 A/D/bias/state",
+                   "batch": w.batch, "seq_len": w.seqlen, "d_inner": w.dim, "d_state": w.dstate,
+                   "global_batch": w.batch * world, "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": f"inputs larger than L2; {st['nsets']} rotating input/output sets"},
+        "channel_tokens_per_s": world * w.channel_tokens / (ms_step * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": profiled_traffic(),
+                     "peak_kind": peak_kind, "kernel": "ss_scan_fwd (scan_fwd_kernel)",
+                     "per_launch_ms": round(per_launch_ms, 5), "algorithmic_bytes_per_launch": bytes_step},
+        "compute_roofline": {"bound": "alu", "unit": "state updates/s", "achieved": alu_achieved,
+                             "peak": alu_peak, "frac": round(alu_achieved / alu_peak, 4),
+                             "basis": "issue-bound: 5 issue slots per (t,d,n) (4 fp32 + 1 MUFU ex2), "
+                                      "25.6 per clk per SM x 148 SMs x median SM clock under load"},
+        "gpu_launches": args.steps * st["launches_per_step"],
+        "clocks": clk,
+    }
+    del st
+    torch.cuda.empty_cache()
+
+    if rank == 0 and not args.no_e2e:
+        e2e_ms, h2d, d2h = bench_e2e(ss, w, x, max(3, min(args.steps, 10)), 2, out_dtype, dev)
+        result["e2e"] = {"value": round(bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                         "path": "pinned host -> device copies, ss_scan_fwd, device -> pinned host copies"}
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_decode:
+        result["decode"] = bench_decode(ss, configs.C4, dev)
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_extra:
+        extra = {}
+        for name in ("c1", "c3"):
+            wc = configs.get_config(name)
+            xc = gen.make_scan_inputs(wc)
+            reps = 10 if name == "c1" else 3
+            stc = bench_scan(ss, wc, xc, reps, 2, out_dtype, dev)
+            torch.cuda.synchronize()
+            run_timed(ss, stc, reps)
+            torch.cuda.synchronize()
+            tot, per = timed_results(stc, reps)
+            ms = statistics.mean(per)
+            bts = wc.algorithmic_bytes("bf16")
+            extra[wc.name] = {"ms_per_launch": round(ms, 4), "hbm_gbs": round(bts / (ms * 1e-3) / 1e9, 1),
+                              "frac_of_hbm_peak": round(bts / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+                              "channel_tokens_per_s": wc.channel_tokens / (ms * 1e-3),
+                              "launches_per_step": stc["launches_per_step"], "l2": f"{stc['nsets']} rotating sets"}
+            del stc, xc
+            torch.cuda.empty_cache()
+        result["per_config"] = extra
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_scan(w, x)
+    return result
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    """The reference arm is the float64 CPU oracle as it stands, timed on the
+    host cores over a bounded sample of the same workload per step."""
+    if rank != 0:
+        return None
+    import oracle
+
+    w = configs.get_config(args.workload)
+    x = gen.make_scan_inputs(w)
+    nthreads = oracle.default_threads()
+    rng = np.random.default_rng(1)
+    n = max(64, min(w.batch * w.dim, 32 * nthreads))
+    per_ch_bytes = w.algorithmic_bytes("bf16") / (w.batch * w.dim)
+    ch = np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.dim, n)], axis=1)
+    for _ in range(args.warmup):
+        oracle.scan(x, channels=ch[: max(1, n // 8)], nthreads=nthreads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan(x, channels=ch, nthreads=nthreads)
+    dt = (time.perf_counter() - t) / args.steps
+    value = per_ch_bytes * n / dt / 1e9
+    sample = f"{n} of {w.batch * w.dim} channels x {w.seqlen} tokens of {w.name} per step"
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{w.name}: batch {w.batch}, L {w.seqlen}, d_inner {w.dim}, d_state {w.dstate}, "
+                               "bf16 inputs (oracle in float64)", "batch": w.batch, "seq_len": w.seqlen,
+                   "d_inner": w.dim, "d_state": w.dstate},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the c1 / c3 scan timings")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warmup raised to 3 (timing rule)")
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    dist_init(world, local)
+    res = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,143 @@
+/*
+ * ss_scan.h — C ABI of the B300 (sm_103a) selective state-space scan library
+ * (libssscan.so).
+ *
+ * What it computes (the S6 layer's scan, forward only). For every batch
+ * element b and channel d, with state h[n] (n < dstate) starting at h0[b,d,:]
+ * (zeros when h0 is NULL), for t = 0 .. seqlen-1:
+ *
+ *   delta   = softplus(delta_raw[b,t,d] + delta_bias[d])
+ *   h[n]    = exp(delta * A[d,n]) * h[n] + delta * B[b,t,n] * u[b,t,d]
+ *   yv      = sum_n C[b,t,n] * h[n] + D[d] * u[b,t,d]
+ *   y[b,t,d]= yv * silu(z[b,t,d])                 (yv itself when z is NULL)
+ *
+ * and h_last[b,d,:] = h after the last step. Passages:
+ *  - recurrence h_t = Abar h_{t-1} + Bbar x_t, y_t = C h_t + D x_t:
+ *    "Transformer时代终结？Mamba的状态空间革命重塑AI底层架构", section 二.1;
+ *  - Abar = exp(delta*A) and the first-order Bbar = delta*B, with delta, B, C
+ *    produced per token and B, C shared by all channels: the mlqm.cn SSM
+ *    tutorial, sections 3.2, 5.2 and the 9.2 step sketch;
+ *  - A = -exp(A_log) keeps |Abar| < 1: "外文文献精读：Mamba - 线性时间序列建模
+ *    与结构化状态空间模型", section 4.1 (A is passed already exponentiated);
+ *  - SiLU gate on the SSM output: "Mamba: Linear-Time Sequence Modeling with
+ *    Selective State Spaces" (review page), method step 3; tutorial section 7.1;
+ *  - softplus for delta is not printed on the pages; it is the standard
+ *    softplus(x) = log(1 + e^x).
+ * The decode entry point is the same step with seqlen = 1 and h updated in
+ * place ("AI 推理系列（十四）：Mamba 的 Selective State Space", section on
+ * Selective Scan for training and Decode: prefill by scan, then per-token
+ * in-place state updates).
+ *
+ * Conventions shared by all entry points:
+ *  - Every data pointer is a DEVICE pointer owned by the caller, 16-byte
+ *    aligned, to a dense row-major (C-contiguous) array. The library never
+ *    allocates device memory and keeps no pointer after a call returns.
+ *  - u, delta_raw, z, B, C share `in_dtype` (SS_F32 or SS_BF16). A, D,
+ *    delta_bias, h0, h_last and the decode state h are float32. y has
+ *    `out_dtype`.
+ *  - dstate must be 16 (SS_ERR_UNSUPPORTED otherwise).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on that stream; the return code covers argument checks and
+ *    launch errors only. A device-side wait that gave up is reported later by
+ *    ss_scan_status().
+ *  - Empty problems (batch == 0 or dim == 0) launch nothing and return SS_OK.
+ *  - On any error the call launches nothing (or stops at the failing launch)
+ *    and ss_last_error() returns a message for the calling host thread.
+ *  - The library runs on compute capability 10.3 devices (B300) only.
+ */
+#ifndef SS_SCAN_H
+#define SS_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SS_OK = 0,
+  SS_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, too-small workspace */
+  SS_ERR_UNSUPPORTED = 2, /* dstate != 16, unknown dtype, wrong device */
+  SS_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  SS_ERR_TIMEOUT = 4      /* a device-side bounded wait gave up (see ss_scan_status) */
+} ss_status;
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int ss_version(void);
+
+/* Message describing the last error on this host thread ("" if none). The
+ * pointer stays valid until the next call on the same thread. */
+const char *ss_last_error(void);
+
+/*
+ * Bytes of device workspace that ss_scan_fwd needs for this problem size. The
+ * scan splits long sequences into chunks whose carries (prod Abar, state) are
+ * combined across thread blocks through this workspace; short sequences need
+ * none (0 is returned). Depends only on the sizes.
+ */
+size_t ss_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate);
+
+/*
+ * Selective scan forward.
+ *  u, delta_raw, z : [batch, seqlen, dim]   in_dtype; z may be NULL (no gate)
+ *  A               : [dim, dstate]          float32 (the negative real diagonal)
+ *  B, C            : [batch, seqlen, dstate] in_dtype, shared by all channels
+ *  D               : [dim] float32 or NULL (no skip term)
+ *  delta_bias      : [dim] float32 or NULL (zero)
+ *  h0              : [batch, dim, dstate] float32 or NULL (zero initial state)
+ *  y               : [batch, seqlen, dim]   out_dtype (output)
+ *  h_last          : [batch, dim, dstate] float32 or NULL (final state, output)
+ *  workspace       : device buffer of at least ss_scan_fwd_workspace_size()
+ *                    bytes (may be NULL when that size is 0). The library
+ *                    initialises what it needs on `stream`; the buffer must not
+ *                    be shared by calls that overlap on the GPU.
+ * seqlen == 0 writes h_last = h0 (or zeros) and nothing else.
+ */
+ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                      ss_dtype in_dtype, ss_dtype out_dtype,
+                      const void *u, const void *delta_raw, const float *A,
+                      const void *B, const void *C, const float *D, const void *z,
+                      const float *delta_bias, const float *h0,
+                      void *y, float *h_last,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Single-token decode step, state updated in place.
+ *  h               : [batch, dim, dstate] float32, read and overwritten
+ *  u, delta_raw, z : [batch, dim] in_dtype; z may be NULL
+ *  B, C            : [batch, dstate] in_dtype
+ *  A               : [dim, dstate] float32; D, delta_bias: [dim] float32 or NULL
+ *  y               : [batch, dim] out_dtype (output)
+ */
+ss_status ss_state_update(int64_t batch, int64_t dim, int64_t dstate,
+                          ss_dtype in_dtype, ss_dtype out_dtype,
+                          float *h, const void *u, const void *delta_raw,
+                          const float *A, const void *B, const void *C, const float *D,
+                          const void *z, const float *delta_bias, void *y, void *stream);
+
+/*
+ * Launch-shape controls for the calling host thread (0 = automatic, the
+ * default). threads_per_channel in {1, 2, 4} sets how many threads share one
+ * channel's 16 states; chunk_len > 0 forces the sequence to be split into
+ * chunks of that many timesteps (rounded up to the 32-step tile), which
+ * engages the cross-block carry path. Results do not depend on these settings
+ * beyond fp32 rounding; ss_scan_fwd_workspace_size() follows them.
+ */
+void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len);
+
+/*
+ * Synchronises `stream`, then reports whether a device-side bounded wait of an
+ * earlier ss_scan_fwd call on it gave up (SS_ERR_TIMEOUT) and clears that
+ * record. `workspace` is the buffer that call used (NULL if it used none).
+ * Returns SS_ERR_CUDA if the stream reports an error.
+ */
+ss_status ss_scan_status(void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_SCAN_H */

@@ -1,0 +1,158 @@
+"""ctypes binding of libssscan.so.
+
+Argument marshalling only: every step of the scan and the decode step runs in
+the library's sm_103a kernels. PyTorch provides device memory and streams.
+The binding refuses to work without the compiled library (no fallback).
+"""
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libssscan.so")
+
+SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT = range(5)
+SS_F32, SS_BF16 = 0, 1
+STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_CUDA",
+                4: "SS_ERR_TIMEOUT"}
+
+# Every function the C header declares, with its ctypes signature.
+_I64, _P, _SZ = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+SIGNATURES = {
+    "ss_version": (ctypes.c_int, []),
+    "ss_last_error": (ctypes.c_char_p, []),
+    "ss_scan_fwd_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
+    "ss_scan_fwd": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "ss_state_update": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ss_scan_set_tuning": (None, [ctypes.c_int, _I64]),
+    "ss_scan_status": (ctypes.c_int, [_P, _P]),
+}
+
+
+class SSError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib(path: str = None) -> ctypes.CDLL:
+    """The loaded library (built by selective_state_space_130_b300/build.py)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"libssscan.so not found at {p}; build it with "
+                          "`python selective_state_space_130_b300/build.py` (nvcc, sm_103a)")
+    L = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(status):
+    if status != SS_OK:
+        raise SSError(status, lib().ss_last_error().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SS_F32
+    if t.dtype == torch.bfloat16:
+        return SS_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _tdt(code: int):
+    return torch.bfloat16 if code == SS_BF16 else torch.float32
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def ss_version() -> int:
+    return lib().ss_version()
+
+
+def ss_last_error() -> str:
+    return lib().ss_last_error().decode()
+
+
+def ss_scan_set_tuning(threads_per_channel: int = 0, chunk_len: int = 0):
+    lib().ss_scan_set_tuning(int(threads_per_channel), int(chunk_len))
+
+
+def ss_scan_fwd_workspace_size(batch, seqlen, dim, dstate=16) -> int:
+    return int(lib().ss_scan_fwd_workspace_size(batch, seqlen, dim, dstate))
+
+
+def ss_scan_fwd(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, h0=None, *, out_dtype=None,
+                y=None, h_last=None, workspace=None, return_h_last=True, stream=None):
+    """Selective scan forward on device tensors.
+
+    u, delta_raw, z: [Bt, L, D]; B, C: [Bt, L, N] (float32 or bfloat16, one dtype);
+    A: [D, N], D, delta_bias: [D], h0: [Bt, D, N] float32. Returns (y, h_last);
+    outputs and workspace are allocated with torch when not given.
+    """
+    Bt, L, Dm = u.shape
+    N = B.shape[-1]
+    code = _dt(u)
+    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    dev = u.device
+    if y is None:
+        y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=dev)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+    ws_bytes = ss_scan_fwd_workspace_size(Bt, L, Dm, N)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().ss_scan_fwd(Bt, L, Dm, N, code, out_code, _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(B), _ptr(C),
+                             _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_last),
+                             ws_ptr, ws_len, _stream(stream)))
+    return y, h_last
+
+
+def ss_state_update(h, u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, *, out_dtype=None, y=None,
+                    stream=None):
+    """One decode step on device tensors; h [S, D, N] float32 is updated in place.
+    u, delta_raw, z: [S, D]; B, C: [S, N]. Returns y [S, D]."""
+    S, Dm = u.shape
+    N = B.shape[-1]
+    code = _dt(u)
+    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    if y is None:
+        y = torch.empty((S, Dm), dtype=_tdt(out_code), device=u.device)
+    _check(lib().ss_state_update(S, Dm, N, code, out_code, _ptr(h), _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(B),
+                                 _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(y), _stream(stream)))
+    return y
+
+
+def ss_scan_status(workspace=None, stream=None):
+    """Raise SSError if a device-side wait of an earlier scan gave up."""
+    _check(lib().ss_scan_status(_ptr(workspace) if workspace is not None else None, _stream(stream)))

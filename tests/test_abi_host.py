@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/ss_scan.h declares, and rejects bad arguments before
+touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import selective_state_space_130_b300 as ss
+from selective_state_space_130_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include"))) if f.endswith(".h")]
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(ss_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("ss_scan_fwd", "ss_state_update", "ss_scan_fwd_workspace_size", "ss_scan_status", "ss_last_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(_lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+        assert name in _lib.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_version():
+    assert ss.ss_version() >= 10000
+
+
+def _scan(**kw):
+    args = dict(batch=1, seqlen=8, dim=8, dstate=16, in_dtype=0, out_dtype=0)
+    args.update({k: v for k, v in kw.items() if k in args})
+    ptrs = dict(u=0x1000, delta_raw=0x2000, A=0x3000, B=0x4000, C=0x5000, D=None, z=None, delta_bias=None,
+                h0=None, y=0x6000, h_last=None, workspace=None)
+    ptrs.update({k: v for k, v in kw.items() if k in ptrs})
+    return ss.lib().ss_scan_fwd(args["batch"], args["seqlen"], args["dim"], args["dstate"], args["in_dtype"],
+                                 args["out_dtype"], ptrs["u"], ptrs["delta_raw"], ptrs["A"], ptrs["B"], ptrs["C"],
+                                 ptrs["D"], ptrs["z"], ptrs["delta_bias"], ptrs["h0"], ptrs["y"], ptrs["h_last"],
+                                 ptrs["workspace"], kw.get("ws_bytes", 0), None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(dstate=8), _lib.SS_ERR_UNSUPPORTED, "dstate"),
+    (dict(dstate=32), _lib.SS_ERR_UNSUPPORTED, "dstate"),
+    (dict(in_dtype=5), _lib.SS_ERR_UNSUPPORTED, "dtype"),
+    (dict(out_dtype=-1), _lib.SS_ERR_UNSUPPORTED, "dtype"),
+    (dict(batch=-1), _lib.SS_ERR_INVALID_ARG, "negative"),
+    (dict(seqlen=-3), _lib.SS_ERR_INVALID_ARG, "negative"),
+    (dict(seqlen=1 << 31), _lib.SS_ERR_INVALID_ARG, "2^31"),
+    (dict(u=None), _lib.SS_ERR_INVALID_ARG, "u must not be NULL"),
+    (dict(delta_raw=None), _lib.SS_ERR_INVALID_ARG, "delta_raw"),
+    (dict(A=None), _lib.SS_ERR_INVALID_ARG, "A must not"),
+    (dict(B=None), _lib.SS_ERR_INVALID_ARG, "B must not"),
+    (dict(C=None), _lib.SS_ERR_INVALID_ARG, "C must not"),
+    (dict(y=None), _lib.SS_ERR_INVALID_ARG, "y must not"),
+    (dict(u=0x1002), _lib.SS_ERR_INVALID_ARG, "aligned"),
+    (dict(B=0x4008), _lib.SS_ERR_INVALID_ARG, "aligned"),
+    (dict(h0=0x7004), _lib.SS_ERR_INVALID_ARG, "aligned"),
+    (dict(z=0x7001), _lib.SS_ERR_INVALID_ARG, "aligned"),
+])
+def test_scan_rejects_bad_arguments(kw, code, msg):
+    st = _scan(**kw)
+    assert st == code
+    assert msg in ss.ss_last_error()
+
+
+def test_empty_problem_is_ok_without_device():
+    assert _scan(batch=0) == _lib.SS_OK
+    assert _scan(dim=0) == _lib.SS_OK
+    assert ss.ss_last_error() == ""
+
+
+def test_state_update_rejects_bad_arguments():
+    L = ss.lib()
+    ok = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None, None, None, 0x7000]
+    st = L.ss_state_update(4, 8, 15, 0, 0, *ok, None)
+    assert st == _lib.SS_ERR_UNSUPPORTED and "dstate" in ss.ss_last_error()
+    bad = list(ok)
+    bad[0] = None  # h
+    assert L.ss_state_update(4, 8, 16, 0, 0, *bad, None) == _lib.SS_ERR_INVALID_ARG
+    bad = list(ok)
+    bad[3] = 0x3004  # A misaligned
+    assert L.ss_state_update(4, 8, 16, 1, 0, *bad, None) == _lib.SS_ERR_INVALID_ARG
+    assert L.ss_state_update(0, 8, 16, 1, 0, *ok, None) == _lib.SS_OK
+
+
+def test_workspace_size_queries():
+    assert ss.ss_scan_fwd_workspace_size(4, 2048, 5120) == 0          # short sequences need none
+    ws = ss.ss_scan_fwd_workspace_size(1, 1 << 20, 1024)
+    assert ws > 0                                                     # long sequences are split
+    assert ss.ss_scan_fwd_workspace_size(1, 1 << 20, 1024, 8) == 0     # unsupported dstate
+    ss.ss_scan_set_tuning(2, 64)
+    try:
+        forced = ss.ss_scan_fwd_workspace_size(1, 1000, 64)
+    finally:
+        ss.ss_scan_set_tuning(0, 0)
+    assert forced > 0
+    assert ss.ss_scan_fwd_workspace_size(1, 1000, 64) == 0
+
+
+def test_binding_raises_typed_errors():
+    with pytest.raises(ss.SSError) as ei:
+        ss._lib._check(_scan(dstate=4))
+    assert ei.value.status == _lib.SS_ERR_UNSUPPORTED

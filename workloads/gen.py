@@ -107,33 +107,38 @@ def make_scan_inputs(w: ScanWorkload, seed: int = None) -> dict:
     return out
 
 
-def make_decode_steps(w: DecodeWorkload, first: int, count: int) -> dict:
+def make_decode_steps(w: DecodeWorkload, first: int, count: int, threads: int = 0) -> dict:
     """Inputs of decode steps [first, first+count): u, delta_raw, z [count, S, D],
     B, C [count, S, N] in w.in_dtype. Step k draws from its own streams, so any
     range of steps can be generated alone."""
     S, D, N = w.streams, w.dim, w.dstate
-    us, ds, zs, bs, cs = [], [], [], [], []
-    for k in range(first, first + count):
-        sk = w.seed * 100_003 + k
-        us.append(_store(randn_blocks(S * D, sk, S_U).view(S, D), w.in_dtype))
-        ds.append(_store(w.delta_raw_scale * randn_blocks(S * D, sk, S_DRAW).view(S, D), w.in_dtype))
-        zs.append(_store(randn_blocks(S * D, sk, S_Z).view(S, D), w.in_dtype))
-        bs.append(_store(randn_blocks(S * N, sk, S_B).view(S, N), w.in_dtype))
-        cs.append(_store(randn_blocks(S * N, sk, S_C).view(S, N), w.in_dtype))
-    return {
-        "u": torch.stack(us).contiguous(),
-        "delta_raw": torch.stack(ds).contiguous(),
-        "z": torch.stack(zs).contiguous(),
-        "B": torch.stack(bs).contiguous(),
-        "C": torch.stack(cs).contiguous(),
+    td = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
+    out = {
+        "u": torch.empty(count, S, D, dtype=td), "delta_raw": torch.empty(count, S, D, dtype=td),
+        "z": torch.empty(count, S, D, dtype=td), "B": torch.empty(count, S, N, dtype=td),
+        "C": torch.empty(count, S, N, dtype=td),
     }
+
+    def fill(i):
+        sk = w.seed * 100_003 + first + i
+        out["u"][i] = _store(randn_blocks(S * D, sk, S_U, threads=1).view(S, D), w.in_dtype)
+        out["delta_raw"][i] = _store(w.delta_raw_scale * randn_blocks(S * D, sk, S_DRAW, threads=1).view(S, D),
+                                     w.in_dtype)
+        out["z"][i] = _store(randn_blocks(S * D, sk, S_Z, threads=1).view(S, D), w.in_dtype)
+        out["B"][i] = _store(randn_blocks(S * N, sk, S_B, threads=1).view(S, N), w.in_dtype)
+        out["C"][i] = _store(randn_blocks(S * N, sk, S_C, threads=1).view(S, N), w.in_dtype)
+
+    n = threads or min(32, os.cpu_count() or 1)
+    with ThreadPoolExecutor(n) as ex:
+        list(ex.map(fill, range(count)))
+    return out
 
 
 def random_scan_inputs(batch, seqlen, dim, dstate, in_dtype="f32", seed=0, delta_raw_scale=0.5,
-                       a_log_jitter=0.0, has_z=True, has_d=True, with_h0=False):
+                       a_log_jitter=0.0, has_z=True, has_d=True, with_h0=False, dt_min=1e-3, dt_max=1e-1):
     """Small ad-hoc problems (edge shapes for tests) with the c0 recipe."""
     w = ScanWorkload("adhoc", batch, seqlen, dim, dstate, in_dtype, seed, delta_raw_scale,
-                     a_log_jitter, has_z=has_z, has_d=has_d)
+                     a_log_jitter, has_z=has_z, has_d=has_d, dt_min=dt_min, dt_max=dt_max)
     x = make_scan_inputs(w)
     if with_h0:
         x["h0"] = randn_blocks(batch * dim * dstate, seed, 99).view(batch, dim, dstate).contiguous()
