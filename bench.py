@@ -33,7 +33,7 @@ from workloads import configs, gen  # noqa: E402
 
 METRIC = "selective-scan HBM GB/s (% of B300 peak) & channel-tokens/s; decode steps/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "sm_max_mhz": 2032.0}
-KERNEL_SOURCES = ["selective_state_space_130_b300/csrc/ss_scan_fwd.cu",
+KERNEL_SOURCES = ["selective_state_space_130_b300/csrc/ss_scan_fwd_kernel.cuh",
                   "selective_state_space_130_b300/csrc/ss_device.cuh",
                   "selective_state_space_130_b300/csrc/ss_internal.h"]
 SCAN_PROFILE = "profiles/ss_scan_fwd_mamba2p8b_layer.md"
@@ -460,6 +460,33 @@ def run_reference(args, world, rank):
     }
 
 
+def profile_launches(args):
+    """Two launches of the scan (or decode) kernel on the chosen workload, no
+    timing: the target of `ncu -k regex:... -s 1 -c 1`."""
+    import selective_state_space_130_b300 as ss
+
+    dev = torch.device("cuda", 0)
+    if args.profile == "scan":
+        w = configs.get_config(args.workload)
+        x = to_dev(gen.make_scan_inputs(w), dev)
+        Bt, L, Dm = w.batch, w.seqlen, w.dim
+        y = torch.empty((Bt, L, Dm), dtype=torch.bfloat16, device=dev)
+        h = torch.empty((Bt, Dm, 16), dtype=torch.float32, device=dev)
+        nb = ss.ss_scan_fwd_workspace_size(Bt, L, Dm)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        for _ in range(2):
+            scan_call(ss, x, y, h, ws)
+        ss.ss_scan_status(ws)
+    else:
+        w = configs.C4
+        A, Dk, bias = (t.to(dev) for t in gen.make_params(w.prefix))
+        st = {k: v.to(dev) for k, v in gen.make_decode_steps(w, 0, 2).items()}
+        h = torch.zeros((w.streams, w.dim, 16), dtype=torch.float32, device=dev)
+        for k in range(2):
+            ss.ss_state_update(h, st["u"][k], st["delta_raw"][k], A, st["B"][k], st["C"][k], Dk, st["z"][k], bias)
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,7 +498,12 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the c1 / c3 scan timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["scan", "decode"], default=None,
+                    help="run 2 launches of one kernel (for an ncu capture of the 2nd) and exit")
     args = ap.parse_args()
+    if args.profile:
+        profile_launches(args)
+        return
     if args.warmup < 3:
         log("warmup raised to 3 (timing rule)")
         args.warmup = 3

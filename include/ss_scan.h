@@ -91,9 +91,12 @@ size_t ss_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, in
  *  y               : [batch, seqlen, dim]   out_dtype (output)
  *  h_last          : [batch, dim, dstate] float32 or NULL (final state, output)
  *  workspace       : device buffer of at least ss_scan_fwd_workspace_size()
- *                    bytes (may be NULL when that size is 0). The library
- *                    initialises what it needs on `stream`; the buffer must not
- *                    be shared by calls that overlap on the GPU.
+ *                    bytes (may be NULL when that size is 0). When a buffer of
+ *                    at least 256 bytes is given, the call also keeps its
+ *                    fault record there (read by ss_scan_status(workspace)),
+ *                    and clears what it uses on `stream` before the kernel.
+ *                    The buffer must not be shared by calls that overlap on
+ *                    the GPU.
  * seqlen == 0 writes h_last = h0 (or zeros) and nothing else.
  */
 ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
@@ -131,7 +134,7 @@ void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len);
 /*
  * Synchronises `stream`, then reports whether a device-side bounded wait of an
  * earlier ss_scan_fwd call on it gave up (SS_ERR_TIMEOUT) and clears that
- * record. `workspace` is the buffer that call used (NULL if it used none).
+ * record. `workspace` is the buffer that call was given (NULL if none).
  * Returns SS_ERR_CUDA if the stream reports an error.
  */
 ss_status ss_scan_status(void *workspace, void *stream);

@@ -15,6 +15,7 @@ namespace ssk {
 int scan_channels_per_block(int sg);
 int scan_tile_len();
 int scan_header_words();
+uint32_t scan_header_magic();
 }  // namespace ssk
 
 namespace {
@@ -75,21 +76,21 @@ namespace ssk {
 
 ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim) {
   ScanPlan pl{};
-  const int64_t channels = batch * dim;
   int sg = g_tune_sg;
   if (sg != 1 && sg != 2 && sg != 4) sg = 2;
   pl.sg = sg;
   pl.cblk = scan_channels_per_block(sg);
   const int tile = scan_tile_len();
-  // Split the sequence only when too few consumer threads would run.
-  const int64_t base_threads = channels * sg;
-  const int64_t target = (int64_t)kSMs * 8 * 32;
+  // Blocks are single warps; split the sequence only when the channel blocks
+  // alone would leave SMs short of warps (target about eight per SM).
+  const int64_t base_warps = batch * ((dim + pl.cblk - 1) / pl.cblk);
+  const int64_t target = (int64_t)kSMs * 8;
   const int64_t min_chunk = 8192;
   int64_t chunk = seqlen;
   if (g_tune_chunk > 0) {
     chunk = g_tune_chunk;
-  } else if (base_threads < target / 2 && seqlen >= 2 * min_chunk) {
-    int64_t k = (target + base_threads - 1) / base_threads;
+  } else if (base_warps < target / 2 && seqlen >= 2 * min_chunk) {
+    int64_t k = (target + base_warps - 1) / base_warps;
     k = std::min<int64_t>(k, seqlen / min_chunk);
     chunk = (seqlen + k - 1) / k;
   }
@@ -184,13 +185,20 @@ ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   p.nchunks = plan.nchunks;
   p.ncblk = (int)((dim + plan.cblk - 1) / plan.cblk);
   if ((double)batch * p.ncblk * p.nchunks > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
-  if (plan.nchunks > 1) {
+  // The fault word lives in the workspace header when a workspace is given
+  // (so ss_scan_status(workspace) reads what this call wrote), else in the
+  // library's own device word. The header is cleared on the stream first.
+  const size_t hdr = (size_t)ssk::scan_header_words() * 4;
+  if (workspace && workspace_bytes >= hdr) {
     p.ws_header = static_cast<uint32_t*>(workspace);
-    const int64_t tiles = batch * (int64_t)p.ncblk * plan.nchunks;
-    const size_t head = (size_t)ssk::scan_header_words() * 4 + (((size_t)tiles * 4 + 255) & ~size_t(255));
-    p.ws_carry = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + head);
     p.fault = p.ws_header + 1;
-    cudaError_t e = cudaMemsetAsync(workspace, 0, head, s);
+    size_t clear = hdr;
+    if (plan.nchunks > 1) {
+      const int64_t tiles = batch * (int64_t)p.ncblk * plan.nchunks;
+      clear = hdr + (((size_t)tiles * 4 + 255) & ~size_t(255));
+      p.ws_carry = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + clear);
+    }
+    cudaError_t e = cudaMemsetAsync(workspace, 0, clear, s);
     if (e != cudaSuccess) return cuda_fail(e, "workspace initialisation");
   } else {
     p.fault = ssk::device_fault_word();
@@ -242,10 +250,15 @@ ss_status ss_scan_status(void* workspace, void* stream) {
     if (fault && (e = cudaMemset(own, 0, sizeof fault)) != cudaSuccess) return cuda_fail(e, "fault word clear");
   }
   if (workspace) {
-    uint32_t* w = static_cast<uint32_t*>(workspace) + 1;
-    if ((e = cudaMemcpy(&f2, w, sizeof f2, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    // words 1 (fault) and 2 (magic written by a scan that used this buffer)
+    uint32_t w[2] = {0, 0};
+    uint32_t* dw = static_cast<uint32_t*>(workspace) + 1;
+    if ((e = cudaMemcpy(w, dw, sizeof w, cudaMemcpyDeviceToHost)) != cudaSuccess)
       return cuda_fail(e, "workspace fault word read");
-    if (f2 && (e = cudaMemset(w, 0, sizeof f2)) != cudaSuccess) return cuda_fail(e, "workspace fault clear");
+    if (w[1] == ssk::scan_header_magic()) {
+      f2 = w[0];
+      if ((e = cudaMemset(dw, 0, sizeof w)) != cudaSuccess) return cuda_fail(e, "workspace fault clear");
+    }
   }
   fault |= f2;
   if (fault)

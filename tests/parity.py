@@ -29,7 +29,7 @@ def run_scan_dev(x, out_dtype=torch.float32, sg=0, chunk=0, check_status=True):
     ss.ss_scan_set_tuning(sg, chunk)
     try:
         ws_bytes = ss.ss_scan_fwd_workspace_size(Bt, L, Dm, 16)
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if ws_bytes else None
         y, h = ss.ss_scan_fwd(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], d.get("D"), d.get("z"),
                               d.get("delta_bias"), d.get("h0"), out_dtype=out_dtype, workspace=ws)
         if check_status:
