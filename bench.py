@@ -73,13 +73,20 @@ def barrier(world):
 
 
 def max_over_ranks(world, v):
+    """Slowest rank's value (timing is max over ranks); works on nccl and gloo."""
     if world == 1:
         return v
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(w, rank):
+    """Each rank scans its own batch: independent inputs, no exchange."""
+    return w.seed + 1000 * rank
 
 
 def load_peaks():
@@ -341,7 +348,7 @@ def run_ours(args, world, rank, local):
     w = configs.get_config(args.workload)
     out_dtype = torch.bfloat16
     peaks, peak_kind = load_peaks()
-    x = gen.make_scan_inputs(w, seed=w.seed + 1000 * rank)
+    x = gen.make_scan_inputs(w, seed=rank_seed(w, rank))
 
     st = bench_scan(ss, w, x, args.steps, args.warmup, out_dtype, dev)
     clocks = ClockSampler(local)
