@@ -132,6 +132,44 @@ ss_status ss_state_update(int64_t batch, int64_t dim, int64_t dstate,
 void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len);
 
 /*
+ * Selective scan forward that allocates nothing (no counterpart on the pages:
+ * it is a deployment variant of ss_scan_fwd, not part of the method).
+ *
+ * For callers that cannot allocate device memory: code running inside another
+ * runtime's memory pool or a graph-building framework that hands a plugin only
+ * its input and output buffers, or a serving loop that must not call
+ * cudaMalloc (which can synchronise the device) once it is running. Such a
+ * caller cannot provide the workspace that long sequences need. This entry
+ * point takes that scratch from a fixed array the library declares in device
+ * memory: SS_SCAN_NOALLOC_SCRATCH_BYTES on every GPU that loads the library,
+ * held until the process exits. It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * Arguments, layouts and results are those of ss_scan_fwd, without the
+ * workspace arguments. Behaviour:
+ *  - A problem whose scratch need (ss_scan_fwd_workspace_size) exceeds
+ *    SS_SCAN_NOALLOC_SCRATCH_BYTES is rejected with SS_ERR_INVALID_ARG before
+ *    anything is launched; use ss_scan_fwd with a workspace for it.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and keeps it; make that first call before any CUDA
+ *    stream capture begins.
+ *  - All calls on a device share the one array. Each call clears, on its
+ *    stream, the part that must start at zero. Calls that overlap on the GPU
+ *    (different streams, or different host threads without ordering) race on
+ *    the array and give wrong results: serialise them.
+ *  - A device-side wait that gives up is recorded in the library's own fault
+ *    word: ss_scan_status(NULL, stream) reports it.
+ */
+#define SS_SCAN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+ss_status ss_scan_fwd_noalloc(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                              ss_dtype in_dtype, ss_dtype out_dtype,
+                              const void *u, const void *delta_raw, const float *A,
+                              const void *B, const void *C, const float *D, const void *z,
+                              const float *delta_bias, const float *h0,
+                              void *y, float *h_last, void *stream);
+
+/*
  * Synchronises `stream`, then reports whether a device-side bounded wait of an
  * earlier ss_scan_fwd call on it gave up (SS_ERR_TIMEOUT) and clears that
  * record. `workspace` is the buffer that call was given (NULL if none).

@@ -15,6 +15,8 @@ LIB_PATH = os.path.join(HERE, "libssscan.so")
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT = range(5)
 SS_F32, SS_BF16 = 0, 1
+# bytes of the fixed scratch array behind ss_scan_fwd_noalloc (SS_SCAN_NOALLOC_SCRATCH_BYTES in the header)
+SS_SCAN_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_CUDA",
                 4: "SS_ERR_TIMEOUT"}
 
@@ -28,6 +30,8 @@ SIGNATURES = {
                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "ss_state_update": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ss_scan_fwd_noalloc": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                           _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
 }
@@ -156,3 +160,26 @@ def ss_state_update(h, u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, *
 def ss_scan_status(workspace=None, stream=None):
     """Raise SSError if a device-side wait of an earlier scan gave up."""
     _check(lib().ss_scan_status(_ptr(workspace) if workspace is not None else None, _stream(stream)))
+
+
+def ss_scan_fwd_noalloc(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, h0=None, *, out_dtype=None,
+                        y=None, h_last=None, return_h_last=True, stream=None):
+    """Selective scan forward through the entry point that allocates nothing on
+    the library side: its cross-block scratch is a fixed array inside the
+    library (SS_SCAN_NOALLOC_SCRATCH_BYTES per device). Same arguments and
+    results as ss_scan_fwd, without a workspace; outputs are allocated with
+    torch here only when not given. Calls that overlap on the GPU race on the
+    shared scratch."""
+    Bt, L, Dm = u.shape
+    N = B.shape[-1]
+    code = _dt(u)
+    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    dev = u.device
+    if y is None:
+        y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=dev)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+    _check(lib().ss_scan_fwd_noalloc(Bt, L, Dm, N, code, out_code, _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(B),
+                                     _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_last),
+                                     _stream(stream)))
+    return y, h_last

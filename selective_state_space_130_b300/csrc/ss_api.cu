@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <string>
 
 #include "ss_internal.h"
@@ -268,3 +269,127 @@ ss_status ss_scan_status(void* workspace, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Scan forward with library-owned scratch, for callers that cannot allocate.
+//
+// Some callers have no device allocator to hand: code that runs inside another
+// runtime's memory pool, a plugin handed only its input and output buffers, or
+// a program that must not call cudaMalloc once it is serving. For them this
+// entry point takes the cross-block carry scratch from a fixed array that the
+// library itself declares in device memory. Every GPU that loads the library
+// holds SS_SCAN_NOALLOC_SCRATCH_BYTES of it until the process exits.
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[SS_SCAN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on device `dev` (the current device).
+// The name g_noalloc_scratch in host code is only a host-side handle, so the
+// address is resolved once per device with that device current.
+ss_status noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(SS_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "scratch address lookup");
+    if (!p) return fail(SS_ERR_CUDA, "scratch address lookup returned NULL");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" ss_status ss_scan_fwd_noalloc(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                                         ss_dtype in_dtype, ss_dtype out_dtype, const void* u,
+                                         const void* delta_raw, const float* A, const void* B, const void* C,
+                                         const float* D, const void* z, const float* delta_bias, const float* h0,
+                                         void* y, float* h_last, void* stream) {
+  g_err.clear();
+  if (dstate != ssk::kDState) return fail(SS_ERR_UNSUPPORTED, "dstate must be 16 (got %lld)", (long long)dstate);
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, out %d)", (int)in_dtype, (int)out_dtype);
+  if (batch < 0 || seqlen < 0 || dim < 0)
+    return fail(SS_ERR_INVALID_ARG, "negative size (batch %lld, seqlen %lld, dim %lld)", (long long)batch,
+                (long long)seqlen, (long long)dim);
+  if (batch > INT32_MAX || seqlen > INT32_MAX || dim > INT32_MAX)
+    return fail(SS_ERR_INVALID_ARG, "a size exceeds 2^31-1");
+  if (batch == 0 || dim == 0) return SS_OK;
+  if ((double)batch * (double)seqlen * (double)dim > 4.0e18) return fail(SS_ERR_INVALID_ARG, "problem too large");
+  const void* need[] = {u, delta_raw, A, B, C, y};
+  const char* names[] = {"u", "delta_raw", "A", "B", "C", "y"};
+  if (seqlen > 0) {
+    for (int i = 0; i < 6; i++)
+      if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
+  }
+  const void* all[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, h_last};
+  const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last"};
+  for (int i = 0; i < 11; i++)
+    if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+
+  const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim);
+  if (seqlen > 0 && plan.workspace > (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES)
+    return fail(SS_ERR_INVALID_ARG,
+                "this problem needs %zu bytes of scratch; the no-allocation scan holds at most %zu (use ss_scan_fwd "
+                "with a caller-provided workspace)",
+                plan.workspace, (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES);
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(dev, &scratch)) != SS_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (seqlen == 0) {
+    if (!h_last) return SS_OK;
+    const size_t hbytes = (size_t)batch * dim * ssk::kDState * sizeof(float);
+    e = h0 ? cudaMemcpyAsync(h_last, h0, hbytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(h_last, 0, hbytes, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
+  }
+
+  ssk::ScanParams p{};
+  p.u = u;
+  p.delta_raw = delta_raw;
+  p.z = z;
+  p.B = B;
+  p.C = C;
+  p.A = A;
+  p.D = D;
+  p.delta_bias = delta_bias;
+  p.h0 = h0;
+  p.y = y;
+  p.h_last = h_last;
+  p.batch = batch;
+  p.seqlen = seqlen;
+  p.dim = dim;
+  p.chunk_len = plan.chunk_len;
+  p.nchunks = plan.nchunks;
+  p.ncblk = (int)((dim + plan.cblk - 1) / plan.cblk);
+  if ((double)batch * p.ncblk * p.nchunks > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
+  // Device-side waits that give up are recorded in the library's own fault
+  // word, which ss_scan_status(NULL, stream) reads and clears.
+  p.fault = ssk::device_fault_word();
+  if (!p.fault) return fail(SS_ERR_CUDA, "cannot resolve the library fault word");
+  if (plan.nchunks > 1) {
+    // The scratch keeps the previous call's contents: the ticket counter and
+    // the per-chunk flags must start at zero, so clear them on the stream.
+    const int64_t tiles = batch * (int64_t)p.ncblk * plan.nchunks;
+    const size_t clear = (size_t)ssk::scan_header_words() * 4 + (((size_t)tiles * 4 + 255) & ~size_t(255));
+    p.ws_header = static_cast<uint32_t*>(scratch);
+    p.ws_carry = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + clear);
+    e = cudaMemsetAsync(scratch, 0, clear, s);
+    if (e != cudaSuccess) return cuda_fail(e, "scratch initialisation");
+  }
+  const bool tma = ((size_t)dim * dsize(in_dtype)) % 16 == 0;
+  e = ssk::launch_scan_fwd(p, plan, in_dtype, out_dtype, tma, s);
+  if (e != cudaSuccess) return cuda_fail(e, "scan launch");
+  return SS_OK;
+}
