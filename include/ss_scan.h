@@ -73,10 +73,12 @@ int ss_version(void);
 const char *ss_last_error(void);
 
 /*
- * Bytes of device workspace that ss_scan_fwd needs for this problem size. The
- * scan splits long sequences into chunks whose carries (prod Abar, state) are
- * combined across thread blocks through this workspace; short sequences need
- * none (0 is returned). Depends only on the sizes.
+ * Bytes of device workspace that ss_scan_fwd needs for this problem size (for
+ * either input dtype). When the work is split along the sequence, states and
+ * chunk carries (prod Abar, state) pass between warps through this workspace,
+ * together with a ticket counter and per-boundary flags; problems run as one
+ * warp per channel block need none (0 is returned). Depends only on the sizes
+ * and the calling thread's tuning settings.
  */
 size_t ss_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate);
 
@@ -123,13 +125,15 @@ ss_status ss_state_update(int64_t batch, int64_t dim, int64_t dstate,
 
 /*
  * Launch-shape controls for the calling host thread (0 = automatic, the
- * default). threads_per_channel in {1, 2, 4} sets how many threads share one
- * channel's 16 states; chunk_len > 0 forces the sequence to be split into
- * chunks of that many timesteps (rounded up to the 32-step tile), which
- * engages the cross-block carry path. Results do not depend on these settings
- * beyond fp32 rounding; ss_scan_fwd_workspace_size() follows them.
+ * default, for each). threads_per_channel in {1, 2} sets how many threads share
+ * one channel's 16 states. chunk_len > 0 forces the sequence to be split into
+ * chunks of that many timesteps (rounded up to the 32-step tile), which engages
+ * the cross-block carry path. warps_per_scheduler in {1..4} sets how many warps
+ * the scan aims to keep on each SM sub-partition when it splits the work into
+ * equal ranges. Results do not depend on these settings beyond fp32 rounding;
+ * ss_scan_fwd_workspace_size() follows them.
  */
-void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len);
+void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int warps_per_scheduler);
 
 /*
  * Selective scan forward that allocates nothing (no counterpart on the pages:

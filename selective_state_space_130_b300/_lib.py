@@ -32,7 +32,7 @@ SIGNATURES = {
                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ss_scan_fwd_noalloc": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "ss_scan_set_tuning": (None, [ctypes.c_int, _I64]),
+    "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
 }
 
@@ -106,8 +106,8 @@ def ss_last_error() -> str:
     return lib().ss_last_error().decode()
 
 
-def ss_scan_set_tuning(threads_per_channel: int = 0, chunk_len: int = 0):
-    lib().ss_scan_set_tuning(int(threads_per_channel), int(chunk_len))
+def ss_scan_set_tuning(threads_per_channel: int = 0, chunk_len: int = 0, warps_per_scheduler: int = 0):
+    lib().ss_scan_set_tuning(int(threads_per_channel), int(chunk_len), int(warps_per_scheduler))
 
 
 def ss_scan_fwd_workspace_size(batch, seqlen, dim, dstate=16) -> int:

@@ -12,21 +12,17 @@
 
 #include "ss_internal.h"
 
-namespace ssk {
-int scan_channels_per_block(int sg);
-int scan_tile_len();
-int scan_header_words();
-uint32_t scan_header_magic();
-}  // namespace ssk
-
 namespace {
 
 thread_local std::string g_err;
 thread_local int g_tune_sg = 0;           // 0 = automatic
 thread_local int64_t g_tune_chunk = 0;    // 0 = automatic
+thread_local int g_tune_wps = 0;          // warps per SM sub-partition; 0 = automatic
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0
 constexpr int kSMs = 148;
+constexpr int kSchedulers = kSMs * 4;  // SM sub-partitions (warp schedulers)
+constexpr int64_t kMinChunk = 8192;    // shortest sequence chunk of the chunked mode
 
 ss_status fail(ss_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ss_status fail(ss_status st, const char* fmt, ...) {
@@ -75,62 +71,94 @@ size_t dsize(ss_dtype t) { return t == SS_BF16 ? 2 : 4; }
 
 namespace ssk {
 
-ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim) {
+ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype) {
   ScanPlan pl{};
   int sg = g_tune_sg;
-  if (sg != 1 && sg != 2 && sg != 4) sg = 2;
+  // one lane per channel costs the fewest instructions per state update; two
+  // lanes per channel halve each lane's work, which pays only when there are
+  // too few channel blocks to give every other SM sub-partition a warp
+  if (sg != 1 && sg != 2) sg = batch * ((dim + 31) / 32) >= kSchedulers / 2 ? 1 : 2;
   pl.sg = sg;
-  pl.cblk = scan_channels_per_block(sg);
+  pl.cblk = scan_channels_per_warp(sg);
   const int tile = scan_tile_len();
-  // Blocks are single warps; split the sequence only when the channel blocks
-  // alone would leave SMs short of warps (target about eight per SM).
-  const int64_t base_warps = batch * ((dim + pl.cblk - 1) / pl.cblk);
-  const int64_t target = (int64_t)kSMs * 8;
-  const int64_t min_chunk = 8192;
-  int64_t chunk = seqlen;
+  const int64_t ncblk = (dim + pl.cblk - 1) / pl.cblk;
+  const int64_t nblk = batch * ncblk;
+  const int64_t T = seqlen > 0 ? (seqlen + tile - 1) / tile : 1;
+  const int wps = (g_tune_wps >= 1 && g_tune_wps <= 4) ? g_tune_wps : 2;
+  const int64_t target = (int64_t)kSMs * std::min(scan_warps_per_sm(in_dtype, sg), 4 * wps);
+  pl.mode = kModeStatic;
+  pl.nworkers = nblk;
+  pl.chunk_tiles = T;
+  pl.nchunks = 1;
   if (g_tune_chunk > 0) {
-    chunk = g_tune_chunk;
-  } else if (base_warps < target / 2 && seqlen >= 2 * min_chunk) {
-    int64_t k = (target + base_warps - 1) / base_warps;
-    k = std::min<int64_t>(k, seqlen / min_chunk);
-    chunk = (seqlen + k - 1) / k;
+    pl.chunk_tiles = std::max<int64_t>(1, (g_tune_chunk + tile - 1) / tile);
+  } else if (nblk >= kSchedulers) {
+    // equal ranges for a multiple of the scheduler count; at least one block
+    // per range keeps every hand-over one level deep
+    const int64_t g = std::min(target, (nblk / kSchedulers) * kSchedulers);
+    if (g < nblk) {
+      pl.mode = kModeStreamK;
+      pl.nworkers = g;
+    }
+  } else if (seqlen >= 2 * kMinChunk) {
+    int64_t k = (target + nblk - 1) / nblk;
+    k = std::min<int64_t>(k, seqlen / kMinChunk);
+    pl.chunk_tiles = (T + k - 1) / k;
   }
-  chunk = std::max<int64_t>(tile, ((chunk + tile - 1) / tile) * tile);
-  pl.chunk_len = chunk;
-  pl.nchunks = seqlen > 0 ? (int)((seqlen + chunk - 1) / chunk) : 1;
+  if (pl.chunk_tiles < T) {
+    pl.nchunks = (int)((T + pl.chunk_tiles - 1) / pl.chunk_tiles);
+    if (pl.nchunks > 1) {
+      pl.mode = kModeChunked;
+      pl.nworkers = nblk * pl.nchunks;
+    }
+  }
+  const size_t hdr = (size_t)scan_header_words() * 4;
   pl.workspace = 0;
-  if (pl.nchunks > 1) {
-    const int64_t ncblk = (dim + pl.cblk - 1) / pl.cblk;
-    const int64_t tiles = batch * ncblk * pl.nchunks;
-    const size_t head = (size_t)scan_header_words() * 4 + (((size_t)tiles * 4 + 255) & ~size_t(255));
-    pl.workspace = head + (size_t)tiles * pl.cblk * 48 * sizeof(float);
+  if (pl.mode == kModeStreamK) {
+    pl.workspace = hdr + (((size_t)pl.nworkers * 4 + 255) & ~size_t(255)) +
+                   (size_t)pl.nworkers * pl.cblk * kDState * sizeof(float);
+  } else if (pl.mode == kModeChunked) {
+    const int64_t items = nblk * pl.nchunks;
+    pl.workspace = hdr + (((size_t)items * 4 + 255) & ~size_t(255)) + (size_t)items * pl.cblk * 48 * sizeof(float);
   }
   return pl;
 }
 
+size_t scan_bind_workspace(ScanParams& p, const ScanPlan& plan, void* workspace) {
+  const int64_t ncblk = (p.dim + plan.cblk - 1) / plan.cblk;
+  p.ncblk = (int)ncblk;
+  p.nblk = p.batch * ncblk;
+  p.tiles_per_blk = p.seqlen > 0 ? (p.seqlen + scan_tile_len() - 1) / scan_tile_len() : 1;
+  p.mode = plan.mode;
+  p.nworkers = plan.nworkers;
+  p.chunk_tiles = plan.chunk_tiles;
+  p.nchunks = plan.nchunks;
+  p.ws_header = nullptr;
+  p.flags = nullptr;
+  p.ws_carry = nullptr;
+  if (plan.mode == kModeStatic || !workspace) return 0;
+  const int64_t nflags = plan.mode == kModeStreamK ? plan.nworkers : p.nblk * plan.nchunks;
+  const size_t hdr = (size_t)scan_header_words() * 4;
+  const size_t clear = hdr + (((size_t)nflags * 4 + 255) & ~size_t(255));
+  p.ws_header = static_cast<uint32_t*>(workspace);
+  p.flags = p.ws_header + scan_header_words();
+  p.ws_carry = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + clear);
+  return clear;
+}
+
 }  // namespace ssk
 
-extern "C" {
+namespace {
 
-int ss_version(void) { return kVersion; }
-
-const char* ss_last_error(void) { return g_err.c_str(); }
-
-void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len) {
-  g_tune_sg = threads_per_channel;
-  g_tune_chunk = chunk_len;
-}
-
-size_t ss_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
-  if (batch <= 0 || seqlen <= 0 || dim <= 0 || dstate != ssk::kDState) return 0;
-  return ssk::plan_scan(batch, seqlen, dim).workspace;
-}
-
-ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
+// Argument checks, planning and launch shared by ss_scan_fwd and
+// ss_scan_fwd_noalloc. `workspace` is the caller's buffer or the library's
+// scratch; `own_fault` routes device-side timeouts to the library's fault word
+// instead of the workspace header.
+ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
                       ss_dtype out_dtype, const void* u, const void* delta_raw, const float* A, const void* B,
                       const void* C, const float* D, const void* z, const float* delta_bias, const float* h0,
-                      void* y, float* h_last, void* workspace, size_t workspace_bytes, void* stream) {
-  g_err.clear();
+                      void* y, float* h_last, void* workspace, size_t workspace_bytes, bool noalloc,
+                      void* stream) {
   if (dstate != ssk::kDState) return fail(SS_ERR_UNSUPPORTED, "dstate must be 16 (got %lld)", (long long)dstate);
   if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
     return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, out %d)", (int)in_dtype, (int)out_dtype);
@@ -151,21 +179,26 @@ ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last", "workspace"};
   for (int i = 0; i < 12; i++)
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim, in_dtype);
+  if (seqlen > 0 && plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) {
+    if (noalloc)
+      return fail(SS_ERR_INVALID_ARG,
+                  "this problem needs %zu bytes of scratch; the no-allocation scan holds at most %zu (use ss_scan_fwd "
+                  "with a caller-provided workspace)",
+                  plan.workspace, workspace_bytes);
+    return fail(SS_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu%s)", plan.workspace, workspace_bytes,
+                workspace ? "" : ", NULL");
+  }
   ss_status st = check_device();
   if (st != SS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t hbytes = (size_t)batch * dim * ssk::kDState * sizeof(float);
   if (seqlen == 0) {
     if (!h_last) return SS_OK;
+    const size_t hbytes = (size_t)batch * dim * ssk::kDState * sizeof(float);
     cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, hbytes, cudaMemcpyDeviceToDevice, s)
                        : cudaMemsetAsync(h_last, 0, hbytes, s);
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
   }
-
-  const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen, dim);
-  if (plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace))
-    return fail(SS_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu%s)", plan.workspace, workspace_bytes,
-                workspace ? "" : ", NULL");
 
   ssk::ScanParams p{};
   p.u = u;
@@ -182,33 +215,62 @@ ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   p.batch = batch;
   p.seqlen = seqlen;
   p.dim = dim;
-  p.chunk_len = plan.chunk_len;
-  p.nchunks = plan.nchunks;
-  p.ncblk = (int)((dim + plan.cblk - 1) / plan.cblk);
-  if ((double)batch * p.ncblk * p.nchunks > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
-  // The fault word lives in the workspace header when a workspace is given
-  // (so ss_scan_status(workspace) reads what this call wrote), else in the
-  // library's own device word. The header is cleared on the stream first.
+  if ((double)plan.nworkers > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
+  size_t clear = ssk::scan_bind_workspace(p, plan, plan.workspace > 0 ? workspace : nullptr);
+  // The fault word: the workspace header when the caller gave a workspace (so
+  // ss_scan_status(workspace) reads what this call wrote), else the library's
+  // own device word (ss_scan_status(NULL)).
   const size_t hdr = (size_t)ssk::scan_header_words() * 4;
-  if (workspace && workspace_bytes >= hdr) {
-    p.ws_header = static_cast<uint32_t*>(workspace);
-    p.fault = p.ws_header + 1;
-    size_t clear = hdr;
-    if (plan.nchunks > 1) {
-      const int64_t tiles = batch * (int64_t)p.ncblk * plan.nchunks;
-      clear = hdr + (((size_t)tiles * 4 + 255) & ~size_t(255));
-      p.ws_carry = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + clear);
+  if (!noalloc && workspace && workspace_bytes >= hdr) {
+    if (!p.ws_header) {
+      p.ws_header = static_cast<uint32_t*>(workspace);
+      clear = hdr;
     }
-    cudaError_t e = cudaMemsetAsync(workspace, 0, clear, s);
-    if (e != cudaSuccess) return cuda_fail(e, "workspace initialisation");
+    p.fault = p.ws_header + 1;
   } else {
     p.fault = ssk::device_fault_word();
     if (!p.fault) return fail(SS_ERR_CUDA, "cannot resolve the library fault word");
   }
+  cudaError_t e;
+  if (clear > 0) {
+    // ticket counter, fault word and hand-over flags start at zero; a reused
+    // buffer keeps the previous call's values, so clear them on the stream
+    e = cudaMemsetAsync(p.ws_header, 0, clear, s);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace initialisation");
+  }
   const bool tma = ((size_t)dim * dsize(in_dtype)) % 16 == 0;
-  cudaError_t e = ssk::launch_scan_fwd(p, plan, in_dtype, out_dtype, tma, s);
+  e = ssk::launch_scan_fwd(p, plan, in_dtype, out_dtype, tma, s);
   if (e != cudaSuccess) return cuda_fail(e, "scan launch");
   return SS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ss_version(void) { return kVersion; }
+
+const char* ss_last_error(void) { return g_err.c_str(); }
+
+void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int warps_per_scheduler) {
+  g_tune_sg = threads_per_channel;
+  g_tune_chunk = chunk_len;
+  g_tune_wps = warps_per_scheduler;
+}
+
+size_t ss_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
+  if (batch <= 0 || seqlen <= 0 || dim <= 0 || dstate != ssk::kDState) return 0;
+  return std::max(ssk::plan_scan(batch, seqlen, dim, SS_F32).workspace,
+                  ssk::plan_scan(batch, seqlen, dim, SS_BF16).workspace);
+}
+
+ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
+                      ss_dtype out_dtype, const void* u, const void* delta_raw, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias, const float* h0,
+                      void* y, float* h_last, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  return scan_common(batch, seqlen, dim, dstate, in_dtype, out_dtype, u, delta_raw, A, B, C, D, z, delta_bias, h0, y,
+                     h_last, workspace, workspace_bytes, false, stream);
 }
 
 ss_status ss_state_update(int64_t batch, int64_t dim, int64_t dstate, ss_dtype in_dtype, ss_dtype out_dtype,
@@ -312,84 +374,24 @@ extern "C" ss_status ss_scan_fwd_noalloc(int64_t batch, int64_t seqlen, int64_t 
                                          const float* D, const void* z, const float* delta_bias, const float* h0,
                                          void* y, float* h_last, void* stream) {
   g_err.clear();
-  if (dstate != ssk::kDState) return fail(SS_ERR_UNSUPPORTED, "dstate must be 16 (got %lld)", (long long)dstate);
-  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
-    return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, out %d)", (int)in_dtype, (int)out_dtype);
-  if (batch < 0 || seqlen < 0 || dim < 0)
-    return fail(SS_ERR_INVALID_ARG, "negative size (batch %lld, seqlen %lld, dim %lld)", (long long)batch,
-                (long long)seqlen, (long long)dim);
-  if (batch > INT32_MAX || seqlen > INT32_MAX || dim > INT32_MAX)
-    return fail(SS_ERR_INVALID_ARG, "a size exceeds 2^31-1");
-  if (batch == 0 || dim == 0) return SS_OK;
-  if ((double)batch * (double)seqlen * (double)dim > 4.0e18) return fail(SS_ERR_INVALID_ARG, "problem too large");
-  const void* need[] = {u, delta_raw, A, B, C, y};
-  const char* names[] = {"u", "delta_raw", "A", "B", "C", "y"};
-  if (seqlen > 0) {
-    for (int i = 0; i < 6; i++)
-      if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
+  // sizes beyond the fixed scratch are refused before any device call
+  if (batch > 0 && seqlen > 0 && dim > 0 && dstate == ssk::kDState && valid_dtype(in_dtype)) {
+    const size_t need = ssk::plan_scan(batch, seqlen, dim, in_dtype).workspace;
+    if (need > (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES)
+      return fail(SS_ERR_INVALID_ARG,
+                  "this problem needs %zu bytes of scratch; the no-allocation scan holds at most %zu (use ss_scan_fwd "
+                  "with a caller-provided workspace)",
+                  need, (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES);
   }
-  const void* all[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, h_last};
-  const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last"};
-  for (int i = 0; i < 11; i++)
-    if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
-
-  const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim);
-  if (seqlen > 0 && plan.workspace > (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES)
-    return fail(SS_ERR_INVALID_ARG,
-                "this problem needs %zu bytes of scratch; the no-allocation scan holds at most %zu (use ss_scan_fwd "
-                "with a caller-provided workspace)",
-                plan.workspace, (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES);
-  ss_status st = check_device();
-  if (st != SS_OK) return st;
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   void* scratch = nullptr;
-  if ((st = noalloc_scratch(dev, &scratch)) != SS_OK) return st;
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (seqlen == 0) {
-    if (!h_last) return SS_OK;
-    const size_t hbytes = (size_t)batch * dim * ssk::kDState * sizeof(float);
-    e = h0 ? cudaMemcpyAsync(h_last, h0, hbytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(h_last, 0, hbytes, s);
-    return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
+  if (batch > 0 && dim > 0 && seqlen > 0) {
+    ss_status st = check_device();
+    if (st != SS_OK) return st;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if ((st = noalloc_scratch(dev, &scratch)) != SS_OK) return st;
   }
-
-  ssk::ScanParams p{};
-  p.u = u;
-  p.delta_raw = delta_raw;
-  p.z = z;
-  p.B = B;
-  p.C = C;
-  p.A = A;
-  p.D = D;
-  p.delta_bias = delta_bias;
-  p.h0 = h0;
-  p.y = y;
-  p.h_last = h_last;
-  p.batch = batch;
-  p.seqlen = seqlen;
-  p.dim = dim;
-  p.chunk_len = plan.chunk_len;
-  p.nchunks = plan.nchunks;
-  p.ncblk = (int)((dim + plan.cblk - 1) / plan.cblk);
-  if ((double)batch * p.ncblk * p.nchunks > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
-  // Device-side waits that give up are recorded in the library's own fault
-  // word, which ss_scan_status(NULL, stream) reads and clears.
-  p.fault = ssk::device_fault_word();
-  if (!p.fault) return fail(SS_ERR_CUDA, "cannot resolve the library fault word");
-  if (plan.nchunks > 1) {
-    // The scratch keeps the previous call's contents: the ticket counter and
-    // the per-chunk flags must start at zero, so clear them on the stream.
-    const int64_t tiles = batch * (int64_t)p.ncblk * plan.nchunks;
-    const size_t clear = (size_t)ssk::scan_header_words() * 4 + (((size_t)tiles * 4 + 255) & ~size_t(255));
-    p.ws_header = static_cast<uint32_t*>(scratch);
-    p.ws_carry = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + clear);
-    e = cudaMemsetAsync(scratch, 0, clear, s);
-    if (e != cudaSuccess) return cuda_fail(e, "scratch initialisation");
-  }
-  const bool tma = ((size_t)dim * dsize(in_dtype)) % 16 == 0;
-  e = ssk::launch_scan_fwd(p, plan, in_dtype, out_dtype, tma, s);
-  if (e != cudaSuccess) return cuda_fail(e, "scan launch");
-  return SS_OK;
+  return scan_common(batch, seqlen, dim, dstate, in_dtype, out_dtype, u, delta_raw, A, B, C, D, z, delta_bias, h0, y,
+                     h_last, scratch, SS_SCAN_NOALLOC_SCRATCH_BYTES, true, stream);
 }

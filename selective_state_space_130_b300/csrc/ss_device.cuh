@@ -57,6 +57,61 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- packed fp32x2
+// A pair of fp32 values in one 64-bit register pair, for the sm_100+ packed
+// FFMA2 / FMUL2 / FADD2 instructions (one issue slot for two lanes of work).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+// The unpack is a register-pair view (no instruction); the half that is not
+// returned is an unused asm output.
+#pragma nv_diagnostic push
+#pragma nv_diag_suppress 550
+__device__ __forceinline__ float f2lo(f2 r) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float f2hi(f2 r) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+  return b;
+}
+#pragma nv_diagnostic pop
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---------------------------------------------------------------- global stores
+// Output stores written as explicit, predicated st.global. The compiler then
+// knows they cannot alias shared memory (later shared-memory loads stay free to
+// move above them), and the guard is a predicate rather than a branch, so an
+// unrolled token loop stays one basic block that the scheduler can interleave.
+__device__ __forceinline__ void st_out(float* p, float v, bool on) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.f32 [%0], %1;\n\t}" ::"l"(p), "f"(v),
+               "r"((unsigned)on));
+}
+__device__ __forceinline__ void st_out(__nv_bfloat16* p, float v, bool on) {
+  const unsigned short b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.b16 [%0], %1;\n\t}" ::"l"(p), "h"(b),
+               "r"((unsigned)on));
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -13,7 +13,15 @@ namespace ssk {
 
 constexpr int kDState = 16;
 
-// Parameters of one scan launch (device pointers, sizes, flags).
+// How the (channel block, 32-step tile) work of one scan is split among warps.
+enum ScanMode : int {
+  kModeStatic = 0,   // one warp per channel block, whole sequence; no workspace
+  kModeStreamK = 1,  // contiguous equal ranges of the tile space per warp; states
+                     // handed over at block-interior range boundaries
+  kModeChunked = 2   // sequence chunks per block, carries combined by look-back
+};
+
+// Parameters of one scan launch (device pointers, sizes, schedule).
 struct ScanParams {
   const void* u;
   const void* delta_raw;
@@ -26,14 +34,20 @@ struct ScanParams {
   const float* h0;          // may be null
   void* y;
   float* h_last;            // may be null
-  // chunk carries (workspace), used when nchunks > 1
-  uint32_t* ws_header;      // [0] ticket counter, [1] fault word; then per-tile flags
-  float* ws_carry;          // per (tile, channel): P[16], S_local[16], S_incl[16]
+  // workspace (stream-K and chunked modes)
+  uint32_t* ws_header;      // [0] ticket counter, [1] fault word, [2] magic; may be null (static mode)
+  uint32_t* flags;          // stream-K: one per worker; chunked: one per (block, chunk)
+  float* ws_carry;          // stream-K: handed-over states [worker][channel][16];
+                            // chunked: per (block, chunk, channel) P[16], S_local[16], S_incl[16]
   unsigned int* fault;      // fault word (workspace header or the library's own)
   int64_t batch, seqlen, dim;
-  int64_t chunk_len;        // timesteps per chunk (multiple of the tile length)
-  int nchunks;              // chunks per sequence (1 = no split along L)
+  int mode;                 // ScanMode
   int ncblk;                // channel blocks per batch element
+  int64_t nblk;             // batch * ncblk
+  int64_t tiles_per_blk;    // ceil(seqlen / tile)
+  int64_t nworkers;         // warps with work (stream-K: ranges; chunked: nblk * nchunks)
+  int64_t chunk_tiles;      // chunked: tiles per chunk
+  int nchunks;              // chunked: chunks per block
 };
 
 // Parameters of one decode step.
@@ -53,18 +67,33 @@ struct StepParams {
 
 // Launch plan for a scan problem.
 struct ScanPlan {
-  int sg;             // threads per channel (1, 2 or 4); each owns 16/sg states
-  int cblk;           // channels per thread block
-  int nchunks;        // chunks per sequence
-  int64_t chunk_len;  // timesteps per chunk
-  size_t workspace;   // bytes of workspace needed
+  int sg;               // threads per channel (1 or 2); each owns 16/sg states
+  int cblk;             // channels per warp
+  int mode;             // ScanMode
+  int64_t nworkers;     // warps with work
+  int64_t chunk_tiles;  // chunked mode: tiles per chunk
+  int nchunks;          // chunked mode: chunks per block
+  size_t workspace;     // bytes of workspace needed
 };
 
-ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim);
+ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype);
+
+// Fill the schedule fields of `p` from `plan` and carve `workspace` (at least
+// plan.workspace bytes, may be null when that is 0). Returns the number of
+// leading workspace bytes that must be zero before the launch.
+size_t scan_bind_workspace(ScanParams& p, const ScanPlan& plan, void* workspace);
 
 // Launchers; return cudaSuccess or the launch error.
 cudaError_t launch_scan_fwd(const ScanParams& p, const ScanPlan& plan, ss_dtype in_dtype, ss_dtype out_dtype,
                             bool use_tma, cudaStream_t stream);
+
+// Shape constants of the scan kernels.
+int scan_channels_per_warp(int sg);
+int scan_tile_len();
+int scan_warps_per_block();
+int scan_header_words();
+uint32_t scan_header_magic();
+int scan_warps_per_sm(ss_dtype in_dtype, int sg);  // resident warps per SM allowed by shared memory
 cudaError_t launch_state_update(const StepParams& p, ss_dtype in_dtype, ss_dtype out_dtype, cudaStream_t stream);
 
 // The library's own fault word (device symbol), used when no workspace is given.

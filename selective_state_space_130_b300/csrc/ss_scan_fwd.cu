@@ -11,25 +11,20 @@ namespace ssk {
 // Fault word used by calls that are given no workspace.
 __device__ unsigned int g_fault_word = 0;
 
-int scan_channels_per_block(int sg) { return 32 / sg; }
+int scan_channels_per_warp(int sg) { return 32 / sg; }
 int scan_tile_len() { return scan_detail::kTile; }
+int scan_warps_per_block() { return scan_detail::kWarps; }
 int scan_header_words() { return scan_detail::kHeaderWords; }
 uint32_t scan_header_magic() { return scan_detail::kHeaderMagic; }
 
-int scan_smem_bytes(ss_dtype in_dtype, int sg) {
+int scan_warps_per_sm(ss_dtype in_dtype, int sg) {
   using scan_detail::Cfg;
-  if (in_dtype == SS_BF16) {
-    switch (sg) {
-      case 1: return Cfg<__nv_bfloat16, 1>::SMEM;
-      case 2: return Cfg<__nv_bfloat16, 2>::SMEM;
-      default: return Cfg<__nv_bfloat16, 4>::SMEM;
-    }
-  }
-  switch (sg) {
-    case 1: return Cfg<float, 1>::SMEM;
-    case 2: return Cfg<float, 2>::SMEM;
-    default: return Cfg<float, 4>::SMEM;
-  }
+  int blocks;
+  if (in_dtype == SS_BF16)
+    blocks = sg == 1 ? Cfg<__nv_bfloat16, 1>::BLOCKS_PER_SM : Cfg<__nv_bfloat16, 2>::BLOCKS_PER_SM;
+  else
+    blocks = sg == 1 ? Cfg<float, 1>::BLOCKS_PER_SM : Cfg<float, 2>::BLOCKS_PER_SM;
+  return blocks * scan_detail::kWarps;
 }
 
 unsigned int* device_fault_word() {

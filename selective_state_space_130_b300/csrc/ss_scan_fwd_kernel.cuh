@@ -1,39 +1,49 @@
 // Selective-scan (S6) forward kernel for sm_103a (template; instantiated per
 // input/output dtype pair in ss_scan_fwd_<in>_<out>.cu).
 //
-// Work decomposition. A thread block is ONE warp that owns DC = 32/SG
-// consecutive channels of one batch element over one chunk of the sequence.
-// Each channel's 16-element fp32 state lives in registers of SG lanes (16/SG
-// states each). Small one-warp blocks let the ~20k channels of a layer spread
-// evenly over the 148 SMs in a single wave (about nine warps per SM).
+// What one warp computes. A warp owns DC = 32/SG consecutive channels of one
+// batch element (a "channel block"). With SG = 1 each lane owns one channel and
+// all 16 of its fp32 states; with SG = 2 two lanes share a channel, 8 states
+// each. Per token the lane computes delta = softplus(delta_raw + bias),
+// Abar = 2^(delta * A * log2 e), h = Abar*h + (delta*u)*B, y = C.h + D*u and
+// y *= silu(z): the fused, SRAM-resident scan the Mamba pages describe (review
+// page, method step 2; "Transformer时代终结？" section 二.3), laid out for B300.
+// The state update runs on packed f32x2 FMUL2/FFMA2 (two states per issue
+// slot); the exponentials run on the MUFU pipe. On B300 that pair of pipes,
+// not HBM, bounds the exact fp32 recurrence: about 30 state updates per clock
+// per SM at best against 4 bytes of HBM traffic per 16 updates.
 //
-// Data path per block. Tiles of kTile timesteps flow through a kStages-deep
-// shared-memory ring: u, delta_raw, z ([kTile, DC] boxes) and the tile's B and
-// C rows ([kTile, 16] boxes) arrive by TMA (cp.async.bulk.tensor), completion
-// counted on one mbarrier per stage; the warp issues tile k+kStages-1 before it
-// waits for tile k. bf16 B/C rows are converted once per tile into an fp32
-// buffer that every channel of the block reads by broadcast. The warp then
-// walks the tile token by token: delta = softplus(delta_raw + bias),
-// Abar = 2^(delta * A * log2 e), h = Abar*h + (delta*u)*B, y = C.h + D*u,
-// y *= silu(z). With SG > 1 the SG lanes of a channel take turns computing the
-// per-token scalars (one token each) and exchange them by shuffle; the readout
-// is reduce-scattered so each lane stores one token. Only y and the final
-// state leave the chip: the fused, SRAM-resident scan of the Mamba pages
-// (review page, method step 2; "Transformer时代终结？" section 二.3), laid out
-// for B300 rather than translated.
+// Data path. Tiles of kTile timesteps stream through a kStages-deep ring in
+// the warp's shared memory: u, delta_raw, z ([kTile, DC] boxes) and the tile's
+// B and C rows ([kTile, 16]) arrive by TMA (cp.async.bulk.tensor) with
+// completion counted on one mbarrier per stage, issued by the warp itself
+// kStages-1 tiles ahead. bf16 B/C rows are widened once per tile into an fp32
+// buffer read by broadcast. Only y and the final state leave the chip. A
+// block holds kWarps independent warps (one per SM sub-partition).
 //
-// Long sequences are split into chunks so that enough warps run. A chunk's
-// carry pair (P = prod Abar = exp(A * sum delta), S = state reached from a zero
-// start) composes as (P1,S1) o (P2,S2) = (P1 P2, P2 S1 + S2) ("外文文献精读"
-// section 2.2 block combination; mlqm.cn tutorial section 6 associativity).
-// Chunks publish their pair to a workspace and resolve their incoming state by
-// decoupled look-back over predecessors (a single-pass chained scan; tickets
-// taken in launch order make every awaited predecessor a started block). A
-// chunk that started from zero then recomputes its head from the true
-// incoming state and stops once, for every state n, the carried-in part
-// P_t,n * h_in,n is at most 2^-24 of the true state (for A <= 0 it only decays
-// further), so the outputs equal the sequential recurrence up to fp32
-// rounding.
+// Work split (ScanMode).
+//  - static: one warp per channel block, the whole sequence.
+//  - stream-K: the (channel block, tile) space, block-major, is cut into
+//    nworkers equal contiguous ranges, at least one block long each, so a range
+//    crosses at most one block start in its interior... and holds at most one
+//    partial block at either end. A warp first runs the head of the block its
+//    range ends in (from that block's initial state) and hands the state at
+//    its range end to the next warp, then runs the rest of its range in order;
+//    the first segment, when it starts inside a block, waits for the state the
+//    previous warp handed over (almost always already there). Equal ranges keep
+//    every SM sub-partition equally busy whatever the channel count.
+//  - chunked (long sequences, few channel blocks): each block's sequence is
+//    cut into chunks run by different warps. A chunk's carry pair
+//    (P = prod Abar = exp(A * sum delta), S = state reached from zero) composes
+//    as (P1,S1) o (P2,S2) = (P1 P2, P2 S1 + S2) ("外文文献精读" section 2.2;
+//    mlqm.cn tutorial section 6). Chunks publish their pair and resolve their
+//    incoming state by decoupled look-back, then recompute their head from the
+//    true state until, for every state n, the carried-in part P_t,n * h_in,n is
+//    at most 2^-24 of h_t,n (for A <= 0 it only decays further): the outputs
+//    equal the sequential recurrence up to fp32 rounding.
+// Warps take their worker index from a ticket counter in launch order, so a
+// warp only ever waits for warps that have already started; every wait is
+// bounded and reports a timeout through the fault word.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -47,17 +57,22 @@ namespace scan_detail {
 
 constexpr int kTile = 32;    // timesteps per pipeline stage
 constexpr int kStages = 3;   // TMA ring depth
+constexpr int kWarps = 4;    // warps (independent workers) per block
+constexpr int kUnroll = 8;   // tokens per step of the token loop (written out by hand below)
 constexpr float kStopRel = 5.9604645e-8f;  // 2^-24
 
 constexpr uint32_t kFlagAggregate = 1u;
 constexpr uint32_t kFlagInclusive = 2u;
+constexpr uint32_t kFlagHanded = 1u;
 constexpr int kHeaderWords = 64;
 constexpr uint32_t kHeaderMagic = 0x53535753u;  // header word 2: "this call used the workspace"
+constexpr int kSmemPerSM = 233472;              // 228 KiB per SM, 1 KiB of it reserved per block
 
 template <typename TIn, int SG>
 struct Cfg {
   static constexpr int NS = kDState / SG;  // states per lane
-  static constexpr int DC = 32 / SG;       // channels per block (one warp)
+  static constexpr int NP = NS / 2;        // packed state pairs per lane
+  static constexpr int DC = 32 / SG;       // channels per warp
   static constexpr bool BF = sizeof(TIn) == 2;
   static constexpr int XB = kTile * DC * (int)sizeof(TIn);        // one u / delta_raw / z tile
   static constexpr int RB = kTile * kDState * (int)sizeof(TIn);   // one raw B or C tile
@@ -66,7 +81,9 @@ struct Cfg {
   static constexpr int OFF_BCF = kStages * STAGE;                  // fp32 B|C of the current tile (bf16 only)
   static constexpr int BCF = BF ? 2 * kTile * kDState * 4 : 0;
   static constexpr int OFF_BAR = OFF_BCF + BCF;
-  static constexpr int SMEM = OFF_BAR + kStages * 8 + 32 + 128;    // + alignment slack
+  static constexpr int WARP_SMEM = (OFF_BAR + kStages * 8 + 127) & ~127;
+  static constexpr int SMEM = kWarps * WARP_SMEM + 128;            // + base alignment slack
+  static constexpr int BLOCKS_PER_SM = kSmemPerSM / (SMEM + 1024);
 };
 
 // softplus(x) = log(1 + e^x), from w = e^x:
@@ -88,81 +105,44 @@ __device__ __forceinline__ float softplus_fast(float x) {
   return x > 20.f ? x : r;
 }
 
-struct TokenScalars {
-  float dl, du, post, gate;
-};
-
-template <int SG>
-__device__ __forceinline__ float reduce_scatter(const float (&part)[SG], int s) {
-  if constexpr (SG == 1) {
-    return part[0];
-  } else if constexpr (SG == 2) {
-    const float keep = s ? part[1] : part[0];
-    const float send = s ? part[0] : part[1];
-    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
-  } else {
-    const bool hi = (s & 2) != 0;
-    const float k0 = hi ? part[2] : part[0], k1 = hi ? part[3] : part[1];
-    const float o0 = hi ? part[0] : part[2], o1 = hi ? part[1] : part[3];
-    const float q0 = k0 + __shfl_xor_sync(0xffffffffu, o0, 2);
-    const float q1 = k1 + __shfl_xor_sync(0xffffffffu, o1, 2);
-    const bool lo = (s & 1) != 0;
-    return (lo ? q1 : q0) + __shfl_xor_sync(0xffffffffu, lo ? q0 : q1, 1);
-  }
-}
-
-template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, bool CHUNKED>
-__global__ void __launch_bounds__(32) scan_fwd_kernel(const __grid_constant__ ScanParams p,
-                                                      const __grid_constant__ CUtensorMap tm_u,
-                                                      const __grid_constant__ CUtensorMap tm_dr,
-                                                      const __grid_constant__ CUtensorMap tm_z,
-                                                      const __grid_constant__ CUtensorMap tm_b,
-                                                      const __grid_constant__ CUtensorMap tm_c) {
+template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, int MODE>
+__global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_constant__ ScanParams p,
+                                                                  const __grid_constant__ CUtensorMap tm_u,
+                                                                  const __grid_constant__ CUtensorMap tm_dr,
+                                                                  const __grid_constant__ CUtensorMap tm_z,
+                                                                  const __grid_constant__ CUtensorMap tm_b,
+                                                                  const __grid_constant__ CUtensorMap tm_c) {
   using K = Cfg<TIn, SG>;
-  constexpr int NS = K::NS, DC = K::DC;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  constexpr int NS = K::NS, NP = K::NP, DC = K::DC;
+  constexpr unsigned FULL = 0xffffffffu;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // 128-byte aligned base, derived from the shared array by pointer arithmetic
+  // only (a round trip through an integer would hide from the compiler that
+  // every tile access is a shared-memory access)
+  const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
+  uint8_t* smem = smem_raw + pad + warp * K::WARP_SMEM;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
-  const int lane = threadIdx.x;
-  const int s = lane % SG;
-  const int cw = lane / SG;  // channel within the block
+  const int s = lane % SG;   // which part of the channel's states this lane holds
+  const int cw = lane / SG;  // channel within the warp's block
   const int n0 = s * NS;
 
-  // ---- which (batch, channel block, chunk) this block owns
-  int vb = blockIdx.x;
-  if constexpr (CHUNKED) {
-    if (lane == 0) vb = (int)atomicAdd(p.ws_header, 1u);  // launch-order ticket
-    vb = __shfl_sync(0xffffffffu, vb, 0);
+  // ---- worker index
+  int64_t wid;
+  if constexpr (MODE == kModeStatic) {
+    wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+  } else {
+    uint32_t t = 0;
+    if (lane == 0) t = atomicAdd(p.ws_header, 1u);  // launch-order ticket
+    wid = __shfl_sync(FULL, t, 0);
   }
+  if (wid >= p.nworkers) return;
   if (lane == 0) {
     for (int i = 0; i < kStages; i++) mbar_init(&full[i], 1);
     fence_mbar_init();
-    if (p.ws_header && vb == 0) p.ws_header[2] = kHeaderMagic;
+    if (p.ws_header && wid == 0) p.ws_header[2] = kHeaderMagic;
   }
   __syncwarp();
-  const int per_chunk = (int)p.batch * p.ncblk;
-  const int chunk = CHUNKED ? vb / per_chunk : 0;
-  const int rem = CHUNKED ? vb % per_chunk : vb;
-  const int b = rem / p.ncblk, cb = rem % p.ncblk;
-  const int64_t L = p.seqlen, Dm = p.dim;
-  const int64_t t_begin = (int64_t)chunk * p.chunk_len;
-  const int64_t t_end = CHUNKED ? min(L, t_begin + p.chunk_len) : L;
-  const int n_tiles = (int)((t_end - t_begin + kTile - 1) / kTile);
-  const int64_t d = (int64_t)cb * DC + cw;
-  const bool dvalid = d < Dm;
-  const int x0 = cb * DC;
-
-  // ---- per-channel constants and the state
-  float A2[NS], h[NS];
-#pragma unroll
-  for (int n = 0; n < NS; n++) {
-    A2[n] = dvalid ? __ldg(p.A + d * kDState + n0 + n) * kLog2e : 0.f;
-    h[n] = (dvalid && p.h0 && chunk == 0) ? __ldg(p.h0 + ((int64_t)b * Dm + d) * kDState + n0 + n) : 0.f;
-  }
-  const float bias_d = (dvalid && p.delta_bias) ? __ldg(p.delta_bias + d) : 0.f;
-  const float D_d = (dvalid && p.D) ? __ldg(p.D + d) : 0.f;
-  TOut* const yout = static_cast<TOut*>(p.y);
-
   if (TMA && lane == 0) {
     tma_prefetch_desc(&tm_u);
     tma_prefetch_desc(&tm_dr);
@@ -171,22 +151,74 @@ __global__ void __launch_bounds__(32) scan_fwd_kernel(const __grid_constant__ Sc
     tma_prefetch_desc(&tm_c);
   }
 
-  int g_issued = 0, g_done = 0;  // tiles issued / consumed (mbarrier phase bookkeeping)
-  bool abort = false;
+  const int64_t T = p.tiles_per_blk, L = p.seqlen, Dm = p.dim;
+  const int ncblk = p.ncblk;
 
-  // Issue the loads of the tile starting at t0 into the next ring slot.
-  auto issue = [&](int64_t t0) {
-    const int st = g_issued % kStages;
+  // ---- the worker's steps: step q runs tile j of channel block blk
+  int64_t r0 = 0, zs = 0, zlen = 0, af = 0, nfull = 0, nsteps = 0;  // stream-K
+  int64_t cblk = 0, c = 0, j0 = 0, nk = 0;        // chunked
+  if constexpr (MODE == kModeStatic) {
+    nsteps = T;
+  } else if constexpr (MODE == kModeStreamK) {
+    const int64_t total = p.nblk * T;
+    r0 = wid * total / p.nworkers;
+    const int64_t r1 = (wid + 1) * total / p.nworkers;
+    const int64_t tail = r1 % T;  // tiles of the last block inside the range
+    if (tail != 0) {
+      zs = r1 - tail;
+      zlen = tail;
+    } else {
+      zs = r1;
+    }
+    const int64_t head = r0 % T;
+    af = head != 0 ? r0 - head + T : r0;  // first block start at or after r0
+    nfull = zs - af;                     // tiles of whole blocks
+    nsteps = r1 - r0;
+  } else {
+    c = wid / p.nblk;
+    cblk = wid % p.nblk;
+    j0 = c * p.chunk_tiles;
+    nk = min(T, j0 + p.chunk_tiles) - j0;
+    nsteps = c == 0 ? nk : 2 * nk;  // chunks after the first recompute their head
+  }
+  auto step_tile = [&](int64_t q, int64_t& blk, int64_t& j) {
+    if constexpr (MODE == kModeStatic) {
+      blk = wid;
+      j = q;
+    } else if constexpr (MODE == kModeStreamK) {
+      // the head of the last block (handed over to the next warp), then the
+      // whole blocks, then the first segment, which waits for the previous
+      // warp's hand-over: with ranges of at least one block that hand-over is
+      // already done by the time this warp gets there
+      const int64_t g = q < zlen ? zs + q : (q < zlen + nfull ? af + (q - zlen) : r0 + (q - zlen - nfull));
+      blk = g / T;
+      j = g - blk * T;
+    } else {
+      blk = cblk;
+      j = j0 + (q < nk ? q : q - nk);
+    }
+  };
+
+  // ---- TMA ring
+  int64_t q_issued = 0;
+  bool abort = false;
+  auto issue = [&](int64_t q) {
+    int64_t blk, j;
+    step_tile(q, blk, j);
+    const int st = (int)(q % kStages);
     uint8_t* base = smem + st * K::STAGE;
+    const int b = (int)(blk / ncblk);
+    const int x0 = (int)(blk % ncblk) * DC;
+    const int y0 = (int)(j * kTile);
     if constexpr (TMA) {
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_expect_tx(&full[st], (HAS_Z ? 3 : 2) * K::XB + 2 * K::RB);
-        tma_load_3d(base + K::OFF_U, &tm_u, x0, (int)t0, b, &full[st]);
-        tma_load_3d(base + K::OFF_DR, &tm_dr, x0, (int)t0, b, &full[st]);
-        if (HAS_Z) tma_load_3d(base + K::OFF_Z, &tm_z, x0, (int)t0, b, &full[st]);
-        tma_load_3d(base + K::OFF_B, &tm_b, 0, (int)t0, b, &full[st]);
-        tma_load_3d(base + K::OFF_C, &tm_c, 0, (int)t0, b, &full[st]);
+        tma_load_3d(base + K::OFF_U, &tm_u, x0, y0, b, &full[st]);
+        tma_load_3d(base + K::OFF_DR, &tm_dr, x0, y0, b, &full[st]);
+        if (HAS_Z) tma_load_3d(base + K::OFF_Z, &tm_z, x0, y0, b, &full[st]);
+        tma_load_3d(base + K::OFF_B, &tm_b, 0, y0, b, &full[st]);
+        tma_load_3d(base + K::OFF_C, &tm_c, 0, y0, b, &full[st]);
         mbar_arrive(&full[st]);
       }
     } else {
@@ -198,8 +230,8 @@ __global__ void __launch_bounds__(32) scan_fwd_kernel(const __grid_constant__ Sc
       TIn* sdr = reinterpret_cast<TIn*>(base + K::OFF_DR);
       TIn* sz = reinterpret_cast<TIn*>(base + K::OFF_Z);
       for (int i = lane; i < kTile * DC; i += 32) {
-        const int tt = i / DC, c = i % DC;
-        const int64_t t = t0 + tt, dd = (int64_t)x0 + c;
+        const int tt = i / DC, cc = i % DC;
+        const int64_t t = (int64_t)y0 + tt, dd = (int64_t)x0 + cc;
         TIn vu = from_f32<TIn>(0.f), vr = vu, vz = vu;
         if (t < L && dd < Dm) {
           const int64_t gi = ((int64_t)b * L + t) * Dm + dd;
@@ -216,7 +248,7 @@ __global__ void __launch_bounds__(32) scan_fwd_kernel(const __grid_constant__ Sc
       TIn* sB = reinterpret_cast<TIn*>(base + K::OFF_B);
       TIn* sC = reinterpret_cast<TIn*>(base + K::OFF_C);
       for (int i = lane; i < kTile * kDState; i += 32) {
-        const int64_t t = t0 + i / kDState;
+        const int64_t t = (int64_t)y0 + i / kDState;
         const bool ok = t < L;
         const int64_t gi = ((int64_t)b * L + (ok ? t : 0)) * kDState + i % kDState;
         sB[i] = ok ? gB[gi] : from_f32<TIn>(0.f);
@@ -225,36 +257,42 @@ __global__ void __launch_bounds__(32) scan_fwd_kernel(const __grid_constant__ Sc
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[st]);
     }
-    g_issued++;
   };
-
-  // Wait for the next ring slot; returns the fp32 B|C base of the tile
-  // (converted once here when the inputs are bf16).
-  auto acquire = [&]() -> const float* {
-    const int st = g_done % kStages;
-    if (!abort && !mbar_wait(&full[st], (g_done / kStages) & 1)) {
+  // issue every step below qmax not yet issued; the caller has synchronised
+  // the warp, so the ring slot being refilled is no longer read
+  auto issue_upto = [&](int64_t qmax) {
+    const int64_t lim = min(qmax, nsteps);
+    while (q_issued < lim) {
+      issue(q_issued);
+      q_issued++;
+    }
+  };
+  // wait for step q's tile; returns the fp32 B|C rows of the tile
+  auto acquire = [&](int64_t q) -> const float* {
+    const int st = (int)(q % kStages);
+    if (!abort && !mbar_wait(&full[st], (uint32_t)((q / kStages) & 1))) {
       abort = true;
       atomicOr(p.fault, kFaultTileWait);
     }
     __syncwarp();
     const uint8_t* base = smem + st * K::STAGE;
     if constexpr (K::BF) {
-      // lane r converts row r of B and of C
+      // lane r widens row r of B and of C
       const uint4* rb = reinterpret_cast<const uint4*>(base + K::OFF_B) + lane * 2;
       const uint4* rc = reinterpret_cast<const uint4*>(base + K::OFF_C) + lane * 2;
       float4* fb = reinterpret_cast<float4*>(smem + K::OFF_BCF) + lane * 4;
       float4* fc = reinterpret_cast<float4*>(smem + K::OFF_BCF + kTile * kDState * 4) + lane * 4;
 #pragma unroll
-      for (int q = 0; q < 2; q++) {
-        const uint4 vb4 = rb[q], vc4 = rc[q];
-        fb[2 * q] = make_float4(__uint_as_float(vb4.x << 16), __uint_as_float(vb4.x & 0xffff0000u),
-                                __uint_as_float(vb4.y << 16), __uint_as_float(vb4.y & 0xffff0000u));
-        fb[2 * q + 1] = make_float4(__uint_as_float(vb4.z << 16), __uint_as_float(vb4.z & 0xffff0000u),
-                                    __uint_as_float(vb4.w << 16), __uint_as_float(vb4.w & 0xffff0000u));
-        fc[2 * q] = make_float4(__uint_as_float(vc4.x << 16), __uint_as_float(vc4.x & 0xffff0000u),
-                                __uint_as_float(vc4.y << 16), __uint_as_float(vc4.y & 0xffff0000u));
-        fc[2 * q + 1] = make_float4(__uint_as_float(vc4.z << 16), __uint_as_float(vc4.z & 0xffff0000u),
-                                    __uint_as_float(vc4.w << 16), __uint_as_float(vc4.w & 0xffff0000u));
+      for (int qq = 0; qq < 2; qq++) {
+        const uint4 vb4 = rb[qq], vc4 = rc[qq];
+        fb[2 * qq] = make_float4(__uint_as_float(vb4.x << 16), __uint_as_float(vb4.x & 0xffff0000u),
+                                 __uint_as_float(vb4.y << 16), __uint_as_float(vb4.y & 0xffff0000u));
+        fb[2 * qq + 1] = make_float4(__uint_as_float(vb4.z << 16), __uint_as_float(vb4.z & 0xffff0000u),
+                                     __uint_as_float(vb4.w << 16), __uint_as_float(vb4.w & 0xffff0000u));
+        fc[2 * qq] = make_float4(__uint_as_float(vc4.x << 16), __uint_as_float(vc4.x & 0xffff0000u),
+                                 __uint_as_float(vc4.y << 16), __uint_as_float(vc4.y & 0xffff0000u));
+        fc[2 * qq + 1] = make_float4(__uint_as_float(vc4.z << 16), __uint_as_float(vc4.z & 0xffff0000u),
+                                     __uint_as_float(vc4.w << 16), __uint_as_float(vc4.w & 0xffff0000u));
       }
       __syncwarp();
       return reinterpret_cast<const float*>(smem + K::OFF_BCF);
@@ -263,201 +301,331 @@ __global__ void __launch_bounds__(32) scan_fwd_kernel(const __grid_constant__ Sc
     }
   };
 
-  // Per-token scalars of token tt of the current tile (this lane's channel).
-  auto scalars = [&](const uint8_t* base, int tt) -> TokenScalars {
-    const TIn* su = reinterpret_cast<const TIn*>(base + K::OFF_U);
-    const TIn* sdr = reinterpret_cast<const TIn*>(base + K::OFF_DR);
-    const TIn* sz = reinterpret_cast<const TIn*>(base + K::OFF_Z);
-    const float xu = to_f32(su[tt * DC + cw]);
-    TokenScalars r;
-    r.dl = softplus_fast(to_f32(sdr[tt * DC + cw]) + bias_d);
-    r.du = r.dl * xu;
-    r.post = D_d * xu;
-    r.gate = HAS_Z ? silu(to_f32(sz[tt * DC + cw])) : 1.f;
-    return r;
+  // ---- per-channel constants of the current block and the state
+  f2 A2p[NP], hp[NP];
+  float bias_d = 0.f, D_d = 0.f;
+  int64_t d = 0;
+  bool dvalid = false;
+  TOut* ycol = nullptr;  // y[b, 0, d]
+  int64_t hoff = 0;      // element offset of this lane's states in h0 / h_last
+  auto load_block = [&](int64_t blk) {
+    const int64_t b = blk / ncblk;
+    d = (blk % ncblk) * DC + cw;
+    dvalid = d < Dm;
+    const int64_t dc = dvalid ? d : 0;
+#pragma unroll
+    for (int i = 0; i < NP; i++) {
+      const float2 a = dvalid ? __ldg(reinterpret_cast<const float2*>(p.A + dc * kDState + n0) + i)
+                              : make_float2(0.f, 0.f);
+      A2p[i] = pk(a.x * kLog2e, a.y * kLog2e);
+    }
+    bias_d = (dvalid && p.delta_bias) ? __ldg(p.delta_bias + dc) : 0.f;
+    D_d = (dvalid && p.D) ? __ldg(p.D + dc) : 0.f;
+    ycol = static_cast<TOut*>(p.y) + (b * L) * Dm + dc;
+    hoff = (b * Dm + dc) * kDState + n0;
+  };
+  auto set_state_initial = [&]() {
+#pragma unroll
+    for (int i = 0; i < NP; i++) {
+      float2 v = make_float2(0.f, 0.f);
+      if (dvalid && p.h0) v = __ldg(reinterpret_cast<const float2*>(p.h0 + hoff) + i);
+      hp[i] = pk(v.x, v.y);
+    }
   };
 
-  float ssum = 0.f;  // sum of delta over the tokens consumed in the current pass
-
-  // One group of SG tokens starting at token tg of the tile; the first
-  // `nvalid` tokens of the group are real (SG for full tiles).
-  auto group = [&](const float* bcf, int tg, const TokenScalars& sc, int nvalid, TOut* yrow) {
-    float dlv[SG], duv[SG];
+  // One state update of this lane's NS states for one token; returns the
+  // lane's part of C.h.
+  auto update = [&](float dl, float du, const float* brow, const float* crow) -> float {
+    const f2 dl2 = pk(dl, dl), du2 = pk(du, du);
+    const ulonglong2* bq = reinterpret_cast<const ulonglong2*>(brow);
+    const ulonglong2* cq = reinterpret_cast<const ulonglong2*>(crow);
+    f2 acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
-    for (int j = 0; j < SG; j++) {
-      if constexpr (SG == 1) {
-        dlv[j] = sc.dl;
-        duv[j] = sc.du;
-      } else {
-        const int src = (lane & ~(SG - 1)) | j;
-        dlv[j] = __shfl_sync(0xffffffffu, sc.dl, src);
-        duv[j] = __shfl_sync(0xffffffffu, sc.du, src);
+    for (int i = 0; i < NP / 2; i++) {
+      const ulonglong2 bv = bq[i], cv = cq[i];
+      {
+        const f2 x = mul2(dl2, A2p[2 * i]);
+        const f2 a = pk(ex2(f2lo(x)), ex2(f2hi(x)));
+        hp[2 * i] = fma2(a, hp[2 * i], mul2(du2, bv.x));
+        acc0 = fma2(cv.x, hp[2 * i], acc0);
+      }
+      {
+        const f2 x = mul2(dl2, A2p[2 * i + 1]);
+        const f2 a = pk(ex2(f2lo(x)), ex2(f2hi(x)));
+        hp[2 * i + 1] = fma2(a, hp[2 * i + 1], mul2(du2, bv.y));
+        acc1 = fma2(cv.y, hp[2 * i + 1], acc1);
       }
     }
-    float part[SG];
+    const f2 a = add2(acc0, acc1);
+    return f2lo(a) + f2hi(a);
+  };
+
+  float ssum = 0.f;  // sum of delta over the tokens of the current pass (chunked mode)
+
+  // Run `tlen` tokens of the acquired tile (slot `st`) starting at timestep t0.
+  auto run_tile = [&](int st, const float* bcf, int64_t t0, int tlen) {
+    const uint8_t* base = smem + st * K::STAGE;
+    const TIn* su = reinterpret_cast<const TIn*>(base + K::OFF_U) + cw;
+    const TIn* sdr = reinterpret_cast<const TIn*>(base + K::OFF_DR) + cw;
+    const TIn* sz = reinterpret_cast<const TIn*>(base + K::OFF_Z) + cw;
+    const float* brow = bcf + n0;
+    const float* crow = bcf + kTile * kDState + n0;
+    if constexpr (SG == 1) {
+      TOut* yp = ycol + t0 * Dm;
+      auto token = [&](int tt) {
+        const float xu = to_f32(su[tt * DC]);
+        const float dl = softplus_fast(to_f32(sdr[tt * DC]) + bias_d);
+        const float g = HAS_Z ? silu(to_f32(sz[tt * DC])) : 1.f;
+        const float yv = update(dl, dl * xu, brow + tt * kDState, crow + tt * kDState);
+        st_out(yp + tt * Dm, fmaf(D_d, xu, yv) * g, dvalid);
+        if constexpr (MODE == kModeChunked) ssum += dl;
+      };
+      if (tlen == kTile) {
+        // eight tokens of straight-line code per iteration: the scheduler
+        // overlaps one token's scalar chain with its neighbours' state updates
+#pragma unroll 1
+        for (int tt = 0; tt < kTile; tt += kUnroll) {
+          token(tt);
+          token(tt + 1);
+          token(tt + 2);
+          token(tt + 3);
+          token(tt + 4);
+          token(tt + 5);
+          token(tt + 6);
+          token(tt + 7);
+        }
+      } else {
+#pragma unroll 1
+        for (int tt = 0; tt < tlen; tt++) token(tt);
+      }
+    } else {
+      // token pair (tt, tt+1): lane s computes the scalars of token tt+s and
+      // stores its y; the pair exchanges (delta, delta*u) and the halves of C.h
+      TOut* yp = ycol + (t0 + s) * Dm;
+      auto pair = [&](int tt, bool two) {
+        const int tm = tt + s;  // may be tlen for an odd tail: a row of the tile buffer, unused
+        const float xu = to_f32(su[tm * DC]);
+        const float dl = softplus_fast(to_f32(sdr[tm * DC]) + bias_d);
+        const float g = HAS_Z ? silu(to_f32(sz[tm * DC])) : 1.f;
+        const float du = dl * xu;
+        const float dlo = __shfl_xor_sync(FULL, dl, 1), duo = __shfl_xor_sync(FULL, du, 1);
+        const float pa = update(s ? dlo : dl, s ? duo : du, brow + tt * kDState, crow + tt * kDState);
+        float pb = 0.f;
+        if (two) pb = update(s ? dl : dlo, s ? du : duo, brow + (tt + 1) * kDState, crow + (tt + 1) * kDState);
+        const float keep = s ? pb : pa, send = s ? pa : pb;
+        const float yv = keep + __shfl_xor_sync(FULL, send, 1);
+        st_out(yp + tt * Dm, fmaf(D_d, xu, yv) * g, dvalid && (two || s == 0));
+        if constexpr (MODE == kModeChunked) ssum += (s ? dlo : dl) + (two ? (s ? dl : dlo) : 0.f);
+      };
+      if (tlen == kTile) {
+#pragma unroll 1
+        for (int tt = 0; tt < kTile; tt += kUnroll) {
+          pair(tt, true);
+          pair(tt + 2, true);
+          pair(tt + 4, true);
+          pair(tt + 6, true);
+        }
+      } else {
+#pragma unroll 1
+        for (int tt = 0; tt < tlen; tt += 2) pair(tt, tt + 1 < tlen);
+      }
+    }
+  };
+
+  auto store_h = [&](float* dst) {
 #pragma unroll
-    for (int j = 0; j < SG; j++) {
-      part[j] = 0.f;
-      if (j < nvalid) {
-        const float4* bq = reinterpret_cast<const float4*>(bcf + (tg + j) * kDState + n0);
-        const float4* cq = reinterpret_cast<const float4*>(bcf + kTile * kDState + (tg + j) * kDState + n0);
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-        for (int q = 0; q < NS / 4; q++) {
-          const float4 bv = bq[q], cv = cq[q];
-          const float bb[4] = {bv.x, bv.y, bv.z, bv.w}, cc[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-          for (int k = 0; k < 4; k++) {
-            const int n = 4 * q + k;
-            const float a = ex2(dlv[j] * A2[n]);
-            h[n] = fmaf(a, h[n], duv[j] * bb[k]);
-            if (k & 1) acc1 = fmaf(cc[k], h[n], acc1);
-            else acc0 = fmaf(cc[k], h[n], acc0);
+    for (int i = 0; i < NP; i++) reinterpret_cast<float2*>(dst)[i] = make_float2(f2lo(hp[i]), f2hi(hp[i]));
+  };
+  // bounded wait (lane 0) for a flag to become nonzero; every lane then
+  // acquires it itself. Returns the flag value (forced nonzero on timeout).
+  auto wait_flag = [&](uint32_t* f) -> uint32_t {
+    uint32_t v = 0;
+    if (lane == 0) {
+      v = ld_acquire_gpu(f);
+      if (v == 0 && !abort) {
+        const uint64_t tw = globaltimer();
+        while ((v = ld_acquire_gpu(f)) == 0) {
+          if (globaltimer() - tw > kWaitNs) {
+            atomicOr(p.fault, kFaultLookback);
+            abort = true;
+            break;
           }
         }
-        part[j] = acc0 + acc1;
-        if constexpr (CHUNKED) ssum += dlv[j];
       }
     }
-    const float yv = reduce_scatter<SG>(part, s);
-    if (s < nvalid && dvalid) *yrow = from_f32<TOut>((yv + sc.post) * sc.gate);
+    v = __shfl_sync(FULL, v, 0);
+    abort = __shfl_sync(FULL, abort ? 1 : 0, 0) != 0;
+    if (v != 0) v = ld_acquire_gpu(f);
+    return v == 0 ? kFlagInclusive : v;
   };
 
-  // Process the acquired tile of `tlen` tokens starting at timestep t0.
-  auto tile = [&](const float* bcf, int64_t t0, int tlen) {
-    const uint8_t* base = smem + (g_done % kStages) * K::STAGE;
-    TOut* yrow = yout + ((int64_t)b * L + t0 + s) * Dm + d;
-    const int64_t ystep = (int64_t)SG * Dm;
-    if (tlen == kTile) {
-      TokenScalars sc = scalars(base, s);
-#pragma unroll
-      for (int tg = 0; tg < kTile; tg += SG) {
-        TokenScalars nx = sc;
-        if (tg + SG < kTile) nx = scalars(base, tg + SG + s);  // next group's scalars, ahead of time
-        group(bcf, tg, sc, SG, yrow);
-        yrow += ystep;
-        sc = nx;
-      }
-    } else {
-      for (int tg = 0; tg < tlen; tg += SG) {
-        const int tt = tg + s;
-        TokenScalars sc{0.f, 0.f, 0.f, 1.f};
-        if (tt < tlen) sc = scalars(base, tt);
-        group(bcf, tg, sc, min(SG, tlen - tg), yrow);
-        yrow += ystep;
-      }
-    }
-  };
+  float hin[MODE == kModeChunked ? NS : 1];  // chunked: the true state entering the chunk
+  hin[0] = 0.f;
 
-  // Stream tiles [0, ntiles) of the chunk; with `stop_check`, stop after the
-  // first tile at whose end the carried-in part is negligible. Loads issued
-  // past the stop point are drained before returning.
-  auto pass = [&](int ntiles, bool stop_check, const float* hin) {
-    const int pre = min(kStages - 1, ntiles);
-    for (int i = 0; i < pre; i++) issue(t_begin + (int64_t)i * kTile);
-    for (int k = 0; k < ntiles; k++) {
-      if (k + kStages - 1 < ntiles) issue(t_begin + (int64_t)(k + kStages - 1) * kTile);
-      const float* bcf = acquire();
-      const int64_t t0 = t_begin + (int64_t)k * kTile;
-      tile(bcf, t0, (int)min((int64_t)kTile, t_end - t0));
-      g_done++;
-      if (stop_check && k + 1 < ntiles) {
-        bool done = true;
-#pragma unroll
-        for (int n = 0; n < NS; n++) {
-          const float carried = fabsf(ex2(A2[n] * ssum) * hin[n]);
-          done = done && (A2[n] <= 0.f) && (carried <= kStopRel * fabsf(h[n]));
-        }
-        if (__all_sync(0xffffffffu, done || !dvalid) || abort) break;
-      }
-    }
-    while (g_done < g_issued) {
-      const int st = g_done % kStages;
-      if (!abort && !mbar_wait(&full[st], (g_done / kStages) & 1)) {
-        abort = true;
-        atomicOr(p.fault, kFaultTileWait);
-      }
-      g_done++;
-    }
-  };
-
-  pass(n_tiles, false, nullptr);
-
-  float* hl_out = (dvalid && p.h_last) ? p.h_last + ((int64_t)b * Dm + d) * kDState + n0 : nullptr;
-  if constexpr (!CHUNKED) {
-    if (hl_out) {
-#pragma unroll
-      for (int n = 0; n < NS; n++) hl_out[n] = h[n];
-    }
-  } else {
-    // ---- chunk carries: publish the local pair, look back, publish inclusive
-    const int64_t tile_id = ((int64_t)b * p.ncblk + cb) * p.nchunks + chunk;
-    uint32_t* flags = p.ws_header + kHeaderWords;
-    float* carry_me = p.ws_carry + ((size_t)tile_id * DC + cw) * 48 + n0;
-    if (chunk == 0) {
-#pragma unroll
-      for (int n = 0; n < NS; n++) carry_me[32 + n] = h[n];
-    } else {
-#pragma unroll
-      for (int n = 0; n < NS; n++) {
-        carry_me[n] = ex2(A2[n] * ssum);  // P = exp(A * sum delta)
-        carry_me[16 + n] = h[n];          // S = state from a zero start
-      }
-    }
-    __threadfence();
+  // ---- main loop over the worker's steps
+  issue_upto(kStages - 1);
+  int64_t q = 0;
+  for (; q < nsteps; q++) {
     __syncwarp();
-    if (lane == 0) st_release_gpu(&flags[tile_id], chunk == 0 ? kFlagInclusive : kFlagAggregate);
-    if (chunk == 0) return;
+    issue_upto(q + kStages);
+    int64_t blk, j;
+    step_tile(q, blk, j);
 
-    float Pa[NS], Sa[NS];
+    // segment start: per-channel constants and the incoming state
+    if constexpr (MODE == kModeStatic) {
+      if (q == 0) {
+        load_block(blk);
+        set_state_initial();
+      }
+    } else if constexpr (MODE == kModeStreamK) {
+      if (q == 0 || q == zlen || q == zlen + nfull || j == 0) {
+        load_block(blk);
+        if (j == 0) {
+          set_state_initial();
+        } else {
+          // the first segment starts inside a block: take the state the
+          // previous worker handed over at this range boundary
+          wait_flag(p.flags + wid);
+          const float* src = p.ws_carry + (size_t)wid * DC * kDState + cw * kDState + n0;
 #pragma unroll
-    for (int n = 0; n < NS; n++) {
-      Pa[n] = 1.f;
-      Sa[n] = 0.f;
+          for (int i = 0; i < NP; i++) {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(src) + i);
+            hp[i] = pk(v.x, v.y);
+          }
+        }
+      }
+    } else {
+      if (q == 0) {
+        load_block(blk);
+        if (c == 0) set_state_initial();
+        else
+          for (int i = 0; i < NP; i++) hp[i] = 0ull;
+        ssum = 0.f;
+      }
     }
-    for (int j = chunk - 1; j >= 0; j--) {
-      const int64_t pid = tile_id - (chunk - j);
-      uint32_t f = 0;
-      if (lane == 0) {
-        f = ld_acquire_gpu(&flags[pid]);
-        if (f == 0 && !abort) {
-          const uint64_t tw = globaltimer();
-          while ((f = ld_acquire_gpu(&flags[pid])) == 0) {
-            if (globaltimer() - tw > kWaitNs) {
-              atomicOr(p.fault, kFaultLookback);
-              f = kFlagInclusive;  // give up: treat as resolved
+
+    const float* bcf = acquire(q);
+    const int64_t t0 = j * kTile;
+    run_tile((int)(q % kStages), bcf, t0, (int)min((int64_t)kTile, L - t0));
+
+    // segment end: final state or hand-over
+    if constexpr (MODE == kModeStatic) {
+      if (j == T - 1 && dvalid && p.h_last) store_h(p.h_last + hoff);
+    } else if constexpr (MODE == kModeStreamK) {
+      if (j == T - 1) {
+        if (dvalid && p.h_last) store_h(p.h_last + hoff);
+      } else if (q + 1 == zlen) {
+        float* dst = p.ws_carry + (size_t)(wid + 1) * DC * kDState + cw * kDState + n0;
+        store_h(dst);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.flags + wid + 1, kFlagHanded);
+      }
+    } else {
+      if (q == nk - 1) {
+        // ---- end of the first pass: publish the chunk's carry, look back
+        const int64_t tile_id = cblk * p.nchunks + c;
+        float* carry_me = p.ws_carry + ((size_t)tile_id * DC + cw) * 48 + n0;
+        float hl[NS];
+#pragma unroll
+        for (int i = 0; i < NP; i++) {
+          hl[2 * i] = f2lo(hp[i]);
+          hl[2 * i + 1] = f2hi(hp[i]);
+        }
+        float A2[NS];
+#pragma unroll
+        for (int i = 0; i < NP; i++) {
+          A2[2 * i] = f2lo(A2p[i]);
+          A2[2 * i + 1] = f2hi(A2p[i]);
+        }
+        if (c == 0) {
+#pragma unroll
+          for (int n = 0; n < NS; n++) carry_me[32 + n] = hl[n];
+        } else {
+#pragma unroll
+          for (int n = 0; n < NS; n++) {
+            carry_me[n] = ex2(A2[n] * ssum);  // P = exp(A * sum delta)
+            carry_me[16 + n] = hl[n];         // S = state from a zero start
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.flags + tile_id, c == 0 ? kFlagInclusive : kFlagAggregate);
+        if (c > 0) {
+          float Pa[NS], Sa[NS];
+#pragma unroll
+          for (int n = 0; n < NS; n++) {
+            Pa[n] = 1.f;
+            Sa[n] = 0.f;
+          }
+          for (int64_t jj = c - 1; jj >= 0; jj--) {
+            const int64_t pid = tile_id - (c - jj);
+            const uint32_t f = wait_flag(p.flags + pid);
+            const float* cp = p.ws_carry + ((size_t)pid * DC + cw) * 48 + n0;
+            if (f == kFlagInclusive) {
+#pragma unroll
+              for (int n = 0; n < NS; n++) Sa[n] = fmaf(Pa[n], __ldcg(cp + 32 + n), Sa[n]);
               break;
             }
+#pragma unroll
+            for (int n = 0; n < NS; n++) {
+              Sa[n] = fmaf(Pa[n], __ldcg(cp + 16 + n), Sa[n]);
+              Pa[n] *= __ldcg(cp + n);
+            }
           }
+          // Sa is the true state entering this chunk
+          float Pend[NS];
+#pragma unroll
+          for (int n = 0; n < NS; n++) Pend[n] = carry_me[n];
+#pragma unroll
+          for (int n = 0; n < NS; n++) {
+            const float incl = fmaf(Pend[n], Sa[n], hl[n]);  // P_end * h_in + S_local
+            carry_me[32 + n] = incl;
+            hl[n] = incl;
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) st_release_gpu(p.flags + tile_id, kFlagInclusive);
+          if (c == p.nchunks - 1 && dvalid && p.h_last) {
+#pragma unroll
+            for (int n = 0; n < NS; n++) p.h_last[hoff + n] = hl[n];
+          }
+          // second pass: recompute the head from the true incoming state
+#pragma unroll
+          for (int i = 0; i < NP; i++) hp[i] = pk(Sa[2 * i], Sa[2 * i + 1]);
+#pragma unroll
+          for (int n = 0; n < NS; n++) hin[n] = Sa[n];
+          ssum = 0.f;
+        } else if (p.nchunks == 1 && dvalid && p.h_last) {
+          store_h(p.h_last + hoff);
+        }
+      } else if (q >= nk && q + 1 < nsteps) {
+        // second pass: stop once the carried-in part is negligible everywhere
+        bool done = true;
+#pragma unroll
+        for (int i = 0; i < NP; i++) {
+          const float a0 = f2lo(A2p[i]), a1 = f2hi(A2p[i]);
+          const float c0 = fabsf(ex2(a0 * ssum) * hin[2 * i]);
+          const float c1 = fabsf(ex2(a1 * ssum) * hin[2 * i + 1]);
+          done = done && a0 <= 0.f && a1 <= 0.f && c0 <= kStopRel * fabsf(f2lo(hp[i])) &&
+                 c1 <= kStopRel * fabsf(f2hi(hp[i]));
+        }
+        if (__all_sync(FULL, done || !dvalid)) {
+          q++;
+          break;
         }
       }
-      f = __shfl_sync(0xffffffffu, f, 0);
-      const float* cp = p.ws_carry + ((size_t)pid * DC + cw) * 48 + n0;
-      if (f == kFlagInclusive) {
-#pragma unroll
-        for (int n = 0; n < NS; n++) Sa[n] = fmaf(Pa[n], __ldcg(cp + 32 + n), Sa[n]);
-        break;
-      }
-#pragma unroll
-      for (int n = 0; n < NS; n++) {
-        Sa[n] = fmaf(Pa[n], __ldcg(cp + 16 + n), Sa[n]);
-        Pa[n] *= __ldcg(cp + n);
-      }
     }
-    // Sa is the true state entering this chunk
-#pragma unroll
-    for (int n = 0; n < NS; n++) {
-      const float incl = fmaf(carry_me[n], Sa[n], h[n]);  // P_end * h_in + S_local
-      carry_me[32 + n] = incl;
-      if (hl_out && chunk == p.nchunks - 1) hl_out[n] = incl;
-      h[n] = Sa[n];  // restart the head from the true incoming state
+    if (abort) {
+      q++;
+      break;
     }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_gpu(&flags[tile_id], kFlagInclusive);
-
-    ssum = 0.f;
-    pass(n_tiles, true, Sa);
+  }
+  // drain loads issued past the last consumed step (bounded waits)
+  __syncwarp();
+  for (int64_t qq = q; qq < q_issued; qq++) {
+    const int st = (int)(qq % kStages);
+    if (!mbar_wait(&full[st], (uint32_t)((qq / kStages) & 1))) atomicOr(p.fault, kFaultTileWait);
   }
 }
 
@@ -495,10 +663,10 @@ inline bool make_map(CUtensorMap* m, const void* ptr, size_t es, int64_t batch, 
   return r == CUDA_SUCCESS;
 }
 
-template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, bool CHUNKED>
+template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, int MODE>
 cudaError_t launch_t(const ScanParams& p, cudaStream_t stream) {
   using K = Cfg<TIn, SG>;
-  auto kern = scan_fwd_kernel<TIn, TOut, SG, TMA, HAS_Z, CHUNKED>;
+  auto kern = scan_fwd_kernel<TIn, TOut, SG, TMA, HAS_Z, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
   if (e != cudaSuccess) return e;
   CUtensorMap mu{}, mdr{}, mz{}, mb{}, mc{};
@@ -511,19 +679,28 @@ cudaError_t launch_t(const ScanParams& p, cudaStream_t stream) {
         !make_map(&mc, p.C, es, p.batch, p.seqlen, kDState, kDState))
       return cudaErrorInvalidValue;
   }
-  const int64_t nblk = p.batch * (int64_t)p.ncblk * p.nchunks;
-  kern<<<(unsigned)nblk, 32, K::SMEM, stream>>>(p, mu, mdr, mz, mb, mc);
+  // the split modes place kWarps workers per block, one per SM sub-partition;
+  // one-warp blocks spread the few warps of the static mode over all SMs
+  const int wpb = MODE == kModeStatic ? 1 : kWarps;
+  const int64_t nblocks = (p.nworkers + wpb - 1) / wpb;
+  const int smem = wpb * K::WARP_SMEM + 128;
+  kern<<<(unsigned)nblocks, 32 * wpb, smem, stream>>>(p, mu, mdr, mz, mb, mc);
   return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z>
+cudaError_t launch_m(const ScanParams& p, cudaStream_t stream) {
+  switch (p.mode) {
+    case kModeStatic: return launch_t<TIn, TOut, SG, TMA, HAS_Z, kModeStatic>(p, stream);
+    case kModeStreamK: return launch_t<TIn, TOut, SG, TMA, HAS_Z, kModeStreamK>(p, stream);
+    case kModeChunked: return launch_t<TIn, TOut, SG, TMA, HAS_Z, kModeChunked>(p, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <typename TIn, typename TOut, int SG, bool TMA>
 cudaError_t launch_z(const ScanParams& p, cudaStream_t stream) {
-  const bool hz = p.z != nullptr, ch = p.nchunks > 1;
-  if (hz)
-    return ch ? launch_t<TIn, TOut, SG, TMA, true, true>(p, stream)
-              : launch_t<TIn, TOut, SG, TMA, true, false>(p, stream);
-  return ch ? launch_t<TIn, TOut, SG, TMA, false, true>(p, stream)
-            : launch_t<TIn, TOut, SG, TMA, false, false>(p, stream);
+  return p.z ? launch_m<TIn, TOut, SG, TMA, true>(p, stream) : launch_m<TIn, TOut, SG, TMA, false>(p, stream);
 }
 
 template <typename TIn, typename TOut, int SG>
@@ -536,7 +713,6 @@ cudaError_t launch_io(const ScanParams& p, int sg, bool tma, cudaStream_t stream
   switch (sg) {
     case 1: return launch_sg<TIn, TOut, 1>(p, tma, stream);
     case 2: return launch_sg<TIn, TOut, 2>(p, tma, stream);
-    case 4: return launch_sg<TIn, TOut, 4>(p, tma, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -99,9 +99,10 @@ def test_state_update_rejects_bad_arguments():
 
 
 def test_workspace_size_queries():
-    assert ss.ss_scan_fwd_workspace_size(4, 2048, 5120) == 0          # short sequences need none
+    assert ss.ss_scan_fwd_workspace_size(1, 512, 256) == 0             # few blocks, short: one warp per block
+    assert ss.ss_scan_fwd_workspace_size(4, 2048, 5120) > 0            # equal-range split hands states over
     ws = ss.ss_scan_fwd_workspace_size(1, 1 << 20, 1024)
-    assert ws > 0                                                     # long sequences are split
+    assert ws > 0                                                     # long sequences are split into chunks
     assert ss.ss_scan_fwd_workspace_size(1, 1 << 20, 1024, 8) == 0     # unsupported dstate
     ss.ss_scan_set_tuning(2, 64)
     try:
