@@ -181,35 +181,67 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     nk = min(T, j0 + p.chunk_tiles) - j0;
     nsteps = c == 0 ? nk : 2 * nk;  // chunks after the first recompute their head
   }
-  auto step_tile = [&](int64_t q, int64_t& blk, int64_t& j) {
+  // Step cursor: step q runs tile j of channel block blk from ring slot st
+  // (mbarrier phase ph). Advancing costs a compare and an add; the divisions
+  // that place a cursor happen only where a new segment or block begins.
+  struct Cursor {
+    int64_t q, blk, j;
+    int b, x0, st;
+    uint32_t ph;
+  };
+  auto place = [&](Cursor& c) {  // (blk, j) and the block's coordinates for step c.q
     if constexpr (MODE == kModeStatic) {
-      blk = wid;
-      j = q;
+      c.blk = wid;
+      c.j = c.q;
     } else if constexpr (MODE == kModeStreamK) {
       // the head of the last block (handed over to the next warp), then the
       // whole blocks, then the first segment, which waits for the previous
       // warp's hand-over: with ranges of at least one block that hand-over is
       // already done by the time this warp gets there
+      const int64_t q = c.q;
       const int64_t g = q < zlen ? zs + q : (q < zlen + nfull ? af + (q - zlen) : r0 + (q - zlen - nfull));
-      blk = g / T;
-      j = g - blk * T;
+      c.blk = g / T;
+      c.j = g - c.blk * T;
     } else {
-      blk = cblk;
-      j = j0 + (q < nk ? q : q - nk);
+      c.blk = cblk;
+      c.j = j0 + (c.q < nk ? c.q : c.q - nk);
+    }
+    c.b = (int)(c.blk / ncblk);
+    c.x0 = (int)(c.blk - (int64_t)c.b * ncblk) * DC;
+  };
+  auto advance = [&](Cursor& c) {
+    c.q++;
+    if (++c.st == kStages) {
+      c.st = 0;
+      c.ph ^= 1u;
+    }
+    bool jump = false;
+    if constexpr (MODE == kModeStreamK) jump = c.q == zlen || c.q == zlen + nfull;
+    if constexpr (MODE == kModeChunked) jump = c.q == nk;
+    if (jump) {
+      place(c);
+    } else if (++c.j == T) {
+      c.j = 0;
+      c.blk++;
+      c.x0 += DC;
+      if (c.x0 >= ncblk * DC) {
+        c.x0 = 0;
+        c.b++;
+      }
     }
   };
+  Cursor ci{0, 0, 0, 0, 0, 0, 0u};  // next step to issue
+  place(ci);
+  Cursor cc = ci;                   // next step to consume
 
   // ---- TMA ring
-  int64_t q_issued = 0;
   bool abort = false;
-  auto issue = [&](int64_t q) {
-    int64_t blk, j;
-    step_tile(q, blk, j);
-    const int st = (int)(q % kStages);
+  auto issue = [&](const Cursor& c) {
+    const int st = c.st;
     uint8_t* base = smem + st * K::STAGE;
-    const int b = (int)(blk / ncblk);
-    const int x0 = (int)(blk % ncblk) * DC;
-    const int y0 = (int)(j * kTile);
+    const int b = c.b;
+    const int x0 = c.x0;
+    const int y0 = (int)(c.j * kTile);
     if constexpr (TMA) {
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -262,37 +294,31 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   // the warp, so the ring slot being refilled is no longer read
   auto issue_upto = [&](int64_t qmax) {
     const int64_t lim = min(qmax, nsteps);
-    while (q_issued < lim) {
-      issue(q_issued);
-      q_issued++;
+    while (ci.q < lim) {
+      issue(ci);
+      advance(ci);
     }
   };
   // wait for step q's tile; returns the fp32 B|C rows of the tile
-  auto acquire = [&](int64_t q) -> const float* {
-    const int st = (int)(q % kStages);
-    if (!abort && !mbar_wait(&full[st], (uint32_t)((q / kStages) & 1))) {
+  auto acquire = [&](const Cursor& c) -> const float* {
+    const int st = c.st;
+    if (!abort && !mbar_wait(&full[st], c.ph)) {
       abort = true;
       atomicOr(p.fault, kFaultTileWait);
     }
     __syncwarp();
     const uint8_t* base = smem + st * K::STAGE;
     if constexpr (K::BF) {
-      // lane r widens row r of B and of C
-      const uint4* rb = reinterpret_cast<const uint4*>(base + K::OFF_B) + lane * 2;
-      const uint4* rc = reinterpret_cast<const uint4*>(base + K::OFF_C) + lane * 2;
-      float4* fb = reinterpret_cast<float4*>(smem + K::OFF_BCF) + lane * 4;
-      float4* fc = reinterpret_cast<float4*>(smem + K::OFF_BCF + kTile * kDState * 4) + lane * 4;
+      // B then C (2 x kTile x 16 bf16, contiguous in the stage) widened to
+      // fp32: per pass each lane takes four consecutive values, so both the
+      // 8-byte loads and the 16-byte stores are contiguous across the warp
+      const uint2* src = reinterpret_cast<const uint2*>(base + K::OFF_B);
+      float4* dst = reinterpret_cast<float4*>(smem + K::OFF_BCF);
 #pragma unroll
-      for (int qq = 0; qq < 2; qq++) {
-        const uint4 vb4 = rb[qq], vc4 = rc[qq];
-        fb[2 * qq] = make_float4(__uint_as_float(vb4.x << 16), __uint_as_float(vb4.x & 0xffff0000u),
-                                 __uint_as_float(vb4.y << 16), __uint_as_float(vb4.y & 0xffff0000u));
-        fb[2 * qq + 1] = make_float4(__uint_as_float(vb4.z << 16), __uint_as_float(vb4.z & 0xffff0000u),
-                                     __uint_as_float(vb4.w << 16), __uint_as_float(vb4.w & 0xffff0000u));
-        fc[2 * qq] = make_float4(__uint_as_float(vc4.x << 16), __uint_as_float(vc4.x & 0xffff0000u),
-                                 __uint_as_float(vc4.y << 16), __uint_as_float(vc4.y & 0xffff0000u));
-        fc[2 * qq + 1] = make_float4(__uint_as_float(vc4.z << 16), __uint_as_float(vc4.z & 0xffff0000u),
-                                     __uint_as_float(vc4.w << 16), __uint_as_float(vc4.w & 0xffff0000u));
+      for (int i = 0; i < (2 * kTile * kDState) / (4 * 32); i++) {
+        const uint2 v = src[i * 32 + lane];
+        dst[i * 32 + lane] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                         __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
       }
       __syncwarp();
       return reinterpret_cast<const float*>(smem + K::OFF_BCF);
@@ -465,11 +491,10 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   // ---- main loop over the worker's steps
   issue_upto(kStages - 1);
   int64_t q = 0;
-  for (; q < nsteps; q++) {
+  for (; q < nsteps; q++, advance(cc)) {
     __syncwarp();
     issue_upto(q + kStages);
-    int64_t blk, j;
-    step_tile(q, blk, j);
+    const int64_t blk = cc.blk, j = cc.j;
 
     // segment start: per-channel constants and the incoming state
     if constexpr (MODE == kModeStatic) {
@@ -504,9 +529,9 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
       }
     }
 
-    const float* bcf = acquire(q);
+    const float* bcf = acquire(cc);
     const int64_t t0 = j * kTile;
-    run_tile((int)(q % kStages), bcf, t0, (int)min((int64_t)kTile, L - t0));
+    run_tile(cc.st, bcf, t0, (int)min((int64_t)kTile, L - t0));
 
     // segment end: final state or hand-over
     if constexpr (MODE == kModeStatic) {
@@ -623,9 +648,13 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   }
   // drain loads issued past the last consumed step (bounded waits)
   __syncwarp();
-  for (int64_t qq = q; qq < q_issued; qq++) {
-    const int st = (int)(qq % kStages);
-    if (!mbar_wait(&full[st], (uint32_t)((qq / kStages) & 1))) atomicOr(p.fault, kFaultTileWait);
+  if (q < nsteps) {
+    if (cc.q != q) {  // left the loop by break: cc still names step q-1
+      cc.q = q - 1;
+      advance(cc);
+    }
+    for (; cc.q < ci.q; advance(cc))
+      if (!mbar_wait(&full[cc.st], cc.ph)) atomicOr(p.fault, kFaultTileWait);
   }
 }
 
