@@ -76,11 +76,14 @@ ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype
   int sg = g_tune_sg;
   // one lane per channel costs the fewest instructions per state update; two
   // lanes per channel halve each lane's work, which pays only when there are
-  // too few channel blocks to give every other SM sub-partition a warp
-  if (sg != 1 && sg != 2) sg = batch * ((dim + 31) / 32) >= kSchedulers / 2 ? 1 : 2;
+  // too few channel blocks to give every other SM sub-partition a warp and the
+  // sequence is too short to be split into chunks
+  if (sg != 1 && sg != 2)
+    sg = (batch * ((dim + 31) / 32) >= kSchedulers / 2 || seqlen >= 2 * kMinChunk) ? 1 : 2;
   pl.sg = sg;
   pl.cblk = scan_channels_per_warp(sg);
-  const int tile = scan_tile_len();
+  const int tile = scan_tile_len(in_dtype, sg);
+  pl.tile = tile;
   const int64_t ncblk = (dim + pl.cblk - 1) / pl.cblk;
   const int64_t nblk = batch * ncblk;
   const int64_t T = seqlen > 0 ? (seqlen + tile - 1) / tile : 1;
@@ -101,7 +104,9 @@ ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype
       pl.nworkers = g;
     }
   } else if (seqlen >= 2 * kMinChunk) {
-    int64_t k = (target + nblk - 1) / nblk;
+    // as many chunks as keep every warp resident at once (a chunk waits only
+    // for earlier chunks, but a second wave would double the makespan)
+    int64_t k = std::max<int64_t>(1, target / nblk);
     k = std::min<int64_t>(k, seqlen / kMinChunk);
     pl.chunk_tiles = (T + k - 1) / k;
   }
@@ -128,7 +133,7 @@ size_t scan_bind_workspace(ScanParams& p, const ScanPlan& plan, void* workspace)
   const int64_t ncblk = (p.dim + plan.cblk - 1) / plan.cblk;
   p.ncblk = (int)ncblk;
   p.nblk = p.batch * ncblk;
-  p.tiles_per_blk = p.seqlen > 0 ? (p.seqlen + scan_tile_len() - 1) / scan_tile_len() : 1;
+  p.tiles_per_blk = p.seqlen > 0 ? (p.seqlen + plan.tile - 1) / plan.tile : 1;
   p.mode = plan.mode;
   p.nworkers = plan.nworkers;
   p.chunk_tiles = plan.chunk_tiles;

@@ -68,6 +68,7 @@ struct StepParams {
 // Launch plan for a scan problem.
 struct ScanPlan {
   int sg;               // threads per channel (1 or 2); each owns 16/sg states
+  int tile;             // timesteps per tile
   int cblk;             // channels per warp
   int mode;             // ScanMode
   int64_t nworkers;     // warps with work
@@ -89,7 +90,7 @@ cudaError_t launch_scan_fwd(const ScanParams& p, const ScanPlan& plan, ss_dtype 
 
 // Shape constants of the scan kernels.
 int scan_channels_per_warp(int sg);
-int scan_tile_len();
+int scan_tile_len(ss_dtype in_dtype, int sg);  // timesteps per tile
 int scan_warps_per_block();
 int scan_header_words();
 uint32_t scan_header_magic();

@@ -12,7 +12,11 @@ namespace ssk {
 __device__ unsigned int g_fault_word = 0;
 
 int scan_channels_per_warp(int sg) { return 32 / sg; }
-int scan_tile_len() { return scan_detail::kTile; }
+int scan_tile_len(ss_dtype in_dtype, int sg) {
+  using scan_detail::Cfg;
+  if (in_dtype == SS_BF16) return sg == 1 ? Cfg<__nv_bfloat16, 1>::TILE : Cfg<__nv_bfloat16, 2>::TILE;
+  return sg == 1 ? Cfg<float, 1>::TILE : Cfg<float, 2>::TILE;
+}
 int scan_warps_per_block() { return scan_detail::kWarps; }
 int scan_header_words() { return scan_detail::kHeaderWords; }
 uint32_t scan_header_magic() { return scan_detail::kHeaderMagic; }

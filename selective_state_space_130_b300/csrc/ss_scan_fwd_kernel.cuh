@@ -13,9 +13,9 @@
 // not HBM, bounds the exact fp32 recurrence: about 30 state updates per clock
 // per SM at best against 4 bytes of HBM traffic per 16 updates.
 //
-// Data path. Tiles of kTile timesteps stream through a kStages-deep ring in
-// the warp's shared memory: u, delta_raw, z ([kTile, DC] boxes) and the tile's
-// B and C rows ([kTile, 16]) arrive by TMA (cp.async.bulk.tensor) with
+// Data path. Tiles of TILE timesteps stream through a kStages-deep ring in
+// the warp's shared memory: u, delta_raw, z ([TILE, DC] boxes) and the tile's
+// B and C rows ([TILE, 16]) arrive by TMA (cp.async.bulk.tensor) with
 // completion counted on one mbarrier per stage, issued by the warp itself
 // kStages-1 tiles ahead. bf16 B/C rows are widened once per tile into an fp32
 // buffer read by broadcast. Only y and the final state leave the chip. A
@@ -55,7 +55,7 @@
 namespace ssk {
 namespace scan_detail {
 
-constexpr int kTile = 32;    // timesteps per pipeline stage
+constexpr int kTile = 32;    // timesteps per pipeline stage (64 for bf16 one-lane channels)
 constexpr int kStages = 3;   // TMA ring depth
 constexpr int kWarps = 4;    // warps (independent workers) per block
 constexpr int kUnroll = 8;   // tokens per step of the token loop (written out by hand below)
@@ -74,12 +74,15 @@ struct Cfg {
   static constexpr int NP = NS / 2;        // packed state pairs per lane
   static constexpr int DC = 32 / SG;       // channels per warp
   static constexpr bool BF = sizeof(TIn) == 2;
-  static constexpr int XB = kTile * DC * (int)sizeof(TIn);        // one u / delta_raw / z tile
-  static constexpr int RB = kTile * kDState * (int)sizeof(TIn);   // one raw B or C tile
+  // timesteps per tile: the bf16 one-lane-per-channel layout fits 64 in the
+  // shared memory of four warps per SM, halving the per-tile ring overhead
+  static constexpr int TILE = (BF && SG == 1) ? 2 * kTile : kTile;
+  static constexpr int XB = TILE * DC * (int)sizeof(TIn);         // one u / delta_raw / z tile
+  static constexpr int RB = TILE * kDState * (int)sizeof(TIn);    // one raw B or C tile
   static constexpr int OFF_U = 0, OFF_DR = XB, OFF_Z = 2 * XB, OFF_B = 3 * XB, OFF_C = 3 * XB + RB;
   static constexpr int STAGE = (3 * XB + 2 * RB + 127) & ~127;
   static constexpr int OFF_BCF = kStages * STAGE;                  // fp32 B|C of the current tile (bf16 only)
-  static constexpr int BCF = BF ? 2 * kTile * kDState * 4 : 0;
+  static constexpr int BCF = BF ? 2 * TILE * kDState * 4 : 0;
   static constexpr int OFF_BAR = OFF_BCF + BCF;
   static constexpr int WARP_SMEM = (OFF_BAR + kStages * 8 + 127) & ~127;
   static constexpr int SMEM = kWarps * WARP_SMEM + 128;            // + base alignment slack
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
                                                                   const __grid_constant__ CUtensorMap tm_b,
                                                                   const __grid_constant__ CUtensorMap tm_c) {
   using K = Cfg<TIn, SG>;
-  constexpr int NS = K::NS, NP = K::NP, DC = K::DC;
+  constexpr int NS = K::NS, NP = K::NP, DC = K::DC, TILE = K::TILE;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     uint8_t* base = smem + st * K::STAGE;
     const int b = c.b;
     const int x0 = c.x0;
-    const int y0 = (int)(c.j * kTile);
+    const int y0 = (int)(c.j * TILE);
     if constexpr (TMA) {
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
       TIn* su = reinterpret_cast<TIn*>(base + K::OFF_U);
       TIn* sdr = reinterpret_cast<TIn*>(base + K::OFF_DR);
       TIn* sz = reinterpret_cast<TIn*>(base + K::OFF_Z);
-      for (int i = lane; i < kTile * DC; i += 32) {
+      for (int i = lane; i < TILE * DC; i += 32) {
         const int tt = i / DC, cc = i % DC;
         const int64_t t = (int64_t)y0 + tt, dd = (int64_t)x0 + cc;
         TIn vu = from_f32<TIn>(0.f), vr = vu, vz = vu;
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
       const TIn* gC = static_cast<const TIn*>(p.C);
       TIn* sB = reinterpret_cast<TIn*>(base + K::OFF_B);
       TIn* sC = reinterpret_cast<TIn*>(base + K::OFF_C);
-      for (int i = lane; i < kTile * kDState; i += 32) {
+      for (int i = lane; i < TILE * kDState; i += 32) {
         const int64_t t = (int64_t)y0 + i / kDState;
         const bool ok = t < L;
         const int64_t gi = ((int64_t)b * L + (ok ? t : 0)) * kDState + i % kDState;
@@ -302,20 +305,20 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   // wait for step q's tile; returns the fp32 B|C rows of the tile
   auto acquire = [&](const Cursor& c) -> const float* {
     const int st = c.st;
-    if (!abort && !mbar_wait(&full[st], c.ph)) {
+    const bool timed_out = !abort && !mbar_wait(&full[st], c.ph);
+    if (__any_sync(FULL, timed_out)) {  // keep `abort` warp-uniform
       abort = true;
-      atomicOr(p.fault, kFaultTileWait);
+      if (lane == 0) atomicOr(p.fault, kFaultTileWait);
     }
-    __syncwarp();
     const uint8_t* base = smem + st * K::STAGE;
     if constexpr (K::BF) {
-      // B then C (2 x kTile x 16 bf16, contiguous in the stage) widened to
+      // B then C (2 x TILE x 16 bf16, contiguous in the stage) widened to
       // fp32: per pass each lane takes four consecutive values, so both the
       // 8-byte loads and the 16-byte stores are contiguous across the warp
       const uint2* src = reinterpret_cast<const uint2*>(base + K::OFF_B);
       float4* dst = reinterpret_cast<float4*>(smem + K::OFF_BCF);
 #pragma unroll
-      for (int i = 0; i < (2 * kTile * kDState) / (4 * 32); i++) {
+      for (int i = 0; i < (2 * TILE * kDState) / (4 * 32); i++) {
         const uint2 v = src[i * 32 + lane];
         dst[i * 32 + lane] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
                                          __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
@@ -395,7 +398,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     const TIn* sdr = reinterpret_cast<const TIn*>(base + K::OFF_DR) + cw;
     const TIn* sz = reinterpret_cast<const TIn*>(base + K::OFF_Z) + cw;
     const float* brow = bcf + n0;
-    const float* crow = bcf + kTile * kDState + n0;
+    const float* crow = bcf + TILE * kDState + n0;
     if constexpr (SG == 1) {
       TOut* yp = ycol + t0 * Dm;
       auto token = [&](int tt) {
@@ -406,11 +409,11 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
         st_out(yp + tt * Dm, fmaf(D_d, xu, yv) * g, dvalid);
         if constexpr (MODE == kModeChunked) ssum += dl;
       };
-      if (tlen == kTile) {
+      if (tlen == TILE) {
         // eight tokens of straight-line code per iteration: the scheduler
         // overlaps one token's scalar chain with its neighbours' state updates
 #pragma unroll 1
-        for (int tt = 0; tt < kTile; tt += kUnroll) {
+        for (int tt = 0; tt < TILE; tt += kUnroll) {
           token(tt);
           token(tt + 1);
           token(tt + 2);
@@ -443,9 +446,9 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
         st_out(yp + tt * Dm, fmaf(D_d, xu, yv) * g, dvalid && (two || s == 0));
         if constexpr (MODE == kModeChunked) ssum += (s ? dlo : dl) + (two ? (s ? dl : dlo) : 0.f);
       };
-      if (tlen == kTile) {
+      if (tlen == TILE) {
 #pragma unroll 1
-        for (int tt = 0; tt < kTile; tt += kUnroll) {
+        for (int tt = 0; tt < TILE; tt += kUnroll) {
           pair(tt, true);
           pair(tt + 2, true);
           pair(tt + 4, true);
@@ -479,9 +482,15 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
         }
       }
     }
+    // lane 0's observation decides for the whole warp (the flag may move on
+    // from aggregate to inclusive meanwhile: a per-lane value could split the
+    // warp); each lane's own acquire load only orders its later reads of the
+    // published record, which any value at or above lane 0's covers
     v = __shfl_sync(FULL, v, 0);
     abort = __shfl_sync(FULL, abort ? 1 : 0, 0) != 0;
-    if (v != 0) v = ld_acquire_gpu(f);
+    if (v != 0)
+      for (int i = 0; i < (1 << 20) && ld_acquire_gpu(f) < v; i++) {
+      }
     return v == 0 ? kFlagInclusive : v;
   };
 
@@ -530,8 +539,8 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     }
 
     const float* bcf = acquire(cc);
-    const int64_t t0 = j * kTile;
-    run_tile(cc.st, bcf, t0, (int)min((int64_t)kTile, L - t0));
+    const int64_t t0 = j * TILE;
+    run_tile(cc.st, bcf, t0, (int)min((int64_t)TILE, L - t0));
 
     // segment end: final state or hand-over
     if constexpr (MODE == kModeStatic) {
@@ -677,14 +686,14 @@ inline EncodeFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a [batch, L, inner] row-major tensor with a [1, kTile, box_inner] box.
+// 3-D map over a [batch, L, inner] row-major tensor with a [1, box_t, box_inner] box.
 inline bool make_map(CUtensorMap* m, const void* ptr, size_t es, int64_t batch, int64_t L, int64_t inner,
-                     int box_inner) {
+                     int box_inner, int box_t) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)L, (cuuint64_t)batch};
   cuuint64_t strides[2] = {(cuuint64_t)inner * es, (cuuint64_t)L * inner * es};
-  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)kTile, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_t, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -701,11 +710,11 @@ cudaError_t launch_t(const ScanParams& p, cudaStream_t stream) {
   CUtensorMap mu{}, mdr{}, mz{}, mb{}, mc{};
   if (TMA) {
     const size_t es = sizeof(TIn);
-    if (!make_map(&mu, p.u, es, p.batch, p.seqlen, p.dim, K::DC) ||
-        !make_map(&mdr, p.delta_raw, es, p.batch, p.seqlen, p.dim, K::DC) ||
-        (HAS_Z && !make_map(&mz, p.z, es, p.batch, p.seqlen, p.dim, K::DC)) ||
-        !make_map(&mb, p.B, es, p.batch, p.seqlen, kDState, kDState) ||
-        !make_map(&mc, p.C, es, p.batch, p.seqlen, kDState, kDState))
+    if (!make_map(&mu, p.u, es, p.batch, p.seqlen, p.dim, K::DC, K::TILE) ||
+        !make_map(&mdr, p.delta_raw, es, p.batch, p.seqlen, p.dim, K::DC, K::TILE) ||
+        (HAS_Z && !make_map(&mz, p.z, es, p.batch, p.seqlen, p.dim, K::DC, K::TILE)) ||
+        !make_map(&mb, p.B, es, p.batch, p.seqlen, kDState, kDState, K::TILE) ||
+        !make_map(&mc, p.C, es, p.batch, p.seqlen, kDState, kDState, K::TILE))
       return cudaErrorInvalidValue;
   }
   // the split modes place kWarps workers per block, one per SM sub-partition;

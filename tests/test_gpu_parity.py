@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import selective_state_space_130_b300 as ss
-from parity import assert_close, run_scan, to_dev
+from parity import assert_close, run_scan, run_scan_dev, to_dev
 from workloads import configs, gen
 
 pytestmark = pytest.mark.gpu
@@ -125,6 +125,27 @@ def test_streamk_matches_static():
     y1, h1 = run_scan(x, F32, sg=1, chunk=1 << 30)  # one chunk: one warp per block, whole sequence
     y2, h2 = run_scan(x, F32, sg=1, wps=2)
     assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
+
+
+@pytest.mark.parametrize("sg", [1, 2])
+def test_chunked_many_chunks_long_sequence(sg):
+    # eight chunks per channel block: look-back walks over predecessors whose
+    # flags move from aggregate to inclusive while they are read (the whole
+    # warp must take one decision per flag); sampled channels against the oracle
+    L, Dm = 1 << 16, 1024
+    x = gen.random_scan_inputs(1, L, Dm, 16, in_dtype="bf16", seed=21, dt_min=1e-3, dt_max=0.1)
+    ss.ss_scan_set_tuning(sg, 0, 0)
+    try:
+        assert ss.ss_scan_fwd_workspace_size(1, L, Dm) > 0
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+    y, h = run_scan_dev(x, F32, sg=sg)
+    ch = np.array([[0, c] for c in (0, 1, 31, 32, 500, 511, 512, 1000, 1023)])
+    yr, hr = oracle.scan(x, channels=ch)
+    yg = y[0, :, ch[:, 1]].T.double().cpu().numpy()
+    hg = h[0, ch[:, 1]].double().cpu().numpy()
+    assert_close(yg, yr, BF16, what="many-chunk y")
+    assert_close(hg, hr, BF16, what="many-chunk h_last")
 
 
 def test_chunked_matches_unchunked():
