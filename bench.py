@@ -37,11 +37,11 @@ KERNEL_SOURCES = ["selective_state_space_130_b300/csrc/ss_scan_fwd_kernel.cuh",
                   "selective_state_space_130_b300/csrc/ss_device.cuh",
                   "selective_state_space_130_b300/csrc/ss_internal.h"]
 SCAN_PROFILE = "profiles/ss_scan_fwd_mamba2p8b_layer.md"
-# Issue-bound compute roof of the state update: each (t, d, n) needs at least
-# 4 fp32 pipe ops (delta*A, (delta*u)*B, the h FMA, the C.h FMA) and one MUFU
-# ex2, each one issue slot; an SM issues 4 warp-instructions (128 lane-ops)
-# per clock, so at most 128 / 5 = 25.6 state updates per clock per SM.
-STATE_UPDATES_PER_CLK_SM = 128.0 / 5.0
+# Compute roof of the state update: each (t, d, n) needs at least 4 fp32 pipe
+# operations (delta*A, (delta*u)*B, the h FMA, the C.h FMA) and one MUFU ex2.
+# A B300 SM has 128 fp32 lanes and retires 32 ex2 per clock, so at most 32 state
+# updates per clock per SM (both pipes saturated, no other work).
+STATE_UPDATES_PER_CLK_SM = 32.0
 SMS = 148
 
 
@@ -211,8 +211,9 @@ def bench_scan(ss, w, x, steps, warmup, out_dtype, dev, nsets=None):
     ss.ss_scan_status(ws)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one scan kernel per step (the workspace clear before it is a memset)
     return dict(sets=sets, ys=ys, hs=hs, ws=ws, ev=ev, t0=t0, t1=t1, nsets=nsets, stream=stream,
-                launches_per_step=(2 if ws_bytes else 1))
+                launches_per_step=1)
 
 
 def run_timed(ss, st, steps):
@@ -282,6 +283,7 @@ def bench_decode(ss, w, dev, timed_steps=64, warmup=8):
     h = 0.1 * torch.randn((S, Dm, 16), generator=g, device=dev, dtype=torch.float32)
     y = torch.empty((S, Dm), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, read after the fill
 
     def step(k):
         ss.ss_state_update(h, su["u"][k], su["delta_raw"][k], A, su["B"][k], su["C"][k], Dk, su["z"][k], bias, y=y)
@@ -291,7 +293,11 @@ def bench_decode(ss, w, dev, timed_steps=64, warmup=8):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(timed_steps)]
     for i in range(timed_steps):
+        # evict the state from L2: write a buffer larger than L2, then read
+        # another one, so the step does not also pay for writing back the
+        # flush's dirty lines
         flush.fill_(i & 0xFF)
+        flush_rd.sum()
         ev[i][0].record()
         step(i % nin)
         ev[i][1].record()
@@ -309,7 +315,7 @@ def bench_decode(ss, w, dev, timed_steps=64, warmup=8):
     bytes_step = w.algorithmic_bytes_per_step("bf16")
     return {"workload": f"{w.name}: {S} streams x d_inner {Dm} x d_state 16, bf16 inputs/y, fp32 state",
             "steps_per_s": 1e3 / cold_ms, "ms_per_step": cold_ms, "hbm_gbs": bytes_step / (cold_ms * 1e-3) / 1e9,
-            "tokens_per_s": S * 1e3 / cold_ms, "l2": "flushed before every timed step",
+            "tokens_per_s": S * 1e3 / cold_ms, "l2": "flushed before every timed step (256 MB write, 256 MB read)",
             "warm_steps_per_s": 1e3 / warm_ms, "warm_note": "1000 back-to-back steps, state may stay in L2"}
 
 
@@ -389,8 +395,9 @@ def run_ours(args, world, rank, local):
                      "per_launch_ms": round(per_launch_ms, 5), "algorithmic_bytes_per_launch": bytes_step},
         "compute_roofline": {"bound": "alu", "unit": "state updates/s", "achieved": alu_achieved,
                              "peak": alu_peak, "frac": round(alu_achieved / alu_peak, 4),
-                             "basis": "issue-bound: 5 issue slots per (t,d,n) (4 fp32 + 1 MUFU ex2), "
-                                      "25.6 per clk per SM x 148 SMs x median SM clock under load"},
+                             "basis": "4 fp32 lane-ops + 1 MUFU ex2 per (t,d,n): 128 fp32 lanes and 32 ex2 "
+                                      "per clk per SM give 32 updates per clk per SM x 148 SMs x median SM "
+                                      "clock under load"},
         "gpu_launches": args.steps * st["launches_per_step"],
         "clocks": clk,
     }
