@@ -108,6 +108,35 @@ __device__ __forceinline__ float softplus_fast(float x) {
   return x > 20.f ? x : r;
 }
 
+// softplus_fast for two values at once: the polynomial, the scaling and the
+// additions run as packed f32x2 operations; the exponentials, logarithms and
+// selections stay per value. Same formula and constants as softplus_fast.
+__device__ __forceinline__ f2 softplus_fast2(f2 x) {
+  const f2 xl = mul2(x, pk(kLog2e, kLog2e));
+  const f2 w = pk(ex2(f2lo(xl)), ex2(f2hi(xl)));
+  f2 p = fma2(w, pk(-1.f / 6.f, -1.f / 6.f), pk(0.2f, 0.2f));
+  p = fma2(w, p, pk(-0.25f, -0.25f));
+  p = fma2(w, p, pk(1.f / 3.f, 1.f / 3.f));
+  p = fma2(w, p, pk(-0.5f, -0.5f));
+  p = fma2(w, p, pk(1.f, 1.f));
+  const f2 series = mul2(w, p);
+  const f2 w1 = add2(w, pk(1.f, 1.f));
+  float l0, l1;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l0) : "f"(f2lo(w1)));
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l1) : "f"(f2hi(w1)));
+  const f2 lg = mul2(pk(l0, l1), pk(kLn2, kLn2));
+  const float r0 = f2lo(w) < 0.0625f ? f2lo(series) : f2lo(lg);
+  const float r1 = f2hi(w) < 0.0625f ? f2hi(series) : f2hi(lg);
+  return pk(f2lo(x) > 20.f ? f2lo(x) : r0, f2hi(x) > 20.f ? f2hi(x) : r1);
+}
+
+// silu for two values: z / (1 + e^-z), the scalings and additions packed
+__device__ __forceinline__ f2 silu2(f2 z) {
+  const f2 e = mul2(z, pk(-kLog2e, -kLog2e));
+  const f2 d = add2(pk(ex2(f2lo(e)), ex2(f2hi(e))), pk(1.f, 1.f));
+  return mul2(z, pk(rcp(f2lo(d)), rcp(f2hi(d))));
+}
+
 template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, int MODE>
 __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_constant__ ScanParams p,
                                                                   const __grid_constant__ CUtensorMap tm_u,
@@ -409,19 +438,30 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
         st_out(yp + tt * Dm, fmaf(D_d, xu, yv) * g, dvalid);
         if constexpr (MODE == kModeChunked) ssum += dl;
       };
+      // two tokens whose per-token scalars are computed as packed pairs
+      const f2 bias2 = pk(bias_d, bias_d), D2 = pk(D_d, D_d);
+      auto token_pair = [&](int tt) {
+        const f2 xu = pk(to_f32(su[tt * DC]), to_f32(su[(tt + 1) * DC]));
+        const f2 dl = softplus_fast2(add2(pk(to_f32(sdr[tt * DC]), to_f32(sdr[(tt + 1) * DC])), bias2));
+        const f2 du = mul2(dl, xu);
+        const f2 post = mul2(D2, xu);
+        const f2 g = HAS_Z ? silu2(pk(to_f32(sz[tt * DC]), to_f32(sz[(tt + 1) * DC]))) : pk(1.f, 1.f);
+        const float y0 = update(f2lo(dl), f2lo(du), brow + tt * kDState, crow + tt * kDState);
+        const float y1 = update(f2hi(dl), f2hi(du), brow + (tt + 1) * kDState, crow + (tt + 1) * kDState);
+        const f2 yv = mul2(add2(pk(y0, y1), post), g);
+        st_out(yp + tt * Dm, f2lo(yv), dvalid);
+        st_out(yp + (tt + 1) * Dm, f2hi(yv), dvalid);
+        if constexpr (MODE == kModeChunked) ssum += f2lo(dl) + f2hi(dl);
+      };
       if (tlen == TILE) {
         // eight tokens of straight-line code per iteration: the scheduler
         // overlaps one token's scalar chain with its neighbours' state updates
 #pragma unroll 1
         for (int tt = 0; tt < TILE; tt += kUnroll) {
-          token(tt);
-          token(tt + 1);
-          token(tt + 2);
-          token(tt + 3);
-          token(tt + 4);
-          token(tt + 5);
-          token(tt + 6);
-          token(tt + 7);
+          token_pair(tt);
+          token_pair(tt + 2);
+          token_pair(tt + 4);
+          token_pair(tt + 6);
         }
       } else {
 #pragma unroll 1
