@@ -440,28 +440,46 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
       };
       // two tokens whose per-token scalars are computed as packed pairs
       const f2 bias2 = pk(bias_d, bias_d), D2 = pk(D_d, D_d);
-      auto token_pair = [&](int tt) {
+      struct PairScalars {
+        f2 dl, du, post, g;
+      };
+      auto scalars_pair = [&](int tt) -> PairScalars {
+        PairScalars r;
         const f2 xu = pk(to_f32(su[tt * DC]), to_f32(su[(tt + 1) * DC]));
-        const f2 dl = softplus_fast2(add2(pk(to_f32(sdr[tt * DC]), to_f32(sdr[(tt + 1) * DC])), bias2));
-        const f2 du = mul2(dl, xu);
-        const f2 post = mul2(D2, xu);
-        const f2 g = HAS_Z ? silu2(pk(to_f32(sz[tt * DC]), to_f32(sz[(tt + 1) * DC]))) : pk(1.f, 1.f);
-        const float y0 = update(f2lo(dl), f2lo(du), brow + tt * kDState, crow + tt * kDState);
-        const float y1 = update(f2hi(dl), f2hi(du), brow + (tt + 1) * kDState, crow + (tt + 1) * kDState);
-        const f2 yv = mul2(add2(pk(y0, y1), post), g);
+        r.dl = softplus_fast2(add2(pk(to_f32(sdr[tt * DC]), to_f32(sdr[(tt + 1) * DC])), bias2));
+        r.du = mul2(r.dl, xu);
+        r.post = mul2(D2, xu);
+        r.g = HAS_Z ? silu2(pk(to_f32(sz[tt * DC]), to_f32(sz[(tt + 1) * DC]))) : pk(1.f, 1.f);
+        return r;
+      };
+      auto update_pair = [&](int tt, const PairScalars& r) {
+        const float y0 = update(f2lo(r.dl), f2lo(r.du), brow + tt * kDState, crow + tt * kDState);
+        const float y1 = update(f2hi(r.dl), f2hi(r.du), brow + (tt + 1) * kDState, crow + (tt + 1) * kDState);
+        const f2 yv = mul2(add2(pk(y0, y1), r.post), r.g);
         st_out(yp + tt * Dm, f2lo(yv), dvalid);
         st_out(yp + (tt + 1) * Dm, f2hi(yv), dvalid);
-        if constexpr (MODE == kModeChunked) ssum += f2lo(dl) + f2hi(dl);
+        if constexpr (MODE == kModeChunked) ssum += f2lo(r.dl) + f2hi(r.dl);
       };
       if (tlen == TILE) {
-        // eight tokens of straight-line code per iteration: the scheduler
-        // overlaps one token's scalar chain with its neighbours' state updates
+        // software-pipelined groups of eight tokens: the loop body computes
+        // the next group's scalars (a long softplus -> ex2 chain) next to the
+        // current group's state updates, so the two overlap in one basic
+        // block; the last group recomputes its own scalars instead of reading
+        // past the tile
+        PairScalars cur0 = scalars_pair(0), cur1 = scalars_pair(2), cur2 = scalars_pair(4), cur3 = scalars_pair(6);
 #pragma unroll 1
         for (int tt = 0; tt < TILE; tt += kUnroll) {
-          token_pair(tt);
-          token_pair(tt + 2);
-          token_pair(tt + 4);
-          token_pair(tt + 6);
+          const int tn = min(tt + kUnroll, TILE - kUnroll);
+          const PairScalars nx0 = scalars_pair(tn), nx1 = scalars_pair(tn + 2), nx2 = scalars_pair(tn + 4),
+                            nx3 = scalars_pair(tn + 6);
+          update_pair(tt, cur0);
+          update_pair(tt + 2, cur1);
+          update_pair(tt + 4, cur2);
+          update_pair(tt + 6, cur3);
+          cur0 = nx0;
+          cur1 = nx1;
+          cur2 = nx2;
+          cur3 = nx3;
         }
       } else {
 #pragma unroll 1
