@@ -392,7 +392,9 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": profiled_traffic(),
                      "peak_kind": peak_kind, "kernel": "ss_scan_fwd (scan_fwd_kernel)",
-                     "per_launch_ms": round(per_launch_ms, 5), "algorithmic_bytes_per_launch": bytes_step},
+                     "per_launch_ms": round(per_launch_ms, 5),
+                     "per_launch_ms_median": round(statistics.median(per), 5),
+                     "per_launch_ms_min": round(min(per), 5), "algorithmic_bytes_per_launch": bytes_step},
         "compute_roofline": {"bound": "alu", "unit": "state updates/s", "achieved": alu_achieved,
                              "peak": alu_peak, "frac": round(alu_achieved / alu_peak, 4),
                              "basis": "4 fp32 lane-ops + 1 MUFU ex2 per (t,d,n): 128 fp32 lanes and 32 ex2 "
@@ -450,7 +452,7 @@ def run_reference(args, world, rank):
     x = gen.make_scan_inputs(w)
     nthreads = oracle.default_threads()
     rng = np.random.default_rng(1)
-    n = max(64, min(w.batch * w.dim, 32 * nthreads))
+    n = max(64, min(w.batch * w.dim, 256 * nthreads))
     per_ch_bytes = w.algorithmic_bytes("bf16") / (w.batch * w.dim)
     ch = np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.dim, n)], axis=1)
     for _ in range(args.warmup):
