@@ -13,7 +13,8 @@ Every function here is pinned by the `-m "not gpu"` tests in
 tests/test_oracle_pins.py (brute-force unrolled sum, LTI convolution checked
 directly and by FFT, delta->0, large delta, chunk associativity, geometric
 closed form, hand-computed L=1, zero/linearity/independence properties,
-decode-equals-scan).
+decode-equals-scan; for the convolution front-end: numpy's convolution,
+impulse responses, chunk continuity through the state, decode-equals-forward).
 """
 
 import ctypes
@@ -44,6 +45,12 @@ def load(path: str = None) -> ctypes.CDLL:
         lib.ss_oracle_state_update.argtypes = [_I64, _I64, _I64, ctypes.c_int, _P,
                                                _P, _P, _P, _P, _P, _P, _P, _P,
                                                _P, _I64, _P]
+        lib.ss_oracle_conv1d.restype = ctypes.c_int
+        lib.ss_oracle_conv1d.argtypes = [_I64, _I64, _I64, _I64, ctypes.c_int, _P, _P, _P, _P,
+                                         ctypes.c_int, _P, _P]
+        lib.ss_oracle_conv1d_update.restype = ctypes.c_int
+        lib.ss_oracle_conv1d_update.argtypes = [_I64, _I64, _I64, ctypes.c_int, _P, _P, _P, _P,
+                                                ctypes.c_int, _P]
         _LIBS[path] = lib
     return _LIBS[path]
 
@@ -147,3 +154,43 @@ def state_update(h: np.ndarray, x: dict, channels=None, lib_path: str = None):
     if rc != 0:
         raise ValueError("oracle state_update rejected its arguments")
     return y.reshape(S, Dm) if full else y
+
+
+def conv1d(x: dict, silu: bool = True, lib_path: str = None):
+    """Causal depthwise convolution front-end in float64 on the host.
+
+    x: dict of CPU tensors x [Bt, L, D] (float32 or bfloat16), weight [D, K] and
+    bias [D] or None (float32), state [Bt, D, K-1] or None (same dtype as x).
+    Returns (y [Bt, L, D], state_out [Bt, D, K-1]) as float64 numpy arrays.
+    """
+    lib = load(lib_path)
+    xx, w, bias, st = x["x"], _f32(x["weight"]), _f32(x.get("bias")), x.get("state")
+    Bt, L, Dm = xx.shape
+    K = w.shape[1]
+    code = _dtype_code(xx)
+    if st is not None and _dtype_code(st) != code:
+        raise TypeError("x and state must share one dtype")
+    y = np.zeros((Bt, L, Dm), dtype=np.float64)
+    so = np.zeros((Bt, Dm, max(K - 1, 0)), dtype=np.float64)
+    rc = lib.ss_oracle_conv1d(Bt, L, Dm, K, code, _ptr(xx), _ptr(w), _ptr(bias), _ptr(st), int(silu),
+                              y.ctypes.data, so.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle conv1d rejected its arguments")
+    return y, so
+
+
+def conv1d_update(state: np.ndarray, x, weight, bias=None, silu: bool = True, lib_path: str = None):
+    """One decode step of the convolution in float64, state [Bt, D, K-1]
+    (float64 numpy, modified in place); x [Bt, D] CPU tensor. Returns y [Bt, D]."""
+    lib = load(lib_path)
+    Bt, Dm = x.shape
+    w = _f32(weight)
+    K = w.shape[1]
+    assert state.dtype == np.float64 and state.flags.c_contiguous and state.shape == (Bt, Dm, K - 1)
+    y = np.zeros((Bt, Dm), dtype=np.float64)
+    rc = lib.ss_oracle_conv1d_update(Bt, Dm, K, _dtype_code(x), state.ctypes.data, _ptr(x.contiguous()), _ptr(w),
+                                     _ptr(_f32(bias)), int(silu), y.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle conv1d_update rejected its arguments")
+    return y
+

@@ -37,6 +37,11 @@
  *
  * Parity pins live in the tests (brute-force unrolled sum, LTI convolution,
  * delta->0, large delta, chunk associativity, closed forms).
+ *
+ * The file also holds the block's causal depthwise convolution front-end and
+ * its decode step (ss_oracle_conv1d, ss_oracle_conv1d_update, at the end),
+ * pinned against numpy's convolution, impulse responses, chunk continuity and
+ * decode-equals-forward.
  */
 #include <math.h>
 #include <pthread.h>
@@ -183,6 +188,81 @@ int ss_oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, int in_dt
     acc += (Dskip ? (double)Dskip[d] : 0.0) * x;
     if (z) acc *= silu(widen(z, in_dtype, i));
     y[c] = acc;
+  }
+  return 0;
+}
+
+/*
+ * Causal depthwise 1-D convolution of the Mamba block's front-end, with SiLU.
+ *
+ * The block feeds the expanded input through a short causal convolution along
+ * the sequence and a SiLU before the selective SSM ("Mamba: Linear-Time
+ * Sequence Modeling with Selective State Spaces" review page, method step 3;
+ * mlqm.cn tutorial section 7.1, the block diagram). Decoding keeps, per
+ * request, the few past inputs that convolution needs ("AI 推理系列（十四）：
+ * Mamba 的 Selective State Space", the decode-state table and the sections on
+ * the request state). The pages give no kernel width, tap order or bias; the
+ * reading taken here, for each batch b and channel d, with width K:
+ *   e[p] = x[b,p,d] for p >= 0, state_in[b,d,p+K-1] for -(K-1) <= p < 0
+ *          (0 when state_in is NULL)
+ *   pre  = bias[d] + sum_{k<K} w[d,k] * e[t-(K-1)+k]
+ *   y[b,t,d] = silu(pre) when silu_on, else pre
+ *   state_out[b,d,k] = e[L-(K-1)+k] for k < K-1   (the last K-1 inputs)
+ * x, state_in: in_dtype; w: [dim][K]; bias: [dim] or NULL.
+ * y: [batch][seqlen][dim] float64; state_out: [batch][dim][K-1] float64 or NULL.
+ */
+int ss_oracle_conv1d(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int in_dtype,
+                     const void *x, const float *w, const float *bias, const void *state_in,
+                     int silu_on, double *y, double *state_out) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || width < 1) return -1;
+  if (in_dtype != ORC_F32 && in_dtype != ORC_BF16) return -1;
+  if (!x || !w || !y) return -1;
+  const int64_t H = width - 1;
+  double *e = (double *)malloc(sizeof(double) * (size_t)(seqlen + H + 1));
+  if (!e) return -1;
+  for (int64_t b = 0; b < batch; b++) {
+    for (int64_t d = 0; d < dim; d++) {
+      /* e[q] holds position p = q - H */
+      for (int64_t q = 0; q < H; q++)
+        e[q] = state_in ? widen(state_in, in_dtype, (b * dim + d) * H + q) : 0.0;
+      for (int64_t t = 0; t < seqlen; t++) e[H + t] = widen(x, in_dtype, (b * seqlen + t) * dim + d);
+      for (int64_t t = 0; t < seqlen; t++) {
+        double pre = bias ? (double)bias[d] : 0.0;
+        for (int64_t k = 0; k < width; k++) pre += (double)w[d * width + k] * e[t + k];
+        y[(b * seqlen + t) * dim + d] = silu_on ? silu(pre) : pre;
+      }
+      if (state_out)
+        for (int64_t k = 0; k < H; k++) state_out[(b * dim + d) * H + k] = e[seqlen + k];
+    }
+  }
+  free(e);
+  return 0;
+}
+
+/*
+ * One decode step of the convolution, state carried in place: state
+ * [batch][dim][K-1] float64 holds the last K-1 inputs, oldest first; x
+ * [batch][dim] in in_dtype is the new input. y = silu(bias + sum_{k<K-1}
+ * w[d,k] state[k] + w[d,K-1] x), then the state drops its oldest entry and
+ * appends x.
+ */
+int ss_oracle_conv1d_update(int64_t batch, int64_t dim, int64_t width, int in_dtype, double *state,
+                            const void *x, const float *w, const float *bias, int silu_on, double *y) {
+  if (batch < 0 || dim < 0 || width < 1) return -1;
+  if (in_dtype != ORC_F32 && in_dtype != ORC_BF16) return -1;
+  if (!x || !w || !y || (width > 1 && !state)) return -1;
+  const int64_t H = width - 1;
+  for (int64_t b = 0; b < batch; b++) {
+    for (int64_t d = 0; d < dim; d++) {
+      double *s = state ? state + (b * dim + d) * H : NULL;
+      const double xv = widen(x, in_dtype, b * dim + d);
+      double pre = bias ? (double)bias[d] : 0.0;
+      for (int64_t k = 0; k < H; k++) pre += (double)w[d * width + k] * s[k];
+      pre += (double)w[d * width + H] * xv;
+      y[b * dim + d] = silu_on ? silu(pre) : pre;
+      for (int64_t k = 0; k + 1 < H; k++) s[k] = s[k + 1];
+      if (H > 0) s[H - 1] = xv;
+    }
   }
   return 0;
 }

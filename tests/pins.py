@@ -335,7 +335,91 @@ def pin_stability_bound(lib=None):
     assert np.all(np.abs(h) <= bound * (1 + 1e-12)), "stability bound violated"
 
 
-ALL_PINS = [pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_large_delta_overwrites,
+# ----------------------------------------------------------------- convolution front-end
+# The block's causal depthwise convolution with SiLU (review page, method step
+# 3; mlqm.cn tutorial section 7.1) and its decode state (the inference page's
+# decode-state table): pinned against numpy's convolution, impulse responses,
+# chunk continuity through the carried state, and decode-equals-forward.
+
+def _conv_ref(x):
+    """Per channel: numpy.convolve of (state, x) with the reversed taps ('valid'),
+    plus bias, then SiLU by scipy's logistic function."""
+    xx = x["x"].double().numpy()
+    w = x["weight"].double().numpy()
+    b = x["bias"].double().numpy() if x.get("bias") is not None else np.zeros(w.shape[0])
+    Bt, L, Dm = xx.shape
+    K = w.shape[1]
+    st = x["state"].double().numpy() if x.get("state") is not None else np.zeros((Bt, Dm, K - 1))
+    pre = np.zeros((Bt, L, Dm))
+    for bb in range(Bt):
+        for d in range(Dm):
+            e = np.concatenate([st[bb, d], xx[bb, :, d]])
+            pre[bb, :, d] = np.convolve(e, w[d][::-1], mode="valid") + b[d]
+    tail = np.concatenate([st, xx.transpose(0, 2, 1)], axis=2)[:, :, -(K - 1):] if K > 1 else np.zeros((Bt, Dm, 0))
+    return pre, tail
+
+
+def pin_conv_numpy(lib=None):
+    from workloads.gen import random_conv_inputs
+    path = lib
+    for (Bt, L, Dm, K, dt, st) in [(2, 17, 5, 4, "f32", True), (1, 9, 3, 2, "bf16", False), (2, 2, 4, 4, "f32", True),
+                                   (1, 12, 2, 3, "bf16", True)]:
+        x = random_conv_inputs(Bt, L, Dm, K, dt, seed=Bt * 100 + L + K, with_state=st)
+        pre, tail = _conv_ref(x)
+        y, so = oracle.conv1d(x, silu=False, lib_path=path)
+        np.testing.assert_allclose(y, pre, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(so, tail, rtol=0, atol=0)
+        ys, _ = oracle.conv1d(x, silu=True, lib_path=path)
+        np.testing.assert_allclose(ys, pre * expit(pre), rtol=1e-12, atol=1e-13)
+
+
+def pin_conv_impulse(lib=None):
+    # a unit impulse at t0 (no state) gives bias + w[d, K-1-j] at t0 + j, bias elsewhere
+    path = lib
+    Dm, K, L, t0 = 3, 4, 12, 5
+    w = torch.tensor([[1.0, 2.0, 3.0, 4.0], [0.5, -1.0, 0.25, 2.0], [-3.0, 0.0, 1.5, 1.0]])
+    bias = torch.tensor([0.1, -0.2, 0.0])
+    xx = torch.zeros(1, L, Dm)
+    xx[0, t0, :] = 1.0
+    y, so = oracle.conv1d({"x": xx, "weight": w, "bias": bias, "state": None}, silu=False, lib_path=path)
+    for d in range(Dm):
+        expect = np.full(L, float(bias[d]))
+        for j in range(K):
+            expect[t0 + j] += float(w[d, K - 1 - j])
+        np.testing.assert_allclose(y[0, :, d], expect, rtol=0, atol=1e-15)
+    assert np.all(so == 0.0)
+
+
+def pin_conv_chunk_continuity(lib=None):
+    # running two halves, the second from the first's final state, equals one pass
+    from workloads.gen import random_conv_inputs
+    path = lib
+    for K in (2, 3, 4):
+        x = random_conv_inputs(2, 23, 6, K, "f32", seed=K, with_state=True)
+        y, so = oracle.conv1d(x, lib_path=path)
+        for m in (1, 2, 10):
+            a = dict(x, x=x["x"][:, :m].contiguous())
+            ya, sa = oracle.conv1d(a, lib_path=path)
+            bpart = dict(x, x=x["x"][:, m:].contiguous(), state=torch.tensor(sa, dtype=torch.float32))
+            yb, sb = oracle.conv1d(bpart, lib_path=path)
+            np.testing.assert_allclose(np.concatenate([ya, yb], axis=1), y, rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(sb, so, rtol=0, atol=0)
+
+
+def pin_conv_decode_equals_forward(lib=None):
+    from workloads.gen import random_conv_inputs
+    path = lib
+    x = random_conv_inputs(3, 11, 7, 4, "bf16", seed=5, with_state=True)
+    y, so = oracle.conv1d(x, lib_path=path)
+    st = x["state"].double().numpy().copy()
+    for t in range(11):
+        yt = oracle.conv1d_update(st, x["x"][:, t].contiguous(), x["weight"], x["bias"], lib_path=path)
+        np.testing.assert_allclose(yt, y[:, t], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(st, so, rtol=0, atol=0)
+
+
+ALL_PINS = [pin_conv_numpy, pin_conv_impulse, pin_conv_chunk_continuity, pin_conv_decode_equals_forward,
+            pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_large_delta_overwrites,
             pin_chunk_associativity, pin_geometric_series, pin_single_step_by_hand, pin_softplus_values,
             pin_zeros, pin_linearity_in_u, pin_independence, pin_decode_equals_scan,
             pin_sampled_channels, pin_bf16_widening, pin_stability_bound]

@@ -33,6 +33,18 @@ MUTANTS = {
     "batch_stride_B": ("const int64_t r = (b * L + t) * N;", "const int64_t r = (t) * N;"),
     "decode_exp_sign": ("hs[n] = exp(delta * (double)A[d * dstate + n]) * hs[n] +",
                         "hs[n] = exp(-delta * (double)A[d * dstate + n]) * hs[n] +"),
+    # convolution front-end
+    "conv_taps_reversed": ("pre += (double)w[d * width + k] * e[t + k];",
+                           "pre += (double)w[d * width + (width - 1 - k)] * e[t + k];"),
+    "conv_drop_bias": ("double pre = bias ? (double)bias[d] : 0.0;\n        for (int64_t k = 0; k < width; k++)",
+                       "double pre = 0.0;\n        for (int64_t k = 0; k < width; k++)"),
+    "conv_not_causal": ("for (int64_t k = 0; k < width; k++) pre += (double)w[d * width + k] * e[t + k];",
+                        "for (int64_t k = 0; k < width; k++) pre += (double)w[d * width + k] * e[t + k + (t + k + 1 < seqlen + H ? 1 : 0)];"),
+    "conv_state_ignored": ("e[q] = state_in ? widen(state_in, in_dtype, (b * dim + d) * H + q) : 0.0;", "e[q] = 0.0;"),
+    "conv_state_out_shift": ("state_out[(b * dim + d) * H + k] = e[seqlen + k];",
+                             "state_out[(b * dim + d) * H + k] = e[seqlen + k - (seqlen + k > 0 ? 1 : 0)];"),
+    "conv_decode_no_shift": ("for (int64_t k = 0; k + 1 < H; k++) s[k] = s[k + 1];", ""),
+    "conv_decode_x_tap": ("pre += (double)w[d * width + H] * xv;", "pre += (double)w[d * width + 0] * xv;"),
 }
 
 

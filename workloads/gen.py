@@ -20,6 +20,7 @@ BLOCK = 1 << 22
 
 # stream ids (one per drawn tensor)
 S_DT, S_ALOG, S_U, S_DRAW, S_Z, S_B, S_C, S_SYM, S_EMB = range(9)
+S_CX, S_CW, S_CB, S_CS = range(9, 13)  # convolution front-end: input, weights, bias, state
 
 
 def _block_seed(seed: int, stream: int, block: int) -> int:
@@ -145,3 +146,21 @@ def random_scan_inputs(batch, seqlen, dim, dstate, in_dtype="f32", seed=0, delta
     else:
         x["h0"] = None
     return x
+
+
+def random_conv_inputs(batch, seqlen, dim, width, in_dtype="bf16", seed=0, with_state=False, has_bias=True):
+    """Inputs of the causal depthwise convolution front-end:
+    x [batch, seqlen, dim] ~ N(0,1) in `in_dtype`; weight [dim, width] ~
+    0.5 N(0,1) and bias [dim] ~ 0.1 N(0,1) in fp32; state [batch, dim, width-1]
+    ~ N(0,1) in `in_dtype` (the inputs before t = 0) or None."""
+    out = {
+        "x": _store(randn_blocks(batch * seqlen * dim, seed, S_CX).view(batch, seqlen, dim), in_dtype).contiguous(),
+        "weight": (0.5 * randn_blocks(dim * width, seed, S_CW)).view(dim, width).contiguous(),
+        "bias": (0.1 * randn_blocks(dim, seed, S_CB)).contiguous() if has_bias else None,
+        "state": None,
+    }
+    if with_state and width > 1:
+        out["state"] = _store(randn_blocks(batch * dim * (width - 1), seed, S_CS).view(batch, dim, width - 1),
+                              in_dtype).contiguous()
+    return out
+
