@@ -319,6 +319,64 @@ def bench_decode(ss, w, dev, timed_steps=64, warmup=8):
             "warm_steps_per_s": 1e3 / warm_ms, "warm_note": "1000 back-to-back steps, state may stay in L2"}
 
 
+def bench_conv1d(ss, dev, hbm_peak, Bt=4, L=2048, Dm=5120, K=4, reps=20):
+    """The block's causal depthwise convolution front-end (width 4, SiLU) on the
+    Mamba-2.8B layer shape, bf16 in and out: HBM-bound, 4 bytes per channel-token.
+    Two rotating input/output sets (each larger than L2). Plus the decode step
+    of its state for 256 streams x 5120 channels."""
+    sets = []
+    for i in range(2):
+        x = gen.random_conv_inputs(Bt, L, Dm, K, "bf16", seed=20 + i)
+        sets.append({k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()})
+    ys = [torch.empty((Bt, L, Dm), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    sts = [torch.empty((Bt, Dm, K - 1), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+
+    def call(i):
+        d = sets[i % 2]
+        ss.ss_conv1d_fwd(d["x"], d["weight"], d["bias"], None, y=ys[i % 2], state_out=sts[i % 2])
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record()
+        call(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = Bt * L * Dm * 4 + Bt * Dm * (K - 1) * 2
+    # decode step of the conv state: 256 streams x 5120 channels
+    S = 256
+    st = torch.randn(S, Dm, K - 1, device=dev).to(torch.bfloat16)
+    xs = torch.randn(S, Dm, device=dev).to(torch.bfloat16)
+    d = sets[0]
+    yd = torch.empty((S, Dm), dtype=torch.bfloat16, device=dev)
+    for _ in range(5):
+        ss.ss_conv1d_update(st, xs, d["weight"], d["bias"], y=yd)
+    torch.cuda.synchronize()
+    # 200 steps captured in one CUDA graph: the step is a few microseconds of
+    # GPU work, below the host cost of a Python call
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(200):
+            ss.ss_conv1d_update(st, xs, d["weight"], d["bias"], y=yd)
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    dec_ms = a.elapsed_time(b) / 200
+    return {"workload": f"causal depthwise conv1d + SiLU, width {K}, batch {Bt} x L {L} x d_inner {Dm}, bf16 in/out",
+            "ms_per_launch": round(ms, 4), "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 4), "algorithmic_bytes": nbytes,
+            "l2": "2 rotating sets of 168 MB",
+            "decode_update_us": round(dec_ms * 1e3, 2),
+            "decode_update_workload": f"{S} streams x {Dm} channels, width {K}, 200 steps in one CUDA graph"}
+
+
 def cpu_baseline_scan(w, x, target_s=12.0):
     """The float64 oracle as it stands, on the host cores, over channels of the
     same workload; scaled to algorithmic GB/s of the sample."""
@@ -434,6 +492,7 @@ def run_ours(args, world, rank, local):
                               "launches_per_step": stc["launches_per_step"], "l2": f"{stc['nsets']} rotating sets"}
             del stc, xc
             torch.cuda.empty_cache()
+        extra["conv1d_front_end"] = bench_conv1d(ss, dev, hbm_peak)
         result["per_config"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_scan(w, x)

@@ -124,6 +124,48 @@ ss_status ss_state_update(int64_t batch, int64_t dim, int64_t dstate,
                           const void *z, const float *delta_bias, void *y, void *stream);
 
 /*
+ * Causal depthwise convolution front-end of the Mamba block, with SiLU.
+ *
+ * The block passes the expanded input through a short causal convolution
+ * along the sequence and a SiLU before the selective SSM ("Mamba: Linear-Time
+ * Sequence Modeling with Selective State Spaces" review page, method step 3;
+ * mlqm.cn tutorial section 7.1, the block diagram). The pages give no width,
+ * tap order or bias; this library reads it as, for each b, d and width K:
+ *
+ *   e[p]       = x[b,p,d] for p >= 0; state_in[b,d,p+K-1] for -(K-1) <= p < 0
+ *                (0 when state_in is NULL)
+ *   pre        = bias[d] + sum_{k<K} weight[d,k] * e[t-(K-1)+k]
+ *   y[b,t,d]   = silu(pre) when silu != 0, else pre
+ *   state_out[b,d,k] = e[seqlen-(K-1)+k], k < K-1   (the last K-1 inputs)
+ *
+ *  x, y      : [batch, seqlen, dim] in_dtype / out_dtype
+ *  weight    : [dim, width] float32; bias: [dim] float32 or NULL
+ *  state_in  : [batch, dim, width-1] in_dtype or NULL; state_out: same shape,
+ *              in_dtype, or NULL; the two must be different buffers
+ *  width     : 2, 3 or 4 (SS_ERR_UNSUPPORTED otherwise)
+ * seqlen == 0 copies state_in (or zeros) to state_out and writes no y.
+ */
+ss_status ss_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width,
+                        ss_dtype in_dtype, ss_dtype out_dtype,
+                        const void *x, const float *weight, const float *bias,
+                        const void *state_in, int silu, void *y, void *state_out, void *stream);
+
+/*
+ * One decode step of the convolution: the request's conv state (the inputs
+ * the convolution still needs) is read and updated in place ("AI 推理系列（十
+ * 四）：Mamba 的 Selective State Space", the decode-state table: per-layer SSM
+ * state and conv state updated each token).
+ *  state : [batch, dim, width-1] in_dtype, oldest input first; on return it
+ *          holds the last width-1 inputs including x
+ *  x     : [batch, dim] in_dtype;  y: [batch, dim] out_dtype
+ *  y = silu(bias + sum_{k<K-1} weight[d,k] state[k] + weight[d,K-1] x)
+ */
+ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width,
+                           ss_dtype in_dtype, ss_dtype out_dtype,
+                           void *state, const void *x, const float *weight, const float *bias,
+                           int silu, void *y, void *stream);
+
+/*
  * Launch-shape controls for the calling host thread (0 = automatic, the
  * default, for each). threads_per_channel in {1, 2} sets how many threads share
  * one channel's 16 states. chunk_len > 0 forces the sequence to be split into

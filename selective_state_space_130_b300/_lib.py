@@ -32,6 +32,10 @@ SIGNATURES = {
                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ss_scan_fwd_noalloc": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ss_conv1d_fwd": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                     _P, _P, _P, _P, ctypes.c_int, _P, _P, _P]),
+    "ss_conv1d_update": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                        _P, _P, _P, _P, ctypes.c_int, _P, _P]),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
 }
@@ -183,3 +187,37 @@ def ss_scan_fwd_noalloc(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, 
                                      _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_last),
                                      _stream(stream)))
     return y, h_last
+
+
+def ss_conv1d_fwd(x, weight, bias=None, state=None, *, silu=True, out_dtype=None, y=None, state_out=None,
+                  return_state=True, stream=None):
+    """Causal depthwise convolution front-end on device tensors.
+    x: [Bt, L, D] (float32 or bfloat16); weight: [D, K] float32; bias: [D] float32;
+    state: [Bt, D, K-1] in x's dtype (the inputs before t = 0) or None.
+    Returns (y [Bt, L, D], state_out [Bt, D, K-1]); outputs are allocated with torch when not given."""
+    Bt, L, Dm = x.shape
+    K = weight.shape[1]
+    code = _dt(x)
+    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    if y is None:
+        y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=x.device)
+    if state_out is None and return_state:
+        state_out = torch.empty((Bt, Dm, K - 1), dtype=x.dtype, device=x.device)
+    _check(lib().ss_conv1d_fwd(Bt, L, Dm, K, code, out_code, _ptr(x), _ptr(weight), _ptr(bias), _ptr(state),
+                               int(bool(silu)), _ptr(y), _ptr(state_out), _stream(stream)))
+    return y, state_out
+
+
+def ss_conv1d_update(state, x, weight, bias=None, *, silu=True, out_dtype=None, y=None, stream=None):
+    """One decode step of the convolution; state [S, D, K-1] (x's dtype) is updated
+    in place with x [S, D]. Returns y [S, D]."""
+    S, Dm = x.shape
+    K = weight.shape[1]
+    code = _dt(x)
+    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    if y is None:
+        y = torch.empty((S, Dm), dtype=_tdt(out_code), device=x.device)
+    _check(lib().ss_conv1d_update(S, Dm, K, code, out_code, _ptr(state), _ptr(x), _ptr(weight), _ptr(bias),
+                                  int(bool(silu)), _ptr(y), _stream(stream)))
+    return y
+

@@ -305,6 +305,69 @@ ss_status ss_state_update(int64_t batch, int64_t dim, int64_t dstate, ss_dtype i
   return SS_OK;
 }
 
+ss_status ss_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, ss_dtype in_dtype,
+                        ss_dtype out_dtype, const void* x, const float* weight, const float* bias,
+                        const void* state_in, int silu_on, void* y, void* state_out, void* stream) {
+  g_err.clear();
+  if (width < 2 || width > 4) return fail(SS_ERR_UNSUPPORTED, "width must be 2, 3 or 4 (got %lld)", (long long)width);
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, out %d)", (int)in_dtype, (int)out_dtype);
+  if (batch < 0 || seqlen < 0 || dim < 0) return fail(SS_ERR_INVALID_ARG, "negative size");
+  if (batch > INT32_MAX || seqlen > INT32_MAX || dim > INT32_MAX)
+    return fail(SS_ERR_INVALID_ARG, "a size exceeds 2^31-1");
+  if (batch == 0 || dim == 0) return SS_OK;
+  if (!weight) return fail(SS_ERR_INVALID_ARG, "weight must not be NULL");
+  if (seqlen > 0 && (!x || !y)) return fail(SS_ERR_INVALID_ARG, "x and y must not be NULL");
+  const void* all[] = {x, weight, bias, state_in, y, state_out};
+  const char* names[] = {"x", "weight", "bias", "state_in", "y", "state_out"};
+  for (int i = 0; i < 6; i++)
+    if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  if (state_in && state_in == state_out)
+    return fail(SS_ERR_INVALID_ARG, "state_out must not be the buffer state_in (use a second buffer)");
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (seqlen == 0) {
+    if (!state_out) return SS_OK;
+    const size_t bytes = (size_t)batch * dim * (width - 1) * dsize(in_dtype);
+    cudaError_t e = state_in ? cudaMemcpyAsync(state_out, state_in, bytes, cudaMemcpyDeviceToDevice, s)
+                             : cudaMemsetAsync(state_out, 0, bytes, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
+  }
+  ssk::ConvParams p{x, weight, bias, state_in, y, state_out, batch, seqlen, dim, (int)width, silu_on ? 1 : 0};
+  const bool vec = ((size_t)dim * dsize(in_dtype)) % 16 == 0;
+  cudaError_t e = ssk::launch_conv1d_fwd(p, in_dtype, out_dtype, vec, s);
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d launch");
+  return SS_OK;
+}
+
+ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width, ss_dtype in_dtype, ss_dtype out_dtype,
+                           void* state, const void* x, const float* weight, const float* bias, int silu_on, void* y,
+                           void* stream) {
+  g_err.clear();
+  if (width < 2 || width > 4) return fail(SS_ERR_UNSUPPORTED, "width must be 2, 3 or 4 (got %lld)", (long long)width);
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, out %d)", (int)in_dtype, (int)out_dtype);
+  if (batch < 0 || dim < 0) return fail(SS_ERR_INVALID_ARG, "negative size");
+  if (batch == 0 || dim == 0) return SS_OK;
+  const void* need[] = {state, x, weight, y};
+  const char* names[] = {"state", "x", "weight", "y"};
+  for (int i = 0; i < 4; i++)
+    if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
+  const void* all[] = {state, x, weight, bias, y};
+  const char* all_names[] = {"state", "x", "weight", "bias", "y"};
+  for (int i = 0; i < 5; i++)
+    if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  ssk::ConvParams p{x, weight, bias, nullptr, y, state, batch, 1, dim, (int)width, silu_on ? 1 : 0};
+  // whole 16-byte vectors of channels per thread when a vector never straddles two batch rows
+  const bool vec = ((size_t)dim * dsize(in_dtype)) % 16 == 0;
+  cudaError_t e = ssk::launch_conv1d_update(p, in_dtype, out_dtype, vec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d update launch");
+  return SS_OK;
+}
+
 ss_status ss_scan_status(void* workspace, void* stream) {
   g_err.clear();
   cudaStream_t s = static_cast<cudaStream_t>(stream);

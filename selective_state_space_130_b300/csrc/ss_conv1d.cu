@@ -1,0 +1,406 @@
+// Causal depthwise convolution front-end of the Mamba block (width K <= 4,
+// optional SiLU) and its single-token decode step, for sm_103a.
+//
+// The block feeds the expanded input through a short causal convolution along
+// the sequence and a SiLU before the selective SSM ("Mamba: Linear-Time
+// Sequence Modeling with Selective State Spaces" review page, method step 3;
+// mlqm.cn tutorial section 7.1). Decoding keeps per request only the last K-1
+// inputs that convolution needs ("AI 推理系列（十四）：Mamba 的 Selective State
+// Space", the decode-state table and the request-state sections). Tap k
+// multiplies x[t-(K-1)+k]; the state holds the K-1 inputs before t = 0,
+// oldest first.
+//
+// Both kernels are HBM-bound streams: the forward reads x once and writes y
+// once (plus a halo of K-1 rows per 8-row chunk, served by L2). A thread owns
+// one 16-byte vector of channels (8 bf16 or 4 fp32; one channel when the row
+// is not vector-aligned) over kConvTT timesteps and issues every load of its
+// window before any arithmetic: 11 x 16 B in flight per thread, two blocks of
+// 256 threads per SM. Warps cover
+// consecutive channel vectors, so each row access is a contiguous 512 B.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ss_device.cuh"
+#include "ss_internal.h"
+
+namespace ssk {
+namespace {
+
+constexpr int kConvThreads = 256;
+constexpr int kConvTT = 8;   // timesteps per thread
+
+// V consecutive elements of a row, loaded as one vector (or one element)
+template <typename T, int V>
+struct Row {
+  static constexpr int kWords = (int)(V * sizeof(T) / 4);  // 32-bit words (0 for a lone bf16)
+  static constexpr int kN = kWords > 0 ? kWords : 1;        // storage words
+  uint32_t w[kN];
+};
+
+template <typename T, int V>
+__device__ __forceinline__ Row<T, V> load_row(const T* p) {
+  Row<T, V> r;
+  if constexpr (V * sizeof(T) == 16) {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+    r.w[2] = v.z;
+    r.w[3] = v.w;
+  } else if constexpr (sizeof(T) == 4) {
+    r.w[0] = __float_as_uint(__ldcs(reinterpret_cast<const float*>(p)));
+  } else {
+    r.w[0] = (uint32_t)__bfloat16_as_ushort(p[0]);
+  }
+  return r;
+}
+
+template <typename T, int V>
+__device__ __forceinline__ float row_get(const Row<T, V>& r, int v) {
+  if constexpr (sizeof(T) == 4) {
+    return __uint_as_float(r.w[v]);
+  } else if constexpr (V == 1) {
+    return __uint_as_float(r.w[0] << 16);
+  } else {
+    const uint32_t w = r.w[v >> 1];
+    return __uint_as_float((v & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T raw_elem(uint32_t bits);
+template <>
+__device__ __forceinline__ float raw_elem<float>(uint32_t bits) {
+  return __uint_as_float(bits);
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 raw_elem<__nv_bfloat16>(uint32_t bits) {
+  return __ushort_as_bfloat16((unsigned short)bits);
+}
+
+// the raw stored bits of element v (exact copy for the carried state)
+template <typename T, int V>
+__device__ __forceinline__ T row_raw(const Row<T, V>& r, int v) {
+  if constexpr (sizeof(T) == 4) {
+    return raw_elem<T>(r.w[v]);
+  } else if constexpr (V == 1) {
+    return raw_elem<T>(r.w[0]);
+  } else {
+    const uint32_t w = r.w[v >> 1];
+    return raw_elem<T>((v & 1) ? (w >> 16) : (w & 0xffffu));
+  }
+}
+
+template <typename TOut, int V>
+__device__ __forceinline__ void store_out(TOut* p, const float (&o)[V]) {
+  if constexpr (sizeof(TOut) == 2 && V == 8) {
+    uint4 v;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+      w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o[2 * i])) |
+             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o[2 * i + 1])) << 16);
+    __stcs(reinterpret_cast<uint4*>(p), v);
+  } else if constexpr (sizeof(TOut) == 4 && V % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < V / 4; i++)
+      __stcs(reinterpret_cast<float4*>(p) + i, make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; i++) p[i] = from_f32<TOut>(o[i]);
+  }
+}
+
+template <typename TIn, typename TOut, int K, int V, bool SILU>
+__global__ void __launch_bounds__(kConvThreads, 2) conv1d_fwd_kernel(const __grid_constant__ ConvParams p) {
+  constexpr int H = K - 1;
+  constexpr int W = kConvTT + H;  // window rows
+  const int64_t L = p.seqlen, Dm = p.dim;
+  const int64_t nvec = Dm / V;
+  const int64_t nt = (L + kConvTT - 1) / kConvTT;
+  const int64_t gid = (int64_t)blockIdx.x * kConvThreads + threadIdx.x;
+  if (gid >= p.batch * nt * nvec) return;
+  const int64_t vec = gid % nvec, rest = gid / nvec;
+  const int64_t tc = rest % nt, b = rest / nt;
+  const int64_t d0 = vec * V, t0 = tc * kConvTT;
+  const TIn* gx = static_cast<const TIn*>(p.x);
+  const TIn* gs = static_cast<const TIn*>(p.state_in);
+
+  // the window: rows t0-H .. t0+kConvTT-1, all loads first
+  Row<TIn, V> win[W];
+#pragma unroll
+  for (int r = 0; r < W; r++) {
+    const int64_t t = t0 - H + r;
+    if (t >= 0 && t < L) {
+      win[r] = load_row<TIn, V>(gx + (b * L + t) * Dm + d0);
+    } else if (t < 0 && gs) {
+      // the carried inputs before t = 0: state[b, d, t + H] per channel
+#pragma unroll
+      for (int i = 0; i < Row<TIn, V>::kN; i++) win[r].w[i] = 0u;
+      if constexpr (sizeof(TIn) == 4) {
+#pragma unroll
+        for (int v = 0; v < V; v++)
+          win[r].w[v] = __float_as_uint(reinterpret_cast<const float*>(gs)[(b * Dm + d0 + v) * H + t + H]);
+      } else if constexpr (V == 1) {
+        win[r].w[0] = (uint32_t)__bfloat16_as_ushort(gs[(b * Dm + d0) * H + t + H]);
+      } else {
+#pragma unroll
+        for (int v = 0; v < V; v++) {
+          const uint32_t bits = (uint32_t)__bfloat16_as_ushort(gs[(b * Dm + d0 + v) * H + t + H]);
+          win[r].w[v >> 1] |= (v & 1) ? (bits << 16) : bits;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < Row<TIn, V>::kN; i++) win[r].w[i] = 0u;
+    }
+  }
+
+  // taps and biases of the thread's V channels: contiguous, loaded as 16-byte
+  // vectors when the thread owns a vector of channels
+  float w[V * K], bias[V];
+  if constexpr (V > 1) {
+#pragma unroll
+    for (int i = 0; i < V * K / 4; i++) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p.w + d0 * K) + i);
+      w[4 * i] = q.x;
+      w[4 * i + 1] = q.y;
+      w[4 * i + 2] = q.z;
+      w[4 * i + 3] = q.w;
+    }
+#pragma unroll
+    for (int i = 0; i < V / 4; i++) {
+      const float4 q = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + d0) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      bias[4 * i] = q.x;
+      bias[4 * i + 1] = q.y;
+      bias[4 * i + 2] = q.z;
+      bias[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < K; k++) w[k] = __ldg(p.w + d0 * K + k);
+    bias[0] = p.bias ? __ldg(p.bias + d0) : 0.f;
+  }
+
+  // each input row is widened once and scattered into the K outputs that use
+  // it; output j is complete after row j + H and is stored then (a ring of K
+  // partial sums per channel, indexed at compile time)
+  TOut* gy = static_cast<TOut*>(p.y) + (b * L + t0) * Dm + d0;
+  float acc[K][V];
+#pragma unroll
+  for (int r = 0; r < W; r++) {
+    float xr[V];
+#pragma unroll
+    for (int v = 0; v < V; v++) xr[v] = row_get<TIn, V>(win[r], v);
+    // row r is tap k of output j = r - k
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+      const int j = r - k;
+      if (j >= 0 && j < kConvTT) {
+        float (&a)[V] = acc[j % K];
+#pragma unroll
+        for (int v = 0; v < V; v++) a[v] = fmaf(w[v * K + k], xr[v], k == 0 ? bias[v] : a[v]);
+      }
+    }
+    const int jd = r - H;  // the output completed by this row
+    if (jd >= 0 && t0 + jd < L) {
+      float o[V];
+#pragma unroll
+      for (int v = 0; v < V; v++) o[v] = SILU ? silu(acc[jd % K][v]) : acc[jd % K][v];
+      store_out<TOut, V>(gy + jd * Dm, o);
+    }
+  }
+
+  // the chunk holding the last timestep hands on the last H inputs
+  if (p.state_out && t0 + kConvTT >= L) {
+    TIn* so = static_cast<TIn*>(p.state_out);
+    // rows at positions L-H .. L-1 (compile-time row indices keep the window
+    // in registers)
+#pragma unroll
+    for (int r = 0; r < W; r++) {
+      const int64_t k = t0 - H + r - (L - H);  // state slot of window row r
+      if (k >= 0 && k < H) {
+#pragma unroll
+        for (int v = 0; v < V; v++) so[(b * Dm + d0 + v) * H + k] = row_raw<TIn, V>(win[r], v);
+      }
+    }
+  }
+}
+
+// element i of a packed array of T held in 32-bit words (i known at compile time)
+template <typename T>
+__device__ __forceinline__ uint32_t word_elem(const uint32_t* wd, int i) {
+  if constexpr (sizeof(T) == 4) return wd[i];
+  else return (i & 1) ? (wd[i >> 1] >> 16) : (wd[i >> 1] & 0xffffu);
+}
+template <typename T>
+__device__ __forceinline__ void set_word_elem(uint32_t* wd, int i, uint32_t bits) {
+  if constexpr (sizeof(T) == 4) wd[i] = bits;
+  else wd[i >> 1] = (i & 1) ? ((wd[i >> 1] & 0xffffu) | (bits << 16)) : ((wd[i >> 1] & 0xffff0000u) | bits);
+}
+template <typename T>
+__device__ __forceinline__ float bits_f32(uint32_t bits) {
+  return sizeof(T) == 4 ? __uint_as_float(bits) : __uint_as_float(bits << 16);
+}
+
+template <typename TIn, typename TOut, int K, int V, bool SILU>
+__global__ void __launch_bounds__(kConvThreads) conv1d_update_kernel(const __grid_constant__ ConvParams p) {
+  // V consecutive channels per thread: their states (V x H elements) are
+  // contiguous, so state, x and y move as whole 16-byte vectors when V > 1
+  constexpr int H = K - 1;
+  const int64_t g = (int64_t)blockIdx.x * kConvThreads + threadIdx.x;
+  const int64_t c0 = g * V;  // first channel (flattened over batch x dim)
+  if (c0 >= p.batch * p.dim) return;
+  const int64_t d0 = c0 % p.dim;
+  TIn* st = static_cast<TIn*>(p.state_out) + c0 * H;
+  const TIn* gx = static_cast<const TIn*>(p.x) + c0;
+  constexpr int SW = (int)((V * H * sizeof(TIn) + 3) / 4), XW = (int)((V * sizeof(TIn) + 3) / 4);
+  uint32_t sw[SW], xw[XW];
+  if constexpr (V > 1) {
+#pragma unroll
+    for (int i = 0; i < SW / 4; i++) {
+      const uint4 q = reinterpret_cast<const uint4*>(st)[i];
+      sw[4 * i] = q.x;
+      sw[4 * i + 1] = q.y;
+      sw[4 * i + 2] = q.z;
+      sw[4 * i + 3] = q.w;
+    }
+#pragma unroll
+    for (int i = 0; i < XW / 4; i++) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(gx) + i);
+      xw[4 * i] = q.x;
+      xw[4 * i + 1] = q.y;
+      xw[4 * i + 2] = q.z;
+      xw[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < SW; i++) sw[i] = 0u;
+    xw[0] = 0u;
+#pragma unroll
+    for (int k = 0; k < H; k++) set_word_elem<TIn>(sw, k, sizeof(TIn) == 4 ? __float_as_uint(to_f32(st[k])) : (uint32_t)__bfloat16_as_ushort(*reinterpret_cast<const __nv_bfloat16*>(st + k)));
+    set_word_elem<TIn>(xw, 0, sizeof(TIn) == 4 ? __float_as_uint(to_f32(gx[0])) : (uint32_t)__bfloat16_as_ushort(*reinterpret_cast<const __nv_bfloat16*>(gx)));
+  }
+  // taps and biases of the V channels: contiguous, 16-byte vectors when V > 1
+  float w[V * K], bias[V];
+  if constexpr (V > 1) {
+#pragma unroll
+    for (int i = 0; i < V * K / 4; i++) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p.w + d0 * K) + i);
+      w[4 * i] = q.x;
+      w[4 * i + 1] = q.y;
+      w[4 * i + 2] = q.z;
+      w[4 * i + 3] = q.w;
+    }
+#pragma unroll
+    for (int i = 0; i < V / 4; i++) {
+      const float4 q = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + d0) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      bias[4 * i] = q.x;
+      bias[4 * i + 1] = q.y;
+      bias[4 * i + 2] = q.z;
+      bias[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < K; k++) w[k] = __ldg(p.w + d0 * K + k);
+    bias[0] = p.bias ? __ldg(p.bias + d0) : 0.f;
+  }
+  float o[V];
+#pragma unroll
+  for (int v = 0; v < V; v++) {
+    float acc = bias[v];
+#pragma unroll
+    for (int k = 0; k < H; k++) acc = fmaf(w[v * K + k], bits_f32<TIn>(word_elem<TIn>(sw, v * H + k)), acc);
+    acc = fmaf(w[v * K + H], bits_f32<TIn>(word_elem<TIn>(xw, v)), acc);
+    o[v] = SILU ? silu(acc) : acc;
+  }
+  store_out<TOut, V>(static_cast<TOut*>(p.y) + c0, o);
+  // drop each channel's oldest input, append the new one
+  uint32_t nw[SW];
+#pragma unroll
+  for (int i = 0; i < SW; i++) nw[i] = 0u;
+#pragma unroll
+  for (int v = 0; v < V; v++) {
+#pragma unroll
+    for (int k = 0; k + 1 < H; k++) set_word_elem<TIn>(nw, v * H + k, word_elem<TIn>(sw, v * H + k + 1));
+    set_word_elem<TIn>(nw, v * H + H - 1, word_elem<TIn>(xw, v));
+  }
+  if constexpr (V > 1) {
+#pragma unroll
+    for (int i = 0; i < SW / 4; i++) reinterpret_cast<uint4*>(st)[i] = make_uint4(nw[4 * i], nw[4 * i + 1], nw[4 * i + 2], nw[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < H; k++) {
+      const uint32_t bits = word_elem<TIn>(nw, k);
+      if constexpr (sizeof(TIn) == 4) reinterpret_cast<float*>(st)[k] = __uint_as_float(bits);
+      else reinterpret_cast<__nv_bfloat16*>(st)[k] = __ushort_as_bfloat16((unsigned short)bits);
+    }
+  }
+}
+
+template <typename TIn, typename TOut, int K, int V>
+cudaError_t launch_fwd_kv(const ConvParams& p, cudaStream_t s) {
+  const int64_t nt = (p.seqlen + kConvTT - 1) / kConvTT;
+  const int64_t n = p.batch * nt * (p.dim / V);
+  const int64_t blocks = (n + kConvThreads - 1) / kConvThreads;
+  if (p.silu) conv1d_fwd_kernel<TIn, TOut, K, V, true><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
+  else conv1d_fwd_kernel<TIn, TOut, K, V, false><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut, int K>
+cudaError_t launch_fwd_k(const ConvParams& p, bool vec, cudaStream_t s) {
+  constexpr int VV = 16 / (int)sizeof(TIn);
+  return vec ? launch_fwd_kv<TIn, TOut, K, VV>(p, s) : launch_fwd_kv<TIn, TOut, K, 1>(p, s);
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_fwd_io(const ConvParams& p, bool vec, cudaStream_t s) {
+  switch (p.width) {
+    case 2: return launch_fwd_k<TIn, TOut, 2>(p, vec, s);
+    case 3: return launch_fwd_k<TIn, TOut, 3>(p, vec, s);
+    case 4: return launch_fwd_k<TIn, TOut, 4>(p, vec, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename TIn, typename TOut, int K, int V>
+cudaError_t launch_upd_kv(const ConvParams& p, cudaStream_t s) {
+  const int64_t threads = (p.batch * p.dim + V - 1) / V;
+  const int64_t blocks = (threads + kConvThreads - 1) / kConvThreads;
+  if (p.silu) conv1d_update_kernel<TIn, TOut, K, V, true><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
+  else conv1d_update_kernel<TIn, TOut, K, V, false><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_upd_io(const ConvParams& p, bool vec, cudaStream_t s) {
+  constexpr int VV = 16 / (int)sizeof(TIn);
+  switch (p.width) {
+    case 2: return vec ? launch_upd_kv<TIn, TOut, 2, VV>(p, s) : launch_upd_kv<TIn, TOut, 2, 1>(p, s);
+    case 3: return vec ? launch_upd_kv<TIn, TOut, 3, VV>(p, s) : launch_upd_kv<TIn, TOut, 3, 1>(p, s);
+    case 4: return vec ? launch_upd_kv<TIn, TOut, 4, VV>(p, s) : launch_upd_kv<TIn, TOut, 4, 1>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_conv1d_fwd(const ConvParams& p, ss_dtype in_dtype, ss_dtype out_dtype, bool vec,
+                              cudaStream_t stream) {
+  if (in_dtype == SS_BF16)
+    return out_dtype == SS_BF16 ? launch_fwd_io<__nv_bfloat16, __nv_bfloat16>(p, vec, stream)
+                                : launch_fwd_io<__nv_bfloat16, float>(p, vec, stream);
+  return out_dtype == SS_BF16 ? launch_fwd_io<float, __nv_bfloat16>(p, vec, stream)
+                              : launch_fwd_io<float, float>(p, vec, stream);
+}
+
+cudaError_t launch_conv1d_update(const ConvParams& p, ss_dtype in_dtype, ss_dtype out_dtype, bool vec,
+                                 cudaStream_t stream) {
+  if (in_dtype == SS_BF16)
+    return out_dtype == SS_BF16 ? launch_upd_io<__nv_bfloat16, __nv_bfloat16>(p, vec, stream)
+                                : launch_upd_io<__nv_bfloat16, float>(p, vec, stream);
+  return out_dtype == SS_BF16 ? launch_upd_io<float, __nv_bfloat16>(p, vec, stream)
+                              : launch_upd_io<float, float>(p, vec, stream);
+}
+
+}  // namespace ssk

@@ -65,6 +65,21 @@ struct StepParams {
   int64_t batch, dim;
 };
 
+// Parameters of the convolution front-end (forward: x [batch, seqlen, dim],
+// state_in/state_out [batch, dim, width-1]; decode: x [batch, dim], state_out
+// is the state updated in place).
+struct ConvParams {
+  const void* x;
+  const float* w;        // [dim, width]
+  const float* bias;     // [dim] or null
+  const void* state_in;  // may be null (zeros before t = 0)
+  void* y;
+  void* state_out;       // may be null (forward)
+  int64_t batch, seqlen, dim;
+  int width;
+  int silu;
+};
+
 // Launch plan for a scan problem.
 struct ScanPlan {
   int sg;               // threads per channel (1 or 2); each owns 16/sg states
@@ -96,6 +111,10 @@ int scan_header_words();
 uint32_t scan_header_magic();
 int scan_warps_per_sm(ss_dtype in_dtype, int sg);  // resident warps per SM allowed by shared memory
 cudaError_t launch_state_update(const StepParams& p, ss_dtype in_dtype, ss_dtype out_dtype, cudaStream_t stream);
+cudaError_t launch_conv1d_fwd(const ConvParams& p, ss_dtype in_dtype, ss_dtype out_dtype, bool vec,
+                              cudaStream_t stream);
+cudaError_t launch_conv1d_update(const ConvParams& p, ss_dtype in_dtype, ss_dtype out_dtype, bool vec,
+                                 cudaStream_t stream);
 
 // The library's own fault word (device symbol), used when no workspace is given.
 unsigned int* device_fault_word();
