@@ -13,7 +13,8 @@ Every function here is pinned by the `-m "not gpu"` tests in
 tests/test_oracle_pins.py (brute-force unrolled sum, LTI convolution checked
 directly and by FFT, delta->0, large delta, chunk associativity, geometric
 closed form, hand-computed L=1, zero/linearity/independence properties,
-decode-equals-scan; for the convolution front-end: numpy's convolution,
+decode-equals-scan; for the gradients: central finite differences of the
+forward oracle; for the convolution front-end: numpy's convolution,
 impulse responses, chunk continuity through the state, decode-equals-forward).
 """
 
@@ -45,6 +46,8 @@ def load(path: str = None) -> ctypes.CDLL:
         lib.ss_oracle_state_update.argtypes = [_I64, _I64, _I64, ctypes.c_int, _P,
                                                _P, _P, _P, _P, _P, _P, _P, _P,
                                                _P, _I64, _P]
+        lib.ss_oracle_scan_bwd.restype = ctypes.c_int
+        lib.ss_oracle_scan_bwd.argtypes = [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int] + [_P] * 20
         lib.ss_oracle_conv1d.restype = ctypes.c_int
         lib.ss_oracle_conv1d.argtypes = [_I64, _I64, _I64, _I64, ctypes.c_int, _P, _P, _P, _P,
                                          ctypes.c_int, _P, _P]
@@ -193,4 +196,29 @@ def conv1d_update(state: np.ndarray, x, weight, bias=None, silu: bool = True, li
     if rc != 0:
         raise ValueError("oracle conv1d_update rejected its arguments")
     return y
+
+
+def scan_bwd(x: dict, dy, dh_last=None, lib_path: str = None) -> dict:
+    """Gradients of the selective scan in float64 (reverse sweep of the adjoint).
+
+    x: the forward inputs as for scan(); dy [Bt, L, D] CPU tensor (float32 or
+    bfloat16): the gradient of y; dh_last [Bt, D, N] float32 or None: of h_last.
+    Returns float64 numpy arrays du, ddelta_raw, dz [Bt, L, D]; dA [D, N];
+    dB, dC [Bt, L, N]; dD, ddelta_bias [D]; dh0 [Bt, D, N].
+    """
+    lib = load(lib_path)
+    u, dr, z, B, C = x["u"], x["delta_raw"], x.get("z"), x["B"], x["C"]
+    Bt, L, Dm = u.shape
+    N = B.shape[-1]
+    out = {k: np.zeros(sh) for k, sh in [("du", (Bt, L, Dm)), ("ddelta_raw", (Bt, L, Dm)), ("dz", (Bt, L, Dm)),
+                                         ("dA", (Dm, N)), ("dB", (Bt, L, N)), ("dC", (Bt, L, N)), ("dD", (Dm,)),
+                                         ("ddelta_bias", (Dm,)), ("dh0", (Bt, Dm, N))]}
+    rc = lib.ss_oracle_scan_bwd(Bt, L, Dm, N, _dtype_code(u), _dtype_code(dy), _ptr(u), _ptr(dr), _ptr(z), _ptr(B),
+                                _ptr(C), _ptr(_f32(x["A"])), _ptr(_f32(x.get("D"))), _ptr(_f32(x.get("delta_bias"))),
+                                _ptr(_f32(x.get("h0"))), _ptr(dy.contiguous()), _ptr(_f32(dh_last)),
+                                *[out[k].ctypes.data for k in ("du", "ddelta_raw", "dz", "dA", "dB", "dC", "dD",
+                                                               "ddelta_bias", "dh0")])
+    if rc != 0:
+        raise ValueError("oracle scan_bwd rejected its arguments")
+    return out
 

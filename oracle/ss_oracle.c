@@ -38,7 +38,9 @@
  * Parity pins live in the tests (brute-force unrolled sum, LTI convolution,
  * delta->0, large delta, chunk associativity, closed forms).
  *
- * The file also holds the block's causal depthwise convolution front-end and
+ * The file also holds the gradients of the scan (ss_oracle_scan_bwd, pinned by
+ * central finite differences of the forward oracle), and the block's causal
+ * depthwise convolution front-end and
  * its decode step (ss_oracle_conv1d, ss_oracle_conv1d_update, at the end),
  * pinned against numpy's convolution, impulse responses, chunk continuity and
  * decode-equals-forward.
@@ -264,5 +266,113 @@ int ss_oracle_conv1d_update(int64_t batch, int64_t dim, int64_t width, int in_dt
       if (H > 0) s[H - 1] = xv;
     }
   }
+  return 0;
+}
+
+/*
+ * Gradients of the selective scan (the backward pass), by the reverse sweep of
+ * the adjoint state, in float64. The pages train Mamba end to end and say the
+ * backward pass recomputes the forward states instead of storing them (review
+ * page, method step 2 (3); "AI 推理系列（十四）", training section); the
+ * gradients themselves follow from differentiating the recurrence the header
+ * defines. For each channel (b, d), with dyv_t = dy_t * g_t, g_t = silu(z_t)
+ * (1 when z is NULL) and yv_t = sum_n C_t,n h_t,n + D u_t:
+ *   lambda_{L-1} = C_{L-1} dyv_{L-1} + dh_last
+ *   lambda_t     = C_t dyv_t + Abar_{t+1} lambda_{t+1}          (per state n)
+ *   dB[b,t,n]   += lambda_t,n delta_t u_t        (summed over channels d)
+ *   dC[b,t,n]   += dyv_t h_t,n                   (summed over channels d)
+ *   du_t         = dyv_t D + delta_t sum_n lambda_t,n B_t,n
+ *   ddelta_t     = sum_n lambda_t,n (h_{t-1},n Abar_t,n A_n + B_t,n u_t)
+ *   dA[d,n]     += lambda_t,n h_{t-1},n Abar_t,n delta_t
+ *   dD[d]       += dyv_t u_t
+ *   dz_t         = dy_t yv_t silu'(z_t),  silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   ddelta_raw_t = ddelta_t sigmoid(delta_raw_t + bias_d);   dbias[d] += ddelta_raw_t
+ *   dh0[b,d,n]   = Abar_0,n lambda_0,n
+ * dy: [batch][seqlen][dim] in dy_dtype; dh_last, h0: [batch][dim][dstate] or NULL.
+ * Outputs (float64, overwritten): du, ddelta_raw, dz [batch][seqlen][dim]; dA
+ * [dim][dstate]; dB, dC [batch][seqlen][dstate]; dD, dbias [dim]; dh0
+ * [batch][dim][dstate]. Single-threaded (the reductions over channels).
+ */
+static double dsilu(double z) {
+  const double s = 1.0 / (1.0 + exp(-z));
+  return s * (1.0 + z * (1.0 - s));
+}
+
+int ss_oracle_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int in_dtype, int dy_dtype,
+                       const void *u, const void *delta_raw, const void *z, const void *B, const void *C,
+                       const float *A, const float *Dskip, const float *bias, const float *h0, const void *dy,
+                       const float *dh_last, double *du, double *ddelta_raw, double *dz, double *dA, double *dB,
+                       double *dC, double *dD, double *dbias, double *dh0) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0) return -1;
+  if ((in_dtype != ORC_F32 && in_dtype != ORC_BF16) || (dy_dtype != ORC_F32 && dy_dtype != ORC_BF16)) return -1;
+  if (!u || !delta_raw || !B || !C || !A || !dy || !du || !ddelta_raw || !dz || !dA || !dB || !dC || !dD ||
+      !dbias || !dh0)
+    return -1;
+  const int64_t L = seqlen, Dm = dim, N = dstate;
+  memset(dA, 0, sizeof(double) * (size_t)(Dm * N));
+  memset(dB, 0, sizeof(double) * (size_t)(batch * L * N));
+  memset(dC, 0, sizeof(double) * (size_t)(batch * L * N));
+  memset(dD, 0, sizeof(double) * (size_t)Dm);
+  memset(dbias, 0, sizeof(double) * (size_t)Dm);
+  double *hist = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N)); /* hist[t+1] = h_t, hist[0] = h0 */
+  double *lam = (double *)malloc(sizeof(double) * (size_t)N);
+  double *delta = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  if (!hist || !lam || !delta) {
+    free(hist);
+    free(lam);
+    free(delta);
+    return -1;
+  }
+  for (int64_t b = 0; b < batch; b++) {
+    for (int64_t d = 0; d < Dm; d++) {
+      const double bs = bias ? (double)bias[d] : 0.0;
+      const double dsk = Dskip ? (double)Dskip[d] : 0.0;
+      /* forward, keeping every state */
+      for (int64_t n = 0; n < N; n++) hist[n] = h0 ? (double)h0[(b * Dm + d) * N + n] : 0.0;
+      for (int64_t t = 0; t < L; t++) {
+        const int64_t i = (b * L + t) * Dm + d, r = (b * L + t) * N;
+        delta[t] = softplus(widen(delta_raw, in_dtype, i) + bs);
+        const double x = widen(u, in_dtype, i);
+        for (int64_t n = 0; n < N; n++)
+          hist[(t + 1) * N + n] = exp(delta[t] * (double)A[d * N + n]) * hist[t * N + n] +
+                                  delta[t] * widen(B, in_dtype, r + n) * x;
+      }
+      /* reverse sweep of the adjoint state */
+      for (int64_t n = 0; n < N; n++) lam[n] = dh_last ? (double)dh_last[(b * Dm + d) * N + n] : 0.0;
+      for (int64_t t = L - 1; t >= 0; t--) {
+        const int64_t i = (b * L + t) * Dm + d, r = (b * L + t) * N;
+        const double x = widen(u, in_dtype, i);
+        const double dyt = widen(dy, dy_dtype, i);
+        const double zz = z ? widen(z, in_dtype, i) : 0.0;
+        const double g = z ? silu(zz) : 1.0;
+        const double dyv = dyt * g;
+        double yv = dsk * x;
+        for (int64_t n = 0; n < N; n++) yv += widen(C, in_dtype, r + n) * hist[(t + 1) * N + n];
+        double dut = dyv * dsk, ddel = 0.0;
+        for (int64_t n = 0; n < N; n++) {
+          const double a = exp(delta[t] * (double)A[d * N + n]);
+          const double Bn = widen(B, in_dtype, r + n), Cn = widen(C, in_dtype, r + n);
+          /* lambda_t = C_t dyv_t + (already folded) Abar_{t+1} lambda_{t+1} */
+          lam[n] += Cn * dyv;
+          dC[r + n] += dyv * hist[(t + 1) * N + n];
+          dB[r + n] += lam[n] * delta[t] * x;
+          dut += lam[n] * delta[t] * Bn;
+          ddel += lam[n] * (hist[t * N + n] * a * (double)A[d * N + n] + Bn * x);
+          dA[d * N + n] += lam[n] * hist[t * N + n] * a * delta[t];
+          lam[n] *= a; /* becomes Abar_t lambda_t, the carry into step t-1 */
+        }
+        dD[d] += dyv * x;
+        du[i] = dut;
+        dz[i] = z ? dyt * yv * dsilu(zz) : 0.0;
+        const double sg = 1.0 / (1.0 + exp(-(widen(delta_raw, in_dtype, i) + bs)));
+        ddelta_raw[i] = ddel * sg;
+        dbias[d] += ddel * sg;
+      }
+      for (int64_t n = 0; n < N; n++) dh0[(b * Dm + d) * N + n] = lam[n]; /* Abar_0 lambda_0 */
+    }
+  }
+  free(hist);
+  free(lam);
+  free(delta);
   return 0;
 }

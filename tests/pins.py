@@ -418,7 +418,64 @@ def pin_conv_decode_equals_forward(lib=None):
     np.testing.assert_allclose(st, so, rtol=0, atol=0)
 
 
-ALL_PINS = [pin_conv_numpy, pin_conv_impulse, pin_conv_chunk_continuity, pin_conv_decode_equals_forward,
+# ----------------------------------------------------------------- gradients
+# The backward pass the pages' training recomputes (review page, method step 2
+# (3)), pinned against central finite differences of the forward oracle: with
+# loss = sum(w_y * y) + sum(w_h * h_last), dy = w_y and dh_last = w_h; each
+# sampled input entry is moved by +-2^-10 (exact in float32).
+
+def _fd_loss(x, wy, wh, path):
+    y, h = oracle.scan(x, lib_path=path)
+    return float(np.sum(wy * y) + np.sum(wh * h))
+
+
+def pin_backward_finite_differences(lib=None):
+    path = lib
+    rng = np.random.default_rng(5)
+    for (Bt, L, Dm, N, seed, hz, with_h0) in [(2, 9, 3, 4, 1, True, True), (1, 6, 2, 3, 2, False, False)]:
+        x = random_scan_inputs(Bt, L, Dm, N, in_dtype="f32", seed=seed, with_h0=with_h0, has_z=hz,
+                               a_log_jitter=0.3, delta_raw_scale=1.0)
+        if with_h0:
+            x["h0"] = (0.5 * x["h0"]).contiguous()
+        wy = rng.normal(size=(Bt, L, Dm))
+        wh = rng.normal(size=(Bt, Dm, N))
+        g = oracle.scan_bwd(x, torch.tensor(wy, dtype=torch.float32),
+                            torch.tensor(wh, dtype=torch.float32), lib_path=path)
+        # the loss weights as stored in float32 (what the backward saw)
+        wy = torch.tensor(wy, dtype=torch.float32).double().numpy()
+        wh = torch.tensor(wh, dtype=torch.float32).double().numpy()
+        hstep = 2.0 ** -10
+        checks = [("u", "du"), ("delta_raw", "ddelta_raw"), ("B", "dB"), ("C", "dC"), ("A", "dA"), ("D", "dD"),
+                  ("delta_bias", "ddelta_bias")] + ([("z", "dz")] if hz else []) + ([("h0", "dh0")] if with_h0 else [])
+        for name, gname in checks:
+            t = x[name]
+            flat = t.view(-1)
+            for idx in rng.choice(flat.numel(), size=min(6, flat.numel()), replace=False):
+                old = float(flat[idx])
+                flat[idx] = old + hstep
+                lp = _fd_loss(x, wy, wh, path)
+                flat[idx] = old - hstep
+                lm = _fd_loss(x, wy, wh, path)
+                flat[idx] = old
+                fd = (lp - lm) / (2 * hstep)
+                an = g[gname].reshape(-1)[idx]
+                assert abs(fd - an) <= 1e-5 * max(1.0, abs(fd)), (name, int(idx), fd, an)
+        if not hz:
+            assert np.all(g["dz"] == 0.0)
+
+
+def pin_backward_bf16_widening(lib=None):
+    # bf16 inputs give the gradients of the same values held as float32
+    x = random_scan_inputs(2, 11, 3, 4, in_dtype="bf16", seed=8, with_h0=True)
+    xf = {k: (v.float() if isinstance(v, torch.Tensor) and v.dtype == torch.bfloat16 else v) for k, v in x.items()}
+    dy = torch.randn(2, 11, 3, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    g1 = oracle.scan_bwd(x, dy, lib_path=lib)
+    g2 = oracle.scan_bwd(xf, dy.float(), lib_path=lib)
+    for k in g1:
+        np.testing.assert_allclose(g1[k], g2[k], rtol=0, atol=0)
+
+
+ALL_PINS = [pin_backward_finite_differences, pin_backward_bf16_widening, pin_conv_numpy, pin_conv_impulse, pin_conv_chunk_continuity, pin_conv_decode_equals_forward,
             pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_large_delta_overwrites,
             pin_chunk_associativity, pin_geometric_series, pin_single_step_by_hand, pin_softplus_values,
             pin_zeros, pin_linearity_in_u, pin_independence, pin_decode_equals_scan,

@@ -33,6 +33,15 @@ MUTANTS = {
     "batch_stride_B": ("const int64_t r = (b * L + t) * N;", "const int64_t r = (t) * N;"),
     "decode_exp_sign": ("hs[n] = exp(delta * (double)A[d * dstate + n]) * hs[n] +",
                         "hs[n] = exp(-delta * (double)A[d * dstate + n]) * hs[n] +"),
+    # backward pass
+    "bwd_no_decay_of_adjoint": ("lam[n] *= a; /* becomes", "lam[n] *= 1.0; /* becomes"),
+    "bwd_dA_uses_h_t": ("dA[d * N + n] += lam[n] * hist[t * N + n] * a * delta[t];",
+                        "dA[d * N + n] += lam[n] * hist[(t + 1) * N + n] * a * delta[t];"),
+    "bwd_dC_uses_lambda": ("dC[r + n] += dyv * hist[(t + 1) * N + n];", "dC[r + n] += lam[n] * hist[(t + 1) * N + n];"),
+    "bwd_dB_without_delta": ("dB[r + n] += lam[n] * delta[t] * x;", "dB[r + n] += lam[n] * x;"),
+    "bwd_no_softplus_derivative": ("ddelta_raw[i] = ddel * sg;", "ddelta_raw[i] = ddel;"),
+    "bwd_dh_last_ignored": ("lam[n] = dh_last ? (double)dh_last[(b * Dm + d) * N + n] : 0.0;", "lam[n] = 0.0;"),
+    "bwd_gate_derivative_is_sigmoid": ("return s * (1.0 + z * (1.0 - s));", "return s;"),
     # convolution front-end
     "conv_taps_reversed": ("pre += (double)w[d * width + k] * e[t + k];",
                            "pre += (double)w[d * width + (width - 1 - k)] * e[t + k];"),
