@@ -2,7 +2,7 @@
  * ss_scan.h — C ABI of the B300 (sm_103a) selective state-space scan library
  * (libssscan.so).
  *
- * What it computes (the S6 layer's scan, forward only). For every batch
+ * What it computes (the S6 layer's scan; its gradients are in ss_scan_bwd). For every batch
  * element b and channel d, with state h[n] (n < dstate) starting at h0[b,d,:]
  * (zeros when h0 is NULL), for t = 0 .. seqlen-1:
  *
@@ -164,6 +164,62 @@ ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width,
                            ss_dtype in_dtype, ss_dtype out_dtype,
                            void *state, const void *x, const float *weight, const float *bias,
                            int silu, void *y, void *stream);
+
+/*
+ * Gradients of the selective scan (backward pass).
+ *
+ * The pages train the model end to end and say the backward pass recomputes
+ * the scan's intermediate states instead of keeping them in HBM ("Mamba:
+ * Linear-Time Sequence Modeling with Selective State Spaces" review page,
+ * method step 2 (3); "AI 推理系列（十四）：Mamba 的 Selective State Space",
+ * training section). They print no gradient formulas; these are the
+ * derivatives of the forward defined above. Per channel (b, d), with
+ * dyv_t = dy[b,t,d] * silu(z[b,t,d]) (dy itself when z is NULL),
+ * yv_t the ungated output, Abar_t,n = exp(delta_t A[d,n]) and the adjoint
+ * lambda_t,n = dL/dh_t,n:
+ *
+ *   lambda_{L-1} = C_{L-1} dyv_{L-1} + dh_last;  lambda_t = C_t dyv_t + Abar_{t+1} lambda_{t+1}
+ *   du[b,t,d]          = dyv_t D[d] + delta_t sum_n lambda_t,n B[b,t,n]
+ *   ddelta_raw[b,t,d]  = sigmoid(delta_raw + delta_bias[d])
+ *                        * sum_n lambda_t,n (h_{t-1},n Abar_t,n A[d,n] + B[b,t,n] u[b,t,d])
+ *   dz[b,t,d]          = dy yv_t silu'(z),  silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   dA[d,n]           = sum_{b,t} lambda_t,n h_{t-1},n Abar_t,n delta_t
+ *   dB[b,t,n]         = sum_d lambda_t,n delta_t u[b,t,d]
+ *   dC[b,t,n]         = sum_d dyv_t h_t,n
+ *   dD[d]             = sum_{b,t} dyv_t u[b,t,d]
+ *   ddelta_bias[d]    = sum_{b,t} ddelta_raw[b,t,d]
+ *   dh0[b,d,n]        = Abar_0,n lambda_0,n
+ *
+ * Inputs are the forward's (same shapes, dtypes and NULL rules as
+ * ss_scan_fwd) plus
+ *  dy        : [batch, seqlen, dim] dy_dtype (SS_F32 or SS_BF16)
+ *  dh_last   : [batch, dim, dstate] float32 or NULL (zero): gradient of h_last
+ * Outputs (all overwritten):
+ *  du, ddelta_raw : [batch, seqlen, dim] in_dtype
+ *  dz             : [batch, seqlen, dim] in_dtype; required when z is given, ignored otherwise
+ *  dA             : [dim, dstate] float32
+ *  dB, dC         : [batch, seqlen, dstate] float32
+ *  dD, ddelta_bias: [dim] float32 or NULL (not computed)
+ *  dh0            : [batch, dim, dstate] float32 or NULL (not computed)
+ *  workspace      : device buffer of at least ss_scan_bwd_workspace_size() bytes
+ *                   (the states saved every 16 steps); must not be shared by
+ *                   calls that overlap on the GPU.
+ * The sums over channels and time are accumulated with float32 atomic adds,
+ * so dA, dB, dC, dD and ddelta_bias can differ in the last bits from run to
+ * run; the other outputs are deterministic. seqlen == 0 writes dh0 = dh_last
+ * (or zeros) and zero dA, dD, ddelta_bias.
+ */
+size_t ss_scan_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate);
+
+ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                      ss_dtype in_dtype, ss_dtype dy_dtype,
+                      const void *u, const void *delta_raw, const float *A,
+                      const void *B, const void *C, const float *D, const void *z,
+                      const float *delta_bias, const float *h0,
+                      const void *dy, const float *dh_last,
+                      void *du, void *ddelta_raw, void *dz, float *dA, float *dB, float *dC,
+                      float *dD, float *ddelta_bias, float *dh0,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Launch-shape controls for the calling host thread (0 = automatic, the

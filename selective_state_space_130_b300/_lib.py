@@ -36,6 +36,8 @@ SIGNATURES = {
                                      _P, _P, _P, _P, ctypes.c_int, _P, _P, _P]),
     "ss_conv1d_update": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                         _P, _P, _P, _P, ctypes.c_int, _P, _P]),
+    "ss_scan_bwd_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
+    "ss_scan_bwd": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int] + [_P] * 21 + [_SZ, _P]),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
 }
@@ -144,6 +146,47 @@ def ss_scan_fwd(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, h0=None,
                              _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_last),
                              ws_ptr, ws_len, _stream(stream)))
     return y, h_last
+
+
+def ss_scan_bwd_workspace_size(batch, seqlen, dim, dstate=16) -> int:
+    return int(lib().ss_scan_bwd_workspace_size(batch, seqlen, dim, dstate))
+
+
+def ss_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None, dh_last=None, *,
+                out=None, workspace=None, stream=None) -> dict:
+    """Gradients of the selective scan on device tensors.
+
+    Inputs as for ss_scan_fwd, plus dy [Bt, L, D] (float32 or bfloat16) and
+    dh_last [Bt, D, N] float32 or None. Returns a dict: du, ddelta_raw, dz (None
+    without z) in the input dtype; dA [D, N], dB, dC [Bt, L, N], dD,
+    ddelta_bias [D], dh0 [Bt, D, N] in float32. Tensors missing from `out` (and
+    the workspace) are allocated with torch.
+    """
+    Bt, L, Dm = u.shape
+    N = B.shape[-1]
+    code = _dt(u)
+    dev = u.device
+    o = dict(out or {})
+    shapes = {"du": ((Bt, L, Dm), u.dtype), "ddelta_raw": ((Bt, L, Dm), u.dtype), "dA": ((Dm, N), torch.float32),
+              "dB": ((Bt, L, N), torch.float32), "dC": ((Bt, L, N), torch.float32), "dD": ((Dm,), torch.float32),
+              "ddelta_bias": ((Dm,), torch.float32), "dh0": ((Bt, Dm, N), torch.float32)}
+    if z is not None:
+        shapes["dz"] = ((Bt, L, Dm), u.dtype)
+    for k, (sh, dt) in shapes.items():
+        if k not in o:
+            o[k] = torch.empty(sh, dtype=dt, device=dev)
+    o.setdefault("dz", None)
+    ws_bytes = ss_scan_bwd_workspace_size(Bt, L, Dm, N)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().ss_scan_bwd(Bt, L, Dm, N, code, _dt(dy), _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(B), _ptr(C),
+                             _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(dy), _ptr(dh_last),
+                             *[_ptr(o[k]) for k in ("du", "ddelta_raw", "dz", "dA", "dB", "dC", "dD", "ddelta_bias",
+                                                    "dh0")],
+                             ws_ptr, ws_len, _stream(stream)))
+    return o
 
 
 def ss_state_update(h, u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, *, out_dtype=None, y=None,

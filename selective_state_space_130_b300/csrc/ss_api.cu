@@ -368,6 +368,94 @@ ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width, ss_dtype i
   return SS_OK;
 }
 
+size_t ss_scan_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
+  if (batch <= 0 || seqlen <= 0 || dim <= 0 || dstate != ssk::kDState) return 0;
+  return ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim);
+}
+
+ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
+                      ss_dtype dy_dtype, const void* u, const void* delta_raw, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias, const float* h0,
+                      const void* dy, const float* dh_last, void* du, void* ddelta_raw, void* dz, float* dA,
+                      float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (dstate != ssk::kDState) return fail(SS_ERR_UNSUPPORTED, "dstate must be 16 (got %lld)", (long long)dstate);
+  if (!valid_dtype(in_dtype) || !valid_dtype(dy_dtype))
+    return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, dy %d)", (int)in_dtype, (int)dy_dtype);
+  if (batch < 0 || seqlen < 0 || dim < 0) return fail(SS_ERR_INVALID_ARG, "negative size");
+  if (batch > INT32_MAX || seqlen > INT32_MAX || dim > INT32_MAX)
+    return fail(SS_ERR_INVALID_ARG, "a size exceeds 2^31-1");
+  if (batch == 0 || dim == 0) return SS_OK;
+  if ((double)batch * (double)seqlen * (double)dim > 4.0e18) return fail(SS_ERR_INVALID_ARG, "problem too large");
+  if (!A || !dA) return fail(SS_ERR_INVALID_ARG, "A and dA must not be NULL");
+  if (seqlen > 0) {
+    const void* need[] = {u, delta_raw, B, C, dy, du, ddelta_raw, dB, dC};
+    const char* names[] = {"u", "delta_raw", "B", "C", "dy", "du", "ddelta_raw", "dB", "dC"};
+    for (int i = 0; i < 9; i++)
+      if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
+    if (z && !dz) return fail(SS_ERR_INVALID_ARG, "dz must not be NULL when z is given");
+  }
+  const void* all[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dh_last, du, ddelta_raw, dz,
+                       dA, dB, dC, dD, ddelta_bias, dh0, workspace};
+  const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "dy", "dh_last",
+                             "du", "ddelta_raw", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0", "workspace"};
+  for (int i = 0; i < 21; i++)
+    if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  const size_t need_ws = seqlen > 0 ? ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim) : 0;
+  if (need_ws > 0 && (!workspace || workspace_bytes < need_ws))
+    return fail(SS_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu%s)", need_ws, workspace_bytes,
+                workspace ? "" : ", NULL");
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the summed gradients start at zero
+  cudaError_t e = cudaMemsetAsync(dA, 0, (size_t)dim * ssk::kDState * sizeof(float), s);
+  if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, (size_t)dim * sizeof(float), s);
+  if (e == cudaSuccess && ddelta_bias) e = cudaMemsetAsync(ddelta_bias, 0, (size_t)dim * sizeof(float), s);
+  if (e == cudaSuccess && seqlen > 0) e = cudaMemsetAsync(dB, 0, (size_t)batch * seqlen * ssk::kDState * sizeof(float), s);
+  if (e == cudaSuccess && seqlen > 0) e = cudaMemsetAsync(dC, 0, (size_t)batch * seqlen * ssk::kDState * sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, "gradient initialisation");
+  if (seqlen == 0) {
+    // no step: the state gradient passes through unchanged
+    if (!dh0) return SS_OK;
+    const size_t hbytes = (size_t)batch * dim * ssk::kDState * sizeof(float);
+    e = dh_last ? cudaMemcpyAsync(dh0, dh_last, hbytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(dh0, 0, hbytes, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state gradient copy");
+  }
+  ssk::BwdParams p{};
+  p.u = u;
+  p.delta_raw = delta_raw;
+  p.z = z;
+  p.B = B;
+  p.C = C;
+  p.A = A;
+  p.D = D;
+  p.delta_bias = delta_bias;
+  p.h0 = h0;
+  p.dy = dy;
+  p.dh_last = dh_last;
+  p.du = du;
+  p.ddelta_raw = ddelta_raw;
+  p.dz = z ? dz : nullptr;
+  p.dA = dA;
+  p.dB = dB;
+  p.dC = dC;
+  p.dD = dD;
+  p.dbias = ddelta_bias;
+  p.dh0 = dh0;
+  p.ckpt = static_cast<float*>(workspace);
+  p.batch = batch;
+  p.seqlen = seqlen;
+  p.dim = dim;
+  p.ncblk = (int)((dim + 31) / 32);
+  p.nsub = ssk::scan_bwd_subtiles(seqlen);
+  if ((double)batch * p.ncblk > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
+  e = ssk::launch_scan_bwd(p, in_dtype, dy_dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "scan backward launch");
+  return SS_OK;
+}
+
 ss_status ss_scan_status(void* workspace, void* stream) {
   g_err.clear();
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -80,6 +80,35 @@ struct ConvParams {
   int silu;
 };
 
+// Parameters of the scan's backward pass (inputs of the forward, the output
+// gradient, and the gradients written; see ss_scan_bwd).
+struct BwdParams {
+  const void* u;
+  const void* delta_raw;
+  const void* z;            // may be null
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;           // may be null
+  const float* delta_bias;  // may be null
+  const float* h0;          // may be null
+  const void* dy;
+  const float* dh_last;     // may be null
+  void* du;
+  void* ddelta_raw;
+  void* dz;                 // null when z is null
+  float* dA;                // accumulated: zero before the launch
+  float* dB;                // accumulated
+  float* dC;                // accumulated
+  float* dD;                // accumulated; may be null
+  float* dbias;             // accumulated; may be null
+  float* dh0;               // may be null
+  float* ckpt;              // workspace: states saved every few steps
+  int64_t batch, seqlen, dim;
+  int ncblk;                // 32-channel blocks per batch element
+  int64_t nsub;             // recomputed sub-tiles per block
+};
+
 // Launch plan for a scan problem.
 struct ScanPlan {
   int sg;               // threads per channel (1 or 2); each owns 16/sg states
@@ -115,6 +144,10 @@ cudaError_t launch_conv1d_fwd(const ConvParams& p, ss_dtype in_dtype, ss_dtype o
                               cudaStream_t stream);
 cudaError_t launch_conv1d_update(const ConvParams& p, ss_dtype in_dtype, ss_dtype out_dtype, bool vec,
                                  cudaStream_t stream);
+
+cudaError_t launch_scan_bwd(const BwdParams& p, ss_dtype in_dtype, ss_dtype dy_dtype, cudaStream_t stream);
+size_t scan_bwd_checkpoint_bytes(int64_t batch, int64_t seqlen, int64_t dim);
+int64_t scan_bwd_subtiles(int64_t seqlen);
 
 // The library's own fault word (device symbol), used when no workspace is given.
 unsigned int* device_fault_word();

@@ -21,6 +21,7 @@ BLOCK = 1 << 22
 # stream ids (one per drawn tensor)
 S_DT, S_ALOG, S_U, S_DRAW, S_Z, S_B, S_C, S_SYM, S_EMB = range(9)
 S_CX, S_CW, S_CB, S_CS = range(9, 13)  # convolution front-end: input, weights, bias, state
+S_DY, S_DH = range(13, 15)  # backward pass: gradients of y and of h_last
 
 
 def _block_seed(seed: int, stream: int, block: int) -> int:
@@ -164,3 +165,20 @@ def random_conv_inputs(batch, seqlen, dim, width, in_dtype="bf16", seed=0, with_
                               in_dtype).contiguous()
     return out
 
+
+
+def random_output_grads(batch, seqlen, dim, dstate, dy_dtype="f32", seed=0, with_dh_last=True, channels=None,
+                        threads: int = 0):
+    """Gradients arriving at the scan's outputs, for the backward pass: dy
+    [batch, seqlen, dim] in dy_dtype and dh_last [batch, dim, dstate] float32
+    (None unless with_dh_last), standard normal. `channels`, a list of channel
+    indices, keeps only those channels nonzero (the rest exactly 0)."""
+    dy = randn_blocks(batch * seqlen * dim, seed, S_DY, threads).view(batch, seqlen, dim)
+    dh = randn_blocks(batch * dim * dstate, seed, S_DH, threads).view(batch, dim, dstate) if with_dh_last else None
+    if channels is not None:
+        keep = torch.zeros(dim, dtype=torch.bool)
+        keep[torch.as_tensor(channels, dtype=torch.long)] = True
+        dy = dy * keep.to(dy.dtype)
+        if dh is not None:
+            dh = dh * keep.to(dh.dtype)[:, None]
+    return _store(dy, dy_dtype).contiguous(), (dh.contiguous() if dh is not None else None)
