@@ -65,6 +65,16 @@ ss_status check_device() {
 }
 
 bool valid_dtype(int t) { return t == SS_F32 || t == SS_BF16; }
+
+// Lanes per channel of the backward kernel. Two lanes per channel double the
+// warps (one per 16 channels), which spreads the work more evenly over the
+// SM sub-partitions and gives each of them more than one warp to switch
+// between; one lane per channel needs fewer instructions per state and wins
+// once there are several warps per sub-partition anyway.
+int bwd_lanes_per_channel(int64_t batch, int64_t dim) {
+  if (g_tune_sg == 1 || g_tune_sg == 2) return g_tune_sg;
+  return batch * ((dim + 31) / 32) >= 3 * (int64_t)kSchedulers ? 1 : 2;
+}
 size_t dsize(ss_dtype t) { return t == SS_BF16 ? 2 : 4; }
 
 }  // namespace
@@ -370,7 +380,8 @@ ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width, ss_dtype i
 
 size_t ss_scan_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
   if (batch <= 0 || seqlen <= 0 || dim <= 0 || dstate != ssk::kDState) return 0;
-  return ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim);
+  return std::max(ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim, 1),
+                  ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim, 2));
 }
 
 ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
@@ -402,7 +413,8 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
                              "du", "ddelta_raw", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0", "workspace"};
   for (int i = 0; i < 21; i++)
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
-  const size_t need_ws = seqlen > 0 ? ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim) : 0;
+  const int sg = bwd_lanes_per_channel(batch, dim);
+  const size_t need_ws = seqlen > 0 ? ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim, sg) : 0;
   if (need_ws > 0 && (!workspace || workspace_bytes < need_ws))
     return fail(SS_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu%s)", need_ws, workspace_bytes,
                 workspace ? "" : ", NULL");
@@ -448,10 +460,10 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   p.batch = batch;
   p.seqlen = seqlen;
   p.dim = dim;
-  p.ncblk = (int)((dim + 31) / 32);
+  p.ncblk = (int)((dim + 32 / sg - 1) / (32 / sg));
   p.nsub = ssk::scan_bwd_subtiles(seqlen);
   if ((double)batch * p.ncblk > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
-  e = ssk::launch_scan_bwd(p, in_dtype, dy_dtype, s);
+  e = ssk::launch_scan_bwd(p, sg, in_dtype, dy_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "scan backward launch");
   return SS_OK;
 }

@@ -105,7 +105,7 @@ struct BwdParams {
   float* dh0;               // may be null
   float* ckpt;              // workspace: states saved every few steps
   int64_t batch, seqlen, dim;
-  int ncblk;                // 32-channel blocks per batch element
+  int ncblk;                // channel blocks (32 / sg channels) per batch element
   int64_t nsub;             // recomputed sub-tiles per block
 };
 
@@ -145,8 +145,9 @@ cudaError_t launch_conv1d_fwd(const ConvParams& p, ss_dtype in_dtype, ss_dtype o
 cudaError_t launch_conv1d_update(const ConvParams& p, ss_dtype in_dtype, ss_dtype out_dtype, bool vec,
                                  cudaStream_t stream);
 
-cudaError_t launch_scan_bwd(const BwdParams& p, ss_dtype in_dtype, ss_dtype dy_dtype, cudaStream_t stream);
-size_t scan_bwd_checkpoint_bytes(int64_t batch, int64_t seqlen, int64_t dim);
+// sg: lanes per channel (1 or 2); p.ncblk counts blocks of 32 / sg channels
+cudaError_t launch_scan_bwd(const BwdParams& p, int sg, ss_dtype in_dtype, ss_dtype dy_dtype, cudaStream_t stream);
+size_t scan_bwd_checkpoint_bytes(int64_t batch, int64_t seqlen, int64_t dim, int sg);
 int64_t scan_bwd_subtiles(int64_t seqlen);
 
 // The library's own fault word (device symbol), used when no workspace is given.

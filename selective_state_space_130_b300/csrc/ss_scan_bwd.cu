@@ -29,157 +29,325 @@ namespace {
 
 constexpr int kSub = 16;  // timesteps per recomputed sub-tile
 
-struct BwdSmem {
-  float4 hist[kSub + 1][4][32];  // [0]: the state before the sub-tile; [tt+1]: h_t0+tt; [.][state quad][lane]
-  float4 sc[kSub][32];       // per token and lane: (delta, u, dyv, delta_raw + bias)
-  float bc[kSub][2 * kDState];  // B then C rows of the sub-tile
-};
-
-constexpr float kLn2 = 0.6931471805599453f;
-
 __device__ __forceinline__ float sigmoidf_fast(float x) { return rcp(1.f + ex2(-x * kLog2e)); }
 
-template <typename T>
-__device__ __forceinline__ float ld_elem(const void* p, int64_t i) {
-  return to_f32(static_cast<const T*>(p)[i]);
+// Shared memory of one warp: the recomputed states of a sub-tile and two
+// staging buffers of raw inputs (one being read, one being filled). SG lanes
+// share a channel, each holding NS = 16 / SG of its states; a warp covers
+// CW = 32 / SG channels.
+template <typename TIn, typename TDy, int SG>
+struct BwdLayout {
+  static constexpr int CW = 32 / SG;
+  static constexpr int NS = kDState / SG;
+  static constexpr int NQ = NS / 4;  // 16-byte entries per lane per saved state
+  static constexpr int IN_ROW = CW * (int)sizeof(TIn);  // one step of u, delta_raw or z
+  static constexpr int DY_ROW = CW * (int)sizeof(TDy);
+  static constexpr int BC_ROW = kDState * (int)sizeof(TIn);  // one step of B (or C)
+  static constexpr int OFF_U = 0;
+  static constexpr int OFF_DR = OFF_U + kSub * IN_ROW;
+  static constexpr int OFF_Z = OFF_DR + kSub * IN_ROW;
+  static constexpr int OFF_DY = OFF_Z + kSub * IN_ROW;
+  static constexpr int OFF_B = OFF_DY + kSub * DY_ROW;
+  static constexpr int OFF_C = OFF_B + kSub * BC_ROW;
+  static constexpr int STAGE = OFF_C + kSub * BC_ROW;
+  static constexpr int HIST = (kSub + 1) * NQ * 32 * 16;  // one 16-byte entry per (slot, quad, lane)
+  static constexpr int SMEM = HIST + 2 * STAGE;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+// NS consecutive elements as float (this lane's part of a B or C row in shared
+// memory; 16-byte aligned)
+template <typename T, int NS>
+__device__ __forceinline__ void row_part(const uint8_t* p, float (&o)[NS]) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int q = 0; q < NS / 4; q++) {
+      const float4 v = reinterpret_cast<const float4*>(p)[q];
+      o[4 * q] = v.x;
+      o[4 * q + 1] = v.y;
+      o[4 * q + 2] = v.z;
+      o[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < NS / 8; q++) {
+      const uint4 v = reinterpret_cast<const uint4*>(p)[q];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        o[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
+        o[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      }
+    }
+  }
 }
 
-template <typename TIn, typename TDy, bool HAS_Z>
+template <typename T>
+__device__ __forceinline__ float sm_elem(const uint8_t* row, int i) {
+  return to_f32(reinterpret_cast<const T*>(row)[i]);
+}
+
+// Copy kSub rows of `rowb` bytes (rows `stride` elements apart, starting at
+// element `e0` of `base`) into shared memory at `dst`. Rows at or past
+// `nrows` and elements at or past `nelem` within a row are filled with zeros.
+// VEC: 16-byte asynchronous copies (every 16-byte piece lies wholly inside or
+// wholly outside the valid range); otherwise element-wise loads and stores.
+template <typename T, int ROWB, bool VEC>
+__device__ __forceinline__ void stage_rows(uint8_t* dst, const void* base, int64_t e0, int64_t stride, int nrows,
+                                           int nelem, int lane) {
+  constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte piece
+  constexpr int CPR = ROWB / 16;            // pieces per row
+  if constexpr (VEC) {
+    const uint32_t d0 = (uint32_t)__cvta_generic_to_shared(dst);
+#pragma unroll
+    for (int c = lane; c < kSub * CPR; c += 32) {
+      const int tt = c / CPR, k = c % CPR;
+      const bool ok = tt < nrows && k * EPC < nelem;
+      const T* src = static_cast<const T*>(base) + (ok ? e0 + tt * stride + k * EPC : 0);
+      cp_async16(d0 + tt * ROWB + k * 16, src, ok ? 16u : 0u);
+    }
+  } else {
+    constexpr int EPR = ROWB / (int)sizeof(T);  // elements per row
+#pragma unroll 4
+    for (int c = lane; c < kSub * EPR; c += 32) {
+      const int tt = c / EPR, k = c % EPR;
+      const bool ok = tt < nrows && k < nelem;
+      reinterpret_cast<T*>(dst)[c] = ok ? static_cast<const T*>(base)[e0 + tt * stride + k] : from_f32<T>(0.f);
+    }
+  }
+}
+
+// lo/hi of f2 pairs as a flat list of floats
+template <int NP>
+__device__ __forceinline__ void unpack(const f2 (&x)[NP], float* o) {
+#pragma unroll
+  for (int j = 0; j < NP; j++) {
+    o[2 * j] = f2lo(x[j]);
+    o[2 * j + 1] = f2hi(x[j]);
+  }
+}
+
+// Abar for a pair of states: 2^(delta * A2)
+__device__ __forceinline__ f2 abar2(f2 dl2, f2 a2) {
+  const f2 e = mul2(dl2, a2);
+  return pk(ex2(f2lo(e)), ex2(f2hi(e)));
+}
+
+template <typename TIn, typename TDy, int SG, bool HAS_Z, bool VEC>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using LY = BwdLayout<TIn, TDy, SG>;
+  constexpr int CW = LY::CW, NS = LY::NS, NQ = LY::NQ, NP = NS / 2;
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  BwdSmem& S = *reinterpret_cast<BwdSmem*>(smem_raw);
+  ulonglong2* hist = reinterpret_cast<ulonglong2*>(smem_raw);  // [slot][quad][lane], two f2 per entry
+  uint8_t* stage_buf = smem_raw + LY::HIST;
   const int lane = threadIdx.x;
+  const int ch = lane / SG;           // channel within the block
+  const int soff = (lane % SG) * NS;  // first state of this lane
+  const bool owner = (lane % SG) == 0;
   const int64_t blk = blockIdx.x;
   const int64_t b = blk / p.ncblk;
-  const int64_t d = (blk % p.ncblk) * 32 + lane;
+  const int64_t c0 = (blk % p.ncblk) * CW;
+  const int64_t d = c0 + ch;
   const bool dv = d < p.dim;
   const int64_t dc = dv ? d : 0;
   const int64_t L = p.seqlen, Dm = p.dim;
+  const int nch = (int)min((int64_t)CW, Dm - c0);
 
-  // A2 = A log2(e), so that Abar = 2^(delta A2); sums over A2 are scaled back by ln 2
-  float A2[kDState], h[kDState], lam[kDState], dAacc[kDState];
+  // State pairs (states soff + 2j, soff + 2j + 1) in packed f32x2 registers.
+  // A2 = A log2(e), so that Abar = 2^(delta A2); sums over A2 are scaled back by ln 2.
+  f2 A2[NP], h[NP], lam[NP], dAacc[NP];
+  {
+    const int64_t hrow = (b * Dm + dc) * kDState + soff;
 #pragma unroll
-  for (int n = 0; n < kDState; n++) {
-    A2[n] = dv ? __ldg(p.A + dc * kDState + n) * kLog2e : 0.f;
-    h[n] = (dv && p.h0) ? __ldg(p.h0 + (b * Dm + dc) * kDState + n) : 0.f;
-    lam[n] = (dv && p.dh_last) ? __ldg(p.dh_last + (b * Dm + dc) * kDState + n) : 0.f;
-    dAacc[n] = 0.f;
+    for (int j = 0; j < NP; j++) {
+      const float a0 = dv ? __ldg(p.A + dc * kDState + soff + 2 * j) : 0.f;
+      const float a1 = dv ? __ldg(p.A + dc * kDState + soff + 2 * j + 1) : 0.f;
+      A2[j] = pk(a0 * kLog2e, a1 * kLog2e);
+      h[j] = (dv && p.h0) ? pk(__ldg(p.h0 + hrow + 2 * j), __ldg(p.h0 + hrow + 2 * j + 1)) : pk(0.f, 0.f);
+      lam[j] = (dv && p.dh_last) ? pk(__ldg(p.dh_last + hrow + 2 * j), __ldg(p.dh_last + hrow + 2 * j + 1))
+                                 : pk(0.f, 0.f);
+      dAacc[j] = pk(0.f, 0.f);
+    }
   }
   const float bias_d = (dv && p.delta_bias) ? __ldg(p.delta_bias + dc) : 0.f;
   const float D_d = (dv && p.D) ? __ldg(p.D + dc) : 0.f;
   float dDacc = 0.f, dbacc = 0.f;
-  float4* ck = reinterpret_cast<float4*>(p.ckpt) + (size_t)blk * p.nsub * 4 * 32;
+  ulonglong2* ck = reinterpret_cast<ulonglong2*>(p.ckpt) + (size_t)blk * p.nsub * NQ * 32;
 
-  // ---- phase 1: the recurrence forward, its state saved every kSub steps
-  for (int64_t t = 0; t < L; t++) {
-    if (t % kSub == 0) {
-      float4* dst = ck + (size_t)(t / kSub) * 4 * 32;
-#pragma unroll
-      for (int q = 0; q < 4; q++) dst[q * 32 + lane] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+  // stage sub-tile s into buffer s & 1: phase 1 needs u, delta_raw, B; phase 2 everything
+  auto stage = [&](int64_t s, bool all) {
+    uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
+    const int64_t t0 = s * kSub;
+    const int nr = (int)min((int64_t)kSub, L - t0);
+    const int64_t e0 = (b * L + t0) * Dm + c0;
+    stage_rows<TIn, LY::IN_ROW, VEC>(buf + LY::OFF_U, p.u, e0, Dm, nr, nch, lane);
+    stage_rows<TIn, LY::IN_ROW, VEC>(buf + LY::OFF_DR, p.delta_raw, e0, Dm, nr, nch, lane);
+    stage_rows<TIn, LY::BC_ROW, VEC>(buf + LY::OFF_B, p.B, (b * L + t0) * kDState, kDState, nr, kDState, lane);
+    if (all) {
+      if constexpr (HAS_Z) stage_rows<TIn, LY::IN_ROW, VEC>(buf + LY::OFF_Z, p.z, e0, Dm, nr, nch, lane);
+      stage_rows<TDy, LY::DY_ROW, VEC>(buf + LY::OFF_DY, p.dy, e0, Dm, nr, nch, lane);
+      stage_rows<TIn, LY::BC_ROW, VEC>(buf + LY::OFF_C, p.C, (b * L + t0) * kDState, kDState, nr, kDState, lane);
     }
-    const int64_t i = (b * L + t) * Dm + dc;
-    const float xu = dv ? ld_elem<TIn>(p.u, i) : 0.f;
-    const float dl = softplus(ld_elem<TIn>(p.delta_raw, i) + bias_d);
-    const float du = dl * xu;
-    // B row of step t: lane n < 16 loads element n, the warp reads it by shuffle
-    const float bl = ld_elem<TIn>(p.B, (b * L + t) * kDState + (lane & (kDState - 1)));
+    cp_async_commit();
+  };
+  // sum over the SG lanes of a channel
+  auto chan_sum = [&](float x) {
+    if constexpr (SG == 2) x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
+  };
+  // this lane's B or C pairs of step tt of a staged buffer
+  auto row_pairs = [&](const uint8_t* buf, int off, int tt, f2 (&o)[NP]) {
+    float f[NS];
+    row_part<TIn, NS>(buf + off + tt * LY::BC_ROW + soff * (int)sizeof(TIn), f);
 #pragma unroll
-    for (int n = 0; n < kDState; n++) h[n] = fmaf(ex2(dl * A2[n]), h[n], du * __shfl_sync(0xffffffffu, bl, n));
+    for (int j = 0; j < NP; j++) o[j] = pk(f[2 * j], f[2 * j + 1]);
+  };
+
+  // ---- phase 1: the recurrence forward, its state saved at the start of every sub-tile
+  stage(0, false);
+  for (int64_t s = 0; s < p.nsub; s++) {
+    if (s + 1 < p.nsub) stage(s + 1, false);
+    else cp_async_commit();
+    cp_async_wait1();
+    __syncwarp();
+    {
+      ulonglong2* dst = ck + (size_t)s * NQ * 32;
+#pragma unroll
+      for (int q = 0; q < NQ; q++) dst[q * 32 + lane] = make_ulonglong2(h[2 * q], h[2 * q + 1]);
+    }
+    const uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
+    const int ns = (int)min((int64_t)kSub, L - s * kSub);
+    for (int tt = 0; tt < ns; tt++) {
+      const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
+      const float dl = softplus_fast(sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, ch) + bias_d);
+      const f2 dl2 = pk(dl, dl), du2 = pk(dl * xu, dl * xu);
+      f2 Bv[NP];
+      row_pairs(buf, LY::OFF_B, tt, Bv);
+#pragma unroll
+      for (int j = 0; j < NP; j++) h[j] = fma2(abar2(dl2, A2[j]), h[j], mul2(du2, Bv[j]));
+    }
+    __syncwarp();  // buffer s & 1 is refilled next iteration
   }
 
   // ---- phase 2: the sub-tiles in reverse order
+  stage(p.nsub - 1, true);
+  ulonglong2 ck_next[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; q++) ck_next[q] = ck[(size_t)(p.nsub - 1) * NQ * 32 + q * 32 + lane];
   for (int64_t s = p.nsub - 1; s >= 0; s--) {
     const int64_t t0 = s * kSub;
     const int ns = (int)min((int64_t)kSub, L - t0);
-    __syncwarp();  // the previous sub-tile's reads of shared memory are done
-    {
-      const float4* src = ck + (size_t)s * 4 * 32;
+    f2 hh[NP];
 #pragma unroll
-      for (int q = 0; q < 4; q++) S.hist[0][q][lane] = src[q * 32 + lane];
+    for (int q = 0; q < NQ; q++) {
+      hist[q * 32 + lane] = ck_next[q];
+      hh[2 * q] = ck_next[q].x;
+      hh[2 * q + 1] = ck_next[q].y;
     }
-    // B and C rows of the sub-tile (lane r holds element r of the B|C row)
-    for (int tt = 0; tt < ns; tt++) {
-      const int64_t r = (b * L + t0 + tt) * kDState;
-      S.bc[tt][lane] = lane < kDState ? ld_elem<TIn>(p.B, r + lane) : ld_elem<TIn>(p.C, r + lane - kDState);
+    if (s > 0) {
+      stage(s - 1, true);
+#pragma unroll
+      for (int q = 0; q < NQ; q++) ck_next[q] = ck[(size_t)(s - 1) * NQ * 32 + q * 32 + lane];
+    } else {
+      cp_async_commit();
     }
+    cp_async_wait1();
     __syncwarp();
-    // recompute the sub-tile's states; dz and the per-step scalars
-    float hh[kDState];
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-      const float4 v = S.hist[0][q][lane];
-      hh[4 * q] = v.x;
-      hh[4 * q + 1] = v.y;
-      hh[4 * q + 2] = v.z;
-      hh[4 * q + 3] = v.w;
-    }
+    const uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
+    // recompute the sub-tile's states into shared memory (lane-private slots); dz
     for (int tt = 0; tt < ns; tt++) {
       const int64_t i = (b * L + t0 + tt) * Dm + dc;
-      const float xu = dv ? ld_elem<TIn>(p.u, i) : 0.f;
-      const float xr = ld_elem<TIn>(p.delta_raw, i) + bias_d;
-      const float dl = softplus(xr);
-      const float du = dl * xu;
-      float yv = D_d * xu;
+      const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
+      const float dl = softplus_fast(sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, ch) + bias_d);
+      const f2 dl2 = pk(dl, dl), du2 = pk(dl * xu, dl * xu);
+      f2 Bv[NP], Cv[NP];
+      row_pairs(buf, LY::OFF_B, tt, Bv);
+      row_pairs(buf, LY::OFF_C, tt, Cv);
+      f2 y0 = pk(0.f, 0.f), y1 = pk(0.f, 0.f);
 #pragma unroll
-      for (int n = 0; n < kDState; n++) {
-        hh[n] = fmaf(ex2(dl * A2[n]), hh[n], du * S.bc[tt][n]);
-        yv = fmaf(S.bc[tt][kDState + n], hh[n], yv);
+      for (int j = 0; j < NP; j++) {
+        hh[j] = fma2(abar2(dl2, A2[j]), hh[j], mul2(du2, Bv[j]));
+        if (j & 1) y1 = fma2(Cv[j], hh[j], y1);
+        else y0 = fma2(Cv[j], hh[j], y0);
       }
+      ulonglong2* hs = hist + (tt + 1) * NQ * 32 + lane;
 #pragma unroll
-      for (int q = 0; q < 4; q++)
-        S.hist[tt + 1][q][lane] = make_float4(hh[4 * q], hh[4 * q + 1], hh[4 * q + 2], hh[4 * q + 3]);
-      const float dyt = dv ? ld_elem<TDy>(p.dy, i) : 0.f;
-      float dyv = dyt;
+      for (int q = 0; q < NQ; q++) hs[q * 32] = make_ulonglong2(hh[2 * q], hh[2 * q + 1]);
       if constexpr (HAS_Z) {
-        const float zz = ld_elem<TIn>(p.z, i);
+        const f2 ys = add2(y0, y1);
+        const float yv = fmaf(D_d, xu, chan_sum(f2lo(ys) + f2hi(ys)));
+        const float dyt = sm_elem<TDy>(buf + LY::OFF_DY + tt * LY::DY_ROW, ch);
+        const float zz = sm_elem<TIn>(buf + LY::OFF_Z + tt * LY::IN_ROW, ch);
         const float sg = sigmoidf_fast(zz);
-        dyv = dyt * zz * sg;
-        if (dv) static_cast<TIn*>(p.dz)[i] = from_f32<TIn>(dyt * yv * sg * fmaf(zz, 1.f - sg, 1.f));
+        if (dv && owner) static_cast<TIn*>(p.dz)[i] = from_f32<TIn>(dyt * yv * sg * fmaf(zz, 1.f - sg, 1.f));
       }
-      S.sc[tt][lane] = make_float4(dl, xu, dyv, xr);
     }
-    __syncwarp();
     // the adjoint backwards through the sub-tile
     for (int tt = ns - 1; tt >= 0; tt--) {
       const int64_t t = t0 + tt;
-      const float4 sv = S.sc[tt][lane];
-      const float dl = sv.x, xu = sv.y, dyv = sv.z, xr = sv.w;
-      const float dlu = dl * xu;
-      float v[2 * kDState];  // this channel's terms of dB (0..15) and dC (16..31)
-      float dub = 0.f, dda = 0.f;
+      const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
+      const float xr = sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, ch) + bias_d;
+      const float dl = softplus_fast(xr);
+      float dyv = sm_elem<TDy>(buf + LY::OFF_DY + tt * LY::DY_ROW, ch);
+      if constexpr (HAS_Z) dyv *= silu(sm_elem<TIn>(buf + LY::OFF_Z + tt * LY::IN_ROW, ch));
+      const f2 dl2 = pk(dl, dl), dyv2 = pk(dyv, dyv), dlu2 = pk(dl * xu, dl * xu);
+      f2 Bv[NP], Cv[NP];
+      row_pairs(buf, LY::OFF_B, tt, Bv);
+      row_pairs(buf, LY::OFF_C, tt, Cv);
+      f2 vB[NP], vC[NP];  // this lane's terms of dB and dC for its states
+      f2 dub0 = pk(0.f, 0.f), dub1 = pk(0.f, 0.f), dda0 = pk(0.f, 0.f), dda1 = pk(0.f, 0.f);
+      const ulonglong2* hc = hist + (tt + 1) * NQ * 32 + lane;
+      const ulonglong2* hq = hist + tt * NQ * 32 + lane;
 #pragma unroll
-      for (int q = 0; q < 4; q++) {
-        const float4 hc = S.hist[tt + 1][q][lane];
-        const float4 hq = S.hist[tt][q][lane];
-        const float ht[4] = {hc.x, hc.y, hc.z, hc.w};
-        const float hp[4] = {hq.x, hq.y, hq.z, hq.w};
+      for (int q = 0; q < NQ; q++) {
+        const ulonglong2 c4 = hc[q * 32];
+        const ulonglong2 p4 = hq[q * 32];
+        const f2 ht[2] = {c4.x, c4.y};
+        const f2 hp[2] = {p4.x, p4.y};
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const int n = 4 * q + k;
-          const float a = ex2(dl * A2[n]);
-          lam[n] = fmaf(S.bc[tt][kDState + n], dyv, lam[n]);
-          v[kDState + n] = dyv * ht[k];
-          v[n] = lam[n] * dlu;
-          dub = fmaf(lam[n], S.bc[tt][n], dub);
-          const float lpa = lam[n] * (hp[k] * a);
-          dda = fmaf(lpa, A2[n], dda);
-          dAacc[n] = fmaf(lpa, dl, dAacc[n]);
-          lam[n] *= a;
+        for (int k = 0; k < 2; k++) {
+          const int j = 2 * q + k;
+          const f2 a = abar2(dl2, A2[j]);
+          lam[j] = fma2(Cv[j], dyv2, lam[j]);
+          vC[j] = mul2(dyv2, ht[k]);
+          vB[j] = mul2(lam[j], dlu2);
+          const f2 lpa = mul2(lam[j], mul2(hp[k], a));
+          if (k) {
+            dub1 = fma2(lam[j], Bv[j], dub1);
+            dda1 = fma2(lpa, A2[j], dda1);
+          } else {
+            dub0 = fma2(lam[j], Bv[j], dub0);
+            dda0 = fma2(lpa, A2[j], dda0);
+          }
+          dAacc[j] = fma2(lpa, dl2, dAacc[j]);
+          lam[j] = mul2(lam[j], a);
         }
       }
+      const f2 dubs = add2(dub0, dub1), ddas = add2(dda0, dda1);
+      const float dub = chan_sum(f2lo(dubs) + f2hi(dubs));
+      const float dda = chan_sum(f2lo(ddas) + f2hi(ddas));
       // dL/d delta = sum_n lambda (h_prev Abar A + B u) = ln2 * dda + u * dub
       const float ddel = fmaf(kLn2, dda, xu * dub);
       const float dxr = ddel * sigmoidf_fast(xr);
       dbacc += dxr;
       dDacc = fmaf(dyv, xu, dDacc);
       const int64_t i = (b * L + t) * Dm + dc;
-      if (dv) {
+      if (dv && owner) {
         static_cast<TIn*>(p.du)[i] = from_f32<TIn>(fmaf(dyv, D_d, dl * dub));
         static_cast<TIn*>(p.ddelta_raw)[i] = from_f32<TIn>(dxr);
       }
-      // sum over the 32 lanes; after the five stages lane l holds element l
+      // sum over the warp's channels (lanes with the same lane % SG); after
+      // the stages lane l holds element (l / SG) of its v = [dB terms, dC terms]
+      float v[2 * NS];
+      unpack<NP>(vB, v);
+      unpack<NP>(vC, v + NS);
 #pragma unroll
-      for (int m = 16, w = 16; m >= 1; m >>= 1, w >>= 1) {
+      for (int m = 16, w = NS; m >= SG; m >>= 1, w >>= 1) {
         const bool up = (lane & m) != 0;
 #pragma unroll
         for (int e = 0; e < w; e++) {
@@ -188,56 +356,71 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const __grid_constant__ Bw
           v[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
         }
       }
-      float* dst = lane < kDState ? p.dB + (b * L + t) * kDState + lane : p.dC + (b * L + t) * kDState + (lane - kDState);
-      atomicAdd(dst, v[0]);
+      const int e = ch;  // 0 .. 2NS-1
+      float* row = (e < NS ? p.dB : p.dC) + (b * L + t) * kDState + soff;
+      atomicAdd(row + (e < NS ? e : e - NS), v[0]);
     }
+    __syncwarp();  // buffer s & 1 is refilled next iteration
   }
 
   if (dv) {
+    float lf[NS], af[NS];
+    unpack<NP>(lam, lf);
+    unpack<NP>(dAacc, af);
     if (p.dh0) {
 #pragma unroll
-      for (int n = 0; n < kDState; n++) p.dh0[(b * Dm + d) * kDState + n] = lam[n];
+      for (int j = 0; j < NS; j++) p.dh0[(b * Dm + d) * kDState + soff + j] = lf[j];
     }
 #pragma unroll
-    for (int n = 0; n < kDState; n++) atomicAdd(p.dA + d * kDState + n, dAacc[n]);
-    if (p.dD) atomicAdd(p.dD + d, dDacc);
-    if (p.dbias) atomicAdd(p.dbias + d, dbacc);
+    for (int j = 0; j < NS; j++) atomicAdd(p.dA + d * kDState + soff + j, af[j]);
+    if (owner) {
+      if (p.dD) atomicAdd(p.dD + d, dDacc);
+      if (p.dbias) atomicAdd(p.dbias + d, dbacc);
+    }
   }
 }
 
-template <typename TIn, typename TDy>
-cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
-  const int smem = (int)sizeof(BwdSmem);
+template <typename TIn, typename TDy, int SG, bool HAS_Z, bool VEC>
+cudaError_t launch_bwd_k(const BwdParams& p, cudaStream_t s) {
+  const int smem = BwdLayout<TIn, TDy, SG>::SMEM;
   const int64_t nblk = p.batch * (int64_t)p.ncblk;
-  if (p.z) {
-    auto k = scan_bwd_kernel<TIn, TDy, true>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    k<<<(unsigned)nblk, 32, smem, s>>>(p);
-  } else {
-    auto k = scan_bwd_kernel<TIn, TDy, false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    k<<<(unsigned)nblk, 32, smem, s>>>(p);
-  }
+  auto k = scan_bwd_kernel<TIn, TDy, SG, HAS_Z, VEC>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k<<<(unsigned)nblk, 32, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+template <typename TIn, typename TDy, int SG>
+cudaError_t launch_bwd_sg(const BwdParams& p, cudaStream_t s) {
+  // 16-byte copies need every staged row to start on a 16-byte boundary
+  const bool vec = (p.dim * (int64_t)sizeof(TIn)) % 16 == 0 && (p.dim * (int64_t)sizeof(TDy)) % 16 == 0;
+  if (p.z) return vec ? launch_bwd_k<TIn, TDy, SG, true, true>(p, s) : launch_bwd_k<TIn, TDy, SG, true, false>(p, s);
+  return vec ? launch_bwd_k<TIn, TDy, SG, false, true>(p, s) : launch_bwd_k<TIn, TDy, SG, false, false>(p, s);
+}
+
+template <typename TIn, typename TDy>
+cudaError_t launch_bwd_t(const BwdParams& p, int sg, cudaStream_t s) {
+  return sg == 2 ? launch_bwd_sg<TIn, TDy, 2>(p, s) : launch_bwd_sg<TIn, TDy, 1>(p, s);
 }
 
 }  // namespace
 
-size_t scan_bwd_checkpoint_bytes(int64_t batch, int64_t seqlen, int64_t dim) {
-  const int64_t nblk = batch * ((dim + 31) / 32);
+size_t scan_bwd_checkpoint_bytes(int64_t batch, int64_t seqlen, int64_t dim, int sg) {
+  const int64_t cw = 32 / sg;
+  const int64_t nblk = batch * ((dim + cw - 1) / cw);
   const int64_t nsub = (seqlen + kSub - 1) / kSub;
-  return (size_t)nblk * (size_t)nsub * 32 * kDState * sizeof(float);
+  return (size_t)nblk * (size_t)nsub * 32 * (kDState / sg) * sizeof(float);
 }
 
 int64_t scan_bwd_subtiles(int64_t seqlen) { return (seqlen + kSub - 1) / kSub; }
 
-cudaError_t launch_scan_bwd(const BwdParams& p, ss_dtype in_dtype, ss_dtype dy_dtype, cudaStream_t stream) {
+cudaError_t launch_scan_bwd(const BwdParams& p, int sg, ss_dtype in_dtype, ss_dtype dy_dtype, cudaStream_t stream) {
   if (in_dtype == SS_BF16)
-    return dy_dtype == SS_BF16 ? launch_bwd_t<__nv_bfloat16, __nv_bfloat16>(p, stream)
-                               : launch_bwd_t<__nv_bfloat16, float>(p, stream);
-  return dy_dtype == SS_BF16 ? launch_bwd_t<float, __nv_bfloat16>(p, stream) : launch_bwd_t<float, float>(p, stream);
+    return dy_dtype == SS_BF16 ? launch_bwd_t<__nv_bfloat16, __nv_bfloat16>(p, sg, stream)
+                               : launch_bwd_t<__nv_bfloat16, float>(p, sg, stream);
+  return dy_dtype == SS_BF16 ? launch_bwd_t<float, __nv_bfloat16>(p, sg, stream)
+                             : launch_bwd_t<float, float>(p, sg, stream);
 }
 
 }  // namespace ssk

@@ -89,54 +89,6 @@ struct Cfg {
   static constexpr int BLOCKS_PER_SM = kSmemPerSM / (SMEM + 1024);
 };
 
-// softplus(x) = log(1 + e^x), from w = e^x:
-//   x > 20    : x (the correction log1p(e^-x) < 2.1e-9 is below half an ulp of x)
-//   w < 1/16  : series w - w^2/2 + w^3/3 - w^4/4 + w^5/5 - w^6/6 (truncation < w^7/7)
-//   otherwise : ln2 * log2(1 + w); 1 + w >= 1.0625 keeps the MUFU log2's absolute
-//               error a small relative one
-__device__ __forceinline__ float softplus_fast(float x) {
-  const float w = ex2(x * kLog2e);
-  float p = fmaf(w, -1.f / 6.f, 0.2f);
-  p = fmaf(w, p, -0.25f);
-  p = fmaf(w, p, 1.f / 3.f);
-  p = fmaf(w, p, -0.5f);
-  p = fmaf(w, p, 1.f);
-  const float series = w * p;
-  float lg;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(1.f + w));
-  const float r = w < 0.0625f ? series : lg * kLn2;
-  return x > 20.f ? x : r;
-}
-
-// softplus_fast for two values at once: the polynomial, the scaling and the
-// additions run as packed f32x2 operations; the exponentials, logarithms and
-// selections stay per value. Same formula and constants as softplus_fast.
-__device__ __forceinline__ f2 softplus_fast2(f2 x) {
-  const f2 xl = mul2(x, pk(kLog2e, kLog2e));
-  const f2 w = pk(ex2(f2lo(xl)), ex2(f2hi(xl)));
-  f2 p = fma2(w, pk(-1.f / 6.f, -1.f / 6.f), pk(0.2f, 0.2f));
-  p = fma2(w, p, pk(-0.25f, -0.25f));
-  p = fma2(w, p, pk(1.f / 3.f, 1.f / 3.f));
-  p = fma2(w, p, pk(-0.5f, -0.5f));
-  p = fma2(w, p, pk(1.f, 1.f));
-  const f2 series = mul2(w, p);
-  const f2 w1 = add2(w, pk(1.f, 1.f));
-  float l0, l1;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l0) : "f"(f2lo(w1)));
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l1) : "f"(f2hi(w1)));
-  const f2 lg = mul2(pk(l0, l1), pk(kLn2, kLn2));
-  const float r0 = f2lo(w) < 0.0625f ? f2lo(series) : f2lo(lg);
-  const float r1 = f2hi(w) < 0.0625f ? f2hi(series) : f2hi(lg);
-  return pk(f2lo(x) > 20.f ? f2lo(x) : r0, f2hi(x) > 20.f ? f2hi(x) : r1);
-}
-
-// silu for two values: z / (1 + e^-z), the scalings and additions packed
-__device__ __forceinline__ f2 silu2(f2 z) {
-  const f2 e = mul2(z, pk(-kLog2e, -kLog2e));
-  const f2 d = add2(pk(ex2(f2lo(e)), ex2(f2hi(e))), pk(1.f, 1.f));
-  return mul2(z, pk(rcp(f2lo(d)), rcp(f2hi(d))));
-}
-
 template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, int MODE>
 __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_constant__ ScanParams p,
                                                                   const __grid_constant__ CUtensorMap tm_u,

@@ -21,11 +21,15 @@ PER_CHANNEL = ("du", "ddelta_raw", "dz")
 SUMMED = ("dA", "dB", "dC", "dD", "ddelta_bias", "dh0")
 
 
-def _run_bwd(x, dy, dh_last):
+def _run_bwd(x, dy, dh_last, sg=0):
     d = to_dev(x)
-    g = ss.ss_scan_bwd(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], dy.cuda(), d.get("D"), d.get("z"),
-                       d.get("delta_bias"), d.get("h0"), dh_last.cuda() if dh_last is not None else None)
-    torch.cuda.synchronize()
+    ss.ss_scan_set_tuning(sg, 0, 0)
+    try:
+        g = ss.ss_scan_bwd(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], dy.cuda(), d.get("D"), d.get("z"),
+                           d.get("delta_bias"), d.get("h0"), dh_last.cuda() if dh_last is not None else None)
+        torch.cuda.synchronize()
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
     return g
 
 
@@ -56,7 +60,8 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}-dy{s[1]}-b{s[2]}-L{s[3]}-D{s[4]}" for s in SHAPES])
-def test_scan_bwd_matches_oracle(shape):
+@pytest.mark.parametrize("sg", [1, 2])
+def test_scan_bwd_matches_oracle(shape, sg):
     dt, dyt, Bt, L, Dm, h0, hz, hd, hb, hdh = shape
     in_dt = BF16 if dt == "bf16" else F32
     x = gen.random_scan_inputs(Bt, L, Dm, 16, in_dtype=dt, seed=L + Dm, with_h0=h0, has_z=hz, has_d=hd,
@@ -65,8 +70,8 @@ def test_scan_bwd_matches_oracle(shape):
         x["delta_bias"] = None
     dy, dh = gen.random_output_grads(Bt, L, Dm, 16, dyt, seed=L * 3 + Dm, with_dh_last=hdh)
     ref = oracle.scan_bwd(x, dy, dh)
-    g = _run_bwd(x, dy, dh)
-    _compare(g, ref, in_dt, hz, f"bwd {shape}")
+    g = _run_bwd(x, dy, dh, sg)
+    _compare(g, ref, in_dt, hz, f"bwd {shape} sg={sg}")
 
 
 def test_scan_bwd_mid_size_every_output():
@@ -74,8 +79,9 @@ def test_scan_bwd_mid_size_every_output():
     x = gen.random_scan_inputs(2, 512, 1024, 16, in_dtype="bf16", seed=21, with_h0=True, a_log_jitter=0.3)
     dy, dh = gen.random_output_grads(2, 512, 1024, 16, "bf16", seed=22)
     ref = oracle.scan_bwd(x, dy, dh)
-    g = _run_bwd(x, dy, dh)
-    _compare(g, ref, BF16, True, "bwd mid")
+    for sg in (1, 2):
+        g = _run_bwd(x, dy, dh, sg)
+        _compare(g, ref, BF16, True, f"bwd mid sg={sg}")
 
 
 def _slice_channels(x, S):
@@ -102,13 +108,14 @@ def layer():
     return x, S
 
 
-def test_scan_bwd_layer_sampled_channels(layer):
+@pytest.mark.parametrize("sg", [1, 2])
+def test_scan_bwd_layer_sampled_channels(layer, sg):
     # Mamba-2.8B layer (4 x 2048 x 5120, bf16): dense output gradients; the
     # per-channel gradients of sampled channels depend on those channels alone
     x, S = layer
     Bt, L, Dm = x["u"].shape
     dy, dh = gen.random_output_grads(Bt, L, Dm, 16, "bf16", seed=5)
-    g = _run_bwd(x, dy, dh)
+    g = _run_bwd(x, dy, dh, sg)
     idx = torch.as_tensor(S, dtype=torch.long)
     ref = oracle.scan_bwd(_slice_channels(x, S), dy[:, :, idx].contiguous(), dh[:, idx].contiguous())
     for k in PER_CHANNEL:
@@ -119,14 +126,15 @@ def test_scan_bwd_layer_sampled_channels(layer):
     assert_close(_np(g["dh0"][:, idx.cuda()]), ref["dh0"], BF16, what="layer dh0")
 
 
-def test_scan_bwd_layer_channel_sums(layer):
+@pytest.mark.parametrize("sg", [1, 2])
+def test_scan_bwd_layer_channel_sums(layer, sg):
     # output gradients zero outside S: every other channel's adjoint is exactly
     # zero, so dB and dC are the sums over S, which the oracle computes on the
     # channel slice; the kernel still runs over all 5120 channels
     x, S = layer
     Bt, L, Dm = x["u"].shape
     dy, dh = gen.random_output_grads(Bt, L, Dm, 16, "bf16", seed=6, channels=S)
-    g = _run_bwd(x, dy, dh)
+    g = _run_bwd(x, dy, dh, sg)
     idx = torch.as_tensor(S, dtype=torch.long)
     ref = oracle.scan_bwd(_slice_channels(x, S), dy[:, :, idx].contiguous(), dh[:, idx].contiguous())
     assert_close(_np(g["dB"]), ref["dB"], BF16, what="layer dB")
@@ -143,10 +151,11 @@ def test_scan_bwd_layer_channel_sums(layer):
 def test_scan_bwd_per_channel_outputs_deterministic():
     x = gen.random_scan_inputs(2, 200, 96, 16, in_dtype="bf16", seed=4, with_h0=True)
     dy, dh = gen.random_output_grads(2, 200, 96, 16, "bf16", seed=4)
-    g1 = _run_bwd(x, dy, dh)
-    g2 = _run_bwd(x, dy, dh)
-    for k in ("du", "ddelta_raw", "dz", "dh0"):
-        assert torch.equal(g1[k], g2[k]), k
+    for sg in (1, 2):
+        g1 = _run_bwd(x, dy, dh, sg)
+        g2 = _run_bwd(x, dy, dh, sg)
+        for k in ("du", "ddelta_raw", "dz", "dh0"):
+            assert torch.equal(g1[k], g2[k]), (k, sg)
 
 
 def test_scan_bwd_sequence_split_chains():
@@ -205,7 +214,7 @@ def test_scan_bwd_empty_and_errors():
     dz = torch.empty(2, 3, 16, device="cuda")
     st = L.ss_scan_bwd(*args, outs["du"].data_ptr(), outs["ddelta_raw"].data_ptr(), dz.data_ptr(),
                        outs["dA"].data_ptr(), outs["dB"].data_ptr(), outs["dC"].data_ptr(), None, None, None,
-                       ws.data_ptr(), ws.numel() - 16, None)
+                       ws.data_ptr(), 64, None)
     assert st == ss._lib.SS_ERR_INVALID_ARG and "workspace" in ss.ss_last_error()
     # dstate other than 16
     args_n8 = list(args)
