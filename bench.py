@@ -377,6 +377,64 @@ def bench_conv1d(ss, dev, hbm_peak, Bt=4, L=2048, Dm=5120, K=4, reps=20):
             "decode_update_workload": f"{S} streams x {Dm} channels, width {K}, 200 steps in one CUDA graph"}
 
 
+# Compute roof of the backward pass per (t, d, n): recomputing the state and
+# the readout C.h (4 fp32 lane-ops and one ex2), the adjoint update and its
+# products (lambda += C dyv; lambda *= Abar; the dB and dC terms; the du, d delta
+# and dA sums: 9 lane-ops), and the channel sums of the dB and dC terms (2 adds):
+# 15 fp32 lane-ops, so at most 128 / 15 state updates per clock per SM.
+BWD_UPDATES_PER_CLK_SM = 128.0 / 15.0
+
+
+def bench_scan_bwd(ss, w, dev, hbm_peak, clock_mhz, reps=10):
+    """Gradients of the scan (ss_scan_bwd) on the Mamba-2.8B layer shape: bf16
+    inputs and output gradient, fp32 dh_last. One input set of 420 MB (larger
+    than L2)."""
+    x = to_dev(gen.make_scan_inputs(w), dev)
+    Bt, L, Dm, N = w.batch, w.seqlen, w.dim, w.dstate
+    dy, dh = gen.random_output_grads(Bt, L, Dm, N, "bf16", seed=5)
+    dy, dh = dy.to(dev), dh.to(dev)
+    ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bt, L, Dm, N), dtype=torch.uint8, device=dev)
+
+    def call(out=None):
+        return ss.ss_scan_bwd(x["u"], x["delta_raw"], x["A"], x["B"], x["C"], dy, x["D"], x["z"], x["delta_bias"],
+                              None, dh, out=out, workspace=ws)
+
+    out = call()  # allocates the gradients once
+    for _ in range(3):
+        call(out)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record()
+        call(out)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(per)
+    # algorithmic bytes: read u, delta_raw, z, dy and write du, ddelta_raw, dz
+    # (bf16, 14 B per channel-token); read B, C (bf16) and write dB, dC (fp32)
+    # per token; dh_last in, dh0 out (fp32); A, D, bias in and their gradients out
+    nbytes = (Bt * L * Dm * 14 + Bt * L * N * (2 * 2 + 2 * 4) + 2 * Bt * Dm * N * 4 + 2 * Dm * (N + 2) * 4)
+    updates = Bt * L * Dm * N
+    alu_peak = BWD_UPDATES_PER_CLK_SM * SMS * clock_mhz * 1e6
+    achieved = updates / (ms * 1e-3)
+    del x, dy, dh, ws, out
+    torch.cuda.empty_cache()
+    return {"workload": f"gradients of the scan, {w.name}: batch {Bt}, L {L}, d_inner {Dm}, d_state {N}, "
+                        "bf16 inputs / dy / du, ddelta_raw, dz; fp32 dA, dB, dC, dD, dbias, dh0",
+            "ms_per_launch": round(ms, 4), "ms_per_launch_median": round(statistics.median(per), 4),
+            "ms_per_launch_min": round(min(per), 4), "launches_per_call": 1,
+            "channel_tokens_per_s": Bt * L * Dm / (ms * 1e-3),
+            "roofline": {"bound": "alu", "unit": "state updates/s", "achieved": achieved, "peak": alu_peak,
+                         "frac": round(achieved / alu_peak, 4),
+                         "basis": "15 fp32 lane-ops per (t,d,n) (state and readout recompute 4, adjoint 9, "
+                                  "channel sums of the dB/dC terms 2): 128 lanes / 15 per clk per SM x 148 SMs "
+                                  "x median SM clock of the main run"},
+            "hbm": {"algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                    "frac_of_hbm_peak": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 4)},
+            "l2": "one input set of 420 MB (larger than L2)"}
+
+
 def cpu_baseline_scan(w, x, target_s=12.0):
     """The float64 oracle as it stands, on the host cores, over channels of the
     same workload; scaled to algorithmic GB/s of the sample."""
@@ -493,6 +551,7 @@ def run_ours(args, world, rank, local):
             del stc, xc
             torch.cuda.empty_cache()
         extra["conv1d_front_end"] = bench_conv1d(ss, dev, hbm_peak)
+        extra["scan_backward"] = bench_scan_bwd(ss, w, dev, hbm_peak, clock_mhz)
         result["per_config"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_scan(w, x)
@@ -536,7 +595,7 @@ def run_reference(args, world, rank):
 
 
 def profile_launches(args):
-    """Two launches of the scan (or decode) kernel on the chosen workload, no
+    """Two launches of the scan (decode, backward) kernel on the chosen workload, no
     timing: the target of `ncu -k regex:... -s 1 -c 1`."""
     import selective_state_space_130_b300 as ss
 
@@ -552,6 +611,17 @@ def profile_launches(args):
         for _ in range(2):
             scan_call(ss, x, y, h, ws)
         ss.ss_scan_status(ws)
+    elif args.profile == "bwd":
+        w = configs.get_config(args.workload)
+        x = to_dev(gen.make_scan_inputs(w), dev)
+        Bt, L, Dm = w.batch, w.seqlen, w.dim
+        dy, dh = gen.random_output_grads(Bt, L, Dm, 16, "bf16", seed=5)
+        dy, dh = dy.to(dev), dh.to(dev)
+        ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bt, L, Dm), dtype=torch.uint8, device=dev)
+        out = None
+        for _ in range(2):
+            out = ss.ss_scan_bwd(x["u"], x["delta_raw"], x["A"], x["B"], x["C"], dy, x["D"], x["z"],
+                                 x["delta_bias"], None, dh, out=out, workspace=ws)
     else:
         w = configs.C4
         A, Dk, bias = (t.to(dev) for t in gen.make_params(w.prefix))
@@ -573,7 +643,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the c1 / c3 scan timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "decode"], default=None,
+    ap.add_argument("--profile", choices=["scan", "decode", "bwd"], default=None,
                     help="run 2 launches of one kernel (for an ncu capture of the 2nd) and exit")
     args = ap.parse_args()
     if args.profile:

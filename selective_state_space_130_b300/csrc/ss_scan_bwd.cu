@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const __grid_constant__ Bw
     }
     const uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
     const int ns = (int)min((int64_t)kSub, L - s * kSub);
+#pragma unroll 2
     for (int tt = 0; tt < ns; tt++) {
       const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
       const float dl = softplus_fast(sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, ch) + bias_d);
@@ -260,6 +261,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const __grid_constant__ Bw
     __syncwarp();
     const uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
     // recompute the sub-tile's states into shared memory (lane-private slots); dz
+#pragma unroll 2
     for (int tt = 0; tt < ns; tt++) {
       const int64_t i = (b * L + t0 + tt) * Dm + dc;
       const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
@@ -284,10 +286,11 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const __grid_constant__ Bw
         const float dyt = sm_elem<TDy>(buf + LY::OFF_DY + tt * LY::DY_ROW, ch);
         const float zz = sm_elem<TIn>(buf + LY::OFF_Z + tt * LY::IN_ROW, ch);
         const float sg = sigmoidf_fast(zz);
-        if (dv && owner) static_cast<TIn*>(p.dz)[i] = from_f32<TIn>(dyt * yv * sg * fmaf(zz, 1.f - sg, 1.f));
+        st_out(static_cast<TIn*>(p.dz) + i, dyt * yv * sg * fmaf(zz, 1.f - sg, 1.f), dv && owner);
       }
     }
     // the adjoint backwards through the sub-tile
+#pragma unroll 2
     for (int tt = ns - 1; tt >= 0; tt--) {
       const int64_t t = t0 + tt;
       const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
@@ -337,10 +340,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const __grid_constant__ Bw
       dbacc += dxr;
       dDacc = fmaf(dyv, xu, dDacc);
       const int64_t i = (b * L + t) * Dm + dc;
-      if (dv && owner) {
-        static_cast<TIn*>(p.du)[i] = from_f32<TIn>(fmaf(dyv, D_d, dl * dub));
-        static_cast<TIn*>(p.ddelta_raw)[i] = from_f32<TIn>(dxr);
-      }
+      st_out(static_cast<TIn*>(p.du) + i, fmaf(dyv, D_d, dl * dub), dv && owner);
+      st_out(static_cast<TIn*>(p.ddelta_raw) + i, dxr, dv && owner);
       // sum over the warp's channels (lanes with the same lane % SG); after
       // the stages lane l holds element (l / SG) of its v = [dB terms, dC terms]
       float v[2 * NS];
