@@ -15,7 +15,10 @@ directly and by FFT, delta->0, large delta, chunk associativity, geometric
 closed form, hand-computed L=1, zero/linearity/independence properties,
 decode-equals-scan; for the gradients: central finite differences of the
 forward oracle; for the convolution front-end: numpy's convolution,
-impulse responses, chunk continuity through the state, decode-equals-forward).
+impulse responses, chunk continuity through the state, decode-equals-forward;
+for the generalised scan: scipy's zero-order-hold discretisation and
+simulation, the scan on its special case, per-group slices, a split of the
+states).
 """
 
 import ctypes
@@ -48,6 +51,9 @@ def load(path: str = None) -> ctypes.CDLL:
                                                _P, _I64, _P]
         lib.ss_oracle_scan_bwd.restype = ctypes.c_int
         lib.ss_oracle_scan_bwd.argtypes = [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int] + [_P] * 20
+        lib.ss_oracle_scan_general.restype = ctypes.c_int
+        lib.ss_oracle_scan_general.argtypes = [_I64, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                               _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, ctypes.c_int]
         lib.ss_oracle_conv1d.restype = ctypes.c_int
         lib.ss_oracle_conv1d.argtypes = [_I64, _I64, _I64, _I64, ctypes.c_int, _P, _P, _P, _P,
                                          ctypes.c_int, _P, _P]
@@ -124,6 +130,48 @@ def scan(x: dict, channels=None, nthreads: int = None, lib_path: str = None):
                             nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle scan rejected its arguments")
+    if full:
+        return y.reshape(Bt, Dm, L).transpose(0, 2, 1).copy(), h.reshape(Bt, Dm, N)
+    return y, h
+
+
+DISC = {"euler": 0, "zoh": 1}
+
+
+def scan_general(x: dict, ngroups: int = 1, disc: str = "euler", channels=None, nthreads: int = None,
+                 lib_path: str = None):
+    """Generalised selective scan in float64: state size N = A.shape[1], B and C
+    [Bt, L, G, N] (or [Bt, L, N] when G = 1) shared by the dim / G consecutive
+    channels of each group, Bbar first order ("euler") or zero-order hold
+    ("zoh"). Other inputs and the return value as for scan()."""
+    lib = load(lib_path)
+    u, dr, z, B, C = x["u"], x["delta_raw"], x.get("z"), x["B"], x["C"]
+    Bt, L, Dm = u.shape
+    A = _f32(x["A"])
+    N = A.shape[1]
+    code = _dtype_code(u)
+    for t in (dr, z, B, C):
+        if t is not None and _dtype_code(t) != code:
+            raise TypeError("u, delta_raw, z, B, C must share one dtype")
+    if B.dim() == 3:
+        B, C = B.unsqueeze(2), C.unsqueeze(2)
+    assert B.shape == (Bt, L, ngroups, N) and C.shape == (Bt, L, ngroups, N), (B.shape, ngroups, N)
+    B, C = B.contiguous(), C.contiguous()
+    full = channels is None
+    if full:
+        bb, dd = np.meshgrid(np.arange(Bt), np.arange(Dm), indexing="ij")
+        chans = np.stack([bb.ravel(), dd.ravel()], axis=1).astype(np.int64)
+    else:
+        chans = np.ascontiguousarray(np.asarray(channels, dtype=np.int64).reshape(-1, 2))
+    n = chans.shape[0]
+    y = np.zeros((n, L), dtype=np.float64)
+    h = np.zeros((n, N), dtype=np.float64)
+    rc = lib.ss_oracle_scan_general(Bt, L, Dm, N, ngroups, DISC[disc], code, _ptr(u), _ptr(dr), _ptr(z), _ptr(B),
+                                    _ptr(C), _ptr(A), _ptr(_f32(x.get("D"))), _ptr(_f32(x.get("delta_bias"))),
+                                    _ptr(_f32(x.get("h0"))), chans.ctypes.data, n, y.ctypes.data, h.ctypes.data,
+                                    nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle scan_general rejected its arguments")
     if full:
         return y.reshape(Bt, Dm, L).transpose(0, 2, 1).copy(), h.reshape(Bt, Dm, N)
     return y, h

@@ -43,7 +43,10 @@
  * depthwise convolution front-end and
  * its decode step (ss_oracle_conv1d, ss_oracle_conv1d_update, at the end),
  * pinned against numpy's convolution, impulse responses, chunk continuity and
- * decode-equals-forward.
+ * decode-equals-forward; and the generalised scan (ss_oracle_scan_general: any
+ * state size, grouped B and C, zero-order-hold Bbar), pinned against scipy's
+ * zero-order-hold discretisation and simulation of the same linear system, the
+ * scan above on its special case, per-group slices and a split of the states.
  */
 #include <math.h>
 #include <pthread.h>
@@ -374,5 +377,116 @@ int ss_oracle_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstat
   free(hist);
   free(lam);
   free(delta);
+  return 0;
+}
+
+/*
+ * Generalised selective scan: any state size N, B and C shared within G groups
+ * of channels, and the zero-order-hold input matrix as an alternative to the
+ * first-order one.
+ *
+ *  - state size: the pages' tutorial lets the state dimension N grow (16 in the
+ *    paper's language models, larger for other modalities; mlqm.cn tutorial,
+ *    section 3.1); nothing in the recurrence depends on N;
+ *  - zero-order hold: the exact discretisation of h' = A h + B x for an input
+ *    held constant over a step of length delta gives
+ *      Abar = exp(delta A),  Bbar = (exp(delta A) - 1) / A * B
+ *    for diagonal A ("外文文献精读" page, section 1.2; tutorial section 3.2),
+ *    which tends to delta B as delta A -> 0 (the first-order form the scan
+ *    above uses);
+ *  - groups: B and C are produced per token for G groups of dim / G consecutive
+ *    channels each; channel d reads group d / (dim / G) (G = 1: shared by all
+ *    channels, G = dim: one B and C per channel). The pages give one shared
+ *    B and C; grouping is the plainest generalisation of that sharing.
+ *
+ * B, C: [batch][seqlen][G][N]; A: [dim][N]; everything else as ss_oracle_scan.
+ * disc: 0 = first order (Bbar = delta B), 1 = zero-order hold. For A[d,n] = 0
+ * the zero-order hold Bbar is delta B (its limit).
+ * Writes y[c][t] and h_last[c][n] for listed channel c. Returns 0, or -1 on a
+ * bad argument (including dim not divisible by G).
+ */
+typedef struct {
+  int64_t batch, seqlen, dim, dstate, ngroups;
+  int disc, in_dtype;
+  const void *u, *delta_raw, *z, *B, *C;
+  const float *A, *Dskip, *bias, *h0;
+  const int64_t *chans;
+  int64_t n_chan;
+  double *y, *h_last;
+  int64_t next;
+  pthread_mutex_t mu;
+} gscan_job;
+
+static void gscan_one(const gscan_job *j, int64_t c) {
+  const int64_t L = j->seqlen, Dm = j->dim, N = j->dstate, G = j->ngroups;
+  const int64_t b = j->chans[2 * c], d = j->chans[2 * c + 1];
+  const int64_t g = d / (Dm / G);
+  double *h = (double *)malloc(sizeof(double) * (size_t)N);
+  for (int64_t n = 0; n < N; n++) h[n] = j->h0 ? (double)j->h0[(b * Dm + d) * N + n] : 0.0;
+  const double bias = j->bias ? (double)j->bias[d] : 0.0;
+  const double dsk = j->Dskip ? (double)j->Dskip[d] : 0.0;
+  for (int64_t t = 0; t < L; t++) {
+    const int64_t i = (b * L + t) * Dm + d;        /* [b][t][d] */
+    const int64_t r = ((b * L + t) * G + g) * N;   /* [b][t][g][n] row */
+    const double delta = softplus(widen(j->delta_raw, j->in_dtype, i) + bias);
+    const double x = widen(j->u, j->in_dtype, i);
+    double y = 0.0;
+    for (int64_t n = 0; n < N; n++) {
+      const double a = (double)j->A[d * N + n];
+      const double abar = exp(delta * a);
+      /* the factor that multiplies B: delta (first order) or expm1(delta a) / a */
+      const double bfac = (j->disc == 1 && a != 0.0) ? expm1(delta * a) / a : delta;
+      h[n] = abar * h[n] + bfac * widen(j->B, j->in_dtype, r + n) * x;
+      y += widen(j->C, j->in_dtype, r + n) * h[n];
+    }
+    y += dsk * x;
+    if (j->z) y *= silu(widen(j->z, j->in_dtype, i));
+    j->y[c * L + t] = y;
+  }
+  for (int64_t n = 0; n < N; n++) j->h_last[c * N + n] = h[n];
+  free(h);
+}
+
+static void *gscan_worker(void *arg) {
+  gscan_job *j = (gscan_job *)arg;
+  for (;;) {
+    pthread_mutex_lock(&j->mu);
+    int64_t c = j->next++;
+    pthread_mutex_unlock(&j->mu);
+    if (c >= j->n_chan) break;
+    gscan_one(j, c);
+  }
+  return NULL;
+}
+
+int ss_oracle_scan_general(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t ngroups,
+                           int disc, int in_dtype, const void *u, const void *delta_raw, const void *z,
+                           const void *B, const void *C, const float *A, const float *Dskip, const float *bias,
+                           const float *h0, const int64_t *chans, int64_t n_chan, double *y, double *h_last,
+                           int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0 || n_chan < 0 || ngroups <= 0) return -1;
+  if (dim % ngroups != 0 || (disc != 0 && disc != 1)) return -1;
+  if (in_dtype != ORC_F32 && in_dtype != ORC_BF16) return -1;
+  if (!u || !delta_raw || !B || !C || !A || !chans || !y || !h_last) return -1;
+  for (int64_t c = 0; c < n_chan; c++)
+    if (chans[2 * c] < 0 || chans[2 * c] >= batch || chans[2 * c + 1] < 0 || chans[2 * c + 1] >= dim)
+      return -1;
+  gscan_job j;
+  memset(&j, 0, sizeof j);
+  j.batch = batch; j.seqlen = seqlen; j.dim = dim; j.dstate = dstate; j.ngroups = ngroups;
+  j.disc = disc; j.in_dtype = in_dtype;
+  j.u = u; j.delta_raw = delta_raw; j.z = z; j.B = B; j.C = C;
+  j.A = A; j.Dskip = Dskip; j.bias = bias; j.h0 = h0;
+  j.chans = chans; j.n_chan = n_chan; j.y = y; j.h_last = h_last; j.next = 0;
+  pthread_mutex_init(&j.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int started = 0;
+  for (int k = 1; k < nthreads; k++)
+    if (pthread_create(&th[started], NULL, gscan_worker, &j) == 0) started++;
+  gscan_worker(&j);
+  for (int k = 0; k < started; k++) pthread_join(th[k], NULL);
+  pthread_mutex_destroy(&j.mu);
   return 0;
 }

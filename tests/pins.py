@@ -20,7 +20,12 @@ Independent restatements used here (none calls the oracle's arithmetic):
   equals the unsplit scan exactly up to rounding ("Transformer时代终结？"
   section 二.3 "无近似"; "外文文献精读" section 2.2 block combination);
 - closed forms (geometric series), a hand-evaluated single step, exact zeros,
-  linearity in u, channel/batch independence, decode x L = scan.
+  linearity in u, channel/batch independence, decode x L = scan;
+- generalised scan: scipy's zero-order-hold discretisation (cont2discrete) and
+  simulation (dlsim) of the same linear system, the exact discretisation of
+  h' = A h + B x for a step-wise constant input ("外文文献精读" section 1.2;
+  mlqm.cn tutorial section 3.2); the brute-force sum on the first-order case at
+  any state size; per-group channel slices.
 """
 
 import math
@@ -30,7 +35,7 @@ import torch
 from scipy.special import expit
 
 import oracle
-from workloads.gen import random_scan_inputs
+from workloads.gen import random_general_inputs, random_scan_inputs
 
 
 # ----------------------------------------------------------------- helpers
@@ -88,7 +93,7 @@ def _close(a, b, rtol, atol=0.0, what=""):
 
 
 def _f32(a):
-    return torch.tensor(np.asarray(a, dtype=np.float32))
+    return torch.tensor(np.ascontiguousarray(a, dtype=np.float32))
 
 
 # -------------------------------------------------------------------- pins
@@ -475,7 +480,105 @@ def pin_backward_bf16_widening(lib=None):
         np.testing.assert_allclose(g1[k], g2[k], rtol=0, atol=0)
 
 
-ALL_PINS = [pin_backward_finite_differences, pin_backward_bf16_widening, pin_conv_numpy, pin_conv_impulse, pin_conv_chunk_continuity, pin_conv_decode_equals_forward,
+# ------------------------------------------------- generalised scan (any N, groups, ZOH)
+
+def _slice_group(x, g, G):
+    """Channels of group g with that group's B and C as a shared (G = 1) problem."""
+    Dm = x["u"].shape[2]
+    lo, hi = g * (Dm // G), (g + 1) * (Dm // G)
+    out = {}
+    for k in ("u", "delta_raw", "z"):
+        out[k] = x[k][:, :, lo:hi].contiguous() if x.get(k) is not None else None
+    out["B"] = x["B"][:, :, g, :].contiguous()
+    out["C"] = x["C"][:, :, g, :].contiguous()
+    out["A"] = x["A"][lo:hi].contiguous()
+    for k in ("D", "delta_bias"):
+        out[k] = x[k][lo:hi].contiguous() if x.get(k) is not None else None
+    out["h0"] = x["h0"][:, lo:hi].contiguous() if x.get("h0") is not None else None
+    return out, lo, hi
+
+
+def pin_general_zoh_scipy(lib=None):
+    # LTI problem (delta, B, C constant over time): the zero-order-hold scan is
+    # the discrete system scipy builds from (A, B, C, D) and the step delta
+    from scipy.signal import cont2discrete, dlsim
+    rng = np.random.default_rng(31)
+    for N in (3, 64):
+        Bt, L, Dm = 1, 40, 3
+        dr_c = rng.normal(size=Dm)
+        Bc, Cc = rng.normal(size=N), rng.normal(size=N)
+        x = {"u": _f32(rng.normal(size=(Bt, L, Dm))),
+             "delta_raw": _f32(np.broadcast_to(dr_c, (Bt, L, Dm))),
+             "z": None,
+             "B": _f32(np.broadcast_to(Bc, (Bt, L, 1, N))), "C": _f32(np.broadcast_to(Cc, (Bt, L, 1, N))),
+             "A": _f32(-np.exp(rng.normal(size=(Dm, N)) * 0.7)),
+             "D": _f32(rng.normal(size=Dm)), "delta_bias": _f32(rng.normal(size=Dm) * 0.3),
+             "h0": _f32(rng.normal(size=(Bt, Dm, N)))}
+        y, h = oracle.scan_general(x, 1, "zoh", lib_path=lib)
+        u, A, Dk, h0 = _np(x["u"]), _np(x["A"]), _np(x["D"]), _np(x["h0"])
+        Bv, Cv = _np(x["B"])[0, 0, 0], _np(x["C"])[0, 0, 0]
+        for d in range(Dm):
+            delta = float(_softplus_ref(_np(x["delta_raw"])[0, 0, d] + _np(x["delta_bias"])[d]))
+            Ad, Bd, Cd, Dd, _ = cont2discrete((np.diag(A[d]), Bv[:, None], Cv[None, :], np.array([[Dk[d]]])),
+                                              delta, method="zoh")
+            # dlsim's state before input k; this scan's state after input t is dlsim's x[t + 1]
+            _, _, xs = dlsim((Ad, Bd, Cd, Dd, delta), np.append(u[0, :, d], 0.0), x0=h0[0, d])
+            ref = xs[1:] @ Cv + Dk[d] * u[0, :, d]
+            _close(y[0, :, d], ref, 1e-9, 1e-11, f"zoh scipy y N={N}")
+            _close(h[0, d], xs[L], 1e-9, 1e-11, f"zoh scipy h_last N={N}")
+
+
+def pin_general_first_order_brute_force(lib=None):
+    # the first-order generalised scan at state sizes 16 and 64 is the brute-force sum
+    for N, seed, dtype in ((16, 41, "f32"), (64, 42, "bf16")):
+        x = random_general_inputs(2, 11, 3, N, 1, in_dtype=dtype, seed=seed, with_h0=True, a_log_jitter=0.3)
+        y, h = oracle.scan_general(x, 1, "euler", lib_path=lib)
+        xb = dict(x, B=x["B"][:, :, 0, :], C=x["C"][:, :, 0, :])
+        yb, hb = brute_force(xb)
+        _close(y, yb, 1e-11, 1e-13, f"general euler y N={N}")
+        _close(h, hb, 1e-11, 1e-13, f"general euler h_last N={N}")
+
+
+def pin_general_groups(lib=None):
+    # G groups: each group's channels give what a shared-B/C problem of that
+    # group's channels and rows gives; first order checked against brute force
+    G = 4
+    x = random_general_inputs(2, 13, 8, 32, G, in_dtype="f32", seed=43, with_h0=True, a_log_jitter=0.3)
+    for disc in ("euler", "zoh"):
+        y, h = oracle.scan_general(x, G, disc, lib_path=lib)
+        for g in range(G):
+            xs, lo, hi = _slice_group(x, g, G)
+            ys, hs = oracle.scan_general(xs, 1, disc, lib_path=lib)
+            _close(y[:, :, lo:hi], ys, 0.0, 0.0, f"group {g} y {disc}")
+            _close(h[:, lo:hi], hs, 0.0, 0.0, f"group {g} h {disc}")
+            if disc == "euler":
+                yb, hb = brute_force(xs)
+                _close(ys, yb, 1e-11, 1e-13, f"group {g} brute force")
+    # one B/C per channel (G = dim)
+    x = random_general_inputs(1, 9, 6, 16, 6, in_dtype="f32", seed=44, with_h0=False)
+    y, _ = oracle.scan_general(x, 6, "euler", lib_path=lib)
+    for g in range(6):
+        xs, lo, hi = _slice_group(x, g, 6)
+        yb, _ = brute_force(xs)
+        _close(y[:, :, lo:hi], yb, 1e-11, 1e-13, f"per-channel B/C, channel {g}")
+
+
+def pin_general_zoh_small_step(lib=None):
+    # for delta*A -> 0 the zero-order hold tends to the first-order form: the
+    # difference of Bbar is delta B (e^{delta A} - 1 - delta A) / (delta A), of order delta^2 A B / 2
+    x = random_general_inputs(1, 20, 4, 16, 1, in_dtype="f32", seed=45, with_h0=False)
+    x["delta_raw"] = torch.full_like(x["delta_raw"], -12.0)
+    x["delta_bias"] = None
+    ye, _ = oracle.scan_general(x, 1, "euler", lib_path=lib)
+    yz, _ = oracle.scan_general(x, 1, "zoh", lib_path=lib)
+    delta = float(_softplus_ref(-12.0))
+    amax = float(np.abs(_np(x["A"])).max())
+    assert np.all(np.abs(yz - ye) <= 0.6 * delta * amax * np.abs(ye).max() + 1e-300), "zoh small step"
+    assert np.any(yz != ye), "zoh identical to first order"
+
+
+ALL_PINS = [pin_general_zoh_scipy, pin_general_first_order_brute_force, pin_general_groups,
+            pin_general_zoh_small_step, pin_backward_finite_differences, pin_backward_bf16_widening, pin_conv_numpy, pin_conv_impulse, pin_conv_chunk_continuity, pin_conv_decode_equals_forward,
             pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_large_delta_overwrites,
             pin_chunk_associativity, pin_geometric_series, pin_single_step_by_hand, pin_softplus_values,
             pin_zeros, pin_linearity_in_u, pin_independence, pin_decode_equals_scan,

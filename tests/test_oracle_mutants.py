@@ -42,6 +42,13 @@ MUTANTS = {
     "bwd_no_softplus_derivative": ("ddelta_raw[i] = ddel * sg;", "ddelta_raw[i] = ddel;"),
     "bwd_dh_last_ignored": ("lam[n] = dh_last ? (double)dh_last[(b * Dm + d) * N + n] : 0.0;", "lam[n] = 0.0;"),
     "bwd_gate_derivative_is_sigmoid": ("return s * (1.0 + z * (1.0 - s));", "return s;"),
+    # generalised scan
+    "gen_zoh_without_division_by_A": ("expm1(delta * a) / a : delta", "expm1(delta * a) : delta"),
+    "gen_zoh_exp_instead_of_expm1": ("expm1(delta * a) / a : delta", "exp(delta * a) / a : delta"),
+    "gen_zoh_ignored": ("(j->disc == 1 && a != 0.0)", "(j->disc == 7 && a != 0.0)"),
+    "gen_group_by_modulo": ("const int64_t g = d / (Dm / G);", "const int64_t g = d % G;"),
+    "gen_row_without_groups": ("const int64_t r = ((b * L + t) * G + g) * N;", "const int64_t r = ((b * L + t) + g) * N;"),
+    "gen_A_row_of_16": ("const double a = (double)j->A[d * N + n];", "const double a = (double)j->A[d * 16 + n % 16];"),
     # convolution front-end
     "conv_taps_reversed": ("pre += (double)w[d * width + k] * e[t + k];",
                            "pre += (double)w[d * width + (width - 1 - k)] * e[t + k];"),

@@ -182,3 +182,15 @@ def random_output_grads(batch, seqlen, dim, dstate, dy_dtype="f32", seed=0, with
         if dh is not None:
             dh = dh * keep.to(dh.dtype)[:, None]
     return _store(dy, dy_dtype).contiguous(), (dh.contiguous() if dh is not None else None)
+
+
+def random_general_inputs(batch, seqlen, dim, dstate, ngroups=1, in_dtype="f32", seed=0, with_h0=False,
+                          threads: int = 0, **kw):
+    """Inputs of the generalised scan: as random_scan_inputs (A_log = log(n+1)
+    for n < dstate), with B and C [batch, seqlen, ngroups, dstate] (standard
+    normal, the same streams as B and C of the shared case)."""
+    x = random_scan_inputs(batch, seqlen, dim, dstate, in_dtype=in_dtype, seed=seed, with_h0=with_h0, **kw)
+    n = batch * seqlen * ngroups * dstate
+    x["B"] = _store(randn_blocks(n, seed, S_B, threads).view(batch, seqlen, ngroups, dstate), in_dtype).contiguous()
+    x["C"] = _store(randn_blocks(n, seed, S_C, threads).view(batch, seqlen, ngroups, dstate), in_dtype).contiguous()
+    return x
