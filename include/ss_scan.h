@@ -222,6 +222,38 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Generalised selective scan forward: larger states, B and C shared within
+ * groups of channels, and a choice of the input matrix's discretisation.
+ *
+ *  - dstate: 16, 32, 64 or 128. The pages' tutorial lets the state size grow
+ *    beyond the 16 of the language models (mlqm.cn tutorial, section 3.1).
+ *  - ngroups G: B and C are [batch, seqlen, G, dstate]; channel d reads group
+ *    d / (dim / G). G = 1 is the pages' one B and C shared by all channels;
+ *    G = dim gives every channel its own. dim must be a multiple of G.
+ *  - disc: SS_DISC_FIRST_ORDER uses Bbar = delta B, as ss_scan_fwd.
+ *    SS_DISC_ZOH uses the zero-order hold, the exact discretisation of
+ *    h' = A h + B x for an input held over the step: Bbar = (exp(delta A) - 1)
+ *    / A * B, which is delta B where A = 0 ("外文文献精读：Mamba - 线性时间序列
+ *    建模与结构化状态空间模型", section 1.2; mlqm.cn tutorial, section 3.2).
+ *    Abar = exp(delta A) in both.
+ *
+ * Other arguments, layouts, dtypes and conventions are those of ss_scan_fwd
+ * with 16 replaced by dstate (A [dim, dstate]; h0, h_last [batch, dim,
+ * dstate]). No workspace: one warp runs each block of 32 / (dstate / 16)
+ * channels over the whole sequence. SS_ERR_UNSUPPORTED for another dstate or
+ * discretisation, or when the B and C rows of the groups one channel block
+ * spans do not fit in shared memory.
+ */
+typedef enum { SS_DISC_FIRST_ORDER = 0, SS_DISC_ZOH = 1 } ss_disc;
+
+ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t ngroups,
+                              ss_disc disc, ss_dtype in_dtype, ss_dtype out_dtype,
+                              const void *u, const void *delta_raw, const float *A,
+                              const void *B, const void *C, const float *D, const void *z,
+                              const float *delta_bias, const float *h0,
+                              void *y, float *h_last, void *stream);
+
+/*
  * Launch-shape controls for the calling host thread (0 = automatic, the
  * default, for each). threads_per_channel in {1, 2} sets how many threads share
  * one channel's 16 states. chunk_len > 0 forces the sequence to be split into

@@ -15,6 +15,8 @@ LIB_PATH = os.path.join(HERE, "libssscan.so")
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT = range(5)
 SS_F32, SS_BF16 = 0, 1
+SS_DISC_FIRST_ORDER, SS_DISC_ZOH = 0, 1
+DISC = {"first_order": SS_DISC_FIRST_ORDER, "euler": SS_DISC_FIRST_ORDER, "zoh": SS_DISC_ZOH}
 # bytes of the fixed scratch array behind ss_scan_fwd_noalloc (SS_SCAN_NOALLOC_SCRATCH_BYTES in the header)
 SS_SCAN_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_CUDA",
@@ -38,6 +40,8 @@ SIGNATURES = {
                                         _P, _P, _P, _P, ctypes.c_int, _P, _P]),
     "ss_scan_bwd_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
     "ss_scan_bwd": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int] + [_P] * 21 + [_SZ, _P]),
+    "ss_scan_fwd_general": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+                            + [_P] * 11 + [_P]),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
 }
@@ -187,6 +191,27 @@ def ss_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=N
                                                     "dh0")],
                              ws_ptr, ws_len, _stream(stream)))
     return o
+
+
+def ss_scan_fwd_general(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, h0=None, *, disc="first_order",
+                        out_dtype=None, y=None, h_last=None, return_h_last=True, stream=None):
+    """Generalised selective scan on device tensors: dstate = A.shape[1] (16, 32,
+    64 or 128); B, C [Bt, L, G, N] (or [Bt, L, N] for G = 1); disc
+    "first_order" (Bbar = delta B) or "zoh". Returns (y, h_last)."""
+    Bt, L, Dm = u.shape
+    N = A.shape[1]
+    G = 1 if B.dim() == 3 else B.shape[2]
+    code = _dt(u)
+    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    dev = u.device
+    if y is None:
+        y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=dev)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+    _check(lib().ss_scan_fwd_general(Bt, L, Dm, N, G, DISC[disc], code, out_code, _ptr(u), _ptr(delta_raw), _ptr(A),
+                                     _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y),
+                                     _ptr(h_last), _stream(stream)))
+    return y, h_last
 
 
 def ss_state_update(h, u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, *, out_dtype=None, y=None,

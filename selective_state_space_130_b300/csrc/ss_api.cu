@@ -468,6 +468,73 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   return SS_OK;
 }
 
+ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t ngroups,
+                              ss_disc disc, ss_dtype in_dtype, ss_dtype out_dtype, const void* u,
+                              const void* delta_raw, const float* A, const void* B, const void* C, const float* D,
+                              const void* z, const float* delta_bias, const float* h0, void* y, float* h_last,
+                              void* stream) {
+  g_err.clear();
+  if (dstate != 16 && dstate != 32 && dstate != 64 && dstate != 128)
+    return fail(SS_ERR_UNSUPPORTED, "dstate must be 16, 32, 64 or 128 (got %lld)", (long long)dstate);
+  if (disc != SS_DISC_FIRST_ORDER && disc != SS_DISC_ZOH)
+    return fail(SS_ERR_UNSUPPORTED, "unknown discretisation %d", (int)disc);
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, out %d)", (int)in_dtype, (int)out_dtype);
+  if (batch < 0 || seqlen < 0 || dim < 0 || ngroups < 1)
+    return fail(SS_ERR_INVALID_ARG, "negative size or ngroups < 1");
+  if (batch > INT32_MAX || seqlen > INT32_MAX || dim > INT32_MAX)
+    return fail(SS_ERR_INVALID_ARG, "a size exceeds 2^31-1");
+  if (dim > 0 && dim % ngroups != 0)
+    return fail(SS_ERR_INVALID_ARG, "dim (%lld) is not a multiple of ngroups (%lld)", (long long)dim,
+                (long long)ngroups);
+  if (batch == 0 || dim == 0) return SS_OK;
+  if ((double)batch * (double)seqlen * (double)dim * (double)dstate > 4.0e18)
+    return fail(SS_ERR_INVALID_ARG, "problem too large");
+  const void* need[] = {u, delta_raw, A, B, C, y};
+  const char* names[] = {"u", "delta_raw", "A", "B", "C", "y"};
+  if (seqlen > 0) {
+    for (int i = 0; i < 6; i++)
+      if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
+  }
+  const void* all[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, h_last};
+  const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last"};
+  for (int i = 0; i < 11; i++)
+    if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  const int sg = (int)(dstate / 16);
+  const int64_t cw = 32 / sg;
+  const int64_t ncblk = (dim + cw - 1) / cw;
+  const int64_t cpg = dim / ngroups;
+  int ngw_max = 1;
+  for (int64_t k = 0; k < ncblk; k++) {
+    const int64_t c0 = k * cw, c1 = std::min(c0 + cw, dim) - 1;
+    ngw_max = std::max(ngw_max, (int)(c1 / cpg - c0 / cpg + 1));
+  }
+  const int smem = 2 * ssk::scan_general_stage_bytes(dstate, ngw_max, in_dtype);
+  if (smem > 227 * 1024)
+    return fail(SS_ERR_UNSUPPORTED, "staging of %d groups per warp needs %d bytes of shared memory", ngw_max, smem);
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (seqlen == 0) {
+    if (!h_last) return SS_OK;
+    const size_t hbytes = (size_t)batch * dim * dstate * sizeof(float);
+    cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, hbytes, cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(h_last, 0, hbytes, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
+  }
+  const size_t es = dsize(in_dtype);
+  const size_t in_row = (size_t)cw * es;
+  int chunk = 0;
+  if (((size_t)dim * es) % 16 == 0 && in_row % 16 == 0) chunk = 16;
+  else if (((size_t)dim * es) % 4 == 0 && in_row % 4 == 0) chunk = 4;
+  ssk::GenParams p{u, delta_raw, z, B, C, A, D, delta_bias, h0, y, h_last, batch, seqlen, dim, ngroups, cpg,
+                   (int)ncblk, ngw_max, chunk, (int)disc};
+  if ((double)batch * ncblk > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
+  cudaError_t e = ssk::launch_scan_general(p, sg, in_dtype, out_dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "generalised scan launch");
+  return SS_OK;
+}
+
 ss_status ss_scan_status(void* workspace, void* stream) {
   g_err.clear();
   cudaStream_t s = static_cast<cudaStream_t>(stream);

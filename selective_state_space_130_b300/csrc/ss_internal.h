@@ -109,6 +109,27 @@ struct BwdParams {
   int64_t nsub;             // recomputed sub-tiles per block
 };
 
+// Parameters of the generalised scan (state size 16-128, grouped B/C, ZOH).
+struct GenParams {
+  const void* u;
+  const void* delta_raw;
+  const void* z;            // may be null
+  const void* B;            // [batch, seqlen, ngroups, dstate]
+  const void* C;
+  const float* A;           // [dim, dstate]
+  const float* D;           // may be null
+  const float* delta_bias;  // may be null
+  const float* h0;          // may be null
+  void* y;
+  float* h_last;            // may be null
+  int64_t batch, seqlen, dim, ngroups;
+  int64_t cpg;              // channels per group (dim / ngroups)
+  int ncblk;                // channel blocks (32 / sg channels) per batch element
+  int ngw_max;              // most groups one channel block spans
+  int chunk_in;             // staging of u, delta_raw, z rows: 16- or 4-byte copies, or 0 (element-wise)
+  int disc;                 // 0 first order, 1 zero-order hold
+};
+
 // Launch plan for a scan problem.
 struct ScanPlan {
   int sg;               // threads per channel (1 or 2); each owns 16/sg states
@@ -149,6 +170,11 @@ cudaError_t launch_conv1d_update(const ConvParams& p, ss_dtype in_dtype, ss_dtyp
 cudaError_t launch_scan_bwd(const BwdParams& p, int sg, ss_dtype in_dtype, ss_dtype dy_dtype, cudaStream_t stream);
 size_t scan_bwd_checkpoint_bytes(int64_t batch, int64_t seqlen, int64_t dim, int sg);
 int64_t scan_bwd_subtiles(int64_t seqlen);
+
+// sg = dstate / 16 lanes per channel; bytes of one staged 16-step sub-tile
+cudaError_t launch_scan_general(const GenParams& p, int sg, ss_dtype in_dtype, ss_dtype out_dtype,
+                                cudaStream_t stream);
+int scan_general_stage_bytes(int64_t dstate, int ngw_max, ss_dtype in_dtype);
 
 // The library's own fault word (device symbol), used when no workspace is given.
 unsigned int* device_fault_word();

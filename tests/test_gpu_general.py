@@ -1,0 +1,104 @@
+"""GPU parity of the generalised scan (ss_scan_fwd_general: d_state 16-128, B and
+C in groups, first-order or zero-order-hold Bbar) against the float64 oracle,
+through the C ABI: every output on small and ragged problems, sampled channels
+over the whole sequence at the Mamba-2.8B layer size."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_130_b300 as ss
+from parity import assert_close, sample_channels, to_dev
+from workloads import configs, gen
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16 = torch.float32, torch.bfloat16
+
+
+def _run(x, disc, out_dtype):
+    d = to_dev(x)
+    y, h = ss.ss_scan_fwd_general(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], d.get("D"), d.get("z"),
+                                  d.get("delta_bias"), d.get("h0"), disc=disc, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return y.double().cpu().numpy(), h.double().cpu().numpy()
+
+
+# (in_dtype, batch, L, D, N, G, h0, z, D_skip, bias)
+SHAPES = [
+    ("f32", 1, 1, 16, 16, 1, False, True, True, True),
+    ("bf16", 2, 17, 40, 32, 1, True, True, True, True),      # ragged sub-tile and channel block
+    ("f32", 2, 33, 24, 16, 3, True, False, True, True),      # groups of 8 channels: three per warp
+    ("f32", 1, 45, 24, 32, 2, True, True, True, True),       # groups of 12: a warp straddles two
+    ("bf16", 2, 33, 24, 64, 3, True, False, True, True),     # groups of 8 = one warp's channels
+    ("bf16", 1, 100, 64, 128, 8, True, True, False, True),   # 4 channels per warp, 8 groups
+    ("f32", 3, 64, 6, 16, 6, False, True, True, False),      # one B/C per channel
+    ("bf16", 1, 40, 5, 64, 1, True, True, True, True),       # rows of 10 bytes: element-wise staging
+    ("bf16", 2, 21, 6, 128, 2, True, True, True, True),      # rows of 8 bytes: 4-byte copies
+    ("f32", 1, 513, 130, 32, 2, True, True, True, True),
+    ("bf16", 1, 1000, 96, 64, 4, True, True, True, True),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}-b{s[1]}-L{s[2]}-D{s[3]}-N{s[4]}-G{s[5]}" for s in SHAPES])
+@pytest.mark.parametrize("disc", ["first_order", "zoh"])
+def test_general_matches_oracle(shape, disc):
+    dt, Bt, L, Dm, N, G, h0, hz, hd, hb = shape
+    in_dt = BF16 if dt == "bf16" else F32
+    x = gen.random_general_inputs(Bt, L, Dm, N, G, in_dtype=dt, seed=L + Dm + N, with_h0=h0, has_z=hz,
+                                  has_d=hd, a_log_jitter=0.3)
+    if not hb:
+        x["delta_bias"] = None
+    yr, hr = oracle.scan_general(x, G, "zoh" if disc == "zoh" else "euler")
+    for out in (F32, BF16):
+        y, h = _run(x, disc, out)
+        assert_close(y, yr, in_dt, out_bf16=(out == BF16), what=f"general y {shape} {disc}")
+        assert_close(h, hr, in_dt, what=f"general h_last {shape} {disc}")
+
+
+def test_general_first_order_matches_scan():
+    # d_state 16, one group, first order: the specialised scan's problem
+    x = gen.random_scan_inputs(2, 300, 200, 16, in_dtype="bf16", seed=7, with_h0=True)
+    d = to_dev(x)
+    y1, h1 = ss.ss_scan_fwd(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], d["h0"],
+                            out_dtype=F32)
+    y2, h2 = ss.ss_scan_fwd_general(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                                    d["h0"], out_dtype=F32)
+    torch.cuda.synchronize()
+    assert_close(y2.double().cpu().numpy(), y1.double().cpu().numpy(), F32, what="general vs scan y")
+    assert_close(h2.double().cpu().numpy(), h1.double().cpu().numpy(), F32, what="general vs scan h")
+
+
+@pytest.mark.parametrize("N,G,disc", [(64, 1, "zoh"), (128, 8, "first_order")])
+def test_general_layer_sampled(N, G, disc):
+    # Mamba-2.8B layer shape (4 x 2048 x 5120, bf16), larger state: sampled channels over the whole sequence
+    w = configs.C2
+    x = gen.random_general_inputs(w.batch, w.seqlen, w.dim, N, G, in_dtype="bf16", seed=N + G)
+    ch = sample_channels(w.batch, w.dim, 24, seed=N)
+    yr, hr = oracle.scan_general(x, G, "zoh" if disc == "zoh" else "euler", channels=ch)
+    y, h = _run(x, disc, BF16)
+    assert_close(y[ch[:, 0], :, ch[:, 1]], yr, BF16, out_bf16=True, what=f"layer N={N} G={G} y")
+    assert_close(h[ch[:, 0], ch[:, 1]], hr, BF16, what=f"layer N={N} G={G} h_last")
+
+
+def test_general_errors_and_empty():
+    x = gen.random_general_inputs(1, 4, 8, 32, 2, in_dtype="f32", seed=1, with_h0=True)
+    d = to_dev(x)
+    lib = ss.lib()
+    args = lambda N, G, disc: [1, 4, 8, N, G, disc, ss.SS_F32, ss.SS_F32] + [  # noqa: E731
+        t.data_ptr() if t is not None else None for t in (d["u"], d["delta_raw"], d["A"], d["B"], d["C"], d["D"],
+                                                          d["z"], d["delta_bias"], d["h0"])]
+    y = torch.empty(1, 4, 8, device="cuda")
+    for N, G, disc, code in [(48, 2, 0, ss._lib.SS_ERR_UNSUPPORTED), (32, 3, 0, ss._lib.SS_ERR_INVALID_ARG),
+                             (32, 2, 2, ss._lib.SS_ERR_UNSUPPORTED), (32, 0, 0, ss._lib.SS_ERR_INVALID_ARG)]:
+        st = lib.ss_scan_fwd_general(*args(N, G, disc), y.data_ptr(), None, None)
+        assert st == code, (N, G, disc, st, ss.ss_last_error())
+    # L = 0: h_last = h0
+    e = {k: d[k][:, :0].contiguous() for k in ("u", "delta_raw", "z", "B", "C")}
+    hl = torch.full((1, 8, 32), 5.0, device="cuda")
+    ss.ss_scan_fwd_general(e["u"], e["delta_raw"], d["A"], e["B"], e["C"], d["D"], e["z"], d["delta_bias"], d["h0"],
+                           y=torch.empty(1, 0, 8, device="cuda"), h_last=hl)
+    torch.cuda.synchronize()
+    assert torch.equal(hl, d["h0"])
+    np.testing.assert_array_equal(hl.cpu().numpy(), x["h0"].numpy())
