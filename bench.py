@@ -435,6 +435,55 @@ def bench_scan_bwd(ss, w, dev, hbm_peak, clock_mhz, reps=10):
             "l2": "one input set of 420 MB (larger than L2)"}
 
 
+# Compute roof of the generalised scan per (t, d, n): first order as the scan
+# (4 fp32 lane-ops and one ex2: 32 per clock per SM); the zero-order hold adds
+# Abar - 1 and the products with u / A (7 lane-ops: 128 / 7 per clock per SM).
+GEN_UPDATES_PER_CLK_SM = {"first_order": 32.0, "zoh": 128.0 / 7.0}
+
+
+def bench_general(ss, w, dev, hbm_peak, clock_mhz, N, G, disc, reps=10):
+    """ss_scan_fwd_general on the Mamba-2.8B layer shape with a larger state:
+    bf16 inputs and y; one input set (larger than L2)."""
+    x = to_dev(gen.random_general_inputs(w.batch, w.seqlen, w.dim, N, G, in_dtype="bf16", seed=N + G), dev)
+    Bt, L, Dm = w.batch, w.seqlen, w.dim
+    y = torch.empty((Bt, L, Dm), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+
+    def call():
+        ss.ss_scan_fwd_general(x["u"], x["delta_raw"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], None,
+                               disc=disc, y=y, h_last=h)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(per)
+    nbytes = Bt * L * Dm * 8 + Bt * L * G * N * 2 * 2 + Bt * Dm * N * 4 + Dm * (N + 2) * 4
+    updates = Bt * L * Dm * N
+    alu_peak = GEN_UPDATES_PER_CLK_SM[disc] * SMS * clock_mhz * 1e6
+    achieved = updates / (ms * 1e-3)
+    del x, y, h
+    torch.cuda.empty_cache()
+    return {"workload": f"generalised scan, {w.name} shape: batch {Bt}, L {L}, d_inner {Dm}, d_state {N}, "
+                        f"{G} group(s) of B/C, {disc} Bbar, bf16 inputs and y",
+            "ms_per_launch": round(ms, 4), "ms_per_launch_median": round(statistics.median(per), 4),
+            "ms_per_launch_min": round(min(per), 4),
+            "roofline": {"bound": "alu", "unit": "state updates/s", "achieved": achieved, "peak": alu_peak,
+                         "frac": round(achieved / alu_peak, 4),
+                         "basis": ("4 fp32 lane-ops + 1 ex2 per (t,d,n): 32 per clk per SM" if disc == "first_order"
+                                   else "7 fp32 lane-ops per (t,d,n) (first order's 4, Abar - 1, u / A and its "
+                                        "product): 128 / 7 per clk per SM") + " x 148 SMs x median SM clock"},
+            "hbm": {"algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                    "frac_of_hbm_peak": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 4)},
+            "l2": "one input set larger than L2"}
+
+
 def cpu_baseline_scan(w, x, target_s=12.0):
     """The float64 oracle as it stands, on the host cores, over channels of the
     same workload; scaled to algorithmic GB/s of the sample."""
@@ -552,6 +601,8 @@ def run_ours(args, world, rank, local):
             torch.cuda.empty_cache()
         extra["conv1d_front_end"] = bench_conv1d(ss, dev, hbm_peak)
         extra["scan_backward"] = bench_scan_bwd(ss, w, dev, hbm_peak, clock_mhz)
+        extra["general_dstate64_zoh"] = bench_general(ss, w, dev, hbm_peak, clock_mhz, 64, 1, "zoh")
+        extra["general_dstate128_8groups"] = bench_general(ss, w, dev, hbm_peak, clock_mhz, 128, 8, "first_order")
         result["per_config"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_scan(w, x)
@@ -611,6 +662,12 @@ def profile_launches(args):
         for _ in range(2):
             scan_call(ss, x, y, h, ws)
         ss.ss_scan_status(ws)
+    elif args.profile == "general":
+        w = configs.get_config(args.workload)
+        x = to_dev(gen.random_general_inputs(w.batch, w.seqlen, w.dim, 64, 1, in_dtype="bf16", seed=65), dev)
+        for _ in range(2):
+            ss.ss_scan_fwd_general(x["u"], x["delta_raw"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                                   None, disc="zoh")
     elif args.profile == "bwd":
         w = configs.get_config(args.workload)
         x = to_dev(gen.make_scan_inputs(w), dev)
@@ -643,7 +700,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the c1 / c3 scan timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "decode", "bwd"], default=None,
+    ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general"], default=None,
                     help="run 2 launches of one kernel (for an ncu capture of the 2nd) and exit")
     args = ap.parse_args()
     if args.profile:
