@@ -18,7 +18,8 @@ forward oracle; for the convolution front-end: numpy's convolution,
 impulse responses, chunk continuity through the state, decode-equals-forward;
 for the generalised scan: scipy's zero-order-hold discretisation and
 simulation, the scan on its special case, per-group slices, a split of the
-states).
+states; for the state-space-dual layer: its dense semiseparable-matrix form,
+computed in numpy).
 """
 
 import ctypes
@@ -175,6 +176,35 @@ def scan_general(x: dict, ngroups: int = 1, disc: str = "euler", channels=None, 
     if full:
         return y.reshape(Bt, Dm, L).transpose(0, 2, 1).copy(), h.reshape(Bt, Dm, N)
     return y, h
+
+
+def ssd(x: dict, ngroups: int = 1, nthreads: int = None, lib_path: str = None):
+    """State-space-dual (Mamba-2) layer in float64: per head h a scalar decay,
+    h_t = exp(delta_t A_h) h_{t-1} + delta_t x_t B_t^T ([P, N] per head),
+    y_t = h_t C_t + D_h x_t, delta = softplus(dt + dt_bias). That is the
+    selective scan with channels (h, p), A[(h, p), n] = A_h for every n, and
+    the group of head h (B, C shared by H / G consecutive heads), so it runs
+    as scan_general on those expanded inputs.
+
+    x: dict of CPU tensors x [Bt, L, H, P], dt [Bt, L, H], B, C [Bt, L, G, N]
+    (one dtype), A [H], D [H] or None, dt_bias [H] or None, h0 [Bt, H, P, N] or
+    None (float32). Returns float64 (y [Bt, L, H, P], h_last [Bt, H, P, N]).
+    """
+    xx, dt = x["x"], x["dt"]
+    Bt, L, H, P = xx.shape
+    N = x["B"].shape[-1]
+    exp = {
+        "u": xx.reshape(Bt, L, H * P).contiguous(),
+        "delta_raw": dt.repeat_interleave(P, dim=2).contiguous(),
+        "z": None,
+        "B": x["B"], "C": x["C"],
+        "A": _f32(x["A"]).repeat_interleave(P).view(H * P, 1).expand(H * P, N).contiguous(),
+        "D": _f32(x["D"]).repeat_interleave(P).contiguous() if x.get("D") is not None else None,
+        "delta_bias": _f32(x["dt_bias"]).repeat_interleave(P).contiguous() if x.get("dt_bias") is not None else None,
+        "h0": _f32(x["h0"]).reshape(Bt, H * P, N).contiguous() if x.get("h0") is not None else None,
+    }
+    y, h = scan_general(exp, ngroups, "euler", nthreads=nthreads, lib_path=lib_path)
+    return y.reshape(Bt, L, H, P), h.reshape(Bt, H, P, N)
 
 
 def state_update(h: np.ndarray, x: dict, channels=None, lib_path: str = None):

@@ -25,7 +25,12 @@ Independent restatements used here (none calls the oracle's arithmetic):
   simulation (dlsim) of the same linear system, the exact discretisation of
   h' = A h + B x for a step-wise constant input ("外文文献精读" section 1.2;
   mlqm.cn tutorial section 3.2); the brute-force sum on the first-order case at
-  any state size; per-group channel slices.
+  any state size; per-group channel slices;
+- state-space-dual layer: the selective scan with a scalar decay per head is
+  multiplication by the semiseparable matrix M[t, s] = (C_t . B_s) delta_s
+  exp(sum_{s<k<=t} delta_k A) for s <= t ("AI 推理系列（十四）", section on
+  Mamba-2 reorganising the SSM as matrix computation; mlqm.cn tutorial,
+  section 8), built densely here.
 """
 
 import math
@@ -35,7 +40,7 @@ import torch
 from scipy.special import expit
 
 import oracle
-from workloads.gen import random_general_inputs, random_scan_inputs
+from workloads.gen import random_general_inputs, random_scan_inputs, random_ssd_inputs
 
 
 # ----------------------------------------------------------------- helpers
@@ -577,7 +582,47 @@ def pin_general_zoh_small_step(lib=None):
     assert np.any(yz != ye), "zoh identical to first order"
 
 
-ALL_PINS = [pin_general_zoh_scipy, pin_general_first_order_brute_force, pin_general_groups,
+# ------------------------------------------------- state-space-dual (Mamba-2) layer
+
+def ssd_dense(x, G):
+    """y = M x with the dense semiseparable matrix per (batch, head), plus the
+    initial state's decayed readout; h_last from the same weights."""
+    X, dt, B, C = _np(x["x"]), _np(x["dt"]), _np(x["B"]), _np(x["C"])
+    A, Dk, bias, h0 = _np(x["A"]), _np(x.get("D")), _np(x.get("dt_bias")), _np(x.get("h0"))
+    Bt, L, H, P = X.shape
+    N = B.shape[-1]
+    y = np.zeros((Bt, L, H, P))
+    hl = np.zeros((Bt, H, P, N))
+    for b in range(Bt):
+        for hd in range(H):
+            g = hd // (H // G)
+            delta = _softplus_ref(dt[b, :, hd] + (bias[hd] if bias is not None else 0.0))   # [L]
+            cum = np.concatenate([[0.0], np.cumsum(delta * A[hd])])                         # cum[t+1] = sum_{k<=t}
+            seg = cum[1:, None] - cum[None, 1:]                                             # sum_{s<k<=t}
+            M = np.where(np.tri(L, dtype=bool), (C[b, :, g] @ B[b, :, g].T) * delta[None, :] * np.exp(
+                np.where(np.tri(L, dtype=bool), seg, 0.0)), 0.0)
+            y[b, :, hd] = M @ X[b, :, hd]
+            w = np.exp(cum[L] - cum[1:]) * delta                                            # weight of step s in h_last
+            hl[b, hd] = (X[b, :, hd] * w[:, None]).T @ B[b, :, g]
+            if h0 is not None:
+                y[b, :, hd] += np.exp(cum[1:])[:, None] * (C[b, :, g] @ h0[b, hd].T)
+                hl[b, hd] += np.exp(cum[L]) * h0[b, hd]
+            if Dk is not None:
+                y[b, :, hd] += Dk[hd] * X[b, :, hd]
+    return y, hl
+
+
+def pin_ssd_semiseparable(lib=None):
+    for (Bt, L, H, P, N, G, dtype, with_h0, seed) in [(2, 21, 4, 3, 5, 2, "f32", True, 51),
+                                                       (1, 33, 2, 4, 16, 1, "bf16", False, 52)]:
+        x = random_ssd_inputs(Bt, L, H, P, N, G, in_dtype=dtype, seed=seed, with_h0=with_h0)
+        y, h = oracle.ssd(x, G, lib_path=lib)
+        yd, hd = ssd_dense(x, G)
+        _close(y, yd, 1e-10, 1e-12, "ssd y vs semiseparable matrix")
+        _close(h, hd, 1e-10, 1e-12, "ssd h_last vs semiseparable matrix")
+
+
+ALL_PINS = [pin_ssd_semiseparable, pin_general_zoh_scipy, pin_general_first_order_brute_force, pin_general_groups,
             pin_general_zoh_small_step, pin_backward_finite_differences, pin_backward_bf16_widening, pin_conv_numpy, pin_conv_impulse, pin_conv_chunk_continuity, pin_conv_decode_equals_forward,
             pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_large_delta_overwrites,
             pin_chunk_associativity, pin_geometric_series, pin_single_step_by_hand, pin_softplus_values,

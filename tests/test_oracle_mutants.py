@@ -88,3 +88,30 @@ def test_mutant_is_caught(name, tmpdir_mod):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"mutant {name} passed every pin"
+
+
+# Planted mistakes in the state-space-dual wrapper (oracle.ssd expands heads
+# into channels of the generalised scan): each must fail the semiseparable pin.
+SSD_MUTANTS = {
+    "ssd_dt_tiled_not_repeated": ("dt.repeat_interleave(P, dim=2)", "dt.repeat(1, 1, P)"),
+    "ssd_A_tiled_not_repeated": ('_f32(x["A"]).repeat_interleave(P)', '_f32(x["A"]).repeat(P)'),
+    "ssd_zero_order_hold": ('ngroups, "euler"', 'ngroups, "zoh"'),
+    "ssd_bias_dropped": ('if x.get("dt_bias") is not None else None', 'if False else None'),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SSD_MUTANTS))
+def test_ssd_wrapper_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+
+    import oracle
+
+    old, new = SSD_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(oracle.ssd))
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new, 1), f"<{name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, "ssd", ns["ssd"])
+    with pytest.raises(AssertionError):
+        pins.pin_ssd_semiseparable()

@@ -194,3 +194,29 @@ def random_general_inputs(batch, seqlen, dim, dstate, ngroups=1, in_dtype="f32",
     x["B"] = _store(randn_blocks(n, seed, S_B, threads).view(batch, seqlen, ngroups, dstate), in_dtype).contiguous()
     x["C"] = _store(randn_blocks(n, seed, S_C, threads).view(batch, seqlen, ngroups, dstate), in_dtype).contiguous()
     return x
+
+
+def random_ssd_inputs(batch, seqlen, nheads, headdim, dstate, ngroups=1, in_dtype="bf16", seed=0, with_h0=False,
+                      threads: int = 0):
+    """Inputs of the state-space-dual (Mamba-2) layer: x [batch, L, H, P], dt
+    [batch, L, H] (0.5 N(0,1)), B, C [batch, L, G, N] (N(0,1)) in in_dtype; A [H]
+    = -U(1, 16) per head, D [H] = 1, dt_bias [H] = log(expm1(dt0)) with dt0 =
+    exp(U(log 1e-3, log 0.1)) (float32); h0 [batch, H, P, N] or None."""
+    n = batch * seqlen * nheads * headdim
+    x = randn_blocks(n, seed, S_U, threads).view(batch, seqlen, nheads, headdim)
+    dt = 0.5 * randn_blocks(batch * seqlen * nheads, seed, S_DRAW, threads).view(batch, seqlen, nheads)
+    nb = batch * seqlen * ngroups * dstate
+    B = randn_blocks(nb, seed, S_B, threads).view(batch, seqlen, ngroups, dstate)
+    C = randn_blocks(nb, seed, S_C, threads).view(batch, seqlen, ngroups, dstate)
+    g = torch.Generator().manual_seed(_block_seed(seed, S_ALOG, 0))
+    A = -(1.0 + 15.0 * torch.rand(nheads, generator=g, dtype=torch.float64)).float()
+    g = torch.Generator().manual_seed(_block_seed(seed, S_DT, 0))
+    dt0 = torch.exp(math.log(1e-3) + (math.log(0.1) - math.log(1e-3)) * torch.rand(nheads, generator=g,
+                                                                                   dtype=torch.float64))
+    out = {"x": _store(x, in_dtype).contiguous(), "dt": _store(dt, in_dtype).contiguous(),
+           "B": _store(B, in_dtype).contiguous(), "C": _store(C, in_dtype).contiguous(),
+           "A": A.contiguous(), "D": torch.ones(nheads, dtype=torch.float32),
+           "dt_bias": torch.log(torch.expm1(dt0)).float().contiguous()}
+    out["h0"] = (randn_blocks(batch * nheads * headdim * dstate, seed, 99, threads)
+                 .view(batch, nheads, headdim, dstate).contiguous() if with_h0 else None)
+    return out
