@@ -484,6 +484,52 @@ def bench_general(ss, w, dev, hbm_peak, clock_mhz, N, G, disc, reps=10):
             "l2": "one input set larger than L2"}
 
 
+def bench_ssd(ss, dev, hbm_peak, tensor_peak, Bt=4, L=2048, H=80, N=128, G=1, reps=10):
+    """ss_ssd_fwd (state-space-dual layer, tensor-core chunked form) on a Mamba-2
+    2.7B-shaped layer: batch 4, L 2048, 80 heads x 64 channels (d_inner 5120),
+    d_state 128, one group, bf16 in and out. One input set (larger than L2)."""
+    P, Q = 64, 64
+    x = to_dev(gen.random_ssd_inputs(Bt, L, H, P, N, G, in_dtype="bf16", seed=11), dev)
+    y = torch.empty((Bt, L, H, P), dtype=torch.bfloat16, device=dev)
+    hl = torch.empty((Bt, H, P, N), dtype=torch.float32, device=dev)
+
+    def call():
+        ss.ss_ssd_fwd(x["x"], x["dt"], x["A"], x["B"], x["C"], x["D"], x["dt_bias"], None, y=y, h_last=hl)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(per)
+    # bytes: x in and y out (bf16), dt, B, C in, the final state out
+    nbytes = Bt * L * H * P * 2 * 2 + Bt * L * H * 2 + Bt * L * G * N * 2 * 2 + Bt * H * P * N * 4
+    # flops of the chunked form per (batch, head, chunk): the causal half of C B^T
+    # (Q(Q+1)/2 x N) and of M X (Q(Q+1)/2 x P), C H_in (Q x N x P) and B^T X (N x Q x P), 2 per multiply-add
+    tri = Q * (Q + 1) // 2
+    flops = Bt * H * ((L + Q - 1) // Q) * 2 * (tri * N + tri * P + Q * N * P + N * Q * P)
+    t = ms * 1e-3
+    del x, y, hl
+    torch.cuda.empty_cache()
+    return {"workload": f"state-space-dual (Mamba-2) layer: batch {Bt}, L {L}, {H} heads x {P} channels, d_state {N}, "
+                        f"{G} group, chunks of {Q}, bf16 in/out",
+            "ms_per_launch": round(ms, 4), "ms_per_launch_median": round(statistics.median(per), 4),
+            "ms_per_launch_min": round(min(per), 4), "channel_tokens_per_s": Bt * L * H * P / t,
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / t / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(nbytes / t / 1e9 / hbm_peak, 4), "algorithmic_bytes": nbytes,
+                         "note": "at the measured peaks the bytes take longer than the algorithmic flops"},
+            "tensor": {"algorithmic_flops": flops, "achieved_tflops": round(flops / t / 1e12, 2),
+                       "peak_tflops": tensor_peak, "frac": round(flops / t / 1e12 / tensor_peak, 4),
+                       "note": "mma.sync m16n8k16 bf16; operands computed on chip run as two bf16 parts, "
+                               "so the tensor pipe executes about 1.8x the algorithmic flops"},
+            "l2": "one input set of 176 MB (larger than L2)"}
+
+
 def cpu_baseline_scan(w, x, target_s=12.0):
     """The float64 oracle as it stands, on the host cores, over channels of the
     same workload; scaled to algorithmic GB/s of the sample."""
@@ -603,6 +649,7 @@ def run_ours(args, world, rank, local):
         extra["scan_backward"] = bench_scan_bwd(ss, w, dev, hbm_peak, clock_mhz)
         extra["general_dstate64_zoh"] = bench_general(ss, w, dev, hbm_peak, clock_mhz, 64, 1, "zoh")
         extra["general_dstate128_8groups"] = bench_general(ss, w, dev, hbm_peak, clock_mhz, 128, 8, "first_order")
+        extra["ssd_mamba2_2p7b_layer"] = bench_ssd(ss, dev, hbm_peak, float(peaks.get("bf16_tflops", 1786.4)))
         result["per_config"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_scan(w, x)
@@ -662,6 +709,10 @@ def profile_launches(args):
         for _ in range(2):
             scan_call(ss, x, y, h, ws)
         ss.ss_scan_status(ws)
+    elif args.profile == "ssd":
+        x = to_dev(gen.random_ssd_inputs(4, 2048, 80, 64, 128, 1, in_dtype="bf16", seed=11), dev)
+        for _ in range(2):
+            ss.ss_ssd_fwd(x["x"], x["dt"], x["A"], x["B"], x["C"], x["D"], x["dt_bias"], None)
     elif args.profile == "general":
         w = configs.get_config(args.workload)
         x = to_dev(gen.random_general_inputs(w.batch, w.seqlen, w.dim, 64, 1, in_dtype="bf16", seed=65), dev)
@@ -700,7 +751,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the c1 / c3 scan timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general"], default=None,
+    ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general", "ssd"], default=None,
                     help="run 2 launches of one kernel (for an ncu capture of the 2nd) and exit")
     args = ap.parse_args()
     if args.profile:

@@ -254,6 +254,44 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
                               void *y, float *h_last, void *stream);
 
 /*
+ * State-space-dual (Mamba-2) layer forward on the tensor cores.
+ *
+ * The pages say Mamba-2 shows the selective scan to be dual to a structured
+ * (semiseparable) matrix multiplication and re-blocks the state computation so
+ * that more of it runs as matrix products ("AI 推理系列（十四）：Mamba 的
+ * Selective State Space", section on Mamba-2; mlqm.cn tutorial, section 8).
+ * They print no formulas; this library reads the layer as the selective scan
+ * with one scalar decay per head, which is what makes the matrix shared by a
+ * head's channels. Per batch element b and head h, with delta_t =
+ * softplus(dt[b,t,h] + dt_bias[h]) and g = h / (nheads / ngroups):
+ *
+ *   H[p,n]  = exp(delta_t A[h]) H[p,n] + delta_t x[b,t,h,p] B[b,t,g,n]
+ *   y[b,t,h,p] = sum_n H[p,n] C[b,t,g,n] + D[h] x[b,t,h,p]
+ *
+ * from H = h0[b,h] (zeros when NULL); h_last[b,h] = H after the last step.
+ * Equivalently y = M x per (b, h) with M[t,s] = (C_t . B_s) delta_s
+ * exp(A[h] sum_{s<k<=t} delta_k) for s <= t.
+ *
+ *  x            : [batch, seqlen, nheads, headdim] bf16 (in_dtype must be SS_BF16)
+ *  dt           : [batch, seqlen, nheads] bf16
+ *  A            : [nheads] float32 (negative)
+ *  B, C         : [batch, seqlen, ngroups, dstate] bf16
+ *  D, dt_bias   : [nheads] float32 or NULL
+ *  h0, h_last   : [batch, nheads, headdim, dstate] float32 or NULL
+ *  y            : [batch, seqlen, nheads, headdim] out_dtype
+ * headdim must be 64 and dstate 64 or 128 (SS_ERR_UNSUPPORTED otherwise);
+ * nheads must be a multiple of ngroups. Computed in chunks of 64 steps with
+ * bf16 tensor-core products accumulated in float32; the operands computed on
+ * chip (the masked C.B^T, the weighted B, the carried state) enter the
+ * products as two bf16 parts (about 16 significant bits). No workspace.
+ */
+ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                     int64_t ngroups, ss_dtype in_dtype, ss_dtype out_dtype,
+                     const void *x, const void *dt, const float *A, const void *B, const void *C,
+                     const float *D, const float *dt_bias, const float *h0,
+                     void *y, float *h_last, void *stream);
+
+/*
  * Launch-shape controls for the calling host thread (0 = automatic, the
  * default, for each). threads_per_channel in {1, 2} sets how many threads share
  * one channel's 16 states. chunk_len > 0 forces the sequence to be split into

@@ -178,7 +178,7 @@ def scan_general(x: dict, ngroups: int = 1, disc: str = "euler", channels=None, 
     return y, h
 
 
-def ssd(x: dict, ngroups: int = 1, nthreads: int = None, lib_path: str = None):
+def ssd(x: dict, ngroups: int = 1, channels=None, nthreads: int = None, lib_path: str = None):
     """State-space-dual (Mamba-2) layer in float64: per head h a scalar decay,
     h_t = exp(delta_t A_h) h_{t-1} + delta_t x_t B_t^T ([P, N] per head),
     y_t = h_t C_t + D_h x_t, delta = softplus(dt + dt_bias). That is the
@@ -188,7 +188,8 @@ def ssd(x: dict, ngroups: int = 1, nthreads: int = None, lib_path: str = None):
 
     x: dict of CPU tensors x [Bt, L, H, P], dt [Bt, L, H], B, C [Bt, L, G, N]
     (one dtype), A [H], D [H] or None, dt_bias [H] or None, h0 [Bt, H, P, N] or
-    None (float32). Returns float64 (y [Bt, L, H, P], h_last [Bt, H, P, N]).
+    None (float32). Returns float64 (y [Bt, L, H, P], h_last [Bt, H, P, N]);
+    with channels, an int array [n, 3] of (b, h, p), y [n, L] and h_last [n, N].
     """
     xx, dt = x["x"], x["dt"]
     Bt, L, H, P = xx.shape
@@ -203,6 +204,10 @@ def ssd(x: dict, ngroups: int = 1, nthreads: int = None, lib_path: str = None):
         "delta_bias": _f32(x["dt_bias"]).repeat_interleave(P).contiguous() if x.get("dt_bias") is not None else None,
         "h0": _f32(x["h0"]).reshape(Bt, H * P, N).contiguous() if x.get("h0") is not None else None,
     }
+    if channels is not None:
+        ch = np.asarray(channels, dtype=np.int64).reshape(-1, 3)
+        pairs = np.stack([ch[:, 0], ch[:, 1] * P + ch[:, 2]], axis=1)
+        return scan_general(exp, ngroups, "euler", channels=pairs, nthreads=nthreads, lib_path=lib_path)
     y, h = scan_general(exp, ngroups, "euler", nthreads=nthreads, lib_path=lib_path)
     return y.reshape(Bt, L, H, P), h.reshape(Bt, H, P, N)
 

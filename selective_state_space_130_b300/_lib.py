@@ -42,6 +42,7 @@ SIGNATURES = {
     "ss_scan_bwd": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int] + [_P] * 21 + [_SZ, _P]),
     "ss_scan_fwd_general": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
                             + [_P] * 11 + [_P]),
+    "ss_ssd_fwd": (ctypes.c_int, [_I64] * 6 + [ctypes.c_int, ctypes.c_int] + [_P] * 10 + [_P]),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
 }
@@ -211,6 +212,25 @@ def ss_scan_fwd_general(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, 
     _check(lib().ss_scan_fwd_general(Bt, L, Dm, N, G, DISC[disc], code, out_code, _ptr(u), _ptr(delta_raw), _ptr(A),
                                      _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y),
                                      _ptr(h_last), _stream(stream)))
+    return y, h_last
+
+
+def ss_ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, out_dtype=None, y=None, h_last=None,
+               return_h_last=True, stream=None):
+    """State-space-dual (Mamba-2) layer on device tensors: x [Bt, L, H, 64], dt
+    [Bt, L, H], B, C [Bt, L, G, N] (bf16); A, D, dt_bias [H]; h0 [Bt, H, 64, N]
+    float32. Returns (y, h_last)."""
+    Bt, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    code = _dt(x)
+    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    dev = x.device
+    if y is None:
+        y = torch.empty((Bt, L, H, P), dtype=_tdt(out_code), device=dev)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bt, H, P, N), dtype=torch.float32, device=dev)
+    _check(lib().ss_ssd_fwd(Bt, L, H, P, N, G, code, out_code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                            _ptr(dt_bias), _ptr(h0), _ptr(y), _ptr(h_last), _stream(stream)))
     return y, h_last
 
 

@@ -535,6 +535,54 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
   return SS_OK;
 }
 
+ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                     int64_t ngroups, ss_dtype in_dtype, ss_dtype out_dtype, const void* x, const void* dt,
+                     const float* A, const void* B, const void* C, const float* D, const float* dt_bias,
+                     const float* h0, void* y, float* h_last, void* stream) {
+  g_err.clear();
+  if (in_dtype != SS_BF16) return fail(SS_ERR_UNSUPPORTED, "the state-space-dual layer takes bf16 inputs");
+  if (!valid_dtype(out_dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown output dtype %d", (int)out_dtype);
+  if (headdim != 64) return fail(SS_ERR_UNSUPPORTED, "headdim must be 64 (got %lld)", (long long)headdim);
+  if (dstate != 64 && dstate != 128)
+    return fail(SS_ERR_UNSUPPORTED, "dstate must be 64 or 128 (got %lld)", (long long)dstate);
+  if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups < 1)
+    return fail(SS_ERR_INVALID_ARG, "negative size or ngroups < 1");
+  if (batch > INT32_MAX || seqlen > INT32_MAX || nheads > INT32_MAX)
+    return fail(SS_ERR_INVALID_ARG, "a size exceeds 2^31-1");
+  if (nheads > 0 && nheads % ngroups != 0)
+    return fail(SS_ERR_INVALID_ARG, "nheads (%lld) is not a multiple of ngroups (%lld)", (long long)nheads,
+                (long long)ngroups);
+  if (batch == 0 || nheads == 0) return SS_OK;
+  if ((double)batch * (double)seqlen * (double)nheads * 64.0 > 4.0e18)
+    return fail(SS_ERR_INVALID_ARG, "problem too large");
+  if (!A) return fail(SS_ERR_INVALID_ARG, "A must not be NULL");
+  if (seqlen > 0) {
+    const void* need[] = {x, dt, B, C, y};
+    const char* names[] = {"x", "dt", "B", "C", "y"};
+    for (int i = 0; i < 5; i++)
+      if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
+  }
+  const void* all[] = {x, dt, A, B, C, D, dt_bias, h0, y, h_last};
+  const char* all_names[] = {"x", "dt", "A", "B", "C", "D", "dt_bias", "h0", "y", "h_last"};
+  for (int i = 0; i < 10; i++)
+    if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (seqlen == 0) {
+    if (!h_last) return SS_OK;
+    const size_t hbytes = (size_t)batch * nheads * 64 * dstate * sizeof(float);
+    cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, hbytes, cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(h_last, 0, hbytes, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
+  }
+  if ((double)batch * nheads > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
+  ssk::SsdParams p{x, dt, A, B, C, D, dt_bias, h0, y, h_last, batch, seqlen, nheads, ngroups};
+  cudaError_t e = ssk::launch_ssd_fwd(p, (int)dstate, out_dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "state-space-dual launch");
+  return SS_OK;
+}
+
 ss_status ss_scan_status(void* workspace, void* stream) {
   g_err.clear();
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -130,6 +130,21 @@ struct GenParams {
   int disc;                 // 0 first order, 1 zero-order hold
 };
 
+// Parameters of the state-space-dual (Mamba-2) layer forward.
+struct SsdParams {
+  const void* x;            // [batch, seqlen, nheads, 64] bf16
+  const void* dt;           // [batch, seqlen, nheads] bf16
+  const float* A;           // [nheads]
+  const void* B;            // [batch, seqlen, ngroups, dstate] bf16
+  const void* C;
+  const float* D;           // [nheads] or null
+  const float* dt_bias;     // [nheads] or null
+  const float* h0;          // [batch, nheads, 64, dstate] or null
+  void* y;                  // [batch, seqlen, nheads, 64]
+  float* h_last;            // [batch, nheads, 64, dstate] or null
+  int64_t batch, seqlen, nheads, ngroups;
+};
+
 // Launch plan for a scan problem.
 struct ScanPlan {
   int sg;               // threads per channel (1 or 2); each owns 16/sg states
@@ -175,6 +190,8 @@ int64_t scan_bwd_subtiles(int64_t seqlen);
 cudaError_t launch_scan_general(const GenParams& p, int sg, ss_dtype in_dtype, ss_dtype out_dtype,
                                 cudaStream_t stream);
 int scan_general_stage_bytes(int64_t dstate, int ngw_max, ss_dtype in_dtype);
+
+cudaError_t launch_ssd_fwd(const SsdParams& p, int dstate, ss_dtype out_dtype, cudaStream_t stream);
 
 // The library's own fault word (device symbol), used when no workspace is given.
 unsigned int* device_fault_word();

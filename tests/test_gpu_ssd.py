@@ -1,0 +1,113 @@
+"""GPU parity of the state-space-dual (Mamba-2) layer (ss_ssd_fwd, tensor-core
+chunked form) against the float64 oracle (the recurrence with a scalar decay
+per head), through the C ABI: every output on small and ragged problems,
+sampled head channels over the whole sequence at a Mamba-2 2.7B-shaped layer."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_130_b300 as ss
+from parity import assert_close, to_dev
+from workloads import gen
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16 = torch.float32, torch.bfloat16
+
+
+def _run(x, out_dtype):
+    d = to_dev(x)
+    y, h = ss.ss_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d.get("D"), d.get("dt_bias"), d.get("h0"),
+                         out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return y.double().cpu().numpy(), h.double().cpu().numpy()
+
+
+# (batch, L, heads, N, groups, h0)
+SHAPES = [
+    (1, 1, 1, 64, 1, False),      # one step
+    (2, 65, 4, 64, 2, True),      # one step past a chunk
+    (1, 64, 2, 128, 1, False),    # exactly one chunk
+    (1, 130, 3, 128, 1, True),    # ragged third chunk
+    (2, 200, 8, 128, 4, True),    # two heads per group
+    (1, 1000, 2, 64, 2, True),    # 16 chunks of carried state
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"b{s[0]}-L{s[1]}-H{s[2]}-N{s[3]}-G{s[4]}" for s in SHAPES])
+def test_ssd_matches_oracle(shape):
+    Bt, L, H, N, G, h0 = shape
+    x = gen.random_ssd_inputs(Bt, L, H, 64, N, G, in_dtype="bf16", seed=L + H + N, with_h0=h0)
+    yr, hr = oracle.ssd(x, G)
+    for out in (F32, BF16):
+        y, h = _run(x, out)
+        assert_close(y, yr, BF16, out_bf16=(out == BF16), what=f"ssd y {shape}")
+        assert_close(h, hr, BF16, what=f"ssd h_last {shape}")
+    # the products carry about 16 significant bits: the float32 output also
+    # meets the float32-input bound
+    y, h = _run(x, F32)
+    assert_close(y, yr, F32, what=f"ssd y {shape} (float32 bound)")
+    assert_close(h, hr, F32, what=f"ssd h_last {shape} (float32 bound)")
+
+
+def test_ssd_without_skip_and_bias():
+    x = gen.random_ssd_inputs(1, 100, 2, 64, 64, 1, in_dtype="bf16", seed=3, with_h0=True)
+    x["D"] = None
+    x["dt_bias"] = None
+    yr, hr = oracle.ssd(x, 1)
+    y, h = _run(x, F32)
+    assert_close(y, yr, BF16, what="ssd y (no D, no bias)")
+    assert_close(h, hr, BF16, what="ssd h_last (no D, no bias)")
+
+
+def test_ssd_layer_sampled():
+    # Mamba-2 2.7B-shaped layer: batch 4, L 2048, 80 heads of 64 channels (d_inner 5120), d_state 128
+    Bt, L, H, N = 4, 2048, 80, 128
+    x = gen.random_ssd_inputs(Bt, L, H, 64, N, 1, in_dtype="bf16", seed=11)
+    rng = np.random.default_rng(2)
+    ch = np.stack([rng.integers(0, Bt, 24), rng.integers(0, H, 24), rng.integers(0, 64, 24)], axis=1)
+    ch = np.concatenate([ch, [[0, 0, 0], [Bt - 1, H - 1, 63]]])
+    yr, hr = oracle.ssd(x, 1, channels=ch)
+    y, h = _run(x, BF16)
+    assert_close(y[ch[:, 0], :, ch[:, 1], ch[:, 2]], yr, BF16, out_bf16=True, what="layer ssd y")
+    assert_close(h[ch[:, 0], ch[:, 1], ch[:, 2]], hr, BF16, what="layer ssd h_last")
+
+
+def test_ssd_chunk_continuity():
+    # two calls chained through the state equal one call
+    x = gen.random_ssd_inputs(2, 300, 4, 64, 128, 2, in_dtype="bf16", seed=5, with_h0=True)
+    y, h = _run(x, F32)
+    m = 100
+    a = dict(x, x=x["x"][:, :m].contiguous(), dt=x["dt"][:, :m].contiguous(), B=x["B"][:, :m].contiguous(),
+             C=x["C"][:, :m].contiguous())
+    ya, ha = _run(a, F32)
+    bb = dict(x, x=x["x"][:, m:].contiguous(), dt=x["dt"][:, m:].contiguous(), B=x["B"][:, m:].contiguous(),
+              C=x["C"][:, m:].contiguous(), h0=torch.tensor(ha, dtype=torch.float32))
+    yb, hb = _run(bb, F32)
+    # the two runs cut the sequence into chunks at different steps; both are
+    # held to the bound of their bf16 inputs
+    assert_close(np.concatenate([ya, yb], axis=1), y, BF16, what="chained y")
+    assert_close(hb, h, BF16, what="chained h_last")
+
+
+def test_ssd_errors_and_empty():
+    x = gen.random_ssd_inputs(1, 4, 2, 64, 64, 1, in_dtype="bf16", seed=1, with_h0=True)
+    d = to_dev(x)
+    lib = ss.lib()
+    y = torch.empty(1, 4, 2, 64, dtype=torch.bfloat16, device="cuda")
+    ptrs = [t.data_ptr() if t is not None else None for t in (d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"],
+                                                              d["dt_bias"], d["h0"])]
+    for (P, N, G, dt_code, code) in [(32, 64, 1, ss.SS_BF16, ss._lib.SS_ERR_UNSUPPORTED),
+                                     (64, 96, 1, ss.SS_BF16, ss._lib.SS_ERR_UNSUPPORTED),
+                                     (64, 64, 3, ss.SS_BF16, ss._lib.SS_ERR_INVALID_ARG),
+                                     (64, 64, 1, ss.SS_F32, ss._lib.SS_ERR_UNSUPPORTED)]:
+        st = lib.ss_ssd_fwd(1, 4, 2, P, N, G, dt_code, ss.SS_BF16, *ptrs, y.data_ptr(), None, None)
+        assert st == code, (P, N, G, st, ss.ss_last_error())
+    e = {k: d[k][:, :0].contiguous() for k in ("x", "dt", "B", "C")}
+    hl = torch.full((1, 2, 64, 64), 3.0, device="cuda")
+    ss.ss_ssd_fwd(e["x"], e["dt"], d["A"], e["B"], e["C"], d["D"], d["dt_bias"], d["h0"],
+                  y=torch.empty(1, 0, 2, 64, dtype=torch.bfloat16, device="cuda"), h_last=hl)
+    torch.cuda.synchronize()
+    assert torch.equal(hl, d["h0"])

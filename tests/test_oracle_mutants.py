@@ -111,7 +111,7 @@ def test_ssd_wrapper_mutant_is_caught(name, monkeypatch):
     src = textwrap.dedent(inspect.getsource(oracle.ssd))
     assert src.count(old) >= 1, f"mutation site for {name} not found"
     ns = dict(vars(oracle))
-    exec(compile(src.replace(old, new, 1), f"<{name}>", "exec"), ns)
+    exec(compile(src.replace(old, new), f"<{name}>", "exec"), ns)
     monkeypatch.setattr(oracle, "ssd", ns["ssd"])
     with pytest.raises(AssertionError):
         pins.pin_ssd_semiseparable()
