@@ -117,3 +117,94 @@ def test_binding_raises_typed_errors():
     with pytest.raises(ss.SSError) as ei:
         ss._lib._check(_scan(dstate=4))
     assert ei.value.status == _lib.SS_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- backward, generalised scan, SSD layer
+def _bwd(**kw):
+    a = dict(batch=1, seqlen=8, dim=8, dstate=16, in_dtype=0, dy_dtype=0)
+    a.update({k: v for k, v in kw.items() if k in a})
+    p = dict(u=0x1000, delta_raw=0x2000, A=0x3000, B=0x4000, C=0x5000, D=None, z=None, delta_bias=None, h0=None,
+             dy=0x6000, dh_last=None, du=0x7000, ddelta_raw=0x8000, dz=None, dA=0x9000, dB=0xa000, dC=0xb000,
+             dD=None, ddelta_bias=None, dh0=None, workspace=0xc000)
+    p.update({k: v for k, v in kw.items() if k in p})
+    order = ("u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "dy", "dh_last", "du", "ddelta_raw",
+             "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0", "workspace")
+    return ss.lib().ss_scan_bwd(a["batch"], a["seqlen"], a["dim"], a["dstate"], a["in_dtype"], a["dy_dtype"],
+                                *[p[k] for k in order], kw.get("ws_bytes", 1 << 20), None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(dstate=32), _lib.SS_ERR_UNSUPPORTED, "dstate"),
+    (dict(dy_dtype=3), _lib.SS_ERR_UNSUPPORTED, "dtype"),
+    (dict(seqlen=-1), _lib.SS_ERR_INVALID_ARG, "negative"),
+    (dict(dy=None), _lib.SS_ERR_INVALID_ARG, "dy must not"),
+    (dict(dB=None), _lib.SS_ERR_INVALID_ARG, "dB must not"),
+    (dict(dA=None), _lib.SS_ERR_INVALID_ARG, "dA must not"),
+    (dict(z=0xd000), _lib.SS_ERR_INVALID_ARG, "dz must not"),
+    (dict(dh0=0xe008), _lib.SS_ERR_INVALID_ARG, "aligned"),
+    (dict(ws_bytes=16), _lib.SS_ERR_INVALID_ARG, "workspace"),
+    (dict(workspace=None), _lib.SS_ERR_INVALID_ARG, "workspace"),
+])
+def test_scan_bwd_rejects_bad_arguments(kw, code, msg):
+    assert _bwd(**kw) == code
+    assert msg in ss.ss_last_error()
+
+
+def test_scan_bwd_workspace_and_empty():
+    assert _bwd(batch=0) == _lib.SS_OK
+    # the saved states: 2 KB per 32 channels per 16 steps (either lane layout)
+    assert ss.ss_scan_bwd_workspace_size(1, 16, 32) == 2048
+    assert ss.ss_scan_bwd_workspace_size(4, 2048, 5120) == 4 * 160 * 128 * 2048
+    assert ss.ss_scan_bwd_workspace_size(1, 16, 32, 8) == 0
+
+
+def _gen(**kw):
+    a = dict(batch=1, seqlen=8, dim=8, dstate=32, ngroups=2, disc=0, in_dtype=0, out_dtype=0)
+    a.update({k: v for k, v in kw.items() if k in a})
+    p = [kw.get(k, v) for k, v in (("u", 0x1000), ("delta_raw", 0x2000), ("A", 0x3000), ("B", 0x4000),
+                                   ("C", 0x5000), ("D", None), ("z", None), ("delta_bias", None), ("h0", None),
+                                   ("y", 0x6000), ("h_last", None))]
+    return ss.lib().ss_scan_fwd_general(a["batch"], a["seqlen"], a["dim"], a["dstate"], a["ngroups"], a["disc"],
+                                        a["in_dtype"], a["out_dtype"], *p, None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(dstate=48), _lib.SS_ERR_UNSUPPORTED, "dstate"),
+    (dict(dstate=256), _lib.SS_ERR_UNSUPPORTED, "dstate"),
+    (dict(disc=2), _lib.SS_ERR_UNSUPPORTED, "discretisation"),
+    (dict(ngroups=3), _lib.SS_ERR_INVALID_ARG, "multiple of ngroups"),
+    (dict(ngroups=0), _lib.SS_ERR_INVALID_ARG, "ngroups"),
+    (dict(B=None), _lib.SS_ERR_INVALID_ARG, "B must not"),
+    (dict(u=0x1004), _lib.SS_ERR_INVALID_ARG, "aligned"),
+])
+def test_scan_general_rejects_bad_arguments(kw, code, msg):
+    assert _gen(**kw) == code
+    assert msg in ss.ss_last_error()
+
+
+def _ssd(**kw):
+    a = dict(batch=1, seqlen=8, nheads=4, headdim=64, dstate=128, ngroups=2, in_dtype=1, out_dtype=1)
+    a.update({k: v for k, v in kw.items() if k in a})
+    p = [kw.get(k, v) for k, v in (("x", 0x1000), ("dt", 0x2000), ("A", 0x3000), ("B", 0x4000), ("C", 0x5000),
+                                   ("D", None), ("dt_bias", None), ("h0", None), ("y", 0x6000),
+                                   ("h_last", None))]
+    return ss.lib().ss_ssd_fwd(a["batch"], a["seqlen"], a["nheads"], a["headdim"], a["dstate"], a["ngroups"],
+                               a["in_dtype"], a["out_dtype"], *p, None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(in_dtype=0), _lib.SS_ERR_UNSUPPORTED, "bf16"),
+    (dict(headdim=128), _lib.SS_ERR_UNSUPPORTED, "headdim"),
+    (dict(dstate=16), _lib.SS_ERR_UNSUPPORTED, "dstate"),
+    (dict(ngroups=3), _lib.SS_ERR_INVALID_ARG, "multiple of ngroups"),
+    (dict(x=None), _lib.SS_ERR_INVALID_ARG, "x must not"),
+    (dict(dt=0x2002), _lib.SS_ERR_INVALID_ARG, "aligned"),
+])
+def test_ssd_rejects_bad_arguments(kw, code, msg):
+    assert _ssd(**kw) == code
+    assert msg in ss.ss_last_error()
+
+
+def test_new_entry_points_empty_problems_without_device():
+    assert _gen(batch=0) == _lib.SS_OK
+    assert _ssd(nheads=0) == _lib.SS_OK
