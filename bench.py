@@ -624,14 +624,14 @@ def run_ours(args, world, rank, local):
                          "path": "pinned host -> device copies, ss_scan_fwd, device -> pinned host copies"}
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_decode:
-        result["decode"] = bench_decode(ss, configs.C4, dev)
+        result["decode"] = bench_decode(ss, configs.DECODE256, dev)
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_extra:
         extra = {}
-        for name in ("c1", "c3"):
+        for name in ("mamba130m_layer", "dna_1m"):
             wc = configs.get_config(name)
             xc = gen.make_scan_inputs(wc)
-            reps = 10 if name == "c1" else 3
+            reps = 10 if name == "mamba130m_layer" else 3
             stc = bench_scan(ss, wc, xc, reps, 2, out_dtype, dev)
             torch.cuda.synchronize()
             run_timed(ss, stc, reps)
@@ -731,7 +731,7 @@ def profile_launches(args):
             out = ss.ss_scan_bwd(x["u"], x["delta_raw"], x["A"], x["B"], x["C"], dy, x["D"], x["z"],
                                  x["delta_bias"], None, dh, out=out, workspace=ws)
     else:
-        w = configs.C4
+        w = configs.DECODE256
         A, Dk, bias = (t.to(dev) for t in gen.make_params(w.prefix))
         st = {k: v.to(dev) for k, v in gen.make_decode_steps(w, 0, 2).items()}
         h = torch.zeros((w.streams, w.dim, 16), dtype=torch.float32, device=dev)
@@ -746,10 +746,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--workload", default="mamba2p8b_layer",
+                    help="tiny_fp32, mamba130m_layer, mamba2p8b_layer (default), dna_1m")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the c1 / c3 scan timings")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-config timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general", "ssd"], default=None,
                     help="run 2 launches of one kernel (for an ncu capture of the 2nd) and exit")

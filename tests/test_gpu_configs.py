@@ -32,17 +32,17 @@ def _check_sampled(w, x, y, h, out_bf16, nsample, seed):
     return e1, e2
 
 
-@pytest.mark.parametrize("name,nsample", [("c1", 48), ("c2", 48)])
+@pytest.mark.parametrize("name,nsample", [("mamba130m_layer", 48), ("mamba2p8b_layer", 48)])
 @pytest.mark.parametrize("out", [torch.float32, BF16])
 def test_layer_configs(name, nsample, out):
     w = configs.get_config(name)
     x = gen.make_scan_inputs(w)
     y, h = run_scan_dev(x, out)
-    _check_sampled(w, x, y, h, out == BF16, nsample, seed={"c1": 11, "c2": 22}[name])
+    _check_sampled(w, x, y, h, out == BF16, nsample, seed={"mamba130m_layer": 11, "mamba2p8b_layer": 22}[name])
 
 
 def test_dna_1m_config():
-    w = configs.C3
+    w = configs.DNA_1M
     x = gen.make_scan_inputs(w)
     assert ss.ss_scan_fwd_workspace_size(w.batch, w.seqlen, w.dim) > 0  # the cross-chunk carry path is used
     y, h = run_scan_dev(x, BF16)
@@ -50,7 +50,7 @@ def test_dna_1m_config():
 
 
 def test_decode_config():
-    w = configs.C4
+    w = configs.DECODE256
     pre = gen.make_scan_inputs(w.prefix)
     # prefix scan on the GPU gives the initial state of the 256 streams
     d = to_dev(pre)

@@ -73,7 +73,7 @@ def test_general_first_order_matches_scan():
 @pytest.mark.parametrize("N,G,disc", [(64, 1, "zoh"), (128, 8, "first_order")])
 def test_general_layer_sampled(N, G, disc):
     # Mamba-2.8B layer shape (4 x 2048 x 5120, bf16), larger state: sampled channels over the whole sequence
-    w = configs.C2
+    w = configs.MAMBA2P8B_LAYER
     x = gen.random_general_inputs(w.batch, w.seqlen, w.dim, N, G, in_dtype="bf16", seed=N + G)
     ch = sample_channels(w.batch, w.dim, 24, seed=N)
     yr, hr = oracle.scan_general(x, G, "zoh" if disc == "zoh" else "euler", channels=ch)

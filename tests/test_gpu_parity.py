@@ -20,7 +20,7 @@ def _dt(name):
 
 
 def test_config0_tiny_fp32_full():
-    x = gen.make_scan_inputs(configs.C0)
+    x = gen.make_scan_inputs(configs.TINY_FP32)
     x["h0"] = None
     yr, hr = oracle.scan(x)
     for sg in (1, 2):

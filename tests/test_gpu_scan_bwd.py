@@ -101,7 +101,7 @@ def _slice_channels(x, S):
 
 @pytest.fixture(scope="module")
 def layer():
-    x = gen.make_scan_inputs(configs.C2)
+    x = gen.make_scan_inputs(configs.MAMBA2P8B_LAYER)
     x["h0"] = None
     Bt, L, Dm = x["u"].shape
     S = sorted({0, 1, 31, 32, 63, 2047, 2048, 4000, Dm - 33, Dm - 2, Dm - 1})

@@ -45,7 +45,7 @@ def _worker(rank, world, port, out_dir):
     np.save(os.path.join(out_dir, f"t{rank}.npy"), np.array([t]))
     # weak scaling: each rank's own batch is seeded differently
     from workloads import configs
-    np.save(os.path.join(out_dir, f"s{rank}.npy"), np.array([bench.rank_seed(configs.C2, rank)]))
+    np.save(os.path.join(out_dir, f"s{rank}.npy"), np.array([bench.rank_seed(configs.MAMBA2P8B_LAYER, rank)]))
     dist.barrier()
     dist.destroy_process_group()
 

@@ -79,26 +79,20 @@ class DecodeWorkload:
         return b
 
 
-C0 = ScanWorkload("tiny_fp32", batch=1, seqlen=512, dim=256, dstate=16, in_dtype="f32",
-                  seed=0, delta_raw_scale=0.5, a_log_jitter=0.0)
-C1 = ScanWorkload("mamba130m_layer", batch=8, seqlen=2048, dim=1536, dstate=16, in_dtype="bf16",
-                  seed=1, delta_raw_scale=0.5, a_log_jitter=0.0)
-C2 = ScanWorkload("mamba2p8b_layer", batch=4, seqlen=2048, dim=5120, dstate=16, in_dtype="bf16",
-                  seed=2, delta_raw_scale=0.5, a_log_jitter=0.1)
-C3 = ScanWorkload("dna_1m", batch=1, seqlen=1 << 20, dim=1024, dstate=16, in_dtype="bf16",
-                  seed=3, delta_raw_scale=1.0, a_log_jitter=0.0, u_kind="alphabet4")
-C4_PREFIX = ScanWorkload("decode256_prefix", batch=256, seqlen=512, dim=5120, dstate=16,
-                         in_dtype="bf16", seed=40, delta_raw_scale=0.5, a_log_jitter=0.1)
-C4 = DecodeWorkload("decode256", streams=256, dim=5120, dstate=16, steps=1000,
-                    prefix=C4_PREFIX, in_dtype="bf16", seed=4, delta_raw_scale=1.0)
+TINY_FP32 = ScanWorkload("tiny_fp32", batch=1, seqlen=512, dim=256, dstate=16, in_dtype="f32",
+                         seed=0, delta_raw_scale=0.5, a_log_jitter=0.0)
+MAMBA130M_LAYER = ScanWorkload("mamba130m_layer", batch=8, seqlen=2048, dim=1536, dstate=16, in_dtype="bf16",
+                               seed=1, delta_raw_scale=0.5, a_log_jitter=0.0)
+MAMBA2P8B_LAYER = ScanWorkload("mamba2p8b_layer", batch=4, seqlen=2048, dim=5120, dstate=16, in_dtype="bf16",
+                               seed=2, delta_raw_scale=0.5, a_log_jitter=0.1)
+DNA_1M = ScanWorkload("dna_1m", batch=1, seqlen=1 << 20, dim=1024, dstate=16, in_dtype="bf16",
+                      seed=3, delta_raw_scale=1.0, a_log_jitter=0.0, u_kind="alphabet4")
+DECODE256_PREFIX = ScanWorkload("decode256_prefix", batch=256, seqlen=512, dim=5120, dstate=16,
+                                in_dtype="bf16", seed=40, delta_raw_scale=0.5, a_log_jitter=0.1)
+DECODE256 = DecodeWorkload("decode256", streams=256, dim=5120, dstate=16, steps=1000,
+                           prefix=DECODE256_PREFIX, in_dtype="bf16", seed=4, delta_raw_scale=1.0)
 
-CONFIGS = {
-    "c0": C0, "tiny_fp32": C0,
-    "c1": C1, "mamba130m_layer": C1,
-    "c2": C2, "mamba2p8b_layer": C2,
-    "c3": C3, "dna_1m": C3,
-    "c4": C4, "decode256": C4,
-}
+CONFIGS = {w.name: w for w in (TINY_FP32, MAMBA130M_LAYER, MAMBA2P8B_LAYER, DNA_1M, DECODE256)}
 
 
 def get_config(name: str):
