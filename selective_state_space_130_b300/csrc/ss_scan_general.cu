@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(32) scan_general_kernel(const __grid_constant_
   const int64_t c0 = (blk % p.ncblk) * CW;
   const int64_t d = c0 + ch;
   const bool dv = d < p.dim;
-  const int64_t dc = dv ? d : 0;
+  // lanes past the last channel stand in for the block's first channel, so
+  // their group row below is the warp's first staged one (never outside it)
+  const int64_t dc = dv ? d : c0;
   const int64_t L = p.seqlen, Dm = p.dim, G = p.ngroups;
   const int nch = (int)min((int64_t)CW, Dm - c0);
   // the groups this warp's channels span, and this lane's row among them

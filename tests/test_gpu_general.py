@@ -38,6 +38,8 @@ SHAPES = [
     ("bf16", 2, 21, 6, 128, 2, True, True, True, True),      # rows of 8 bytes: 4-byte copies
     ("f32", 1, 513, 130, 32, 2, True, True, True, True),
     ("bf16", 1, 1000, 96, 64, 4, True, True, True, True),
+    ("f32", 1, 20, 1000, 16, 1000, True, True, True, True),  # one B/C per channel, ragged last block at channel 992
+    ("bf16", 2, 30, 200, 32, 40, True, True, True, True),    # groups of 5 channels, ragged last block
 ]
 
 
