@@ -216,7 +216,17 @@ def bench_scan(ss, w, x, steps, warmup, out_dtype, dev, nsets=None):
                 launches_per_step=1)
 
 
+def prime_queue():
+    """Open a timed region behind a short device-side spin (2 M cycles, about
+    1 ms). While it runs the host queues the first timed launches, so their
+    launch latency is not counted as GPU time; every timed step's work still
+    runs inside the region. (With the GPU idle at the start event, the first
+    call of a batch measured 420-510 us against 224 us for the rest.)"""
+    torch.cuda._sleep(2_000_000)
+
+
 def run_timed(ss, st, steps):
+    prime_queue()
     st["t0"].record()
     for i in range(steps):
         k = i % st["nsets"]
@@ -339,6 +349,7 @@ def bench_conv1d(ss, dev, hbm_peak, Bt=4, L=2048, Dm=5120, K=4, reps=20):
         call(i)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    prime_queue()
     for i in range(reps):
         ev[i][0].record()
         call(i)
@@ -404,6 +415,7 @@ def bench_scan_bwd(ss, w, dev, hbm_peak, clock_mhz, reps=10):
         call(out)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    prime_queue()
     for i in range(reps):
         ev[i][0].record()
         call(out)
@@ -457,6 +469,7 @@ def bench_general(ss, w, dev, hbm_peak, clock_mhz, N, G, disc, reps=10):
         call()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    prime_queue()
     for i in range(reps):
         ev[i][0].record()
         call()
@@ -500,6 +513,7 @@ def bench_ssd(ss, dev, hbm_peak, tensor_peak, Bt=4, L=2048, H=80, N=128, G=1, re
         call()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    prime_queue()
     for i in range(reps):
         ev[i][0].record()
         call()
