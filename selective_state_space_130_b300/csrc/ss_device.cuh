@@ -98,45 +98,43 @@ __device__ __forceinline__ f2 add2(f2 a, f2 b) {
 }
 
 // ---------------------------------------------------------------- fast activations
-// softplus(x) = log(1 + e^x), from w = e^x:
-//   x > 20    : x (the correction log1p(e^-x) < 2.1e-9 is below half an ulp of x)
-//   w < 1/16  : series w - w^2/2 + w^3/3 - w^4/4 + w^5/5 - w^6/6 (truncation < w^7/7)
-//   otherwise : ln2 * log2(1 + w); 1 + w >= 1.0625 keeps the MUFU log2's absolute
-//               error a small relative one
+// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(v) with v = e^-|x| in (0, 1].
+// log1p(v) = v * q(v), where q is a degree-7 polynomial fitted (relative-error
+// least squares with reweighting, coefficients rounded to fp32) to
+// log1p(v) / v on [0, 1]; evaluated by Horner in fp32 its relative error is
+// below 3.3e-7 over the whole interval (fit_softplus.py beside this file
+// regenerates the coefficients and the bound). One MUFU ex2 and nine FMA-pipe
+// operations, against ex2 + lg2 on the MUFU pipe for the direct form. Large x
+// gives v -> 0 and exactly x; x below about -87 gives v = 0 (flushed) and 0.
+constexpr float kSp0 = 0.9999998211860657f, kSp1 = -0.4999740421772003f, kSp2 = 0.3327547609806061f,
+                kSp3 = -0.244954451918602f, kSp4 = 0.17745192348957062f, kSp5 = -0.10768099874258041f,
+                kSp6 = 0.04408911243081093f, kSp7 = -0.00853906013071537f;
+
 __device__ __forceinline__ float softplus_fast(float x) {
-  const float w = ex2(x * kLog2e);
-  float p = fmaf(w, -1.f / 6.f, 0.2f);
-  p = fmaf(w, p, -0.25f);
-  p = fmaf(w, p, 1.f / 3.f);
-  p = fmaf(w, p, -0.5f);
-  p = fmaf(w, p, 1.f);
-  const float series = w * p;
-  float lg;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(1.f + w));
-  const float r = w < 0.0625f ? series : lg * kLn2;
-  return x > 20.f ? x : r;
+  const float v = ex2(-fabsf(x) * kLog2e);
+  float q = fmaf(v, kSp7, kSp6);
+  q = fmaf(v, q, kSp5);
+  q = fmaf(v, q, kSp4);
+  q = fmaf(v, q, kSp3);
+  q = fmaf(v, q, kSp2);
+  q = fmaf(v, q, kSp1);
+  q = fmaf(v, q, kSp0);
+  return fmaf(v, q, fmaxf(x, 0.f));
 }
 
-// softplus_fast for two values at once: the polynomial, the scaling and the
-// additions run as packed f32x2 operations; the exponentials, logarithms and
-// selections stay per value. Same formula and constants as softplus_fast.
+// softplus_fast for two values at once: the polynomial runs as packed f32x2
+// operations; the exponentials and the max stay per value.
 __device__ __forceinline__ f2 softplus_fast2(f2 x) {
   const f2 xl = mul2(x, pk(kLog2e, kLog2e));
-  const f2 w = pk(ex2(f2lo(xl)), ex2(f2hi(xl)));
-  f2 p = fma2(w, pk(-1.f / 6.f, -1.f / 6.f), pk(0.2f, 0.2f));
-  p = fma2(w, p, pk(-0.25f, -0.25f));
-  p = fma2(w, p, pk(1.f / 3.f, 1.f / 3.f));
-  p = fma2(w, p, pk(-0.5f, -0.5f));
-  p = fma2(w, p, pk(1.f, 1.f));
-  const f2 series = mul2(w, p);
-  const f2 w1 = add2(w, pk(1.f, 1.f));
-  float l0, l1;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l0) : "f"(f2lo(w1)));
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l1) : "f"(f2hi(w1)));
-  const f2 lg = mul2(pk(l0, l1), pk(kLn2, kLn2));
-  const float r0 = f2lo(w) < 0.0625f ? f2lo(series) : f2lo(lg);
-  const float r1 = f2hi(w) < 0.0625f ? f2hi(series) : f2hi(lg);
-  return pk(f2lo(x) > 20.f ? f2lo(x) : r0, f2hi(x) > 20.f ? f2hi(x) : r1);
+  const f2 v = pk(ex2(-fabsf(f2lo(xl))), ex2(-fabsf(f2hi(xl))));
+  f2 q = fma2(v, pk(kSp7, kSp7), pk(kSp6, kSp6));
+  q = fma2(v, q, pk(kSp5, kSp5));
+  q = fma2(v, q, pk(kSp4, kSp4));
+  q = fma2(v, q, pk(kSp3, kSp3));
+  q = fma2(v, q, pk(kSp2, kSp2));
+  q = fma2(v, q, pk(kSp1, kSp1));
+  q = fma2(v, q, pk(kSp0, kSp0));
+  return fma2(v, q, pk(fmaxf(f2lo(x), 0.f), fmaxf(f2hi(x), 0.f)));
 }
 
 // silu for two values: z / (1 + e^-z), the scalings and additions packed
