@@ -66,8 +66,9 @@ def build(force=False, verbose=False, out=LIB, jobs=0):
         for _, log in results:
             sys.stderr.write(log)
     objs = [o for o, _ in results]
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64", *objs,
-           "-o", out]
+    # no rpath: libcudart.so.13 is found through the loader's search path, or is
+    # already loaded by the host process (PyTorch), which this library then shares
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", out]
     subprocess.run(cmd, check=True)
     return out
 

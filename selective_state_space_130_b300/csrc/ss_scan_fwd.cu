@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "ss_scan_fwd_kernel.cuh"
 
 namespace ssk {
@@ -31,18 +33,22 @@ int scan_warps_per_sm(ss_dtype in_dtype, int sg) {
   return blocks * scan_detail::kWarps;
 }
 
+// The fault word's device address, resolved once per device (with that device
+// current) and cached per device under a mutex: host threads that drive
+// different GPUs each get their own device's address.
 unsigned int* device_fault_word() {
-  static unsigned int* ptr = nullptr;
-  static int dev_cached = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!ptr || dev != dev_cached) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static unsigned int* cache[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
     void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_fault_word) != cudaSuccess) return nullptr;
-    ptr = static_cast<unsigned int*>(a);
-    dev_cached = dev;
+    if (cudaGetSymbolAddress(&a, g_fault_word) != cudaSuccess || !a) return nullptr;
+    cache[dev] = static_cast<unsigned int*>(a);
   }
-  return ptr;
+  return cache[dev];
 }
 
 cudaError_t launch_scan_fwd(const ScanParams& p, const ScanPlan& plan, ss_dtype in_dtype, ss_dtype out_dtype,
