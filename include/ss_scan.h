@@ -294,14 +294,29 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
 /*
  * Launch-shape controls for the calling host thread (0 = automatic, the
  * default, for each). threads_per_channel in {1, 2} sets how many threads share
- * one channel's 16 states. chunk_len > 0 forces the sequence to be split into
- * chunks of that many timesteps (rounded up to the 32-step tile), which engages
- * the cross-block carry path. warps_per_scheduler in {1..4} sets how many warps
- * the scan aims to keep on each SM sub-partition when it splits the work into
- * equal ranges. Results do not depend on these settings beyond fp32 rounding;
+ * one channel's 16 states (a CTA then covers 128 or 64 channels). chunk_len > 0
+ * forces the sequence to be split into chunks of that many timesteps (rounded
+ * up to the tile: 64 steps for bf16 inputs, 32 for float32), which engages the
+ * cross-CTA carry path. max_workers > 0 caps the number of CTAs a split of the
+ * work uses (default: one per SM), which makes range boundaries and hand-overs
+ * more frequent. Results do not depend on these settings beyond fp32 rounding;
  * ss_scan_fwd_workspace_size() follows them.
  */
-void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int warps_per_scheduler);
+void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_workers);
+
+/*
+ * Fault-path controls of ss_scan_fwd for the calling host thread (no
+ * counterpart on the pages; they exist to test the bounded device-side waits).
+ * wait_ns is the limit of every device-side wait of later scans (0 restores
+ * the default of 2 s). withhold_item >= 0 makes the scan never publish one
+ * cross-CTA flag: the hand-over into stream-K worker `withhold_item`, or the
+ * carry of chunk item `withhold_item` (block * nchunks + chunk) in the chunked
+ * split; -1 (the default) publishes all. A withheld flag makes the CTAs that
+ * need it give up after wait_ns, set the fault word and return, so the call
+ * finishes and ss_scan_status() reports SS_ERR_TIMEOUT; its outputs are then
+ * undefined. No wait in the library is unbounded.
+ */
+void ss_scan_set_wait_limit(uint64_t wait_ns, int64_t withhold_item);
 
 /*
  * Selective scan forward that allocates nothing (no counterpart on the pages:

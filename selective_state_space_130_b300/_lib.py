@@ -44,6 +44,7 @@ SIGNATURES = {
                             + [_P] * 11 + [_P]),
     "ss_ssd_fwd": (ctypes.c_int, [_I64] * 6 + [ctypes.c_int, ctypes.c_int] + [_P] * 10 + [_P]),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
+    "ss_scan_set_wait_limit": (None, [ctypes.c_uint64, _I64]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
 }
 
@@ -117,8 +118,12 @@ def ss_last_error() -> str:
     return lib().ss_last_error().decode()
 
 
-def ss_scan_set_tuning(threads_per_channel: int = 0, chunk_len: int = 0, warps_per_scheduler: int = 0):
-    lib().ss_scan_set_tuning(int(threads_per_channel), int(chunk_len), int(warps_per_scheduler))
+def ss_scan_set_tuning(threads_per_channel: int = 0, chunk_len: int = 0, max_workers: int = 0):
+    lib().ss_scan_set_tuning(int(threads_per_channel), int(chunk_len), int(max_workers))
+
+
+def ss_scan_set_wait_limit(wait_ns: int = 0, withhold_item: int = -1):
+    lib().ss_scan_set_wait_limit(int(wait_ns), int(withhold_item))
 
 
 def ss_scan_fwd_workspace_size(batch, seqlen, dim, dstate=16) -> int:

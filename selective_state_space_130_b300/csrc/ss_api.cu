@@ -17,12 +17,13 @@ namespace {
 thread_local std::string g_err;
 thread_local int g_tune_sg = 0;           // 0 = automatic
 thread_local int64_t g_tune_chunk = 0;    // 0 = automatic
-thread_local int g_tune_wps = 0;          // warps per SM sub-partition; 0 = automatic
+thread_local int g_tune_workers = 0;      // cap on the CTAs a split uses; 0 = one per SM
+thread_local uint64_t g_wait_ns = 2000000000ull;  // limit of the scan's device-side waits
+thread_local int64_t g_withhold = -1;     // test knob: hand-over or chunk flag never published
 
-constexpr int kVersion = 10100;  // 1.1.0
-constexpr int kSMs = 148;
-constexpr int kSchedulers = kSMs * 4;  // SM sub-partitions (warp schedulers)
-constexpr int64_t kMinChunk = 8192;    // shortest sequence chunk of the chunked mode
+constexpr int kVersion = 10200;  // 1.2.0
+constexpr int kDefaultSMs = 148;  // B300, when the device cannot be queried
+constexpr int64_t kMinChunk = 8192;  // shortest sequence chunk of the chunked mode
 
 ss_status fail(ss_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ss_status fail(ss_status st, const char* fmt, ...) {
@@ -73,7 +74,7 @@ bool valid_dtype(int t) { return t == SS_F32 || t == SS_BF16; }
 // once there are several warps per sub-partition anyway.
 int bwd_lanes_per_channel(int64_t batch, int64_t dim) {
   if (g_tune_sg == 1 || g_tune_sg == 2) return g_tune_sg;
-  return batch * ((dim + 31) / 32) >= 3 * (int64_t)kSchedulers ? 1 : 2;
+  return batch * ((dim + 31) / 32) >= 3 * 4 * (int64_t)ssk::device_sm_count() ? 1 : 2;
 }
 size_t dsize(ss_dtype t) { return t == SS_BF16 ? 2 : 4; }
 
@@ -81,42 +82,69 @@ size_t dsize(ss_dtype t) { return t == SS_BF16 ? 2 : 4; }
 
 namespace ssk {
 
-ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype) {
+int device_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int cache[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kDefaultSMs;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kDefaultSMs;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Relative cost of one token of one channel block (CTA cycles per token, from
+// the measured token loops on B300): one lane per channel runs 128 channels in
+// about 148 cycles, two lanes per channel 64 channels in about 87.
+static double block_token_cost(int sg) { return sg == 1 ? 148.0 : 87.0; }
+
+ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype, int sms) {
   ScanPlan pl{};
+  const int64_t W = g_tune_workers > 0 ? std::min<int64_t>(sms, g_tune_workers) : sms;  // CTA slots (one per SM)
+  const bool chunkable = seqlen >= 2 * kMinChunk;
   int sg = g_tune_sg;
-  // one lane per channel costs the fewest instructions per state update; two
-  // lanes per channel halve each lane's work, which pays only when there are
-  // too few channel blocks to give every other SM sub-partition a warp and the
-  // sequence is too short to be split into chunks
-  if (sg != 1 && sg != 2)
-    sg = (batch * ((dim + 31) / 32) >= kSchedulers / 2 || seqlen >= 2 * kMinChunk) ? 1 : 2;
+  if (sg != 1 && sg != 2) {
+    // the layout with the smaller estimated makespan: one lane per channel
+    // needs fewer instructions per state update; two lanes per channel give
+    // twice the channel blocks, which pays when one-lane blocks cannot fill
+    // every SM and the sequence is too short to be split into chunks
+    double best = 0.0;
+    for (int cand = 1; cand <= 2; cand++) {
+      const int64_t nb = batch * ((dim + scan_channels_per_block(cand) - 1) / scan_channels_per_block(cand));
+      const double waves = (nb >= W || chunkable) ? (double)nb / (double)W : 1.0;
+      const double est = waves * block_token_cost(cand);
+      if (cand == 1 || est < best) {
+        best = est;
+        sg = cand;
+      }
+    }
+  }
   pl.sg = sg;
-  pl.cblk = scan_channels_per_warp(sg);
+  pl.cblk = scan_channels_per_block(sg);
   const int tile = scan_tile_len(in_dtype, sg);
   pl.tile = tile;
   const int64_t ncblk = (dim + pl.cblk - 1) / pl.cblk;
   const int64_t nblk = batch * ncblk;
   const int64_t T = seqlen > 0 ? (seqlen + tile - 1) / tile : 1;
-  const int wps = (g_tune_wps >= 1 && g_tune_wps <= 4) ? g_tune_wps : 2;
-  const int64_t target = (int64_t)kSMs * std::min(scan_warps_per_sm(in_dtype, sg), 4 * wps);
   pl.mode = kModeStatic;
   pl.nworkers = nblk;
   pl.chunk_tiles = T;
   pl.nchunks = 1;
   if (g_tune_chunk > 0) {
     pl.chunk_tiles = std::max<int64_t>(1, (g_tune_chunk + tile - 1) / tile);
-  } else if (nblk >= kSchedulers) {
-    // equal ranges for a multiple of the scheduler count; at least one block
-    // per range keeps every hand-over one level deep
-    const int64_t g = std::min(target, (nblk / kSchedulers) * kSchedulers);
-    if (g < nblk) {
-      pl.mode = kModeStreamK;
-      pl.nworkers = g;
-    }
-  } else if (seqlen >= 2 * kMinChunk) {
-    // as many chunks as keep every warp resident at once (a chunk waits only
+  } else if (nblk > W) {
+    // equal ranges, one per CTA slot; at least one block per range keeps every
+    // hand-over one level deep
+    pl.mode = kModeStreamK;
+    pl.nworkers = W;
+  } else if (chunkable) {
+    // as many chunks as keep every CTA resident at once (a chunk waits only
     // for earlier chunks, but a second wave would double the makespan)
-    int64_t k = std::max<int64_t>(1, target / nblk);
+    int64_t k = std::max<int64_t>(1, W / nblk);
     k = std::min<int64_t>(k, seqlen / kMinChunk);
     pl.chunk_tiles = (T + k - 1) / k;
   }
@@ -194,7 +222,7 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last", "workspace"};
   for (int i = 0; i < 12; i++)
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
-  const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim, in_dtype);
+  const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim, in_dtype, ssk::device_sm_count());
   if (seqlen > 0 && plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) {
     if (noalloc)
       return fail(SS_ERR_INVALID_ARG,
@@ -230,6 +258,8 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   p.batch = batch;
   p.seqlen = seqlen;
   p.dim = dim;
+  p.wait_ns = g_wait_ns;
+  p.withhold_item = g_withhold;
   if ((double)plan.nworkers > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
   size_t clear = ssk::scan_bind_workspace(p, plan, plan.workspace > 0 ? workspace : nullptr);
   // The fault word: the workspace header when the caller gave a workspace (so
@@ -267,16 +297,22 @@ int ss_version(void) { return kVersion; }
 
 const char* ss_last_error(void) { return g_err.c_str(); }
 
-void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int warps_per_scheduler) {
+void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_workers) {
   g_tune_sg = threads_per_channel;
   g_tune_chunk = chunk_len;
-  g_tune_wps = warps_per_scheduler;
+  g_tune_workers = max_workers;
+}
+
+void ss_scan_set_wait_limit(uint64_t wait_ns, int64_t withhold_item) {
+  g_wait_ns = wait_ns > 0 ? wait_ns : 2000000000ull;
+  g_withhold = withhold_item;
 }
 
 size_t ss_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
   if (batch <= 0 || seqlen <= 0 || dim <= 0 || dstate != ssk::kDState) return 0;
-  return std::max(ssk::plan_scan(batch, seqlen, dim, SS_F32).workspace,
-                  ssk::plan_scan(batch, seqlen, dim, SS_BF16).workspace);
+  const int sms = ssk::device_sm_count();
+  return std::max(ssk::plan_scan(batch, seqlen, dim, SS_F32, sms).workspace,
+                  ssk::plan_scan(batch, seqlen, dim, SS_BF16, sms).workspace);
 }
 
 ss_status ss_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
@@ -659,7 +695,7 @@ extern "C" ss_status ss_scan_fwd_noalloc(int64_t batch, int64_t seqlen, int64_t 
   g_err.clear();
   // sizes beyond the fixed scratch are refused before any device call
   if (batch > 0 && seqlen > 0 && dim > 0 && dstate == ssk::kDState && valid_dtype(in_dtype)) {
-    const size_t need = ssk::plan_scan(batch, seqlen, dim, in_dtype).workspace;
+    const size_t need = ssk::plan_scan(batch, seqlen, dim, in_dtype, ssk::device_sm_count()).workspace;
     if (need > (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES)
       return fail(SS_ERR_INVALID_ARG,
                   "this problem needs %zu bytes of scratch; the no-allocation scan holds at most %zu (use ss_scan_fwd "

@@ -11,7 +11,8 @@ namespace ssk {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 
-// Timeout of every device-side wait (nanoseconds of %globaltimer).
+// Default limit of a device-side wait (nanoseconds of %globaltimer); the scan
+// takes its limit per call (ScanParams::wait_ns).
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // Fault codes written to the fault word.
@@ -184,14 +185,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for phase `parity` of `bar`; false if it did not complete in
-// kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait for phase `parity` of `bar`; false if it did not complete
+// within limit_ns nanoseconds of %globaltimer.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 

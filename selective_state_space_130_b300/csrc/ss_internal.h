@@ -13,10 +13,10 @@ namespace ssk {
 
 constexpr int kDState = 16;
 
-// How the (channel block, 32-step tile) work of one scan is split among warps.
+// How the (channel block, tile) work of one scan is split among CTAs.
 enum ScanMode : int {
-  kModeStatic = 0,   // one warp per channel block, whole sequence; no workspace
-  kModeStreamK = 1,  // contiguous equal ranges of the tile space per warp; states
+  kModeStatic = 0,   // one CTA per channel block, whole sequence; no workspace
+  kModeStreamK = 1,  // contiguous equal ranges of the tile space per CTA; states
                      // handed over at block-interior range boundaries
   kModeChunked = 2   // sequence chunks per block, carries combined by look-back
 };
@@ -40,12 +40,15 @@ struct ScanParams {
   float* ws_carry;          // stream-K: handed-over states [worker][channel][16];
                             // chunked: per (block, chunk, channel) P[16], S_local[16], S_incl[16]
   unsigned int* fault;      // fault word (workspace header or the library's own)
+  uint64_t wait_ns;         // limit of every device-side wait
+  int64_t withhold_item;    // test knob: the hand-over (stream-K worker) or chunk whose
+                            // flag is never published (-1: none)
   int64_t batch, seqlen, dim;
   int mode;                 // ScanMode
   int ncblk;                // channel blocks per batch element
   int64_t nblk;             // batch * ncblk
   int64_t tiles_per_blk;    // ceil(seqlen / tile)
-  int64_t nworkers;         // warps with work (stream-K: ranges; chunked: nblk * nchunks)
+  int64_t nworkers;         // CTAs (static: nblk; stream-K: ranges; chunked: nblk * nchunks)
   int64_t chunk_tiles;      // chunked: tiles per chunk
   int nchunks;              // chunked: chunks per block
 };
@@ -149,15 +152,19 @@ struct SsdParams {
 struct ScanPlan {
   int sg;               // threads per channel (1 or 2); each owns 16/sg states
   int tile;             // timesteps per tile
-  int cblk;             // channels per warp
+  int cblk;             // channels per CTA (channel block)
   int mode;             // ScanMode
-  int64_t nworkers;     // warps with work
+  int64_t nworkers;     // CTAs with work
   int64_t chunk_tiles;  // chunked mode: tiles per chunk
   int nchunks;          // chunked mode: chunks per block
   size_t workspace;     // bytes of workspace needed
 };
 
-ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype);
+// Plan for `sms` streaming multiprocessors (one CTA per SM at a time).
+ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype, int sms);
+// SM count of the current device (cached per device), or a default when it
+// cannot be queried.
+int device_sm_count();
 
 // Fill the schedule fields of `p` from `plan` and carve `workspace` (at least
 // plan.workspace bytes, may be null when that is 0). Returns the number of
@@ -169,12 +176,10 @@ cudaError_t launch_scan_fwd(const ScanParams& p, const ScanPlan& plan, ss_dtype 
                             bool use_tma, cudaStream_t stream);
 
 // Shape constants of the scan kernels.
-int scan_channels_per_warp(int sg);
+int scan_channels_per_block(int sg);           // channels per CTA
 int scan_tile_len(ss_dtype in_dtype, int sg);  // timesteps per tile
-int scan_warps_per_block();
 int scan_header_words();
 uint32_t scan_header_magic();
-int scan_warps_per_sm(ss_dtype in_dtype, int sg);  // resident warps per SM allowed by shared memory
 cudaError_t launch_state_update(const StepParams& p, ss_dtype in_dtype, ss_dtype out_dtype, cudaStream_t stream);
 cudaError_t launch_conv1d_fwd(const ConvParams& p, ss_dtype in_dtype, ss_dtype out_dtype, bool vec,
                               cudaStream_t stream);

@@ -13,25 +13,17 @@ namespace ssk {
 // Fault word used by calls that are given no workspace.
 __device__ unsigned int g_fault_word = 0;
 
-int scan_channels_per_warp(int sg) { return 32 / sg; }
+int scan_channels_per_block(int sg) {
+  using scan_detail::Cfg;
+  return sg == 1 ? Cfg<float, 1>::CC : Cfg<float, 2>::CC;
+}
 int scan_tile_len(ss_dtype in_dtype, int sg) {
   using scan_detail::Cfg;
   if (in_dtype == SS_BF16) return sg == 1 ? Cfg<__nv_bfloat16, 1>::TILE : Cfg<__nv_bfloat16, 2>::TILE;
   return sg == 1 ? Cfg<float, 1>::TILE : Cfg<float, 2>::TILE;
 }
-int scan_warps_per_block() { return scan_detail::kWarps; }
 int scan_header_words() { return scan_detail::kHeaderWords; }
 uint32_t scan_header_magic() { return scan_detail::kHeaderMagic; }
-
-int scan_warps_per_sm(ss_dtype in_dtype, int sg) {
-  using scan_detail::Cfg;
-  int blocks;
-  if (in_dtype == SS_BF16)
-    blocks = sg == 1 ? Cfg<__nv_bfloat16, 1>::BLOCKS_PER_SM : Cfg<__nv_bfloat16, 2>::BLOCKS_PER_SM;
-  else
-    blocks = sg == 1 ? Cfg<float, 1>::BLOCKS_PER_SM : Cfg<float, 2>::BLOCKS_PER_SM;
-  return blocks * scan_detail::kWarps;
-}
 
 // The fault word's device address, resolved once per device (with that device
 // current) and cached per device under a mutex: host threads that drive

@@ -1,49 +1,48 @@
 // Selective-scan (S6) forward kernel for sm_103a (template; instantiated per
 // input/output dtype pair in ss_scan_fwd_<in>_<out>.cu).
 //
-// What one warp computes. A warp owns DC = 32/SG consecutive channels of one
-// batch element (a "channel block"). With SG = 1 each lane owns one channel and
-// all 16 of its fp32 states; with SG = 2 two lanes share a channel, 8 states
-// each. Per token the lane computes delta = softplus(delta_raw + bias),
-// Abar = 2^(delta * A * log2 e), h = Abar*h + (delta*u)*B, y = C.h + D*u and
-// y *= silu(z): the fused, SRAM-resident scan the Mamba pages describe (review
-// page, method step 2; "Transformer时代终结？" section 二.3), laid out for B300.
-// The state update runs on packed f32x2 FMUL2/FFMA2 (two states per issue
-// slot); the exponentials run on the MUFU pipe. On B300 that pair of pipes,
-// not HBM, bounds the exact fp32 recurrence: about 30 state updates per clock
-// per SM at best against 4 bytes of HBM traffic per 16 updates.
+// What a thread computes. A CTA of kWarps warps owns CC consecutive channels
+// of one batch element (a "channel block"); each warp owns DC = 32/SG of them.
+// With SG = 1 each lane owns one channel and all 16 of its fp32 states; with
+// SG = 2 two lanes share a channel, 8 states each. Per token a channel's
+// delta = softplus(delta_raw + bias), Abar = 2^(delta * A * log2 e),
+// h = Abar*h + (delta*u)*B, y = C.h + D*u and y *= silu(z): the fused,
+// SRAM-resident scan the Mamba pages describe (review page, method step 2;
+// "Transformer时代终结？" section 二.3), laid out for B300. The state update runs
+// on packed f32x2 FMUL2/FFMA2 (two states per instruction); the exponentials
+// run on the MUFU pipe. On B300 these two pipes, not HBM, bound the exact fp32
+// recurrence.
 //
-// Data path. Tiles of TILE timesteps stream through a kStages-deep ring in
-// the warp's shared memory: u, delta_raw, z ([TILE, DC] boxes) and the tile's
-// B and C rows ([TILE, 16]) arrive by TMA (cp.async.bulk.tensor) with
-// completion counted on one mbarrier per stage, issued by the warp itself
-// kStages-1 tiles ahead. bf16 B/C rows are widened once per tile into an fp32
-// buffer read by broadcast. Only y and the final state leave the chip. A
-// block holds kWarps independent warps (one per SM sub-partition).
+// Data path. The CTA streams tiles of TILE timesteps through a two-stage ring
+// in shared memory: u, delta_raw, z ([TILE, CC] boxes) and the tile's B and C
+// rows ([TILE, 16]) arrive by TMA (cp.async.bulk.tensor), issued by one thread
+// a tile ahead, with completion counted on one mbarrier per stage. bf16 B/C
+// rows are widened once per tile into fp32 (each warp a quarter) and read by
+// broadcast. One CTA-wide barrier per tile orders the widening and frees the
+// stage the next load overwrites. Only y and the final state leave the chip.
 //
-// Work split (ScanMode).
-//  - static: one warp per channel block, the whole sequence.
+// Work split (ScanMode), in units of (channel block, tile):
+//  - static: one CTA per channel block, the whole sequence.
 //  - stream-K: the (channel block, tile) space, block-major, is cut into
 //    nworkers equal contiguous ranges, at least one block long each, so a range
-//    crosses at most one block start in its interior... and holds at most one
-//    partial block at either end. A warp first runs the head of the block its
-//    range ends in (from that block's initial state) and hands the state at
-//    its range end to the next warp, then runs the rest of its range in order;
-//    the first segment, when it starts inside a block, waits for the state the
-//    previous warp handed over (almost always already there). Equal ranges keep
-//    every SM sub-partition equally busy whatever the channel count.
+//    holds at most one partial block at either end. A CTA first runs the head
+//    of the block its range ends in (from that block's initial state) and hands
+//    the state at its range end to the next CTA, then runs the rest of its
+//    range in order; the first segment, when it starts inside a block, waits
+//    for the state the previous CTA handed over (almost always already there).
 //  - chunked (long sequences, few channel blocks): each block's sequence is
-//    cut into chunks run by different warps. A chunk's carry pair
+//    cut into chunks run by different CTAs. A chunk's carry pair
 //    (P = prod Abar = exp(A * sum delta), S = state reached from zero) composes
 //    as (P1,S1) o (P2,S2) = (P1 P2, P2 S1 + S2) ("外文文献精读" section 2.2;
 //    mlqm.cn tutorial section 6). Chunks publish their pair and resolve their
 //    incoming state by decoupled look-back, then recompute their head from the
-//    true state until, for every state n, the carried-in part P_t,n * h_in,n is
-//    at most 2^-24 of h_t,n (for A <= 0 it only decays further): the outputs
-//    equal the sequential recurrence up to fp32 rounding.
-// Warps take their worker index from a ticket counter in launch order, so a
-// warp only ever waits for warps that have already started; every wait is
-// bounded and reports a timeout through the fault word.
+//    true state until, for every state of every channel of the block, the
+//    carried-in part P_t,n * h_in,n is at most 2^-24 of h_t,n (for A <= 0 it only
+//    decays further): the outputs equal the sequential recurrence up to fp32
+//    rounding.
+// CTAs take their worker index from a ticket counter in launch order, so a CTA
+// only ever waits for CTAs that have already started; every wait is bounded
+// (p.wait_ns) and reports a timeout through the fault word.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -55,10 +54,8 @@
 namespace ssk {
 namespace scan_detail {
 
-constexpr int kTile = 32;    // timesteps per pipeline stage (64 for bf16 one-lane channels)
-constexpr int kStages = 3;   // TMA ring depth
-constexpr int kWarps = 4;    // warps (independent workers) per block
-constexpr int kUnroll = 8;   // tokens per step of the token loop (written out by hand below)
+constexpr int kWarps = 4;    // warps per CTA (one per SM sub-partition)
+constexpr int kStages = 2;   // TMA ring depth (the next tile loads while one is computed)
 constexpr float kStopRel = 5.9604645e-8f;  // 2^-24
 
 constexpr uint32_t kFlagAggregate = 1u;
@@ -66,28 +63,47 @@ constexpr uint32_t kFlagInclusive = 2u;
 constexpr uint32_t kFlagHanded = 1u;
 constexpr int kHeaderWords = 64;
 constexpr uint32_t kHeaderMagic = 0x53535753u;  // header word 2: "this call used the workspace"
-constexpr int kSmemPerSM = 233472;              // 228 KiB per SM, 1 KiB of it reserved per block
 
 template <typename TIn, int SG>
 struct Cfg {
   static constexpr int NS = kDState / SG;  // states per lane
   static constexpr int NP = NS / 2;        // packed state pairs per lane
   static constexpr int DC = 32 / SG;       // channels per warp
+  static constexpr int CC = kWarps * DC;   // channels per CTA (channel block)
   static constexpr bool BF = sizeof(TIn) == 2;
-  // timesteps per tile: the bf16 one-lane-per-channel layout fits 64 in the
-  // shared memory of four warps per SM, halving the per-tile ring overhead
-  static constexpr int TILE = (BF && SG == 1) ? 2 * kTile : kTile;
-  static constexpr int XB = TILE * DC * (int)sizeof(TIn);         // one u / delta_raw / z tile
-  static constexpr int RB = TILE * kDState * (int)sizeof(TIn);    // one raw B or C tile
+  static constexpr int TILE = BF ? 64 : 32;                          // timesteps per tile
+  static constexpr int XB = TILE * CC * (int)sizeof(TIn);           // one u / delta_raw / z tile
+  static constexpr int RB = TILE * kDState * (int)sizeof(TIn);      // one raw B or C tile
   static constexpr int OFF_U = 0, OFF_DR = XB, OFF_Z = 2 * XB, OFF_B = 3 * XB, OFF_C = 3 * XB + RB;
   static constexpr int STAGE = (3 * XB + 2 * RB + 127) & ~127;
-  static constexpr int OFF_BCF = kStages * STAGE;                  // fp32 B|C of the current tile (bf16 only)
-  static constexpr int BCF = BF ? 2 * TILE * kDState * 4 : 0;
-  static constexpr int OFF_BAR = OFF_BCF + BCF;
-  static constexpr int WARP_SMEM = (OFF_BAR + kStages * 8 + 127) & ~127;
-  static constexpr int SMEM = kWarps * WARP_SMEM + 128;            // + base alignment slack
-  static constexpr int BLOCKS_PER_SM = kSmemPerSM / (SMEM + 1024);
+  // fp32 B|C per stage (bf16 inputs): row t holds B[t][16] then C[t][16]
+  static constexpr int BCF = BF ? TILE * 2 * kDState * 4 : 0;
+  static constexpr int OFF_BCF = kStages * STAGE;
+  static constexpr int OFF_BAR = OFF_BCF + kStages * BCF;
+  static constexpr int SMEM = OFF_BAR + kStages * 8 + 128;           // + base alignment slack
 };
+
+// Widen this thread's share of a bf16 B and C tile ([TILE][16] each,
+// contiguous) into the fp32 [TILE][B 16 | C 16] layout.
+template <int TILE>
+__device__ __forceinline__ void widen_bc(const uint8_t* raw_b, float* bcf, int tid) {
+  // one item = 4 consecutive bf16 of B or C (8 bytes) -> 16 bytes of fp32
+  constexpr int ITEMS = 2 * TILE * kDState / 4;
+  constexpr int PER = ITEMS / (32 * kWarps);
+  static_assert(ITEMS % (32 * kWarps) == 0, "widening share");
+  const uint2* src = reinterpret_cast<const uint2*>(raw_b);
+#pragma unroll
+  for (int k = 0; k < PER; k++) {
+    const int i = k * 32 * kWarps + tid;  // item i: tensor i / (TILE*4), row (i / 4) % TILE, quarter i % 4
+    const int which = i / (TILE * 4);
+    const int rem = i - which * TILE * 4;
+    const int row = rem >> 2, qtr = rem & 3;
+    const uint2 v = src[i];
+    reinterpret_cast<float4*>(bcf + row * 32 + which * 16)[qtr] =
+        make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u), __uint_as_float(v.y << 16),
+                    __uint_as_float(v.y & 0xffff0000u));
+  }
+}
 
 template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, int MODE>
 __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_constant__ ScanParams p,
@@ -97,50 +113,48 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
                                                                   const __grid_constant__ CUtensorMap tm_b,
                                                                   const __grid_constant__ CUtensorMap tm_c) {
   using K = Cfg<TIn, SG>;
-  constexpr int NS = K::NS, NP = K::NP, DC = K::DC, TILE = K::TILE;
+  constexpr int NS = K::NS, NP = K::NP, DC = K::DC, CC = K::CC, TILE = K::TILE;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // 128-byte aligned base, derived from the shared array by pointer arithmetic
   // only (a round trip through an integer would hide from the compiler that
   // every tile access is a shared-memory access)
   const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
-  uint8_t* smem = smem_raw + pad + warp * K::WARP_SMEM;
+  uint8_t* smem = smem_raw + pad;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
-  const int s = lane % SG;   // which part of the channel's states this lane holds
-  const int cw = lane / SG;  // channel within the warp's block
+  __shared__ uint32_t s_wid;
+  __shared__ uint32_t s_flag;
+  const int s = lane % SG;        // which part of the channel's states this lane holds
+  const int cw = lane / SG;       // channel within the warp
+  const int cb = warp * DC + cw;  // channel within the CTA's block
   const int n0 = s * NS;
 
-  // ---- worker index
-  int64_t wid;
-  if constexpr (MODE == kModeStatic) {
-    wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
-  } else {
-    uint32_t t = 0;
-    if (lane == 0) t = atomicAdd(p.ws_header, 1u);  // launch-order ticket
-    wid = __shfl_sync(FULL, t, 0);
-  }
-  if (wid >= p.nworkers) return;
-  if (lane == 0) {
+  // ---- worker index (launch-order ticket in the split modes)
+  if (tid == 0) {
+    s_wid = MODE == kModeStatic ? blockIdx.x : atomicAdd(p.ws_header, 1u);
     for (int i = 0; i < kStages; i++) mbar_init(&full[i], 1);
     fence_mbar_init();
-    if (p.ws_header && wid == 0) p.ws_header[2] = kHeaderMagic;
+    if (TMA) {
+      tma_prefetch_desc(&tm_u);
+      tma_prefetch_desc(&tm_dr);
+      if (HAS_Z) tma_prefetch_desc(&tm_z);
+      tma_prefetch_desc(&tm_b);
+      tma_prefetch_desc(&tm_c);
+    }
   }
-  __syncwarp();
-  if (TMA && lane == 0) {
-    tma_prefetch_desc(&tm_u);
-    tma_prefetch_desc(&tm_dr);
-    if (HAS_Z) tma_prefetch_desc(&tm_z);
-    tma_prefetch_desc(&tm_b);
-    tma_prefetch_desc(&tm_c);
-  }
+  __syncthreads();
+  const int64_t wid = s_wid;
+  if (wid >= p.nworkers) return;  // CTA-uniform
+  if (tid == 0 && p.ws_header && wid == 0) p.ws_header[2] = kHeaderMagic;
 
   const int64_t T = p.tiles_per_blk, L = p.seqlen, Dm = p.dim;
   const int ncblk = p.ncblk;
+  const uint64_t wait_ns = p.wait_ns;
 
   // ---- the worker's steps: step q runs tile j of channel block blk
   int64_t r0 = 0, zs = 0, zlen = 0, af = 0, nfull = 0, nsteps = 0;  // stream-K
-  int64_t cblk = 0, c = 0, j0 = 0, nk = 0;        // chunked
+  int64_t cblk = 0, c = 0, j0 = 0, nk = 0;                          // chunked
   if constexpr (MODE == kModeStatic) {
     nsteps = T;
   } else if constexpr (MODE == kModeStreamK) {
@@ -173,142 +187,127 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     int b, x0, st;
     uint32_t ph;
   };
-  auto place = [&](Cursor& c) {  // (blk, j) and the block's coordinates for step c.q
+  auto place = [&](Cursor& cu) {  // (blk, j) and the block's coordinates for step cu.q
     if constexpr (MODE == kModeStatic) {
-      c.blk = wid;
-      c.j = c.q;
+      cu.blk = wid;
+      cu.j = cu.q;
     } else if constexpr (MODE == kModeStreamK) {
-      // the head of the last block (handed over to the next warp), then the
+      // the head of the last block (handed over to the next CTA), then the
       // whole blocks, then the first segment, which waits for the previous
-      // warp's hand-over: with ranges of at least one block that hand-over is
-      // already done by the time this warp gets there
-      const int64_t q = c.q;
+      // CTA's hand-over: with ranges of at least one block that hand-over is
+      // already done by the time this CTA gets there
+      const int64_t q = cu.q;
       const int64_t g = q < zlen ? zs + q : (q < zlen + nfull ? af + (q - zlen) : r0 + (q - zlen - nfull));
-      c.blk = g / T;
-      c.j = g - c.blk * T;
+      cu.blk = g / T;
+      cu.j = g - cu.blk * T;
     } else {
-      c.blk = cblk;
-      c.j = j0 + (c.q < nk ? c.q : c.q - nk);
+      cu.blk = cblk;
+      cu.j = j0 + (cu.q < nk ? cu.q : cu.q - nk);
     }
-    c.b = (int)(c.blk / ncblk);
-    c.x0 = (int)(c.blk - (int64_t)c.b * ncblk) * DC;
+    cu.b = (int)(cu.blk / ncblk);
+    cu.x0 = (int)(cu.blk - (int64_t)cu.b * ncblk) * CC;
   };
-  auto advance = [&](Cursor& c) {
-    c.q++;
-    if (++c.st == kStages) {
-      c.st = 0;
-      c.ph ^= 1u;
+  auto advance = [&](Cursor& cu) {
+    cu.q++;
+    if (++cu.st == kStages) {
+      cu.st = 0;
+      cu.ph ^= 1u;
     }
     bool jump = false;
-    if constexpr (MODE == kModeStreamK) jump = c.q == zlen || c.q == zlen + nfull;
-    if constexpr (MODE == kModeChunked) jump = c.q == nk;
+    if constexpr (MODE == kModeStreamK) jump = cu.q == zlen || cu.q == zlen + nfull;
+    if constexpr (MODE == kModeChunked) jump = cu.q == nk;
     if (jump) {
-      place(c);
-    } else if (++c.j == T) {
-      c.j = 0;
-      c.blk++;
-      c.x0 += DC;
-      if (c.x0 >= ncblk * DC) {
-        c.x0 = 0;
-        c.b++;
+      place(cu);
+    } else if (++cu.j == T) {
+      cu.j = 0;
+      cu.blk++;
+      cu.x0 += CC;
+      if (cu.x0 >= ncblk * CC) {
+        cu.x0 = 0;
+        cu.b++;
       }
     }
   };
-  Cursor ci{0, 0, 0, 0, 0, 0, 0u};  // next step to issue
-  place(ci);
-  Cursor cc = ci;                   // next step to consume
+  Cursor cc{0, 0, 0, 0, 0, 0, 0u};  // the step being run
+  place(cc);
 
-  // ---- TMA ring
-  bool abort = false;
-  auto issue = [&](const Cursor& c) {
-    const int st = c.st;
-    uint8_t* base = smem + st * K::STAGE;
-    const int b = c.b;
-    const int x0 = c.x0;
-    const int y0 = (int)(c.j * TILE);
+  // ---- tile loads
+  // TMA: one thread issues the five boxes of a step into its ring slot
+  auto issue_tma = [&](const Cursor& cu) {
+    uint8_t* base = smem + cu.st * K::STAGE;
+    const int y0 = (int)(cu.j * TILE);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(&full[cu.st], (HAS_Z ? 3 : 2) * K::XB + 2 * K::RB);
+    tma_load_3d(base + K::OFF_U, &tm_u, cu.x0, y0, cu.b, &full[cu.st]);
+    tma_load_3d(base + K::OFF_DR, &tm_dr, cu.x0, y0, cu.b, &full[cu.st]);
+    if (HAS_Z) tma_load_3d(base + K::OFF_Z, &tm_z, cu.x0, y0, cu.b, &full[cu.st]);
+    tma_load_3d(base + K::OFF_B, &tm_b, 0, y0, cu.b, &full[cu.st]);
+    tma_load_3d(base + K::OFF_C, &tm_c, 0, y0, cu.b, &full[cu.st]);
+    mbar_arrive(&full[cu.st]);
+  };
+  // plain loads with bounds checks (shapes no TMA descriptor can cover): the
+  // whole CTA stages the step's tile synchronously
+  auto load_plain = [&](const Cursor& cu) {
+    uint8_t* base = smem + cu.st * K::STAGE;
+    const int64_t y0 = cu.j * TILE;
+    const TIn* gu = static_cast<const TIn*>(p.u);
+    const TIn* gdr = static_cast<const TIn*>(p.delta_raw);
+    const TIn* gz = static_cast<const TIn*>(p.z);
+    TIn* su = reinterpret_cast<TIn*>(base + K::OFF_U);
+    TIn* sdr = reinterpret_cast<TIn*>(base + K::OFF_DR);
+    TIn* sz = reinterpret_cast<TIn*>(base + K::OFF_Z);
+    for (int i = tid; i < TILE * CC; i += 32 * kWarps) {
+      const int tt = i / CC, ch = i % CC;
+      const int64_t t = y0 + tt, dd = (int64_t)cu.x0 + ch;
+      TIn vu = from_f32<TIn>(0.f), vr = vu, vz = vu;
+      if (t < L && dd < Dm) {
+        const int64_t gi = ((int64_t)cu.b * L + t) * Dm + dd;
+        vu = gu[gi];
+        vr = gdr[gi];
+        if (HAS_Z) vz = gz[gi];
+      }
+      su[i] = vu;
+      sdr[i] = vr;
+      if (HAS_Z) sz[i] = vz;
+    }
+    const TIn* gB = static_cast<const TIn*>(p.B);
+    const TIn* gC = static_cast<const TIn*>(p.C);
+    TIn* sB = reinterpret_cast<TIn*>(base + K::OFF_B);
+    TIn* sC = reinterpret_cast<TIn*>(base + K::OFF_C);
+    for (int i = tid; i < TILE * kDState; i += 32 * kWarps) {
+      const int64_t t = y0 + i / kDState;
+      const bool ok = t < L;
+      const int64_t gi = ((int64_t)cu.b * L + (ok ? t : 0)) * kDState + i % kDState;
+      sB[i] = ok ? gB[gi] : from_f32<TIn>(0.f);
+      sC[i] = ok ? gC[gi] : from_f32<TIn>(0.f);
+    }
+  };
+
+  bool abort = false;  // CTA-uniform: set only from CTA-wide votes and broadcasts
+  // Wait for the current step's tile, widen B/C, and synchronise the CTA.
+  // After this barrier every thread has finished the previous step, so the
+  // slot that the next step loads into is free. Returns the fp32 B|C rows.
+  auto acquire = [&](const Cursor& cu) -> const float* {
+    const uint8_t* base = smem + cu.st * K::STAGE;
+    bool timed_out = false;
     if constexpr (TMA) {
-      if (lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect_tx(&full[st], (HAS_Z ? 3 : 2) * K::XB + 2 * K::RB);
-        tma_load_3d(base + K::OFF_U, &tm_u, x0, y0, b, &full[st]);
-        tma_load_3d(base + K::OFF_DR, &tm_dr, x0, y0, b, &full[st]);
-        if (HAS_Z) tma_load_3d(base + K::OFF_Z, &tm_z, x0, y0, b, &full[st]);
-        tma_load_3d(base + K::OFF_B, &tm_b, 0, y0, b, &full[st]);
-        tma_load_3d(base + K::OFF_C, &tm_c, 0, y0, b, &full[st]);
-        mbar_arrive(&full[st]);
-      }
+      timed_out = !mbar_wait(&full[cu.st], cu.ph, wait_ns);
     } else {
-      // plain loads with bounds checks (shapes no TMA descriptor can cover)
-      const TIn* gu = static_cast<const TIn*>(p.u);
-      const TIn* gdr = static_cast<const TIn*>(p.delta_raw);
-      const TIn* gz = static_cast<const TIn*>(p.z);
-      TIn* su = reinterpret_cast<TIn*>(base + K::OFF_U);
-      TIn* sdr = reinterpret_cast<TIn*>(base + K::OFF_DR);
-      TIn* sz = reinterpret_cast<TIn*>(base + K::OFF_Z);
-      for (int i = lane; i < TILE * DC; i += 32) {
-        const int tt = i / DC, cc = i % DC;
-        const int64_t t = (int64_t)y0 + tt, dd = (int64_t)x0 + cc;
-        TIn vu = from_f32<TIn>(0.f), vr = vu, vz = vu;
-        if (t < L && dd < Dm) {
-          const int64_t gi = ((int64_t)b * L + t) * Dm + dd;
-          vu = gu[gi];
-          vr = gdr[gi];
-          if (HAS_Z) vz = gz[gi];
-        }
-        su[i] = vu;
-        sdr[i] = vr;
-        if (HAS_Z) sz[i] = vz;
-      }
-      const TIn* gB = static_cast<const TIn*>(p.B);
-      const TIn* gC = static_cast<const TIn*>(p.C);
-      TIn* sB = reinterpret_cast<TIn*>(base + K::OFF_B);
-      TIn* sC = reinterpret_cast<TIn*>(base + K::OFF_C);
-      for (int i = lane; i < TILE * kDState; i += 32) {
-        const int64_t t = (int64_t)y0 + i / kDState;
-        const bool ok = t < L;
-        const int64_t gi = ((int64_t)b * L + (ok ? t : 0)) * kDState + i % kDState;
-        sB[i] = ok ? gB[gi] : from_f32<TIn>(0.f);
-        sC[i] = ok ? gC[gi] : from_f32<TIn>(0.f);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[st]);
+      __syncthreads();  // every thread is done with the slot before it is restaged
+      load_plain(cu);
+      __syncthreads();
     }
-  };
-  // issue every step below qmax not yet issued; the caller has synchronised
-  // the warp, so the ring slot being refilled is no longer read
-  auto issue_upto = [&](int64_t qmax) {
-    const int64_t lim = min(qmax, nsteps);
-    while (ci.q < lim) {
-      issue(ci);
-      advance(ci);
-    }
-  };
-  // wait for step q's tile; returns the fp32 B|C rows of the tile
-  auto acquire = [&](const Cursor& c) -> const float* {
-    const int st = c.st;
-    const bool timed_out = !abort && !mbar_wait(&full[st], c.ph);
-    if (__any_sync(FULL, timed_out)) {  // keep `abort` warp-uniform
-      abort = true;
-      if (lane == 0) atomicOr(p.fault, kFaultTileWait);
-    }
-    const uint8_t* base = smem + st * K::STAGE;
+    float* bcf = nullptr;
     if constexpr (K::BF) {
-      // B then C (2 x TILE x 16 bf16, contiguous in the stage) widened to
-      // fp32: per pass each lane takes four consecutive values, so both the
-      // 8-byte loads and the 16-byte stores are contiguous across the warp
-      const uint2* src = reinterpret_cast<const uint2*>(base + K::OFF_B);
-      float4* dst = reinterpret_cast<float4*>(smem + K::OFF_BCF);
-#pragma unroll
-      for (int i = 0; i < (2 * TILE * kDState) / (4 * 32); i++) {
-        const uint2 v = src[i * 32 + lane];
-        dst[i * 32 + lane] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
-                                         __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-      }
-      __syncwarp();
-      return reinterpret_cast<const float*>(smem + K::OFF_BCF);
-    } else {
-      return reinterpret_cast<const float*>(base + K::OFF_B);  // fp32 B then C, contiguous
+      bcf = reinterpret_cast<float*>(smem + K::OFF_BCF + cu.st * K::BCF);
+      if (!timed_out) widen_bc<TILE>(base + K::OFF_B, bcf, tid);
     }
+    if (__syncthreads_or(timed_out ? 1 : 0)) {
+      if (tid == 0) atomicOr(p.fault, kFaultTileWait);
+      abort = true;
+    }
+    if constexpr (K::BF) return bcf;
+    else return reinterpret_cast<const float*>(base + K::OFF_B);  // fp32 B then C: [TILE][16] each
   };
 
   // ---- per-channel constants of the current block and the state
@@ -320,7 +319,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   int64_t hoff = 0;      // element offset of this lane's states in h0 / h_last
   auto load_block = [&](int64_t blk) {
     const int64_t b = blk / ncblk;
-    d = (blk % ncblk) * DC + cw;
+    d = (blk % ncblk) * CC + cb;
     dvalid = d < Dm;
     const int64_t dc = dvalid ? d : 0;
 #pragma unroll
@@ -344,11 +343,11 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   };
 
   // One state update of this lane's NS states for one token; returns the
-  // lane's part of C.h.
+  // lane's part of C.h. brow / crow: the token's fp32 B and C rows.
   auto update = [&](float dl, float du, const float* brow, const float* crow) -> float {
     const f2 dl2 = pk(dl, dl), du2 = pk(du, du);
-    const ulonglong2* bq = reinterpret_cast<const ulonglong2*>(brow);
-    const ulonglong2* cq = reinterpret_cast<const ulonglong2*>(crow);
+    const ulonglong2* bq = reinterpret_cast<const ulonglong2*>(brow + n0);
+    const ulonglong2* cq = reinterpret_cast<const ulonglong2*>(crow + n0);
     f2 acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
     for (int i = 0; i < NP / 2; i++) {
@@ -372,41 +371,44 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
 
   float ssum = 0.f;  // sum of delta over the tokens of the current pass (chunked mode)
 
-  // Run `tlen` tokens of the acquired tile (slot `st`) starting at timestep t0.
+  // Run `tlen` tokens of the acquired tile (ring slot st) starting at timestep t0.
   auto run_tile = [&](int st, const float* bcf, int64_t t0, int tlen) {
     const uint8_t* base = smem + st * K::STAGE;
-    const TIn* su = reinterpret_cast<const TIn*>(base + K::OFF_U) + cw;
-    const TIn* sdr = reinterpret_cast<const TIn*>(base + K::OFF_DR) + cw;
-    const TIn* sz = reinterpret_cast<const TIn*>(base + K::OFF_Z) + cw;
-    const float* brow = bcf + n0;
-    const float* crow = bcf + TILE * kDState + n0;
+    const TIn* su = reinterpret_cast<const TIn*>(base + K::OFF_U) + cb;
+    const TIn* sdr = reinterpret_cast<const TIn*>(base + K::OFF_DR) + cb;
+    const TIn* sz = reinterpret_cast<const TIn*>(base + K::OFF_Z) + cb;
+    // token tt's fp32 B and C rows
+    constexpr int BSTR = K::BF ? 2 * kDState : kDState;  // floats between rows
+    constexpr int COFF = K::BF ? kDState : TILE * kDState;
+    auto brow = [&](int tt) { return bcf + tt * BSTR; };
+    auto crow = [&](int tt) { return bcf + COFF + tt * BSTR; };
+    const f2 bias2 = pk(bias_d, bias_d), D2 = pk(D_d, D_d);
+    // scalars of tokens (tt, tt+1) of this lane's channel, as packed pairs
+    struct PairScalars {
+      f2 dl, du, post, g;
+    };
+    auto scalars_pair = [&](int tt) -> PairScalars {
+      PairScalars r;
+      const f2 xu = pk(to_f32(su[tt * CC]), to_f32(su[(tt + 1) * CC]));
+      r.dl = softplus_fast2(add2(pk(to_f32(sdr[tt * CC]), to_f32(sdr[(tt + 1) * CC])), bias2));
+      r.du = mul2(r.dl, xu);
+      r.post = mul2(D2, xu);
+      r.g = HAS_Z ? silu2(pk(to_f32(sz[tt * CC]), to_f32(sz[(tt + 1) * CC]))) : pk(1.f, 1.f);
+      return r;
+    };
     if constexpr (SG == 1) {
       TOut* yp = ycol + t0 * Dm;
       auto token = [&](int tt) {
-        const float xu = to_f32(su[tt * DC]);
-        const float dl = softplus_fast(to_f32(sdr[tt * DC]) + bias_d);
-        const float g = HAS_Z ? silu(to_f32(sz[tt * DC])) : 1.f;
-        const float yv = update(dl, dl * xu, brow + tt * kDState, crow + tt * kDState);
+        const float xu = to_f32(su[tt * CC]);
+        const float dl = softplus_fast(to_f32(sdr[tt * CC]) + bias_d);
+        const float g = HAS_Z ? silu(to_f32(sz[tt * CC])) : 1.f;
+        const float yv = update(dl, dl * xu, brow(tt), crow(tt));
         st_out(yp + tt * Dm, fmaf(D_d, xu, yv) * g, dvalid);
         if constexpr (MODE == kModeChunked) ssum += dl;
       };
-      // two tokens whose per-token scalars are computed as packed pairs
-      const f2 bias2 = pk(bias_d, bias_d), D2 = pk(D_d, D_d);
-      struct PairScalars {
-        f2 dl, du, post, g;
-      };
-      auto scalars_pair = [&](int tt) -> PairScalars {
-        PairScalars r;
-        const f2 xu = pk(to_f32(su[tt * DC]), to_f32(su[(tt + 1) * DC]));
-        r.dl = softplus_fast2(add2(pk(to_f32(sdr[tt * DC]), to_f32(sdr[(tt + 1) * DC])), bias2));
-        r.du = mul2(r.dl, xu);
-        r.post = mul2(D2, xu);
-        r.g = HAS_Z ? silu2(pk(to_f32(sz[tt * DC]), to_f32(sz[(tt + 1) * DC]))) : pk(1.f, 1.f);
-        return r;
-      };
       auto update_pair = [&](int tt, const PairScalars& r) {
-        const float y0 = update(f2lo(r.dl), f2lo(r.du), brow + tt * kDState, crow + tt * kDState);
-        const float y1 = update(f2hi(r.dl), f2hi(r.du), brow + (tt + 1) * kDState, crow + (tt + 1) * kDState);
+        const float y0 = update(f2lo(r.dl), f2lo(r.du), brow(tt), crow(tt));
+        const float y1 = update(f2hi(r.dl), f2hi(r.du), brow(tt + 1), crow(tt + 1));
         const f2 yv = mul2(add2(pk(y0, y1), r.post), r.g);
         st_out(yp + tt * Dm, f2lo(yv), dvalid);
         st_out(yp + (tt + 1) * Dm, f2hi(yv), dvalid);
@@ -420,8 +422,8 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
         // past the tile
         PairScalars cur0 = scalars_pair(0), cur1 = scalars_pair(2), cur2 = scalars_pair(4), cur3 = scalars_pair(6);
 #pragma unroll 1
-        for (int tt = 0; tt < TILE; tt += kUnroll) {
-          const int tn = min(tt + kUnroll, TILE - kUnroll);
+        for (int tt = 0; tt < TILE; tt += 8) {
+          const int tn = min(tt + 8, TILE - 8);
           const PairScalars nx0 = scalars_pair(tn), nx1 = scalars_pair(tn + 2), nx2 = scalars_pair(tn + 4),
                             nx3 = scalars_pair(tn + 6);
           update_pair(tt, cur0);
@@ -438,35 +440,52 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
         for (int tt = 0; tt < tlen; tt++) token(tt);
       }
     } else {
-      // token pair (tt, tt+1): lane s computes the scalars of token tt+s and
-      // stores its y; the pair exchanges (delta, delta*u) and the halves of C.h
-      TOut* yp = ycol + (t0 + s) * Dm;
-      auto pair = [&](int tt, bool two) {
-        const int tm = tt + s;  // may be tlen for an odd tail: a row of the tile buffer, unused
-        const float xu = to_f32(su[tm * DC]);
-        const float dl = softplus_fast(to_f32(sdr[tm * DC]) + bias_d);
-        const float g = HAS_Z ? silu(to_f32(sz[tm * DC])) : 1.f;
-        const float du = dl * xu;
-        const float dlo = __shfl_xor_sync(FULL, dl, 1), duo = __shfl_xor_sync(FULL, du, 1);
-        const float pa = update(s ? dlo : dl, s ? duo : du, brow + tt * kDState, crow + tt * kDState);
-        float pb = 0.f;
-        if (two) pb = update(s ? dl : dlo, s ? du : duo, brow + (tt + 1) * kDState, crow + (tt + 1) * kDState);
-        const float keep = s ? pb : pa, send = s ? pa : pb;
-        const float yv = keep + __shfl_xor_sync(FULL, send, 1);
-        st_out(yp + tt * Dm, fmaf(D_d, xu, yv) * g, dvalid && (two || s == 0));
-        if constexpr (MODE == kModeChunked) ssum += (s ? dlo : dl) + (two ? (s ? dl : dlo) : 0.f);
+      // Two lanes per channel. Per group of four tokens lane s computes the
+      // scalars of tokens tt+2s and tt+2s+1 as a packed pair; the lane pair
+      // swaps them, each lane updates its 8 states for all four tokens, and
+      // lane s finishes y of its own two tokens from both halves of C.h.
+      auto shfl2 = [&](f2 v) -> f2 {
+        return pk(__shfl_xor_sync(FULL, f2lo(v), 1), __shfl_xor_sync(FULL, f2hi(v), 1));
+      };
+      auto group = [&](int tt, const PairScalars& r) {
+        const f2 odl = shfl2(r.dl), odu = shfl2(r.du);
+        const f2 dlA = s ? odl : r.dl, duA = s ? odu : r.du;  // tokens tt, tt+1
+        const f2 dlB = s ? r.dl : odl, duB = s ? r.du : odu;  // tokens tt+2, tt+3
+        const float p0 = update(f2lo(dlA), f2lo(duA), brow(tt), crow(tt));
+        const float p1 = update(f2hi(dlA), f2hi(duA), brow(tt + 1), crow(tt + 1));
+        const float p2 = update(f2lo(dlB), f2lo(duB), brow(tt + 2), crow(tt + 2));
+        const float p3 = update(f2hi(dlB), f2hi(duB), brow(tt + 3), crow(tt + 3));
+        const f2 mine = s ? pk(p2, p3) : pk(p0, p1), theirs = s ? pk(p0, p1) : pk(p2, p3);
+        const f2 yv = mul2(add2(add2(mine, shfl2(theirs)), r.post), r.g);
+        TOut* yp = ycol + (t0 + tt + 2 * s) * Dm;
+        st_out(yp, f2lo(yv), dvalid);
+        st_out(yp + Dm, f2hi(yv), dvalid);
+        if constexpr (MODE == kModeChunked) ssum += (f2lo(dlA) + f2hi(dlA)) + (f2lo(dlB) + f2hi(dlB));
+      };
+      // a single token (the ragged tail): both lanes compute its scalars
+      auto token = [&](int tt) {
+        const float xu = to_f32(su[tt * CC]);
+        const float dl = softplus_fast(to_f32(sdr[tt * CC]) + bias_d);
+        const float g = HAS_Z ? silu(to_f32(sz[tt * CC])) : 1.f;
+        const float part = update(dl, dl * xu, brow(tt), crow(tt));
+        const float yv = part + __shfl_xor_sync(FULL, part, 1);
+        st_out(ycol + (t0 + tt) * Dm, fmaf(D_d, xu, yv) * g, dvalid && s == 0);
+        if constexpr (MODE == kModeChunked) ssum += dl;
       };
       if (tlen == TILE) {
+        PairScalars cur0 = scalars_pair(2 * s), cur1 = scalars_pair(4 + 2 * s);
 #pragma unroll 1
-        for (int tt = 0; tt < TILE; tt += kUnroll) {
-          pair(tt, true);
-          pair(tt + 2, true);
-          pair(tt + 4, true);
-          pair(tt + 6, true);
+        for (int tt = 0; tt < TILE; tt += 8) {
+          const int tn = min(tt + 8, TILE - 8);
+          const PairScalars nx0 = scalars_pair(tn + 2 * s), nx1 = scalars_pair(tn + 4 + 2 * s);
+          group(tt, cur0);
+          group(tt + 4, cur1);
+          cur0 = nx0;
+          cur1 = nx1;
         }
       } else {
 #pragma unroll 1
-        for (int tt = 0; tt < tlen; tt += 2) pair(tt, tt + 1 < tlen);
+        for (int tt = 0; tt < tlen; tt++) token(tt);
       }
     }
   };
@@ -475,44 +494,55 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
 #pragma unroll
     for (int i = 0; i < NP; i++) reinterpret_cast<float2*>(dst)[i] = make_float2(f2lo(hp[i]), f2hi(hp[i]));
   };
-  // bounded wait (lane 0) for a flag to become nonzero; every lane then
-  // acquires it itself. Returns the flag value (forced nonzero on timeout).
+  // Bounded wait (thread 0) for a flag to become nonzero, broadcast to the
+  // CTA; every thread then acquires the flag itself (orders its later reads of
+  // the published record). Returns the flag value; a timeout sets `abort`
+  // CTA-wide and returns kFlagInclusive.
   auto wait_flag = [&](uint32_t* f) -> uint32_t {
-    uint32_t v = 0;
-    if (lane == 0) {
-      v = ld_acquire_gpu(f);
-      if (v == 0 && !abort) {
+    if (tid == 0) {
+      uint32_t v = ld_acquire_gpu(f);
+      if (v == 0) {
         const uint64_t tw = globaltimer();
         while ((v = ld_acquire_gpu(f)) == 0) {
-          if (globaltimer() - tw > kWaitNs) {
+          if (globaltimer() - tw > wait_ns) {
             atomicOr(p.fault, kFaultLookback);
-            abort = true;
             break;
           }
         }
       }
+      s_flag = v;
     }
-    // lane 0's observation decides for the whole warp (the flag may move on
-    // from aggregate to inclusive meanwhile: a per-lane value could split the
-    // warp); each lane's own acquire load only orders its later reads of the
-    // published record, which any value at or above lane 0's covers
-    v = __shfl_sync(FULL, v, 0);
-    abort = __shfl_sync(FULL, abort ? 1 : 0, 0) != 0;
-    if (v != 0)
-      for (int i = 0; i < (1 << 20) && ld_acquire_gpu(f) < v; i++) {
-      }
-    return v == 0 ? kFlagInclusive : v;
+    __syncthreads();
+    // thread 0's observation decides for the whole CTA (the flag may move on
+    // from aggregate to inclusive meanwhile: per-thread values could split the
+    // CTA); each thread's own acquire load only orders its later reads of the
+    // published record, which any value at or above thread 0's covers
+    const uint32_t v = s_flag;
+    __syncthreads();  // s_flag is free for the next wait
+    if (v == 0) {
+      abort = true;
+      return kFlagInclusive;
+    }
+    for (int i = 0; i < (1 << 20) && ld_acquire_gpu(f) < v; i++) {
+    }
+    return v;
+  };
+  // publish: every thread's stores are done (CTA barrier), then thread 0
+  // releases the flag at gpu scope (unless the test knob withholds it)
+  auto publish = [&](uint32_t* f, uint32_t v, bool withhold) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0 && !withhold) st_release_gpu(f, v);
   };
 
   float hin[MODE == kModeChunked ? NS : 1];  // chunked: the true state entering the chunk
   hin[0] = 0.f;
 
   // ---- main loop over the worker's steps
-  issue_upto(kStages - 1);
+  if (TMA && tid == 0 && nsteps > 0) issue_tma(cc);
   int64_t q = 0;
+  bool next_issued = nsteps > 0;  // whether step q's load was issued (TMA)
   for (; q < nsteps; q++, advance(cc)) {
-    __syncwarp();
-    issue_upto(q + kStages);
     const int64_t blk = cc.blk, j = cc.j;
 
     // segment start: per-channel constants and the incoming state
@@ -528,9 +558,9 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
           set_state_initial();
         } else {
           // the first segment starts inside a block: take the state the
-          // previous worker handed over at this range boundary
+          // previous CTA handed over at this range boundary
           wait_flag(p.flags + wid);
-          const float* src = p.ws_carry + (size_t)wid * DC * kDState + cw * kDState + n0;
+          const float* src = p.ws_carry + ((size_t)wid * CC + cb) * kDState + n0;
 #pragma unroll
           for (int i = 0; i < NP; i++) {
             const float2 v = __ldcg(reinterpret_cast<const float2*>(src) + i);
@@ -549,6 +579,17 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     }
 
     const float* bcf = acquire(cc);
+    next_issued = false;
+    if (abort) break;
+    // the slot of the previous step is free: load the next step into it
+    if (TMA && q + 1 < nsteps) {
+      if (tid == 0) {
+        Cursor cn = cc;
+        advance(cn);
+        issue_tma(cn);
+      }
+      next_issued = true;
+    }
     const int64_t t0 = j * TILE;
     run_tile(cc.st, bcf, t0, (int)min((int64_t)TILE, L - t0));
 
@@ -559,29 +600,24 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
       if (j == T - 1) {
         if (dvalid && p.h_last) store_h(p.h_last + hoff);
       } else if (q + 1 == zlen) {
-        float* dst = p.ws_carry + (size_t)(wid + 1) * DC * kDState + cw * kDState + n0;
-        store_h(dst);
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_gpu(p.flags + wid + 1, kFlagHanded);
+        store_h(p.ws_carry + ((size_t)(wid + 1) * CC + cb) * kDState + n0);
+        publish(p.flags + wid + 1, kFlagHanded, wid + 1 == p.withhold_item);
       }
+      if (abort) break;
     } else {
       if (q == nk - 1) {
         // ---- end of the first pass: publish the chunk's carry, look back
         const int64_t tile_id = cblk * p.nchunks + c;
-        float* carry_me = p.ws_carry + ((size_t)tile_id * DC + cw) * 48 + n0;
-        float hl[NS];
+        float* carry_me = p.ws_carry + ((size_t)tile_id * CC + cb) * 48 + n0;
+        float hl[NS], A2[NS];
 #pragma unroll
         for (int i = 0; i < NP; i++) {
           hl[2 * i] = f2lo(hp[i]);
           hl[2 * i + 1] = f2hi(hp[i]);
-        }
-        float A2[NS];
-#pragma unroll
-        for (int i = 0; i < NP; i++) {
           A2[2 * i] = f2lo(A2p[i]);
           A2[2 * i + 1] = f2hi(A2p[i]);
         }
+        const bool withhold = tile_id == p.withhold_item;
         if (c == 0) {
 #pragma unroll
           for (int n = 0; n < NS; n++) carry_me[32 + n] = hl[n];
@@ -592,9 +628,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
             carry_me[16 + n] = hl[n];         // S = state from a zero start
           }
         }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_gpu(p.flags + tile_id, c == 0 ? kFlagInclusive : kFlagAggregate);
+        publish(p.flags + tile_id, c == 0 ? kFlagInclusive : kFlagAggregate, withhold);
         if (c > 0) {
           float Pa[NS], Sa[NS];
 #pragma unroll
@@ -605,7 +639,8 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
           for (int64_t jj = c - 1; jj >= 0; jj--) {
             const int64_t pid = tile_id - (c - jj);
             const uint32_t f = wait_flag(p.flags + pid);
-            const float* cp = p.ws_carry + ((size_t)pid * DC + cw) * 48 + n0;
+            if (abort) break;
+            const float* cp = p.ws_carry + ((size_t)pid * CC + cb) * 48 + n0;
             if (f == kFlagInclusive) {
 #pragma unroll
               for (int n = 0; n < NS; n++) Sa[n] = fmaf(Pa[n], __ldcg(cp + 32 + n), Sa[n]);
@@ -617,19 +652,15 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
               Pa[n] *= __ldcg(cp + n);
             }
           }
+          if (abort) break;
           // Sa is the true state entering this chunk
-          float Pend[NS];
-#pragma unroll
-          for (int n = 0; n < NS; n++) Pend[n] = carry_me[n];
 #pragma unroll
           for (int n = 0; n < NS; n++) {
-            const float incl = fmaf(Pend[n], Sa[n], hl[n]);  // P_end * h_in + S_local
+            const float incl = fmaf(carry_me[n], Sa[n], hl[n]);  // P_end * h_in + S_local
             carry_me[32 + n] = incl;
             hl[n] = incl;
           }
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) st_release_gpu(p.flags + tile_id, kFlagInclusive);
+          publish(p.flags + tile_id, kFlagInclusive, withhold);
           if (c == p.nchunks - 1 && dvalid && p.h_last) {
 #pragma unroll
             for (int n = 0; n < NS; n++) p.h_last[hoff + n] = hl[n];
@@ -654,26 +685,16 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
           done = done && a0 <= 0.f && a1 <= 0.f && c0 <= kStopRel * fabsf(f2lo(hp[i])) &&
                  c1 <= kStopRel * fabsf(f2hi(hp[i]));
         }
-        if (__all_sync(FULL, done || !dvalid)) {
-          q++;
-          break;
-        }
+        if (__syncthreads_and((done || !dvalid) ? 1 : 0)) break;
       }
     }
-    if (abort) {
-      q++;
-      break;
-    }
   }
-  // drain loads issued past the last consumed step (bounded waits)
-  __syncwarp();
-  if (q < nsteps) {
-    if (cc.q != q) {  // left the loop by break: cc still names step q-1
-      cc.q = q - 1;
-      advance(cc);
-    }
-    for (; cc.q < ci.q; advance(cc))
-      if (!mbar_wait(&full[cc.st], cc.ph)) atomicOr(p.fault, kFaultTileWait);
+  // a load issued for a step that was not run must land before the CTA ends
+  // (bounded wait on that slot's phase)
+  if (TMA && tid == 0 && next_issued) {
+    Cursor cn = cc;
+    advance(cn);
+    if (!mbar_wait(&full[cn.st], cn.ph, wait_ns)) atomicOr(p.fault, kFaultTileWait);
   }
 }
 
@@ -711,28 +732,28 @@ inline bool make_map(CUtensorMap* m, const void* ptr, size_t es, int64_t batch, 
   return r == CUDA_SUCCESS;
 }
 
+// Dynamic shared memory of every launch is at least this much, so that two
+// CTAs never share an SM (the split modes size their work for one CTA per SM).
+constexpr int kSmemOneCtaPerSm = 116 * 1024;
+
 template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, int MODE>
 cudaError_t launch_t(const ScanParams& p, cudaStream_t stream) {
   using K = Cfg<TIn, SG>;
   auto kern = scan_fwd_kernel<TIn, TOut, SG, TMA, HAS_Z, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
+  constexpr int smem = K::SMEM > kSmemOneCtaPerSm ? K::SMEM : kSmemOneCtaPerSm;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   CUtensorMap mu{}, mdr{}, mz{}, mb{}, mc{};
   if (TMA) {
     const size_t es = sizeof(TIn);
-    if (!make_map(&mu, p.u, es, p.batch, p.seqlen, p.dim, K::DC, K::TILE) ||
-        !make_map(&mdr, p.delta_raw, es, p.batch, p.seqlen, p.dim, K::DC, K::TILE) ||
-        (HAS_Z && !make_map(&mz, p.z, es, p.batch, p.seqlen, p.dim, K::DC, K::TILE)) ||
+    if (!make_map(&mu, p.u, es, p.batch, p.seqlen, p.dim, K::CC, K::TILE) ||
+        !make_map(&mdr, p.delta_raw, es, p.batch, p.seqlen, p.dim, K::CC, K::TILE) ||
+        (HAS_Z && !make_map(&mz, p.z, es, p.batch, p.seqlen, p.dim, K::CC, K::TILE)) ||
         !make_map(&mb, p.B, es, p.batch, p.seqlen, kDState, kDState, K::TILE) ||
         !make_map(&mc, p.C, es, p.batch, p.seqlen, kDState, kDState, K::TILE))
       return cudaErrorInvalidValue;
   }
-  // the split modes place kWarps workers per block, one per SM sub-partition;
-  // one-warp blocks spread the few warps of the static mode over all SMs
-  const int wpb = MODE == kModeStatic ? 1 : kWarps;
-  const int64_t nblocks = (p.nworkers + wpb - 1) / wpb;
-  const int smem = wpb * K::WARP_SMEM + 128;
-  kern<<<(unsigned)nblocks, 32 * wpb, smem, stream>>>(p, mu, mdr, mz, mb, mc);
+  kern<<<(unsigned)p.nworkers, 32 * kWarps, smem, stream>>>(p, mu, mdr, mz, mb, mc);
   return cudaGetLastError();
 }
 

@@ -16,17 +16,17 @@ def to_dev(x):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
 
 
-def run_scan(x, out_dtype=torch.float32, sg=0, chunk=0, check_status=True, wps=0):
+def run_scan(x, out_dtype=torch.float32, sg=0, chunk=0, check_status=True, workers=0):
     """Run ss_scan_fwd on the GPU for host inputs x; returns float64 numpy (y, h_last)."""
-    y, h = run_scan_dev(x, out_dtype, sg, chunk, check_status, wps)
+    y, h = run_scan_dev(x, out_dtype, sg, chunk, check_status, workers)
     return y.double().cpu().numpy(), h.double().cpu().numpy()
 
 
-def run_scan_dev(x, out_dtype=torch.float32, sg=0, chunk=0, check_status=True, wps=0):
+def run_scan_dev(x, out_dtype=torch.float32, sg=0, chunk=0, check_status=True, workers=0):
     """Run ss_scan_fwd on the GPU for host inputs x; returns the device tensors (y, h_last)."""
     d = to_dev(x)
     Bt, L, Dm = d["u"].shape
-    ss.ss_scan_set_tuning(sg, chunk, wps)
+    ss.ss_scan_set_tuning(sg, chunk, workers)
     try:
         ws_bytes = ss.ss_scan_fwd_workspace_size(Bt, L, Dm, 16)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if ws_bytes else None

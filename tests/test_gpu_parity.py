@@ -88,42 +88,43 @@ def test_chunked_lookback(case):
     assert_close(h, hr, _dt(dt), what="chunked h_last")
 
 
-# Stream-K split: equal ranges of the (channel block, tile) space per warp, with
+# Stream-K split: equal ranges of the (channel block, tile) space per CTA, with
 # states handed over where a range boundary falls inside a channel block. It
-# engages once there are at least as many channel blocks as SM sub-partitions
-# (592 on B300); (batch, dim) below give 608 one-lane blocks / 1197 two-lane ones.
+# engages once there are more channel blocks (128 channels with one lane per
+# channel, 64 with two) than CTA slots (one per SM, or the max_workers cap).
 STREAMK = [
-    # (in_dtype, batch, L, D, sg, warps per scheduler, h0, z)
-    ("bf16", 19, 100, 1000, 1, 2, True, True),    # 608 blocks on 592 warps: most ranges hand over
-    ("bf16", 19, 100, 1000, 2, 2, False, True),   # 1197 blocks on 1184 warps
-    ("bf16", 19, 100, 1000, 2, 1, True, True),    # 1197 blocks on 592 warps: two blocks per range
-    ("f32", 19, 33, 1000, 1, 2, True, False),     # two tiles per block, the second ragged
-    ("f32", 20, 1000, 960, 2, 4, False, True),    # 32 tiles per block, 1200 blocks on 1184 warps
+    # (in_dtype, batch, L, D, sg, max_workers, h0, z)
+    ("bf16", 19, 100, 1000, 1, 0, True, True),     # 152 blocks of 2 tiles on one CTA per SM: most ranges hand over
+    ("bf16", 19, 100, 1000, 2, 0, False, True),    # 304 blocks
+    ("bf16", 19, 100, 1000, 2, 100, True, True),   # 304 blocks on 100 CTAs: three blocks per range
+    ("f32", 19, 33, 1000, 1, 0, True, False),      # two tiles per block, the second ragged
+    ("f32", 20, 1000, 960, 2, 0, False, True),     # 32 tiles per block, 300 blocks
+    ("bf16", 3, 100, 640, 1, 4, True, True),       # 15 blocks on 4 CTAs
 ]
 
 
 @pytest.mark.parametrize("case", STREAMK, ids=[f"{c[0]}-b{c[1]}-L{c[2]}-D{c[3]}-sg{c[4]}-w{c[5]}" for c in STREAMK])
 def test_streamk_handover(case):
-    dt, Bt, L, Dm, sg, wps, h0, hz = case
+    dt, Bt, L, Dm, sg, workers, h0, hz = case
     x = gen.random_scan_inputs(Bt, L, Dm, 16, in_dtype=dt, seed=3 * L + Dm + sg, with_h0=h0, has_z=hz,
                                a_log_jitter=0.2)
-    ss.ss_scan_set_tuning(sg, 0, wps)
+    ss.ss_scan_set_tuning(sg, 0, workers)
     try:
         assert ss.ss_scan_fwd_workspace_size(Bt, L, Dm) > 0  # the split mode needs its hand-over buffer
     finally:
         ss.ss_scan_set_tuning(0, 0, 0)
     yr, hr = oracle.scan(x)
-    y, h = run_scan(x, F32, sg=sg, wps=wps)
+    y, h = run_scan(x, F32, sg=sg, workers=workers)
     assert_close(y, yr, _dt(dt), what="stream-K y")
     assert_close(h, hr, _dt(dt), what="stream-K h_last")
 
 
 def test_streamk_matches_static():
     # the split changes no arithmetic: each state sees the same operations in
-    # the same order, so the outputs are bit-identical to one warp per block
+    # the same order, so the outputs are bit-identical to one CTA per block
     x = gen.random_scan_inputs(19, 100, 1000, 16, in_dtype="bf16", seed=12, with_h0=True)
-    y1, h1 = run_scan(x, F32, sg=1, chunk=1 << 30)  # one chunk: one warp per block, whole sequence
-    y2, h2 = run_scan(x, F32, sg=1, wps=2)
+    y1, h1 = run_scan(x, F32, sg=1, chunk=1 << 30)  # one chunk: one CTA per block, whole sequence
+    y2, h2 = run_scan(x, F32, sg=1, workers=7)
     assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
 
 
