@@ -15,9 +15,11 @@
 //
 // Data path. The CTA streams tiles of TILE timesteps through a two-stage ring
 // in shared memory: u, delta_raw, z ([TILE, CC] boxes) and the tile's B and C
-// rows ([TILE, 16]) arrive by TMA (cp.async.bulk.tensor), issued by one thread
-// a tile ahead, with completion counted on one mbarrier per stage. bf16 B/C
-// rows are widened once per tile into fp32 (each warp a quarter) and read by
+// rows ([TILE, 16]) arrive by TMA (cp.async.bulk.tensor), issued a tile ahead
+// by a fifth warp that computes nothing (issuing five bulk loads takes several
+// hundred cycles, which a compute warp would make its CTA wait for at the next
+// barrier), with completion counted on one mbarrier per stage. bf16 B/C rows
+// are widened once per tile into fp32 (each compute warp a quarter) and read by
 // broadcast. One CTA-wide barrier per tile orders the widening and frees the
 // stage the next load overwrites. Only y and the final state leave the chip.
 //
@@ -54,7 +56,8 @@
 namespace ssk {
 namespace scan_detail {
 
-constexpr int kWarps = 4;    // warps per CTA (one per SM sub-partition)
+constexpr int kWarps = 4;    // compute warps per CTA (one per SM sub-partition)
+constexpr int kThreads = 32 * (kWarps + 1);  // plus one warp that issues the tile loads
 constexpr int kStages = 2;   // TMA ring depth (the next tile loads while one is computed)
 constexpr float kStopRel = 5.9604645e-8f;  // 2^-24
 
@@ -106,7 +109,7 @@ __device__ __forceinline__ void widen_bc(const uint8_t* raw_b, float* bcf, int t
 }
 
 template <typename TIn, typename TOut, int SG, bool TMA, bool HAS_Z, int MODE>
-__global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_constant__ ScanParams p,
+__global__ void __launch_bounds__(kThreads, 1) scan_fwd_kernel(const __grid_constant__ ScanParams p,
                                                                   const __grid_constant__ CUtensorMap tm_u,
                                                                   const __grid_constant__ CUtensorMap tm_dr,
                                                                   const __grid_constant__ CUtensorMap tm_z,
@@ -125,10 +128,12 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
   __shared__ uint32_t s_wid;
   __shared__ uint32_t s_flag;
-  const int s = lane % SG;        // which part of the channel's states this lane holds
-  const int cw = lane / SG;       // channel within the warp
-  const int cb = warp * DC + cw;  // channel within the CTA's block
+  const bool producer = warp == kWarps;  // the load-issuing warp
+  const int s = lane % SG;                // which part of the channel's states this lane holds
+  const int cw = lane / SG;               // channel within the warp
+  const int cb = producer ? 0 : warp * DC + cw;  // channel within the CTA's block
   const int n0 = s * NS;
+  const int tid_issue = kWarps * 32;      // the thread that issues the tile loads
 
   // ---- worker index (launch-order ticket in the split modes)
   if (tid == 0) {
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     TIn* su = reinterpret_cast<TIn*>(base + K::OFF_U);
     TIn* sdr = reinterpret_cast<TIn*>(base + K::OFF_DR);
     TIn* sz = reinterpret_cast<TIn*>(base + K::OFF_Z);
-    for (int i = tid; i < TILE * CC; i += 32 * kWarps) {
+    for (int i = tid; i < TILE * CC; i += kThreads) {
       const int tt = i / CC, ch = i % CC;
       const int64_t t = y0 + tt, dd = (int64_t)cu.x0 + ch;
       TIn vu = from_f32<TIn>(0.f), vr = vu, vz = vu;
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     const TIn* gC = static_cast<const TIn*>(p.C);
     TIn* sB = reinterpret_cast<TIn*>(base + K::OFF_B);
     TIn* sC = reinterpret_cast<TIn*>(base + K::OFF_C);
-    for (int i = tid; i < TILE * kDState; i += 32 * kWarps) {
+    for (int i = tid; i < TILE * kDState; i += kThreads) {
       const int64_t t = y0 + i / kDState;
       const bool ok = t < L;
       const int64_t gi = ((int64_t)cu.b * L + (ok ? t : 0)) * kDState + i % kDState;
@@ -291,7 +296,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     const uint8_t* base = smem + cu.st * K::STAGE;
     bool timed_out = false;
     if constexpr (TMA) {
-      timed_out = !mbar_wait(&full[cu.st], cu.ph, wait_ns);
+      if (!producer) timed_out = !mbar_wait(&full[cu.st], cu.ph, wait_ns);
     } else {
       __syncthreads();  // every thread is done with the slot before it is restaged
       load_plain(cu);
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     float* bcf = nullptr;
     if constexpr (K::BF) {
       bcf = reinterpret_cast<float*>(smem + K::OFF_BCF + cu.st * K::BCF);
-      if (!timed_out) widen_bc<TILE>(base + K::OFF_B, bcf, tid);
+      if (!timed_out && !producer) widen_bc<TILE>(base + K::OFF_B, bcf, tid);
     }
     if (__syncthreads_or(timed_out ? 1 : 0)) {
       if (tid == 0) atomicOr(p.fault, kFaultTileWait);
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   auto load_block = [&](int64_t blk) {
     const int64_t b = blk / ncblk;
     d = (blk % ncblk) * CC + cb;
-    dvalid = d < Dm;
+    dvalid = !producer && d < Dm;
     const int64_t dc = dvalid ? d : 0;
 #pragma unroll
     for (int i = 0; i < NP; i++) {
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   hin[0] = 0.f;
 
   // ---- main loop over the worker's steps
-  if (TMA && tid == 0 && nsteps > 0) issue_tma(cc);
+  if (TMA && tid == tid_issue && nsteps > 0) issue_tma(cc);
   int64_t q = 0;
   bool next_issued = nsteps > 0;  // whether step q's load was issued (TMA)
   for (; q < nsteps; q++, advance(cc)) {
@@ -583,7 +588,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
     if (abort) break;
     // the slot of the previous step is free: load the next step into it
     if (TMA && q + 1 < nsteps) {
-      if (tid == 0) {
+      if (tid == tid_issue) {
         Cursor cn = cc;
         advance(cn);
         issue_tma(cn);
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
       next_issued = true;
     }
     const int64_t t0 = j * TILE;
-    run_tile(cc.st, bcf, t0, (int)min((int64_t)TILE, L - t0));
+    if (!producer) run_tile(cc.st, bcf, t0, (int)min((int64_t)TILE, L - t0));
 
     // segment end: final state or hand-over
     if constexpr (MODE == kModeStatic) {
@@ -600,7 +605,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
       if (j == T - 1) {
         if (dvalid && p.h_last) store_h(p.h_last + hoff);
       } else if (q + 1 == zlen) {
-        store_h(p.ws_carry + ((size_t)(wid + 1) * CC + cb) * kDState + n0);
+        if (!producer) store_h(p.ws_carry + ((size_t)(wid + 1) * CC + cb) * kDState + n0);
         publish(p.flags + wid + 1, kFlagHanded, wid + 1 == p.withhold_item);
       }
       if (abort) break;
@@ -618,7 +623,8 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
           A2[2 * i + 1] = f2hi(A2p[i]);
         }
         const bool withhold = tile_id == p.withhold_item;
-        if (c == 0) {
+        if (producer) {
+        } else if (c == 0) {
 #pragma unroll
           for (int n = 0; n < NS; n++) carry_me[32 + n] = hl[n];
         } else {
@@ -654,11 +660,13 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
           }
           if (abort) break;
           // Sa is the true state entering this chunk
+          if (!producer) {
 #pragma unroll
-          for (int n = 0; n < NS; n++) {
-            const float incl = fmaf(carry_me[n], Sa[n], hl[n]);  // P_end * h_in + S_local
-            carry_me[32 + n] = incl;
-            hl[n] = incl;
+            for (int n = 0; n < NS; n++) {
+              const float incl = fmaf(carry_me[n], Sa[n], hl[n]);  // P_end * h_in + S_local
+              carry_me[32 + n] = incl;
+              hl[n] = incl;
+            }
           }
           publish(p.flags + tile_id, kFlagInclusive, withhold);
           if (c == p.nchunks - 1 && dvalid && p.h_last) {
@@ -691,7 +699,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) scan_fwd_kernel(const __grid_c
   }
   // a load issued for a step that was not run must land before the CTA ends
   // (bounded wait on that slot's phase)
-  if (TMA && tid == 0 && next_issued) {
+  if (TMA && tid == tid_issue && next_issued) {
     Cursor cn = cc;
     advance(cn);
     if (!mbar_wait(&full[cn.st], cn.ph, wait_ns)) atomicOr(p.fault, kFaultTileWait);
@@ -753,7 +761,7 @@ cudaError_t launch_t(const ScanParams& p, cudaStream_t stream) {
         !make_map(&mc, p.C, es, p.batch, p.seqlen, kDState, kDState, K::TILE))
       return cudaErrorInvalidValue;
   }
-  kern<<<(unsigned)p.nworkers, 32 * kWarps, smem, stream>>>(p, mu, mdr, mz, mb, mc);
+  kern<<<(unsigned)p.nworkers, kThreads, smem, stream>>>(p, mu, mdr, mz, mb, mc);
   return cudaGetLastError();
 }
 
