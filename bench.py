@@ -246,41 +246,60 @@ def timed_results(st, steps):
     return total, per
 
 
-def bench_e2e(ss, w, x, steps, warmup, out_dtype, dev):
+def bench_e2e(ss, w, x, steps, warmup, out_dtype, dev, nstreams=3):
     """Through the public call with HOST buffers: every step copies its inputs
-    from pinned host memory, runs the scan and copies y and h_last back."""
+    from pinned host memory, runs the scan and copies y and h_last back. The
+    batch elements are independent scans, so each one is copied in, scanned and
+    copied out on one of `nstreams` streams in turn: the copies of one element
+    overlap the scan of another and the two copy directions overlap each other."""
     keys = ("u", "delta_raw", "z", "B", "C")
     host = {k: x[k].pin_memory() for k in keys}
     params = to_dev({k: x[k] for k in ("A", "D", "delta_bias")}, dev)
-    dbuf = {k: torch.empty_like(host[k], device=dev) for k in keys}
     Bt, L, Dm = w.batch, w.seqlen, w.dim
-    y = torch.empty((Bt, L, Dm), dtype=out_dtype, device=dev)
-    h = torch.empty((Bt, Dm, 16), dtype=torch.float32, device=dev)
-    y_host = torch.empty(y.shape, dtype=out_dtype).pin_memory()
-    h_host = torch.empty(h.shape, dtype=torch.float32).pin_memory()
-    ws_bytes = ss.ss_scan_fwd_workspace_size(Bt, L, Dm)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    y_host = torch.empty((Bt, L, Dm), dtype=out_dtype).pin_memory()
+    h_host = torch.empty((Bt, Dm, 16), dtype=torch.float32).pin_memory()
+    S = max(1, min(nstreams, Bt))
+    streams = [torch.cuda.Stream(device=dev) for _ in range(S)]
+    # per-stream device buffers for one batch element
+    dbuf = [{k: torch.empty_like(host[k][:1], device=dev) for k in keys} for _ in range(S)]
+    ys = [torch.empty((1, L, Dm), dtype=out_dtype, device=dev) for _ in range(S)]
+    hs = [torch.empty((1, Dm, 16), dtype=torch.float32, device=dev) for _ in range(S)]
+    ws_bytes = ss.ss_scan_fwd_workspace_size(1, L, Dm)
+    wss = [torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None for _ in range(S)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = y.numel() * y.element_size() + h.numel() * 4
+    d2h = y_host.numel() * y_host.element_size() + h_host.numel() * 4
+    main = torch.cuda.current_stream(dev)
 
     def one():
-        for k in keys:
-            dbuf[k].copy_(host[k], non_blocking=True)
-        d = dict(dbuf, **params)
-        scan_call(ss, d, y, h, ws)
-        y_host.copy_(y, non_blocking=True)
-        h_host.copy_(h, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(main)
+        for st in streams:
+            st.wait_event(start)
+        for b in range(Bt):
+            k = b % S
+            with torch.cuda.stream(streams[k]):
+                for key in keys:
+                    dbuf[k][key].copy_(host[key][b:b + 1], non_blocking=True)
+                scan_call(ss, dict(dbuf[k], **params), ys[k], hs[k], wss[k])
+                y_host[b:b + 1].copy_(ys[k], non_blocking=True)
+                h_host[b:b + 1].copy_(hs[k], non_blocking=True)
+        for st in streams:
+            done = torch.cuda.Event()
+            done.record(st)
+            main.wait_event(done)
 
     for _ in range(warmup):
         one()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    a.record(main)
     for _ in range(steps):
         one()
-    b.record()
+    b.record(main)
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps, h2d, d2h
+    for k in range(S):
+        ss.ss_scan_status(wss[k], stream=streams[k])
+    return a.elapsed_time(b) / steps, h2d, d2h, S
 
 
 def bench_decode(ss, w, dev, timed_steps=64, warmup=8):
@@ -325,12 +344,32 @@ def bench_decode(ss, w, dev, timed_steps=64, warmup=8):
     b.record()
     torch.cuda.synchronize()
     warm_ms = a.elapsed_time(b) / nwarm
+    # the same back-to-back steps captured in one CUDA graph: the device rate
+    # without a Python call and a launch per step
+    ngraph = 200
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(ngraph):
+            step(i % nin)
+    graph.replay()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(5):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    graph_ms = a.elapsed_time(b) / (5 * ngraph)
+    del graph
     cold_ms = statistics.mean(cold)
     bytes_step = w.algorithmic_bytes_per_step("bf16")
     return {"workload": f"{w.name}: {S} streams x d_inner {Dm} x d_state 16, bf16 inputs/y, fp32 state",
             "steps_per_s": 1e3 / cold_ms, "ms_per_step": cold_ms, "hbm_gbs": bytes_step / (cold_ms * 1e-3) / 1e9,
             "tokens_per_s": S * 1e3 / cold_ms, "l2": "flushed before every timed step (256 MB write, 256 MB read)",
-            "warm_steps_per_s": 1e3 / warm_ms, "warm_note": "1000 back-to-back steps, state may stay in L2"}
+            "warm_steps_per_s": 1e3 / warm_ms,
+            "warm_note": "1000 back-to-back steps, one Python call and launch each (bound by the host dispatch); "
+                         "state may stay in L2",
+            "graph_steps_per_s": 1e3 / graph_ms,
+            "graph_note": f"{ngraph} back-to-back steps captured in one CUDA graph, replayed 5 times; state may stay in L2"}
 
 
 def bench_conv1d(ss, dev, hbm_peak, Bt=4, L=2048, Dm=5120, K=4, reps=20):
@@ -575,6 +614,34 @@ def cpu_baseline_scan(w, x, target_s=12.0):
                       f"{total_t:.1f} s wall", "channel_tokens_per_s": total_ch * w.seqlen / total_t}
 
 
+def cpu_oracle_sample(w, x, target_s=3.0):
+    """The float64 oracle on a bounded sample of channels of workload w: all
+    host cores, and (on the short-sequence layers) one thread, as
+    channel-tokens/s and algorithmic GB/s of the sample."""
+    import oracle
+
+    nthreads = oracle.default_threads()
+    per_ch_bytes = w.algorithmic_bytes("bf16") / (w.batch * w.dim)
+    rng = np.random.default_rng(2)
+    out = {"cores": nthreads}
+    for label, nt in (("all_cores", nthreads), ("one_thread", 1)):
+        if label == "one_thread" and w.seqlen > 65536:
+            continue
+        n, total_ch, total_t = nt, 0, 0.0
+        while total_t < target_s and total_ch < w.batch * w.dim:
+            ch = np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.dim, n)], axis=1)
+            t = time.perf_counter()
+            oracle.scan(x, channels=ch, nthreads=nt)
+            dt = time.perf_counter() - t
+            total_ch += n
+            total_t += dt
+            n = max(nt, int(min(w.batch * w.dim - total_ch, n * max(1.0, (target_s - total_t) / max(dt, 1e-3)))))
+        out[label] = {"channel_tokens_per_s": total_ch * w.seqlen / total_t,
+                      "gbs": per_ch_bytes * total_ch / total_t / 1e9, "threads": nt,
+                      "sample": f"{total_ch} channels x {w.seqlen} tokens, {total_t:.1f} s wall"}
+    return out
+
+
 def run_ours(args, world, rank, local):
     import selective_state_space_130_b300 as ss
 
@@ -636,10 +703,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
 
     if rank == 0 and not args.no_e2e:
-        e2e_ms, h2d, d2h = bench_e2e(ss, w, x, max(3, min(args.steps, 10)), 2, out_dtype, dev)
+        e2e_ms, h2d, d2h, nstr = bench_e2e(ss, w, x, max(3, min(args.steps, 10)), 2, out_dtype, dev)
         result["e2e"] = {"value": round(bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                         "path": "pinned host -> device copies, ss_scan_fwd, device -> pinned host copies"}
+                         "path": "pinned host -> device copies, ss_scan_fwd, device -> pinned host copies, "
+                                 f"one batch element per call on {nstr} streams in turn (copies overlap scans)"}
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_decode:
         result["decode"] = bench_decode(ss, configs.DECODE256, dev)
@@ -661,6 +729,8 @@ def run_ours(args, world, rank, local):
                               "frac_of_hbm_peak": round(bts / (ms * 1e-3) / 1e9 / hbm_peak, 4),
                               "channel_tokens_per_s": wc.channel_tokens / (ms * 1e-3),
                               "launches_per_step": stc["launches_per_step"], "l2": f"{stc['nsets']} rotating sets"}
+            if not args.no_cpu_baseline:
+                extra[wc.name]["cpu_oracle"] = cpu_oracle_sample(wc, xc)
             del stc, xc
             torch.cuda.empty_cache()
         extra["conv1d_front_end"] = bench_conv1d(ss, dev, hbm_peak)
@@ -727,6 +797,10 @@ def profile_launches(args):
         for _ in range(2):
             scan_call(ss, x, y, h, ws)
         ss.ss_scan_status(ws)
+    elif args.profile == "conv1d":
+        x = to_dev(gen.random_conv_inputs(4, 2048, 5120, 4, "bf16", seed=20), dev)
+        for _ in range(2):
+            ss.ss_conv1d_fwd(x["x"], x["weight"], x["bias"], None)
     elif args.profile == "ssd":
         x = to_dev(gen.random_ssd_inputs(4, 2048, 80, 64, 128, 1, in_dtype="bf16", seed=11), dev)
         for _ in range(2):
@@ -770,7 +844,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general", "ssd"], default=None,
+    ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general", "ssd", "conv1d"], default=None,
                     help="run 2 launches of one kernel (for an ncu capture of the 2nd) and exit")
     args = ap.parse_args()
     if args.profile:
