@@ -380,7 +380,9 @@ ss_status ss_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t widt
                              : cudaMemsetAsync(state_out, 0, bytes, s);
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
   }
-  ssk::ConvParams p{x, weight, bias, state_in, y, state_out, batch, seqlen, dim, (int)width, silu_on ? 1 : 0};
+  ssk::ConvParams p{x, weight, bias, state_in, y, state_out, batch, seqlen, dim, (int)width, silu_on ? 1 : 0,
+                    ssk::device_fault_word()};
+  if (!p.fault) return fail(SS_ERR_CUDA, "cannot resolve the library fault word");
   const bool vec = ((size_t)dim * dsize(in_dtype)) % 16 == 0;
   cudaError_t e = ssk::launch_conv1d_fwd(p, in_dtype, out_dtype, vec, s);
   if (e != cudaSuccess) return cuda_fail(e, "conv1d launch");
@@ -406,7 +408,7 @@ ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width, ss_dtype i
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
   ss_status st = check_device();
   if (st != SS_OK) return st;
-  ssk::ConvParams p{x, weight, bias, nullptr, y, state, batch, 1, dim, (int)width, silu_on ? 1 : 0};
+  ssk::ConvParams p{x, weight, bias, nullptr, y, state, batch, 1, dim, (int)width, silu_on ? 1 : 0, nullptr};
   // whole 16-byte vectors of channels per thread when a vector never straddles two batch rows
   const bool vec = ((size_t)dim * dsize(in_dtype)) % 16 == 0;
   cudaError_t e = ssk::launch_conv1d_update(p, in_dtype, out_dtype, vec, static_cast<cudaStream_t>(stream));

@@ -11,14 +11,19 @@
 // oldest first.
 //
 // Both kernels are HBM-bound streams: the forward reads x once and writes y
-// once (plus a halo of K-1 rows per 8-row chunk, served by L2). A thread owns
-// one 16-byte vector of channels (8 bf16 or 4 fp32; one channel when the row
-// is not vector-aligned) over kConvTT timesteps and issues every load of its
-// window before any arithmetic: 11 x 16 B in flight per thread, two blocks of
-// 256 threads per SM. Warps cover
-// consecutive channel vectors, so each row access is a contiguous 512 B.
+// once (plus a halo of K-1 rows per tile, served by L2).
+//  - Rows of 16-byte-aligned width stream through shared memory: persistent
+//    CTAs take tiles of [64 timesteps + halo, 256 bytes of channels] in turn; a
+//    producer warp keeps a four-stage ring of TMA (cp.async.bulk.tensor) loads
+//    in flight, so the HBM requests never pause while a tile is computed, and
+//    four compute warps run the taps, bias and SiLU on channel pairs as packed
+//    f32x2 arithmetic.
+//  - Other rows: a thread owns one channel over kConvTT timesteps and issues
+//    every load of its window before any arithmetic.
 #include <cuda_bf16.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "ss_device.cuh"
 #include "ss_internal.h"
@@ -337,6 +342,214 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_update_kernel(const __gri
   }
 }
 
+
+// ---------------------------------------------------------------- TMA-streamed forward pass
+constexpr int kTT = 64;         // timesteps per tile
+constexpr int kRing = 4;        // ring stages
+constexpr int kCompute = 4;     // compute warps (plus one producer warp)
+
+template <typename TIn, int K>
+struct ConvTile {
+  static constexpr int H = K - 1;
+  static constexpr int CB = 256 / (int)sizeof(TIn);  // channels per tile (256-byte rows)
+  static constexpr int ROWS = kTT + H;                // box height: the tile and its halo
+  static constexpr int STAGE = ROWS * 256;            // bytes per ring stage (a multiple of 128)
+  static constexpr int NPAIR = CB / 2;
+  static constexpr int SPLIT = 32 * kCompute / NPAIR; // threads per channel pair (row ranges)
+  static constexpr int RPT = kTT / SPLIT;             // output rows per thread
+  static constexpr int OFF_BAR = kRing * STAGE;
+  static constexpr int SMEM = OFF_BAR + 2 * kRing * 8 + 128;
+};
+
+template <typename TIn, typename TOut, int K, bool SILU>
+__global__ void __launch_bounds__(32 * (kCompute + 1), 2) conv1d_fwd_tma_kernel(const __grid_constant__ ConvParams p,
+                                                                            const __grid_constant__ CUtensorMap tm_x) {
+  using CT = ConvTile<TIn, K>;
+  constexpr int H = CT::H, CB = CT::CB, NPAIR = CT::NPAIR, RPT = CT::RPT;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
+  uint8_t* smem = smem_raw + pad;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CT::OFF_BAR);
+  uint64_t* empty = full + kRing;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kRing; i++) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCompute);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t L = p.seqlen, Dm = p.dim;
+  const int64_t ntile = (L + kTT - 1) / kTT, ncb = (Dm + CB - 1) / CB;
+  const int64_t nunits = p.batch * ntile * ncb;
+  const int64_t G = gridDim.x;
+  // unit u: channel block u % ncb, tile (u / ncb) % ntile, batch element u / (ncb * ntile)
+
+  if (warp == kCompute) {
+    // ---- producer: one thread keeps the ring full
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      int64_t k = 0;
+      for (int64_t u = blockIdx.x; u < nunits; u += G, k++) {
+        const int s = (int)(k % kRing);
+        if (k >= kRing && !mbar_wait(&empty[s], (uint32_t)(((k / kRing) - 1) & 1))) {
+          atomicOr(p.fault, kFaultTileWait);
+          break;
+        }
+        const int64_t cbk = u % ncb, rest = u / ncb;
+        const int64_t j = rest % ntile, b = rest / ntile;
+        fence_proxy_async_smem();
+        mbar_expect_tx(&full[s], CT::STAGE);
+        tma_load_3d(smem + s * CT::STAGE, &tm_x, (int)(cbk * CB), (int)(j * kTT - H), (int)b, &full[s]);
+        mbar_arrive(&full[s]);
+      }
+    }
+    return;
+  }
+
+  // ---- compute warps: thread = (channel pair q, row range rr)
+  const int q = tid % NPAIR, rr = tid / NPAIR;
+  const int r0 = rr * RPT;  // first output row of the range in the tile
+  int64_t k = 0;
+  for (int64_t u = blockIdx.x; u < nunits; u += G, k++) {
+    const int s = (int)(k % kRing);
+    const bool ok = mbar_wait(&full[s], (uint32_t)((k / kRing) & 1));
+    if (__any_sync(0xffffffffu, !ok)) {  // warp-uniform
+      if (lane == 0) atomicOr(p.fault, kFaultTileWait);
+      break;
+    }
+    const int64_t cbk = u % ncb, rest = u / ncb;
+    const int64_t j = rest % ntile, b = rest / ntile;
+    const int64_t t0 = j * kTT, d = cbk * CB + 2 * q;  // first timestep of the tile, first channel of the pair
+    const bool dv = d < Dm;                           // Dm is even here: the pair is whole or absent
+    TIn* tile = reinterpret_cast<TIn*>(smem + s * CT::STAGE);  // row i = timestep t0 - H + i
+    const TIn* gs = static_cast<const TIn*>(p.state_in);
+    // rows before t = 0 (zero-filled by the load) come from the carried state;
+    // only the thread range that reads them patches its own pair's columns
+    const bool patch = j == 0 && gs && rr == 0 && dv;
+    if (patch) {
+#pragma unroll
+      for (int i = 0; i < H; i++) {
+        tile[i * CB + 2 * q] = gs[(b * Dm + d) * H + i];
+        tile[i * CB + 2 * q + 1] = gs[(b * Dm + d + 1) * H + i];
+      }
+    }
+    // taps and bias of the pair: w2[k] = (w[d][k], w[d+1][k])
+    f2 w2[K], bias2 = pk(0.f, 0.f);
+    if (dv) {
+      float wf[2 * K];
+#pragma unroll
+      for (int i = 0; i < K; i++) {  // 2K contiguous floats, 8-byte aligned (d even)
+        const float2 v = __ldg(reinterpret_cast<const float2*>(p.w + d * K) + i);
+        wf[2 * i] = v.x;
+        wf[2 * i + 1] = v.y;
+      }
+#pragma unroll
+      for (int i = 0; i < K; i++) w2[i] = pk(wf[i], wf[K + i]);
+      if (p.bias) {
+        const float2 bv = __ldg(reinterpret_cast<const float2*>(p.bias + d));
+        bias2 = pk(bv.x, bv.y);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < K; i++) w2[i] = pk(0.f, 0.f);
+    }
+    auto ld_pair = [&](int row) -> f2 {  // widened (channel d, channel d+1) of tile row `row`
+      if constexpr (sizeof(TIn) == 4) {
+        const float2 v = *reinterpret_cast<const float2*>(tile + row * CB + 2 * q);
+        return pk(v.x, v.y);
+      } else {
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(tile + row * CB + 2 * q);
+        return pk(__uint_as_float(wd << 16), __uint_as_float(wd & 0xffff0000u));
+      }
+    };
+    // sliding window over the tile rows r .. r+H for output row r
+    f2 win[K];
+#pragma unroll
+    for (int i = 0; i < H; i++) win[i] = ld_pair(r0 + i);
+    TOut* yrow = static_cast<TOut*>(p.y) + (b * L + t0 + r0) * Dm + d;
+#pragma unroll 8
+    for (int r = 0; r < RPT; r++) {
+      win[H] = ld_pair(r0 + r + H);
+      f2 a = bias2;
+#pragma unroll
+      for (int i = 0; i < K; i++) a = fma2(w2[i], win[i], a);
+      if (SILU) a = silu2(a);
+      if (dv && t0 + r0 + r < L) {
+        if constexpr (sizeof(TOut) == 2) {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(f2lo(a), f2hi(a));
+          __stcs(reinterpret_cast<unsigned int*>(yrow), *reinterpret_cast<const unsigned int*>(&h2));
+        } else {
+          __stcs(reinterpret_cast<float2*>(yrow), make_float2(f2lo(a), f2hi(a)));
+        }
+      }
+      yrow += Dm;
+#pragma unroll
+      for (int i = 0; i < H; i++) win[i] = win[i + 1];
+    }
+    // the tile holding the last timestep hands on the last H inputs (raw bits)
+    if (p.state_out && j == ntile - 1 && rr == 0 && dv) {
+      TIn* so = static_cast<TIn*>(p.state_out);
+#pragma unroll
+      for (int i = 0; i < H; i++) {
+        const int64_t row = (L - H + i) - (t0 - H);  // tile row of timestep L-H+i (>= 0: t0 <= L-1)
+        so[(b * Dm + d) * H + i] = tile[row * CB + 2 * q];
+        so[(b * Dm + d + 1) * H + i] = tile[row * CB + 2 * q + 1];
+      }
+    }
+    // the stage may be refilled by the next load: order this thread's
+    // shared-memory writes before that async-proxy write
+    if (patch) fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+using ConvEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline ConvEncodeFn conv_encode_fn() {
+  static const ConvEncodeFn fn = []() -> ConvEncodeFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<ConvEncodeFn>(f);
+    return nullptr;
+  }();
+  return fn;
+}
+
+template <typename TIn, typename TOut, int K>
+cudaError_t launch_fwd_tma(const ConvParams& p, cudaStream_t s) {
+  using CT = ConvTile<TIn, K>;
+  ConvEncodeFn fn = conv_encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  CUtensorMap m{};
+  const size_t es = sizeof(TIn);
+  cuuint64_t dims[3] = {(cuuint64_t)p.dim, (cuuint64_t)p.seqlen, (cuuint64_t)p.batch};
+  cuuint64_t strides[2] = {(cuuint64_t)p.dim * es, (cuuint64_t)p.seqlen * p.dim * es};
+  cuuint32_t box[3] = {(cuuint32_t)CT::CB, (cuuint32_t)CT::ROWS, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (fn(&m, dt, 3, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+      CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int64_t ntile = (p.seqlen + kTT - 1) / kTT, ncb = (p.dim + CT::CB - 1) / CT::CB;
+  const int64_t nunits = p.batch * ntile * ncb;
+  const int sms = device_sm_count();
+  const int64_t grid = std::min<int64_t>(nunits, 2 * (int64_t)sms);
+  auto kern = p.silu ? conv1d_fwd_tma_kernel<TIn, TOut, K, true> : conv1d_fwd_tma_kernel<TIn, TOut, K, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CT::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)grid, 32 * (kCompute + 1), CT::SMEM, s>>>(p, m);
+  return cudaGetLastError();
+}
+
 template <typename TIn, typename TOut, int K, int V>
 cudaError_t launch_fwd_kv(const ConvParams& p, cudaStream_t s) {
   const int64_t nt = (p.seqlen + kConvTT - 1) / kConvTT;
@@ -349,8 +562,9 @@ cudaError_t launch_fwd_kv(const ConvParams& p, cudaStream_t s) {
 
 template <typename TIn, typename TOut, int K>
 cudaError_t launch_fwd_k(const ConvParams& p, bool vec, cudaStream_t s) {
-  constexpr int VV = 16 / (int)sizeof(TIn);
-  return vec ? launch_fwd_kv<TIn, TOut, K, VV>(p, s) : launch_fwd_kv<TIn, TOut, K, 1>(p, s);
+  // 16-byte-aligned rows stream through shared memory by TMA; others take the
+  // per-thread window kernel, one channel per thread
+  return vec ? launch_fwd_tma<TIn, TOut, K>(p, s) : launch_fwd_kv<TIn, TOut, K, 1>(p, s);
 }
 
 template <typename TIn, typename TOut>

@@ -81,6 +81,7 @@ struct ConvParams {
   int64_t batch, seqlen, dim;
   int width;
   int silu;
+  unsigned int* fault;   // the library's fault word (bounded waits of the forward pass)
 };
 
 // Parameters of the scan's backward pass (inputs of the forward, the output
