@@ -339,7 +339,12 @@ void ss_scan_set_wait_limit(uint64_t wait_ns, int64_t withhold_item);
  *    anything is launched; use ss_scan_fwd with a workspace for it.
  *  - The first call on each device looks up the array's device address (with
  *    that device current) and keeps it; make that first call before any CUDA
- *    stream capture begins.
+ *    stream capture begins. The address belongs to the device's primary
+ *    context (the one the CUDA runtime uses): calls must come from that
+ *    context, and none may follow a cudaDeviceReset() of the device in the
+ *    same process (the kept address would then be stale).
+ *  - Argument errors (sizes, dtypes, NULL or misaligned pointers) are reported
+ *    before any device call, as by ss_scan_fwd.
  *  - All calls on a device share the one array. Each call clears, on its
  *    stream, the part that must start at zero. Calls that overlap on the GPU
  *    (different streams, or different host threads without ordering) race on

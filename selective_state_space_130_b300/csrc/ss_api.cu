@@ -193,15 +193,14 @@ size_t scan_bind_workspace(ScanParams& p, const ScanPlan& plan, void* workspace)
 
 namespace {
 
-// Argument checks, planning and launch shared by ss_scan_fwd and
-// ss_scan_fwd_noalloc. `workspace` is the caller's buffer or the library's
-// scratch; `own_fault` routes device-side timeouts to the library's fault word
-// instead of the workspace header.
-ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
-                      ss_dtype out_dtype, const void* u, const void* delta_raw, const float* A, const void* B,
-                      const void* C, const float* D, const void* z, const float* delta_bias, const float* h0,
-                      void* y, float* h_last, void* workspace, size_t workspace_bytes, bool noalloc,
-                      void* stream) {
+// Checks of the scan's arguments that need no device (sizes, dtypes, NULL
+// and misaligned pointers), shared by ss_scan_fwd and ss_scan_fwd_noalloc.
+// Sets *empty when the problem has no channel (nothing to do).
+ss_status scan_check_args(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
+                          ss_dtype out_dtype, const void* u, const void* delta_raw, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias, const float* h0,
+                          const void* y, const float* h_last, const void* workspace, bool* empty) {
+  *empty = false;
   if (dstate != ssk::kDState) return fail(SS_ERR_UNSUPPORTED, "dstate must be 16 (got %lld)", (long long)dstate);
   if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
     return fail(SS_ERR_UNSUPPORTED, "unknown dtype (in %d, out %d)", (int)in_dtype, (int)out_dtype);
@@ -210,7 +209,10 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
                 (long long)seqlen, (long long)dim);
   if (batch > INT32_MAX || seqlen > INT32_MAX || dim > INT32_MAX)
     return fail(SS_ERR_INVALID_ARG, "a size exceeds 2^31-1");
-  if (batch == 0 || dim == 0) return SS_OK;
+  if (batch == 0 || dim == 0) {
+    *empty = true;
+    return SS_OK;
+  }
   if ((double)batch * (double)seqlen * (double)dim > 4.0e18) return fail(SS_ERR_INVALID_ARG, "problem too large");
   const void* need[] = {u, delta_raw, A, B, C, y};
   const char* names[] = {"u", "delta_raw", "A", "B", "C", "y"};
@@ -222,6 +224,22 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last", "workspace"};
   for (int i = 0; i < 12; i++)
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  return SS_OK;
+}
+
+// Argument checks, planning and launch shared by ss_scan_fwd and
+// ss_scan_fwd_noalloc. `workspace` is the caller's buffer or the library's
+// scratch; `noalloc` routes device-side timeouts to the library's fault word
+// instead of the workspace header.
+ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
+                      ss_dtype out_dtype, const void* u, const void* delta_raw, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias, const float* h0,
+                      void* y, float* h_last, void* workspace, size_t workspace_bytes, bool noalloc,
+                      void* stream) {
+  bool empty = false;
+  ss_status st0 = scan_check_args(batch, seqlen, dim, dstate, in_dtype, out_dtype, u, delta_raw, A, B, C, D, z,
+                                  delta_bias, h0, y, h_last, workspace, &empty);
+  if (st0 != SS_OK || empty) return st0;
   const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim, in_dtype, ssk::device_sm_count());
   if (seqlen > 0 && plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) {
     if (noalloc)
@@ -695,8 +713,12 @@ extern "C" ss_status ss_scan_fwd_noalloc(int64_t batch, int64_t seqlen, int64_t 
                                          const float* D, const void* z, const float* delta_bias, const float* h0,
                                          void* y, float* h_last, void* stream) {
   g_err.clear();
-  // sizes beyond the fixed scratch are refused before any device call
-  if (batch > 0 && seqlen > 0 && dim > 0 && dstate == ssk::kDState && valid_dtype(in_dtype)) {
+  // argument checks, then sizes beyond the fixed scratch, before any device call
+  bool empty = false;
+  ss_status st0 = scan_check_args(batch, seqlen, dim, dstate, in_dtype, out_dtype, u, delta_raw, A, B, C, D, z,
+                                  delta_bias, h0, y, h_last, nullptr, &empty);
+  if (st0 != SS_OK || empty) return st0;
+  if (seqlen > 0) {
     const size_t need = ssk::plan_scan(batch, seqlen, dim, in_dtype, ssk::device_sm_count()).workspace;
     if (need > (size_t)SS_SCAN_NOALLOC_SCRATCH_BYTES)
       return fail(SS_ERR_INVALID_ARG,

@@ -208,3 +208,83 @@ def test_ssd_rejects_bad_arguments(kw, code, msg):
 def test_new_entry_points_empty_problems_without_device():
     assert _gen(batch=0) == _lib.SS_OK
     assert _ssd(nheads=0) == _lib.SS_OK
+
+
+# ---------------------------------------------------------------- the scan planner (no device: sizes only)
+HDR = 64 * 4  # workspace header bytes
+
+
+def _ws(batch, seqlen, dim, tuning=(0, 0, 0)):
+    ss.ss_scan_set_tuning(*tuning)
+    try:
+        return ss.ss_scan_fwd_workspace_size(batch, seqlen, dim)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+
+
+def test_plan_follows_the_number_of_cta_slots():
+    # one lane per channel: blocks of 128 channels. 2 x 1000 channels = 16
+    # blocks. With at least 16 CTA slots every block gets its own CTA (no
+    # workspace); with fewer, the equal-range split hands states over between
+    # CTAs through a workspace of one flag and one 128 x 16 fp32 state per CTA.
+    assert _ws(2, 100, 1000, (1, 0, 16)) == 0
+    assert _ws(2, 100, 1000, (1, 0, 148)) == 0
+    for w in (1, 4, 15):
+        flags = (w * 4 + 255) // 256 * 256
+        assert _ws(2, 100, 1000, (1, 0, w)) == HDR + flags + w * 128 * 16 * 4
+    # two lanes per channel: blocks of 64 channels, 32 blocks
+    assert _ws(2, 100, 1000, (2, 0, 32)) == 0
+    assert _ws(2, 100, 1000, (2, 0, 31)) == HDR + 256 + 31 * 64 * 16 * 4
+
+
+def test_plan_chunked_workspace():
+    # forced chunks of 64 steps (bf16 tiles of 64): 1000 steps -> 16 chunks per
+    # block; each (block, chunk) keeps a flag and a 48-float carry per channel
+    need = _ws(1, 1000, 64, (1, 64, 0))
+    items = 1 * 16
+    assert need >= HDR + 256 + items * 128 * 48 * 4
+
+
+# ---------------------------------------------------------------- the no-allocation scan: argument checks
+def _noalloc(**kw):
+    args = dict(batch=1, seqlen=8, dim=8, dstate=16, in_dtype=0, out_dtype=0)
+    args.update({k: v for k, v in kw.items() if k in args})
+    ptrs = dict(u=0x1000, delta_raw=0x2000, A=0x3000, B=0x4000, C=0x5000, D=None, z=None, delta_bias=None,
+                h0=None, y=0x6000, h_last=None)
+    ptrs.update({k: v for k, v in kw.items() if k in ptrs})
+    return ss.lib().ss_scan_fwd_noalloc(args["batch"], args["seqlen"], args["dim"], args["dstate"], args["in_dtype"],
+                                        args["out_dtype"], ptrs["u"], ptrs["delta_raw"], ptrs["A"], ptrs["B"],
+                                        ptrs["C"], ptrs["D"], ptrs["z"], ptrs["delta_bias"], ptrs["h0"], ptrs["y"],
+                                        ptrs["h_last"], None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(dstate=8), _lib.SS_ERR_UNSUPPORTED, "dstate"),
+    (dict(in_dtype=7), _lib.SS_ERR_UNSUPPORTED, "dtype"),
+    (dict(batch=-2), _lib.SS_ERR_INVALID_ARG, "negative"),
+    (dict(dim=1 << 31), _lib.SS_ERR_INVALID_ARG, "2^31"),
+    (dict(u=None), _lib.SS_ERR_INVALID_ARG, "u must not be NULL"),
+    (dict(y=None), _lib.SS_ERR_INVALID_ARG, "y must not be NULL"),
+    (dict(B=0x4004), _lib.SS_ERR_INVALID_ARG, "aligned"),
+    (dict(h_last=0x8008), _lib.SS_ERR_INVALID_ARG, "aligned"),
+])
+def test_noalloc_rejects_bad_arguments_without_device(kw, code, msg):
+    assert _noalloc(**kw) == code
+    assert msg in ss.ss_last_error()
+
+
+def test_noalloc_rejects_oversized_scratch_without_device():
+    # chunks of one 64-step tile over 2^22 steps need far more scratch than the
+    # fixed array: refused before any device call
+    ss.ss_scan_set_tuning(0, 32, 0)
+    try:
+        st = _noalloc(batch=1, seqlen=1 << 22, dim=1024, in_dtype=1, out_dtype=1)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+    assert st == _lib.SS_ERR_INVALID_ARG
+    assert "scratch" in ss.ss_last_error()
+
+
+def test_noalloc_empty_problem_is_ok_without_device():
+    assert _noalloc(batch=0) == _lib.SS_OK
+    assert _noalloc(dim=0) == _lib.SS_OK

@@ -75,3 +75,29 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     assert st == _lib.SS_ERR_INVALID_ARG
     assert "scratch" in ss.ss_last_error()
     torch.cuda.synchronize()
+
+
+def test_noalloc_allocates_nothing():
+    # the entry point exists for callers that cannot allocate: after one
+    # warm-up call (which resolves the scratch array's address and loads the
+    # kernels), a call with preallocated outputs leaves the device's free
+    # memory and torch's allocation count unchanged
+    x = gen.random_scan_inputs(2, 20000, 64, 16, in_dtype="bf16", seed=5, with_h0=True)
+    d = to_dev(x)
+    assert ss.ss_scan_fwd_workspace_size(2, 20000, 64) > 0  # this shape does use the scratch
+    y = torch.empty((2, 20000, 64), dtype=torch.float32, device="cuda")
+    h = torch.empty((2, 64, 16), dtype=torch.float32, device="cuda")
+    ss.ss_scan_fwd_noalloc(*_args(d), y=y, h_last=h)
+    ss.ss_scan_status(None)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    n0 = torch.cuda.memory_stats()["allocation.all.allocated"]
+    ss.ss_scan_fwd_noalloc(*_args(d), y=y, h_last=h)
+    ss.ss_scan_status(None)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    n1 = torch.cuda.memory_stats()["allocation.all.allocated"]
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+    assert n1 == n0, "torch allocated during the call"
+    y_ref, h_ref = _with_workspace(d, torch.float32)
+    assert_close(y.double().cpu().numpy(), y_ref.double().cpu().numpy(), torch.bfloat16, what="y")
