@@ -94,6 +94,20 @@ def _tdt(code: int):
     return torch.bfloat16 if code == SS_BF16 else torch.float32
 
 
+def _out_code(in_code, out_dtype, y):
+    """Output dtype code: out_dtype if given, else that of a given y, else the
+    input dtype. A given y must have the output dtype."""
+    if out_dtype is not None:
+        code = _dt(torch.empty(0, dtype=out_dtype))
+    elif y is not None:
+        code = _dt(y)
+    else:
+        code = in_code
+    if y is not None and _dt(y) != code:
+        raise TypeError(f"y has dtype {y.dtype}, the output dtype is {_tdt(code)}")
+    return code
+
+
 def _ptr(t):
     if t is None:
         return None
@@ -141,7 +155,7 @@ def ss_scan_fwd(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, h0=None,
     Bt, L, Dm = u.shape
     N = B.shape[-1]
     code = _dt(u)
-    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    out_code = _out_code(code, out_dtype, y)
     dev = u.device
     if y is None:
         y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=dev)
@@ -208,7 +222,7 @@ def ss_scan_fwd_general(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, 
     N = A.shape[1]
     G = 1 if B.dim() == 3 else B.shape[2]
     code = _dt(u)
-    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    out_code = _out_code(code, out_dtype, y)
     dev = u.device
     if y is None:
         y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=dev)
@@ -228,7 +242,7 @@ def ss_ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, out_dtype=None,
     Bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     code = _dt(x)
-    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    out_code = _out_code(code, out_dtype, y)
     dev = x.device
     if y is None:
         y = torch.empty((Bt, L, H, P), dtype=_tdt(out_code), device=dev)
@@ -246,7 +260,7 @@ def ss_state_update(h, u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, *
     S, Dm = u.shape
     N = B.shape[-1]
     code = _dt(u)
-    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    out_code = _out_code(code, out_dtype, y)
     if y is None:
         y = torch.empty((S, Dm), dtype=_tdt(out_code), device=u.device)
     _check(lib().ss_state_update(S, Dm, N, code, out_code, _ptr(h), _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(B),
@@ -270,7 +284,7 @@ def ss_scan_fwd_noalloc(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, 
     Bt, L, Dm = u.shape
     N = B.shape[-1]
     code = _dt(u)
-    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    out_code = _out_code(code, out_dtype, y)
     dev = u.device
     if y is None:
         y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=dev)
@@ -291,7 +305,7 @@ def ss_conv1d_fwd(x, weight, bias=None, state=None, *, silu=True, out_dtype=None
     Bt, L, Dm = x.shape
     K = weight.shape[1]
     code = _dt(x)
-    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    out_code = _out_code(code, out_dtype, y)
     if y is None:
         y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=x.device)
     if state_out is None and return_state:
@@ -307,7 +321,7 @@ def ss_conv1d_update(state, x, weight, bias=None, *, silu=True, out_dtype=None, 
     S, Dm = x.shape
     K = weight.shape[1]
     code = _dt(x)
-    out_code = code if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    out_code = _out_code(code, out_dtype, y)
     if y is None:
         y = torch.empty((S, Dm), dtype=_tdt(out_code), device=x.device)
     _check(lib().ss_conv1d_update(S, Dm, K, code, out_code, _ptr(state), _ptr(x), _ptr(weight), _ptr(bias),
