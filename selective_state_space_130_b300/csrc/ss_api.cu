@@ -633,7 +633,8 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "empty-sequence state copy");
   }
   if ((double)batch * nheads > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
-  ssk::SsdParams p{x, dt, A, B, C, D, dt_bias, h0, y, h_last, batch, seqlen, nheads, ngroups};
+  ssk::SsdParams p{x, dt, A, B, C, D, dt_bias, h0, y, h_last, batch, seqlen, nheads, ngroups,
+                   ssk::device_fault_word(), g_wait_ns};
   cudaError_t e = ssk::launch_ssd_fwd(p, (int)dstate, out_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "state-space-dual launch");
   return SS_OK;

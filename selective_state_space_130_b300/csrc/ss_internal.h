@@ -147,6 +147,8 @@ struct SsdParams {
   void* y;                  // [batch, seqlen, nheads, 64]
   float* h_last;            // [batch, nheads, 64, dstate] or null
   int64_t batch, seqlen, nheads, ngroups;
+  unsigned int* fault;      // the library's fault word (timed-out waits)
+  uint64_t wait_ns;         // limit of a device-side wait; 0 = the default
 };
 
 // Launch plan for a scan problem.
@@ -198,6 +200,8 @@ cudaError_t launch_scan_general(const GenParams& p, int sg, ss_dtype in_dtype, s
 int scan_general_stage_bytes(int64_t dstate, int ngw_max, ss_dtype in_dtype);
 
 cudaError_t launch_ssd_fwd(const SsdParams& p, int dstate, ss_dtype out_dtype, cudaStream_t stream);
+// d_state 128 on the tcgen05 tensor cores (ss_ssd_tc.cu)
+cudaError_t launch_ssd_fwd_tc(const SsdParams& p, ss_dtype out_dtype, cudaStream_t stream);
 
 // The library's own fault word (device symbol), used when no workspace is given.
 unsigned int* device_fault_word();

@@ -402,9 +402,8 @@ cudaError_t launch_n(const SsdParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_ssd_fwd(const SsdParams& p, int dstate, ss_dtype out_dtype, cudaStream_t stream) {
-  if (dstate == 64)
-    return out_dtype == SS_BF16 ? launch_n<64, __nv_bfloat16>(p, stream) : launch_n<64, float>(p, stream);
-  return out_dtype == SS_BF16 ? launch_n<128, __nv_bfloat16>(p, stream) : launch_n<128, float>(p, stream);
+  if (dstate == 128) return launch_ssd_fwd_tc(p, out_dtype, stream);
+  return out_dtype == SS_BF16 ? launch_n<64, __nv_bfloat16>(p, stream) : launch_n<64, float>(p, stream);
 }
 
 }  // namespace ssk

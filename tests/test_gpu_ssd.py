@@ -33,6 +33,10 @@ SHAPES = [
     (1, 130, 3, 128, 1, True),    # ragged third chunk
     (2, 200, 8, 128, 4, True),    # two heads per group
     (1, 1000, 2, 64, 2, True),    # 16 chunks of carried state
+    (1, 128, 2, 128, 1, True),    # exactly one 128-step chunk of the d_state 128 kernel
+    (1, 129, 2, 128, 2, False),   # one step past it
+    (1, 1000, 2, 128, 2, True),   # eight chunks of carried state, ragged tail
+    (3, 384, 6, 128, 3, True),    # three full chunks, two heads per group
 ]
 
 
