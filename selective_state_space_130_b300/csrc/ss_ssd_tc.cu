@@ -11,27 +11,28 @@
 // Space", section on Mamba-2 reorganising the SSM as matrix computation;
 // mlqm.cn tutorial, section 8). For a chunk of Q = 128 steps, with cs_t the
 // decay (base 2) accumulated inside the chunk and H_in the state entering it:
-//   S = C B^T                                  [t, s]  (K = n)
-//   M = S o 2^(cs_t - cs_s) o delta_s, s <= t  (else 0)
-//   Y = M X + 2^cs_t o (C H_in^T) + D X        [t, p]  (K = s, K = n)
-//   H_out^T = 2^cs_end H_in^T + W^T X,  W = B o 2^(cs_end - cs_s) delta_s   [n, p]  (K = s)
+//   S = C B^T                                              [t, s]  (K = n)
+//   M = S o 2^(cs_t - cs_s) o delta_s for s <= t, else 0; plus D_h on the diagonal
+//   Y = M X + 2^cs_t o (C H_in^T)                           [t, p]  (K = s, K = n)
+//   H_out^T = 2^cs_end H_in^T + B^T X',  X' = diag(2^(cs_end - cs_s) delta_s) X   [n, p]  (K = s)
 //
-// One CTA of four warps owns one (batch, head) and walks its chunks in order;
-// the state stays in registers (thread n holds row n of H^T). Per chunk:
+// One CTA of eight warps owns one (batch, head) and walks its chunks in order;
+// the state stays in registers (two threads per row n of H^T, 32 columns
+// each). Per chunk:
 //  - one thread loads the chunk's C and B (two 64-column boxes each) and x by
-//    TMA with 128-byte swizzling, the layout the tensor core reads;
-//  - S = C B^T runs as eight K=16 steps of tcgen05.mma (M = 128 rows t, N =
-//    128 columns s) into tensor memory;
-//  - thread t reads row t of S from tensor memory (tcgen05.ld) and writes row t
-//    of M; thread s turns row s of B into row s of W in place (B is read only
-//    by S); M, W and the state are computed in fp32 and enter the products as
-//    a bf16 high part and a bf16 remainder (two products each, about 16
-//    significant bits); x, B and C enter as the stored bf16 values;
-//  - Y1 = M X, Y2 = C H_in^T and H_l^T = W^T X run on the tensor core
-//    (operands in shared memory, K-major or MN-major descriptors);
-//  - thread t writes y_t = Y1_t + 2^cs_t Y2_t + D x_t; thread n updates row n of
-//    the state, H^T = 2^cs_end H^T + H_l^T, and writes its two parts for the
-//    next chunk's Y2.
+//    TMA with 128-byte swizzling, the layout the tensor core reads; each load
+//    is issued as soon as the products of the previous chunk have released its
+//    buffer, so it lands while that chunk finishes;
+//  - S = C B^T and Y2 = C H_in^T go to the tensor core together (Y2 needs only
+//    the state entering the chunk);
+//  - the threads scale row s of x by its state weight into X' (then B^T X' goes
+//    to the tensor core) and turn row t of S, read from tensor memory
+//    (tcgen05.ld), into row t of M (then M X goes to the tensor core); M, X'
+//    and the state are computed in fp32 and enter the products as a bf16 high
+//    part and a bf16 remainder (two products each, about 16 significant bits);
+//    x, B and C enter as the stored bf16 values;
+//  - the state update H^T = 2^cs_end H^T + B^T X' runs in registers and writes
+//    the state's two parts for the next chunk; then y_t = Y1_t + 2^cs_t Y2_t.
 // Every wait is bounded and reports a timeout through the library fault word.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -46,9 +47,17 @@ namespace {
 constexpr int kQ = 128;  // chunk length (the rows of every product)
 constexpr int kP = 64;   // head channels
 constexpr int kN = 128;  // state size
-constexpr int kThreads = 256;  // two threads per row of a product, each taking half its columns
-constexpr uint32_t kTmemCols = 512;  // S [0,128), Y1 [128,192), Y2 [192,256), H_l [256,320)
-constexpr uint32_t kColS = 0, kColY1 = 128, kColY2 = 192, kColH = 256;
+constexpr int kComputeWarps = 8;  // two threads per row of a product, each taking half its columns
+constexpr int kCompute = 32 * kComputeWarps;
+constexpr int kThreads = kCompute + 32;  // + one warp that issues the copies and products
+// The compute thread that issues the y stores: one outside warps 0-3, which
+// compute the chunk's scalars (its waits on the stores stay off their path).
+constexpr int kStoreTid = 128;
+// Tensor-memory columns: S [0,128), Y1 [128,192), Y2 [192,320) (the products
+// with the state's high part, then with its remainder), H_l [320,448) (with
+// X''s high part, then its remainder), the state [448,512)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColY1 = 128, kColY2 = 192, kColH = 320, kColState = 448;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base). A "tile" is
 // 128 rows of 128 bytes (64 bf16) in the 128-byte swizzle: the 16-byte piece c
@@ -57,11 +66,11 @@ struct TcSmem {
   static constexpr int TILE = 128 * 128;      // 16 KB
   static constexpr int C0 = 0;                // C [t][n 0..63], C1 = n 64..127
   static constexpr int C1 = C0 + TILE;
-  static constexpr int B0 = C1 + TILE;        // B [s][n 0..63] (then W's high part), B1 = n 64..127
+  static constexpr int B0 = C1 + TILE;        // B [s][n 0..63], B1 = n 64..127
   static constexpr int B1 = B0 + TILE;
-  static constexpr int WL0 = B1 + TILE;       // W's remainder [s][n 0..63], WL1 = n 64..127
-  static constexpr int WL1 = WL0 + TILE;
-  static constexpr int X = WL1 + TILE;        // x [s][p]
+  static constexpr int XH = B1 + TILE;        // X' high [s][p]
+  static constexpr int XL = XH + TILE;        // X' remainder
+  static constexpr int X = XL + TILE;         // x [s][p]
   static constexpr int MH0 = X + TILE;        // M high [t][s 0..63], MH1 = s 64..127
   static constexpr int MH1 = MH0 + TILE;
   static constexpr int ML0 = MH1 + TILE;      // M remainder
@@ -71,8 +80,9 @@ struct TcSmem {
   static constexpr int DL = HL + TILE;        // delta_t [128] f32
   static constexpr int CS = DL + 512;         // cs_t [128] f32
   static constexpr int WSUM = CS + 512;       // warp sums of the prefix scan [4] f32
-  static constexpr int BAR = WSUM + 64;       // mbarriers: tma_cb, tma_x, mma_s, mma_rest
-  static constexpr int TSLOT = BAR + 64;      // tensor-memory base address
+  static constexpr int DTB = WSUM + 64;       // dt words of two chunks [2][128] u32 (see the kernel)
+  static constexpr int BAR = DTB + 1024;      // mbarriers, see the kernel (at most 16)
+  static constexpr int TSLOT = BAR + 128;     // tensor-memory base address
   static constexpr int BYTES = TSLOT + 64;
   static constexpr int ALLOC = BYTES + 1024;  // + alignment slack
 };
@@ -111,9 +121,9 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// 32 consecutive fp32 columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 32 consecutive fp32 columns of this thread's tensor-memory lane, without
+// waiting: the registers are valid after tmem_wait_ld
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -122,9 +132,61 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+// wait for this thread's tensor-memory loads; r is passed through so that no
+// use of it is scheduled before the wait
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+// store 32 consecutive fp32 columns of this thread's tensor-memory lane and
+// wait for the store
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 4-D tiled TMA store from shared memory (coordinates innermost first; the
+// parts of the box outside the tensor are not written)
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// One product over K = 128 as eight K = 16 steps. Operands are tiles of 128
+// rows x 128 bytes in the 128-byte swizzle at shared addresses a and b. A
+// K-major operand holds K in two 64-column tiles one tile apart (a step is 32
+// bytes along the row, the second four steps in the next tile); an MN-major
+// operand holds K along its rows (a step is 16 rows, 2048 bytes). a_lbo,
+// b_lbo: the leading byte offsets (for an MN-major operand 128 wide, the
+// distance between its two 64-wide halves). The step is added to the
+// descriptor's address field (bytes / 16).
+__device__ __forceinline__ void mma_k128(uint32_t d, uint32_t a, bool a_kmajor, uint32_t b, bool b_kmajor,
+                                         uint32_t a_lbo, uint32_t b_lbo, uint32_t id) {
+  const uint64_t ad = sdesc(a, a_lbo, 1024), bd = sdesc(b, b_lbo, 1024);
+#pragma unroll 1
+  for (int kk = 0; kk < 8; kk++) {
+    const uint32_t kstep = (uint32_t)((kk & 3) * 2 + (kk >> 2) * (128 * 128 / 16));  // K-major
+    const uint32_t mstep = (uint32_t)(kk * 128);                                      // MN-major
+    mma(d, ad + (a_kmajor ? kstep : mstep), bd + (b_kmajor ? kstep : mstep), id, kk > 0);
+  }
 }
 // 4-D tiled TMA load (coordinates innermost first)
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
@@ -134,6 +196,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
+}
+// 16-byte shared-memory load that the compiler keeps in program order with
+// the surrounding memory accesses
+__device__ __forceinline__ float4 lds_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
 }
 // eight floats -> eight bf16 (16 bytes), high part and remainder
 __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
@@ -158,41 +230,51 @@ __device__ __forceinline__ void widen8(uint4 w, float (&v)[8]) {
   }
 }
 
+__device__ __forceinline__ void bar_sync_compute() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// barrier over the 256 compute threads that returns the OR of v over them
+__device__ __forceinline__ bool bar_or_compute(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, 256, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 template <typename TOut>
 __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_constant__ SsdParams p,
                                                             const __grid_constant__ CUtensorMap tm_x,
                                                             const __grid_constant__ CUtensorMap tm_b,
-                                                            const __grid_constant__ CUtensorMap tm_c) {
+                                                            const __grid_constant__ CUtensorMap tm_c,
+                                                            const __grid_constant__ CUtensorMap tm_y) {
   using SM = TcSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t s0 = smem_u32(sm);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SM::BAR);  // 0 C and B, 1 x, 2 S product, 3 the other products
+  // Barriers. Completed by the copy engine or the tensor core: C and B
+  // loaded, x loaded, S done, Y1 done, Y2 done, B^T X' done. Completed by the
+  // 256 compute threads: X' written, M written (S read), state written (B^T X'
+  // read), y written (Y1 and Y2 read).
+  // The last one: the M tiles, which stage y, are free again (thread 0).
+  enum { kBarCB = 0, kBarX, kBarS, kBarY1, kBarY2, kBarH, kRdyX, kRdyM, kRdyH, kRdyY, kStg, kNumBars };
+  static_assert(kNumBars * 8 <= SM::TSLOT - SM::BAR, "the barriers overlap the tensor-memory slot");
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SM::BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM::TSLOT);
   float* dls = reinterpret_cast<float*>(sm + SM::DL);
   float* css = reinterpret_cast<float*>(sm + SM::CS);
   float* wsum = reinterpret_cast<float*>(sm + SM::WSUM);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = tid & (kQ - 1);  // row of the products this thread reads and writes
-  const int hf = tid >> 7;         // which half of the columns
-  const int wq = warp & 3;         // the warp's tensor-memory lane quarter: rows 32wq .. 32wq+31
   const int64_t bh = blockIdx.x;
   const int64_t b = bh / p.nheads, h = bh % p.nheads;
   const int64_t L = p.seqlen, H = p.nheads, G = p.ngroups;
-  const int grp = (int)(h / (H / G));
-  const float a2 = __ldg(p.A + h) * kLog2e;  // decay exponent per unit delta, base 2
-  const float dtb = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
-  const float Dh = p.D ? __ldg(p.D + h) : 0.f;
-  const __nv_bfloat16* DT = static_cast<const __nv_bfloat16*>(p.dt);
   const int64_t nchunk = (L + kQ - 1) / kQ;
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
 
   if (tid == 0) {
-    for (int i = 0; i < 4; i++) mbar_init(&bar[i], 1);
+    for (int i = 0; i < kNumBars; i++) mbar_init(&bar[i], (i < kRdyX || i == kStg) ? 1 : kCompute);
     fence_mbar_init();
-    tma_prefetch_desc(&tm_x);
-    tma_prefetch_desc(&tm_b);
-    tma_prefetch_desc(&tm_c);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
@@ -204,253 +286,370 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tlane = tmem + ((uint32_t)(wq * 32) << 16);  // this warp's tensor-memory lanes
-
-  // what thread 0 has issued and nobody has waited for yet (for the drain
-  // after a timed-out wait), and the phase each barrier is at
-  bool pend[4] = {false, false, false, false};
-  uint32_t ph[4] = {0, 0, 0, 0};
-  auto issue_cb = [&](int64_t c) {
-    const int t0 = (int)(c * kQ);
-    mbar_expect_tx(&bar[0], 4 * SM::TILE);
-    tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, (int)b, &bar[0]);
-    tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, (int)b, &bar[0]);
-    tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, (int)b, &bar[0]);
-    tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, (int)b, &bar[0]);
-    mbar_arrive(&bar[0]);
-    pend[0] = true;
-  };
-  auto issue_x = [&](int64_t c) {
-    mbar_expect_tx(&bar[1], SM::TILE);
-    tma_load_4d(sm + SM::X, &tm_x, 0, (int)h, (int)(c * kQ), (int)b, &bar[1]);
-    mbar_arrive(&bar[1]);
-    pend[1] = true;
-  };
-  // every thread waits for barrier i; false (for the whole CTA) if any gave up
-  auto wait_all = [&](int i) -> bool {
-    const bool mine = mbar_wait(&bar[i], ph[i], wait_ns);
-    if (__syncthreads_or(mine ? 0 : 1)) {
-      if (tid == 0) atomicOr(p.fault, kFaultTileWait);
-      return false;
+  uint32_t ph = 0;    // bit i: the phase of barrier i this thread waits for next
+  bool fail = false;  // this thread gave up on a wait
+  // wait for the next phase of barrier i; after a timeout the phase stays
+  // (it is the one still in flight)
+  auto wait = [&](int i) {
+    if (mbar_wait(&bar[i], (ph >> i) & 1u, wait_ns)) {
+      ph ^= 1u << i;
+      return true;
     }
-    ph[i] ^= 1u;
-    pend[i] = false;
-    return true;
+    fail = true;
+    return false;
   };
+  const bool has_h0 = p.h0 != nullptr;
 
-  // the state: thread (row n, half hf) holds H^T[n][32 hf .. 32 hf + 31]
-  float hst[32];
-  {
-    const float* h0 = p.h0 ? p.h0 + (b * H + h) * kP * kN : nullptr;
-#pragma unroll
-    for (int q = 0; q < 32; q++) hst[q] = h0 ? __ldg(h0 + (32 * hf + q) * kN + row) : 0.f;
-  }
-  // the state's two bf16 parts, row n of H^T, for the next chunk's C H^T
-  auto write_state = [&]() {
-#pragma unroll
-    for (int c8 = 0; c8 < 4; c8++) {
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 8; i++) v[i] = hst[8 * c8 + i];
-      uint4 hi, lo;
-      split8(v, hi, lo);
-      *reinterpret_cast<uint4*>(sm + SM::HH + sw128(row, 32 * hf + 8 * c8)) = hi;
-      *reinterpret_cast<uint4*>(sm + SM::HL + sw128(row, 32 * hf + 8 * c8)) = lo;
-    }
-  };
-  bool state_nonzero = p.h0 != nullptr;
-  if (state_nonzero) write_state();
-
-  if (tid == 0 && nchunk > 0) {
-    issue_cb(0);
-    issue_x(0);
-  }
-  bool ok = true;  // CTA-uniform: no wait has timed out
-  for (int64_t c = 0; c < nchunk; c++) {
-    const int64_t t0 = c * kQ;
-    // ---- delta and the decay (base 2) accumulated inside the chunk, inclusive
-    {
-      float dl = 0.f, sc = 0.f;
-      if (hf == 0) {
-        dl = t0 + row < L ? softplus_fast(__bfloat162float(DT[(b * L + t0 + row) * H + h]) + dtb) : 0.f;
-        sc = dl * a2;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_up_sync(0xffffffffu, sc, o);
-          if (lane >= o) sc += v;
+  if (warp == kComputeWarps) {
+    // ============ the issuing warp: one lane loads tiles and runs the products
+    if (lane == 0) {
+      const int grp = (int)(h / (H / G));
+      uint32_t nissue[kRdyX] = {};  // copies or commits issued per barrier (for the drain after a timeout)
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_b);
+      tma_prefetch_desc(&tm_c);
+      auto issue_cb = [&](int64_t c) {
+        const int t0 = (int)(c * kQ);
+        mbar_expect_tx(&bar[kBarCB], 4 * SM::TILE);
+        tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, (int)b, &bar[kBarCB]);
+        tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, (int)b, &bar[kBarCB]);
+        tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, (int)b, &bar[kBarCB]);
+        tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, (int)b, &bar[kBarCB]);
+        mbar_arrive(&bar[kBarCB]);
+        nissue[kBarCB]++;
+      };
+      auto issue_x = [&](int64_t c) {
+        mbar_expect_tx(&bar[kBarX], SM::TILE);
+        tma_load_4d(sm + SM::X, &tm_x, 0, (int)h, (int)(c * kQ), (int)b, &bar[kBarX]);
+        mbar_arrive(&bar[kBarX]);
+        nissue[kBarX]++;
+      };
+      auto commit = [&](int i) {
+        mma_commit(&bar[i]);
+        nissue[i]++;
+      };
+      issue_cb(0);
+      issue_x(0);
+      for (int64_t c = 0; c < nchunk; c++) {
+        // S = C B^T (S's columns were read by the previous chunk's M)
+        if (!wait(kBarCB)) break;
+        tc_fence_after();
+        mma_k128(tmem + kColS, s0 + SM::C0, true, s0 + SM::B0, true, 16, 16, idesc(kQ, kQ, 0, 0));
+        commit(kBarS);
+        // Y2 = C H_in^T, once the state entering the chunk is written and the
+        // previous chunk's y has read Y2's columns
+        if (c > 0 || has_h0) {
+          if (!wait(kRdyH)) break;
+          if (c > 0 && !wait(kRdyY)) break;
+          tc_fence_after();
+          // A K-major (C); B MN-major: H^T's high part and remainder side by
+          // side (N = 128, the two tiles one tile apart)
+          mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HH, false, 16, SM::TILE, idesc(kQ, 2 * kP, 0, 1));
+          commit(kBarY2);
         }
-        if (lane == 31) wsum[warp] = sc;
-      }
-      __syncthreads();
-      if (hf == 0) {
-        for (int w = 0; w < warp; w++) sc += wsum[w];
-        dls[row] = dl;
-        css[row] = sc;
-      }
-      __syncthreads();
-    }
-    // ---- S = C B^T
-    if (!(ok = wait_all(0))) break;
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id = idesc(kQ, kQ, 0, 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; kk++) {
-        const uint32_t off = (kk & 3) * 32;
-        const uint64_t ad = sdesc(s0 + (kk < 4 ? SM::C0 : SM::C1) + off, 16, 1024);
-        const uint64_t bd = sdesc(s0 + (kk < 4 ? SM::B0 : SM::B1) + off, 16, 1024);
-        mma(tmem + kColS, ad, bd, id, kk > 0);
-      }
-      mma_commit(&bar[2]);
-      pend[2] = true;
-    }
-    if (!(ok = wait_all(2))) break;
-    tc_fence_after();
-    // ---- M (row t, columns s in half hf) from S; W (row s, columns n in half hf) in place of B
-    {
-      const float cst = css[row];
+        // H_l^T = B^T X' (A = B read MN-major: its two n halves are one tile apart)
+        if (!wait(kBarX) || !wait(kRdyX)) break;
+        tc_fence_after();
+        // (B: X''s high part and remainder side by side, N = 128)
+        mma_k128(tmem + kColH, s0 + SM::B0, false, s0 + SM::XH, false, SM::TILE, SM::TILE, idesc(kN, 2 * kP, 1, 1));
+        commit(kBarH);
+        // Y1 = M X
+        if (!wait(kRdyM)) break;
+        tc_fence_after();
+        {
+          const uint64_t bd = sdesc(s0 + SM::X, 16, 1024);
+          const uint64_t ah = sdesc(s0 + SM::MH0, 16, 1024), al = sdesc(s0 + SM::ML0, 16, 1024);
 #pragma unroll 1
-      for (int j = 0; j < 2; j++) {
-        const int sb = 64 * hf + 32 * j;  // first column s of this block of 32
-        float sv[32];
-        const bool any = sb <= 32 * wq + 31;  // warp-uniform: some row of the warp reaches column sb
-        if (any) tmem_ld32(tlane + kColS + sb, sv);
-#pragma unroll
-        for (int c8 = 0; c8 < 4; c8++) {
-          float v[8];
-#pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const int s = sb + c8 * 8 + i;
-            v[i] = (any && s <= row) ? sv[c8 * 8 + i] * ex2(cst - css[s]) * dls[s] : 0.f;
+          for (int kk = 0; kk < 16; kk++) {  // M's high part, then its remainder, times x
+            const int k = kk & 7;
+            const uint32_t kstep = (uint32_t)((k & 3) * 2 + (k >> 2) * (SM::TILE / 16));
+            mma(tmem + kColY1, (kk < 8 ? ah : al) + kstep, bd + (uint32_t)(k * 128), idesc(kQ, kP, 0, 1), kk > 0);
           }
-          uint4 hi, lo;
-          split8(v, hi, lo);
-          const int col = 32 * j + 8 * c8;
-          *reinterpret_cast<uint4*>(sm + (hf ? SM::MH1 : SM::MH0) + sw128(row, col)) = hi;
-          *reinterpret_cast<uint4*>(sm + (hf ? SM::ML1 : SM::ML0) + sw128(row, col)) = lo;
+        }
+        commit(kBarY1);
+        if (c + 1 < nchunk) {
+          // products complete in issue order: B^T X' done means S and Y2 are
+          // too, so C and B are free; Y1 done frees x
+          if (!wait(kBarH)) break;
+          issue_cb(c + 1);
+          if (!wait(kBarY1)) break;
+          issue_x(c + 1);
         }
       }
-      const float ws = ex2(css[kQ - 1] - css[row]) * dls[row];  // 2^(cs_end - cs_s) delta_s, s = row
+      if (fail) {
+        // a wait gave up: record it, and wait (bounded) for the last copy and
+        // product issued on each barrier (the k-th completion of a barrier
+        // ends phase k, of parity k & 1) before shared and tensor memory are
+        // released
+        atomicOr(p.fault, kFaultTileWait);
 #pragma unroll
-      for (int c8 = 0; c8 < 8; c8++) {
-        uint8_t* pb = sm + (hf ? SM::B1 : SM::B0) + sw128(row, 8 * c8);
+        for (int i = 0; i < kRdyX; i++)
+          if (nissue[i]) mbar_wait(&bar[i], (nissue[i] - 1) & 1u, wait_ns);
+      }
+    }
+  } else {
+    // ============ 256 compute threads: two per row of the products
+    const int row = tid & (kQ - 1);  // row of the products this thread reads and writes
+    const int hf = tid >> 7;         // which half of the columns
+    const int wq = warp & 3;         // the warp's tensor-memory lane quarter: rows 32wq .. 32wq+31
+    const uint32_t tlane = tmem + ((uint32_t)(wq * 32) << 16);
+    const float a2 = __ldg(p.A + h) * kLog2e;  // decay exponent per unit delta, base 2
+    const float dtbias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
+    const float Dh = p.D ? __ldg(p.D + h) : 0.f;
+    const __nv_bfloat16* dt_all = static_cast<const __nv_bfloat16*>(p.dt);
+    const int64_t dt_last = p.batch * L * H - 1;  // index of dt's last element
+    uint32_t* dtb = reinterpret_cast<uint32_t*>(sm + SM::DTB);
+    // Row t of chunk c needs dt[b, t, h]. It is fetched a chunk ahead by an
+    // asynchronous 4-byte copy of the aligned pair of bf16 that holds it (a
+    // plain load would be waited for by this thread's next release fence), or,
+    // for dt's very last element when it starts a pair, by a plain load.
+    auto fetch_dt = [&](int64_t c) {
+      const int64_t t = c * kQ + row;
+      uint32_t* dst = dtb + (c & 1) * kQ + row;
+      if (t >= L) return;
+      const int64_t i = (b * L + t) * H + h;
+      if ((i & 1) == 0 && i == dt_last) {
+        *dst = (uint32_t)__bfloat16_as_ushort(dt_all[i]);
+      } else {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(dt_all + (i & ~(int64_t)1))
+                     : "memory");
+      }
+    };
+    auto dt_of = [&](int64_t c) -> float {  // this row's dt in chunk c, once its copy is complete
+      const int64_t i = (b * L + c * kQ + row) * H + h;
+      const uint32_t w = dtb[(c & 1) * kQ + row];
+      return __uint_as_float(((i & 1) ? (w >> 16) : (w & 0xffffu)) << 16);
+    };
+
+    // the state lives in tensor memory: thread (row n, half hf) owns
+    // H^T[n][32 hf .. 32 hf + 31], columns kColState + 32 hf of lane n
+    const uint32_t tstate = tlane + kColState + 32 * hf;
+    // the state's two bf16 parts, row n of H^T, for the next chunk's C H^T
+    auto write_state = [&](const uint32_t (&hv)[32]) {
+#pragma unroll
+      for (int c8 = 0; c8 < 4; c8++) {
         float v[8];
-        widen8(*reinterpret_cast<const uint4*>(pb), v);
 #pragma unroll
-        for (int i = 0; i < 8; i++) v[i] *= ws;
+        for (int i = 0; i < 8; i++) v[i] = __uint_as_float(hv[8 * c8 + i]);
         uint4 hi, lo;
         split8(v, hi, lo);
-        *reinterpret_cast<uint4*>(pb) = hi;
-        *reinterpret_cast<uint4*>(sm + (hf ? SM::WL1 : SM::WL0) + sw128(row, 8 * c8)) = lo;
+        *reinterpret_cast<uint4*>(sm + SM::HH + sw128(row, 32 * hf + 8 * c8)) = hi;
+        *reinterpret_cast<uint4*>(sm + SM::HL + sw128(row, 32 * hf + 8 * c8)) = lo;
       }
-    }
-    fence_proxy_async_smem();  // M, W and the state are read by the tensor core next
-    if (!(ok = wait_all(1))) break;  // x of the chunk; also orders the writes above before the issue
-    // ---- Y1 = M X, H_l^T = W^T X, Y2 = C H_in^T
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idy = idesc(kQ, kP, 0, 1);  // A K-major (M or C), B MN-major (x or H^T)
-      const uint32_t idh = idesc(kN, kP, 1, 1);  // A MN-major (W), B MN-major (x)
-#pragma unroll
-      for (int part = 0; part < 2; part++) {
-        const int mb0 = part ? SM::ML0 : SM::MH0, mb1 = part ? SM::ML1 : SM::MH1;
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const uint64_t ad = sdesc(s0 + (kk < 4 ? mb0 : mb1) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc(s0 + SM::X + kk * 2048, 16, 1024);
-          mma(tmem + kColY1, ad, bd, idy, part > 0 || kk > 0);
-        }
-      }
-#pragma unroll
-      for (int part = 0; part < 2; part++) {
-        // the two 64-column halves (n < 64, n >= 64) of W are one tile apart
-        const int wb = part ? SM::WL0 : SM::B0;
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const uint64_t ad = sdesc(s0 + wb + kk * 2048, SM::TILE, 1024);
-          const uint64_t bd = sdesc(s0 + SM::X + kk * 2048, 16, 1024);
-          mma(tmem + kColH, ad, bd, idh, part > 0 || kk > 0);
-        }
-      }
-      if (state_nonzero) {
-#pragma unroll
-        for (int part = 0; part < 2; part++) {
-          const int hb = part ? SM::HL : SM::HH;
-#pragma unroll
-          for (int kk = 0; kk < 8; kk++) {
-            const uint64_t ad = sdesc(s0 + (kk < 4 ? SM::C0 : SM::C1) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc(s0 + hb + kk * 2048, 16, 1024);
-            mma(tmem + kColY2, ad, bd, idy, part > 0 || kk > 0);
-          }
-        }
-      }
-      mma_commit(&bar[3]);
-      pend[3] = true;
-    }
-    if (!(ok = wait_all(3))) break;
-    tc_fence_after();
-    // C, B (now W) and M are no longer read: load the next chunk's C and B
-    if (tid == 0 && c + 1 < nchunk) issue_cb(c + 1);
-    // ---- y of row t, columns p in half hf: Y1 + 2^cs_t Y2 + D x
+    };
     {
-      const float et = ex2(css[row]);
-      const int pb = 32 * hf;
-      float y1[32], y2[32];
-      tmem_ld32(tlane + kColY1 + pb, y1);
-      if (state_nonzero) tmem_ld32(tlane + kColY2 + pb, y2);
-      if (t0 + row < L) {
-        TOut* yrow = static_cast<TOut*>(p.y) + ((b * L + t0 + row) * H + h) * kP + pb;
+      uint32_t hv[32];
+      const float* h0 = has_h0 ? p.h0 + (b * H + h) * kP * kN : nullptr;
+#pragma unroll
+      for (int q = 0; q < 32; q++) hv[q] = __float_as_uint(h0 ? __ldg(h0 + (32 * hf + q) * kN + row) : 0.f);
+      tmem_st32(tstate, hv);
+      if (has_h0) {
+        write_state(hv);
+        fence_proxy_async_smem();  // read by the tensor core
+      }
+      tc_fence_before();
+      if (has_h0) mbar_arrive(&bar[kRdyH]);
+    }
+    if (hf == 0) {
+      fetch_dt(0);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int64_t c = 0; c < nchunk; c++) {
+      const int64_t t0 = c * kQ;
+      // ---- delta and the decay (base 2) accumulated inside the chunk, inclusive
+      {
+        float dl = 0.f, sc = 0.f;
+        if (hf == 0) {
+          asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk c (fetched a chunk ago)
+          dl = t0 + row < L ? softplus_fast(dt_of(c) + dtbias) : 0.f;
+          if (c + 1 < nchunk) {
+            fetch_dt(c + 1);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+          }
+          sc = dl * a2;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o) sc += v;
+          }
+          if (lane == 31) wsum[warp] = sc;
+        }
+        // every compute thread is past the previous chunk (css, dls free); a
+        // timeout anywhere ends the loop for all of them
+        if (bar_or_compute(fail)) break;
+        if (hf == 0) {
+          for (int w = 0; w < warp; w++) sc += wsum[w];
+          dls[row] = dl;
+          css[row] = sc;
+        }
+        bar_sync_compute();
+      }
+      // ---- X' (row s, columns p in half hf) = 2^(cs_end - cs_s) delta_s x_s
+      wait(kBarX);
+      {
+        const float ws = ex2(css[kQ - 1] - css[row]) * dls[row];
 #pragma unroll
         for (int c8 = 0; c8 < 4; c8++) {
-          float xv[8], o[8];
-          widen8(*reinterpret_cast<const uint4*>(sm + SM::X + sw128(row, pb + c8 * 8)), xv);
+          const int off = sw128(row, 32 * hf + 8 * c8);
+          float v[8];
+          widen8(*reinterpret_cast<const uint4*>(sm + SM::X + off), v);
 #pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const float yy = state_nonzero ? fmaf(et, y2[c8 * 8 + i], y1[c8 * 8 + i]) : y1[c8 * 8 + i];
-            o[i] = fmaf(Dh, xv[i], yy);
+          for (int i = 0; i < 8; i++) v[i] *= ws;
+          uint4 hi, lo;
+          split8(v, hi, lo);
+          *reinterpret_cast<uint4*>(sm + SM::XH + off) = hi;
+          *reinterpret_cast<uint4*>(sm + SM::XL + off) = lo;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar[kRdyX]);
+      if (tid == kStoreTid) {  // the previous chunk's y store has read its staging tiles
+        bulk_wait_read();
+        mbar_arrive(&bar[kStg]);
+      }
+      // ---- M (row t, columns s in half hf) from S, D_h on the diagonal. Of
+      // the 32-column blocks kb0, kb0 + 1 of this thread, block k holds
+      // nonzeros for the warp's rows only if k <= wq (warp-uniform).
+      wait(kBarS);
+      wait(kStg);
+      tc_fence_after();
+      {
+        const float cst = css[row];
+        const int kb0 = 2 * hf;
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+          const int k = kb0 + j;
+          uint8_t* mh = sm + (hf ? SM::MH1 : SM::MH0);
+          uint8_t* ml = sm + (hf ? SM::ML1 : SM::ML0);
+          uint32_t sr[32];
+          if (k <= wq) {
+            tmem_ld32_async(tlane + kColS + 32 * k, sr);
+            tmem_wait_ld(sr);
           }
-          if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; c8++) {
+            const int sb = 32 * k + 8 * c8;
+            float v[8];
+            if (k <= wq) {
+              // (the loads are ordered after the previous group's stores, which
+              // keeps one group of values live at a time)
+              const float4 ca = lds_f4(css + sb), cb = lds_f4(css + sb + 4);
+              const float4 da = lds_f4(dls + sb), db = lds_f4(dls + sb + 4);
+              const float csv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+              const float dlv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+#pragma unroll
+              for (int i = 0; i < 8; i++) v[i] = __uint_as_float(sr[8 * c8 + i]) * ex2(cst - csv[i]) * dlv[i];
+              if (k == wq) {  // the block that holds the diagonal: causal mask, D_h on it
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                  const int s = sb + i;
+                  v[i] = s < row ? v[i] : (s == row ? v[i] + Dh : 0.f);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; i++) v[i] = 0.f;
+            }
+            uint4 hi, lo;
+            split8(v, hi, lo);
+            const int col = 32 * j + 8 * c8;
+            *reinterpret_cast<uint4*>(mh + sw128(row, col)) = hi;
+            *reinterpret_cast<uint4*>(ml + sw128(row, col)) = lo;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar[kRdyM]);
+      // ---- the state, row n of H^T: 2^cs_end H^T + H_l^T (Y2, issued before
+      // B^T X', has read the state's previous parts)
+      wait(kBarH);
+      tc_fence_after();
+      {
+        const float dec = ex2(css[kQ - 1]);
+        uint32_t hl[32], hv[32];
+        {
+          uint32_t hl2[32];
+          tmem_ld32_async(tlane + kColH + 32 * hf, hl);
+          tmem_ld32_async(tlane + kColH + kP + 32 * hf, hl2);
+          tmem_wait_ld(hl);
+          tmem_wait_ld(hl2);
+#pragma unroll
+          for (int i = 0; i < 32; i++) hl[i] = __float_as_uint(__uint_as_float(hl[i]) + __uint_as_float(hl2[i]));
+        }
+        tmem_ld32_async(tstate, hv);
+        tmem_wait_ld(hv);
+#pragma unroll
+        for (int i = 0; i < 32; i++) hv[i] = __float_as_uint(fmaf(dec, __uint_as_float(hv[i]), __uint_as_float(hl[i])));
+        tmem_st32(tstate, hv);
+        write_state(hv);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar[kRdyH]);
+      // ---- y of row t, columns p in half hf: Y1 + 2^cs_t Y2, staged in
+      // shared memory (M's high-part tiles, no longer read) and stored by TMA
+      wait(kBarY1);
+      const bool y2 = c > 0 || has_h0;
+      if (y2) wait(kBarY2);
+      tc_fence_after();
+      {
+        const int pb = 32 * hf;
+        uint32_t r1[32], r2[32];
+        if (y2) {  // Y2 = the product with the state's high part + the one with its remainder
+          uint32_t r3[32];
+          tmem_ld32_async(tlane + kColY2 + pb, r2);
+          tmem_ld32_async(tlane + kColY2 + kP + pb, r3);
+          tmem_wait_ld(r2);
+          tmem_wait_ld(r3);
+#pragma unroll
+          for (int i = 0; i < 32; i++) r2[i] = __float_as_uint(__uint_as_float(r2[i]) + __uint_as_float(r3[i]));
+        }
+        tmem_ld32_async(tlane + kColY1 + pb, r1);
+        tmem_wait_ld(r1);
+        tc_fence_before();
+        mbar_arrive(&bar[kRdyY]);  // Y1 and Y2 are read
+        const float et = ex2(css[row]);
+        float* o = reinterpret_cast<float*>(r1);
+        if (y2) {
+#pragma unroll
+          for (int i = 0; i < 32; i++) o[i] = fmaf(et, __uint_as_float(r2[i]), o[i]);
+        }
+        if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; c8++) {
             uint32_t w4[4];
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-              const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+              const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[8 * c8 + 2 * i], o[8 * c8 + 2 * i + 1]);
               w4[i] = *reinterpret_cast<const uint32_t*>(&v2);
             }
-            *reinterpret_cast<uint4*>(yrow + c8 * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          } else {
-            *reinterpret_cast<float4*>(yrow + c8 * 8) = make_float4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<float4*>(yrow + c8 * 8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(sm + SM::MH0 + sw128(row, pb + 8 * c8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
+        } else {  // fp32: tile hf holds columns 32 hf .. 32 hf + 31, 128 bytes a row
+#pragma unroll
+          for (int c4 = 0; c4 < 8; c4++)
+            *reinterpret_cast<float4*>(sm + (hf ? SM::MH1 : SM::MH0) + row * 128 + ((c4 ^ (row & 7)) << 4)) =
+                make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+        }
+        fence_proxy_async_smem();
+        bar_sync_compute();
+        if (tid == kStoreTid) {
+          tma_store_4d(&tm_y, sm + SM::MH0, 0, (int)h, (int)t0, (int)b);
+          if constexpr (sizeof(TOut) == 4) tma_store_4d(&tm_y, sm + SM::MH1, 32, (int)h, (int)t0, (int)b);
         }
       }
     }
-    // ---- the state, row n of H^T: 2^cs_end H^T + H_l^T
-    {
-      const float dec = ex2(css[kQ - 1]);
-      float hl[32];
-      tmem_ld32(tlane + kColH + 32 * hf, hl);
-#pragma unroll
-      for (int i = 0; i < 32; i++) hst[i] = fmaf(dec, hst[i], hl[i]);
-      write_state();
-      state_nonzero = true;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();  // x is no longer read; the state is written for the next chunk
-    if (tid == 0 && c + 1 < nchunk) issue_x(c + 1);
-  }
-
-  if (ok) {
-    if (p.h_last) {
+    if (!fail && p.h_last) {
+      uint32_t hv[32];
+      tmem_ld32_async(tstate, hv);
+      tmem_wait_ld(hv);
       float* hl = p.h_last + (b * H + h) * kP * kN;
 #pragma unroll
-      for (int q = 0; q < 32; q++) hl[(32 * hf + q) * kN + row] = hst[q];
+      for (int q = 0; q < 32; q++) hl[(32 * hf + q) * kN + row] = __uint_as_float(hv[q]);
     }
-  } else if (tid == 0) {
-    // a wait gave up: wait (bounded) for what this CTA still has in flight
-    // before its shared and tensor memory are released
-    for (int i = 0; i < 4; i++)
-      if (pend[i]) mbar_wait(&bar[i], ph[i], wait_ns);
+    if (tid == kStoreTid) bulk_wait_all();  // the y stores are complete
+    if (fail && tid == 0) atomicOr(p.fault, kFaultTileWait);
   }
   tc_fence_before();
   __syncthreads();
@@ -475,32 +674,34 @@ TcEncodeFn tc_encode_fn() {
   return fn;
 }
 
-// 4-D bf16 map over a row-major [d3, d2, d1, d0] tensor with a [1, 128, 1, 64]
-// box (64 innermost elements = 128 bytes, 128 rows of d2) in the 128-byte swizzle
-bool make_map_4d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3) {
+// 4-D map over a row-major [d3, d2, d1, d0] tensor of 2- or 4-byte elements
+// with a [1, 128, 1, 128 bytes] box (128 rows of d2) in the 128-byte swizzle
+bool make_map_4d(CUtensorMap* m, const void* ptr, int esize, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3) {
   TcEncodeFn fn = tc_encode_fn();
   if (!fn) return false;
+  const uint64_t e = (uint64_t)esize;
   cuuint64_t dims[4] = {d0, d1, d2, d3};
-  cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kQ, 1};
+  cuuint64_t strides[3] = {d0 * e, d0 * d1 * e, d0 * d1 * d2 * e};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / esize), 1, (cuuint32_t)kQ, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename TOut>
 cudaError_t launch_tc(const SsdParams& p, cudaStream_t s) {
-  CUtensorMap mx{}, mb{}, mc{};
-  // x [batch, L, H, 64]; B, C [batch, L, G, 128]
-  if (!make_map_4d(&mx, p.x, kP, (uint64_t)p.nheads, (uint64_t)p.seqlen, (uint64_t)p.batch) ||
-      !make_map_4d(&mb, p.B, kN, (uint64_t)p.ngroups, (uint64_t)p.seqlen, (uint64_t)p.batch) ||
-      !make_map_4d(&mc, p.C, kN, (uint64_t)p.ngroups, (uint64_t)p.seqlen, (uint64_t)p.batch))
+  CUtensorMap mx{}, mb{}, mc{}, my{};
+  // x, y [batch, L, H, 64]; B, C [batch, L, G, 128]
+  const uint64_t L = (uint64_t)p.seqlen, Bt = (uint64_t)p.batch, H = (uint64_t)p.nheads, G = (uint64_t)p.ngroups;
+  if (!make_map_4d(&mx, p.x, 2, kP, H, L, Bt) || !make_map_4d(&mb, p.B, 2, kN, G, L, Bt) ||
+      !make_map_4d(&mc, p.C, 2, kN, G, L, Bt) || !make_map_4d(&my, p.y, (int)sizeof(TOut), kP, H, L, Bt))
     return cudaErrorInvalidValue;
   auto k = ssd_tc_kernel<TOut>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::ALLOC);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)(p.batch * p.nheads), kThreads, TcSmem::ALLOC, s>>>(p, mx, mb, mc);
+  k<<<(unsigned)(p.batch * p.nheads), kThreads, TcSmem::ALLOC, s>>>(p, mx, mb, mc, my);
   return cudaGetLastError();
 }
 
