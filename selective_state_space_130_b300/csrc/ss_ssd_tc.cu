@@ -16,23 +16,27 @@
 //   Y = M X + 2^cs_t o (C H_in^T)                           [t, p]  (K = s, K = n)
 //   H_out^T = 2^cs_end H_in^T + B^T X',  X' = diag(2^(cs_end - cs_s) delta_s) X   [n, p]  (K = s)
 //
-// One CTA of eight warps owns one (batch, head) and walks its chunks in order;
-// the state stays in registers (two threads per row n of H^T, 32 columns
-// each). Per chunk:
-//  - one thread loads the chunk's C and B (two 64-column boxes each) and x by
-//    TMA with 128-byte swizzling, the layout the tensor core reads; each load
-//    is issued as soon as the products of the previous chunk have released its
-//    buffer, so it lands while that chunk finishes;
-//  - S = C B^T and Y2 = C H_in^T go to the tensor core together (Y2 needs only
-//    the state entering the chunk);
-//  - the threads scale row s of x by its state weight into X' (then B^T X' goes
-//    to the tensor core) and turn row t of S, read from tensor memory
-//    (tcgen05.ld), into row t of M (then M X goes to the tensor core); M, X'
-//    and the state are computed in fp32 and enter the products as a bf16 high
-//    part and a bf16 remainder (two products each, about 16 significant bits);
-//    x, B and C enter as the stored bf16 values;
-//  - the state update H^T = 2^cs_end H^T + B^T X' runs in registers and writes
-//    the state's two parts for the next chunk; then y_t = Y1_t + 2^cs_t Y2_t.
+// One CTA owns one (batch, head) and walks its chunks in order. One thread of
+// a ninth warp issues every TMA copy and tensor-core product; eight compute
+// warps (two threads per row of a product, each taking half its columns) do
+// the element-wise work and signal the issuer through mbarriers, so no
+// compute thread ever waits for an issue. Per chunk:
+//  - C and B (two 64-column boxes each) and x arrive by TMA in the 128-byte
+//    swizzle, the layout the tensor core reads; each load is issued as soon as
+//    the previous chunk's products have released its buffer;
+//  - S = C B^T and Y2 = C H_in^T go to the tensor core first (Y2 needs only the
+//    state entering the chunk); the compute threads meanwhile take delta and
+//    the decay sums (dt was fetched a chunk ahead by cp.async);
+//  - they scale row s of x by its state weight into X' (then B^T X' runs), and
+//    turn row t of S, read from tensor memory, into row t of M, written back
+//    over S (then M X runs with A read from tensor memory);
+//  - the state H^T = 2^cs_end H^T + B^T X', kept in tensor memory, is updated
+//    and its two parts written to shared memory for the next chunk's Y2; y_t =
+//    Y1_t + 2^cs_t Y2_t is staged in shared memory and written by TMA.
+// M, X' and the state are computed in fp32 and enter the products as a bf16
+// high part and a bf16 remainder (about 16 significant bits; the two parts sit
+// side by side along N where they are the B operand, so one N = 128 product
+// covers both); x, B and C enter as the stored bf16 values.
 // Every wait is bounded and reports a timeout through the library fault word.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -49,15 +53,21 @@ constexpr int kP = 64;   // head channels
 constexpr int kN = 128;  // state size
 constexpr int kComputeWarps = 8;  // two threads per row of a product, each taking half its columns
 constexpr int kCompute = 32 * kComputeWarps;
-constexpr int kThreads = kCompute + 32;  // + one warp that issues the copies and products
+// + three warps whose first lanes issue the copies and products: a single
+// thread issues about one tcgen05.mma per hundred-odd cycles whatever its N,
+// and several issuing warps overlap, so independent products go to different
+// issuers
+constexpr int kIssuers = 3;
+constexpr int kThreads = kCompute + 32 * kIssuers;
 // The compute thread that issues the y stores: one outside warps 0-3, which
 // compute the chunk's scalars (its waits on the stores stay off their path).
 constexpr int kStoreTid = 128;
-// Tensor-memory columns: S [0,128), Y1 [128,192), Y2 [192,320) (the products
-// with the state's high part, then with its remainder), H_l [320,448) (with
-// X''s high part, then its remainder), the state [448,512)
+// Tensor-memory columns: S (then M) [0,128); Y1 as two accumulators, over s
+// < 64 [128,192) and over s >= 64 [192,256); Y2 [256,320) (the products with
+// the state's high part and with its remainder, summed); H_l [320,448) (with
+// X''s high part, then its remainder, side by side); the state [448,512)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColY1 = 128, kColY2 = 192, kColH = 320, kColState = 448;
+constexpr uint32_t kColS = 0, kColY1a = 128, kColY1b = 192, kColY2 = 256, kColH = 320, kColState = 448;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base). A "tile" is
 // 128 rows of 128 bytes (64 bf16) in the 128-byte swizzle: the 16-byte piece c
@@ -70,17 +80,17 @@ struct TcSmem {
   static constexpr int B1 = B0 + TILE;
   static constexpr int XH = B1 + TILE;        // X' high [s][p]
   static constexpr int XL = XH + TILE;        // X' remainder
-  static constexpr int X = XL + TILE;         // x [s][p]
-  static constexpr int MH0 = X + TILE;        // M high [t][s 0..63], MH1 = s 64..127
-  static constexpr int MH1 = MH0 + TILE;
-  static constexpr int ML0 = MH1 + TILE;      // M remainder
-  static constexpr int ML1 = ML0 + TILE;
-  static constexpr int HH = ML1 + TILE;       // H^T high [n][p]
+  static constexpr int X0 = XL + TILE;        // x [s][p] of even chunks, X1 of odd ones
+  static constexpr int X1 = X0 + TILE;
+  static constexpr int YS0 = X1 + TILE;       // y staged for its TMA store [t][p] (bf16: one tile; fp32: two)
+  static constexpr int YS1 = YS0 + TILE;
+  static constexpr int HH = YS1 + TILE;       // H^T high [n][p]
   static constexpr int HL = HH + TILE;        // H^T remainder
-  static constexpr int DL = HL + TILE;        // delta_t [128] f32
-  static constexpr int CS = DL + 512;         // cs_t [128] f32
-  static constexpr int WSUM = CS + 512;       // warp sums of the prefix scan [4] f32
-  static constexpr int DTB = WSUM + 64;       // dt words of two chunks [2][128] u32 (see the kernel)
+  static constexpr int DL = HL + TILE;        // delta_t of two chunks [2][128] f32
+  static constexpr int CS = DL + 1024;        // cs_t of two chunks [2][128] f32
+  static constexpr int WSUM = CS + 1024;      // warp sums of the prefix scans [2][4] f32
+  static constexpr int QS = WSUM + 64;        // q_s of two chunks [2][128] f32 (see the kernel)
+  static constexpr int DTB = QS + 1024;       // dt words of two chunks [2][128] u32 (see the kernel)
   static constexpr int BAR = DTB + 1024;      // mbarriers, see the kernel (at most 16)
   static constexpr int TSLOT = BAR + 128;     // tensor-memory base address
   static constexpr int BYTES = TSLOT + 64;
@@ -113,6 +123,15 @@ __device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t a, uint64_t b, uin
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(id), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+// the same with A read from tensor memory (row i in lane i, two bf16 of
+// consecutive K per 32-bit column, the even one in the low half)
+__device__ __forceinline__ void mma_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t id, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(id), "r"(accumulate ? 1u : 0u)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -179,13 +198,13 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // distance between its two 64-wide halves). The step is added to the
 // descriptor's address field (bytes / 16).
 __device__ __forceinline__ void mma_k128(uint32_t d, uint32_t a, bool a_kmajor, uint32_t b, bool b_kmajor,
-                                         uint32_t a_lbo, uint32_t b_lbo, uint32_t id) {
+                                         uint32_t a_lbo, uint32_t b_lbo, uint32_t id, bool accumulate = false) {
   const uint64_t ad = sdesc(a, a_lbo, 1024), bd = sdesc(b, b_lbo, 1024);
 #pragma unroll 1
   for (int kk = 0; kk < 8; kk++) {
     const uint32_t kstep = (uint32_t)((kk & 3) * 2 + (kk >> 2) * (128 * 128 / 16));  // K-major
     const uint32_t mstep = (uint32_t)(kk * 128);                                      // MN-major
-    mma(d, ad + (a_kmajor ? kstep : mstep), bd + (b_kmajor ? kstep : mstep), id, kk > 0);
+    mma(d, ad + (a_kmajor ? kstep : mstep), bd + (b_kmajor ? kstep : mstep), id, accumulate || kk > 0);
   }
 }
 // 4-D tiled TMA load (coordinates innermost first)
@@ -196,16 +215,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
-}
-// 16-byte shared-memory load that the compiler keeps in program order with
-// the surrounding memory accesses
-__device__ __forceinline__ float4 lds_f4(const float* p) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(smem_u32(p))
-               : "memory");
-  return v;
 }
 // eight floats -> eight bf16 (16 bytes), high part and remainder
 __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
@@ -254,17 +263,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t s0 = smem_u32(sm);
   // Barriers. Completed by the copy engine or the tensor core: C and B
-  // loaded, x loaded, S done, Y1 done, Y2 done, B^T X' done. Completed by the
-  // 256 compute threads: X' written, M written (S read), state written (B^T X'
-  // read), y written (Y1 and Y2 read).
-  // The last one: the M tiles, which stage y, are free again (thread 0).
-  enum { kBarCB = 0, kBarX, kBarS, kBarY1, kBarY2, kBarH, kRdyX, kRdyM, kRdyH, kRdyY, kStg, kNumBars };
+  // loaded, x of an even / odd chunk loaded, S done, the two halves of Y1
+  // done, Y2 done, B^T X' done. Completed by the 256 compute threads: X'
+  // written, M's column blocks 0 and 2 written, M's blocks 1 and 3 written (S
+  // read), the state written (B^T X' read), Y1 and Y2 read. By one compute
+  // thread: the y staging tiles are free again.
+  enum {
+    kBarCB = 0, kBarX0, kBarX1, kBarS, kBarY1a, kBarY1b, kBarY2, kBarH,
+    kRdyX, kRdyM0, kRdyM1, kRdyH, kRdyY, kStg, kNumBars
+  };
   static_assert(kNumBars * 8 <= SM::TSLOT - SM::BAR, "the barriers overlap the tensor-memory slot");
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SM::BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM::TSLOT);
-  float* dls = reinterpret_cast<float*>(sm + SM::DL);
-  float* css = reinterpret_cast<float*>(sm + SM::CS);
-  float* wsum = reinterpret_cast<float*>(sm + SM::WSUM);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t bh = blockIdx.x;
   const int64_t b = bh / p.nheads, h = bh % p.nheads;
@@ -300,87 +310,118 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   };
   const bool has_h0 = p.h0 != nullptr;
 
-  if (warp == kComputeWarps) {
-    // ============ the issuing warp: one lane loads tiles and runs the products
+  if (warp >= kComputeWarps) {
+    // ============ the issuing warps: lane 0 of each issues. Issuer 0: the
+    // tile loads, S and H_l; issuer 1: Y2, then Y1 over M's blocks 0 and 1;
+    // issuer 2: Y1 over M's blocks 2 and 3.
+    const int role = warp - kComputeWarps;
     if (lane == 0) {
-      const int grp = (int)(h / (H / G));
       uint32_t nissue[kRdyX] = {};  // copies or commits issued per barrier (for the drain after a timeout)
-      tma_prefetch_desc(&tm_x);
-      tma_prefetch_desc(&tm_b);
-      tma_prefetch_desc(&tm_c);
-      auto issue_cb = [&](int64_t c) {
-        const int t0 = (int)(c * kQ);
-        mbar_expect_tx(&bar[kBarCB], 4 * SM::TILE);
-        tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, (int)b, &bar[kBarCB]);
-        tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, (int)b, &bar[kBarCB]);
-        tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, (int)b, &bar[kBarCB]);
-        tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, (int)b, &bar[kBarCB]);
-        mbar_arrive(&bar[kBarCB]);
-        nissue[kBarCB]++;
-      };
-      auto issue_x = [&](int64_t c) {
-        mbar_expect_tx(&bar[kBarX], SM::TILE);
-        tma_load_4d(sm + SM::X, &tm_x, 0, (int)h, (int)(c * kQ), (int)b, &bar[kBarX]);
-        mbar_arrive(&bar[kBarX]);
-        nissue[kBarX]++;
-      };
       auto commit = [&](int i) {
         mma_commit(&bar[i]);
         nissue[i]++;
       };
-      issue_cb(0);
-      issue_x(0);
-      for (int64_t c = 0; c < nchunk; c++) {
-        // S = C B^T (S's columns were read by the previous chunk's M)
-        if (!wait(kBarCB)) break;
-        tc_fence_after();
-        mma_k128(tmem + kColS, s0 + SM::C0, true, s0 + SM::B0, true, 16, 16, idesc(kQ, kQ, 0, 0));
-        commit(kBarS);
-        // Y2 = C H_in^T, once the state entering the chunk is written and the
-        // previous chunk's y has read Y2's columns
-        if (c > 0 || has_h0) {
-          if (!wait(kRdyH)) break;
-          if (c > 0 && !wait(kRdyY)) break;
-          tc_fence_after();
-          // A K-major (C); B MN-major: H^T's high part and remainder side by
-          // side (N = 128, the two tiles one tile apart)
-          mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HH, false, 16, SM::TILE, idesc(kQ, 2 * kP, 0, 1));
-          commit(kBarY2);
-        }
-        // H_l^T = B^T X' (A = B read MN-major: its two n halves are one tile apart)
-        if (!wait(kBarX) || !wait(kRdyX)) break;
-        tc_fence_after();
-        // (B: X''s high part and remainder side by side, N = 128)
-        mma_k128(tmem + kColH, s0 + SM::B0, false, s0 + SM::XH, false, SM::TILE, SM::TILE, idesc(kN, 2 * kP, 1, 1));
-        commit(kBarH);
-        // Y1 = M X
-        if (!wait(kRdyM)) break;
-        tc_fence_after();
-        {
-          const uint64_t bd = sdesc(s0 + SM::X, 16, 1024);
-          const uint64_t ah = sdesc(s0 + SM::MH0, 16, 1024), al = sdesc(s0 + SM::ML0, 16, 1024);
+      // Y1 over M's S block blk (s in [32 blk, 32 blk + 32): K steps 2 blk and
+      // 2 blk + 1, the high parts and the remainders) into accumulator d
+      auto y1_block = [&](uint32_t d, uint32_t xs, int blk, bool first) {
+        const uint64_t bd = sdesc(xs, 16, 1024);
 #pragma unroll 1
-          for (int kk = 0; kk < 16; kk++) {  // M's high part, then its remainder, times x
-            const int k = kk & 7;
-            const uint32_t kstep = (uint32_t)((k & 3) * 2 + (k >> 2) * (SM::TILE / 16));
-            mma(tmem + kColY1, (kk < 8 ? ah : al) + kstep, bd + (uint32_t)(k * 128), idesc(kQ, kP, 0, 1), kk > 0);
+        for (int i = 0; i < 4; i++) {
+          const int e = i & 1, part = i >> 1, k = 2 * blk + e;
+          const uint32_t ta = tmem + kColS + 32 * blk + 8 * e + 16 * part;
+          mma_ta(tmem + d, ta, bd + (uint32_t)(k * 128), idesc(kQ, kP, 0, 1), !first || i > 0);
+        }
+      };
+      if (role == 0) {
+        const int grp = (int)(h / (H / G));
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_c);
+        auto issue_cb = [&](int64_t c) {
+          const int t0 = (int)(c * kQ);
+          mbar_expect_tx(&bar[kBarCB], 4 * SM::TILE);
+          tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, (int)b, &bar[kBarCB]);
+          tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, (int)b, &bar[kBarCB]);
+          tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, (int)b, &bar[kBarCB]);
+          tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, (int)b, &bar[kBarCB]);
+          mbar_arrive(&bar[kBarCB]);
+          nissue[kBarCB]++;
+        };
+        auto issue_x = [&](int64_t c) {  // into the buffer of the chunk's parity
+          const int xb = kBarX0 + (int)(c & 1);
+          mbar_expect_tx(&bar[xb], SM::TILE);
+          tma_load_4d(sm + ((c & 1) ? SM::X1 : SM::X0), &tm_x, 0, (int)h, (int)(c * kQ), (int)b, &bar[xb]);
+          mbar_arrive(&bar[xb]);
+          if (c & 1)
+            nissue[kBarX1]++;
+          else
+            nissue[kBarX0]++;
+        };
+        issue_cb(0);
+        issue_x(0);
+        for (int64_t c = 0; c < nchunk; c++) {
+          // S = C B^T (S's columns were read by the previous chunk's Y1)
+          if (!wait(kBarCB)) break;
+          tc_fence_after();
+          mma_k128(tmem + kColS, s0 + SM::C0, true, s0 + SM::B0, true, 16, 16, idesc(kQ, kQ, 0, 0));
+          commit(kBarS);
+          // x of the next chunk, into the buffer of the chunk before this one
+          // (its Y1 is done, its X' written)
+          if (c + 1 < nchunk) issue_x(c + 1);
+          // H_l^T = B^T X' (A = B read MN-major: its two n halves are one tile
+          // apart; B: X''s high part and remainder side by side, N = 128)
+          if (!wait(kRdyX)) break;
+          tc_fence_after();
+          mma_k128(tmem + kColH, s0 + SM::B0, false, s0 + SM::XH, false, SM::TILE, SM::TILE, idesc(kN, 2 * kP, 1, 1));
+          commit(kBarH);
+          if (c + 1 < nchunk) {
+            // C and B are free once S, H_l (in issue order) and Y2 are done;
+            // S's columns and this x once both halves of Y1 are
+            if (!wait(kBarH) || ((c > 0 || has_h0) && !wait(kBarY2))) break;
+            issue_cb(c + 1);
+            if (!wait(kBarY1a) || !wait(kBarY1b)) break;
           }
         }
-        commit(kBarY1);
-        if (c + 1 < nchunk) {
-          // products complete in issue order: B^T X' done means S and Y2 are
-          // too, so C and B are free; Y1 done frees x
-          if (!wait(kBarH)) break;
-          issue_cb(c + 1);
-          if (!wait(kBarY1)) break;
-          issue_x(c + 1);
+      } else if (role == 1) {
+        for (int64_t c = 0; c < nchunk; c++) {
+          const uint32_t xs = s0 + ((c & 1) ? SM::X1 : SM::X0);
+          if (!wait(kBarCB)) break;                // C of the chunk
+          if (c > 0 && !wait(kRdyY)) break;        // the previous y has read Y1a and Y2
+          // Y2 = C H_in^T: A K-major (C), B MN-major (H^T), the high part and
+          // then the remainder into one accumulator
+          if (c > 0 || has_h0) {
+            if (!wait(kRdyH)) break;  // the state entering the chunk is written
+            tc_fence_after();
+            mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HH, false, 16, 16, idesc(kQ, kP, 0, 1));
+            mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HL, false, 16, 16, idesc(kQ, kP, 0, 1), true);
+            commit(kBarY2);
+          }
+          if (!wait(kRdyM0)) break;
+          tc_fence_after();
+          y1_block(kColY1a, xs, 0, true);
+          if (!wait(kRdyM1)) break;
+          tc_fence_after();
+          y1_block(kColY1a, xs, 1, false);
+          commit(kBarY1a);
+        }
+      } else {
+        for (int64_t c = 0; c < nchunk; c++) {
+          const uint32_t xs = s0 + ((c & 1) ? SM::X1 : SM::X0);
+          if (c > 0 && !wait(kRdyY)) break;  // the previous y has read Y1b
+          if (!wait(kRdyM0)) break;
+          tc_fence_after();
+          y1_block(kColY1b, xs, 2, true);
+          if (!wait(kRdyM1)) break;
+          tc_fence_after();
+          y1_block(kColY1b, xs, 3, false);
+          commit(kBarY1b);
         }
       }
       if (fail) {
         // a wait gave up: record it, and wait (bounded) for the last copy and
-        // product issued on each barrier (the k-th completion of a barrier
-        // ends phase k, of parity k & 1) before shared and tensor memory are
-        // released
+        // product this thread issued on each barrier (the k-th completion of a
+        // barrier ends phase k, of parity k & 1) before shared and tensor
+        // memory are released
         atomicOr(p.fault, kFaultTileWait);
 #pragma unroll
         for (int i = 0; i < kRdyX; i++)
@@ -396,6 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     const float a2 = __ldg(p.A + h) * kLog2e;  // decay exponent per unit delta, base 2
     const float dtbias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
+    float* const dls2 = reinterpret_cast<float*>(sm + SM::DL);   // [2][128]: chunk c in half c & 1
+    float* const css2 = reinterpret_cast<float*>(sm + SM::CS);   // [2][128]
+    float* const wsum2 = reinterpret_cast<float*>(sm + SM::WSUM);  // [2][4]
+    float* const qs2 = reinterpret_cast<float*>(sm + SM::QS);      // [2][128]
     const __nv_bfloat16* dt_all = static_cast<const __nv_bfloat16*>(p.dt);
     const int64_t dt_last = p.batch * L * H - 1;  // index of dt's last element
     uint32_t* dtb = reinterpret_cast<uint32_t*>(sm + SM::DTB);
@@ -419,6 +464,37 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       const int64_t i = (b * L + c * kQ + row) * H + h;
       const uint32_t w = dtb[(c & 1) * kQ + row];
       return __uint_as_float(((i & 1) ? (w >> 16) : (w & 0xffffu)) << 16);
+    };
+    // delta and the decay (base 2) accumulated inside chunk cc, inclusive,
+    // into half cc & 1 of dls2 / css2, and q_s = 2^(cs_e - cs_s) delta_s with e
+    // the last step of s's block of 32 (threads of the first column half,
+    // warp w holding block w; all compute threads take part in its barrier).
+    // Visible to the others after the next barrier.
+    auto scalars = [&](int64_t cc) {
+      float dl = 0.f, sc = 0.f;
+      float* ws = wsum2 + (cc & 1) * 4;
+      if (hf == 0) {
+        asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk cc
+        dl = cc * kQ + row < L ? softplus_fast(dt_of(cc) + dtbias) : 0.f;
+        if (cc + 1 < nchunk) {
+          fetch_dt(cc + 1);
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        sc = dl * a2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_up_sync(0xffffffffu, sc, o);
+          if (lane >= o) sc += v;
+        }
+        if (lane == 31) ws[warp] = sc;
+      }
+      bar_sync_compute();
+      if (hf == 0) {
+        for (int w = 0; w < warp; w++) sc += ws[w];
+        dls2[(cc & 1) * kQ + row] = dl;
+        css2[(cc & 1) * kQ + row] = sc;
+        qs2[(cc & 1) * kQ + row] = ex2(__shfl_sync(0xffffffffu, sc, 31) - sc) * dl;
+      }
     };
 
     // the state lives in tensor memory: thread (row n, half hf) owns
@@ -454,45 +530,24 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       fetch_dt(0);
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
+    scalars(0);
+    bar_sync_compute();
+    bool aborted = false;  // the loop ended on a timed-out wait
     for (int64_t c = 0; c < nchunk; c++) {
       const int64_t t0 = c * kQ;
-      // ---- delta and the decay (base 2) accumulated inside the chunk, inclusive
-      {
-        float dl = 0.f, sc = 0.f;
-        if (hf == 0) {
-          asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk c (fetched a chunk ago)
-          dl = t0 + row < L ? softplus_fast(dt_of(c) + dtbias) : 0.f;
-          if (c + 1 < nchunk) {
-            fetch_dt(c + 1);
-            asm volatile("cp.async.commit_group;" ::: "memory");
-          }
-          sc = dl * a2;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float v = __shfl_up_sync(0xffffffffu, sc, o);
-            if (lane >= o) sc += v;
-          }
-          if (lane == 31) wsum[warp] = sc;
-        }
-        // every compute thread is past the previous chunk (css, dls free); a
-        // timeout anywhere ends the loop for all of them
-        if (bar_or_compute(fail)) break;
-        if (hf == 0) {
-          for (int w = 0; w < warp; w++) sc += wsum[w];
-          dls[row] = dl;
-          css[row] = sc;
-        }
-        bar_sync_compute();
-      }
+      const float* dls = dls2 + (c & 1) * kQ;
+      const float* css = css2 + (c & 1) * kQ;
+      const float* qsv = qs2 + (c & 1) * kQ;
+      const uint8_t* xs = sm + ((c & 1) ? SM::X1 : SM::X0);
       // ---- X' (row s, columns p in half hf) = 2^(cs_end - cs_s) delta_s x_s
-      wait(kBarX);
+      wait(kBarX0 + (int)(c & 1));
       {
         const float ws = ex2(css[kQ - 1] - css[row]) * dls[row];
 #pragma unroll
         for (int c8 = 0; c8 < 4; c8++) {
           const int off = sw128(row, 32 * hf + 8 * c8);
           float v[8];
-          widen8(*reinterpret_cast<const uint4*>(sm + SM::X + off), v);
+          widen8(*reinterpret_cast<const uint4*>(xs + off), v);
 #pragma unroll
           for (int i = 0; i < 8; i++) v[i] *= ws;
           uint4 hi, lo;
@@ -507,11 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         bulk_wait_read();
         mbar_arrive(&bar[kStg]);
       }
-      // ---- M (row t, columns s in half hf) from S, D_h on the diagonal. Of
-      // the 32-column blocks kb0, kb0 + 1 of this thread, block k holds
-      // nonzeros for the warp's rows only if k <= wq (warp-uniform).
+      // ---- M (row t, columns s in half hf) from S, D_h on the diagonal,
+      // written over S in tensor memory, where Y1 = M X reads it as its A
+      // operand: the 32 columns of S block k (s in [32k, 32k + 32)) take the
+      // block's high parts (16 columns, two bf16 each, the even s in the low
+      // half) and then its remainders. This thread's blocks are kb0 and kb0 +
+      // 1; the issuer starts Y1 on blocks 0 and 2 once every thread has
+      // written its first one. Block k holds nonzeros for the warp's rows only
+      // if k <= wq (warp-uniform).
       wait(kBarS);
-      wait(kStg);
       tc_fence_after();
       {
         const float cst = css[row];
@@ -519,32 +578,39 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int j = 0; j < 2; j++) {
           const int k = kb0 + j;
-          uint8_t* mh = sm + (hf ? SM::MH1 : SM::MH0);
-          uint8_t* ml = sm + (hf ? SM::ML1 : SM::ML0);
           uint32_t sr[32];
           if (k <= wq) {
             tmem_ld32_async(tlane + kColS + 32 * k, sr);
             tmem_wait_ld(sr);
           }
+          uint32_t mw[32];  // [0, 16) the high parts, [16, 32) the remainders
 #pragma unroll
           for (int c8 = 0; c8 < 4; c8++) {
             const int sb = 32 * k + 8 * c8;
             float v[8];
-            if (k <= wq) {
-              // (the loads are ordered after the previous group's stores, which
-              // keeps one group of values live at a time)
-              const float4 ca = lds_f4(css + sb), cb = lds_f4(css + sb + 4);
-              const float4 da = lds_f4(dls + sb), db = lds_f4(dls + sb + 4);
+            if (k < wq) {
+              // below the diagonal block: 2^(cs_t - cs_s) = 2^(cs_t - cs_e) 2^(cs_e - cs_s),
+              // e the block's last step; both factors are at most 1
+              const float4 qa = *reinterpret_cast<const float4*>(qsv + sb);
+              const float4 qb = *reinterpret_cast<const float4*>(qsv + sb + 4);
+              const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+              const float rt = ex2(cst - css[32 * k + 31]);
+#pragma unroll
+              for (int i = 0; i < 8; i++) v[i] = __uint_as_float(sr[8 * c8 + i]) * qv[i] * rt;
+            } else if (k == wq) {
+              const float4 ca = *reinterpret_cast<const float4*>(css + sb);
+              const float4 cb = *reinterpret_cast<const float4*>(css + sb + 4);
+              const float4 da = *reinterpret_cast<const float4*>(dls + sb);
+              const float4 db = *reinterpret_cast<const float4*>(dls + sb + 4);
               const float csv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
               const float dlv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
 #pragma unroll
               for (int i = 0; i < 8; i++) v[i] = __uint_as_float(sr[8 * c8 + i]) * ex2(cst - csv[i]) * dlv[i];
-              if (k == wq) {  // the block that holds the diagonal: causal mask, D_h on it
+              // the block that holds the diagonal: causal mask, D_h on it
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                  const int s = sb + i;
-                  v[i] = s < row ? v[i] : (s == row ? v[i] + Dh : 0.f);
-                }
+              for (int i = 0; i < 8; i++) {
+                const int s = sb + i;
+                v[i] = s < row ? v[i] : (s == row ? v[i] + Dh : 0.f);
               }
             } else {
 #pragma unroll
@@ -552,15 +618,20 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
             }
             uint4 hi, lo;
             split8(v, hi, lo);
-            const int col = 32 * j + 8 * c8;
-            *reinterpret_cast<uint4*>(mh + sw128(row, col)) = hi;
-            *reinterpret_cast<uint4*>(ml + sw128(row, col)) = lo;
+            mw[4 * c8 + 0] = hi.x;
+            mw[4 * c8 + 1] = hi.y;
+            mw[4 * c8 + 2] = hi.z;
+            mw[4 * c8 + 3] = hi.w;
+            mw[16 + 4 * c8 + 0] = lo.x;
+            mw[16 + 4 * c8 + 1] = lo.y;
+            mw[16 + 4 * c8 + 2] = lo.z;
+            mw[16 + 4 * c8 + 3] = lo.w;
           }
+          tmem_st32(tlane + kColS + 32 * k, mw);
+          tc_fence_before();
+          mbar_arrive(&bar[j == 0 ? kRdyM0 : kRdyM1]);
         }
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bar[kRdyM]);
       // ---- the state, row n of H^T: 2^cs_end H^T + H_l^T (Y2, issued before
       // B^T X', has read the state's previous parts)
       wait(kBarH);
@@ -587,26 +658,32 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar[kRdyH]);
+      // ---- the next chunk's delta and decay sums, while Y1 runs
+      if (c + 1 < nchunk) scalars(c + 1);
       // ---- y of row t, columns p in half hf: Y1 + 2^cs_t Y2, staged in
-      // shared memory (M's high-part tiles, no longer read) and stored by TMA
-      wait(kBarY1);
+      // shared memory and stored by TMA
+      wait(kBarY1a);
+      wait(kBarY1b);
       const bool y2 = c > 0 || has_h0;
       if (y2) wait(kBarY2);
       tc_fence_after();
+      bool abort;
       {
         const int pb = 32 * hf;
         uint32_t r1[32], r2[32];
-        if (y2) {  // Y2 = the product with the state's high part + the one with its remainder
+        {  // Y1 = the half over s < 64 + the half over s >= 64
           uint32_t r3[32];
-          tmem_ld32_async(tlane + kColY2 + pb, r2);
-          tmem_ld32_async(tlane + kColY2 + kP + pb, r3);
-          tmem_wait_ld(r2);
+          tmem_ld32_async(tlane + kColY1a + pb, r1);
+          tmem_ld32_async(tlane + kColY1b + pb, r3);
+          tmem_wait_ld(r1);
           tmem_wait_ld(r3);
 #pragma unroll
-          for (int i = 0; i < 32; i++) r2[i] = __float_as_uint(__uint_as_float(r2[i]) + __uint_as_float(r3[i]));
+          for (int i = 0; i < 32; i++) r1[i] = __float_as_uint(__uint_as_float(r1[i]) + __uint_as_float(r3[i]));
         }
-        tmem_ld32_async(tlane + kColY1 + pb, r1);
-        tmem_wait_ld(r1);
+        if (y2) {
+          tmem_ld32_async(tlane + kColY2 + pb, r2);
+          tmem_wait_ld(r2);
+        }
         tc_fence_before();
         mbar_arrive(&bar[kRdyY]);  // Y1 and Y2 are read
         const float et = ex2(css[row]);
@@ -615,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
 #pragma unroll
           for (int i = 0; i < 32; i++) o[i] = fmaf(et, __uint_as_float(r2[i]), o[i]);
         }
+        wait(kStg);  // the previous chunk's y store has read the staging tiles
         if constexpr (sizeof(TOut) == 2) {
 #pragma unroll
           for (int c8 = 0; c8 < 4; c8++) {
@@ -624,23 +702,27 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
               const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[8 * c8 + 2 * i], o[8 * c8 + 2 * i + 1]);
               w4[i] = *reinterpret_cast<const uint32_t*>(&v2);
             }
-            *reinterpret_cast<uint4*>(sm + SM::MH0 + sw128(row, pb + 8 * c8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            *reinterpret_cast<uint4*>(sm + SM::YS0 + sw128(row, pb + 8 * c8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         } else {  // fp32: tile hf holds columns 32 hf .. 32 hf + 31, 128 bytes a row
 #pragma unroll
           for (int c4 = 0; c4 < 8; c4++)
-            *reinterpret_cast<float4*>(sm + (hf ? SM::MH1 : SM::MH0) + row * 128 + ((c4 ^ (row & 7)) << 4)) =
+            *reinterpret_cast<float4*>(sm + (hf ? SM::YS1 : SM::YS0) + row * 128 + ((c4 ^ (row & 7)) << 4)) =
                 make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
         }
         fence_proxy_async_smem();
-        bar_sync_compute();
-        if (tid == kStoreTid) {
-          tma_store_4d(&tm_y, sm + SM::MH0, 0, (int)h, (int)t0, (int)b);
-          if constexpr (sizeof(TOut) == 4) tma_store_4d(&tm_y, sm + SM::MH1, 32, (int)h, (int)t0, (int)b);
+        // every row is staged and the next chunk's scalars are written; a
+        // timeout anywhere ends the loop for every compute thread
+        abort = bar_or_compute(fail);
+        aborted = abort;
+        if (!abort && tid == kStoreTid) {
+          tma_store_4d(&tm_y, sm + SM::YS0, 0, (int)h, (int)t0, (int)b);
+          if constexpr (sizeof(TOut) == 4) tma_store_4d(&tm_y, sm + SM::YS1, 32, (int)h, (int)t0, (int)b);
         }
       }
+      if (abort) break;
     }
-    if (!fail && p.h_last) {
+    if (!aborted && p.h_last) {  // (aborted is the same for every compute thread)
       uint32_t hv[32];
       tmem_ld32_async(tstate, hv);
       tmem_wait_ld(hv);
@@ -649,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       for (int q = 0; q < 32; q++) hl[(32 * hf + q) * kN + row] = __uint_as_float(hv[q]);
     }
     if (tid == kStoreTid) bulk_wait_all();  // the y stores are complete
-    if (fail && tid == 0) atomicOr(p.fault, kFaultTileWait);
+    if (aborted && tid == 0) atomicOr(p.fault, kFaultTileWait);
   }
   tc_fence_before();
   __syncthreads();

@@ -115,3 +115,19 @@ def test_ssd_errors_and_empty():
                   y=torch.empty(1, 0, 2, 64, dtype=torch.bfloat16, device="cuda"), h_last=hl)
     torch.cuda.synchronize()
     assert torch.equal(hl, d["h0"])
+
+
+@pytest.mark.parametrize("dt_level,a_scale", [(4.0, 1.0), (-6.0, 0.01), (2.0, 8.0)],
+                         ids=["strong-decay", "almost-no-decay", "decay-underflows"])
+def test_ssd_decay_extremes(dt_level, a_scale):
+    # delta ~ softplus(dt_level) with A scaled by a_scale: a decay so strong
+    # that the state forgets within a few steps (the factors of the decay
+    # between steps underflow to zero), and one so weak that a chunk carries
+    # almost all of it; both must stay finite and within the bound
+    x = gen.random_ssd_inputs(2, 300, 4, 64, 128, 2, in_dtype="bf16", seed=17, with_h0=True)
+    x["dt_bias"] = torch.full_like(x["dt_bias"], dt_level)
+    x["A"] = (x["A"] * a_scale).contiguous()
+    yr, hr = oracle.ssd(x, 2)
+    y, h = _run(x, F32)
+    assert_close(y, yr, BF16, what=f"ssd y, dt level {dt_level}, A x {a_scale}")
+    assert_close(h, hr, BF16, what=f"ssd h_last, dt level {dt_level}, A x {a_scale}")
