@@ -216,27 +216,17 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
-// eight floats -> eight bf16 (16 bytes), high part and remainder
-__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int i = 0; i < 4; i++) {
-    const __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-    const float2 hf = __bfloat1622float2(hh);
-    const __nv_bfloat162 ll = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
-    h[i] = *reinterpret_cast<const uint32_t*>(&hh);
-    l[i] = *reinterpret_cast<const uint32_t*>(&ll);
-  }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
-__device__ __forceinline__ void widen8(uint4 w, float (&v)[8]) {
-  const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; i++) {
-    v[2 * i] = __uint_as_float(a[i] << 16);
-    v[2 * i + 1] = __uint_as_float(a[i] & 0xffff0000u);
-  }
+__device__ __forceinline__ f2 splat2(float a) { return pk(a, a); }
+// a pair of floats -> its bf16 high parts (one word, the first value in the
+// low half) and the bf16 remainders
+__device__ __forceinline__ void split2(f2 v, uint32_t& hi, uint32_t& lo) {
+  uint32_t h, l;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(f2hi(v)), "f"(f2lo(v)));
+  const f2 hv = pk(__uint_as_float(h << 16), __uint_as_float(h & 0xffff0000u));
+  const f2 r = fma2(hv, splat2(-1.f), v);  // exact: v minus its rounded high part
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l) : "f"(f2hi(r)), "f"(f2lo(r)));
+  hi = h;
+  lo = l;
 }
 
 __device__ __forceinline__ void bar_sync_compute() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -504,13 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     auto write_state = [&](const uint32_t (&hv)[32]) {
 #pragma unroll
       for (int c8 = 0; c8 < 4; c8++) {
-        float v[8];
+        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int i = 0; i < 8; i++) v[i] = __uint_as_float(hv[8 * c8 + i]);
-        uint4 hi, lo;
-        split8(v, hi, lo);
-        *reinterpret_cast<uint4*>(sm + SM::HH + sw128(row, 32 * hf + 8 * c8)) = hi;
-        *reinterpret_cast<uint4*>(sm + SM::HL + sw128(row, 32 * hf + 8 * c8)) = lo;
+        for (int i = 0; i < 4; i++)
+          split2(pk(__uint_as_float(hv[8 * c8 + 2 * i]), __uint_as_float(hv[8 * c8 + 2 * i + 1])), hi[i], lo[i]);
+        *reinterpret_cast<uint4*>(sm + SM::HH + sw128(row, 32 * hf + 8 * c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sm + SM::HL + sw128(row, 32 * hf + 8 * c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     };
     {
@@ -542,18 +531,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       // ---- X' (row s, columns p in half hf) = 2^(cs_end - cs_s) delta_s x_s
       wait(kBarX0 + (int)(c & 1));
       {
-        const float ws = ex2(css[kQ - 1] - css[row]) * dls[row];
+        const f2 ws = splat2(ex2(css[kQ - 1] - css[row]) * dls[row]);
 #pragma unroll
         for (int c8 = 0; c8 < 4; c8++) {
           const int off = sw128(row, 32 * hf + 8 * c8);
-          float v[8];
-          widen8(*reinterpret_cast<const uint4*>(xs + off), v);
+          const uint4 xw = *reinterpret_cast<const uint4*>(xs + off);
+          const uint32_t w[4] = {xw.x, xw.y, xw.z, xw.w};
+          uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int i = 0; i < 8; i++) v[i] *= ws;
-          uint4 hi, lo;
-          split8(v, hi, lo);
-          *reinterpret_cast<uint4*>(sm + SM::XH + off) = hi;
-          *reinterpret_cast<uint4*>(sm + SM::XL + off) = lo;
+          for (int i = 0; i < 4; i++)
+            split2(mul2(pk(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)), ws), hi[i], lo[i]);
+          *reinterpret_cast<uint4*>(sm + SM::XH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + SM::XL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       fence_proxy_async_smem();
@@ -575,59 +564,42 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       {
         const float cst = css[row];
         const int kb0 = 2 * hf;
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < 2; j++) {
           const int k = kb0 + j;
-          uint32_t sr[32];
-          if (k <= wq) {
+          uint32_t sr[32];  // S block k, then M's words: [0, 16) the high parts, [16, 32) the remainders
+          if (k < wq) {
+            // below the diagonal block: 2^(cs_t - cs_s) = 2^(cs_t - cs_e) 2^(cs_e - cs_s),
+            // e the block's last step; both factors are at most 1
+            tmem_ld32_async(tlane + kColS + 32 * k, sr);
+            const f2 rt = splat2(ex2(cst - css[32 * k + 31]));
+            tmem_wait_ld(sr);
+            uint32_t lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) {  // (pair i reads S words 2i, 2i + 1 >= i: writing word i is safe)
+              const float2 q = *reinterpret_cast<const float2*>(qsv + 32 * k + 2 * i);
+              const f2 v = mul2(mul2(pk(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), pk(q.x, q.y)), rt);
+              split2(v, sr[i], lo[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; i++) sr[16 + i] = lo[i];
+          } else if (k == wq) {  // the block that holds the diagonal: causal mask, D_h on it
             tmem_ld32_async(tlane + kColS + 32 * k, sr);
             tmem_wait_ld(sr);
-          }
-          uint32_t mw[32];  // [0, 16) the high parts, [16, 32) the remainders
+            float v[32];
 #pragma unroll
-          for (int c8 = 0; c8 < 4; c8++) {
-            const int sb = 32 * k + 8 * c8;
-            float v[8];
-            if (k < wq) {
-              // below the diagonal block: 2^(cs_t - cs_s) = 2^(cs_t - cs_e) 2^(cs_e - cs_s),
-              // e the block's last step; both factors are at most 1
-              const float4 qa = *reinterpret_cast<const float4*>(qsv + sb);
-              const float4 qb = *reinterpret_cast<const float4*>(qsv + sb + 4);
-              const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-              const float rt = ex2(cst - css[32 * k + 31]);
-#pragma unroll
-              for (int i = 0; i < 8; i++) v[i] = __uint_as_float(sr[8 * c8 + i]) * qv[i] * rt;
-            } else if (k == wq) {
-              const float4 ca = *reinterpret_cast<const float4*>(css + sb);
-              const float4 cb = *reinterpret_cast<const float4*>(css + sb + 4);
-              const float4 da = *reinterpret_cast<const float4*>(dls + sb);
-              const float4 db = *reinterpret_cast<const float4*>(dls + sb + 4);
-              const float csv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-              const float dlv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-#pragma unroll
-              for (int i = 0; i < 8; i++) v[i] = __uint_as_float(sr[8 * c8 + i]) * ex2(cst - csv[i]) * dlv[i];
-              // the block that holds the diagonal: causal mask, D_h on it
-#pragma unroll
-              for (int i = 0; i < 8; i++) {
-                const int s = sb + i;
-                v[i] = s < row ? v[i] : (s == row ? v[i] + Dh : 0.f);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; i++) v[i] = 0.f;
+            for (int i = 0; i < 32; i++) {
+              const int s = 32 * k + i;
+              const float m = __uint_as_float(sr[i]) * ex2(cst - css[s]) * dls[s];
+              v[i] = s < row ? m : (s == row ? m + Dh : 0.f);
             }
-            uint4 hi, lo;
-            split8(v, hi, lo);
-            mw[4 * c8 + 0] = hi.x;
-            mw[4 * c8 + 1] = hi.y;
-            mw[4 * c8 + 2] = hi.z;
-            mw[4 * c8 + 3] = hi.w;
-            mw[16 + 4 * c8 + 0] = lo.x;
-            mw[16 + 4 * c8 + 1] = lo.y;
-            mw[16 + 4 * c8 + 2] = lo.z;
-            mw[16 + 4 * c8 + 3] = lo.w;
+#pragma unroll
+            for (int i = 0; i < 16; i++) split2(pk(v[2 * i], v[2 * i + 1]), sr[i], sr[16 + i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i++) sr[i] = 0u;
           }
-          tmem_st32(tlane + kColS + 32 * k, mw);
+          tmem_st32(tlane + kColS + 32 * k, sr);
           tc_fence_before();
           mbar_arrive(&bar[j == 0 ? kRdyM0 : kRdyM1]);
         }
