@@ -217,6 +217,14 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 __device__ __forceinline__ f2 splat2(float a) { return pk(a, a); }
+// pair i (words 2i, 2i + 1) of a word array as packed floats
+__device__ __forceinline__ f2 get2(const uint32_t* w, int i) {
+  return pk(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+}
+__device__ __forceinline__ void set2(uint32_t* w, int i, f2 v) {
+  w[2 * i] = __float_as_uint(f2lo(v));
+  w[2 * i + 1] = __float_as_uint(f2hi(v));
+}
 // a pair of floats -> its bf16 high parts (one word, the first value in the
 // low half) and the bf16 remainders
 __device__ __forceinline__ void split2(f2 v, uint32_t& hi, uint32_t& lo) {
@@ -578,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int i = 0; i < 16; i++) {  // (pair i reads S words 2i, 2i + 1 >= i: writing word i is safe)
               const float2 q = *reinterpret_cast<const float2*>(qsv + 32 * k + 2 * i);
-              const f2 v = mul2(mul2(pk(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), pk(q.x, q.y)), rt);
+              const f2 v = mul2(mul2(get2(sr, i), pk(q.x, q.y)), rt);
               split2(v, sr[i], lo[i]);
             }
 #pragma unroll
@@ -586,15 +594,20 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           } else if (k == wq) {  // the block that holds the diagonal: causal mask, D_h on it
             tmem_ld32_async(tlane + kColS + 32 * k, sr);
             tmem_wait_ld(sr);
-            float v[32];
+            uint32_t lo[16];
+            const int dr = row - 32 * k;  // the diagonal's position in the block
 #pragma unroll
-            for (int i = 0; i < 32; i++) {
-              const int s = 32 * k + i;
-              const float m = __uint_as_float(sr[i]) * ex2(cst - css[s]) * dls[s];
-              v[i] = s < row ? m : (s == row ? m + Dh : 0.f);
+            for (int i = 0; i < 16; i++) {  // (pair i reads S words 2i, 2i + 1 >= i: writing word i is safe)
+              const float2 cs = *reinterpret_cast<const float2*>(css + 32 * k + 2 * i);
+              const float2 dl = *reinterpret_cast<const float2*>(dls + 32 * k + 2 * i);
+              f2 m = mul2(mul2(get2(sr, i), pk(ex2(cst - cs.x), ex2(cst - cs.y))), pk(dl.x, dl.y));
+              float m0 = f2lo(m), m1 = f2hi(m);
+              m0 = 2 * i < dr ? m0 : (2 * i == dr ? m0 + Dh : 0.f);
+              m1 = 2 * i + 1 < dr ? m1 : (2 * i + 1 == dr ? m1 + Dh : 0.f);
+              split2(pk(m0, m1), sr[i], lo[i]);
             }
 #pragma unroll
-            for (int i = 0; i < 16; i++) split2(pk(v[2 * i], v[2 * i + 1]), sr[i], sr[16 + i]);
+            for (int i = 0; i < 16; i++) sr[16 + i] = lo[i];
           } else {
 #pragma unroll
             for (int i = 0; i < 32; i++) sr[i] = 0u;
@@ -618,12 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           tmem_wait_ld(hl);
           tmem_wait_ld(hl2);
 #pragma unroll
-          for (int i = 0; i < 32; i++) hl[i] = __float_as_uint(__uint_as_float(hl[i]) + __uint_as_float(hl2[i]));
+          for (int i = 0; i < 16; i++) set2(hl, i, add2(get2(hl, i), get2(hl2, i)));
         }
         tmem_ld32_async(tstate, hv);
         tmem_wait_ld(hv);
+        const f2 dec2 = splat2(dec);
 #pragma unroll
-        for (int i = 0; i < 32; i++) hv[i] = __float_as_uint(fmaf(dec, __uint_as_float(hv[i]), __uint_as_float(hl[i])));
+        for (int i = 0; i < 16; i++) set2(hv, i, fma2(dec2, get2(hv, i), get2(hl, i)));
         tmem_st32(tstate, hv);
         write_state(hv);
       }
@@ -650,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           tmem_wait_ld(r1);
           tmem_wait_ld(r3);
 #pragma unroll
-          for (int i = 0; i < 32; i++) r1[i] = __float_as_uint(__uint_as_float(r1[i]) + __uint_as_float(r3[i]));
+          for (int i = 0; i < 16; i++) set2(r1, i, add2(get2(r1, i), get2(r3, i)));
         }
         if (y2) {
           tmem_ld32_async(tlane + kColY2 + pb, r2);
@@ -658,12 +672,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         }
         tc_fence_before();
         mbar_arrive(&bar[kRdyY]);  // Y1 and Y2 are read
-        const float et = ex2(css[row]);
-        float* o = reinterpret_cast<float*>(r1);
         if (y2) {
+          const f2 et = splat2(ex2(css[row]));
 #pragma unroll
-          for (int i = 0; i < 32; i++) o[i] = fmaf(et, __uint_as_float(r2[i]), o[i]);
+          for (int i = 0; i < 16; i++) set2(r1, i, fma2(et, get2(r2, i), get2(r1, i)));
         }
+        const float* o = reinterpret_cast<const float*>(r1);
         wait(kStg);  // the previous chunk's y store has read the staging tiles
         if constexpr (sizeof(TOut) == 2) {
 #pragma unroll
