@@ -280,16 +280,35 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
  *  h0, h_last   : [batch, nheads, headdim, dstate] float32 or NULL
  *  y            : [batch, seqlen, nheads, headdim] out_dtype
  * headdim must be 64 and dstate 64 or 128 (SS_ERR_UNSUPPORTED otherwise);
- * nheads must be a multiple of ngroups. Computed in chunks of 64 steps with
- * bf16 tensor-core products accumulated in float32; the operands computed on
- * chip (the masked C.B^T, the weighted B, the carried state) enter the
- * products as two bf16 parts (about 16 significant bits). No workspace.
+ * nheads must be a multiple of ngroups. Computed in chunks (128 steps for
+ * dstate 128, on tcgen05 tensor cores; 64 for dstate 64) with bf16 products
+ * accumulated in float32; the operands computed on chip (the masked C.B^T,
+ * the weighted x or B, the carried state) enter the products as two bf16
+ * parts (about 16 significant bits).
+ *
+ * workspace (optional, device, 16-byte aligned, caller-owned, at least
+ * ss_ssd_fwd_workspace_size bytes when given): with it, a dstate 128 call may
+ * split each (batch, head) sequence into pieces run by different CTAs that
+ * hand the state on through the workspace (so that batch * nheads sequences
+ * fill every SM); its first few KB are reset by the call (on `stream`) and it
+ * must not be shared by calls that can run at the same time. NULL runs one CTA
+ * per sequence. A workspace smaller than needed is SS_ERR_INVALID_ARG. A
+ * hand-over that does not arrive within the wait limit (see
+ * ss_scan_set_wait_limit) ends the waiting pieces and is reported by
+ * ss_scan_status(NULL, stream) as SS_ERR_TIMEOUT; the outputs are then
+ * undefined.
  */
 ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
                      int64_t ngroups, ss_dtype in_dtype, ss_dtype out_dtype,
                      const void *x, const void *dt, const float *A, const void *B, const void *C,
                      const float *D, const float *dt_bias, const float *h0,
-                     void *y, float *h_last, void *stream);
+                     void *y, float *h_last, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of workspace ss_ssd_fwd can use for this problem (0: it never splits
+ * such a problem). Pure host computation: no device call, no error state.
+ */
+size_t ss_ssd_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate);
 
 /*
  * Launch-shape controls for the calling host thread (0 = automatic, the
@@ -300,7 +319,9 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
  * cross-CTA carry path. max_workers > 0 caps the number of CTAs a split of the
  * work uses (default: one per SM), which makes range boundaries and hand-overs
  * more frequent. Results do not depend on these settings beyond fp32 rounding;
- * ss_scan_fwd_workspace_size() follows them.
+ * ss_scan_fwd_workspace_size() follows them. For ss_ssd_fwd (dstate 128, with
+ * a workspace) chunk_len > 0 sets the length of the pieces a sequence is split
+ * into (rounded up to 128 steps) instead of the automatic plan.
  */
 void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_workers);
 
@@ -314,7 +335,9 @@ void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_work
  * split; -1 (the default) publishes all. A withheld flag makes the CTAs that
  * need it give up after wait_ns, set the fault word and return, so the call
  * finishes and ss_scan_status() reports SS_ERR_TIMEOUT; its outputs are then
- * undefined. No wait in the library is unbounded.
+ * undefined. No wait in the library is unbounded. They apply to ss_ssd_fwd
+ * too: there withhold_item is the piece (in the order CTAs take them: piece q
+ * of sequence u is item q * batch * nheads + u) whose state is never handed on.
  */
 void ss_scan_set_wait_limit(uint64_t wait_ns, int64_t withhold_item);
 

@@ -42,7 +42,8 @@ SIGNATURES = {
     "ss_scan_bwd": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int] + [_P] * 21 + [_SZ, _P]),
     "ss_scan_fwd_general": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
                             + [_P] * 11 + [_P]),
-    "ss_ssd_fwd": (ctypes.c_int, [_I64] * 6 + [ctypes.c_int, ctypes.c_int] + [_P] * 10 + [_P]),
+    "ss_ssd_fwd": (ctypes.c_int, [_I64] * 6 + [ctypes.c_int, ctypes.c_int] + [_P] * 11 + [ctypes.c_size_t, _P]),
+    "ss_ssd_fwd_workspace_size": (ctypes.c_size_t, [_I64] * 4),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
     "ss_scan_set_wait_limit": (None, [ctypes.c_uint64, _I64]),
     "ss_scan_status": (ctypes.c_int, [_P, _P]),
@@ -234,11 +235,17 @@ def ss_scan_fwd_general(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, 
     return y, h_last
 
 
+def ss_ssd_fwd_workspace_size(batch, seqlen, nheads, dstate):
+    return int(lib().ss_ssd_fwd_workspace_size(batch, seqlen, nheads, dstate))
+
+
 def ss_ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, out_dtype=None, y=None, h_last=None,
-               return_h_last=True, stream=None):
+               workspace=None, return_h_last=True, stream=None):
     """State-space-dual (Mamba-2) layer on device tensors: x [Bt, L, H, 64], dt
     [Bt, L, H], B, C [Bt, L, G, N] (bf16); A, D, dt_bias [H]; h0 [Bt, H, 64, N]
-    float32. Returns (y, h_last)."""
+    float32. Returns (y, h_last). The workspace (uint8) is allocated with torch
+    when the problem can use one and none is given; workspace=False runs
+    without one."""
     Bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     code = _dt(x)
@@ -248,8 +255,13 @@ def ss_ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, out_dtype=None,
         y = torch.empty((Bt, L, H, P), dtype=_tdt(out_code), device=dev)
     if h_last is None and return_h_last:
         h_last = torch.empty((Bt, H, P, N), dtype=torch.float32, device=dev)
+    if workspace is None:
+        ws_bytes = ss_ssd_fwd_workspace_size(Bt, L, H, N)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else False
+    ws_ptr = _ptr(workspace) if workspace is not False else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not False else 0
     _check(lib().ss_ssd_fwd(Bt, L, H, P, N, G, code, out_code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                            _ptr(dt_bias), _ptr(h0), _ptr(y), _ptr(h_last), _stream(stream)))
+                            _ptr(dt_bias), _ptr(h0), _ptr(y), _ptr(h_last), ws_ptr, ws_len, _stream(stream)))
     return y, h_last
 
 

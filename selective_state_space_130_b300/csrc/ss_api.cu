@@ -309,6 +309,45 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
 
 }  // namespace
 
+namespace ssk {
+// Pieces per (batch, head) sequence for the d_state 128 kernel. Each CTA runs
+// one piece; CTAs run one per SM, so with `units` sequences the layer takes
+// about ceil(units * pieces / sms) rounds of a piece each. A CTA costs its
+// chunks plus a fixed 1.6 chunks (start-up, pipeline fill, taking over and
+// handing on the state: fitted to B300 timings of the Mamba-2 2.7B layer
+// split into 1 to 16 pieces); the plan with the smallest estimate wins (fewer
+// pieces on a tie).
+int64_t plan_ssd_pieces(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate, int sms,
+                        int64_t force_steps) {
+  const int64_t nchunk = (seqlen + 127) / 128, units = batch * nheads;
+  if (dstate != 128 || nchunk <= 1 || units <= 0) return 1;
+  if (force_steps > 0) {
+    const int64_t pc = std::max<int64_t>(1, (force_steps + 127) / 128);
+    return (nchunk + pc - 1) / pc;
+  }
+  int64_t best = 1;
+  double best_cost = 0;
+  for (int64_t P = 1; P <= nchunk; P++) {
+    const int64_t pc = (nchunk + P - 1) / P, pe = (nchunk + pc - 1) / pc;
+    if (pe != P) continue;
+    const double rounds = (double)((units * pe + sms - 1) / sms);
+    const double cost = rounds * ((double)pc + 1.6);
+    if (P == 1 || cost < best_cost - 1e-9) {
+      best = pe;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+// The split's workspace: a ticket counter (256 bytes), one flag per sequence
+// (padded to 256 bytes), then one fp32 state per sequence.
+size_t ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate) {
+  const int64_t nchunk = (seqlen + 127) / 128, units = batch * nheads;
+  if (dstate != 128 || nchunk <= 1 || units <= 0) return 0;
+  return 256 + (size_t)((units * 4 + 255) / 256 * 256) + (size_t)units * 64 * 128 * sizeof(float);
+}
+}  // namespace ssk
+
 extern "C" {
 
 int ss_version(void) { return kVersion; }
@@ -591,10 +630,18 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
   return SS_OK;
 }
 
+
+size_t ss_ssd_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate) {
+  if (batch < 0 || seqlen < 0 || nheads < 0) return 0;
+  if ((double)batch * (double)nheads * (double)seqlen > 4.0e18) return 0;
+  return ssk::ssd_workspace_bytes(batch, seqlen, nheads, dstate);
+}
+
 ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
                      int64_t ngroups, ss_dtype in_dtype, ss_dtype out_dtype, const void* x, const void* dt,
                      const float* A, const void* B, const void* C, const float* D, const float* dt_bias,
-                     const float* h0, void* y, float* h_last, void* stream) {
+                     const float* h0, void* y, float* h_last, void* workspace, size_t workspace_bytes,
+                     void* stream) {
   g_err.clear();
   if (in_dtype != SS_BF16) return fail(SS_ERR_UNSUPPORTED, "the state-space-dual layer takes bf16 inputs");
   if (!valid_dtype(out_dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown output dtype %d", (int)out_dtype);
@@ -618,10 +665,13 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
     for (int i = 0; i < 5; i++)
       if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
   }
-  const void* all[] = {x, dt, A, B, C, D, dt_bias, h0, y, h_last};
-  const char* all_names[] = {"x", "dt", "A", "B", "C", "D", "dt_bias", "h0", "y", "h_last"};
-  for (int i = 0; i < 10; i++)
+  const void* all[] = {x, dt, A, B, C, D, dt_bias, h0, y, h_last, workspace};
+  const char* all_names[] = {"x", "dt", "A", "B", "C", "D", "dt_bias", "h0", "y", "h_last", "workspace"};
+  for (int i = 0; i < 11; i++)
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  const size_t need = ssk::ssd_workspace_bytes(batch, seqlen, nheads, dstate);
+  if (workspace && need > 0 && workspace_bytes < need)
+    return fail(SS_ERR_INVALID_ARG, "workspace too small (%zu bytes, need %zu)", workspace_bytes, need);
   ss_status st = check_device();
   if (st != SS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -635,7 +685,30 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
   if ((double)batch * nheads > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
   ssk::SsdParams p{x, dt, A, B, C, D, dt_bias, h0, y, h_last, batch, seqlen, nheads, ngroups,
                    ssk::device_fault_word(), g_wait_ns};
-  cudaError_t e = ssk::launch_ssd_fwd(p, (int)dstate, out_dtype, s);
+  p.pieces = 1;
+  p.piece_chunks = (seqlen + 127) / 128;
+  p.ws_ticket = nullptr;
+  p.ws_flags = nullptr;
+  p.ws_state = nullptr;
+  p.withhold_piece = g_withhold;
+  cudaError_t e = cudaSuccess;
+  if (workspace && need > 0) {
+    const int64_t P = ssk::plan_ssd_pieces(batch, seqlen, nheads, dstate, ssk::device_sm_count(), g_tune_chunk);
+    if (P > 1) {
+      if ((double)batch * (double)nheads * (double)P > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
+      const int64_t nchunk = (seqlen + 127) / 128;
+      uint8_t* w = static_cast<uint8_t*>(workspace);
+      const size_t flags_bytes = (size_t)((batch * nheads * 4 + 255) / 256 * 256);
+      p.pieces = P;
+      p.piece_chunks = (nchunk + P - 1) / P;
+      p.ws_ticket = reinterpret_cast<unsigned int*>(w);
+      p.ws_flags = reinterpret_cast<unsigned int*>(w + 256);
+      p.ws_state = reinterpret_cast<float*>(w + 256 + flags_bytes);
+      if ((e = cudaMemsetAsync(w, 0, 256 + flags_bytes, s)) != cudaSuccess)
+        return cuda_fail(e, "state-space-dual workspace reset");
+    }
+  }
+  e = ssk::launch_ssd_fwd(p, (int)dstate, out_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "state-space-dual launch");
   return SS_OK;
 }

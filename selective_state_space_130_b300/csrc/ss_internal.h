@@ -149,7 +149,21 @@ struct SsdParams {
   int64_t batch, seqlen, nheads, ngroups;
   unsigned int* fault;      // the library's fault word (timed-out waits)
   uint64_t wait_ns;         // limit of a device-side wait; 0 = the default
+  // Sequence split (d_state 128): each (batch, head) sequence runs as `pieces`
+  // pieces of `piece_chunks` 128-step chunks, taken by CTAs in the order of a
+  // ticket counter; piece q > 0 starts from the state piece q - 1 left in
+  // ws_state[(batch, head)], published through ws_flags[(batch, head)] = q.
+  // pieces == 1: one CTA per (batch, head), no workspace.
+  int64_t pieces, piece_chunks;
+  unsigned int* ws_ticket;  // zeroed before the launch
+  unsigned int* ws_flags;   // [batch * nheads], zeroed before the launch
+  float* ws_state;          // [batch * nheads, 64, dstate]
+  int64_t withhold_piece;   // test knob: this ticket does not publish its state (-1: none)
 };
+// SSD split plan: pieces per (batch, head) sequence for `sms` SMs, and the
+// workspace bytes the split needs (0 when it cannot help).
+int64_t plan_ssd_pieces(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate, int sms, int64_t force_steps);
+size_t ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate);
 
 // Launch plan for a scan problem.
 struct ScanPlan {

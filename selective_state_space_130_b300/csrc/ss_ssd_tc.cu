@@ -92,7 +92,7 @@ struct TcSmem {
   static constexpr int QS = WSUM + 64;        // q_s of two chunks [2][128] f32 (see the kernel)
   static constexpr int DTB = QS + 1024;       // dt words of two chunks [2][128] u32 (see the kernel)
   static constexpr int BAR = DTB + 1024;      // mbarriers, see the kernel (at most 16)
-  static constexpr int TSLOT = BAR + 128;     // tensor-memory base address
+  static constexpr int TSLOT = BAR + 128;     // tensor-memory base address, then the piece's ticket
   static constexpr int BYTES = TSLOT + 64;
   static constexpr int ALLOC = BYTES + 1024;  // + alignment slack
 };
@@ -274,15 +274,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SM::BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM::TSLOT);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t bh = blockIdx.x;
-  const int64_t b = bh / p.nheads, h = bh % p.nheads;
   const int64_t L = p.seqlen, H = p.nheads, G = p.ngroups;
   const int64_t nchunk = (L + kQ - 1) / kQ;
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
+  uint32_t* tk_slot = tslot + 1;
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; i++) mbar_init(&bar[i], (i < kRdyX || i == kStg) ? 1 : kCompute);
     fence_mbar_init();
+    // the piece this CTA runs: tickets in launch order, so a piece's
+    // predecessor always belongs to a CTA that started earlier
+    *tk_slot = p.pieces > 1 ? atomicAdd(p.ws_ticket, 1u) : blockIdx.x;
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
@@ -294,6 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  const int64_t ticket = *tk_slot;
+  const int64_t units = p.batch * H;
+  const int64_t bh = ticket % units, piece = ticket / units;
+  const int64_t b = bh / H, h = bh % H;
+  const int64_t c_begin = piece * p.piece_chunks;
+  const int64_t c_end = c_begin + p.piece_chunks < nchunk ? c_begin + p.piece_chunks : nchunk;
+  const bool last_piece = piece == p.pieces - 1;
   uint32_t ph = 0;    // bit i: the phase of barrier i this thread waits for next
   bool fail = false;  // this thread gave up on a wait
   // wait for the next phase of barrier i; after a timeout the phase stays
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     fail = true;
     return false;
   };
-  const bool has_h0 = p.h0 != nullptr;
+  const bool has_h0 = piece > 0 || p.h0 != nullptr;  // a state enters the piece
 
   if (warp >= kComputeWarps) {
     // ============ the issuing warps: lane 0 of each issues. Issuer 0: the
@@ -355,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           else
             nissue[kBarX0]++;
         };
-        issue_cb(0);
-        issue_x(0);
-        for (int64_t c = 0; c < nchunk; c++) {
+        issue_cb(c_begin);
+        issue_x(c_begin);
+        for (int64_t c = c_begin; c < c_end; c++) {
           // S = C B^T (S's columns were read by the previous chunk's Y1)
           if (!wait(kBarCB)) break;
           tc_fence_after();
@@ -365,29 +374,29 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           commit(kBarS);
           // x of the next chunk, into the buffer of the chunk before this one
           // (its Y1 is done, its X' written)
-          if (c + 1 < nchunk) issue_x(c + 1);
+          if (c + 1 < c_end) issue_x(c + 1);
           // H_l^T = B^T X' (A = B read MN-major: its two n halves are one tile
           // apart; B: X''s high part and remainder side by side, N = 128)
           if (!wait(kRdyX)) break;
           tc_fence_after();
           mma_k128(tmem + kColH, s0 + SM::B0, false, s0 + SM::XH, false, SM::TILE, SM::TILE, idesc(kN, 2 * kP, 1, 1));
           commit(kBarH);
-          if (c + 1 < nchunk) {
+          if (c + 1 < c_end) {
             // C and B are free once S, H_l (in issue order) and Y2 are done;
             // S's columns and this x once both halves of Y1 are
-            if (!wait(kBarH) || ((c > 0 || has_h0) && !wait(kBarY2))) break;
+            if (!wait(kBarH) || ((c > c_begin || has_h0) && !wait(kBarY2))) break;
             issue_cb(c + 1);
             if (!wait(kBarY1a) || !wait(kBarY1b)) break;
           }
         }
       } else if (role == 1) {
-        for (int64_t c = 0; c < nchunk; c++) {
+        for (int64_t c = c_begin; c < c_end; c++) {
           const uint32_t xs = s0 + ((c & 1) ? SM::X1 : SM::X0);
-          if (!wait(kBarCB)) break;                // C of the chunk
-          if (c > 0 && !wait(kRdyY)) break;        // the previous y has read Y1a and Y2
+          if (!wait(kBarCB)) break;                    // C of the chunk
+          if (c > c_begin && !wait(kRdyY)) break;      // the previous y has read Y1a and Y2
           // Y2 = C H_in^T: A K-major (C), B MN-major (H^T), the high part and
           // then the remainder into one accumulator
-          if (c > 0 || has_h0) {
+          if (c > c_begin || has_h0) {
             if (!wait(kRdyH)) break;  // the state entering the chunk is written
             tc_fence_after();
             mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HH, false, 16, 16, idesc(kQ, kP, 0, 1));
@@ -403,9 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           commit(kBarY1a);
         }
       } else {
-        for (int64_t c = 0; c < nchunk; c++) {
+        for (int64_t c = c_begin; c < c_end; c++) {
           const uint32_t xs = s0 + ((c & 1) ? SM::X1 : SM::X0);
-          if (c > 0 && !wait(kRdyY)) break;  // the previous y has read Y1b
+          if (c > c_begin && !wait(kRdyY)) break;  // the previous y has read Y1b
           if (!wait(kRdyM0)) break;
           tc_fence_after();
           y1_block(kColY1b, xs, 2, true);
@@ -474,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       if (hf == 0) {
         asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk cc
         dl = cc * kQ + row < L ? softplus_fast(dt_of(cc) + dtbias) : 0.f;
-        if (cc + 1 < nchunk) {
+        if (cc + 1 < c_end) {
           fetch_dt(cc + 1);
           asm volatile("cp.async.commit_group;" ::: "memory");
         }
@@ -510,11 +519,24 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         *reinterpret_cast<uint4*>(sm + SM::HL + sw128(row, 32 * hf + 8 * c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     };
+    // the state entering the piece: h0 (or zeros) for the first piece of a
+    // sequence, else the one the previous piece published (a bounded wait)
+    bool aborted = false;  // a wait timed out; the same for every compute thread
+    if (piece > 0) {
+      bool got = true;
+      if (tid == 0) {
+        const uint32_t* flag = p.ws_flags + bh;
+        got = ld_acquire_gpu(flag) >= (uint32_t)piece;
+        const uint64_t t_start = globaltimer();
+        while (!got && globaltimer() - t_start <= wait_ns) got = ld_acquire_gpu(flag) >= (uint32_t)piece;
+      }
+      aborted = bar_or_compute(!got);
+    }
     {
       uint32_t hv[32];
-      const float* h0 = has_h0 ? p.h0 + (b * H + h) * kP * kN : nullptr;
+      const float* h0 = piece > 0 ? p.ws_state + bh * kP * kN : (p.h0 ? p.h0 + bh * kP * kN : nullptr);
 #pragma unroll
-      for (int q = 0; q < 32; q++) hv[q] = __float_as_uint(h0 ? __ldg(h0 + (32 * hf + q) * kN + row) : 0.f);
+      for (int q = 0; q < 32; q++) hv[q] = __float_as_uint(h0 && !aborted ? h0[(32 * hf + q) * kN + row] : 0.f);
       tmem_st32(tstate, hv);
       if (has_h0) {
         write_state(hv);
@@ -524,13 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       if (has_h0) mbar_arrive(&bar[kRdyH]);
     }
     if (hf == 0) {
-      fetch_dt(0);
+      fetch_dt(c_begin);
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    scalars(0);
+    scalars(c_begin);
     bar_sync_compute();
-    bool aborted = false;  // the loop ended on a timed-out wait
-    for (int64_t c = 0; c < nchunk; c++) {
+    for (int64_t c = c_begin; c < c_end && !aborted; c++) {
       const int64_t t0 = c * kQ;
       const float* dls = dls2 + (c & 1) * kQ;
       const float* css = css2 + (c & 1) * kQ;
@@ -645,12 +666,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       tc_fence_before();
       mbar_arrive(&bar[kRdyH]);
       // ---- the next chunk's delta and decay sums, while Y1 runs
-      if (c + 1 < nchunk) scalars(c + 1);
+      if (c + 1 < c_end) scalars(c + 1);
       // ---- y of row t, columns p in half hf: Y1 + 2^cs_t Y2, staged in
       // shared memory and stored by TMA
       wait(kBarY1a);
       wait(kBarY1b);
-      const bool y2 = c > 0 || has_h0;
+      const bool y2 = c > c_begin || has_h0;
       if (y2) wait(kBarY2);
       tc_fence_after();
       bool abort;
@@ -708,13 +729,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
       }
       if (abort) break;
     }
-    if (!aborted && p.h_last) {  // (aborted is the same for every compute thread)
+    // the state leaving the piece: h_last after the last piece, else the
+    // hand-over slot, published for the next piece
+    float* hout = last_piece ? p.h_last : p.ws_state;
+    if (!aborted && hout) {  // (aborted is the same for every compute thread)
       uint32_t hv[32];
       tmem_ld32_async(tstate, hv);
       tmem_wait_ld(hv);
-      float* hl = p.h_last + (b * H + h) * kP * kN;
+      float* hl = hout + bh * kP * kN;
 #pragma unroll
       for (int q = 0; q < 32; q++) hl[(32 * hf + q) * kN + row] = __uint_as_float(hv[q]);
+    }
+    if (!last_piece) {
+      bar_sync_compute();  // every thread's part of the state is written
+      if (tid == 0 && !aborted && ticket != p.withhold_piece) {
+        __threadfence();
+        st_release_gpu(p.ws_flags + bh, (uint32_t)(piece + 1));
+      }
     }
     if (tid == kStoreTid) bulk_wait_all();  // the y stores are complete
     if (aborted && tid == 0) atomicOr(p.fault, kFaultTileWait);
@@ -769,7 +800,7 @@ cudaError_t launch_tc(const SsdParams& p, cudaStream_t s) {
   auto k = ssd_tc_kernel<TOut>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::ALLOC);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)(p.batch * p.nheads), kThreads, TcSmem::ALLOC, s>>>(p, mx, mb, mc, my);
+  k<<<(unsigned)(p.batch * p.nheads * p.pieces), kThreads, TcSmem::ALLOC, s>>>(p, mx, mb, mc, my);
   return cudaGetLastError();
 }
 

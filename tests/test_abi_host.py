@@ -187,9 +187,9 @@ def _ssd(**kw):
     a.update({k: v for k, v in kw.items() if k in a})
     p = [kw.get(k, v) for k, v in (("x", 0x1000), ("dt", 0x2000), ("A", 0x3000), ("B", 0x4000), ("C", 0x5000),
                                    ("D", None), ("dt_bias", None), ("h0", None), ("y", 0x6000),
-                                   ("h_last", None))]
+                                   ("h_last", None), ("workspace", None))]
     return ss.lib().ss_ssd_fwd(a["batch"], a["seqlen"], a["nheads"], a["headdim"], a["dstate"], a["ngroups"],
-                               a["in_dtype"], a["out_dtype"], *p, None)
+                               a["in_dtype"], a["out_dtype"], *p, kw.get("workspace_bytes", 0), None)
 
 
 @pytest.mark.parametrize("kw,code,msg", [
@@ -203,6 +203,22 @@ def _ssd(**kw):
 def test_ssd_rejects_bad_arguments(kw, code, msg):
     assert _ssd(**kw) == code
     assert msg in ss.ss_last_error()
+
+
+def test_ssd_workspace_size_and_checks():
+    # one ticket counter (256 bytes), one flag per (batch, head) padded to 256
+    # bytes, one 64 x 128 fp32 state per (batch, head); nothing for d_state 64
+    # or a single chunk, which never split
+    assert ss.ss_ssd_fwd_workspace_size(4, 2048, 80, 128) == 256 + 1280 + 320 * 64 * 128 * 4
+    assert ss.ss_ssd_fwd_workspace_size(1, 300, 3, 128) == 256 + 256 + 3 * 64 * 128 * 4
+    assert ss.ss_ssd_fwd_workspace_size(4, 2048, 80, 64) == 0
+    assert ss.ss_ssd_fwd_workspace_size(2, 128, 8, 128) == 0
+    assert ss.ss_ssd_fwd_workspace_size(-1, 128, 8, 128) == 0
+    need = ss.ss_ssd_fwd_workspace_size(1, 300, 4, 128)
+    assert _ssd(seqlen=300, workspace=0x10000, workspace_bytes=need - 1) == _lib.SS_ERR_INVALID_ARG
+    assert "workspace" in ss.ss_last_error()
+    assert _ssd(seqlen=300, workspace=0x10008, workspace_bytes=need) == _lib.SS_ERR_INVALID_ARG
+    assert "workspace" in ss.ss_last_error()
 
 
 def test_new_entry_points_empty_problems_without_device():

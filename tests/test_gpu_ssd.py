@@ -107,7 +107,7 @@ def test_ssd_errors_and_empty():
                                      (64, 96, 1, ss.SS_BF16, ss._lib.SS_ERR_UNSUPPORTED),
                                      (64, 64, 3, ss.SS_BF16, ss._lib.SS_ERR_INVALID_ARG),
                                      (64, 64, 1, ss.SS_F32, ss._lib.SS_ERR_UNSUPPORTED)]:
-        st = lib.ss_ssd_fwd(1, 4, 2, P, N, G, dt_code, ss.SS_BF16, *ptrs, y.data_ptr(), None, None)
+        st = lib.ss_ssd_fwd(1, 4, 2, P, N, G, dt_code, ss.SS_BF16, *ptrs, y.data_ptr(), None, None, 0, None)
         assert st == code, (P, N, G, st, ss.ss_last_error())
     e = {k: d[k][:, :0].contiguous() for k in ("x", "dt", "B", "C")}
     hl = torch.full((1, 2, 64, 64), 3.0, device="cuda")
@@ -131,3 +131,64 @@ def test_ssd_decay_extremes(dt_level, a_scale):
     y, h = _run(x, F32)
     assert_close(y, yr, BF16, what=f"ssd y, dt level {dt_level}, A x {a_scale}")
     assert_close(h, hr, BF16, what=f"ssd h_last, dt level {dt_level}, A x {a_scale}")
+
+
+# (batch, L, heads, groups, h0, piece length in steps): sequences split into
+# pieces run by different CTAs, the state handed on through the workspace
+SPLITS = [(1, 1000, 2, 2, True, 128), (2, 1000, 3, 1, False, 256), (1, 1100, 4, 2, True, 384),
+          (3, 700, 2, 1, True, 512)]
+
+
+@pytest.mark.parametrize("case", SPLITS, ids=[f"b{c[0]}-L{c[1]}-H{c[2]}-G{c[3]}-piece{c[5]}" for c in SPLITS])
+def test_ssd_split_sequences(case):
+    Bt, L, H, G, h0, piece = case
+    x = gen.random_ssd_inputs(Bt, L, H, 64, 128, G, in_dtype="bf16", seed=L + piece, with_h0=h0)
+    yr, hr = oracle.ssd(x, G)
+    ss.ss_scan_set_tuning(0, piece, 0)
+    try:
+        y, h = _run(x, F32)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+    ss.ss_scan_status(None)
+    assert_close(y, yr, BF16, what=f"split ssd y {case}")
+    assert_close(h, hr, BF16, what=f"split ssd h_last {case}")
+    assert_close(y, yr, F32, what=f"split ssd y {case} (float32 bound)")
+
+
+def test_ssd_without_workspace():
+    # no workspace: one CTA per (batch, head), the whole sequence in order
+    x = gen.random_ssd_inputs(2, 1000, 3, 64, 128, 1, in_dtype="bf16", seed=9, with_h0=True)
+    yr, hr = oracle.ssd(x, 1)
+    d = to_dev(x)
+    y, h = ss.ss_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], d["h0"],
+                         out_dtype=F32, workspace=False)
+    torch.cuda.synchronize()
+    assert_close(y.double().cpu().numpy(), yr, BF16, what="ssd y without workspace")
+    assert_close(h.double().cpu().numpy(), hr, BF16, what="ssd h_last without workspace")
+
+
+def test_ssd_withheld_hand_over_times_out():
+    # piece 0 of sequence 0 never hands its state on: piece 1 of that sequence
+    # gives up after the short limit, the call finishes, the status reports the
+    # timeout once, and a clean call is correct again
+    x = gen.random_ssd_inputs(1, 1000, 2, 64, 128, 1, in_dtype="bf16", seed=41, with_h0=True)
+    d = to_dev(x)
+    ss.ss_scan_set_tuning(0, 256, 0)
+    try:
+        ss.ss_scan_set_wait_limit(2_000_000, 0)
+        try:
+            ss.ss_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], d["h0"], out_dtype=F32)
+        finally:
+            ss.ss_scan_set_wait_limit(0, -1)
+        torch.cuda.synchronize()
+        with pytest.raises(ss.SSError) as ei:
+            ss.ss_scan_status(None)
+        assert ei.value.status == ss._lib.SS_ERR_TIMEOUT
+        ss.ss_scan_status(None)
+        y, h = _run(x, F32)
+        ss.ss_scan_status(None)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+    yr, hr = oracle.ssd(x, 1)
+    assert_close(y, yr, BF16, what="ssd y after a timed-out hand-over")
+    assert_close(h, hr, BF16, what="ssd h_last after a timed-out hand-over")
