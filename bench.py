@@ -544,13 +544,17 @@ def bench_ssd(ss, dev, hbm_peak, tensor_peak, Bt=4, L=2048, H=80, N=128, G=1, re
     """ss_ssd_fwd (state-space-dual layer, tensor-core chunked form) on a Mamba-2
     2.7B-shaped layer: batch 4, L 2048, 80 heads x 64 channels (d_inner 5120),
     d_state 128, one group, bf16 in and out. One input set (larger than L2)."""
-    P, Q = 64, 64
+    P = 64
+    Q = 128 if N == 128 else 64  # the kernel's chunk length
     x = to_dev(gen.random_ssd_inputs(Bt, L, H, P, N, G, in_dtype="bf16", seed=11), dev)
     y = torch.empty((Bt, L, H, P), dtype=torch.bfloat16, device=dev)
     hl = torch.empty((Bt, H, P, N), dtype=torch.float32, device=dev)
+    nws = ss.ss_ssd_fwd_workspace_size(Bt, L, H, N)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else False
 
     def call():
-        ss.ss_ssd_fwd(x["x"], x["dt"], x["A"], x["B"], x["C"], x["D"], x["dt_bias"], None, y=y, h_last=hl)
+        ss.ss_ssd_fwd(x["x"], x["dt"], x["A"], x["B"], x["C"], x["D"], x["dt_bias"], None, y=y, h_last=hl,
+                      workspace=ws)
 
     for _ in range(3):
         call()
@@ -582,8 +586,9 @@ def bench_ssd(ss, dev, hbm_peak, tensor_peak, Bt=4, L=2048, H=80, N=128, G=1, re
                          "note": "at the measured peaks the bytes take longer than the algorithmic flops"},
             "tensor": {"algorithmic_flops": flops, "achieved_tflops": round(flops / t / 1e12, 2),
                        "peak_tflops": tensor_peak, "frac": round(flops / t / 1e12 / tensor_peak, 4),
-                       "note": "mma.sync m16n8k16 bf16; operands computed on chip run as two bf16 parts, "
-                               "so the tensor pipe executes about 1.8x the algorithmic flops"},
+                       "note": "tcgen05.mma kind::f16 (bf16 operands, fp32 accumulators in tensor memory); "
+                               "operands computed on chip (M, X', the state) run as two bf16 parts, so the tensor "
+                               "pipe executes about 1.8x the algorithmic flops"},
             "l2": "one input set of 176 MB (larger than L2)"}
 
 

@@ -102,7 +102,7 @@ int device_sm_count() {
 // about 148 cycles, two lanes per channel 64 channels in about 87.
 static double block_token_cost(int sg) { return sg == 1 ? 148.0 : 87.0; }
 
-ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype, int sms) {
+ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype, int sms, bool with_workspace) {
   ScanPlan pl{};
   const int64_t W = g_tune_workers > 0 ? std::min<int64_t>(sms, g_tune_workers) : sms;  // CTA slots (one per SM)
   const bool chunkable = seqlen >= 2 * kMinChunk;
@@ -134,7 +134,9 @@ ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype
   pl.nworkers = nblk;
   pl.chunk_tiles = T;
   pl.nchunks = 1;
-  if (g_tune_chunk > 0) {
+  if (!with_workspace) {
+    // static: every block runs its whole sequence
+  } else if (g_tune_chunk > 0) {
     pl.chunk_tiles = std::max<int64_t>(1, (g_tune_chunk + tile - 1) / tile);
   } else if (nblk > W) {
     // equal ranges, one per CTA slot; at least one block per range keeps every
@@ -235,12 +237,13 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
                       ss_dtype out_dtype, const void* u, const void* delta_raw, const float* A, const void* B,
                       const void* C, const float* D, const void* z, const float* delta_bias, const float* h0,
                       void* y, float* h_last, void* workspace, size_t workspace_bytes, bool noalloc,
-                      void* stream) {
+                      void* stream, bool static_only = false) {
   bool empty = false;
   ss_status st0 = scan_check_args(batch, seqlen, dim, dstate, in_dtype, out_dtype, u, delta_raw, A, B, C, D, z,
                                   delta_bias, h0, y, h_last, workspace, &empty);
   if (st0 != SS_OK || empty) return st0;
-  const ssk::ScanPlan plan = ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim, in_dtype, ssk::device_sm_count());
+  const ssk::ScanPlan plan =
+      ssk::plan_scan(batch, seqlen > 0 ? seqlen : 1, dim, in_dtype, ssk::device_sm_count(), !static_only);
   if (seqlen > 0 && plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) {
     if (noalloc)
       return fail(SS_ERR_INVALID_ARG,
@@ -585,6 +588,12 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
   if (batch == 0 || dim == 0) return SS_OK;
   if ((double)batch * (double)seqlen * (double)dim * (double)dstate > 4.0e18)
     return fail(SS_ERR_INVALID_ARG, "problem too large");
+  // d_state 16, one group, first order is exactly the selective scan of
+  // ss_scan_fwd (B and C [batch, seqlen, 1, 16] are [batch, seqlen, 16]): run it
+  // on that kernel, in its static split, which needs no workspace
+  if (dstate == 16 && ngroups == 1 && disc == SS_DISC_FIRST_ORDER)
+    return scan_common(batch, seqlen, dim, dstate, in_dtype, out_dtype, u, delta_raw, A, B, C, D, z, delta_bias, h0,
+                       y, h_last, nullptr, 0, false, stream, true);
   const void* need[] = {u, delta_raw, A, B, C, y};
   const char* names[] = {"u", "delta_raw", "A", "B", "C", "y"};
   if (seqlen > 0) {

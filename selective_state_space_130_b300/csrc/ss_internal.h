@@ -178,7 +178,10 @@ struct ScanPlan {
 };
 
 // Plan for `sms` streaming multiprocessors (one CTA per SM at a time).
-ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype, int sms);
+// with_workspace false: the static plan only (one CTA per channel block, no
+// cross-CTA hand-over, no workspace).
+ScanPlan plan_scan(int64_t batch, int64_t seqlen, int64_t dim, ss_dtype in_dtype, int sms,
+                   bool with_workspace = true);
 // SM count of the current device (cached per device), or a default when it
 // cannot be queried.
 int device_sm_count();
