@@ -632,9 +632,11 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
   if (((size_t)dim * es) % 16 == 0 && in_row % 16 == 0) chunk = 16;
   else if (((size_t)dim * es) % 4 == 0 && in_row % 4 == 0) chunk = 4;
   ssk::GenParams p{u, delta_raw, z, B, C, A, D, delta_bias, h0, y, h_last, batch, seqlen, dim, ngroups, cpg,
-                   (int)ncblk, ngw_max, chunk, (int)disc};
+                   (int)ncblk, ngw_max, chunk, (int)disc, ssk::device_fault_word(), g_wait_ns};
   if ((double)batch * ncblk > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
-  cudaError_t e = ssk::launch_scan_general(p, sg, in_dtype, out_dtype, s);
+  cudaError_t e = ssk::scan_general_cta_supported(dim, dstate, cpg, in_dtype)
+                      ? ssk::launch_scan_general_cta(p, dstate, in_dtype, out_dtype, s)
+                      : ssk::launch_scan_general(p, sg, in_dtype, out_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "generalised scan launch");
   return SS_OK;
 }

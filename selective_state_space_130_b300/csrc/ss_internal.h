@@ -132,6 +132,8 @@ struct GenParams {
   int ngw_max;              // most groups one channel block spans
   int chunk_in;             // staging of u, delta_raw, z rows: 16- or 4-byte copies, or 0 (element-wise)
   int disc;                 // 0 first order, 1 zero-order hold
+  unsigned int* fault;      // the library's fault word (timed-out waits)
+  uint64_t wait_ns;         // limit of a device-side wait; 0 = the default
 };
 
 // Parameters of the state-space-dual (Mamba-2) layer forward.
@@ -215,6 +217,11 @@ int64_t scan_bwd_subtiles(int64_t seqlen);
 cudaError_t launch_scan_general(const GenParams& p, int sg, ss_dtype in_dtype, ss_dtype out_dtype,
                                 cudaStream_t stream);
 int scan_general_stage_bytes(int64_t dstate, int ngw_max, ss_dtype in_dtype);
+// CTA-cooperative generalised scan (ss_scan_general_cta.cu): d_state 32, 64 or
+// 128 with every CTA's channels in one group and 16-byte rows.
+bool scan_general_cta_supported(int64_t dim, int64_t dstate, int64_t cpg, ss_dtype in_dtype);
+cudaError_t launch_scan_general_cta(const GenParams& p, int64_t dstate, ss_dtype in_dtype, ss_dtype out_dtype,
+                                    cudaStream_t stream);
 
 cudaError_t launch_ssd_fwd(const SsdParams& p, int dstate, ss_dtype out_dtype, cudaStream_t stream);
 // d_state 128 on the tcgen05 tensor cores (ss_ssd_tc.cu)

@@ -1,0 +1,385 @@
+// Generalised selective scan forward for sm_103a, CTA-cooperative variant for
+// state sizes 32, 64 and 128 (the recurrence is the one of ss_scan_general.cu:
+// delta = softplus(delta_raw + bias), Abar_n = exp(delta A_n), Bbar_n = delta
+// B_n or, for the zero-order hold, (Abar_n - 1) / A_n B_n; h_n = Abar_n h_n +
+// Bbar_n u; y = (sum_n C_n h_n + D u) silu(z); mlqm.cn tutorial, sections 3.1
+// and 3.2; "外文文献精读：Mamba - 线性时间序列建模与结构化状态空间模型",
+// section 1.2).
+//
+// A CTA owns CC consecutive channels of one batch element, all in one group of
+// B and C, and walks the sequence in tiles of kTile steps. SG = N / 16 lanes
+// share a channel, 16 fp32 states each; a warp covers 32 / SG channels, four
+// compute warps cover CC. A fifth warp only loads: the tile's u, delta_raw and
+// z boxes [kTile, CC] and the group's B and C rows [kTile, N] arrive by TMA
+// into a ring of stages, completion counted on one mbarrier per stage, the
+// stage released through a second one. The compute warps widen the tile's B
+// and C once into fp32 shared memory (each thread a slice), read by all of
+// them.
+//
+// Tokens run in groups of SG: lane j of a channel's SG lanes computes the
+// scalars of token j of the group (delta, delta u, the gate) once for the
+// channel and hands them to the channel's other lanes by shuffle; after the
+// SG state updates a transpose-reduce over the channel's lanes leaves lane j
+// with token j's readout, which it gates and stores. So the per-token work is
+// done once per channel, not once per lane.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ss_device.cuh"
+#include "ss_internal.h"
+
+namespace ssk {
+namespace {
+
+constexpr int kCW = 4;                   // compute warps
+constexpr int kCThreads = 32 * (kCW + 1);  // plus one warp that issues the loads
+constexpr int kTile = 32;                // steps per tile
+
+template <typename TIn, int N>
+struct GCfg {
+  static constexpr int SG = N / 16;        // lanes per channel
+  static constexpr int DC = 32 / SG;       // channels per warp
+  static constexpr int CC = kCW * DC;      // channels per CTA
+  static constexpr int ES = (int)sizeof(TIn);
+  static constexpr int XB = kTile * CC * ES;    // one u, delta_raw or z tile
+  static constexpr int RB = kTile * N * ES;     // one raw B or C tile
+  static constexpr int OFF_U = 0, OFF_DR = XB, OFF_Z = 2 * XB, OFF_B = 3 * XB, OFF_C = 3 * XB + RB;
+  static constexpr int STAGE = 3 * XB + 2 * RB;
+  static constexpr int RING = ES == 2 ? 3 : 2;  // stages
+  static constexpr int OFF_W = RING * STAGE;    // widened B then C, fp32 [kTile][N] each
+  static constexpr int WB = kTile * N * 4;
+  static constexpr int OFF_BAR = OFF_W + 2 * WB;  // full[RING], empty[RING]
+  static constexpr int SMEM = OFF_BAR + 2 * RING * 8;
+  static_assert(kTile % SG == 0, "token groups must tile a tile");
+};
+
+__device__ __forceinline__ void bar_compute() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// barrier over the compute threads that returns the OR of v over them
+__device__ __forceinline__ bool bar_compute_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+template <typename T>
+__device__ __forceinline__ float ld_elem(const uint8_t* base, int i) {
+  return to_f32(reinterpret_cast<const T*>(base)[i]);
+}
+// e^x - 1 for a pair, given e = e^x from the MUFU exponential: below |x| =
+// 1/32 the series x + x^2/2 + x^3/6 + x^4/24 (truncation under x^5/120, a
+// relative 8e-9), above it e - 1 (whose absolute error is then a relative one
+// below 1e-5 of the result)
+__device__ __forceinline__ f2 expm1_pair2(f2 x, f2 e) {
+  f2 p = fma2(x, pk(1.f / 24.f, 1.f / 24.f), pk(1.f / 6.f, 1.f / 6.f));
+  p = fma2(x, p, pk(0.5f, 0.5f));
+  p = fma2(x, p, pk(1.f, 1.f));
+  const f2 ser = mul2(x, p);
+  const f2 em = add2(e, pk(-1.f, -1.f));
+  const float r0 = fabsf(f2lo(x)) < 0.03125f ? f2lo(ser) : f2lo(em);
+  const float r1 = fabsf(f2hi(x)) < 0.03125f ? f2hi(ser) : f2hi(em);
+  return pk(r0, r1);
+}
+
+template <typename TIn, typename TOut, int N, bool ZOH>
+__global__ void __launch_bounds__(kCThreads, 2) scan_general_cta_kernel(const __grid_constant__ GenParams p,
+                                                                    const __grid_constant__ CUtensorMap tm_u,
+                                                                    const __grid_constant__ CUtensorMap tm_dr,
+                                                                    const __grid_constant__ CUtensorMap tm_z,
+                                                                    const __grid_constant__ CUtensorMap tm_b,
+                                                                    const __grid_constant__ CUtensorMap tm_c) {
+  using K = GCfg<TIn, N>;
+  constexpr int SG = K::SG, DC = K::DC, CC = K::CC;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
+  uint64_t* empty = full + K::RING;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t ncb = p.dim / CC;
+  const int64_t b = blockIdx.x / ncb, c0 = (blockIdx.x % ncb) * CC;
+  const int64_t L = p.seqlen, Dm = p.dim;
+  const int grp = (int)(c0 / p.cpg);
+  const int64_t ntile = (L + kTile - 1) / kTile;
+  const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
+  const bool has_z = p.z != nullptr;
+
+  if (tid == 0) {
+    for (int i = 0; i < K::RING; i++) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCW * 32);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCW) {
+    // ============ the load warp: one lane keeps the ring full
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_u);
+      tma_prefetch_desc(&tm_dr);
+      if (has_z) tma_prefetch_desc(&tm_z);
+      tma_prefetch_desc(&tm_b);
+      tma_prefetch_desc(&tm_c);
+      const uint32_t bytes = (uint32_t)((has_z ? 3 : 2) * K::XB + 2 * K::RB);
+      int64_t k = 0;
+      bool ok = true;
+      for (; k < ntile; k++) {
+        const int s = (int)(k % K::RING);
+        // the stage's previous tile is released by every compute thread
+        if (k >= K::RING && !mbar_wait(&empty[s], (uint32_t)(((k / K::RING) - 1) & 1), wait_ns)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * K::STAGE;
+        const int t0 = (int)(k * kTile);
+        mbar_expect_tx(&full[s], bytes);
+        tma_load_3d(st + K::OFF_U, &tm_u, (int)c0, t0, (int)b, &full[s]);
+        tma_load_3d(st + K::OFF_DR, &tm_dr, (int)c0, t0, (int)b, &full[s]);
+        if (has_z) tma_load_3d(st + K::OFF_Z, &tm_z, (int)c0, t0, (int)b, &full[s]);
+        tma_load_4d(st + K::OFF_B, &tm_b, 0, grp, t0, (int)b, &full[s]);
+        tma_load_4d(st + K::OFF_C, &tm_c, 0, grp, t0, (int)b, &full[s]);
+        mbar_arrive(&full[s]);
+      }
+      if (!ok) {
+        // a wait gave up: record it, and wait (bounded) for the loads still in
+        // flight before the CTA's shared memory is released
+        atomicOr(p.fault, kFaultTileWait);
+        for (int64_t q = k > K::RING ? k - K::RING : 0; q < k; q++)
+          mbar_wait(&full[q % K::RING], (uint32_t)((q / K::RING) & 1), wait_ns);
+      }
+    }
+    return;
+  }
+
+  // ============ compute warps: SG lanes per channel, 16 states each. Lane j
+  // owns the quads of states j, j + SG, j + 2 SG, j + 3 SG (quad Q = states 4Q
+  // .. 4Q + 3): a warp's 16-byte reads of a B or C row then cover consecutive
+  // quads, free of bank conflicts. Pair q of the lane is states qst(q), + 1.
+  const int ch = lane / SG, j = lane % SG;
+  auto qst = [&](int q) { return 4 * (j + SG * (q >> 1)) + 2 * (q & 1); };
+  const int chl = warp * DC + ch;  // channel within the CTA
+  const int64_t d = c0 + chl;
+  const bool dv = d < Dm;
+  f2 A2[8], h[8];
+  [[maybe_unused]] f2 invA[8], zm[8];
+#pragma unroll
+  for (int q = 0; q < 8; q++) {
+    const float a0 = dv ? __ldg(p.A + d * N + qst(q)) : 0.f;
+    const float a1 = dv ? __ldg(p.A + d * N + qst(q) + 1) : 0.f;
+    A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
+    const float* h0 = (dv && p.h0) ? p.h0 + (b * Dm + d) * N : nullptr;
+    h[q] = h0 ? pk(__ldg(h0 + qst(q)), __ldg(h0 + qst(q) + 1)) : pk(0.f, 0.f);
+    if constexpr (ZOH) {
+      invA[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+      zm[q] = pk(a0 != 0.f ? 0.f : 1.f, a1 != 0.f ? 0.f : 1.f);  // A = 0: Bbar = delta B
+    }
+  }
+  const float bias = (dv && p.delta_bias) ? __ldg(p.delta_bias + d) : 0.f;
+  const float Dd = (dv && p.D) ? __ldg(p.D + d) : 0.f;
+  float* wB = reinterpret_cast<float*>(smem + K::OFF_W);
+  float* wC = wB + kTile * N;
+
+  bool fail = false;
+  for (int64_t k = 0; k < ntile; k++) {
+    const int s = (int)(k % K::RING);
+    const int64_t t0 = k * kTile;
+    const uint8_t* st = smem + s * K::STAGE;
+    const bool got = mbar_wait(&full[s], (uint32_t)((k / K::RING) & 1), wait_ns);
+    // every compute thread is past the previous tile (the widened rows are
+    // free); a timeout anywhere ends the loop for all of them
+    if (bar_compute_or(!got)) {
+      fail = true;
+      break;
+    }
+    const float* Bt;
+    const float* Ct;
+    if constexpr (K::ES == 2) {  // widen the tile's B and C once, each thread a slice
+      const uint4* rb = reinterpret_cast<const uint4*>(st + K::OFF_B);
+      const uint4* rc = reinterpret_cast<const uint4*>(st + K::OFF_C);
+      for (int i = tid; i < kTile * N / 8; i += kCW * 32) {
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+          const uint4 w = which ? rc[i] : rb[i];
+          float4* o = reinterpret_cast<float4*>((which ? wC : wB) + 8 * i);
+          o[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                             __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+          o[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                             __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+        }
+      }
+      bar_compute();
+      Bt = wB;
+      Ct = wC;
+    } else {
+      Bt = reinterpret_cast<const float*>(st + K::OFF_B);
+      Ct = reinterpret_cast<const float*>(st + K::OFF_C);
+    }
+#pragma unroll 1
+    for (int g = 0; g < kTile; g += SG) {
+      // this lane's token of the group: its scalars, once per channel
+      const int tl = g + j;
+      const int64_t t = t0 + tl;
+      const bool tv = t < L;
+      const float xu = ld_elem<TIn>(st + K::OFF_U, tl * CC + chl);
+      const float dl = tv ? softplus_fast(ld_elem<TIn>(st + K::OFF_DR, tl * CC + chl) + bias) : 0.f;
+      float acc[SG];
+#pragma unroll
+      for (int kk = 0; kk < SG; kk++) {  // token g + kk, its scalars from lane kk of the channel
+        const int src = ch * SG + kk;
+        const float dlk = __shfl_sync(0xffffffffu, dl, src);
+        const float xuk = __shfl_sync(0xffffffffu, xu, src);
+        const f2 dl2 = pk(dlk, dlk);
+        [[maybe_unused]] const f2 du2 = pk(dlk * xuk, dlk * xuk);
+        [[maybe_unused]] const f2 xu2 = pk(xuk, xuk);
+        const float4* Bp = reinterpret_cast<const float4*>(Bt + (g + kk) * N) + j;  // quad j, then + SG per step
+        const float4* Cp = reinterpret_cast<const float4*>(Ct + (g + kk) * N) + j;
+        f2 y0 = pk(0.f, 0.f), y1 = pk(0.f, 0.f);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; q4++) {
+          const float4 bq = Bp[SG * q4], cq = Cp[SG * q4];
+          const f2 bv[2] = {pk(bq.x, bq.y), pk(bq.z, bq.w)};
+          const f2 cv[2] = {pk(cq.x, cq.y), pk(cq.z, cq.w)};
+#pragma unroll
+          for (int e = 0; e < 2; e++) {
+            const int q = 2 * q4 + e;
+            const f2 e2 = mul2(dl2, A2[q]);
+            const f2 a = pk(ex2(f2lo(e2)), ex2(f2hi(e2)));
+            if constexpr (ZOH) {
+              // Bbar u = (Abar - 1) / A * u, or delta u where A = 0
+              const f2 em1 = expm1_pair2(mul2(e2, pk(kLn2, kLn2)), a);
+              const f2 bu = fma2(zm[q], du2, mul2(em1, mul2(invA[q], xu2)));
+              h[q] = fma2(a, h[q], mul2(bu, bv[e]));
+            } else {
+              h[q] = fma2(a, h[q], mul2(du2, bv[e]));
+            }
+            if (e) y1 = fma2(cv[e], h[q], y1);
+            else y0 = fma2(cv[e], h[q], y0);
+          }
+        }
+        const f2 ys = add2(y0, y1);
+        acc[kk] = f2lo(ys) + f2hi(ys);
+      }
+      // sum each token's readout over the channel's SG lanes so that lane j
+      // ends with token j's: at each level the lanes with bit m set keep the
+      // upper half of their values and send the lower half
+#pragma unroll
+      for (int m = SG / 2, w = SG / 2; m >= 1; m >>= 1, w >>= 1) {
+        const bool up = (j & m) != 0;
+#pragma unroll
+        for (int e = 0; e < w; e++) {
+          const float keep = up ? acc[e + w] : acc[e];
+          const float send = up ? acc[e] : acc[e + w];
+          acc[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      float yv = fmaf(Dd, xu, acc[0]);
+      if (has_z) yv *= silu(ld_elem<TIn>(st + K::OFF_Z, tl * CC + chl));
+      st_out(static_cast<TOut*>(p.y) + (b * L + t) * Dm + d, yv, dv && tv);
+    }
+    mbar_arrive(&empty[s]);  // this thread is done with the stage
+  }
+  if (!fail && dv && p.h_last) {
+    float* hl = p.h_last + (b * Dm + d) * N;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      hl[qst(q)] = f2lo(h[q]);
+      hl[qst(q) + 1] = f2hi(h[q]);
+    }
+  }
+  if (fail && tid == 0) atomicOr(p.fault, kFaultTileWait);
+}
+
+using GEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+GEncodeFn genc_fn() {
+  static const GEncodeFn fn = []() -> GEncodeFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<GEncodeFn>(f);
+    return nullptr;
+  }();
+  return fn;
+}
+
+// tiled map over a row-major tensor of `rank` dims (innermost first), no
+// swizzle, zero fill outside it
+bool gmap(CUtensorMap* m, const void* ptr, int es, int rank, const uint64_t* dims, const uint32_t* box) {
+  GEncodeFn fn = genc_fn();
+  if (!fn) return false;
+  cuuint64_t gd[4], gs[3];
+  cuuint32_t bx[4], estr[4] = {1, 1, 1, 1};
+  uint64_t stride = (uint64_t)es;
+  for (int i = 0; i < rank; i++) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    if (i > 0) gs[i - 1] = stride;
+    stride *= dims[i];
+  }
+  return fn(m, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank,
+            const_cast<void*>(ptr), gd, gs, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename TIn, typename TOut, int N>
+cudaError_t launch_gcta(const GenParams& p, cudaStream_t s) {
+  using K = GCfg<TIn, N>;
+  CUtensorMap mu{}, mdr{}, mz{}, mb{}, mc{};
+  const uint64_t L = (uint64_t)p.seqlen, Bt = (uint64_t)p.batch, Dm = (uint64_t)p.dim, G = (uint64_t)p.ngroups;
+  const uint64_t dx[3] = {Dm, L, Bt};
+  const uint32_t bxx[3] = {(uint32_t)K::CC, (uint32_t)kTile, 1};
+  const uint64_t dbc[4] = {(uint64_t)N, G, L, Bt};
+  const uint32_t bbc[4] = {(uint32_t)N, 1, (uint32_t)kTile, 1};
+  if (!gmap(&mu, p.u, K::ES, 3, dx, bxx) || !gmap(&mdr, p.delta_raw, K::ES, 3, dx, bxx) ||
+      (p.z && !gmap(&mz, p.z, K::ES, 3, dx, bxx)) || !gmap(&mb, p.B, K::ES, 4, dbc, bbc) ||
+      !gmap(&mc, p.C, K::ES, 4, dbc, bbc))
+    return cudaErrorInvalidValue;
+  auto k = p.disc == 1 ? scan_general_cta_kernel<TIn, TOut, N, true> : scan_general_cta_kernel<TIn, TOut, N, false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.batch * (p.dim / K::CC);
+  k<<<(unsigned)grid, kCThreads, K::SMEM, s>>>(p, mu, mdr, mz, mb, mc);
+  return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_gcta_n(const GenParams& p, int64_t dstate, cudaStream_t s) {
+  if (dstate == 32) return launch_gcta<TIn, TOut, 32>(p, s);
+  if (dstate == 64) return launch_gcta<TIn, TOut, 64>(p, s);
+  return launch_gcta<TIn, TOut, 128>(p, s);
+}
+
+}  // namespace
+
+bool scan_general_cta_supported(int64_t dim, int64_t dstate, int64_t cpg, ss_dtype in_dtype) {
+  if (dstate != 32 && dstate != 64 && dstate != 128) return false;
+  const int64_t cc = kCW * (32 / (dstate / 16));  // channels per CTA
+  const int64_t es = in_dtype == SS_BF16 ? 2 : 4;
+  return cpg % cc == 0 && (dim * es) % 16 == 0 && genc_fn() != nullptr;
+}
+
+cudaError_t launch_scan_general_cta(const GenParams& p, int64_t dstate, ss_dtype in_dtype, ss_dtype out_dtype,
+                                    cudaStream_t stream) {
+  if (in_dtype == SS_BF16)
+    return out_dtype == SS_BF16 ? launch_gcta_n<__nv_bfloat16, __nv_bfloat16>(p, dstate, stream)
+                                : launch_gcta_n<__nv_bfloat16, float>(p, dstate, stream);
+  return out_dtype == SS_BF16 ? launch_gcta_n<float, __nv_bfloat16>(p, dstate, stream)
+                              : launch_gcta_n<float, float>(p, dstate, stream);
+}
+
+}  // namespace ssk

@@ -40,7 +40,22 @@ SHAPES = [
     ("bf16", 1, 1000, 96, 64, 4, True, True, True, True),
     ("f32", 1, 20, 1000, 16, 1000, True, True, True, True),  # one B/C per channel, ragged last block at channel 992
     ("bf16", 2, 30, 200, 32, 40, True, True, True, True),    # groups of 5 channels, ragged last block
+    # shapes the CTA-cooperative kernel takes (every CTA's channels in one group,
+    # 16-byte rows): 64, 32 or 16 channels per CTA, sequences ending inside a tile
+    ("bf16", 2, 100, 64, 32, 1, True, True, True, True),
+    ("f32", 1, 77, 64, 64, 2, True, True, True, True),
+    ("bf16", 3, 65, 48, 128, 3, False, True, False, True),
+    ("bf16", 1, 300, 128, 64, 1, True, False, True, True),
+    ("f32", 2, 40, 32, 128, 1, True, True, True, False),
 ]
+
+
+def test_cta_shapes_take_the_cta_kernel():
+    # the new shapes above are the ones whose CTAs (4 warps of 32 / (N / 16)
+    # channels) each hold channels of one group
+    for dt, Bt, L, Dm, N, G, *_ in SHAPES[-5:]:
+        cc = 4 * (32 // (N // 16))
+        assert (Dm // G) % cc == 0 and (Dm * (2 if dt == "bf16" else 4)) % 16 == 0
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{s[0]}-b{s[1]}-L{s[2]}-D{s[3]}-N{s[4]}-G{s[5]}" for s in SHAPES])
@@ -82,6 +97,19 @@ def test_general_layer_sampled(N, G, disc):
     y, h = _run(x, disc, BF16)
     assert_close(y[ch[:, 0], :, ch[:, 1]], yr, BF16, out_bf16=True, what=f"layer N={N} G={G} y")
     assert_close(h[ch[:, 0], ch[:, 1]], hr, BF16, what=f"layer N={N} G={G} h_last")
+
+
+def test_general_zoh_with_zero_a():
+    # zero-order hold where some A_n are 0: Bbar = delta B there (the CTA
+    # kernel's shape: 32 channels of one group per CTA)
+    x = gen.random_general_inputs(2, 90, 64, 64, 1, in_dtype="bf16", seed=12, with_h0=True)
+    A = x["A"].clone()
+    A[:, ::5] = 0.0
+    x["A"] = A.contiguous()
+    yr, hr = oracle.scan_general(x, 1, "zoh")
+    y, h = _run(x, "zoh", F32)
+    assert_close(y, yr, BF16, what="general zoh y, some A = 0")
+    assert_close(h, hr, BF16, what="general zoh h_last, some A = 0")
 
 
 def test_general_errors_and_empty():
