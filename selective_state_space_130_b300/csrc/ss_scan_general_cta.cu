@@ -32,8 +32,8 @@
 namespace ssk {
 namespace {
 
-constexpr int kCW = 4;                   // compute warps
-constexpr int kCThreads = 32 * (kCW + 1);  // plus one warp that issues the loads
+constexpr int kCW = 4;                   // warps per CTA
+constexpr int kCThreads = 32 * kCW;
 constexpr int kTile = 32;                // steps per tile
 
 template <typename TIn, int N>
@@ -46,11 +46,11 @@ struct GCfg {
   static constexpr int RB = kTile * N * ES;     // one raw B or C tile
   static constexpr int OFF_U = 0, OFF_DR = XB, OFF_Z = 2 * XB, OFF_B = 3 * XB, OFF_C = 3 * XB + RB;
   static constexpr int STAGE = 3 * XB + 2 * RB;
-  static constexpr int RING = ES == 2 ? 3 : 2;  // stages
+  static constexpr int RING = (ES == 2 && N <= 64) ? 3 : 2;  // stages (three CTAs per SM fit in shared memory)
   static constexpr int OFF_W = RING * STAGE;    // widened B then C, fp32 [kTile][N] each
   static constexpr int WB = kTile * N * 4;
-  static constexpr int OFF_BAR = OFF_W + 2 * WB;  // full[RING], empty[RING]
-  static constexpr int SMEM = OFF_BAR + 2 * RING * 8;
+  static constexpr int OFF_BAR = OFF_W + 2 * WB;  // full[RING]
+  static constexpr int SMEM = OFF_BAR + RING * 8;
   static_assert(kTile % SG == 0, "token groups must tile a tile");
 };
 
@@ -94,7 +94,7 @@ __device__ __forceinline__ f2 expm1_pair2(f2 x, f2 e) {
 }
 
 template <typename TIn, typename TOut, int N, bool ZOH>
-__global__ void __launch_bounds__(kCThreads, 2) scan_general_cta_kernel(const __grid_constant__ GenParams p,
+__global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __grid_constant__ GenParams p,
                                                                     const __grid_constant__ CUtensorMap tm_u,
                                                                     const __grid_constant__ CUtensorMap tm_dr,
                                                                     const __grid_constant__ CUtensorMap tm_z,
@@ -104,7 +104,6 @@ __global__ void __launch_bounds__(kCThreads, 2) scan_general_cta_kernel(const __
   constexpr int SG = K::SG, DC = K::DC, CC = K::CC;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
-  uint64_t* empty = full + K::RING;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t ncb = p.dim / CC;
   const int64_t b = blockIdx.x / ncb, c0 = (blockIdx.x % ncb) * CC;
@@ -114,53 +113,34 @@ __global__ void __launch_bounds__(kCThreads, 2) scan_general_cta_kernel(const __
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
   const bool has_z = p.z != nullptr;
 
+  // Thread 0 issues the loads: tile k goes to stage k % RING once every
+  // thread is past tile k - 1, which last used that stage.
+  const uint32_t tile_bytes = (uint32_t)((has_z ? 3 : 2) * K::XB + 2 * K::RB);
+  uint32_t nissued = 0;  // tiles issued (thread 0; for the drain after a timeout)
+  auto issue = [&](int64_t k) {
+    const int s = (int)(k % K::RING);
+    uint8_t* st = smem + s * K::STAGE;
+    const int t0 = (int)(k * kTile);
+    mbar_expect_tx(&full[s], tile_bytes);
+    tma_load_3d(st + K::OFF_U, &tm_u, (int)c0, t0, (int)b, &full[s]);
+    tma_load_3d(st + K::OFF_DR, &tm_dr, (int)c0, t0, (int)b, &full[s]);
+    if (has_z) tma_load_3d(st + K::OFF_Z, &tm_z, (int)c0, t0, (int)b, &full[s]);
+    tma_load_4d(st + K::OFF_B, &tm_b, 0, grp, t0, (int)b, &full[s]);
+    tma_load_4d(st + K::OFF_C, &tm_c, 0, grp, t0, (int)b, &full[s]);
+    mbar_arrive(&full[s]);
+    nissued++;
+  };
   if (tid == 0) {
-    for (int i = 0; i < K::RING; i++) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kCW * 32);
-    }
+    for (int i = 0; i < K::RING; i++) mbar_init(&full[i], 1);
     fence_mbar_init();
+    tma_prefetch_desc(&tm_u);
+    tma_prefetch_desc(&tm_dr);
+    if (has_z) tma_prefetch_desc(&tm_z);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_c);
+    for (int64_t k = 0; k < K::RING - 1 && k < ntile; k++) issue(k);
   }
   __syncthreads();
-
-  if (warp == kCW) {
-    // ============ the load warp: one lane keeps the ring full
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_u);
-      tma_prefetch_desc(&tm_dr);
-      if (has_z) tma_prefetch_desc(&tm_z);
-      tma_prefetch_desc(&tm_b);
-      tma_prefetch_desc(&tm_c);
-      const uint32_t bytes = (uint32_t)((has_z ? 3 : 2) * K::XB + 2 * K::RB);
-      int64_t k = 0;
-      bool ok = true;
-      for (; k < ntile; k++) {
-        const int s = (int)(k % K::RING);
-        // the stage's previous tile is released by every compute thread
-        if (k >= K::RING && !mbar_wait(&empty[s], (uint32_t)(((k / K::RING) - 1) & 1), wait_ns)) {
-          ok = false;
-          break;
-        }
-        uint8_t* st = smem + s * K::STAGE;
-        const int t0 = (int)(k * kTile);
-        mbar_expect_tx(&full[s], bytes);
-        tma_load_3d(st + K::OFF_U, &tm_u, (int)c0, t0, (int)b, &full[s]);
-        tma_load_3d(st + K::OFF_DR, &tm_dr, (int)c0, t0, (int)b, &full[s]);
-        if (has_z) tma_load_3d(st + K::OFF_Z, &tm_z, (int)c0, t0, (int)b, &full[s]);
-        tma_load_4d(st + K::OFF_B, &tm_b, 0, grp, t0, (int)b, &full[s]);
-        tma_load_4d(st + K::OFF_C, &tm_c, 0, grp, t0, (int)b, &full[s]);
-        mbar_arrive(&full[s]);
-      }
-      if (!ok) {
-        // a wait gave up: record it, and wait (bounded) for the loads still in
-        // flight before the CTA's shared memory is released
-        atomicOr(p.fault, kFaultTileWait);
-        for (int64_t q = k > K::RING ? k - K::RING : 0; q < k; q++)
-          mbar_wait(&full[q % K::RING], (uint32_t)((q / K::RING) & 1), wait_ns);
-      }
-    }
-    return;
-  }
 
   // ============ compute warps: SG lanes per channel, 16 states each. Lane j
   // owns the quads of states j, j + SG, j + 2 SG, j + 3 SG (quad Q = states 4Q
@@ -202,6 +182,7 @@ __global__ void __launch_bounds__(kCThreads, 2) scan_general_cta_kernel(const __
       fail = true;
       break;
     }
+    if (tid == 0 && k + K::RING - 1 < ntile) issue(k + K::RING - 1);  // into the stage tile k - 1 used
     const float* Bt;
     const float* Ct;
     if constexpr (K::ES == 2) {  // widen the tile's B and C once, each thread a slice
@@ -287,7 +268,6 @@ __global__ void __launch_bounds__(kCThreads, 2) scan_general_cta_kernel(const __
       if (has_z) yv *= silu(ld_elem<TIn>(st + K::OFF_Z, tl * CC + chl));
       st_out(static_cast<TOut*>(p.y) + (b * L + t) * Dm + d, yv, dv && tv);
     }
-    mbar_arrive(&empty[s]);  // this thread is done with the stage
   }
   if (!fail && dv && p.h_last) {
     float* hl = p.h_last + (b * Dm + d) * N;
@@ -297,7 +277,13 @@ __global__ void __launch_bounds__(kCThreads, 2) scan_general_cta_kernel(const __
       hl[qst(q) + 1] = f2hi(h[q]);
     }
   }
-  if (fail && tid == 0) atomicOr(p.fault, kFaultTileWait);
+  if (fail && tid == 0) {
+    // a wait gave up: record it, and wait (bounded) for the loads still in
+    // flight (the last RING - 1 issued) before the CTA's shared memory is released
+    atomicOr(p.fault, kFaultTileWait);
+    for (uint32_t q = nissued > K::RING - 1 ? nissued - (K::RING - 1) : 0; q < nissued; q++)
+      mbar_wait(&full[q % K::RING], (q / K::RING) & 1u, wait_ns);
+  }
 }
 
 using GEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
