@@ -78,20 +78,14 @@ template <typename T>
 __device__ __forceinline__ float ld_elem(const uint8_t* base, int i) {
   return to_f32(reinterpret_cast<const T*>(base)[i]);
 }
-// e^x - 1 for a pair, given e = e^x from the MUFU exponential: below |x| =
-// 1/32 the series x + x^2/2 + x^3/6 + x^4/24 (truncation under x^5/120, a
-// relative 8e-9), above it e - 1 (whose absolute error is then a relative one
-// below 1e-5 of the result)
-__device__ __forceinline__ f2 expm1_pair2(f2 x, f2 e) {
-  f2 p = fma2(x, pk(1.f / 24.f, 1.f / 24.f), pk(1.f / 6.f, 1.f / 6.f));
-  p = fma2(x, p, pk(0.5f, 0.5f));
-  p = fma2(x, p, pk(1.f, 1.f));
-  const f2 ser = mul2(x, p);
-  const f2 em = add2(e, pk(-1.f, -1.f));
-  const float r0 = fabsf(f2lo(x)) < 0.03125f ? f2lo(ser) : f2lo(em);
-  const float r1 = fabsf(f2hi(x)) < 0.03125f ? f2hi(ser) : f2hi(em);
-  return pk(r0, r1);
-}
+// Coefficients of phi(x) = (e^x - 1) / x = 1 + x/2 + x^2/6 + x^3/24 + ... in
+// powers of e2 = x log2(e): phi = 1 + kPhi1 e2 + kPhi2 e2^2 + kPhi3 e2^3 (kPhi1 =
+// ln2 / 2, kPhi2 = ln2^2 / 6, kPhi3 = ln2^3 / 24), and the series' range |x| <
+// 1/32 in units of e2.
+constexpr float kPhi1 = 0.34657359027997264f;
+constexpr float kPhi2 = 0.08007550231970023f;
+constexpr float kPhi3 = 0.013876027166205394f;
+constexpr float kZohSeries = 0.045084220027780106f;  // (1/32) log2(e)
 
 template <typename TIn, typename TOut, int N, bool ZOH>
 __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __grid_constant__ GenParams p,
@@ -152,7 +146,7 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
   const int64_t d = c0 + chl;
   const bool dv = d < Dm;
   f2 A2[8], h[8];
-  [[maybe_unused]] f2 invA[8], zm[8];
+  [[maybe_unused]] f2 invA[8];
 #pragma unroll
   for (int q = 0; q < 8; q++) {
     const float a0 = dv ? __ldg(p.A + d * N + qst(q)) : 0.f;
@@ -160,10 +154,7 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
     A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
     const float* h0 = (dv && p.h0) ? p.h0 + (b * Dm + d) * N : nullptr;
     h[q] = h0 ? pk(__ldg(h0 + qst(q)), __ldg(h0 + qst(q) + 1)) : pk(0.f, 0.f);
-    if constexpr (ZOH) {
-      invA[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
-      zm[q] = pk(a0 != 0.f ? 0.f : 1.f, a1 != 0.f ? 0.f : 1.f);  // A = 0: Bbar = delta B
-    }
+    if constexpr (ZOH) invA[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
   }
   const float bias = (dv && p.delta_bias) ? __ldg(p.delta_bias + d) : 0.f;
   const float Dd = (dv && p.D) ? __ldg(p.D + d) : 0.f;
@@ -237,9 +228,19 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
             const f2 e2 = mul2(dl2, A2[q]);
             const f2 a = pk(ex2(f2lo(e2)), ex2(f2hi(e2)));
             if constexpr (ZOH) {
-              // Bbar u = (Abar - 1) / A * u, or delta u where A = 0
-              const f2 em1 = expm1_pair2(mul2(e2, pk(kLn2, kLn2)), a);
-              const f2 bu = fma2(zm[q], du2, mul2(em1, mul2(invA[q], xu2)));
+              // Bbar u = (Abar - 1) / A * u = delta u phi(x), x = delta A, phi(x)
+              // = (e^x - 1) / x. Below |x| = 1/32, delta u times phi's series
+              // 1 + x/2 + x^2/6 + x^3/24 (truncation under x^4/120, a relative
+              // 1e-8), written in e2 = x log2 e; above it (Abar - 1) u / A,
+              // whose Abar from the MUFU exponential then has a relative error
+              // below 1e-5 of Abar - 1. A = 0 gives x = 0: delta u.
+              f2 ph = fma2(e2, pk(kPhi3, kPhi3), pk(kPhi2, kPhi2));
+              ph = fma2(e2, ph, pk(kPhi1, kPhi1));
+              ph = fma2(e2, ph, pk(1.f, 1.f));
+              const f2 bs = mul2(du2, ph);
+              const f2 be = mul2(add2(a, pk(-1.f, -1.f)), mul2(invA[q], xu2));
+              const f2 bu = pk(fabsf(f2lo(e2)) < kZohSeries ? f2lo(bs) : f2lo(be),
+                               fabsf(f2hi(e2)) < kZohSeries ? f2hi(bs) : f2hi(be));
               h[q] = fma2(a, h[q], mul2(bu, bv[e]));
             } else {
               h[q] = fma2(a, h[q], mul2(du2, bv[e]));
