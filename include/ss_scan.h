@@ -280,14 +280,14 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
  *  h0, h_last   : [batch, nheads, headdim, dstate] float32 or NULL
  *  y            : [batch, seqlen, nheads, headdim] out_dtype
  * headdim must be 64 and dstate 64 or 128 (SS_ERR_UNSUPPORTED otherwise);
- * nheads must be a multiple of ngroups. Computed in chunks (128 steps for
- * dstate 128, on tcgen05 tensor cores; 64 for dstate 64) with bf16 products
- * accumulated in float32; the operands computed on chip (the masked C.B^T,
- * the weighted x or B, the carried state) enter the products as two bf16
- * parts (about 16 significant bits).
+ * nheads must be a multiple of ngroups. Computed in chunks of 128 steps on the
+ * tcgen05 tensor cores, products accumulated in float32 in tensor memory
+ * (dstate 64 runs as 128 with B and C zero-padded); the operands computed on
+ * chip (the masked C.B^T, the weighted x, the carried state) enter the
+ * products as two bf16 parts (about 16 significant bits).
  *
  * workspace (optional, device, 16-byte aligned, caller-owned, at least
- * ss_ssd_fwd_workspace_size bytes when given): with it, a dstate 128 call may
+ * ss_ssd_fwd_workspace_size bytes when given): with it, a call may
  * split each (batch, head) sequence into pieces run by different CTAs that
  * hand the state on through the workspace (so that batch * nheads sequences
  * fill every SM); its first few KB are reset by the call (on `stream`) and it

@@ -313,7 +313,7 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
 }  // namespace
 
 namespace ssk {
-// Pieces per (batch, head) sequence for the d_state 128 kernel. Each CTA runs
+// Pieces per (batch, head) sequence for the tcgen05 kernel. Each CTA runs
 // one piece; CTAs run one per SM, so with `units` sequences the layer takes
 // about ceil(units * pieces / sms) rounds of a piece each. A CTA costs its
 // chunks plus a fixed 1.6 chunks (start-up, pipeline fill, taking over and
@@ -323,7 +323,7 @@ namespace ssk {
 int64_t plan_ssd_pieces(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate, int sms,
                         int64_t force_steps) {
   const int64_t nchunk = (seqlen + 127) / 128, units = batch * nheads;
-  if (dstate != 128 || nchunk <= 1 || units <= 0) return 1;
+  if ((dstate != 64 && dstate != 128) || nchunk <= 1 || units <= 0) return 1;
   if (force_steps > 0) {
     const int64_t pc = std::max<int64_t>(1, (force_steps + 127) / 128);
     return (nchunk + pc - 1) / pc;
@@ -346,7 +346,7 @@ int64_t plan_ssd_pieces(int64_t batch, int64_t seqlen, int64_t nheads, int64_t d
 // (padded to 256 bytes), then one fp32 state per sequence.
 size_t ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate) {
   const int64_t nchunk = (seqlen + 127) / 128, units = batch * nheads;
-  if (dstate != 128 || nchunk <= 1 || units <= 0) return 0;
+  if ((dstate != 64 && dstate != 128) || nchunk <= 1 || units <= 0) return 0;
   return 256 + (size_t)((units * 4 + 255) / 256 * 256) + (size_t)units * 64 * 128 * sizeof(float);
 }
 }  // namespace ssk
@@ -695,7 +695,7 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
   }
   if ((double)batch * nheads > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
   ssk::SsdParams p{x, dt, A, B, C, D, dt_bias, h0, y, h_last, batch, seqlen, nheads, ngroups,
-                   ssk::device_fault_word(), g_wait_ns};
+                   ssk::device_fault_word(), g_wait_ns, dstate};
   p.pieces = 1;
   p.piece_chunks = (seqlen + 127) / 128;
   p.ws_ticket = nullptr;
@@ -719,7 +719,7 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
         return cuda_fail(e, "state-space-dual workspace reset");
     }
   }
-  e = ssk::launch_ssd_fwd(p, (int)dstate, out_dtype, s);
+  e = ssk::launch_ssd_fwd_tc(p, out_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "state-space-dual launch");
   return SS_OK;
 }

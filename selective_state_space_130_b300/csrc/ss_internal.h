@@ -151,7 +151,8 @@ struct SsdParams {
   int64_t batch, seqlen, nheads, ngroups;
   unsigned int* fault;      // the library's fault word (timed-out waits)
   uint64_t wait_ns;         // limit of a device-side wait; 0 = the default
-  // Sequence split (d_state 128): each (batch, head) sequence runs as `pieces`
+  int64_t dstate;           // 64 or 128 (64: B and C run zero-padded to 128 columns)
+  // Sequence split: each (batch, head) sequence runs as `pieces`
   // pieces of `piece_chunks` 128-step chunks, taken by CTAs in the order of a
   // ticket counter; piece q > 0 starts from the state piece q - 1 left in
   // ws_state[(batch, head)], published through ws_flags[(batch, head)] = q.
@@ -159,7 +160,7 @@ struct SsdParams {
   int64_t pieces, piece_chunks;
   unsigned int* ws_ticket;  // zeroed before the launch
   unsigned int* ws_flags;   // [batch * nheads], zeroed before the launch
-  float* ws_state;          // [batch * nheads, 64, dstate]
+  float* ws_state;          // [batch * nheads, 64, 128]
   int64_t withhold_piece;   // test knob: this ticket does not publish its state (-1: none)
 };
 // SSD split plan: pieces per (batch, head) sequence for `sms` SMs, and the
@@ -223,8 +224,7 @@ bool scan_general_cta_supported(int64_t dim, int64_t dstate, int64_t cpg, ss_dty
 cudaError_t launch_scan_general_cta(const GenParams& p, int64_t dstate, ss_dtype in_dtype, ss_dtype out_dtype,
                                     cudaStream_t stream);
 
-cudaError_t launch_ssd_fwd(const SsdParams& p, int dstate, ss_dtype out_dtype, cudaStream_t stream);
-// d_state 128 on the tcgen05 tensor cores (ss_ssd_tc.cu)
+// the state-space-dual layer on the tcgen05 tensor cores (ss_ssd_tc.cu)
 cudaError_t launch_ssd_fwd_tc(const SsdParams& p, ss_dtype out_dtype, cudaStream_t stream);
 
 // The library's own fault word (device symbol), used when no workspace is given.

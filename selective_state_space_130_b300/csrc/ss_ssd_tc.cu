@@ -534,9 +534,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     }
     {
       uint32_t hv[32];
-      const float* h0 = piece > 0 ? p.ws_state + bh * kP * kN : (p.h0 ? p.h0 + bh * kP * kN : nullptr);
+      // (h0 is [64, dstate]; the hand-over slot [64, 128]; state rows past
+      // dstate are zero and stay zero, B's padded columns being zero)
+      const int64_t sstride = piece > 0 ? kN : p.dstate;
+      const float* h0 = piece > 0 ? p.ws_state + bh * kP * kN : (p.h0 ? p.h0 + bh * kP * p.dstate : nullptr);
+      const bool rin = h0 && !aborted && row < sstride;
 #pragma unroll
-      for (int q = 0; q < 32; q++) hv[q] = __float_as_uint(h0 && !aborted ? h0[(32 * hf + q) * kN + row] : 0.f);
+      for (int q = 0; q < 32; q++) hv[q] = __float_as_uint(rin ? h0[(32 * hf + q) * sstride + row] : 0.f);
       tmem_st32(tstate, hv);
       if (has_h0) {
         write_state(hv);
@@ -731,14 +735,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     }
     // the state leaving the piece: h_last after the last piece, else the
     // hand-over slot, published for the next piece
-    float* hout = last_piece ? p.h_last : p.ws_state;
-    if (!aborted && hout) {  // (aborted is the same for every compute thread)
+    const int64_t ostride = last_piece ? p.dstate : kN;  // h_last [64, dstate]; the slot [64, 128]
+    float* hout = last_piece ? (p.h_last ? p.h_last + bh * kP * p.dstate : nullptr) : p.ws_state + bh * kP * kN;
+    if (!aborted && hout && row < ostride) {  // (the same for every thread of a warp)
       uint32_t hv[32];
       tmem_ld32_async(tstate, hv);
       tmem_wait_ld(hv);
-      float* hl = hout + bh * kP * kN;
 #pragma unroll
-      for (int q = 0; q < 32; q++) hl[(32 * hf + q) * kN + row] = __uint_as_float(hv[q]);
+      for (int q = 0; q < 32; q++) hout[(32 * hf + q) * ostride + row] = __uint_as_float(hv[q]);
     }
     if (!last_piece) {
       bar_sync_compute();  // every thread's part of the state is written
@@ -794,8 +798,11 @@ cudaError_t launch_tc(const SsdParams& p, cudaStream_t s) {
   CUtensorMap mx{}, mb{}, mc{}, my{};
   // x, y [batch, L, H, 64]; B, C [batch, L, G, 128]
   const uint64_t L = (uint64_t)p.seqlen, Bt = (uint64_t)p.batch, H = (uint64_t)p.nheads, G = (uint64_t)p.ngroups;
-  if (!make_map_4d(&mx, p.x, 2, kP, H, L, Bt) || !make_map_4d(&mb, p.B, 2, kN, G, L, Bt) ||
-      !make_map_4d(&mc, p.C, 2, kN, G, L, Bt) || !make_map_4d(&my, p.y, (int)sizeof(TOut), kP, H, L, Bt))
+  // B and C [.., dstate]: with dstate 64 the box at column 64 lies wholly
+  // outside the tensor and is zero-filled, padding both to 128 columns
+  const uint64_t N = (uint64_t)p.dstate;
+  if (!make_map_4d(&mx, p.x, 2, kP, H, L, Bt) || !make_map_4d(&mb, p.B, 2, N, G, L, Bt) ||
+      !make_map_4d(&mc, p.C, 2, N, G, L, Bt) || !make_map_4d(&my, p.y, (int)sizeof(TOut), kP, H, L, Bt))
     return cudaErrorInvalidValue;
   auto k = ssd_tc_kernel<TOut>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::ALLOC);

@@ -207,11 +207,12 @@ def test_ssd_rejects_bad_arguments(kw, code, msg):
 
 def test_ssd_workspace_size_and_checks():
     # one ticket counter (256 bytes), one flag per (batch, head) padded to 256
-    # bytes, one 64 x 128 fp32 state per (batch, head); nothing for d_state 64
-    # or a single chunk, which never split
+    # bytes, one 64 x 128 fp32 state per (batch, head) (d_state 64 runs padded
+    # to 128); nothing for a single chunk, which never splits
     assert ss.ss_ssd_fwd_workspace_size(4, 2048, 80, 128) == 256 + 1280 + 320 * 64 * 128 * 4
     assert ss.ss_ssd_fwd_workspace_size(1, 300, 3, 128) == 256 + 256 + 3 * 64 * 128 * 4
-    assert ss.ss_ssd_fwd_workspace_size(4, 2048, 80, 64) == 0
+    assert ss.ss_ssd_fwd_workspace_size(4, 2048, 80, 64) == ss.ss_ssd_fwd_workspace_size(4, 2048, 80, 128)
+    assert ss.ss_ssd_fwd_workspace_size(4, 2048, 80, 32) == 0
     assert ss.ss_ssd_fwd_workspace_size(2, 128, 8, 128) == 0
     assert ss.ss_ssd_fwd_workspace_size(-1, 128, 8, 128) == 0
     need = ss.ss_ssd_fwd_workspace_size(1, 300, 4, 128)

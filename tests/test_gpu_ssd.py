@@ -192,3 +192,19 @@ def test_ssd_withheld_hand_over_times_out():
     yr, hr = oracle.ssd(x, 1)
     assert_close(y, yr, BF16, what="ssd y after a timed-out hand-over")
     assert_close(h, hr, BF16, what="ssd h_last after a timed-out hand-over")
+
+
+def test_ssd_split_sequences_dstate64():
+    # d_state 64 runs with B and C zero-padded to 128 columns; split into
+    # pieces, with an initial state
+    x = gen.random_ssd_inputs(2, 900, 3, 64, 64, 3, in_dtype="bf16", seed=64, with_h0=True)
+    yr, hr = oracle.ssd(x, 3)
+    ss.ss_scan_set_tuning(0, 256, 0)
+    try:
+        y, h = _run(x, F32)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+    ss.ss_scan_status(None)
+    assert_close(y, yr, BF16, what="split ssd y, d_state 64")
+    assert_close(h, hr, BF16, what="split ssd h_last, d_state 64")
+    assert_close(y, yr, F32, what="split ssd y, d_state 64 (float32 bound)")
