@@ -138,7 +138,9 @@ ss_status ss_state_update(int64_t batch, int64_t dim, int64_t dstate,
  *   y[b,t,d]   = silu(pre) when silu != 0, else pre
  *   state_out[b,d,k] = e[seqlen-(K-1)+k], k < K-1   (the last K-1 inputs)
  *
- *  x, y      : [batch, seqlen, dim] in_dtype / out_dtype
+ *  x, y      : [batch, seqlen, dim] in_dtype / out_dtype; y must not overlap
+ *              x (a tile's first K-1 rows are read from x after the tile
+ *              before it may have been written), else SS_ERR_INVALID_ARG
  *  weight    : [dim, width] float32; bias: [dim] float32 or NULL
  *  state_in  : [batch, dim, width-1] in_dtype or NULL; state_out: same shape,
  *              in_dtype, or NULL; the two must be different buffers

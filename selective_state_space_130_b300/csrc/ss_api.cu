@@ -430,6 +430,18 @@ ss_status ss_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t widt
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
   if (state_in && state_in == state_out)
     return fail(SS_ERR_INVALID_ARG, "state_out must not be the buffer state_in (use a second buffer)");
+  if (seqlen > 0) {
+    // byte spans, saturated; [x0, x0 + nx) and [y0, y0 + ny) overlap when the
+    // later start lies inside the earlier span
+    uint64_t n = 0, nx = UINT64_MAX, ny = UINT64_MAX;
+    if (!__builtin_mul_overflow((uint64_t)batch, (uint64_t)seqlen, &n) &&
+        !__builtin_mul_overflow(n, (uint64_t)dim, &n)) {
+      if (__builtin_mul_overflow(n, (uint64_t)dsize(in_dtype), &nx)) nx = UINT64_MAX;
+      if (__builtin_mul_overflow(n, (uint64_t)dsize(out_dtype), &ny)) ny = UINT64_MAX;
+    }
+    const uint64_t x0 = (uint64_t)(uintptr_t)x, y0 = (uint64_t)(uintptr_t)y;
+    if (x0 >= y0 ? x0 - y0 < ny : y0 - x0 < nx) return fail(SS_ERR_INVALID_ARG, "y must not overlap x");
+  }
   ss_status st = check_device();
   if (st != SS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -13,17 +13,19 @@
 // Both kernels are HBM-bound streams: the forward reads x once and writes y
 // once (plus a halo of K-1 rows per tile, served by L2).
 //  - Rows of 16-byte-aligned width stream through shared memory: persistent
-//    CTAs take tiles of [64 timesteps + halo, 256 bytes of channels] in turn; a
-//    producer warp keeps a four-stage ring of TMA (cp.async.bulk.tensor) loads
-//    in flight, so the HBM requests never pause while a tile is computed, and
-//    four compute warps run the taps, bias and SiLU on channel pairs as packed
-//    f32x2 arithmetic.
+//    CTAs (three per SM) take ranges of tiles of [64 timesteps + halo, 256 bytes
+//    of channels]; a producer warp keeps a four-stage ring of TMA
+//    (cp.async.bulk.tensor) loads in flight, so the HBM requests never pause
+//    while a tile is computed, and four compute warps run the taps, bias and
+//    SiLU on channel pairs as packed f32x2 arithmetic. y of x's type goes back
+//    into the stage and leaves by one bulk-tensor store per tile.
 //  - Other rows: a thread owns one channel over kConvTT timesteps and issues
 //    every load of its window before any arithmetic.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "ss_device.cuh"
 #include "ss_internal.h"
@@ -347,6 +349,7 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_update_kernel(const __gri
 constexpr int kTT = 64;         // timesteps per tile
 constexpr int kRing = 4;        // ring stages
 constexpr int kCompute = 4;     // compute warps (plus one producer warp)
+constexpr int kConvBar = 1;     // named barrier of the compute warps (0 is __syncthreads)
 
 template <typename TIn, int K>
 struct ConvTile {
@@ -361,11 +364,52 @@ struct ConvTile {
   static constexpr int SMEM = OFF_BAR + 2 * kRing * 8 + 128;
 };
 
+// bulk-tensor store of a box of shared memory to global memory; the copy
+// drops the box's elements that fall outside the tensor
+__device__ __forceinline__ void conv_tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void conv_bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed store but the newest has finished reading shared memory
+__device__ __forceinline__ void conv_bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void conv_bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void conv_bar_compute() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kConvBar), "n"(32 * kCompute) : "memory");
+}
+// barrier of the compute warps that also ORs a flag over them
+__device__ __forceinline__ bool conv_bar_or_compute(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kConvBar), "n"(32 * kCompute)
+      : "memory");
+  return r != 0;
+}
+
+// Units of work are (channel block, batch element, tile), the tile varying
+// fastest. CTA i takes the contiguous range [i n / G, (i + 1) n / G) of the n
+// units, so its taps change only where the range crosses a channel block.
+//
+// When x and y have one type (kStage), y goes back into the stage it was
+// computed from: stage row r + H holds timestep t0 + r of both. A thread
+// overwrites a row only after its own last read of it, and the first H rows of
+// a thread's range, which the range before it also writes, are read before the
+// tile's first barrier. One bulk-tensor store per tile then writes the 64 rows;
+// rows past the sequence end and channels past dim are dropped by the copy. The
+// stage returns to the producer once that store has read it. Mixed types store
+// y from registers.
 template <typename TIn, typename TOut, int K, bool SILU>
-__global__ void __launch_bounds__(32 * (kCompute + 1), 2) conv1d_fwd_tma_kernel(const __grid_constant__ ConvParams p,
-                                                                            const __grid_constant__ CUtensorMap tm_x) {
+__global__ void __launch_bounds__(32 * (kCompute + 1), 3) conv1d_fwd_tma_kernel(const __grid_constant__ ConvParams p,
+                                                                            const __grid_constant__ CUtensorMap tm_x,
+                                                                            const __grid_constant__ CUtensorMap tm_y) {
   using CT = ConvTile<TIn, K>;
   constexpr int H = CT::H, CB = CT::CB, NPAIR = CT::NPAIR, RPT = CT::RPT;
+  constexpr bool kStage = std::is_same<TIn, TOut>::value;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
   uint8_t* smem = smem_raw + pad;
@@ -375,7 +419,7 @@ __global__ void __launch_bounds__(32 * (kCompute + 1), 2) conv1d_fwd_tma_kernel(
   if (tid == 0) {
     for (int i = 0; i < kRing; i++) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kCompute);
+      mbar_init(&empty[i], kStage ? 1 : kCompute);
     }
     fence_mbar_init();
   }
@@ -384,21 +428,23 @@ __global__ void __launch_bounds__(32 * (kCompute + 1), 2) conv1d_fwd_tma_kernel(
   const int64_t ntile = (L + kTT - 1) / kTT, ncb = (Dm + CB - 1) / CB;
   const int64_t nunits = p.batch * ntile * ncb;
   const int64_t G = gridDim.x;
-  // unit u: channel block u % ncb, tile (u / ncb) % ntile, batch element u / (ncb * ntile)
+  const int64_t u_begin = (int64_t)blockIdx.x * nunits / G, u_end = ((int64_t)blockIdx.x + 1) * nunits / G;
+  // unit u: tile u % ntile, batch element (u / ntile) % batch, channel block u / (ntile * batch)
 
   if (warp == kCompute) {
     // ---- producer: one thread keeps the ring full
     if (lane == 0) {
       tma_prefetch_desc(&tm_x);
+      if (kStage) tma_prefetch_desc(&tm_y);
       int64_t k = 0;
-      for (int64_t u = blockIdx.x; u < nunits; u += G, k++) {
+      for (int64_t u = u_begin; u < u_end; u++, k++) {
         const int s = (int)(k % kRing);
         if (k >= kRing && !mbar_wait(&empty[s], (uint32_t)(((k / kRing) - 1) & 1))) {
           atomicOr(p.fault, kFaultTileWait);
           break;
         }
-        const int64_t cbk = u % ncb, rest = u / ncb;
-        const int64_t j = rest % ntile, b = rest / ntile;
+        const int64_t j = u % ntile, rest = u / ntile;
+        const int64_t b = rest % p.batch, cbk = rest / p.batch;
         fence_proxy_async_smem();
         mbar_expect_tx(&full[s], CT::STAGE);
         tma_load_3d(smem + s * CT::STAGE, &tm_x, (int)(cbk * CB), (int)(j * kTT - H), (int)b, &full[s]);
@@ -411,23 +457,50 @@ __global__ void __launch_bounds__(32 * (kCompute + 1), 2) conv1d_fwd_tma_kernel(
   // ---- compute warps: thread = (channel pair q, row range rr)
   const int q = tid % NPAIR, rr = tid / NPAIR;
   const int r0 = rr * RPT;  // first output row of the range in the tile
+  const TIn* gs = static_cast<const TIn*>(p.state_in);
+  f2 w2[K], bias2 = pk(0.f, 0.f);  // taps and bias of the pair: w2[k] = (w[d][k], w[d+1][k])
+  int64_t wcb = -1;                // channel block the taps belong to
   int64_t k = 0;
-  for (int64_t u = blockIdx.x; u < nunits; u += G, k++) {
+  for (int64_t u = u_begin; u < u_end; u++, k++) {
     const int s = (int)(k % kRing);
-    const bool ok = mbar_wait(&full[s], (uint32_t)((k / kRing) & 1));
-    if (__any_sync(0xffffffffu, !ok)) {  // warp-uniform
-      if (lane == 0) atomicOr(p.fault, kFaultTileWait);
-      break;
-    }
-    const int64_t cbk = u % ncb, rest = u / ncb;
-    const int64_t j = rest % ntile, b = rest / ntile;
+    const int64_t j = u % ntile, rest = u / ntile;
+    const int64_t b = rest % p.batch, cbk = rest / p.batch;
     const int64_t t0 = j * kTT, d = cbk * CB + 2 * q;  // first timestep of the tile, first channel of the pair
     const bool dv = d < Dm;                           // Dm is even here: the pair is whole or absent
+    if (cbk != wcb) {  // CTA-uniform; the loads overlap the wait below
+      wcb = cbk;
+      if (dv) {
+        float wf[2 * K];
+#pragma unroll
+        for (int i = 0; i < K; i++) {  // 2K contiguous floats, 8-byte aligned (d even)
+          const float2 v = __ldg(reinterpret_cast<const float2*>(p.w + d * K) + i);
+          wf[2 * i] = v.x;
+          wf[2 * i + 1] = v.y;
+        }
+#pragma unroll
+        for (int i = 0; i < K; i++) w2[i] = pk(wf[i], wf[K + i]);
+        bias2 = pk(0.f, 0.f);
+        if (p.bias) {
+          const float2 bv = __ldg(reinterpret_cast<const float2*>(p.bias + d));
+          bias2 = pk(bv.x, bv.y);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < K; i++) w2[i] = pk(0.f, 0.f);
+        bias2 = pk(0.f, 0.f);
+      }
+    }
+    const bool ok = mbar_wait(&full[s], (uint32_t)((k / kRing) & 1));
+    if constexpr (!kStage) {
+      if (__any_sync(0xffffffffu, !ok)) {  // warp-uniform
+        if (lane == 0) atomicOr(p.fault, kFaultTileWait);
+        break;
+      }
+    }
     TIn* tile = reinterpret_cast<TIn*>(smem + s * CT::STAGE);  // row i = timestep t0 - H + i
-    const TIn* gs = static_cast<const TIn*>(p.state_in);
     // rows before t = 0 (zero-filled by the load) come from the carried state;
     // only the thread range that reads them patches its own pair's columns
-    const bool patch = j == 0 && gs && rr == 0 && dv;
+    const bool patch = ok && j == 0 && gs && rr == 0 && dv;
     if (patch) {
 #pragma unroll
       for (int i = 0; i < H; i++) {
@@ -435,26 +508,19 @@ __global__ void __launch_bounds__(32 * (kCompute + 1), 2) conv1d_fwd_tma_kernel(
         tile[i * CB + 2 * q + 1] = gs[(b * Dm + d + 1) * H + i];
       }
     }
-    // taps and bias of the pair: w2[k] = (w[d][k], w[d+1][k])
-    f2 w2[K], bias2 = pk(0.f, 0.f);
-    if (dv) {
-      float wf[2 * K];
+    // the tile holding the last timestep hands on the last H inputs (raw bits),
+    // read before any y overwrites them
+    const bool hand_on = ok && p.state_out && j == ntile - 1 && rr == 0 && dv;
+    auto hand_on_state = [&]() {
+      TIn* so = static_cast<TIn*>(p.state_out);
 #pragma unroll
-      for (int i = 0; i < K; i++) {  // 2K contiguous floats, 8-byte aligned (d even)
-        const float2 v = __ldg(reinterpret_cast<const float2*>(p.w + d * K) + i);
-        wf[2 * i] = v.x;
-        wf[2 * i + 1] = v.y;
+      for (int i = 0; i < H; i++) {
+        const int64_t row = (L - H + i) - (t0 - H);  // tile row of timestep L-H+i (>= 0: t0 <= L-1)
+        so[(b * Dm + d) * H + i] = tile[row * CB + 2 * q];
+        so[(b * Dm + d + 1) * H + i] = tile[row * CB + 2 * q + 1];
       }
-#pragma unroll
-      for (int i = 0; i < K; i++) w2[i] = pk(wf[i], wf[K + i]);
-      if (p.bias) {
-        const float2 bv = __ldg(reinterpret_cast<const float2*>(p.bias + d));
-        bias2 = pk(bv.x, bv.y);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < K; i++) w2[i] = pk(0.f, 0.f);
-    }
+    };
+    if (kStage && hand_on) hand_on_state();
     auto ld_pair = [&](int row) -> f2 {  // widened (channel d, channel d+1) of tile row `row`
       if constexpr (sizeof(TIn) == 4) {
         const float2 v = *reinterpret_cast<const float2*>(tile + row * CB + 2 * q);
@@ -468,42 +534,69 @@ __global__ void __launch_bounds__(32 * (kCompute + 1), 2) conv1d_fwd_tma_kernel(
     f2 win[K];
 #pragma unroll
     for (int i = 0; i < H; i++) win[i] = ld_pair(r0 + i);
-    TOut* yrow = static_cast<TOut*>(p.y) + (b * L + t0 + r0) * Dm + d;
-#pragma unroll 8
-    for (int r = 0; r < RPT; r++) {
-      win[H] = ld_pair(r0 + r + H);
-      f2 a = bias2;
+    if constexpr (kStage) {
+      if (conv_bar_or_compute(!ok)) {  // CTA-uniform
+        if (tid == 0) atomicOr(p.fault, kFaultTileWait);
+        break;
+      }
 #pragma unroll
-      for (int i = 0; i < K; i++) a = fma2(w2[i], win[i], a);
-      if (SILU) a = silu2(a);
-      if (dv && t0 + r0 + r < L) {
-        if constexpr (sizeof(TOut) == 2) {
+      for (int r = 0; r < RPT; r++) {
+        win[H] = ld_pair(r0 + r + H);
+        f2 a = bias2;
+#pragma unroll
+        for (int i = 0; i < K; i++) a = fma2(w2[i], win[i], a);
+        if (SILU) a = silu2(a);
+        TIn* dst = tile + (r0 + r + H) * CB + 2 * q;
+        if constexpr (sizeof(TIn) == 2) {
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(f2lo(a), f2hi(a));
-          __stcs(reinterpret_cast<unsigned int*>(yrow), *reinterpret_cast<const unsigned int*>(&h2));
+          *reinterpret_cast<__nv_bfloat162*>(dst) = h2;
         } else {
-          __stcs(reinterpret_cast<float2*>(yrow), make_float2(f2lo(a), f2hi(a)));
+          *reinterpret_cast<float2*>(dst) = make_float2(f2lo(a), f2hi(a));
         }
-      }
-      yrow += Dm;
 #pragma unroll
-      for (int i = 0; i < H; i++) win[i] = win[i + 1];
-    }
-    // the tile holding the last timestep hands on the last H inputs (raw bits)
-    if (p.state_out && j == ntile - 1 && rr == 0 && dv) {
-      TIn* so = static_cast<TIn*>(p.state_out);
-#pragma unroll
-      for (int i = 0; i < H; i++) {
-        const int64_t row = (L - H + i) - (t0 - H);  // tile row of timestep L-H+i (>= 0: t0 <= L-1)
-        so[(b * Dm + d) * H + i] = tile[row * CB + 2 * q];
-        so[(b * Dm + d + 1) * H + i] = tile[row * CB + 2 * q + 1];
+        for (int i = 0; i < H; i++) win[i] = win[i + 1];
       }
+      // order this thread's y writes before the bulk store's reads
+      fence_proxy_async_smem();
+      conv_bar_compute();
+      if (tid == 0) {
+        conv_tma_store_3d(&tm_y, smem + s * CT::STAGE + H * 256, (int)(cbk * CB), (int)t0, (int)b);
+        conv_bulk_commit();
+        // the previous tile's store has read its stage: hand that stage back
+        conv_bulk_wait_read1();
+        if (k > 0) mbar_arrive(&empty[(int)((k - 1) % kRing)]);
+      }
+    } else {
+      TOut* yrow = static_cast<TOut*>(p.y) + (b * L + t0 + r0) * Dm + d;
+#pragma unroll 8
+      for (int r = 0; r < RPT; r++) {
+        win[H] = ld_pair(r0 + r + H);
+        f2 a = bias2;
+#pragma unroll
+        for (int i = 0; i < K; i++) a = fma2(w2[i], win[i], a);
+        if (SILU) a = silu2(a);
+        if (dv && t0 + r0 + r < L) {
+          if constexpr (sizeof(TOut) == 2) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(f2lo(a), f2hi(a));
+            __stcs(reinterpret_cast<unsigned int*>(yrow), *reinterpret_cast<const unsigned int*>(&h2));
+          } else {
+            __stcs(reinterpret_cast<float2*>(yrow), make_float2(f2lo(a), f2hi(a)));
+          }
+        }
+        yrow += Dm;
+#pragma unroll
+        for (int i = 0; i < H; i++) win[i] = win[i + 1];
+      }
+      if (hand_on) hand_on_state();
+      // the stage may be refilled by the next load: order this thread's
+      // shared-memory writes before that async-proxy write
+      if (patch) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // the stage may be refilled by the next load: order this thread's
-    // shared-memory writes before that async-proxy write
-    if (patch) fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
   }
+  // shared memory must outlive the reads of the stores in flight
+  if (kStage && tid == 0) conv_bulk_wait_all();
 }
 
 using ConvEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -526,27 +619,36 @@ inline ConvEncodeFn conv_encode_fn() {
 template <typename TIn, typename TOut, int K>
 cudaError_t launch_fwd_tma(const ConvParams& p, cudaStream_t s) {
   using CT = ConvTile<TIn, K>;
+  constexpr bool kStage = std::is_same<TIn, TOut>::value;
   ConvEncodeFn fn = conv_encode_fn();
   if (!fn) return cudaErrorInvalidValue;
-  CUtensorMap m{};
+  CUtensorMap mx{}, my{};
   const size_t es = sizeof(TIn);
   cuuint64_t dims[3] = {(cuuint64_t)p.dim, (cuuint64_t)p.seqlen, (cuuint64_t)p.batch};
   cuuint64_t strides[2] = {(cuuint64_t)p.dim * es, (cuuint64_t)p.seqlen * p.dim * es};
   cuuint32_t box[3] = {(cuuint32_t)CT::CB, (cuuint32_t)CT::ROWS, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  if (fn(&m, dt, 3, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  if (fn(&mx, dt, 3, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
       CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  if (kStage) {  // y: the same shape and type as x, stored 64 rows at a time
+    cuuint32_t ybox[3] = {(cuuint32_t)CT::CB, (cuuint32_t)kTT, 1};
+    if (fn(&my, dt, 3, p.y, dims, strides, ybox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else {
+    my = mx;  // unused
+  }
   const int64_t ntile = (p.seqlen + kTT - 1) / kTT, ncb = (p.dim + CT::CB - 1) / CT::CB;
   const int64_t nunits = p.batch * ntile * ncb;
   const int sms = device_sm_count();
-  const int64_t grid = std::min<int64_t>(nunits, 2 * (int64_t)sms);
+  const int64_t grid = std::min<int64_t>(nunits, 3 * (int64_t)sms);  // three CTAs per SM
   auto kern = p.silu ? conv1d_fwd_tma_kernel<TIn, TOut, K, true> : conv1d_fwd_tma_kernel<TIn, TOut, K, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CT::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, 32 * (kCompute + 1), CT::SMEM, s>>>(p, m);
+  kern<<<(unsigned)grid, 32 * (kCompute + 1), CT::SMEM, s>>>(p, mx, my);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import selective_state_space_130_b300 as ss
 from selective_state_space_130_b300 import _lib
@@ -220,6 +221,40 @@ def test_ssd_workspace_size_and_checks():
     assert "workspace" in ss.ss_last_error()
     assert _ssd(seqlen=300, workspace=0x10008, workspace_bytes=need) == _lib.SS_ERR_INVALID_ARG
     assert "workspace" in ss.ss_last_error()
+
+
+def _conv(**kw):
+    a = dict(batch=2, seqlen=16, dim=64, width=4, in_dtype=1, out_dtype=1)
+    a.update({k: v for k, v in kw.items() if k in a})
+    p = [kw.get(k, v) for k, v in (("x", 0x10000), ("weight", 0x1000), ("bias", None), ("state_in", None))]
+    q = [kw.get(k, v) for k, v in (("y", 0x40000), ("state_out", None))]
+    return ss.lib().ss_conv1d_fwd(a["batch"], a["seqlen"], a["dim"], a["width"], a["in_dtype"], a["out_dtype"],
+                                  *p, 1, *q, None)
+
+
+# x spans 2 * 16 * 64 * 2 = 4096 bytes from 0x10000 in bf16
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(width=5), _lib.SS_ERR_UNSUPPORTED, "width"),
+    (dict(weight=None), _lib.SS_ERR_INVALID_ARG, "weight"),
+    (dict(y=0x10008), _lib.SS_ERR_INVALID_ARG, "aligned"),
+    (dict(y=0x10000), _lib.SS_ERR_INVALID_ARG, "overlap"),
+    (dict(y=0x10ff0), _lib.SS_ERR_INVALID_ARG, "overlap"),
+    (dict(y=0x10000 - 4096 + 16), _lib.SS_ERR_INVALID_ARG, "overlap"),
+    (dict(y=0x10000 - 2 * 4096 + 16, out_dtype=0), _lib.SS_ERR_INVALID_ARG, "overlap"),
+    (dict(state_in=0x8000, state_out=0x8000), _lib.SS_ERR_INVALID_ARG, "state_out"),
+])
+def test_conv1d_rejects_bad_arguments(kw, code, msg):
+    assert _conv(**kw) == code
+    assert msg in ss.ss_last_error()
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="the call would launch on made-up addresses")
+def test_conv1d_adjacent_buffers_pass_the_overlap_check():
+    # y ending where x starts, or starting where x ends, is no overlap: the
+    # call gets past the argument checks to the device check, which fails here
+    for y in (0x10000 - 4096, 0x10000 + 4096):
+        _conv(y=y)
+        assert "overlap" not in ss.ss_last_error()
 
 
 def test_new_entry_points_empty_problems_without_device():

@@ -92,6 +92,22 @@ def test_conv1d_full_layer_shape():
     assert np.array_equal(so.double().cpu().numpy(), sr)
 
 
+@pytest.mark.parametrize("dt,width", [("bf16", 4), ("f32", 3)])
+def test_conv1d_ranges_cross_blocks(dt, width):
+    # 3 x 4000 x 1288: 63 tiles of 64 steps (the last 32 rows), 11 or 21
+    # channel blocks (the last partial), so each CTA's range of about five
+    # units crosses batch elements and channel blocks; carried state in and
+    # out, y in x's type (staged in shared memory, one bulk store per tile)
+    # and in the other type (stored from registers)
+    in_dt = BF16 if dt == "bf16" else F32
+    x = gen.random_conv_inputs(3, 4000, 1288, width, dt, seed=11, with_state=True)
+    yr, sr = oracle.conv1d(x)
+    for out in (in_dt, F32 if in_dt == BF16 else BF16):
+        y, so = _run(x, out)
+        assert_close(y.double().cpu().numpy(), yr, in_dt, out_bf16=(out == BF16), what=f"conv y out={out}")
+        assert np.array_equal(so.double().cpu().numpy(), sr)
+
+
 def test_conv1d_empty_and_errors():
     x = gen.random_conv_inputs(2, 3, 16, 4, "bf16", seed=1, with_state=True)
     d = _dev(x)
