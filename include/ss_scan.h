@@ -289,14 +289,15 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
  * products as two bf16 parts (about 16 significant bits).
  *
  * workspace (optional, device, 16-byte aligned, caller-owned, at least
- * ss_ssd_fwd_workspace_size bytes when given): with it, a call may
- * split each (batch, head) sequence into pieces run by different CTAs that
- * hand the state on through the workspace (so that batch * nheads sequences
- * fill every SM); its first few KB are reset by the call (on `stream`) and it
- * must not be shared by calls that can run at the same time. NULL runs one CTA
- * per sequence. A workspace smaller than needed is SS_ERR_INVALID_ARG. A
+ * ss_ssd_fwd_workspace_size bytes when given): with it and more (batch, head)
+ * sequences than SMs, a call runs one CTA per SM, each taking an equal
+ * contiguous share of all the sequences' chunks; where a share starts inside a
+ * sequence, the state is handed on through the workspace from the CTA with
+ * the share before. Its first few KB are reset by the call (on `stream`) and
+ * it must not be shared by calls that can run at the same time. NULL runs one
+ * CTA per sequence. A workspace smaller than needed is SS_ERR_INVALID_ARG. A
  * hand-over that does not arrive within the wait limit (see
- * ss_scan_set_wait_limit) ends the waiting pieces and is reported by
+ * ss_scan_set_wait_limit) ends the waiting CTAs and is reported by
  * ss_scan_status(NULL, stream) as SS_ERR_TIMEOUT; the outputs are then
  * undefined.
  */
@@ -321,9 +322,10 @@ size_t ss_ssd_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, 
  * cross-CTA carry path. max_workers > 0 caps the number of CTAs a split of the
  * work uses (default: one per SM), which makes range boundaries and hand-overs
  * more frequent. Results do not depend on these settings beyond fp32 rounding;
- * ss_scan_fwd_workspace_size() follows them. For ss_ssd_fwd (dstate 128, with
- * a workspace) chunk_len > 0 sets the length of the pieces a sequence is split
- * into (rounded up to 128 steps) instead of the automatic plan.
+ * ss_scan_fwd_workspace_size() follows them. For ss_ssd_fwd (with a
+ * workspace) chunk_len > 0 sets the length of the CTAs' shares of the chunks
+ * (rounded up to 128 steps) instead of the automatic plan, so that shares
+ * start inside sequences even on small problems.
  */
 void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_workers);
 
@@ -338,8 +340,8 @@ void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_work
  * need it give up after wait_ns, set the fault word and return, so the call
  * finishes and ss_scan_status() reports SS_ERR_TIMEOUT; its outputs are then
  * undefined. No wait in the library is unbounded. They apply to ss_ssd_fwd
- * too: there withhold_item is the piece (in the order CTAs take them: piece q
- * of sequence u is item q * batch * nheads + u) whose state is never handed on.
+ * too: there withhold_item is the share of chunks (the shares in sequence
+ * order, numbered from 0) whose state is never handed on.
  */
 void ss_scan_set_wait_limit(uint64_t wait_ns, int64_t withhold_item);
 

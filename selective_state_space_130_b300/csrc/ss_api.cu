@@ -313,34 +313,23 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
 }  // namespace
 
 namespace ssk {
-// Pieces per (batch, head) sequence for the tcgen05 kernel. Each CTA runs
-// one piece; CTAs run one per SM, so with `units` sequences the layer takes
-// about ceil(units * pieces / sms) rounds of a piece each. A CTA costs its
-// chunks plus a fixed 1.6 chunks (start-up, pipeline fill, taking over and
-// handing on the state: fitted to B300 timings of the Mamba-2 2.7B layer
-// split into 1 to 16 pieces); the plan with the smallest estimate wins (fewer
-// pieces on a tie).
-int64_t plan_ssd_pieces(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate, int sms,
+// CTAs (contiguous ranges of the sequences' chunks) for the tcgen05 kernel
+// with a workspace. A CTA fills an SM (its shared and tensor memory), so CTAs
+// run one per SM. With at most one sequence per SM, one CTA per sequence is
+// best: a split cannot shorten a sequence, whose state runs through its chunks
+// in order. With more sequences than SMs, one CTA per SM takes an equal share
+// of all the chunks, so that no SM idles while others run a last partial round
+// of sequences. force_steps > 0 sets the range length instead (rounded up to
+// whole 128-step chunks), which makes hand-overs on small problems.
+int64_t plan_ssd_ranges(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate, int sms,
                         int64_t force_steps) {
   const int64_t nchunk = (seqlen + 127) / 128, units = batch * nheads;
-  if ((dstate != 64 && dstate != 128) || nchunk <= 1 || units <= 0) return 1;
+  if ((dstate != 64 && dstate != 128) || nchunk <= 1 || units <= 0) return units;
   if (force_steps > 0) {
-    const int64_t pc = std::max<int64_t>(1, (force_steps + 127) / 128);
-    return (nchunk + pc - 1) / pc;
+    const int64_t rc = std::max<int64_t>(1, (force_steps + 127) / 128);
+    return (units * nchunk + rc - 1) / rc;
   }
-  int64_t best = 1;
-  double best_cost = 0;
-  for (int64_t P = 1; P <= nchunk; P++) {
-    const int64_t pc = (nchunk + P - 1) / P, pe = (nchunk + pc - 1) / pc;
-    if (pe != P) continue;
-    const double rounds = (double)((units * pe + sms - 1) / sms);
-    const double cost = rounds * ((double)pc + 1.6);
-    if (P == 1 || cost < best_cost - 1e-9) {
-      best = pe;
-      best_cost = cost;
-    }
-  }
-  return best;
+  return units <= sms ? units : (int64_t)sms;
 }
 // The split's workspace: a ticket counter (256 bytes), one flag per sequence
 // (padded to 256 bytes), then one fp32 state per sequence.
@@ -708,22 +697,19 @@ ss_status ss_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
   if ((double)batch * nheads > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
   ssk::SsdParams p{x, dt, A, B, C, D, dt_bias, h0, y, h_last, batch, seqlen, nheads, ngroups,
                    ssk::device_fault_word(), g_wait_ns, dstate};
-  p.pieces = 1;
-  p.piece_chunks = (seqlen + 127) / 128;
+  p.ranges = batch * nheads;  // one CTA per sequence
   p.ws_ticket = nullptr;
   p.ws_flags = nullptr;
   p.ws_state = nullptr;
-  p.withhold_piece = g_withhold;
+  p.withhold_range = g_withhold;
   cudaError_t e = cudaSuccess;
   if (workspace && need > 0) {
-    const int64_t P = ssk::plan_ssd_pieces(batch, seqlen, nheads, dstate, ssk::device_sm_count(), g_tune_chunk);
-    if (P > 1) {
-      if ((double)batch * (double)nheads * (double)P > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
-      const int64_t nchunk = (seqlen + 127) / 128;
+    const int64_t R = ssk::plan_ssd_ranges(batch, seqlen, nheads, dstate, ssk::device_sm_count(), g_tune_chunk);
+    if (R != p.ranges) {  // ranges that cut sequences: hand-overs through the workspace
+      if ((double)R > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
       uint8_t* w = static_cast<uint8_t*>(workspace);
       const size_t flags_bytes = (size_t)((batch * nheads * 4 + 255) / 256 * 256);
-      p.pieces = P;
-      p.piece_chunks = (nchunk + P - 1) / P;
+      p.ranges = R;
       p.ws_ticket = reinterpret_cast<unsigned int*>(w);
       p.ws_flags = reinterpret_cast<unsigned int*>(w + 256);
       p.ws_state = reinterpret_cast<float*>(w + 256 + flags_bytes);

@@ -152,20 +152,22 @@ struct SsdParams {
   unsigned int* fault;      // the library's fault word (timed-out waits)
   uint64_t wait_ns;         // limit of a device-side wait; 0 = the default
   int64_t dstate;           // 64 or 128 (64: B and C run zero-padded to 128 columns)
-  // Sequence split: each (batch, head) sequence runs as `pieces`
-  // pieces of `piece_chunks` 128-step chunks, taken by CTAs in the order of a
-  // ticket counter; piece q > 0 starts from the state piece q - 1 left in
-  // ws_state[(batch, head)], published through ws_flags[(batch, head)] = q.
-  // pieces == 1: one CTA per (batch, head), no workspace.
-  int64_t pieces, piece_chunks;
-  unsigned int* ws_ticket;  // zeroed before the launch
+  // Work split: the chunks of all (batch, head) sequences, sequence-major,
+  // cut into `ranges` contiguous ranges, one per CTA. With a workspace the
+  // CTAs take ranges in the order of a ticket counter, and a range that starts
+  // inside a sequence starts from the state the range before it left in
+  // ws_state[(batch, head)], published through ws_flags[(batch, head)] = the
+  // chunk where the hand-over happens. Without one (ws_ticket null) there is
+  // one range per sequence, taken by block index.
+  int64_t ranges;
+  unsigned int* ws_ticket;  // zeroed before the launch, or null
   unsigned int* ws_flags;   // [batch * nheads], zeroed before the launch
   float* ws_state;          // [batch * nheads, 64, 128]
-  int64_t withhold_piece;   // test knob: this ticket does not publish its state (-1: none)
+  int64_t withhold_range;   // test knob: this ticket does not publish its state (-1: none)
 };
-// SSD split plan: pieces per (batch, head) sequence for `sms` SMs, and the
-// workspace bytes the split needs (0 when it cannot help).
-int64_t plan_ssd_pieces(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate, int sms, int64_t force_steps);
+// SSD split plan: CTAs (ranges of the sequences' chunks) for `sms` SMs, and
+// the workspace bytes a split needs (0 when it cannot help).
+int64_t plan_ssd_ranges(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate, int sms, int64_t force_steps);
 size_t ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate);
 
 // Launch plan for a scan problem.

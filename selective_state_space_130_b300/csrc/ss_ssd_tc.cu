@@ -92,9 +92,18 @@ struct TcSmem {
   static constexpr int QS = WSUM + 64;        // q_s of two chunks [2][128] f32 (see the kernel)
   static constexpr int DTB = QS + 1024;       // dt words of two chunks [2][128] u32 (see the kernel)
   static constexpr int BAR = DTB + 1024;      // mbarriers, see the kernel (at most 16)
-  static constexpr int TSLOT = BAR + 128;     // tensor-memory base address, then the piece's ticket
+  static constexpr int TSLOT = BAR + 128;     // tensor-memory base address, the CTA's ticket, then its range (RangeDesc)
   static constexpr int BYTES = TSLOT + 64;
   static constexpr int ALLOC = BYTES + 1024;  // + alignment slack
+};
+
+// A CTA's range of chunks as the segments it runs, in shared memory: read at
+// each segment's start, not held in registers through the chunk loops.
+struct RangeDesc {
+  int64_t u0;    // the range's first sequence
+  int nseg;      // sequences it touches
+  int cb_first;  // its first chunk in sequence u0
+  int ce_last;   // one past its last chunk in sequence u0 + nseg - 1
 };
 
 __device__ __forceinline__ int sw128(int r, int c) {  // byte offset of bf16 (r, c) in a tile
@@ -264,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   // loaded, x of an even / odd chunk loaded, S done, the two halves of Y1
   // done, Y2 done, B^T X' done. Completed by the 256 compute threads: X'
   // written, M's column blocks 0 and 2 written, M's blocks 1 and 3 written (S
-  // read), the state written (B^T X' read), Y1 and Y2 read. By one compute
-  // thread: the y staging tiles are free again.
+  // read), the state entering the next chunk written (B^T X' read), Y1 and Y2
+  // read. By one compute thread: the y staging tiles are free again.
   enum {
     kBarCB = 0, kBarX0, kBarX1, kBarS, kBarY1a, kBarY1b, kBarY2, kBarH,
     kRdyX, kRdyM0, kRdyM1, kRdyH, kRdyY, kStg, kNumBars
@@ -279,12 +288,30 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
   uint32_t* tk_slot = tslot + 1;
 
+  // The chunks of all sequences in (batch, head)-major order are cut into
+  // p.ranges contiguous ranges, one per CTA. A range covers the tail of one
+  // sequence, whole sequences and the head of another; it runs the head first
+  // (its state goes to the CTA with the next range), then the whole ones, then
+  // the tail, whose entering state the CTA with the previous range published
+  // when it ran its own head first. A range inside one sequence is a single
+  // segment that waits for its predecessor.
+  volatile RangeDesc* rd = reinterpret_cast<volatile RangeDesc*>(tslot + 2);
   if (tid == 0) {
     for (int i = 0; i < kNumBars; i++) mbar_init(&bar[i], (i < kRdyX || i == kStg) ? 1 : kCompute);
     fence_mbar_init();
-    // the piece this CTA runs: tickets in launch order, so a piece's
-    // predecessor always belongs to a CTA that started earlier
-    *tk_slot = p.pieces > 1 ? atomicAdd(p.ws_ticket, 1u) : blockIdx.x;
+    // the range this CTA runs: tickets in launch order, so the CTA that hands
+    // a state on to this one has always started earlier
+    const int64_t ticket = p.ws_ticket ? atomicAdd(p.ws_ticket, 1u) : blockIdx.x;
+    *tk_slot = (uint32_t)ticket;
+    const int64_t T = p.batch * H * nchunk;
+    // ranges of T / ranges chunks, the first T % ranges one longer
+    const int64_t q = T / p.ranges, r = T % p.ranges;
+    const int64_t g0 = ticket * q + (ticket < r ? ticket : r), g1 = g0 + q + (ticket < r ? 1 : 0);
+    const int64_t u0 = g0 / nchunk, u1 = (g1 - 1) / nchunk;
+    rd->u0 = u0;
+    rd->nseg = g1 > g0 ? (int)(u1 - u0 + 1) : 0;
+    rd->cb_first = (int)(g0 - u0 * nchunk);
+    rd->ce_last = (int)(g1 - u1 * nchunk);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
@@ -297,12 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const int64_t ticket = *tk_slot;
-  const int64_t units = p.batch * H;
-  const int64_t bh = ticket % units, piece = ticket / units;
-  const int64_t b = bh / H, h = bh % H;
-  const int64_t c_begin = piece * p.piece_chunks;
-  const int64_t c_end = c_begin + p.piece_chunks < nchunk ? c_begin + p.piece_chunks : nchunk;
-  const bool last_piece = piece == p.pieces - 1;
+  struct Seg {
+    int64_t u;   // sequence (batch * nheads + head)
+    int cb, ce;  // its chunks [cb, ce)
+  };
+  auto nsegs = [&]() -> int { return rd->nseg; };
+  auto segment = [&](int s) -> Seg {  // the s-th segment the CTA runs
+    const int n = rd->nseg;
+    const int64_t u0 = rd->u0;
+    if (n == 1) return {u0, rd->cb_first, rd->ce_last};
+    if (s == 0) return {u0 + n - 1, 0, rd->ce_last};
+    if (s == n - 1) return {u0, rd->cb_first, (int)nchunk};
+    return {u0 + s, 0, (int)nchunk};
+  };
   uint32_t ph = 0;    // bit i: the phase of barrier i this thread waits for next
   bool fail = false;  // this thread gave up on a wait
   // wait for the next phase of barrier i; after a timeout the phase stays
@@ -315,12 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     fail = true;
     return false;
   };
-  const bool has_h0 = piece > 0 || p.h0 != nullptr;  // a state enters the piece
 
   if (warp >= kComputeWarps) {
     // ============ the issuing warps: lane 0 of each issues. Issuer 0: the
     // tile loads, S and H_l; issuer 1: Y2, then Y1 over M's blocks 0 and 1;
-    // issuer 2: Y1 over M's blocks 2 and 3.
+    // issuer 2: Y1 over M's blocks 2 and 3. Buffers and barriers of a chunk
+    // follow the parity of its place k in the CTA's run.
     const int role = warp - kComputeWarps;
     if (lane == 0) {
       uint32_t nissue[kRdyX] = {};  // copies or commits issued per barrier (for the drain after a timeout)
@@ -339,89 +373,103 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           mma_ta(tmem + d, ta, bd + (uint32_t)(k * 128), idesc(kQ, kP, 0, 1), !first || i > 0);
         }
       };
+      int k = 0;  // chunks this CTA has begun
       if (role == 0) {
-        const int grp = (int)(h / (H / G));
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_b);
         tma_prefetch_desc(&tm_c);
-        auto issue_cb = [&](int64_t c) {
-          const int t0 = (int)(c * kQ);
-          mbar_expect_tx(&bar[kBarCB], 4 * SM::TILE);
-          tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, (int)b, &bar[kBarCB]);
-          tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, (int)b, &bar[kBarCB]);
-          tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, (int)b, &bar[kBarCB]);
-          tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, (int)b, &bar[kBarCB]);
-          mbar_arrive(&bar[kBarCB]);
-          nissue[kBarCB]++;
-        };
-        auto issue_x = [&](int64_t c) {  // into the buffer of the chunk's parity
-          const int xb = kBarX0 + (int)(c & 1);
-          mbar_expect_tx(&bar[xb], SM::TILE);
-          tma_load_4d(sm + ((c & 1) ? SM::X1 : SM::X0), &tm_x, 0, (int)h, (int)(c * kQ), (int)b, &bar[xb]);
-          mbar_arrive(&bar[xb]);
-          if (c & 1)
-            nissue[kBarX1]++;
-          else
-            nissue[kBarX0]++;
-        };
-        issue_cb(c_begin);
-        issue_x(c_begin);
-        for (int64_t c = c_begin; c < c_end; c++) {
-          // S = C B^T (S's columns were read by the previous chunk's Y1)
-          if (!wait(kBarCB)) break;
-          tc_fence_after();
-          mma_k128(tmem + kColS, s0 + SM::C0, true, s0 + SM::B0, true, 16, 16, idesc(kQ, kQ, 0, 0));
-          commit(kBarS);
-          // x of the next chunk, into the buffer of the chunk before this one
-          // (its Y1 is done, its X' written)
-          if (c + 1 < c_end) issue_x(c + 1);
-          // H_l^T = B^T X' (A = B read MN-major: its two n halves are one tile
-          // apart; B: X''s high part and remainder side by side, N = 128)
-          if (!wait(kRdyX)) break;
-          tc_fence_after();
-          mma_k128(tmem + kColH, s0 + SM::B0, false, s0 + SM::XH, false, SM::TILE, SM::TILE, idesc(kN, 2 * kP, 1, 1));
-          commit(kBarH);
-          if (c + 1 < c_end) {
+        for (int sg = 0; sg < nsegs() && !fail; sg++) {
+          const Seg sq = segment(sg);
+          const int b = (int)(sq.u / H), h = (int)(sq.u % H);
+          const int grp = (int)(h / (H / G));
+          const bool has_h0 = sq.cb > 0 || p.h0 != nullptr;  // a state enters the segment
+          auto issue_cb = [&](int64_t c) {
+            const int t0 = (int)(c * kQ);
+            mbar_expect_tx(&bar[kBarCB], 4 * SM::TILE);
+            tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, (int)b, &bar[kBarCB]);
+            tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, (int)b, &bar[kBarCB]);
+            tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, (int)b, &bar[kBarCB]);
+            tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, (int)b, &bar[kBarCB]);
+            mbar_arrive(&bar[kBarCB]);
+            nissue[kBarCB]++;
+          };
+          auto issue_x = [&](int64_t c, int kc) {  // chunk c, k-th of the run: buffer kc & 1
+            const int xb = kBarX0 + (int)(kc & 1);
+            mbar_expect_tx(&bar[xb], SM::TILE);
+            tma_load_4d(sm + ((kc & 1) ? SM::X1 : SM::X0), &tm_x, 0, (int)h, (int)(c * kQ), (int)b, &bar[xb]);
+            mbar_arrive(&bar[xb]);
+            nissue[xb]++;
+          };
+          // (the previous segment's last products have released C, B, S and
+          // its x buffer: waited for below)
+          issue_cb(sq.cb);
+          issue_x(sq.cb, k);
+          for (int c = sq.cb; c < sq.ce; c++, k++) {
+            // S = C B^T (S's columns were read by the previous chunk's Y1)
+            if (!wait(kBarCB)) break;
+            tc_fence_after();
+            mma_k128(tmem + kColS, s0 + SM::C0, true, s0 + SM::B0, true, 16, 16, idesc(kQ, kQ, 0, 0));
+            commit(kBarS);
+            // x of the next chunk, into the buffer of the chunk before this one
+            // (its Y1 is done, its X' written)
+            if (c + 1 < sq.ce) issue_x(c + 1, k + 1);
+            // H_l^T = B^T X' (A = B read MN-major: its two n halves are one tile
+            // apart; B: X''s high part and remainder side by side, N = 128)
+            if (!wait(kRdyX)) break;
+            tc_fence_after();
+            mma_k128(tmem + kColH, s0 + SM::B0, false, s0 + SM::XH, false, SM::TILE, SM::TILE, idesc(kN, 2 * kP, 1, 1));
+            commit(kBarH);
             // C and B are free once S, H_l (in issue order) and Y2 are done;
-            // S's columns and this x once both halves of Y1 are
-            if (!wait(kBarH) || ((c > c_begin || has_h0) && !wait(kBarY2))) break;
-            issue_cb(c + 1);
-            if (!wait(kBarY1a) || !wait(kBarY1b)) break;
+            // S's columns and this x once both halves of Y1 are. After the
+            // segment's last chunk the same waits let the next segment start.
+            // The next copy may complete the C/B barrier's next phase only
+            // once issuer 1 has seen this one: Y2 and Y1a come after its wait.
+            const bool y2 = c > sq.cb || has_h0;
+            if (!wait(kBarH) || (y2 && !wait(kBarY2)) || (!y2 && !wait(kBarY1a))) break;
+            if (c + 1 < sq.ce) issue_cb(c + 1);
+            if ((y2 && !wait(kBarY1a)) || !wait(kBarY1b)) break;
           }
         }
       } else if (role == 1) {
-        for (int64_t c = c_begin; c < c_end; c++) {
-          const uint32_t xs = s0 + ((c & 1) ? SM::X1 : SM::X0);
-          if (!wait(kBarCB)) break;                    // C of the chunk
-          if (c > c_begin && !wait(kRdyY)) break;      // the previous y has read Y1a and Y2
-          // Y2 = C H_in^T: A K-major (C), B MN-major (H^T), the high part and
-          // then the remainder into one accumulator
-          if (c > c_begin || has_h0) {
-            if (!wait(kRdyH)) break;  // the state entering the chunk is written
+        for (int sg = 0; sg < nsegs() && !fail; sg++) {
+          const Seg sq = segment(sg);
+          const bool has_h0 = sq.cb > 0 || p.h0 != nullptr;
+          for (int c = sq.cb; c < sq.ce; c++, k++) {
+            const uint32_t xs = s0 + ((k & 1) ? SM::X1 : SM::X0);
+            if (!wait(kBarCB)) break;            // C of the chunk
+            if (k > 0 && !wait(kRdyY)) break;    // the previous chunk's y has read Y1a and Y2
+            // Y2 = C H_in^T: A K-major (C), B MN-major (H^T), the high part and
+            // then the remainder into one accumulator
+            if (c > sq.cb || has_h0) {
+              if (!wait(kRdyH)) break;  // the state entering the chunk is written
+              tc_fence_after();
+              mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HH, false, 16, 16, idesc(kQ, kP, 0, 1));
+              mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HL, false, 16, 16, idesc(kQ, kP, 0, 1), true);
+              commit(kBarY2);
+            }
+            if (!wait(kRdyM0)) break;
             tc_fence_after();
-            mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HH, false, 16, 16, idesc(kQ, kP, 0, 1));
-            mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HL, false, 16, 16, idesc(kQ, kP, 0, 1), true);
-            commit(kBarY2);
+            y1_block(kColY1a, xs, 0, true);
+            if (!wait(kRdyM1)) break;
+            tc_fence_after();
+            y1_block(kColY1a, xs, 1, false);
+            commit(kBarY1a);
           }
-          if (!wait(kRdyM0)) break;
-          tc_fence_after();
-          y1_block(kColY1a, xs, 0, true);
-          if (!wait(kRdyM1)) break;
-          tc_fence_after();
-          y1_block(kColY1a, xs, 1, false);
-          commit(kBarY1a);
         }
       } else {
-        for (int64_t c = c_begin; c < c_end; c++) {
-          const uint32_t xs = s0 + ((c & 1) ? SM::X1 : SM::X0);
-          if (c > c_begin && !wait(kRdyY)) break;  // the previous y has read Y1b
-          if (!wait(kRdyM0)) break;
-          tc_fence_after();
-          y1_block(kColY1b, xs, 2, true);
-          if (!wait(kRdyM1)) break;
-          tc_fence_after();
-          y1_block(kColY1b, xs, 3, false);
-          commit(kBarY1b);
+        for (int sg = 0; sg < nsegs() && !fail; sg++) {
+          const Seg sq = segment(sg);
+          for (int c = sq.cb; c < sq.ce; c++, k++) {
+            const uint32_t xs = s0 + ((k & 1) ? SM::X1 : SM::X0);
+            if (k > 0 && !wait(kRdyY)) break;  // the previous chunk's y has read Y1b
+            if (!wait(kRdyM0)) break;
+            tc_fence_after();
+            y1_block(kColY1b, xs, 2, true);
+            if (!wait(kRdyM1)) break;
+            tc_fence_after();
+            y1_block(kColY1b, xs, 3, false);
+            commit(kBarY1b);
+          }
         }
       }
       if (fail) {
@@ -441,69 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     const int hf = tid >> 7;         // which half of the columns
     const int wq = warp & 3;         // the warp's tensor-memory lane quarter: rows 32wq .. 32wq+31
     const uint32_t tlane = tmem + ((uint32_t)(wq * 32) << 16);
-    const float a2 = __ldg(p.A + h) * kLog2e;  // decay exponent per unit delta, base 2
-    const float dtbias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
-    const float Dh = p.D ? __ldg(p.D + h) : 0.f;
-    float* const dls2 = reinterpret_cast<float*>(sm + SM::DL);   // [2][128]: chunk c in half c & 1
+    float* const dls2 = reinterpret_cast<float*>(sm + SM::DL);   // [2][128]: the k-th chunk in half k & 1
     float* const css2 = reinterpret_cast<float*>(sm + SM::CS);   // [2][128]
     float* const wsum2 = reinterpret_cast<float*>(sm + SM::WSUM);  // [2][4]
     float* const qs2 = reinterpret_cast<float*>(sm + SM::QS);      // [2][128]
     const __nv_bfloat16* dt_all = static_cast<const __nv_bfloat16*>(p.dt);
     const int64_t dt_last = p.batch * L * H - 1;  // index of dt's last element
     uint32_t* dtb = reinterpret_cast<uint32_t*>(sm + SM::DTB);
-    // Row t of chunk c needs dt[b, t, h]. It is fetched a chunk ahead by an
-    // asynchronous 4-byte copy of the aligned pair of bf16 that holds it (a
-    // plain load would be waited for by this thread's next release fence), or,
-    // for dt's very last element when it starts a pair, by a plain load.
-    auto fetch_dt = [&](int64_t c) {
-      const int64_t t = c * kQ + row;
-      uint32_t* dst = dtb + (c & 1) * kQ + row;
-      if (t >= L) return;
-      const int64_t i = (b * L + t) * H + h;
-      if ((i & 1) == 0 && i == dt_last) {
-        *dst = (uint32_t)__bfloat16_as_ushort(dt_all[i]);
-      } else {
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(dt_all + (i & ~(int64_t)1))
-                     : "memory");
-      }
-    };
-    auto dt_of = [&](int64_t c) -> float {  // this row's dt in chunk c, once its copy is complete
-      const int64_t i = (b * L + c * kQ + row) * H + h;
-      const uint32_t w = dtb[(c & 1) * kQ + row];
-      return __uint_as_float(((i & 1) ? (w >> 16) : (w & 0xffffu)) << 16);
-    };
-    // delta and the decay (base 2) accumulated inside chunk cc, inclusive,
-    // into half cc & 1 of dls2 / css2, and q_s = 2^(cs_e - cs_s) delta_s with e
-    // the last step of s's block of 32 (threads of the first column half,
-    // warp w holding block w; all compute threads take part in its barrier).
-    // Visible to the others after the next barrier.
-    auto scalars = [&](int64_t cc) {
-      float dl = 0.f, sc = 0.f;
-      float* ws = wsum2 + (cc & 1) * 4;
-      if (hf == 0) {
-        asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk cc
-        dl = cc * kQ + row < L ? softplus_fast(dt_of(cc) + dtbias) : 0.f;
-        if (cc + 1 < c_end) {
-          fetch_dt(cc + 1);
-          asm volatile("cp.async.commit_group;" ::: "memory");
-        }
-        sc = dl * a2;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_up_sync(0xffffffffu, sc, o);
-          if (lane >= o) sc += v;
-        }
-        if (lane == 31) ws[warp] = sc;
-      }
-      bar_sync_compute();
-      if (hf == 0) {
-        for (int w = 0; w < warp; w++) sc += ws[w];
-        dls2[(cc & 1) * kQ + row] = dl;
-        css2[(cc & 1) * kQ + row] = sc;
-        qs2[(cc & 1) * kQ + row] = ex2(__shfl_sync(0xffffffffu, sc, 31) - sc) * dl;
-      }
-    };
-
     // the state lives in tensor memory: thread (row n, half hf) owns
     // H^T[n][32 hf .. 32 hf + 31], columns kColState + 32 hf of lane n
     const uint32_t tstate = tlane + kColState + 32 * hf;
@@ -519,236 +511,310 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         *reinterpret_cast<uint4*>(sm + SM::HL + sw128(row, 32 * hf + 8 * c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     };
-    // the state entering the piece: h0 (or zeros) for the first piece of a
-    // sequence, else the one the previous piece published (a bounded wait)
     bool aborted = false;  // a wait timed out; the same for every compute thread
-    if (piece > 0) {
-      bool got = true;
-      if (tid == 0) {
-        const uint32_t* flag = p.ws_flags + bh;
-        got = ld_acquire_gpu(flag) >= (uint32_t)piece;
-        const uint64_t t_start = globaltimer();
-        while (!got && globaltimer() - t_start <= wait_ns) got = ld_acquire_gpu(flag) >= (uint32_t)piece;
-      }
-      aborted = bar_or_compute(!got);
-    }
-    {
-      uint32_t hv[32];
-      // (h0 is [64, dstate]; the hand-over slot [64, 128]; state rows past
-      // dstate are zero and stay zero, B's padded columns being zero)
-      const int64_t sstride = piece > 0 ? kN : p.dstate;
-      const float* h0 = piece > 0 ? p.ws_state + bh * kP * kN : (p.h0 ? p.h0 + bh * kP * p.dstate : nullptr);
-      const bool rin = h0 && !aborted && row < sstride;
-#pragma unroll
-      for (int q = 0; q < 32; q++) hv[q] = __float_as_uint(rin ? h0[(32 * hf + q) * sstride + row] : 0.f);
-      tmem_st32(tstate, hv);
-      if (has_h0) {
-        write_state(hv);
-        fence_proxy_async_smem();  // read by the tensor core
-      }
-      tc_fence_before();
-      if (has_h0) mbar_arrive(&bar[kRdyH]);
-    }
-    if (hf == 0) {
-      fetch_dt(c_begin);
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    }
-    scalars(c_begin);
-    bar_sync_compute();
-    for (int64_t c = c_begin; c < c_end && !aborted; c++) {
-      const int64_t t0 = c * kQ;
-      const float* dls = dls2 + (c & 1) * kQ;
-      const float* css = css2 + (c & 1) * kQ;
-      const float* qsv = qs2 + (c & 1) * kQ;
-      const uint8_t* xs = sm + ((c & 1) ? SM::X1 : SM::X0);
-      // ---- X' (row s, columns p in half hf) = 2^(cs_end - cs_s) delta_s x_s
-      wait(kBarX0 + (int)(c & 1));
-      {
-        const f2 ws = splat2(ex2(css[kQ - 1] - css[row]) * dls[row]);
-#pragma unroll
-        for (int c8 = 0; c8 < 4; c8++) {
-          const int off = sw128(row, 32 * hf + 8 * c8);
-          const uint4 xw = *reinterpret_cast<const uint4*>(xs + off);
-          const uint32_t w[4] = {xw.x, xw.y, xw.z, xw.w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int i = 0; i < 4; i++)
-            split2(mul2(pk(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)), ws), hi[i], lo[i]);
-          *reinterpret_cast<uint4*>(sm + SM::XH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(sm + SM::XL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    int k = 0;             // chunks this CTA has begun
+    for (int sg = 0; sg < nsegs() && !aborted; sg++) {
+      const Seg sq = segment(sg);
+      const int b = (int)(sq.u / H), h = (int)(sq.u % H);
+      const bool has_h0 = sq.cb > 0 || p.h0 != nullptr;  // a state enters the segment
+      const float a2 = __ldg(p.A + h) * kLog2e;  // decay exponent per unit delta, base 2
+      const float dtbias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
+      const float Dh = p.D ? __ldg(p.D + h) : 0.f;
+      // Row t of chunk c needs dt[b, t, h]. It is fetched a chunk ahead by an
+      // asynchronous 4-byte copy of the aligned pair of bf16 that holds it (a
+      // plain load would be waited for by this thread's next release fence),
+      // or, for dt's very last element when it starts a pair, by a plain load.
+      auto fetch_dt = [&](int64_t c, int kc) {
+        const int64_t t = c * kQ + row;
+        uint32_t* dst = dtb + (kc & 1) * kQ + row;
+        if (t >= L) return;
+        const int64_t i = (b * L + t) * H + h;
+        if ((i & 1) == 0 && i == dt_last) {
+          *dst = (uint32_t)__bfloat16_as_ushort(dt_all[i]);
+        } else {
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                       "l"(dt_all + (i & ~(int64_t)1))
+                       : "memory");
         }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bar[kRdyX]);
-      if (tid == kStoreTid) {  // the previous chunk's y store has read its staging tiles
-        bulk_wait_read();
-        mbar_arrive(&bar[kStg]);
-      }
-      // ---- M (row t, columns s in half hf) from S, D_h on the diagonal,
-      // written over S in tensor memory, where Y1 = M X reads it as its A
-      // operand: the 32 columns of S block k (s in [32k, 32k + 32)) take the
-      // block's high parts (16 columns, two bf16 each, the even s in the low
-      // half) and then its remainders. This thread's blocks are kb0 and kb0 +
-      // 1; the issuer starts Y1 on blocks 0 and 2 once every thread has
-      // written its first one. Block k holds nonzeros for the warp's rows only
-      // if k <= wq (warp-uniform).
-      wait(kBarS);
-      tc_fence_after();
-      {
-        const float cst = css[row];
-        const int kb0 = 2 * hf;
-#pragma unroll 1
-        for (int j = 0; j < 2; j++) {
-          const int k = kb0 + j;
-          uint32_t sr[32];  // S block k, then M's words: [0, 16) the high parts, [16, 32) the remainders
-          if (k < wq) {
-            // below the diagonal block: 2^(cs_t - cs_s) = 2^(cs_t - cs_e) 2^(cs_e - cs_s),
-            // e the block's last step; both factors are at most 1
-            tmem_ld32_async(tlane + kColS + 32 * k, sr);
-            const f2 rt = splat2(ex2(cst - css[32 * k + 31]));
-            tmem_wait_ld(sr);
-            uint32_t lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; i++) {  // (pair i reads S words 2i, 2i + 1 >= i: writing word i is safe)
-              const float2 q = *reinterpret_cast<const float2*>(qsv + 32 * k + 2 * i);
-              const f2 v = mul2(mul2(get2(sr, i), pk(q.x, q.y)), rt);
-              split2(v, sr[i], lo[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; i++) sr[16 + i] = lo[i];
-          } else if (k == wq) {  // the block that holds the diagonal: causal mask, D_h on it
-            tmem_ld32_async(tlane + kColS + 32 * k, sr);
-            tmem_wait_ld(sr);
-            uint32_t lo[16];
-            const int dr = row - 32 * k;  // the diagonal's position in the block
-#pragma unroll
-            for (int i = 0; i < 16; i++) {  // (pair i reads S words 2i, 2i + 1 >= i: writing word i is safe)
-              const float2 cs = *reinterpret_cast<const float2*>(css + 32 * k + 2 * i);
-              const float2 dl = *reinterpret_cast<const float2*>(dls + 32 * k + 2 * i);
-              f2 m = mul2(mul2(get2(sr, i), pk(ex2(cst - cs.x), ex2(cst - cs.y))), pk(dl.x, dl.y));
-              float m0 = f2lo(m), m1 = f2hi(m);
-              m0 = 2 * i < dr ? m0 : (2 * i == dr ? m0 + Dh : 0.f);
-              m1 = 2 * i + 1 < dr ? m1 : (2 * i + 1 == dr ? m1 + Dh : 0.f);
-              split2(pk(m0, m1), sr[i], lo[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; i++) sr[16 + i] = lo[i];
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; i++) sr[i] = 0u;
+      };
+      auto dt_of = [&](int64_t c, int kc) -> float {  // this row's dt in chunk c, once its copy is complete
+        const int64_t i = (b * L + c * kQ + row) * H + h;
+        const uint32_t w = dtb[(kc & 1) * kQ + row];
+        return __uint_as_float(((i & 1) ? (w >> 16) : (w & 0xffffu)) << 16);
+      };
+      // delta and the decay (base 2) accumulated inside chunk cc (the kc-th
+      // of the run), inclusive, into half kc & 1 of dls2 / css2, and q_s =
+      // 2^(cs_e - cs_s) delta_s with e the last step of s's block of 32
+      // (threads of the first column half, warp w holding block w; all compute
+      // threads take part in its barrier). Visible to the others after the
+      // next barrier.
+      auto scalars = [&](int64_t cc, int kc) {
+        float dl = 0.f, sc = 0.f;
+        float* ws = wsum2 + (kc & 1) * 4;
+        if (hf == 0) {
+          asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk cc
+          dl = cc * kQ + row < L ? softplus_fast(dt_of(cc, kc) + dtbias) : 0.f;
+          if (cc + 1 < sq.ce) {
+            fetch_dt(cc + 1, kc + 1);
+            asm volatile("cp.async.commit_group;" ::: "memory");
           }
-          tmem_st32(tlane + kColS + 32 * k, sr);
-          tc_fence_before();
-          mbar_arrive(&bar[j == 0 ? kRdyM0 : kRdyM1]);
+          sc = dl * a2;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o) sc += v;
+          }
+          if (lane == 31) ws[warp] = sc;
         }
+        bar_sync_compute();
+        if (hf == 0) {
+          for (int w = 0; w < warp; w++) sc += ws[w];
+          dls2[(kc & 1) * kQ + row] = dl;
+          css2[(kc & 1) * kQ + row] = sc;
+          qs2[(kc & 1) * kQ + row] = ex2(__shfl_sync(0xffffffffu, sc, 31) - sc) * dl;
+        }
+      };
+      // the state entering the segment: h0 (or zeros) at a sequence's start,
+      // else the one the CTA with the previous range published (a bounded wait)
+      if (sq.cb > 0) {
+        bool got = true;
+        if (tid == 0) {
+          const uint32_t* flag = p.ws_flags + sq.u;
+          got = ld_acquire_gpu(flag) >= (uint32_t)sq.cb;
+          const uint64_t t_start = globaltimer();
+          while (!got && globaltimer() - t_start <= wait_ns) got = ld_acquire_gpu(flag) >= (uint32_t)sq.cb;
+        }
+        aborted = bar_or_compute(!got);
       }
-      // ---- the state, row n of H^T: 2^cs_end H^T + H_l^T (Y2, issued before
-      // B^T X', has read the state's previous parts)
-      wait(kBarH);
-      tc_fence_after();
       {
-        const float dec = ex2(css[kQ - 1]);
-        uint32_t hl[32], hv[32];
-        {
-          uint32_t hl2[32];
-          tmem_ld32_async(tlane + kColH + 32 * hf, hl);
-          tmem_ld32_async(tlane + kColH + kP + 32 * hf, hl2);
-          tmem_wait_ld(hl);
-          tmem_wait_ld(hl2);
+        uint32_t hv[32];
+        // (h0 is [64, dstate]; the hand-over slot [64, 128]; state rows past
+        // dstate are zero and stay zero, B's padded columns being zero)
+        const int64_t sstride = sq.cb > 0 ? kN : p.dstate;
+        const float* h0 =
+            sq.cb > 0 ? p.ws_state + sq.u * kP * kN : (p.h0 ? p.h0 + sq.u * kP * p.dstate : nullptr);
+        const bool rin = h0 && !aborted && row < sstride;
 #pragma unroll
-          for (int i = 0; i < 16; i++) set2(hl, i, add2(get2(hl, i), get2(hl2, i)));
-        }
-        tmem_ld32_async(tstate, hv);
-        tmem_wait_ld(hv);
-        const f2 dec2 = splat2(dec);
-#pragma unroll
-        for (int i = 0; i < 16; i++) set2(hv, i, fma2(dec2, get2(hv, i), get2(hl, i)));
+        for (int q = 0; q < 32; q++) hv[q] = __float_as_uint(rin ? h0[(32 * hf + q) * sstride + row] : 0.f);
         tmem_st32(tstate, hv);
-        write_state(hv);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bar[kRdyH]);
-      // ---- the next chunk's delta and decay sums, while Y1 runs
-      if (c + 1 < c_end) scalars(c + 1);
-      // ---- y of row t, columns p in half hf: Y1 + 2^cs_t Y2, staged in
-      // shared memory and stored by TMA
-      wait(kBarY1a);
-      wait(kBarY1b);
-      const bool y2 = c > c_begin || has_h0;
-      if (y2) wait(kBarY2);
-      tc_fence_after();
-      bool abort;
-      {
-        const int pb = 32 * hf;
-        uint32_t r1[32], r2[32];
-        {  // Y1 = the half over s < 64 + the half over s >= 64
-          uint32_t r3[32];
-          tmem_ld32_async(tlane + kColY1a + pb, r1);
-          tmem_ld32_async(tlane + kColY1b + pb, r3);
-          tmem_wait_ld(r1);
-          tmem_wait_ld(r3);
-#pragma unroll
-          for (int i = 0; i < 16; i++) set2(r1, i, add2(get2(r1, i), get2(r3, i)));
-        }
-        if (y2) {
-          tmem_ld32_async(tlane + kColY2 + pb, r2);
-          tmem_wait_ld(r2);
+        // (the previous segment's last C H_in^T has read the two parts: its
+        // completion was waited for before that chunk's state update)
+        if (has_h0) {
+          write_state(hv);
+          fence_proxy_async_smem();  // read by the tensor core
         }
         tc_fence_before();
-        mbar_arrive(&bar[kRdyY]);  // Y1 and Y2 are read
-        if (y2) {
-          const f2 et = splat2(ex2(css[row]));
-#pragma unroll
-          for (int i = 0; i < 16; i++) set2(r1, i, fma2(et, get2(r2, i), get2(r1, i)));
-        }
-        const float* o = reinterpret_cast<const float*>(r1);
-        wait(kStg);  // the previous chunk's y store has read the staging tiles
-        if constexpr (sizeof(TOut) == 2) {
+        if (has_h0) mbar_arrive(&bar[kRdyH]);
+      }
+      if (aborted) break;
+      if (hf == 0) {
+        fetch_dt(sq.cb, k);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+      scalars(sq.cb, k);
+      bar_sync_compute();
+      for (int c = sq.cb; c < sq.ce && !aborted; c++, k++) {
+        const int64_t t0 = (int64_t)c * kQ;
+        const float* dls = dls2 + (k & 1) * kQ;
+        const float* css = css2 + (k & 1) * kQ;
+        const float* qsv = qs2 + (k & 1) * kQ;
+        const uint8_t* xs = sm + ((k & 1) ? SM::X1 : SM::X0);
+        const bool y2 = c > sq.cb || has_h0;  // a state enters the chunk: C H_in^T runs
+        // ---- X' (row s, columns p in half hf) = 2^(cs_end - cs_s) delta_s x_s
+        wait(kBarX0 + (int)(k & 1));
+        {
+          const f2 ws = splat2(ex2(css[kQ - 1] - css[row]) * dls[row]);
 #pragma unroll
           for (int c8 = 0; c8 < 4; c8++) {
-            uint32_t w4[4];
+            const int off = sw128(row, 32 * hf + 8 * c8);
+            const uint4 xw = *reinterpret_cast<const uint4*>(xs + off);
+            const uint32_t w[4] = {xw.x, xw.y, xw.z, xw.w};
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[8 * c8 + 2 * i], o[8 * c8 + 2 * i + 1]);
-              w4[i] = *reinterpret_cast<const uint32_t*>(&v2);
-            }
-            *reinterpret_cast<uint4*>(sm + SM::YS0 + sw128(row, pb + 8 * c8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            for (int i = 0; i < 4; i++)
+              split2(mul2(pk(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)), ws), hi[i], lo[i]);
+            *reinterpret_cast<uint4*>(sm + SM::XH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm + SM::XL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
-        } else {  // fp32: tile hf holds columns 32 hf .. 32 hf + 31, 128 bytes a row
-#pragma unroll
-          for (int c4 = 0; c4 < 8; c4++)
-            *reinterpret_cast<float4*>(sm + (hf ? SM::YS1 : SM::YS0) + row * 128 + ((c4 ^ (row & 7)) << 4)) =
-                make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
         }
         fence_proxy_async_smem();
-        // every row is staged and the next chunk's scalars are written; a
-        // timeout anywhere ends the loop for every compute thread
-        abort = bar_or_compute(fail);
-        aborted = abort;
-        if (!abort && tid == kStoreTid) {
-          tma_store_4d(&tm_y, sm + SM::YS0, 0, (int)h, (int)t0, (int)b);
-          if constexpr (sizeof(TOut) == 4) tma_store_4d(&tm_y, sm + SM::YS1, 32, (int)h, (int)t0, (int)b);
+        mbar_arrive(&bar[kRdyX]);
+        if (tid == kStoreTid) {  // the previous chunk's y store has read its staging tiles
+          bulk_wait_read();
+          mbar_arrive(&bar[kStg]);
         }
-      }
-      if (abort) break;
-    }
-    // the state leaving the piece: h_last after the last piece, else the
-    // hand-over slot, published for the next piece
-    const int64_t ostride = last_piece ? p.dstate : kN;  // h_last [64, dstate]; the slot [64, 128]
-    float* hout = last_piece ? (p.h_last ? p.h_last + bh * kP * p.dstate : nullptr) : p.ws_state + bh * kP * kN;
-    if (!aborted && hout && row < ostride) {  // (the same for every thread of a warp)
-      uint32_t hv[32];
-      tmem_ld32_async(tstate, hv);
-      tmem_wait_ld(hv);
+        // ---- M (row t, columns s in half hf) from S, D_h on the diagonal,
+        // written over S in tensor memory, where Y1 = M X reads it as its A
+        // operand: the 32 columns of S block k (s in [32k, 32k + 32)) take the
+        // block's high parts (16 columns, two bf16 each, the even s in the low
+        // half) and then its remainders. This thread's blocks are kb0 and kb0 +
+        // 1; the issuer starts Y1 on blocks 0 and 2 once every thread has
+        // written its first one. Block k holds nonzeros for the warp's rows only
+        // if k <= wq (warp-uniform).
+        wait(kBarS);
+        tc_fence_after();
+        {
+          const float cst = css[row];
+          const int kb0 = 2 * hf;
+#pragma unroll 1
+          for (int j = 0; j < 2; j++) {
+            const int kb = kb0 + j;
+            uint32_t sr[32];  // S block kb, then M's words: [0, 16) the high parts, [16, 32) the remainders
+            if (kb < wq) {
+              // below the diagonal block: 2^(cs_t - cs_s) = 2^(cs_t - cs_e) 2^(cs_e - cs_s),
+              // e the block's last step; both factors are at most 1
+              tmem_ld32_async(tlane + kColS + 32 * kb, sr);
+              const f2 rt = splat2(ex2(cst - css[32 * kb + 31]));
+              tmem_wait_ld(sr);
+              uint32_t lo[16];
 #pragma unroll
-      for (int q = 0; q < 32; q++) hout[(32 * hf + q) * ostride + row] = __uint_as_float(hv[q]);
-    }
-    if (!last_piece) {
-      bar_sync_compute();  // every thread's part of the state is written
-      if (tid == 0 && !aborted && ticket != p.withhold_piece) {
-        __threadfence();
-        st_release_gpu(p.ws_flags + bh, (uint32_t)(piece + 1));
+              for (int i = 0; i < 16; i++) {  // (pair i reads S words 2i, 2i + 1 >= i: writing word i is safe)
+                const float2 q = *reinterpret_cast<const float2*>(qsv + 32 * kb + 2 * i);
+                const f2 v = mul2(mul2(get2(sr, i), pk(q.x, q.y)), rt);
+                split2(v, sr[i], lo[i]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; i++) sr[16 + i] = lo[i];
+            } else if (kb == wq) {  // the block that holds the diagonal: causal mask, D_h on it
+              tmem_ld32_async(tlane + kColS + 32 * kb, sr);
+              tmem_wait_ld(sr);
+              uint32_t lo[16];
+              const int dr = row - 32 * kb;  // the diagonal's position in the block
+#pragma unroll
+              for (int i = 0; i < 16; i++) {  // (pair i reads S words 2i, 2i + 1 >= i: writing word i is safe)
+                const float2 cs = *reinterpret_cast<const float2*>(css + 32 * kb + 2 * i);
+                const float2 dl = *reinterpret_cast<const float2*>(dls + 32 * kb + 2 * i);
+                f2 m = mul2(mul2(get2(sr, i), pk(ex2(cst - cs.x), ex2(cst - cs.y))), pk(dl.x, dl.y));
+                float m0 = f2lo(m), m1 = f2hi(m);
+                m0 = 2 * i < dr ? m0 : (2 * i == dr ? m0 + Dh : 0.f);
+                m1 = 2 * i + 1 < dr ? m1 : (2 * i + 1 == dr ? m1 + Dh : 0.f);
+                split2(pk(m0, m1), sr[i], lo[i]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; i++) sr[16 + i] = lo[i];
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; i++) sr[i] = 0u;
+            }
+            tmem_st32(tlane + kColS + 32 * kb, sr);
+            tc_fence_before();
+            mbar_arrive(&bar[j == 0 ? kRdyM0 : kRdyM1]);
+          }
+        }
+        // ---- the state, row n of H^T: 2^cs_end H^T + H_l^T. Its two parts
+        // are rewritten only after this chunk's C H_in^T has read them (that
+        // product's own completion: it comes from another issuing thread than
+        // B^T X'); a segment's last chunk writes them for no further product.
+        wait(kBarH);
+        if (y2) wait(kBarY2);
+        tc_fence_after();
+        {
+          const float dec = ex2(css[kQ - 1]);
+          uint32_t hl[32], hv[32];
+          {
+            uint32_t hl2[32];
+            tmem_ld32_async(tlane + kColH + 32 * hf, hl);
+            tmem_ld32_async(tlane + kColH + kP + 32 * hf, hl2);
+            tmem_wait_ld(hl);
+            tmem_wait_ld(hl2);
+#pragma unroll
+            for (int i = 0; i < 16; i++) set2(hl, i, add2(get2(hl, i), get2(hl2, i)));
+          }
+          tmem_ld32_async(tstate, hv);
+          tmem_wait_ld(hv);
+          const f2 dec2 = splat2(dec);
+#pragma unroll
+          for (int i = 0; i < 16; i++) set2(hv, i, fma2(dec2, get2(hv, i), get2(hl, i)));
+          tmem_st32(tstate, hv);
+          if (c + 1 < sq.ce) {
+            write_state(hv);
+            fence_proxy_async_smem();
+          }
+        }
+        tc_fence_before();
+        if (c + 1 < sq.ce) mbar_arrive(&bar[kRdyH]);
+        // ---- the next chunk's delta and decay sums, while Y1 runs
+        if (c + 1 < sq.ce) scalars(c + 1, k + 1);
+        // ---- y of row t, columns p in half hf: Y1 + 2^cs_t Y2, staged in
+        // shared memory and stored by TMA
+        wait(kBarY1a);
+        wait(kBarY1b);
+        tc_fence_after();
+        bool abort;
+        {
+          const int pb = 32 * hf;
+          uint32_t r1[32], r2[32];
+          {  // Y1 = the half over s < 64 + the half over s >= 64
+            uint32_t r3[32];
+            tmem_ld32_async(tlane + kColY1a + pb, r1);
+            tmem_ld32_async(tlane + kColY1b + pb, r3);
+            tmem_wait_ld(r1);
+            tmem_wait_ld(r3);
+#pragma unroll
+            for (int i = 0; i < 16; i++) set2(r1, i, add2(get2(r1, i), get2(r3, i)));
+          }
+          if (y2) {
+            tmem_ld32_async(tlane + kColY2 + pb, r2);
+            tmem_wait_ld(r2);
+          }
+          tc_fence_before();
+          mbar_arrive(&bar[kRdyY]);  // Y1 and Y2 are read
+          if (y2) {
+            const f2 et = splat2(ex2(css[row]));
+#pragma unroll
+            for (int i = 0; i < 16; i++) set2(r1, i, fma2(et, get2(r2, i), get2(r1, i)));
+          }
+          const float* o = reinterpret_cast<const float*>(r1);
+          wait(kStg);  // the previous chunk's y store has read the staging tiles
+          if constexpr (sizeof(TOut) == 2) {
+#pragma unroll
+            for (int c8 = 0; c8 < 4; c8++) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int i = 0; i < 4; i++) {
+                const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[8 * c8 + 2 * i], o[8 * c8 + 2 * i + 1]);
+                w4[i] = *reinterpret_cast<const uint32_t*>(&v2);
+              }
+              *reinterpret_cast<uint4*>(sm + SM::YS0 + sw128(row, pb + 8 * c8)) =
+                  make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          } else {  // fp32: tile hf holds columns 32 hf .. 32 hf + 31, 128 bytes a row
+#pragma unroll
+            for (int c4 = 0; c4 < 8; c4++)
+              *reinterpret_cast<float4*>(sm + (hf ? SM::YS1 : SM::YS0) + row * 128 + ((c4 ^ (row & 7)) << 4)) =
+                  make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+          }
+          fence_proxy_async_smem();
+          // every row is staged and the next chunk's scalars are written; a
+          // timeout anywhere ends the run for every compute thread
+          abort = bar_or_compute(fail);
+          aborted = abort;
+          if (!abort && tid == kStoreTid) {
+            tma_store_4d(&tm_y, sm + SM::YS0, 0, (int)h, (int)t0, (int)b);
+            if constexpr (sizeof(TOut) == 4) tma_store_4d(&tm_y, sm + SM::YS1, 32, (int)h, (int)t0, (int)b);
+          }
+        }
+        if (abort) break;
+      }
+      if (aborted) break;
+      // the state leaving the segment: h_last at the sequence's end, else the
+      // hand-over slot, published for the CTA with the next range
+      const bool seq_end = sq.ce == nchunk;
+      const int64_t ostride = seq_end ? p.dstate : kN;  // h_last [64, dstate]; the slot [64, 128]
+      float* hout = seq_end ? (p.h_last ? p.h_last + sq.u * kP * p.dstate : nullptr) : p.ws_state + sq.u * kP * kN;
+      if (hout && row < ostride) {  // (the same for every thread of a warp)
+        uint32_t hv[32];
+        tmem_ld32_async(tstate, hv);
+        tmem_wait_ld(hv);
+#pragma unroll
+        for (int q = 0; q < 32; q++) hout[(32 * hf + q) * ostride + row] = __uint_as_float(hv[q]);
+      }
+      if (!seq_end) {
+        bar_sync_compute();  // every thread's part of the state is written
+        if (tid == 0 && ticket != p.withhold_range) {
+          __threadfence();
+          st_release_gpu(p.ws_flags + sq.u, (uint32_t)sq.ce);
+        }
       }
     }
     if (tid == kStoreTid) bulk_wait_all();  // the y stores are complete
@@ -807,7 +873,7 @@ cudaError_t launch_tc(const SsdParams& p, cudaStream_t s) {
   auto k = ssd_tc_kernel<TOut>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::ALLOC);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)(p.batch * p.nheads * p.pieces), kThreads, TcSmem::ALLOC, s>>>(p, mx, mb, mc, my);
+  k<<<(unsigned)p.ranges, kThreads, TcSmem::ALLOC, s>>>(p, mx, mb, mc, my);
   return cudaGetLastError();
 }
 

@@ -133,26 +133,43 @@ def test_ssd_decay_extremes(dt_level, a_scale):
     assert_close(h, hr, BF16, what=f"ssd h_last, dt level {dt_level}, A x {a_scale}")
 
 
-# (batch, L, heads, groups, h0, piece length in steps): sequences split into
-# pieces run by different CTAs, the state handed on through the workspace
+# (batch, L, heads, groups, h0, share length in steps): the chunks of all
+# sequences cut into contiguous shares, one per CTA, the state handed on
+# through the workspace where a share starts inside a sequence. Shares of one
+# chunk make chains of hand-overs; shares of 3 and 11 chunks (sequences of 8)
+# cross sequence ends, so a CTA runs the next sequence's head before the
+# tail it takes over; shares of 20 chunks hold two whole sequences each.
 SPLITS = [(1, 1000, 2, 2, True, 128), (2, 1000, 3, 1, False, 256), (1, 1100, 4, 2, True, 384),
-          (3, 700, 2, 1, True, 512)]
+          (3, 700, 2, 1, True, 512), (2, 1000, 3, 1, True, 384), (2, 1000, 3, 3, False, 1408),
+          (2, 1000, 3, 1, True, 2560)]
 
 
-@pytest.mark.parametrize("case", SPLITS, ids=[f"b{c[0]}-L{c[1]}-H{c[2]}-G{c[3]}-piece{c[5]}" for c in SPLITS])
+@pytest.mark.parametrize("case", SPLITS, ids=[f"b{c[0]}-L{c[1]}-H{c[2]}-G{c[3]}-share{c[5]}" for c in SPLITS])
 def test_ssd_split_sequences(case):
-    Bt, L, H, G, h0, piece = case
-    x = gen.random_ssd_inputs(Bt, L, H, 64, 128, G, in_dtype="bf16", seed=L + piece, with_h0=h0)
+    Bt, L, H, G, h0, share = case
+    x = gen.random_ssd_inputs(Bt, L, H, 64, 128, G, in_dtype="bf16", seed=L + share, with_h0=h0)
     yr, hr = oracle.ssd(x, G)
-    ss.ss_scan_set_tuning(0, piece, 0)
+    ss.ss_scan_set_tuning(0, share, 0)
     try:
-        y, h = _run(x, F32)
+        for out in (F32, BF16):
+            y, h = _run(x, out)
+            ss.ss_scan_status(None)
+            assert_close(y, yr, BF16, out_bf16=(out == BF16), what=f"split ssd y {case}")
+            assert_close(h, hr, BF16, what=f"split ssd h_last {case}")
     finally:
         ss.ss_scan_set_tuning(0, 0, 0)
+
+
+def test_ssd_more_sequences_than_sms():
+    # 2 x 80 heads = 160 sequences of 3 chunks: the automatic plan gives every
+    # SM an equal share of the 480 chunks, with hand-overs between CTAs; every
+    # output checked
+    x = gen.random_ssd_inputs(2, 300, 80, 64, 128, 4, in_dtype="bf16", seed=160, with_h0=True)
+    yr, hr = oracle.ssd(x, 4)
+    y, h = _run(x, BF16)
     ss.ss_scan_status(None)
-    assert_close(y, yr, BF16, what=f"split ssd y {case}")
-    assert_close(h, hr, BF16, what=f"split ssd h_last {case}")
-    assert_close(y, yr, F32, what=f"split ssd y {case} (float32 bound)")
+    assert_close(y, yr, BF16, out_bf16=True, what="ssd y, 160 sequences")
+    assert_close(h, hr, BF16, what="ssd h_last, 160 sequences")
 
 
 def test_ssd_without_workspace():
@@ -168,8 +185,9 @@ def test_ssd_without_workspace():
 
 
 def test_ssd_withheld_hand_over_times_out():
-    # piece 0 of sequence 0 never hands its state on: piece 1 of that sequence
-    # gives up after the short limit, the call finishes, the status reports the
+    # shares of two chunks: share 0 (sequence 0, chunks 0-1) never hands its
+    # state on, so share 1 of that sequence gives up after the short limit
+    # (and share 2 after it), the call finishes, the status reports the
     # timeout once, and a clean call is correct again
     x = gen.random_ssd_inputs(1, 1000, 2, 64, 128, 1, in_dtype="bf16", seed=41, with_h0=True)
     d = to_dev(x)
@@ -196,7 +214,7 @@ def test_ssd_withheld_hand_over_times_out():
 
 def test_ssd_split_sequences_dstate64():
     # d_state 64 runs with B and C zero-padded to 128 columns; split into
-    # pieces, with an initial state
+    # shares of two chunks, with an initial state
     x = gen.random_ssd_inputs(2, 900, 3, 64, 64, 3, in_dtype="bf16", seed=64, with_h0=True)
     yr, hr = oracle.ssd(x, 3)
     ss.ss_scan_set_tuning(0, 256, 0)
