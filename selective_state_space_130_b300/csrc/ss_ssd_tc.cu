@@ -325,17 +325,27 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
   const uint32_t tmem = *tslot;
   const int64_t ticket = *tk_slot;
   struct Seg {
-    int64_t u;   // sequence (batch * nheads + head)
+    int64_t u;   // sequence (batch * nheads + head; below 2^31)
+    int b, h;    // its batch element and head
     int cb, ce;  // its chunks [cb, ce)
   };
   auto nsegs = [&]() -> int { return rd->nseg; };
   auto segment = [&](int s) -> Seg {  // the s-th segment the CTA runs
     const int n = rd->nseg;
     const int64_t u0 = rd->u0;
-    if (n == 1) return {u0, rd->cb_first, rd->ce_last};
-    if (s == 0) return {u0 + n - 1, 0, rd->ce_last};
-    if (s == n - 1) return {u0, rd->cb_first, (int)nchunk};
-    return {u0 + s, 0, (int)nchunk};
+    int64_t u;
+    int cb, ce;
+    if (n == 1) {
+      u = u0, cb = rd->cb_first, ce = rd->ce_last;
+    } else if (s == 0) {
+      u = u0 + n - 1, cb = 0, ce = rd->ce_last;
+    } else if (s == n - 1) {
+      u = u0, cb = rd->cb_first, ce = (int)nchunk;
+    } else {
+      u = u0 + s, cb = 0, ce = (int)nchunk;
+    }
+    const uint32_t u32 = (uint32_t)u, H32 = (uint32_t)H;
+    return {u, (int)(u32 / H32), (int)(u32 % H32), cb, ce};
   };
   uint32_t ph = 0;    // bit i: the phase of barrier i this thread waits for next
   bool fail = false;  // this thread gave up on a wait
@@ -378,33 +388,43 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_b);
         tma_prefetch_desc(&tm_c);
+        const int hpg = (int)(H / G);  // heads per group
+        // the copies of chunk c of segment q (the kc-th chunk of the run)
+        auto issue_cb = [&](const Seg& q, int c) {
+          const int b = q.b, grp = q.h / hpg, t0 = c * kQ;
+          mbar_expect_tx(&bar[kBarCB], 4 * SM::TILE);
+          tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, b, &bar[kBarCB]);
+          tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, b, &bar[kBarCB]);
+          tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, b, &bar[kBarCB]);
+          tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, b, &bar[kBarCB]);
+          mbar_arrive(&bar[kBarCB]);
+          nissue[kBarCB]++;
+        };
+        auto issue_x = [&](const Seg& q, int c, int kc) {  // into buffer kc & 1
+          const int xb = kBarX0 + (kc & 1);
+          mbar_expect_tx(&bar[xb], SM::TILE);
+          tma_load_4d(sm + ((kc & 1) ? SM::X1 : SM::X0), &tm_x, 0, q.h, c * kQ, q.b, &bar[xb]);
+          mbar_arrive(&bar[xb]);
+          nissue[xb]++;
+        };
         for (int sg = 0; sg < nsegs() && !fail; sg++) {
           const Seg sq = segment(sg);
-          const int b = (int)(sq.u / H), h = (int)(sq.u % H);
-          const int grp = (int)(h / (H / G));
           const bool has_h0 = sq.cb > 0 || p.h0 != nullptr;  // a state enters the segment
-          auto issue_cb = [&](int64_t c) {
-            const int t0 = (int)(c * kQ);
-            mbar_expect_tx(&bar[kBarCB], 4 * SM::TILE);
-            tma_load_4d(sm + SM::C0, &tm_c, 0, grp, t0, (int)b, &bar[kBarCB]);
-            tma_load_4d(sm + SM::C1, &tm_c, 64, grp, t0, (int)b, &bar[kBarCB]);
-            tma_load_4d(sm + SM::B0, &tm_b, 0, grp, t0, (int)b, &bar[kBarCB]);
-            tma_load_4d(sm + SM::B1, &tm_b, 64, grp, t0, (int)b, &bar[kBarCB]);
-            mbar_arrive(&bar[kBarCB]);
-            nissue[kBarCB]++;
-          };
-          auto issue_x = [&](int64_t c, int kc) {  // chunk c, k-th of the run: buffer kc & 1
-            const int xb = kBarX0 + (int)(kc & 1);
-            mbar_expect_tx(&bar[xb], SM::TILE);
-            tma_load_4d(sm + ((kc & 1) ? SM::X1 : SM::X0), &tm_x, 0, (int)h, (int)(c * kQ), (int)b, &bar[xb]);
-            mbar_arrive(&bar[xb]);
-            nissue[xb]++;
-          };
-          // (the previous segment's last products have released C, B, S and
-          // its x buffer: waited for below)
-          issue_cb(sq.cb);
-          issue_x(sq.cb, k);
+          if (sg == 0) {  // later segments' first copies were issued during the segment before
+            issue_cb(sq, sq.cb);
+            issue_x(sq, sq.cb, k);
+          }
           for (int c = sq.cb; c < sq.ce; c++, k++) {
+            // the chunk after this one in the run: the next of the segment, or
+            // the first of the next segment (u < 0: none)
+            Seg nx = sq;
+            nx.cb = c + 1;
+            if (c + 1 == sq.ce) {
+              if (sg + 1 < nsegs())
+                nx = segment(sg + 1);
+              else
+                nx.u = -1;
+            }
             // S = C B^T (S's columns were read by the previous chunk's Y1)
             if (!wait(kBarCB)) break;
             tc_fence_after();
@@ -412,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
             commit(kBarS);
             // x of the next chunk, into the buffer of the chunk before this one
             // (its Y1 is done, its X' written)
-            if (c + 1 < sq.ce) issue_x(c + 1, k + 1);
+            if (nx.u >= 0) issue_x(nx, nx.cb, k + 1);
             // H_l^T = B^T X' (A = B read MN-major: its two n halves are one tile
             // apart; B: X''s high part and remainder side by side, N = 128)
             if (!wait(kRdyX)) break;
@@ -420,14 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
             mma_k128(tmem + kColH, s0 + SM::B0, false, s0 + SM::XH, false, SM::TILE, SM::TILE, idesc(kN, 2 * kP, 1, 1));
             commit(kBarH);
             // C and B are free once S, H_l (in issue order) and Y2 are done;
-            // S's columns and this x once both halves of Y1 are. After the
-            // segment's last chunk the same waits let the next segment start.
-            // The next copy may complete the C/B barrier's next phase only
-            // once issuer 1 has seen this one: Y2 and Y1a come after its wait.
-            const bool y2 = c > sq.cb || has_h0;
-            if (!wait(kBarH) || (y2 && !wait(kBarY2)) || (!y2 && !wait(kBarY1a))) break;
-            if (c + 1 < sq.ce) issue_cb(c + 1);
-            if ((y2 && !wait(kBarY1a)) || !wait(kBarY1b)) break;
+            // S's columns and this x once both halves of Y1 are. (Issuer 1
+            // has seen this copy's phase before Y2, or does not wait for it.)
+            if (!wait(kBarH) || ((c > sq.cb || has_h0) && !wait(kBarY2))) break;
+            if (nx.u >= 0) issue_cb(nx, nx.cb);
+            if (!wait(kBarY1a) || !wait(kBarY1b)) break;
           }
         }
       } else if (role == 1) {
@@ -436,11 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
           const bool has_h0 = sq.cb > 0 || p.h0 != nullptr;
           for (int c = sq.cb; c < sq.ce; c++, k++) {
             const uint32_t xs = s0 + ((k & 1) ? SM::X1 : SM::X0);
-            if (!wait(kBarCB)) break;            // C of the chunk
-            if (k > 0 && !wait(kRdyY)) break;    // the previous chunk's y has read Y1a and Y2
+            const bool y2 = c > sq.cb || has_h0;
+            // C of the chunk, for Y2. Without Y2 the phase is passed over
+            // unwaited: issuer 0 copies the next C only after this chunk's H_l
+            // and Y2 are done (so it cannot run two phases ahead of this
+            // thread's next wait), and this chunk's copy has landed before
+            // this thread's next wait (M, waited for below, follows S, which
+            // follows the copy)
+            if (y2) {
+              if (!wait(kBarCB)) break;
+            } else {
+              ph ^= 1u << kBarCB;
+            }
+            if (k > 0 && !wait(kRdyY)) break;  // the previous chunk's y has read Y1a and Y2
             // Y2 = C H_in^T: A K-major (C), B MN-major (H^T), the high part and
             // then the remainder into one accumulator
-            if (c > sq.cb || has_h0) {
+            if (y2) {
               if (!wait(kRdyH)) break;  // the state entering the chunk is written
               tc_fence_after();
               mma_k128(tmem + kColY2, s0 + SM::C0, true, s0 + SM::HH, false, 16, 16, idesc(kQ, kP, 0, 1));
@@ -511,69 +539,72 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         *reinterpret_cast<uint4*>(sm + SM::HL + sw128(row, 32 * hf + 8 * c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     };
+    // Row t of chunk c of sequence u needs dt[b, t, h]. It is fetched a chunk
+    // ahead by an asynchronous 4-byte copy of the aligned pair of bf16 that
+    // holds it (a plain load would be waited for by this thread's next release
+    // fence), or, for dt's very last element when it starts a pair, by a plain
+    // load; the kc-th chunk of the run goes to half kc & 1.
+    auto dt_index = [&](const Seg& q, int c) { return ((int64_t)q.b * L + (int64_t)c * kQ + row) * H + q.h; };
+    auto fetch_dt = [&](const Seg& q, int c, int kc) {
+      uint32_t* dst = dtb + (kc & 1) * kQ + row;
+      if ((int64_t)c * kQ + row >= L) return;
+      const int64_t i = dt_index(q, c);
+      if ((i & 1) == 0 && i == dt_last) {
+        *dst = (uint32_t)__bfloat16_as_ushort(dt_all[i]);
+      } else {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(dt_all + (i & ~(int64_t)1))
+                     : "memory");
+      }
+    };
+    // delta and the decay (base 2) accumulated inside chunk cc of segment sg
+    // (the kc-th chunk of the run), inclusive, into half kc & 1 of dls2 /
+    // css2, and q_s = 2^(cs_e - cs_s) delta_s with e the last step of s's
+    // block of 32 (threads of the first column half, warp w holding block w;
+    // all compute threads take part in its barrier). Visible to the others
+    // after the next barrier. Also fetches the dt of the chunk after cc in the
+    // run: the next of the segment or the first of the next segment.
+    auto scalars = [&](const Seg& sq, int sg, int cc, int kc) {  // (sq: segment sg)
+      float dl = 0.f, sc = 0.f;
+      float* ws = wsum2 + (kc & 1) * 4;
+      if (hf == 0) {
+        const float a2 = __ldg(p.A + sq.h) * kLog2e;  // decay exponent per unit delta, base 2
+        const float dtbias = p.dt_bias ? __ldg(p.dt_bias + sq.h) : 0.f;
+        asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk cc
+        if ((int64_t)cc * kQ + row < L) {
+          const int64_t i = dt_index(sq, cc);
+          const uint32_t w = dtb[(kc & 1) * kQ + row];
+          dl = softplus_fast(__uint_as_float(((i & 1) ? (w >> 16) : (w & 0xffffu)) << 16) + dtbias);
+        }
+        if (cc + 1 < sq.ce) {
+          fetch_dt(sq, cc + 1, kc + 1);
+        } else if (sg + 1 < nsegs()) {
+          const Seg nq = segment(sg + 1);
+          fetch_dt(nq, nq.cb, kc + 1);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        sc = dl * a2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_up_sync(0xffffffffu, sc, o);
+          if (lane >= o) sc += v;
+        }
+        if (lane == 31) ws[warp] = sc;
+      }
+      bar_sync_compute();
+      if (hf == 0) {
+        for (int w = 0; w < warp; w++) sc += ws[w];
+        dls2[(kc & 1) * kQ + row] = dl;
+        css2[(kc & 1) * kQ + row] = sc;
+        qs2[(kc & 1) * kQ + row] = ex2(__shfl_sync(0xffffffffu, sc, 31) - sc) * dl;
+      }
+    };
     bool aborted = false;  // a wait timed out; the same for every compute thread
     int k = 0;             // chunks this CTA has begun
     for (int sg = 0; sg < nsegs() && !aborted; sg++) {
       const Seg sq = segment(sg);
-      const int b = (int)(sq.u / H), h = (int)(sq.u % H);
+      const int b = sq.b, h = sq.h;
       const bool has_h0 = sq.cb > 0 || p.h0 != nullptr;  // a state enters the segment
-      const float a2 = __ldg(p.A + h) * kLog2e;  // decay exponent per unit delta, base 2
-      const float dtbias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
       const float Dh = p.D ? __ldg(p.D + h) : 0.f;
-      // Row t of chunk c needs dt[b, t, h]. It is fetched a chunk ahead by an
-      // asynchronous 4-byte copy of the aligned pair of bf16 that holds it (a
-      // plain load would be waited for by this thread's next release fence),
-      // or, for dt's very last element when it starts a pair, by a plain load.
-      auto fetch_dt = [&](int64_t c, int kc) {
-        const int64_t t = c * kQ + row;
-        uint32_t* dst = dtb + (kc & 1) * kQ + row;
-        if (t >= L) return;
-        const int64_t i = (b * L + t) * H + h;
-        if ((i & 1) == 0 && i == dt_last) {
-          *dst = (uint32_t)__bfloat16_as_ushort(dt_all[i]);
-        } else {
-          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
-                       "l"(dt_all + (i & ~(int64_t)1))
-                       : "memory");
-        }
-      };
-      auto dt_of = [&](int64_t c, int kc) -> float {  // this row's dt in chunk c, once its copy is complete
-        const int64_t i = (b * L + c * kQ + row) * H + h;
-        const uint32_t w = dtb[(kc & 1) * kQ + row];
-        return __uint_as_float(((i & 1) ? (w >> 16) : (w & 0xffffu)) << 16);
-      };
-      // delta and the decay (base 2) accumulated inside chunk cc (the kc-th
-      // of the run), inclusive, into half kc & 1 of dls2 / css2, and q_s =
-      // 2^(cs_e - cs_s) delta_s with e the last step of s's block of 32
-      // (threads of the first column half, warp w holding block w; all compute
-      // threads take part in its barrier). Visible to the others after the
-      // next barrier.
-      auto scalars = [&](int64_t cc, int kc) {
-        float dl = 0.f, sc = 0.f;
-        float* ws = wsum2 + (kc & 1) * 4;
-        if (hf == 0) {
-          asm volatile("cp.async.wait_all;" ::: "memory");  // this row's dt of chunk cc
-          dl = cc * kQ + row < L ? softplus_fast(dt_of(cc, kc) + dtbias) : 0.f;
-          if (cc + 1 < sq.ce) {
-            fetch_dt(cc + 1, kc + 1);
-            asm volatile("cp.async.commit_group;" ::: "memory");
-          }
-          sc = dl * a2;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float v = __shfl_up_sync(0xffffffffu, sc, o);
-            if (lane >= o) sc += v;
-          }
-          if (lane == 31) ws[warp] = sc;
-        }
-        bar_sync_compute();
-        if (hf == 0) {
-          for (int w = 0; w < warp; w++) sc += ws[w];
-          dls2[(kc & 1) * kQ + row] = dl;
-          css2[(kc & 1) * kQ + row] = sc;
-          qs2[(kc & 1) * kQ + row] = ex2(__shfl_sync(0xffffffffu, sc, 31) - sc) * dl;
-        }
-      };
       // the state entering the segment: h0 (or zeros) at a sequence's start,
       // else the one the CTA with the previous range published (a bounded wait)
       if (sq.cb > 0) {
@@ -607,12 +638,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         if (has_h0) mbar_arrive(&bar[kRdyH]);
       }
       if (aborted) break;
-      if (hf == 0) {
-        fetch_dt(sq.cb, k);
-        asm volatile("cp.async.commit_group;" ::: "memory");
+      if (sg == 0) {  // later segments' first scalars were computed during the segment before
+        if (hf == 0) {
+          fetch_dt(sq, sq.cb, k);
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        scalars(sq, sg, sq.cb, k);
+        bar_sync_compute();
       }
-      scalars(sq.cb, k);
-      bar_sync_compute();
       for (int c = sq.cb; c < sq.ce && !aborted; c++, k++) {
         const int64_t t0 = (int64_t)c * kQ;
         const float* dls = dls2 + (k & 1) * kQ;
@@ -733,8 +766,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         }
         tc_fence_before();
         if (c + 1 < sq.ce) mbar_arrive(&bar[kRdyH]);
-        // ---- the next chunk's delta and decay sums, while Y1 runs
-        if (c + 1 < sq.ce) scalars(c + 1, k + 1);
+        // ---- the next chunk's delta and decay sums, while Y1 runs (the
+        // next segment's first chunk after a segment's last)
+        if (c + 1 < sq.ce) {
+          scalars(sq, sg, c + 1, k + 1);
+        } else if (sg + 1 < nsegs()) {
+          const Seg nq = segment(sg + 1);
+          scalars(nq, sg + 1, nq.cb, k + 1);
+        }
         // ---- y of row t, columns p in half hf: Y1 + 2^cs_t Y2, staged in
         // shared memory and stored by TMA
         wait(kBarY1a);
