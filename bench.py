@@ -503,10 +503,13 @@ def bench_general(ss, w, dev, hbm_peak, clock_mhz, N, G, disc, reps=10):
     Bt, L, Dm = w.batch, w.seqlen, w.dim
     y = torch.empty((Bt, L, Dm), dtype=torch.bfloat16, device=dev)
     h = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+    # the split's workspace, allocated once outside the timed region
+    ws_bytes = ss.ss_scan_fwd_general_workspace_size(Bt, L, Dm, N, G, disc, torch.bfloat16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else False
 
     def call():
         ss.ss_scan_fwd_general(x["u"], x["delta_raw"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], None,
-                               disc=disc, y=y, h_last=h)
+                               disc=disc, y=y, h_last=h, workspace=ws)
 
     for _ in range(3):
         call()
@@ -524,7 +527,7 @@ def bench_general(ss, w, dev, hbm_peak, clock_mhz, N, G, disc, reps=10):
     updates = Bt * L * Dm * N
     alu_peak = GEN_UPDATES_PER_CLK_SM[disc] * SMS * clock_mhz * 1e6
     achieved = updates / (ms * 1e-3)
-    del x, y, h
+    del x, y, h, ws
     torch.cuda.empty_cache()
     return {"workload": f"generalised scan, {w.name} shape: batch {Bt}, L {L}, d_inner {Dm}, d_state {N}, "
                         f"{G} group(s) of B/C, {disc} Bbar, bf16 inputs and y",

@@ -241,10 +241,29 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
  *
  * Other arguments, layouts, dtypes and conventions are those of ss_scan_fwd
  * with 16 replaced by dstate (A [dim, dstate]; h0, h_last [batch, dim,
- * dstate]). No workspace: one warp runs each block of 32 / (dstate / 16)
- * channels over the whole sequence. SS_ERR_UNSUPPORTED for another dstate or
- * discretisation, or when the B and C rows of the groups one channel block
- * spans do not fit in shared memory.
+ * dstate]).
+ *
+ * Kernels. d_state 16 in one group with SS_DISC_FIRST_ORDER runs on the
+ * ss_scan_fwd kernel. d_state 32, 64 or 128, when each group's channels are a
+ * multiple of the CTA's block of 4 * 32 / (dstate / 16) channels and rows are
+ * 16-byte aligned, runs on a CTA-cooperative kernel. Other shapes run one warp
+ * per block of 32 / (dstate / 16) channels over the whole sequence.
+ *
+ * workspace (optional, device, 16-byte aligned, caller-owned, at least
+ * ss_scan_fwd_general_workspace_size bytes when given): with it, and more
+ * channel blocks (batch elements x blocks) than resident CTAs, the CTA kernel
+ * runs one CTA per slot, each taking an equal contiguous share of all blocks'
+ * 32-step tiles. Where a share starts inside a block's sequence, the state is
+ * handed on through the workspace from the CTA with the share before. Its
+ * first few KB are reset by the call (on `stream`), and it must not be shared
+ * by calls that can run at the same time. NULL runs one CTA per block. A
+ * workspace smaller than needed is SS_ERR_INVALID_ARG. A hand-over that does
+ * not arrive within the wait limit (ss_scan_set_wait_limit) ends the waiting
+ * CTAs and is reported by ss_scan_status(NULL, stream) as SS_ERR_TIMEOUT; the
+ * outputs are then undefined.
+ *
+ * SS_ERR_UNSUPPORTED for another dstate or discretisation, or when the B and C
+ * rows of the groups one channel block spans do not fit in shared memory.
  */
 typedef enum { SS_DISC_FIRST_ORDER = 0, SS_DISC_ZOH = 1 } ss_disc;
 
@@ -253,7 +272,16 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
                               const void *u, const void *delta_raw, const float *A,
                               const void *B, const void *C, const float *D, const void *z,
                               const float *delta_bias, const float *h0,
-                              void *y, float *h_last, void *stream);
+                              void *y, float *h_last, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * Bytes of workspace ss_scan_fwd_general can use for this problem (0: it never
+ * splits such a problem). Pure host computation: no device call, no error
+ * state.
+ */
+size_t ss_scan_fwd_general_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                                          int64_t ngroups, ss_disc disc, ss_dtype in_dtype);
 
 /*
  * State-space-dual (Mamba-2) layer forward on the tensor cores.
@@ -322,10 +350,11 @@ size_t ss_ssd_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, 
  * cross-CTA carry path. max_workers > 0 caps the number of CTAs a split of the
  * work uses (default: one per SM), which makes range boundaries and hand-overs
  * more frequent. Results do not depend on these settings beyond fp32 rounding;
- * ss_scan_fwd_workspace_size() follows them. For ss_ssd_fwd (with a
- * workspace) chunk_len > 0 sets the length of the CTAs' shares of the chunks
- * (rounded up to 128 steps) instead of the automatic plan, so that shares
- * start inside sequences even on small problems.
+ * ss_scan_fwd_workspace_size() follows them. For ss_ssd_fwd and
+ * ss_scan_fwd_general (with a workspace) chunk_len > 0 sets the length of the
+ * CTAs' shares (rounded up to 128 steps for ss_ssd_fwd, 32 for the generalised
+ * scan's CTA kernel) instead of the automatic plan, so that shares start inside
+ * sequences even on small problems.
  */
 void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_workers);
 
@@ -340,8 +369,8 @@ void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_work
  * need it give up after wait_ns, set the fault word and return, so the call
  * finishes and ss_scan_status() reports SS_ERR_TIMEOUT; its outputs are then
  * undefined. No wait in the library is unbounded. They apply to ss_ssd_fwd
- * too: there withhold_item is the share of chunks (the shares in sequence
- * order, numbered from 0) whose state is never handed on.
+ * and ss_scan_fwd_general too: there withhold_item is the share (the shares in
+ * sequence order, numbered from 0) whose state is never handed on.
  */
 void ss_scan_set_wait_limit(uint64_t wait_ns, int64_t withhold_item);
 

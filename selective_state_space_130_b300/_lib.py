@@ -41,7 +41,8 @@ SIGNATURES = {
     "ss_scan_bwd_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
     "ss_scan_bwd": (ctypes.c_int, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int] + [_P] * 21 + [_SZ, _P]),
     "ss_scan_fwd_general": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
-                            + [_P] * 11 + [_P]),
+                            + [_P] * 12 + [ctypes.c_size_t, _P]),
+    "ss_scan_fwd_general_workspace_size": (ctypes.c_size_t, [_I64] * 5 + [ctypes.c_int, ctypes.c_int]),
     "ss_ssd_fwd": (ctypes.c_int, [_I64] * 6 + [ctypes.c_int, ctypes.c_int] + [_P] * 11 + [ctypes.c_size_t, _P]),
     "ss_ssd_fwd_workspace_size": (ctypes.c_size_t, [_I64] * 4),
     "ss_scan_set_tuning": (None, [ctypes.c_int, _I64, ctypes.c_int]),
@@ -214,11 +215,19 @@ def ss_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=N
     return o
 
 
+def ss_scan_fwd_general_workspace_size(batch, seqlen, dim, dstate, ngroups=1, disc="first_order",
+                                       in_dtype=torch.bfloat16):
+    code = SS_BF16 if in_dtype == torch.bfloat16 else SS_F32
+    return int(lib().ss_scan_fwd_general_workspace_size(batch, seqlen, dim, dstate, ngroups, DISC[disc], code))
+
+
 def ss_scan_fwd_general(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, h0=None, *, disc="first_order",
-                        out_dtype=None, y=None, h_last=None, return_h_last=True, stream=None):
+                        out_dtype=None, y=None, h_last=None, workspace=None, return_h_last=True, stream=None):
     """Generalised selective scan on device tensors: dstate = A.shape[1] (16, 32,
     64 or 128); B, C [Bt, L, G, N] (or [Bt, L, N] for G = 1); disc
-    "first_order" (Bbar = delta B) or "zoh". Returns (y, h_last)."""
+    "first_order" (Bbar = delta B) or "zoh". Returns (y, h_last). The workspace
+    (uint8) is allocated with torch when the problem can use one and none is
+    given; workspace=False runs without one."""
     Bt, L, Dm = u.shape
     N = A.shape[1]
     G = 1 if B.dim() == 3 else B.shape[2]
@@ -229,9 +238,14 @@ def ss_scan_fwd_general(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, 
         y = torch.empty((Bt, L, Dm), dtype=_tdt(out_code), device=dev)
     if h_last is None and return_h_last:
         h_last = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+    if workspace is None:
+        ws_bytes = ss_scan_fwd_general_workspace_size(Bt, L, Dm, N, G, disc, u.dtype)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else False
+    ws_ptr = _ptr(workspace) if workspace is not False else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not False else 0
     _check(lib().ss_scan_fwd_general(Bt, L, Dm, N, G, DISC[disc], code, out_code, _ptr(u), _ptr(delta_raw), _ptr(A),
                                      _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y),
-                                     _ptr(h_last), _stream(stream)))
+                                     _ptr(h_last), ws_ptr, ws_len, _stream(stream)))
     return y, h_last
 
 

@@ -567,11 +567,23 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   return SS_OK;
 }
 
+size_t ss_scan_fwd_general_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                                          int64_t ngroups, ss_disc disc, ss_dtype in_dtype) {
+  // the CTA kernel splits units; d_state 16 in one group with the first-order
+  // rule runs on the scan kernel's static split, and other shapes on the
+  // one-warp kernel, neither of which uses one
+  if (batch <= 0 || seqlen <= 0 || dim <= 0 || ngroups < 1 || dim % ngroups != 0 || !valid_dtype(in_dtype))
+    return 0;
+  if (dstate == 16 || !ssk::scan_general_cta_shape_ok(dim, dstate, dim / ngroups, in_dtype)) return 0;
+  (void)disc;
+  return ssk::scan_general_cta_workspace_bytes(batch, seqlen, dim, dstate);
+}
+
 ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t ngroups,
                               ss_disc disc, ss_dtype in_dtype, ss_dtype out_dtype, const void* u,
                               const void* delta_raw, const float* A, const void* B, const void* C, const float* D,
                               const void* z, const float* delta_bias, const float* h0, void* y, float* h_last,
-                              void* stream) {
+                              void* workspace, size_t workspace_bytes, void* stream) {
   g_err.clear();
   if (dstate != 16 && dstate != 32 && dstate != 64 && dstate != 128)
     return fail(SS_ERR_UNSUPPORTED, "dstate must be 16, 32, 64 or 128 (got %lld)", (long long)dstate);
@@ -601,10 +613,16 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
     for (int i = 0; i < 6; i++)
       if (!need[i]) return fail(SS_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
   }
-  const void* all[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, h_last};
-  const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last"};
-  for (int i = 0; i < 11; i++)
+  const void* all[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, h_last, workspace};
+  const char* all_names[] = {"u", "delta_raw", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "h_last",
+                             "workspace"};
+  for (int i = 0; i < 12; i++)
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
+  const size_t ws_need = ss_scan_fwd_general_workspace_size(batch, seqlen, dim, dstate, ngroups, disc, in_dtype);
+  if (workspace && ws_need > 0 && workspace_bytes < ws_need)
+    return fail(SS_ERR_INVALID_ARG, "workspace too small (%zu bytes, need %zu)", workspace_bytes, ws_need);
+  if (ws_need > 0 && (double)batch * (double)dim > 2.0e9)
+    return fail(SS_ERR_INVALID_ARG, "problem too large");
   const int sg = (int)(dstate / 16);
   const int64_t cw = 32 / sg;
   const int64_t ncblk = (dim + cw - 1) / cw;
@@ -634,6 +652,9 @@ ss_status ss_scan_fwd_general(int64_t batch, int64_t seqlen, int64_t dim, int64_
   else if (((size_t)dim * es) % 4 == 0 && in_row % 4 == 0) chunk = 4;
   ssk::GenParams p{u, delta_raw, z, B, C, A, D, delta_bias, h0, y, h_last, batch, seqlen, dim, ngroups, cpg,
                    (int)ncblk, ngw_max, chunk, (int)disc, ssk::device_fault_word(), g_wait_ns};
+  p.workspace = ws_need > 0 ? workspace : nullptr;
+  p.force_steps = g_tune_chunk;
+  p.withhold_range = g_withhold;
   if ((double)batch * ncblk > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
   cudaError_t e = ssk::scan_general_cta_supported(dim, dstate, cpg, in_dtype)
                       ? ssk::launch_scan_general_cta(p, dstate, in_dtype, out_dtype, s)

@@ -134,6 +134,20 @@ struct GenParams {
   int disc;                 // 0 first order, 1 zero-order hold
   unsigned int* fault;      // the library's fault word (timed-out waits)
   uint64_t wait_ns;         // limit of a device-side wait; 0 = the default
+  // Work split of the CTA kernel. Its (unit, tile) items (a unit is one
+  // channel block of one batch element), unit-major, are cut into `ranges`
+  // contiguous shares, one per CTA. With a workspace the CTAs take shares by
+  // ticket, and a share that starts inside a unit starts from the state the
+  // share before it left in ws_state[unit], published through ws_flags[unit]
+  // = the tile where the hand-over happens. The launch plans the shares from
+  // `workspace` (null: one CTA per unit) and `force_steps`.
+  void* workspace;          // the caller's workspace, or null
+  int64_t force_steps;      // > 0: share length in steps instead of the automatic plan
+  int64_t withhold_range;   // test knob: this share does not publish its state (-1: none)
+  int64_t ranges;           // set by the launch
+  unsigned int* ws_ticket;  //   ticket counter (or null: shares by block index)
+  unsigned int* ws_flags;   //   [units]
+  float* ws_state;          //   [units, 2048]
 };
 
 // Parameters of the state-space-dual (Mamba-2) layer forward.
@@ -223,6 +237,10 @@ int scan_general_stage_bytes(int64_t dstate, int ngw_max, ss_dtype in_dtype);
 // CTA-cooperative generalised scan (ss_scan_general_cta.cu): d_state 32, 64 or
 // 128 with every CTA's channels in one group and 16-byte rows.
 bool scan_general_cta_supported(int64_t dim, int64_t dstate, int64_t cpg, ss_dtype in_dtype);
+// the shape conditions alone (no driver query)
+bool scan_general_cta_shape_ok(int64_t dim, int64_t dstate, int64_t cpg, ss_dtype in_dtype);
+// Workspace bytes the CTA kernel can use to split units across CTAs (0: none).
+size_t scan_general_cta_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate);
 cudaError_t launch_scan_general_cta(const GenParams& p, int64_t dstate, ss_dtype in_dtype, ss_dtype out_dtype,
                                     cudaStream_t stream);
 

@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "ss_device.cuh"
 #include "ss_internal.h"
 
@@ -50,9 +52,25 @@ struct GCfg {
   static constexpr int OFF_W = RING * STAGE;    // widened B then C, fp32 [kTile][N] each
   static constexpr int WB = kTile * N * 4;
   static constexpr int OFF_BAR = OFF_W + 2 * WB;  // full[RING]
-  static constexpr int SMEM = OFF_BAR + RING * 8;
+  static constexpr int OFF_RANGE = OFF_BAR + RING * 8;  // the CTA's share and thread 0's load cursor (GRange)
+  static constexpr int SMEM = OFF_RANGE + 64;
   static_assert(kTile % SG == 0, "token groups must tile a tile");
 };
+
+// A CTA's share of the (unit, tile) items, unit-major (a unit is one channel
+// block of one batch element), as the segments it runs, and thread 0's load
+// cursor (the next tile of the run to load), in shared memory: read at a
+// segment's start or a load, not held in registers through the token loop.
+struct GRange {
+  int u0;        // the share's first unit
+  int nseg;      // units it touches
+  int tb_first;  // its first tile in unit u0
+  int te_last;   // one past its last tile in unit u0 + nseg - 1
+  int isg;       // load cursor: segment
+  int itile;     //   and tile
+  uint32_t ticket;
+};
+static_assert(sizeof(GRange) <= 64, "GRange outgrows its slot");
 
 __device__ __forceinline__ void bar_compute() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // barrier over the compute threads that returns the OR of v over them
@@ -98,41 +116,92 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
   constexpr int SG = K::SG, DC = K::DC, CC = K::CC;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
+  volatile GRange* rd = reinterpret_cast<volatile GRange*>(smem + K::OFF_RANGE);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t ncb = p.dim / CC;
-  const int64_t b = blockIdx.x / ncb, c0 = (blockIdx.x % ncb) * CC;
+  const int ncb = (int)(p.dim / CC);  // channel blocks per batch element
   const int64_t L = p.seqlen, Dm = p.dim;
-  const int grp = (int)(c0 / p.cpg);
-  const int64_t ntile = (L + kTile - 1) / kTile;
+  const int ntile = (int)((L + kTile - 1) / kTile);
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
   const bool has_z = p.z != nullptr;
 
-  // Thread 0 issues the loads: tile k goes to stage k % RING once every
-  // thread is past tile k - 1, which last used that stage.
+  // The items of all units, unit-major, are cut into p.ranges contiguous
+  // shares, one per CTA. A share covers the tail of one unit, whole units and
+  // the head of another; the CTA runs the head first (its state goes to the
+  // CTA with the next share), then the whole units, then the tail, whose
+  // entering state the CTA with the previous share published when it ran its
+  // own head first. A share inside one unit is a single segment that waits
+  // for its predecessor.
+  struct Seg {
+    int u, b, c0, grp;  // unit, its batch element, first channel and group
+    int tb, te;         // its tiles [tb, te)
+  };
+  auto segment = [&](int sgi) -> Seg {  // the sgi-th segment the CTA runs
+    const int n = rd->nseg, u0 = rd->u0;
+    int u, tb, te;
+    if (n == 1) {
+      u = u0, tb = rd->tb_first, te = rd->te_last;
+    } else if (sgi == 0) {
+      u = u0 + n - 1, tb = 0, te = rd->te_last;
+    } else if (sgi == n - 1) {
+      u = u0, tb = rd->tb_first, te = ntile;
+    } else {
+      u = u0 + sgi, tb = 0, te = ntile;
+    }
+    const int c0 = (int)((uint32_t)u % (uint32_t)ncb) * CC;
+    return {u, (int)((uint32_t)u / (uint32_t)ncb), c0, (int)(c0 / p.cpg), tb, te};
+  };
+
+  // Thread 0 issues the loads in the order of the run: the n-th tile goes to
+  // stage n % RING once every thread is past the tile before it in that stage.
   const uint32_t tile_bytes = (uint32_t)((has_z ? 3 : 2) * K::XB + 2 * K::RB);
   uint32_t nissued = 0;  // tiles issued (thread 0; for the drain after a timeout)
-  auto issue = [&](int64_t k) {
-    const int s = (int)(k % K::RING);
+  auto issue_next = [&]() {  // thread 0: the tile under the load cursor, if any
+    int sgi = rd->isg;
+    if (sgi >= rd->nseg) return;
+    const Seg q = segment(sgi);
+    const int tile = rd->itile;
+    const int s = (int)(nissued % K::RING);
     uint8_t* st = smem + s * K::STAGE;
-    const int t0 = (int)(k * kTile);
+    const int t0 = tile * kTile;
     mbar_expect_tx(&full[s], tile_bytes);
-    tma_load_3d(st + K::OFF_U, &tm_u, (int)c0, t0, (int)b, &full[s]);
-    tma_load_3d(st + K::OFF_DR, &tm_dr, (int)c0, t0, (int)b, &full[s]);
-    if (has_z) tma_load_3d(st + K::OFF_Z, &tm_z, (int)c0, t0, (int)b, &full[s]);
-    tma_load_4d(st + K::OFF_B, &tm_b, 0, grp, t0, (int)b, &full[s]);
-    tma_load_4d(st + K::OFF_C, &tm_c, 0, grp, t0, (int)b, &full[s]);
+    tma_load_3d(st + K::OFF_U, &tm_u, q.c0, t0, q.b, &full[s]);
+    tma_load_3d(st + K::OFF_DR, &tm_dr, q.c0, t0, q.b, &full[s]);
+    if (has_z) tma_load_3d(st + K::OFF_Z, &tm_z, q.c0, t0, q.b, &full[s]);
+    tma_load_4d(st + K::OFF_B, &tm_b, 0, q.grp, t0, q.b, &full[s]);
+    tma_load_4d(st + K::OFF_C, &tm_c, 0, q.grp, t0, q.b, &full[s]);
     mbar_arrive(&full[s]);
     nissued++;
+    if (tile + 1 < q.te) {
+      rd->itile = tile + 1;
+    } else {
+      sgi++;
+      rd->isg = sgi;
+      if (sgi < rd->nseg) rd->itile = segment(sgi).tb;
+    }
   };
   if (tid == 0) {
     for (int i = 0; i < K::RING; i++) mbar_init(&full[i], 1);
     fence_mbar_init();
+    // the share this CTA runs: tickets in launch order, so the CTA that hands
+    // a state on to this one has always started earlier
+    const int64_t ticket = p.ws_ticket ? atomicAdd(p.ws_ticket, 1u) : blockIdx.x;
+    const int64_t T = p.batch * ncb * (int64_t)ntile;
+    const int64_t qn = T / p.ranges, rm = T % p.ranges;  // shares of qn items, the first rm one longer
+    const int64_t g0 = ticket * qn + (ticket < rm ? ticket : rm), g1 = g0 + qn + (ticket < rm ? 1 : 0);
+    const int64_t u0 = g0 / ntile, u1 = (g1 - 1) / ntile;
+    rd->u0 = (int)u0;
+    rd->nseg = g1 > g0 ? (int)(u1 - u0 + 1) : 0;
+    rd->tb_first = (int)(g0 - u0 * ntile);
+    rd->te_last = (int)(g1 - u1 * ntile);
+    rd->ticket = (uint32_t)ticket;
+    rd->isg = 0;
+    rd->itile = rd->nseg > 0 ? segment(0).tb : 0;
     tma_prefetch_desc(&tm_u);
     tma_prefetch_desc(&tm_dr);
     if (has_z) tma_prefetch_desc(&tm_z);
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_c);
-    for (int64_t k = 0; k < K::RING - 1 && k < ntile; k++) issue(k);
+    for (int i = 0; i < K::RING - 1; i++) issue_next();
   }
   __syncthreads();
 
@@ -143,139 +212,180 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
   const int ch = lane / SG, j = lane % SG;
   auto qst = [&](int q) { return 4 * (j + SG * (q >> 1)) + 2 * (q & 1); };
   const int chl = warp * DC + ch;  // channel within the CTA
-  const int64_t d = c0 + chl;
-  const bool dv = d < Dm;
-  f2 A2[8], h[8];
-  [[maybe_unused]] f2 invA[8];
-#pragma unroll
-  for (int q = 0; q < 8; q++) {
-    const float a0 = dv ? __ldg(p.A + d * N + qst(q)) : 0.f;
-    const float a1 = dv ? __ldg(p.A + d * N + qst(q) + 1) : 0.f;
-    A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
-    const float* h0 = (dv && p.h0) ? p.h0 + (b * Dm + d) * N : nullptr;
-    h[q] = h0 ? pk(__ldg(h0 + qst(q)), __ldg(h0 + qst(q) + 1)) : pk(0.f, 0.f);
-    if constexpr (ZOH) invA[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
-  }
-  const float bias = (dv && p.delta_bias) ? __ldg(p.delta_bias + d) : 0.f;
-  const float Dd = (dv && p.D) ? __ldg(p.D + d) : 0.f;
   float* wB = reinterpret_cast<float*>(smem + K::OFF_W);
   float* wC = wB + kTile * N;
 
   bool fail = false;
-  for (int64_t k = 0; k < ntile; k++) {
-    const int s = (int)(k % K::RING);
-    const int64_t t0 = k * kTile;
-    const uint8_t* st = smem + s * K::STAGE;
-    const bool got = mbar_wait(&full[s], (uint32_t)((k / K::RING) & 1), wait_ns);
-    // every compute thread is past the previous tile (the widened rows are
-    // free); a timeout anywhere ends the loop for all of them
-    if (bar_compute_or(!got)) {
-      fail = true;
-      break;
-    }
-    if (tid == 0 && k + K::RING - 1 < ntile) issue(k + K::RING - 1);  // into the stage tile k - 1 used
-    const float* Bt;
-    const float* Ct;
-    if constexpr (K::ES == 2) {  // widen the tile's B and C once, each thread a slice
-      const uint4* rb = reinterpret_cast<const uint4*>(st + K::OFF_B);
-      const uint4* rc = reinterpret_cast<const uint4*>(st + K::OFF_C);
-      for (int i = tid; i < kTile * N / 8; i += kCW * 32) {
-#pragma unroll
-        for (int which = 0; which < 2; which++) {
-          const uint4 w = which ? rc[i] : rb[i];
-          float4* o = reinterpret_cast<float4*>((which ? wC : wB) + 8 * i);
-          o[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                             __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-          o[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
-                             __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
-        }
-      }
-      bar_compute();
-      Bt = wB;
-      Ct = wC;
-    } else {
-      Bt = reinterpret_cast<const float*>(st + K::OFF_B);
-      Ct = reinterpret_cast<const float*>(st + K::OFF_C);
-    }
-#pragma unroll 1
-    for (int g = 0; g < kTile; g += SG) {
-      // this lane's token of the group: its scalars, once per channel
-      const int tl = g + j;
-      const int64_t t = t0 + tl;
-      const bool tv = t < L;
-      const float xu = ld_elem<TIn>(st + K::OFF_U, tl * CC + chl);
-      const float dl = tv ? softplus_fast(ld_elem<TIn>(st + K::OFF_DR, tl * CC + chl) + bias) : 0.f;
-      float acc[SG];
-#pragma unroll
-      for (int kk = 0; kk < SG; kk++) {  // token g + kk, its scalars from lane kk of the channel
-        const int src = ch * SG + kk;
-        const float dlk = __shfl_sync(0xffffffffu, dl, src);
-        const float xuk = __shfl_sync(0xffffffffu, xu, src);
-        const f2 dl2 = pk(dlk, dlk);
-        [[maybe_unused]] const f2 du2 = pk(dlk * xuk, dlk * xuk);
-        [[maybe_unused]] const f2 xu2 = pk(xuk, xuk);
-        const float4* Bp = reinterpret_cast<const float4*>(Bt + (g + kk) * N) + j;  // quad j, then + SG per step
-        const float4* Cp = reinterpret_cast<const float4*>(Ct + (g + kk) * N) + j;
-        f2 y0 = pk(0.f, 0.f), y1 = pk(0.f, 0.f);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; q4++) {
-          const float4 bq = Bp[SG * q4], cq = Cp[SG * q4];
-          const f2 bv[2] = {pk(bq.x, bq.y), pk(bq.z, bq.w)};
-          const f2 cv[2] = {pk(cq.x, cq.y), pk(cq.z, cq.w)};
-#pragma unroll
-          for (int e = 0; e < 2; e++) {
-            const int q = 2 * q4 + e;
-            const f2 e2 = mul2(dl2, A2[q]);
-            const f2 a = pk(ex2(f2lo(e2)), ex2(f2hi(e2)));
-            if constexpr (ZOH) {
-              // Bbar u = (Abar - 1) / A * u = delta u phi(x), x = delta A, phi(x)
-              // = (e^x - 1) / x. Below |x| = 1/32, delta u times phi's series
-              // 1 + x/2 + x^2/6 + x^3/24 (truncation under x^4/120, a relative
-              // 1e-8), written in e2 = x log2 e; above it (Abar - 1) u / A,
-              // whose Abar from the MUFU exponential then has a relative error
-              // below 1e-5 of Abar - 1. A = 0 gives x = 0: delta u.
-              f2 ph = fma2(e2, pk(kPhi3, kPhi3), pk(kPhi2, kPhi2));
-              ph = fma2(e2, ph, pk(kPhi1, kPhi1));
-              ph = fma2(e2, ph, pk(1.f, 1.f));
-              const f2 bs = mul2(du2, ph);
-              const f2 be = mul2(add2(a, pk(-1.f, -1.f)), mul2(invA[q], xu2));
-              const f2 bu = pk(fabsf(f2lo(e2)) < kZohSeries ? f2lo(bs) : f2lo(be),
-                               fabsf(f2hi(e2)) < kZohSeries ? f2hi(bs) : f2hi(be));
-              h[q] = fma2(a, h[q], mul2(bu, bv[e]));
-            } else {
-              h[q] = fma2(a, h[q], mul2(du2, bv[e]));
-            }
-            if (e) y1 = fma2(cv[e], h[q], y1);
-            else y0 = fma2(cv[e], h[q], y0);
-          }
-        }
-        const f2 ys = add2(y0, y1);
-        acc[kk] = f2lo(ys) + f2hi(ys);
-      }
-      // sum each token's readout over the channel's SG lanes so that lane j
-      // ends with token j's: at each level the lanes with bit m set keep the
-      // upper half of their values and send the lower half
-#pragma unroll
-      for (int m = SG / 2, w = SG / 2; m >= 1; m >>= 1, w >>= 1) {
-        const bool up = (j & m) != 0;
-#pragma unroll
-        for (int e = 0; e < w; e++) {
-          const float keep = up ? acc[e + w] : acc[e];
-          const float send = up ? acc[e] : acc[e + w];
-          acc[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-        }
-      }
-      float yv = fmaf(Dd, xu, acc[0]);
-      if (has_z) yv *= silu(ld_elem<TIn>(st + K::OFF_Z, tl * CC + chl));
-      st_out(static_cast<TOut*>(p.y) + (b * L + t) * Dm + d, yv, dv && tv);
-    }
-  }
-  if (!fail && dv && p.h_last) {
-    float* hl = p.h_last + (b * Dm + d) * N;
+  int k = 0;  // tiles of the run begun
+  for (int sgi = 0; sgi < rd->nseg && !fail; sgi++) {
+    const Seg sq = segment(sgi);
+    const int64_t b = sq.b, d = sq.c0 + chl;
+    const bool dv = d < Dm;
+    f2 A2[8], h[8];
+    [[maybe_unused]] f2 invA[8];
 #pragma unroll
     for (int q = 0; q < 8; q++) {
-      hl[qst(q)] = f2lo(h[q]);
-      hl[qst(q) + 1] = f2hi(h[q]);
+      const float a0 = dv ? __ldg(p.A + d * N + qst(q)) : 0.f;
+      const float a1 = dv ? __ldg(p.A + d * N + qst(q) + 1) : 0.f;
+      A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
+      if constexpr (ZOH) invA[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+    }
+    const float bias = (dv && p.delta_bias) ? __ldg(p.delta_bias + d) : 0.f;
+    const float Dd = (dv && p.D) ? __ldg(p.D + d) : 0.f;
+    // the state entering the segment: h0 (or zeros) at the unit's start, else
+    // the one the CTA with the previous share published (a bounded wait)
+    float* slot = p.ws_state ? p.ws_state + ((int64_t)sq.u * CC + chl) * N : nullptr;  // [CC][N] per unit
+    const float* hin = nullptr;
+    if (sq.tb > 0) {
+      bool got = true;
+      if (tid == 0) {
+        const uint32_t* flag = p.ws_flags + sq.u;
+        got = ld_acquire_gpu(flag) >= (uint32_t)sq.tb;
+        const uint64_t t_start = globaltimer();
+        while (!got && globaltimer() - t_start <= wait_ns) got = ld_acquire_gpu(flag) >= (uint32_t)sq.tb;
+      }
+      if (bar_compute_or(!got)) {
+        fail = true;
+        break;
+      }
+      hin = slot;
+    } else if (dv && p.h0) {
+      hin = p.h0 + (b * Dm + d) * N;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; q++) h[q] = hin ? pk(hin[qst(q)], hin[qst(q) + 1]) : pk(0.f, 0.f);
+
+    for (int tile = sq.tb; tile < sq.te; tile++, k++) {
+      const int s = k % K::RING;
+      const int64_t t0 = (int64_t)tile * kTile;
+      const uint8_t* st = smem + s * K::STAGE;
+      const bool got = mbar_wait(&full[s], (uint32_t)((k / K::RING) & 1), wait_ns);
+      // every compute thread is past the previous tile (the widened rows and
+      // its stage are free); a timeout anywhere ends the run for all of them
+      if (bar_compute_or(!got)) {
+        fail = true;
+        break;
+      }
+      if (tid == 0) issue_next();  // into the stage the previous tile used
+      const float* Bt;
+      const float* Ct;
+      if constexpr (K::ES == 2) {  // widen the tile's B and C once, each thread a slice
+        const uint4* rb = reinterpret_cast<const uint4*>(st + K::OFF_B);
+        const uint4* rc = reinterpret_cast<const uint4*>(st + K::OFF_C);
+        for (int i = tid; i < kTile * N / 8; i += kCW * 32) {
+#pragma unroll
+          for (int which = 0; which < 2; which++) {
+            const uint4 w = which ? rc[i] : rb[i];
+            float4* o = reinterpret_cast<float4*>((which ? wC : wB) + 8 * i);
+            o[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                               __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+            o[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                               __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+          }
+        }
+        bar_compute();
+        Bt = wB;
+        Ct = wC;
+      } else {
+        Bt = reinterpret_cast<const float*>(st + K::OFF_B);
+        Ct = reinterpret_cast<const float*>(st + K::OFF_C);
+      }
+#pragma unroll 1
+      for (int g = 0; g < kTile; g += SG) {
+        // this lane's token of the group: its scalars, once per channel
+        const int tl = g + j;
+        const int64_t t = t0 + tl;
+        const bool tv = t < L;
+        const float xu = ld_elem<TIn>(st + K::OFF_U, tl * CC + chl);
+        const float dl = tv ? softplus_fast(ld_elem<TIn>(st + K::OFF_DR, tl * CC + chl) + bias) : 0.f;
+        float acc[SG];
+#pragma unroll
+        for (int kk = 0; kk < SG; kk++) {  // token g + kk, its scalars from lane kk of the channel
+          const int src = ch * SG + kk;
+          const float dlk = __shfl_sync(0xffffffffu, dl, src);
+          const float xuk = __shfl_sync(0xffffffffu, xu, src);
+          const f2 dl2 = pk(dlk, dlk);
+          [[maybe_unused]] const f2 du2 = pk(dlk * xuk, dlk * xuk);
+          [[maybe_unused]] const f2 xu2 = pk(xuk, xuk);
+          const float4* Bp = reinterpret_cast<const float4*>(Bt + (g + kk) * N) + j;  // quad j, then + SG per step
+          const float4* Cp = reinterpret_cast<const float4*>(Ct + (g + kk) * N) + j;
+          f2 y0 = pk(0.f, 0.f), y1 = pk(0.f, 0.f);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; q4++) {
+            const float4 bq = Bp[SG * q4], cq = Cp[SG * q4];
+            const f2 bv[2] = {pk(bq.x, bq.y), pk(bq.z, bq.w)};
+            const f2 cv[2] = {pk(cq.x, cq.y), pk(cq.z, cq.w)};
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+              const int q = 2 * q4 + e;
+              const f2 e2 = mul2(dl2, A2[q]);
+              const f2 a = pk(ex2(f2lo(e2)), ex2(f2hi(e2)));
+              if constexpr (ZOH) {
+                // Bbar u = (Abar - 1) / A * u = delta u phi(x), x = delta A, phi(x)
+                // = (e^x - 1) / x. Below |x| = 1/32, delta u times phi's series
+                // 1 + x/2 + x^2/6 + x^3/24 (truncation under x^4/120, a relative
+                // 1e-8), written in e2 = x log2 e; above it (Abar - 1) u / A,
+                // whose Abar from the MUFU exponential then has a relative error
+                // below 1e-5 of Abar - 1. A = 0 gives x = 0: delta u.
+                f2 ph = fma2(e2, pk(kPhi3, kPhi3), pk(kPhi2, kPhi2));
+                ph = fma2(e2, ph, pk(kPhi1, kPhi1));
+                ph = fma2(e2, ph, pk(1.f, 1.f));
+                const f2 bs = mul2(du2, ph);
+                const f2 be = mul2(add2(a, pk(-1.f, -1.f)), mul2(invA[q], xu2));
+                const f2 bu = pk(fabsf(f2lo(e2)) < kZohSeries ? f2lo(bs) : f2lo(be),
+                                 fabsf(f2hi(e2)) < kZohSeries ? f2hi(bs) : f2hi(be));
+                h[q] = fma2(a, h[q], mul2(bu, bv[e]));
+              } else {
+                h[q] = fma2(a, h[q], mul2(du2, bv[e]));
+              }
+              if (e) y1 = fma2(cv[e], h[q], y1);
+              else y0 = fma2(cv[e], h[q], y0);
+            }
+          }
+          const f2 ys = add2(y0, y1);
+          acc[kk] = f2lo(ys) + f2hi(ys);
+        }
+        // sum each token's readout over the channel's SG lanes so that lane j
+        // ends with token j's: at each level the lanes with bit m set keep the
+        // upper half of their values and send the lower half
+#pragma unroll
+        for (int m = SG / 2, w = SG / 2; m >= 1; m >>= 1, w >>= 1) {
+          const bool up = (j & m) != 0;
+#pragma unroll
+          for (int e = 0; e < w; e++) {
+            const float keep = up ? acc[e + w] : acc[e];
+            const float send = up ? acc[e] : acc[e + w];
+            acc[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+        float yv = fmaf(Dd, xu, acc[0]);
+        if (has_z) yv *= silu(ld_elem<TIn>(st + K::OFF_Z, tl * CC + chl));
+        st_out(static_cast<TOut*>(p.y) + (b * L + t) * Dm + d, yv, dv && tv);
+      }
+    }
+    if (fail) break;
+    // the state leaving the segment: h_last at the unit's end, else the
+    // hand-over slot, published for the CTA with the next share
+    if (sq.te == ntile) {
+      if (dv && p.h_last) {
+        float* hl = p.h_last + (b * Dm + d) * N;
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+          hl[qst(q)] = f2lo(h[q]);
+          hl[qst(q) + 1] = f2hi(h[q]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        slot[qst(q)] = f2lo(h[q]);
+        slot[qst(q) + 1] = f2hi(h[q]);
+      }
+      bar_compute();  // every thread's part of the state is written
+      if (tid == 0 && rd->ticket != (uint32_t)p.withhold_range) {
+        __threadfence();
+        st_release_gpu(p.ws_flags + sq.u, (uint32_t)sq.te);
+      }
     }
   }
   if (fail && tid == 0) {
@@ -339,8 +449,37 @@ cudaError_t launch_gcta(const GenParams& p, cudaStream_t s) {
   auto k = p.disc == 1 ? scan_general_cta_kernel<TIn, TOut, N, true> : scan_general_cta_kernel<TIn, TOut, N, false>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
   if (e != cudaSuccess) return e;
-  const int64_t grid = p.batch * (p.dim / K::CC);
-  k<<<(unsigned)grid, kCThreads, K::SMEM, s>>>(p, mu, mdr, mz, mb, mc);
+  // Shares: with a workspace and more units than CTA slots (resident CTAs per
+  // SM x SMs), one share per slot, each an equal part of all the items, so
+  // that no SM idles while others run a last partial round of units; a split
+  // cannot shorten a unit, whose state runs through its tiles in order.
+  // Otherwise one CTA per unit.
+  GenParams q = p;
+  const int64_t units = p.batch * (p.dim / K::CC), ntile = ((int64_t)L + kTile - 1) / kTile;
+  q.ranges = units;
+  q.ws_ticket = nullptr;
+  q.ws_flags = nullptr;
+  q.ws_state = nullptr;
+  if (p.workspace && ntile > 1) {
+    int occ = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kCThreads, K::SMEM)) != cudaSuccess) return e;
+    const int64_t slots = (int64_t)std::max(occ, 1) * device_sm_count();
+    int64_t R = units <= slots ? units : slots;
+    if (p.force_steps > 0) {
+      const int64_t rt = std::max<int64_t>(1, (p.force_steps + kTile - 1) / kTile);
+      R = (units * ntile + rt - 1) / rt;
+    }
+    if (R != units) {
+      uint8_t* w = static_cast<uint8_t*>(p.workspace);
+      const size_t flags_bytes = (size_t)((units * 4 + 255) / 256 * 256);
+      q.ranges = R;
+      q.ws_ticket = reinterpret_cast<unsigned int*>(w);
+      q.ws_flags = reinterpret_cast<unsigned int*>(w + 256);
+      q.ws_state = reinterpret_cast<float*>(w + 256 + flags_bytes);
+      if ((e = cudaMemsetAsync(w, 0, 256 + flags_bytes, s)) != cudaSuccess) return e;
+    }
+  }
+  k<<<(unsigned)q.ranges, kCThreads, K::SMEM, s>>>(q, mu, mdr, mz, mb, mc);
   return cudaGetLastError();
 }
 
@@ -353,11 +492,24 @@ cudaError_t launch_gcta_n(const GenParams& p, int64_t dstate, cudaStream_t s) {
 
 }  // namespace
 
-bool scan_general_cta_supported(int64_t dim, int64_t dstate, int64_t cpg, ss_dtype in_dtype) {
+bool scan_general_cta_shape_ok(int64_t dim, int64_t dstate, int64_t cpg, ss_dtype in_dtype) {
   if (dstate != 32 && dstate != 64 && dstate != 128) return false;
   const int64_t cc = kCW * (32 / (dstate / 16));  // channels per CTA
   const int64_t es = in_dtype == SS_BF16 ? 2 : 4;
-  return cpg % cc == 0 && (dim * es) % 16 == 0 && genc_fn() != nullptr;
+  return cpg % cc == 0 && (dim * es) % 16 == 0;
+}
+
+bool scan_general_cta_supported(int64_t dim, int64_t dstate, int64_t cpg, ss_dtype in_dtype) {
+  return scan_general_cta_shape_ok(dim, dstate, cpg, in_dtype) && genc_fn() != nullptr;
+}
+
+// A ticket counter (256 bytes), one flag per unit (padded to 256 bytes), then
+// one [CC, dstate] fp32 state per unit: CC * dstate = 2048 whatever dstate.
+size_t scan_general_cta_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
+  if ((dstate != 32 && dstate != 64 && dstate != 128) || batch <= 0 || dim <= 0 || seqlen <= kTile) return 0;
+  const int64_t units = batch * (dim / (kCW * (32 / (dstate / 16))));
+  if (units <= 0) return 0;
+  return 256 + (size_t)((units * 4 + 255) / 256 * 256) + (size_t)units * 2048 * sizeof(float);
 }
 
 cudaError_t launch_scan_general_cta(const GenParams& p, int64_t dstate, ss_dtype in_dtype, ss_dtype out_dtype,

@@ -164,9 +164,9 @@ def _gen(**kw):
     a.update({k: v for k, v in kw.items() if k in a})
     p = [kw.get(k, v) for k, v in (("u", 0x1000), ("delta_raw", 0x2000), ("A", 0x3000), ("B", 0x4000),
                                    ("C", 0x5000), ("D", None), ("z", None), ("delta_bias", None), ("h0", None),
-                                   ("y", 0x6000), ("h_last", None))]
+                                   ("y", 0x6000), ("h_last", None), ("workspace", None))]
     return ss.lib().ss_scan_fwd_general(a["batch"], a["seqlen"], a["dim"], a["dstate"], a["ngroups"], a["disc"],
-                                        a["in_dtype"], a["out_dtype"], *p, None)
+                                        a["in_dtype"], a["out_dtype"], *p, kw.get("workspace_bytes", 0), None)
 
 
 @pytest.mark.parametrize("kw,code,msg", [
@@ -181,6 +181,27 @@ def _gen(**kw):
 def test_scan_general_rejects_bad_arguments(kw, code, msg):
     assert _gen(**kw) == code
     assert msg in ss.ss_last_error()
+
+
+def test_scan_general_workspace_size_and_checks():
+    # the CTA kernel's split: a ticket counter (256 bytes), one flag per
+    # channel block (padded to 256 bytes), one 2048-float state per block;
+    # blocks are 32, 16 and 64 channels at d_state 64, 128 and 32
+    ws = ss.ss_scan_fwd_general_workspace_size
+    assert ws(4, 2048, 5120, 64, 1, "zoh") == 256 + 2560 + 640 * 2048 * 4
+    assert ws(4, 2048, 5120, 128, 8) == 256 + 5120 + 1280 * 2048 * 4
+    assert ws(2, 100, 256, 32, 2) == 256 + 256 + 8 * 2048 * 4
+    assert ws(4, 2048, 5120, 16, 1) == 0       # the scan kernel's static split
+    assert ws(4, 2048, 5120, 16, 4) == 0       # the one-warp kernel
+    assert ws(1, 32, 256, 64, 1) == 0          # one tile: nothing to split
+    assert ws(2, 100, 40, 64, 1) == 0          # 40 channels: not whole 32-channel blocks
+    assert ws(2, 100, 256, 64, 1, in_dtype=torch.float32) == ws(2, 100, 256, 64, 1)
+    need = ws(1, 300, 64, 64, 1, "first_order", torch.float32)
+    kw = dict(seqlen=300, dim=64, dstate=64, ngroups=1)
+    assert _gen(workspace=0x10000, workspace_bytes=need - 1, **kw) == _lib.SS_ERR_INVALID_ARG
+    assert "workspace" in ss.ss_last_error()
+    assert _gen(workspace=0x10008, workspace_bytes=need, **kw) == _lib.SS_ERR_INVALID_ARG
+    assert "workspace" in ss.ss_last_error()
 
 
 def _ssd(**kw):

@@ -122,7 +122,7 @@ def test_general_errors_and_empty():
     y = torch.empty(1, 4, 8, device="cuda")
     for N, G, disc, code in [(48, 2, 0, ss._lib.SS_ERR_UNSUPPORTED), (32, 3, 0, ss._lib.SS_ERR_INVALID_ARG),
                              (32, 2, 2, ss._lib.SS_ERR_UNSUPPORTED), (32, 0, 0, ss._lib.SS_ERR_INVALID_ARG)]:
-        st = lib.ss_scan_fwd_general(*args(N, G, disc), y.data_ptr(), None, None)
+        st = lib.ss_scan_fwd_general(*args(N, G, disc), y.data_ptr(), None, None, 0, None)
         assert st == code, (N, G, disc, st, ss.ss_last_error())
     # L = 0: h_last = h0
     e = {k: d[k][:, :0].contiguous() for k in ("u", "delta_raw", "z", "B", "C")}
@@ -132,3 +132,74 @@ def test_general_errors_and_empty():
     torch.cuda.synchronize()
     assert torch.equal(hl, d["h0"])
     np.testing.assert_array_equal(hl.cpu().numpy(), x["h0"].numpy())
+
+
+# (in_dtype, batch, L, D, N, G, disc, share length in steps): the CTA kernel's
+# 32-step tiles of all channel blocks cut into contiguous shares, one per CTA,
+# the state handed on through the workspace where a share starts inside a
+# block's sequence. One-tile shares make chains of hand-overs; shares of 3 and
+# 13 tiles start and end inside sequences and cross block ends, so a CTA runs
+# the next block's head before the tail it takes over; 20-tile shares hold two
+# whole blocks
+GEN_SPLITS = [("f32", 2, 200, 64, 128, 2, "first_order", 32), ("bf16", 2, 300, 128, 64, 1, "zoh", 96),
+              ("bf16", 3, 300, 128, 32, 2, "zoh", 416), ("bf16", 3, 300, 128, 32, 2, "first_order", 640),
+              ("f32", 1, 333, 64, 64, 1, "zoh", 96)]
+
+
+@pytest.mark.parametrize("case", GEN_SPLITS, ids=[f"{c[0]}-b{c[1]}-L{c[2]}-D{c[3]}-N{c[4]}-G{c[5]}-{c[6]}-share{c[7]}"
+                                                  for c in GEN_SPLITS])
+def test_general_split_shares(case):
+    dt, Bt, L, Dm, N, G, disc, share = case
+    x = gen.random_general_inputs(Bt, L, Dm, N, G, in_dtype=dt, seed=L + share, with_h0=True)
+    yr, hr = oracle.scan_general(x, G, "zoh" if disc == "zoh" else "euler")
+    in_dt = BF16 if dt == "bf16" else F32
+    ss.ss_scan_set_tuning(0, share, 0)
+    try:
+        for out in (F32, BF16):
+            y, h = _run(x, disc, out)
+            ss.ss_scan_status(None)
+            assert_close(y, yr, in_dt, out_bf16=(out == BF16), what=f"split general y {case}")
+            assert_close(h, hr, in_dt, what=f"split general h_last {case}")
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+
+
+def test_general_more_blocks_than_slots():
+    # 8 x 160 blocks of 32 channels at d_state 64 outnumber the resident CTAs:
+    # the automatic plan gives every slot an equal share of the 5120 tiles,
+    # with hand-overs between CTAs; every output checked
+    x = gen.random_general_inputs(8, 100, 5120, 64, 1, in_dtype="bf16", seed=1280, with_h0=True)
+    yr, hr = oracle.scan_general(x, 1, "zoh")
+    y, h = _run(x, "zoh", BF16)
+    ss.ss_scan_status(None)
+    assert_close(y, yr, BF16, out_bf16=True, what="general y, 1280 blocks")
+    assert_close(h, hr, BF16, what="general h_last, 1280 blocks")
+
+
+def test_general_withheld_hand_over_times_out():
+    # shares of two tiles: share 0 (block 0, tiles 0-1) never hands its state
+    # on, so the shares after it in that block give up after the short limit,
+    # the call finishes, the status reports the timeout once, and a clean call
+    # is correct again
+    x = gen.random_general_inputs(1, 300, 64, 64, 1, in_dtype="bf16", seed=43, with_h0=True)
+    d = to_dev(x)
+    ss.ss_scan_set_tuning(0, 64, 0)
+    try:
+        ss.ss_scan_set_wait_limit(2_000_000, 0)
+        try:
+            ss.ss_scan_fwd_general(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                                   d["h0"], disc="zoh", out_dtype=F32)
+        finally:
+            ss.ss_scan_set_wait_limit(0, -1)
+        torch.cuda.synchronize()
+        with pytest.raises(ss.SSError) as ei:
+            ss.ss_scan_status(None)
+        assert ei.value.status == ss._lib.SS_ERR_TIMEOUT
+        ss.ss_scan_status(None)
+        y, h = _run(x, "zoh", F32)
+        ss.ss_scan_status(None)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+    yr, hr = oracle.scan_general(x, 1, "zoh")
+    assert_close(y, yr, BF16, what="general y after a timed-out hand-over")
+    assert_close(h, hr, BF16, what="general h_last after a timed-out hand-over")
