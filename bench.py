@@ -813,12 +813,14 @@ def profile_launches(args):
         x = to_dev(gen.random_ssd_inputs(4, 2048, 80, 64, 128, 1, in_dtype="bf16", seed=11), dev)
         for _ in range(2):
             ss.ss_ssd_fwd(x["x"], x["dt"], x["A"], x["B"], x["C"], x["D"], x["dt_bias"], None)
-    elif args.profile == "general":
+    elif args.profile in ("general", "general128"):
+        # d_state 64, one group, zero-order hold; or d_state 128, 8 groups, first order
+        N, G, disc = (64, 1, "zoh") if args.profile == "general" else (128, 8, "first_order")
         w = configs.get_config(args.workload)
-        x = to_dev(gen.random_general_inputs(w.batch, w.seqlen, w.dim, 64, 1, in_dtype="bf16", seed=65), dev)
+        x = to_dev(gen.random_general_inputs(w.batch, w.seqlen, w.dim, N, G, in_dtype="bf16", seed=N + 1), dev)
         for _ in range(2):
             ss.ss_scan_fwd_general(x["u"], x["delta_raw"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
-                                   None, disc="zoh")
+                                   None, disc=disc)
     elif args.profile == "bwd":
         w = configs.get_config(args.workload)
         x = to_dev(gen.make_scan_inputs(w), dev)
@@ -852,7 +854,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general", "ssd", "conv1d"], default=None,
+    ap.add_argument("--profile", choices=["scan", "decode", "bwd", "general", "general128", "ssd", "conv1d"],
+                    default=None,
                     help="run 2 launches of one kernel (for an ncu capture of the 2nd) and exit")
     args = ap.parse_args()
     if args.profile:
