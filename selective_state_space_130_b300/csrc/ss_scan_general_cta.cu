@@ -305,8 +305,12 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
           const float dlk = __shfl_sync(0xffffffffu, dl, src);
           const float xuk = __shfl_sync(0xffffffffu, xu, src);
           const f2 dl2 = pk(dlk, dlk);
-          [[maybe_unused]] const f2 du2 = pk(dlk * xuk, dlk * xuk);
+          const float duk = dlk * xuk;
+          [[maybe_unused]] const f2 du2 = pk(duk, duk);
           [[maybe_unused]] const f2 xu2 = pk(xuk, xuk);
+          // the zero-order hold's series coefficients times delta u (once per token)
+          [[maybe_unused]] const f2 s1 = pk(duk * kPhi1, duk * kPhi1), s2 = pk(duk * kPhi2, duk * kPhi2),
+                                   s3 = pk(duk * kPhi3, duk * kPhi3);
           const float4* Bp = reinterpret_cast<const float4*>(Bt + (g + kk) * N) + j;  // quad j, then + SG per step
           const float4* Cp = reinterpret_cast<const float4*>(Ct + (g + kk) * N) + j;
           f2 y0 = pk(0.f, 0.f), y1 = pk(0.f, 0.f);
@@ -324,13 +328,13 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
                 // Bbar u = (Abar - 1) / A * u = delta u phi(x), x = delta A, phi(x)
                 // = (e^x - 1) / x. Below |x| = 1/32, delta u times phi's series
                 // 1 + x/2 + x^2/6 + x^3/24 (truncation under x^4/120, a relative
-                // 1e-8), written in e2 = x log2 e; above it (Abar - 1) u / A,
-                // whose Abar from the MUFU exponential then has a relative error
-                // below 1e-5 of Abar - 1. A = 0 gives x = 0: delta u.
-                f2 ph = fma2(e2, pk(kPhi3, kPhi3), pk(kPhi2, kPhi2));
-                ph = fma2(e2, ph, pk(kPhi1, kPhi1));
-                ph = fma2(e2, ph, pk(1.f, 1.f));
-                const f2 bs = mul2(du2, ph);
+                // 1e-8), written in e2 = x log2 e, its coefficients already
+                // times delta u; above it (Abar - 1) u / A, whose Abar from the
+                // MUFU exponential then has a relative error below 1e-5 of
+                // Abar - 1. A = 0 gives x = 0: delta u.
+                f2 bs = fma2(e2, s3, s2);
+                bs = fma2(e2, bs, s1);
+                bs = fma2(e2, bs, du2);
                 const f2 be = mul2(add2(a, pk(-1.f, -1.f)), mul2(invA[q], xu2));
                 const f2 bu = pk(fabsf(f2lo(e2)) < kZohSeries ? f2lo(bs) : f2lo(be),
                                  fabsf(f2hi(e2)) < kZohSeries ? f2hi(bs) : f2hi(be));
