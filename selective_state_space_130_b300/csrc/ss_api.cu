@@ -312,6 +312,15 @@ ss_status scan_common(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
 
 }  // namespace
 
+// The backward's workspace with `sg` lanes per channel: the checkpoints, then
+// (from a 256-byte boundary) the hand-over area of a split over warps.
+static size_t bwd_checkpoint_span(int64_t batch, int64_t seqlen, int64_t dim, int sg) {
+  return (ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim, sg) + 255) / 256 * 256;
+}
+static size_t bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int sg) {
+  return bwd_checkpoint_span(batch, seqlen, dim, sg) + ssk::scan_bwd_handover_bytes(batch, dim, sg);
+}
+
 namespace ssk {
 // CTAs (contiguous ranges of the sequences' chunks) for the tcgen05 kernel
 // with a workspace. A CTA fills an SM (its shared and tensor memory), so CTAs
@@ -479,8 +488,7 @@ ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width, ss_dtype i
 
 size_t ss_scan_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
   if (batch <= 0 || seqlen <= 0 || dim <= 0 || dstate != ssk::kDState) return 0;
-  return std::max(ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim, 1),
-                  ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim, 2));
+  return std::max(bwd_workspace_bytes(batch, seqlen, dim, 1), bwd_workspace_bytes(batch, seqlen, dim, 2));
 }
 
 ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, ss_dtype in_dtype,
@@ -513,7 +521,7 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   for (int i = 0; i < 21; i++)
     if (all[i] && !aligned16(all[i])) return fail(SS_ERR_INVALID_ARG, "%s is not 16-byte aligned", all_names[i]);
   const int sg = bwd_lanes_per_channel(batch, dim);
-  const size_t need_ws = seqlen > 0 ? ssk::scan_bwd_checkpoint_bytes(batch, seqlen, dim, sg) : 0;
+  const size_t need_ws = seqlen > 0 ? bwd_workspace_bytes(batch, seqlen, dim, sg) : 0;
   if (need_ws > 0 && (!workspace || workspace_bytes < need_ws))
     return fail(SS_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu%s)", need_ws, workspace_bytes,
                 workspace ? "" : ", NULL");
@@ -562,6 +570,22 @@ ss_status ss_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   p.ncblk = (int)((dim + 32 / sg - 1) / (32 / sg));
   p.nsub = ssk::scan_bwd_subtiles(seqlen);
   if ((double)batch * p.ncblk > 2.0e9) return fail(SS_ERR_INVALID_ARG, "grid too large");
+  {
+    const int64_t blocks = batch * (int64_t)p.ncblk;
+    uint8_t* w = static_cast<uint8_t*>(workspace) + bwd_checkpoint_span(batch, seqlen, dim, sg);
+    const size_t fb = (size_t)((blocks * 4 + 255) / 256 * 256);
+    p.flags_h = reinterpret_cast<unsigned int*>(w);
+    p.flags_lam = reinterpret_cast<unsigned int*>(w + fb);
+    p.ws_h = reinterpret_cast<float*>(w + 2 * fb);
+    p.ws_lam = p.ws_h + blocks * 32 * ssk::kDState;
+    p.fault = ssk::device_fault_word();
+    p.wait_ns = g_wait_ns;
+    p.withhold_share = g_withhold;
+    // chunk_len > 0: shares of that many steps (whole 16-step sub-tiles)
+    const int64_t rt = g_tune_chunk > 0 ? std::max<int64_t>(1, (g_tune_chunk + 15) / 16) : 0;
+    p.force_shares = rt > 0 ? (blocks * p.nsub + rt - 1) / rt : 0;
+    if (!p.fault) return fail(SS_ERR_CUDA, "cannot resolve the library fault word");
+  }
   e = ssk::launch_scan_bwd(p, sg, in_dtype, dy_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "scan backward launch");
   return SS_OK;

@@ -111,6 +111,21 @@ struct BwdParams {
   int64_t batch, seqlen, dim;
   int ncblk;                // channel blocks (32 / sg channels) per batch element
   int64_t nsub;             // recomputed sub-tiles per block
+  // Work split: the (block, sub-tile) items of all blocks, block-major, cut
+  // into `nshares` contiguous shares, one per warp. Where a share starts
+  // inside a block, the state entering it comes from the share before (through
+  // ws_h / flags_h = the sub-tile of the cut), and the adjoint leaving it goes
+  // back (through ws_lam / flags_lam = nsub - that sub-tile). nshares equal to
+  // the number of blocks: one warp per block, no hand-over.
+  int64_t nshares;
+  unsigned int* flags_h;    // [blocks], zeroed before the launch
+  unsigned int* flags_lam;  // [blocks], zeroed before the launch
+  float* ws_h;              // [blocks, 512]
+  float* ws_lam;            // [blocks, 512]
+  unsigned int* fault;      // the library's fault word (timed-out waits)
+  uint64_t wait_ns;         // limit of a device-side wait; 0 = the default
+  int64_t withhold_share;   // test knob: this share publishes no hand-over (-1: none)
+  int64_t force_shares;     // > 0: this many shares instead of the automatic plan (needs the slots)
 };
 
 // Parameters of the generalised scan (state size 16-128, grouped B/C, ZOH).
@@ -229,6 +244,7 @@ cudaError_t launch_conv1d_update(const ConvParams& p, ss_dtype in_dtype, ss_dtyp
 cudaError_t launch_scan_bwd(const BwdParams& p, int sg, ss_dtype in_dtype, ss_dtype dy_dtype, cudaStream_t stream);
 size_t scan_bwd_checkpoint_bytes(int64_t batch, int64_t seqlen, int64_t dim, int sg);
 int64_t scan_bwd_subtiles(int64_t seqlen);
+size_t scan_bwd_handover_bytes(int64_t batch, int64_t dim, int sg);
 
 // sg = dstate / 16 lanes per channel; bytes of one staged 16-step sub-tile
 cudaError_t launch_scan_general(const GenParams& p, int sg, ss_dtype in_dtype, ss_dtype out_dtype,

@@ -153,9 +153,17 @@ def test_scan_bwd_rejects_bad_arguments(kw, code, msg):
 
 def test_scan_bwd_workspace_and_empty():
     assert _bwd(batch=0) == _lib.SS_OK
-    # the saved states: 2 KB per 32 channels per 16 steps (either lane layout)
-    assert ss.ss_scan_bwd_workspace_size(1, 16, 32) == 2048
-    assert ss.ss_scan_bwd_workspace_size(4, 2048, 5120) == 4 * 160 * 128 * 2048
+    # the saved states, 2 KB per 32 channels per 16 steps (either lane layout),
+    # padded to 256 bytes; then the hand-over area of a split over warps: two
+    # flags per block of 16 channels (two lanes per channel, the larger case),
+    # each array padded to 256 bytes, and two 2 KB slots per block
+    def size(batch, seqlen, dim):
+        blocks = batch * dim // 16
+        ckpt = batch * dim // 32 * ((seqlen + 15) // 16) * 2048
+        return (ckpt + 255) // 256 * 256 + 2 * ((blocks * 4 + 255) // 256 * 256) + 2 * blocks * 2048
+    assert ss.ss_scan_bwd_workspace_size(1, 16, 32) == size(1, 16, 32) == 2048 + 512 + 8192
+    assert ss.ss_scan_bwd_workspace_size(4, 2048, 5120) == size(4, 2048, 5120)
+    assert size(4, 2048, 5120) == 4 * 160 * 128 * 2048 + 2 * 5120 + 2 * 1280 * 2048
     assert ss.ss_scan_bwd_workspace_size(1, 16, 32, 8) == 0
 
 

@@ -223,3 +223,67 @@ def test_scan_bwd_empty_and_errors():
                        outs["dA"].data_ptr(), outs["dB"].data_ptr(), outs["dC"].data_ptr(), None, None, None,
                        ws.data_ptr(), ws.numel(), None)
     assert st == ss._lib.SS_ERR_UNSUPPORTED
+
+
+def _run_bwd_shares(x, dy, dh_last, sg, share):
+    ss.ss_scan_set_tuning(sg, share, 0)
+    try:
+        return _run_bwd_tuned(x, dy, dh_last)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+
+
+def _run_bwd_tuned(x, dy, dh_last):
+    d = to_dev(x)
+    g = ss.ss_scan_bwd(d["u"], d["delta_raw"], d["A"], d["B"], d["C"], dy.cuda(), d.get("D"), d.get("z"),
+                       d.get("delta_bias"), d.get("h0"), dh_last.cuda() if dh_last is not None else None)
+    torch.cuda.synchronize()
+    return g
+
+
+# (in_dtype, batch, L, D, sg, share length in steps): the blocks' 16-step
+# sub-tiles cut into contiguous shares, one per warp. Where a share starts
+# inside a block, the state comes from the share before and the adjoint goes
+# back to it. One-sub-tile shares make chains of hand-overs both ways; shares
+# of 3 and 7 sub-tiles cross block ends (a warp runs the next block's forward
+# sweep first and its reverse sweep last); 400-step shares hold whole blocks
+BWD_SPLITS = [("f32", 2, 300, 64, 2, 16), ("bf16", 2, 300, 64, 2, 48), ("f32", 3, 200, 96, 1, 112),
+              ("bf16", 1, 1000, 64, 1, 400), ("bf16", 2, 333, 130, 2, 48)]
+
+
+@pytest.mark.parametrize("case", BWD_SPLITS, ids=[f"{c[0]}-b{c[1]}-L{c[2]}-D{c[3]}-sg{c[4]}-share{c[5]}"
+                                                  for c in BWD_SPLITS])
+def test_scan_bwd_split_shares(case):
+    dt, Bt, L, Dm, sg, share = case
+    in_dt = BF16 if dt == "bf16" else F32
+    x = gen.random_scan_inputs(Bt, L, Dm, 16, in_dtype=dt, seed=L + share, with_h0=True, a_log_jitter=0.3)
+    dy, dh = gen.random_output_grads(Bt, L, Dm, 16, dt, seed=L + Dm)
+    ref = oracle.scan_bwd(x, dy, dh)
+    g = _run_bwd_shares(x, dy, dh, sg, share)
+    ss.ss_scan_status(None)
+    _compare(g, ref, in_dt, True, f"bwd split {case}")
+
+
+def test_scan_bwd_withheld_hand_over_times_out():
+    # shares of two sub-tiles: share 0 (block 0, sub-tiles 0-1) hands nothing
+    # on, so the share after it gives up waiting for its state (and share 0
+    # for the adjoint it would have got back); the call finishes, the status
+    # reports the timeout once, and a clean call is correct again
+    x = gen.random_scan_inputs(1, 200, 32, 16, in_dtype="f32", seed=44, with_h0=True)
+    dy, dh = gen.random_output_grads(1, 200, 32, 16, "f32", seed=45)
+    ss.ss_scan_set_tuning(2, 32, 0)
+    try:
+        ss.ss_scan_set_wait_limit(2_000_000, 0)
+        try:
+            _run_bwd_tuned(x, dy, dh)
+        finally:
+            ss.ss_scan_set_wait_limit(0, -1)
+        with pytest.raises(ss.SSError) as ei:
+            ss.ss_scan_status(None)
+        assert ei.value.status == ss._lib.SS_ERR_TIMEOUT
+        ss.ss_scan_status(None)
+        g = _run_bwd_tuned(x, dy, dh)
+        ss.ss_scan_status(None)
+    finally:
+        ss.ss_scan_set_tuning(0, 0, 0)
+    _compare(g, oracle.scan_bwd(x, dy, dh), F32, True, "bwd after a timed-out hand-over")
