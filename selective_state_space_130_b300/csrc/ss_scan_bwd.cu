@@ -51,7 +51,14 @@ struct BwdLayout {
   static constexpr int OFF_C = OFF_B + kSub * BC_ROW;
   static constexpr int STAGE = OFF_C + kSub * BC_ROW;
   static constexpr int HIST = (kSub + 1) * NQ * 32 * 16;  // one 16-byte entry per (slot, quad, lane)
-  static constexpr int SMEM = HIST + 2 * STAGE;
+  // the current sub-tile's B and C widened to fp32 (bf16 inputs; fp32 ones are
+  // read from the stage), and its delta = softplus(delta_raw + bias) per step
+  // and channel, each computed once per sub-tile
+  static constexpr bool WIDEN = sizeof(TIn) == 2;
+  static constexpr int OFF_WB = HIST + 2 * STAGE;
+  static constexpr int OFF_WC = OFF_WB + (WIDEN ? kSub * kDState * 4 : 0);
+  static constexpr int OFF_DL = OFF_WC + (WIDEN ? kSub * kDState * 4 : 0);
+  static constexpr int SMEM = OFF_DL + kSub * CW * 4;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -201,6 +208,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
   int nch = 0;
   f2 A2[NP];
   float bias_d = 0.f, D_d = 0.f;
+  float bias_p = 0.f;  // bias of channel lane % CW, whose deltas this lane computes in prep
   auto set_block = [&](int64_t u) {
     b = u / p.ncblk;
     c0 = (u % p.ncblk) * CW;
@@ -216,6 +224,8 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
     }
     bias_d = (dv && p.delta_bias) ? __ldg(p.delta_bias + dc) : 0.f;
     D_d = (dv && p.D) ? __ldg(p.D + dc) : 0.f;
+    const int64_t dp = c0 + lane % CW;
+    bias_p = (dp < Dm && p.delta_bias) ? __ldg(p.delta_bias + dp) : 0.f;
   };
   // stage sub-tile s of the current block into buffer s & 1: the forward sweep
   // needs u, delta_raw, B; the reverse sweep everything
@@ -246,6 +256,55 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
 #pragma unroll
     for (int j = 0; j < NP; j++) o[j] = pk(f[2 * j], f[2 * j + 1]);
   };
+  float* wB = reinterpret_cast<float*>(smem_raw + LY::OFF_WB);
+  float* wC = reinterpret_cast<float*>(smem_raw + LY::OFF_WC);
+  float* dlt = reinterpret_cast<float*>(smem_raw + LY::OFF_DL);  // [kSub][CW]
+  // Once sub-tile data has landed in `buf`: its B (and C) widened to fp32, and
+  // delta for every (step, channel), lane l taking channel l % CW. Read after
+  // the next __syncwarp.
+  auto prep = [&](const uint8_t* buf, int ns, bool with_c) {
+    if constexpr (LY::WIDEN) {  // kSub x 16 bf16 = 512 bytes: one 16-byte piece per lane
+#pragma unroll
+      for (int which = 0; which < 2; which++) {
+        if (which == 1 && !with_c) break;
+        const uint4 w = reinterpret_cast<const uint4*>(buf + (which ? LY::OFF_C : LY::OFF_B))[lane];
+        float4* o = reinterpret_cast<float4*>((which ? wC : wB) + 8 * lane);
+        o[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+        o[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                           __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+      }
+    }
+    const int cp = lane % CW;
+#pragma unroll
+    for (int tt = lane / CW; tt < kSub; tt += 32 / CW)
+      if (tt < ns) dlt[tt * CW + cp] = softplus_fast(sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, cp) + bias_p);
+  };
+  // this lane's B or C pairs of step tt of the current sub-tile
+  auto rowB = [&](const uint8_t* buf, int tt, f2 (&o)[NP]) {
+    if constexpr (LY::WIDEN) {
+#pragma unroll
+      for (int qq = 0; qq < NS / 4; qq++) {
+        const float4 v = reinterpret_cast<const float4*>(wB + tt * kDState + soff)[qq];
+        o[2 * qq] = pk(v.x, v.y);
+        o[2 * qq + 1] = pk(v.z, v.w);
+      }
+    } else {
+      row_pairs(buf, LY::OFF_B, tt, o);
+    }
+  };
+  auto rowC = [&](const uint8_t* buf, int tt, f2 (&o)[NP]) {
+    if constexpr (LY::WIDEN) {
+#pragma unroll
+      for (int qq = 0; qq < NS / 4; qq++) {
+        const float4 v = reinterpret_cast<const float4*>(wC + tt * kDState + soff)[qq];
+        o[2 * qq] = pk(v.x, v.y);
+        o[2 * qq + 1] = pk(v.z, v.w);
+      }
+    } else {
+      row_pairs(buf, LY::OFF_C, tt, o);
+    }
+  };
   // this lane's 2 NP floats of a hand-over slot ([block][32 lanes][16])
   auto slot = [&](float* base, int64_t u) { return base + (u * 32 + lane) * kDState; };
 
@@ -274,20 +333,22 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
       else cp_async_commit();
       cp_async_wait1();
       __syncwarp();
+      const uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
+      const int ns = (int)min((int64_t)kSub, L - s * kSub);
+      prep(buf, ns, false);
       {
         ulonglong2* dst = ck + (size_t)s * NQ * 32;
 #pragma unroll
         for (int qq = 0; qq < NQ; qq++) dst[qq * 32 + lane] = make_ulonglong2(h[2 * qq], h[2 * qq + 1]);
       }
-      const uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
-      const int ns = (int)min((int64_t)kSub, L - s * kSub);
+      __syncwarp();
 #pragma unroll 2
       for (int tt = 0; tt < ns; tt++) {
         const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
-        const float dl = softplus_fast(sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, ch) + bias_d);
+        const float dl = dlt[tt * CW + ch];
         const f2 dl2 = pk(dl, dl), du2 = pk(dl * xu, dl * xu);
         f2 Bv[NP];
-        row_pairs(buf, LY::OFF_B, tt, Bv);
+        rowB(buf, tt, Bv);
 #pragma unroll
         for (int j = 0; j < NP; j++) h[j] = fma2(abar2(dl2, A2[j]), h[j], mul2(du2, Bv[j]));
       }
@@ -354,16 +415,18 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
       cp_async_wait1();
       __syncwarp();
       const uint8_t* buf = stage_buf + (s & 1) * LY::STAGE;
+      prep(buf, ns, true);
+      __syncwarp();
       // recompute the sub-tile's states into shared memory (lane-private slots); dz
 #pragma unroll 2
       for (int tt = 0; tt < ns; tt++) {
         const int64_t i = (b * L + t0 + tt) * Dm + dc;
         const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
-        const float dl = softplus_fast(sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, ch) + bias_d);
+        const float dl = dlt[tt * CW + ch];
         const f2 dl2 = pk(dl, dl), du2 = pk(dl * xu, dl * xu);
         f2 Bv[NP], Cv[NP];
-        row_pairs(buf, LY::OFF_B, tt, Bv);
-        row_pairs(buf, LY::OFF_C, tt, Cv);
+        rowB(buf, tt, Bv);
+        rowC(buf, tt, Cv);
         f2 y0 = pk(0.f, 0.f), y1 = pk(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < NP; j++) {
@@ -389,13 +452,13 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
         const int64_t t = t0 + tt;
         const float xu = sm_elem<TIn>(buf + LY::OFF_U + tt * LY::IN_ROW, ch);
         const float xr = sm_elem<TIn>(buf + LY::OFF_DR + tt * LY::IN_ROW, ch) + bias_d;
-        const float dl = softplus_fast(xr);
+        const float dl = dlt[tt * CW + ch];
         float dyv = sm_elem<TDy>(buf + LY::OFF_DY + tt * LY::DY_ROW, ch);
         if constexpr (HAS_Z) dyv *= silu(sm_elem<TIn>(buf + LY::OFF_Z + tt * LY::IN_ROW, ch));
         const f2 dl2 = pk(dl, dl), dyv2 = pk(dyv, dyv), dlu2 = pk(dl * xu, dl * xu);
         f2 Bv[NP], Cv[NP];
-        row_pairs(buf, LY::OFF_B, tt, Bv);
-        row_pairs(buf, LY::OFF_C, tt, Cv);
+        rowB(buf, tt, Bv);
+        rowC(buf, tt, Cv);
         f2 vB[NP], vC[NP];  // this lane's terms of dB and dC for its states
         f2 dub0 = pk(0.f, 0.f), dub1 = pk(0.f, 0.f), dda0 = pk(0.f, 0.f), dda1 = pk(0.f, 0.f);
         const ulonglong2* hc = hist + (tt + 1) * NQ * 32 + lane;
