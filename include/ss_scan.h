@@ -204,8 +204,19 @@ ss_status ss_conv1d_update(int64_t batch, int64_t dim, int64_t width,
  *  dD, ddelta_bias: [dim] float32 or NULL (not computed)
  *  dh0            : [batch, dim, dstate] float32 or NULL (not computed)
  *  workspace      : device buffer of at least ss_scan_bwd_workspace_size() bytes
- *                   (the states saved every 16 steps); must not be shared by
- *                   calls that overlap on the GPU.
+ *                   (the states saved every 16 steps, then the hand-over area
+ *                   of a split); must not be shared by calls that overlap on
+ *                   the GPU.
+ * Work split. One warp runs one block of 32 / (lanes per channel) channels
+ * over the whole sequence. With more blocks than resident warps, every warp
+ * takes an equal contiguous share of all blocks' 16-step sub-tiles instead:
+ * where a share cuts a block, the forward state is handed on and the adjoint
+ * handed back through the workspace. Those hand-overs need every warp resident
+ * at once, so that launch is cooperative; where the device refuses it, the
+ * call falls back to one warp per block. A hand-over that does not arrive
+ * within the wait limit (ss_scan_set_wait_limit) ends the waiting warps and
+ * is reported by ss_scan_status(NULL, stream) as SS_ERR_TIMEOUT; the outputs
+ * are then undefined.
  * The sums over channels and time are accumulated with float32 atomic adds,
  * so dA, dB, dC, dD and ddelta_bias can differ in the last bits from run to
  * run; the other outputs are deterministic. seqlen == 0 writes dh0 = dh_last
@@ -350,11 +361,12 @@ size_t ss_ssd_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, 
  * cross-CTA carry path. max_workers > 0 caps the number of CTAs a split of the
  * work uses (default: one per SM), which makes range boundaries and hand-overs
  * more frequent. Results do not depend on these settings beyond fp32 rounding;
- * ss_scan_fwd_workspace_size() follows them. For ss_ssd_fwd and
- * ss_scan_fwd_general (with a workspace) chunk_len > 0 sets the length of the
- * CTAs' shares (rounded up to 128 steps for ss_ssd_fwd, 32 for the generalised
- * scan's CTA kernel) instead of the automatic plan, so that shares start inside
- * sequences even on small problems.
+ * ss_scan_fwd_workspace_size() follows them. For ss_ssd_fwd, ss_scan_fwd_general
+ * (with a workspace) and ss_scan_bwd, chunk_len > 0 sets the length of the
+ * shares (rounded up to 128 steps for ss_ssd_fwd, 32 for the generalised
+ * scan's CTA kernel, 16 for the backward) instead of the automatic plan, so
+ * that shares start inside sequences even on small problems; threads_per_channel
+ * also sets the backward's lanes per channel.
  */
 void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_workers);
 
@@ -368,9 +380,9 @@ void ss_scan_set_tuning(int threads_per_channel, int64_t chunk_len, int max_work
  * split; -1 (the default) publishes all. A withheld flag makes the CTAs that
  * need it give up after wait_ns, set the fault word and return, so the call
  * finishes and ss_scan_status() reports SS_ERR_TIMEOUT; its outputs are then
- * undefined. No wait in the library is unbounded. They apply to ss_ssd_fwd
- * and ss_scan_fwd_general too: there withhold_item is the share (the shares in
- * sequence order, numbered from 0) whose state is never handed on.
+ * undefined. No wait in the library is unbounded. They apply to ss_ssd_fwd,
+ * ss_scan_fwd_general and ss_scan_bwd too: there withhold_item is the share
+ * (the shares in sequence order, numbered from 0) that hands nothing on.
  */
 void ss_scan_set_wait_limit(uint64_t wait_ns, int64_t withhold_item);
 
