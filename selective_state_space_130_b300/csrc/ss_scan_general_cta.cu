@@ -38,7 +38,7 @@ constexpr int kCW = 4;                   // warps per CTA
 constexpr int kCThreads = 32 * kCW;
 constexpr int kTile = 32;                // steps per tile
 
-template <typename TIn, int N>
+template <typename TIn, int N, bool ZOH>
 struct GCfg {
   static constexpr int SG = N / 16;        // lanes per channel
   static constexpr int DC = 32 / SG;       // channels per warp
@@ -48,9 +48,18 @@ struct GCfg {
   static constexpr int RB = kTile * N * ES;     // one raw B or C tile
   static constexpr int OFF_U = 0, OFF_DR = XB, OFF_Z = 2 * XB, OFF_B = 3 * XB, OFF_C = 3 * XB + RB;
   static constexpr int STAGE = 3 * XB + 2 * RB;
-  static constexpr int RING = (ES == 2 && N <= 64) ? 3 : 2;  // stages (three CTAs per SM fit in shared memory)
-  static constexpr int OFF_W = RING * STAGE;    // widened B then C, fp32 [kTile][N] each
-  static constexpr int WB = kTile * N * 4;
+  static constexpr int RING = (ES == 2 && N <= 64) ? 3 : 2;  // stages (three or four CTAs per SM fit in shared memory)
+  // bf16 rows of d_state 128 with the first-order rule are read from the
+  // stage as they are, each lane widening its quads, instead of through a
+  // widened fp32 copy: without the copy's 32 KB a fourth CTA fits on an SM,
+  // which this latency-bound case needs more than it needs the fewer
+  // instructions (1.68 -> 1.41 ms on the layer shape). The zero-order hold is
+  // issue-bound, and the widening in its token loop made it slower (2.45 ->
+  // 2.64 ms at d_state 128, 1.30 -> 1.43 ms at 64).
+  static constexpr bool RAW = ES == 2 && N == 128 && !ZOH;
+  static constexpr int CTAS = RAW ? 4 : 3;      // resident CTAs per SM the kernel is built for
+  static constexpr int OFF_W = RING * STAGE;    // widened B then C, fp32 [kTile][N] each (none when RAW)
+  static constexpr int WB = RAW ? 0 : kTile * N * 4;
   static constexpr int OFF_BAR = OFF_W + 2 * WB;  // full[RING]
   static constexpr int OFF_RANGE = OFF_BAR + RING * 8;  // the CTA's share and thread 0's load cursor (GRange)
   static constexpr int SMEM = OFF_RANGE + 64;
@@ -106,13 +115,13 @@ constexpr float kPhi3 = 0.013876027166205394f;
 constexpr float kZohSeries = 0.045084220027780106f;  // (1/32) log2(e)
 
 template <typename TIn, typename TOut, int N, bool ZOH>
-__global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __grid_constant__ GenParams p,
+__global__ void __launch_bounds__(kCThreads, GCfg<TIn, N, ZOH>::CTAS) scan_general_cta_kernel(const __grid_constant__ GenParams p,
                                                                     const __grid_constant__ CUtensorMap tm_u,
                                                                     const __grid_constant__ CUtensorMap tm_dr,
                                                                     const __grid_constant__ CUtensorMap tm_z,
                                                                     const __grid_constant__ CUtensorMap tm_b,
                                                                     const __grid_constant__ CUtensorMap tm_c) {
-  using K = GCfg<TIn, N>;
+  using K = GCfg<TIn, N, ZOH>;
   constexpr int SG = K::SG, DC = K::DC, CC = K::CC;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
@@ -269,7 +278,10 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
       if (tid == 0) issue_next();  // into the stage the previous tile used
       const float* Bt;
       const float* Ct;
-      if constexpr (K::ES == 2) {  // widen the tile's B and C once, each thread a slice
+      if constexpr (K::RAW) {  // (unused: the token loop reads the stage)
+        Bt = reinterpret_cast<const float*>(st);
+        Ct = reinterpret_cast<const float*>(st);
+      } else if constexpr (K::ES == 2) {  // widen the tile's B and C once, each thread a slice
         const uint4* rb = reinterpret_cast<const uint4*>(st + K::OFF_B);
         const uint4* rc = reinterpret_cast<const uint4*>(st + K::OFF_C);
         for (int i = tid; i < kTile * N / 8; i += kCW * 32) {
@@ -316,7 +328,19 @@ __global__ void __launch_bounds__(kCThreads, 3) scan_general_cta_kernel(const __
           f2 y0 = pk(0.f, 0.f), y1 = pk(0.f, 0.f);
 #pragma unroll
           for (int q4 = 0; q4 < 4; q4++) {
-            const float4 bq = Bp[SG * q4], cq = Cp[SG * q4];
+            float4 bq, cq;
+            if constexpr (K::RAW) {  // quad j + SG q4 of the raw bf16 rows
+              const int e = ((g + kk) * N + 4 * (j + SG * q4)) * 2;
+              const uint2 rb = *reinterpret_cast<const uint2*>(st + K::OFF_B + e);
+              const uint2 rc = *reinterpret_cast<const uint2*>(st + K::OFF_C + e);
+              bq = make_float4(__uint_as_float(rb.x << 16), __uint_as_float(rb.x & 0xffff0000u),
+                               __uint_as_float(rb.y << 16), __uint_as_float(rb.y & 0xffff0000u));
+              cq = make_float4(__uint_as_float(rc.x << 16), __uint_as_float(rc.x & 0xffff0000u),
+                               __uint_as_float(rc.y << 16), __uint_as_float(rc.y & 0xffff0000u));
+            } else {
+              bq = Bp[SG * q4];
+              cq = Cp[SG * q4];
+            }
             const f2 bv[2] = {pk(bq.x, bq.y), pk(bq.z, bq.w)};
             const f2 cv[2] = {pk(cq.x, cq.y), pk(cq.z, cq.w)};
 #pragma unroll
@@ -437,9 +461,9 @@ bool gmap(CUtensorMap* m, const void* ptr, int es, int rank, const uint64_t* dim
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename TIn, typename TOut, int N>
+template <typename TIn, typename TOut, int N, bool ZOH>
 cudaError_t launch_gcta(const GenParams& p, cudaStream_t s) {
-  using K = GCfg<TIn, N>;
+  using K = GCfg<TIn, N, ZOH>;
   CUtensorMap mu{}, mdr{}, mz{}, mb{}, mc{};
   const uint64_t L = (uint64_t)p.seqlen, Bt = (uint64_t)p.batch, Dm = (uint64_t)p.dim, G = (uint64_t)p.ngroups;
   const uint64_t dx[3] = {Dm, L, Bt};
@@ -450,7 +474,7 @@ cudaError_t launch_gcta(const GenParams& p, cudaStream_t s) {
       (p.z && !gmap(&mz, p.z, K::ES, 3, dx, bxx)) || !gmap(&mb, p.B, K::ES, 4, dbc, bbc) ||
       !gmap(&mc, p.C, K::ES, 4, dbc, bbc))
     return cudaErrorInvalidValue;
-  auto k = p.disc == 1 ? scan_general_cta_kernel<TIn, TOut, N, true> : scan_general_cta_kernel<TIn, TOut, N, false>;
+  auto k = scan_general_cta_kernel<TIn, TOut, N, ZOH>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
   if (e != cudaSuccess) return e;
   // Shares: with a workspace and more units than CTA slots (resident CTAs per
@@ -489,9 +513,10 @@ cudaError_t launch_gcta(const GenParams& p, cudaStream_t s) {
 
 template <typename TIn, typename TOut>
 cudaError_t launch_gcta_n(const GenParams& p, int64_t dstate, cudaStream_t s) {
-  if (dstate == 32) return launch_gcta<TIn, TOut, 32>(p, s);
-  if (dstate == 64) return launch_gcta<TIn, TOut, 64>(p, s);
-  return launch_gcta<TIn, TOut, 128>(p, s);
+  const bool zoh = p.disc == 1;
+  if (dstate == 32) return zoh ? launch_gcta<TIn, TOut, 32, true>(p, s) : launch_gcta<TIn, TOut, 32, false>(p, s);
+  if (dstate == 64) return zoh ? launch_gcta<TIn, TOut, 64, true>(p, s) : launch_gcta<TIn, TOut, 64, false>(p, s);
+  return zoh ? launch_gcta<TIn, TOut, 128, true>(p, s) : launch_gcta<TIn, TOut, 128, false>(p, s);
 }
 
 }  // namespace

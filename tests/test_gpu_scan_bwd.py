@@ -287,3 +287,15 @@ def test_scan_bwd_withheld_hand_over_times_out():
     finally:
         ss.ss_scan_set_tuning(0, 0, 0)
     _compare(g, oracle.scan_bwd(x, dy, dh), F32, True, "bwd after a timed-out hand-over")
+
+
+def test_scan_bwd_shares_beyond_resident_warps_fall_back():
+    # one-sub-tile shares of 64 blocks x 32 sub-tiles = 2048 shares, more than
+    # the resident warps a cooperative launch allows: the call runs one warp
+    # per block instead, with the same gradients
+    x = gen.random_scan_inputs(1, 512, 1024, 16, in_dtype="bf16", seed=46, with_h0=True)
+    dy, dh = gen.random_output_grads(1, 512, 1024, 16, "bf16", seed=47)
+    ref = oracle.scan_bwd(x, dy, dh)
+    g = _run_bwd_shares(x, dy, dh, 2, 16)
+    ss.ss_scan_status(None)
+    _compare(g, ref, BF16, True, "bwd, shares past the resident warps")
