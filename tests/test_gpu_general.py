@@ -164,16 +164,24 @@ def test_general_split_shares(case):
         ss.ss_scan_set_tuning(0, 0, 0)
 
 
-def test_general_more_blocks_than_slots():
-    # 8 x 160 blocks of 32 channels at d_state 64 outnumber the resident CTAs:
-    # the automatic plan gives every slot an equal share of the 5120 tiles,
+# (batch, L, D, N, G, disc): more channel blocks than resident CTAs. 8 x 160
+# blocks of 32 channels at d_state 64 (ZOH, three CTAs per SM); 2 x 320 blocks
+# of 16 channels at d_state 128 with the first-order rule (raw bf16 rows, four
+# CTAs per SM)
+MANY_BLOCKS = [(8, 100, 5120, 64, 1, "zoh"), (2, 300, 5120, 128, 8, "first_order")]
+
+
+@pytest.mark.parametrize("case", MANY_BLOCKS, ids=[f"b{c[0]}-L{c[1]}-N{c[3]}-G{c[4]}-{c[5]}" for c in MANY_BLOCKS])
+def test_general_more_blocks_than_slots(case):
+    # the automatic plan gives every slot an equal share of all blocks' tiles,
     # with hand-overs between CTAs; every output checked
-    x = gen.random_general_inputs(8, 100, 5120, 64, 1, in_dtype="bf16", seed=1280, with_h0=True)
-    yr, hr = oracle.scan_general(x, 1, "zoh")
-    y, h = _run(x, "zoh", BF16)
+    Bt, L, Dm, N, G, disc = case
+    x = gen.random_general_inputs(Bt, L, Dm, N, G, in_dtype="bf16", seed=Bt * Dm // 32 + N, with_h0=True)
+    yr, hr = oracle.scan_general(x, G, "zoh" if disc == "zoh" else "euler")
+    y, h = _run(x, disc, BF16)
     ss.ss_scan_status(None)
-    assert_close(y, yr, BF16, out_bf16=True, what="general y, 1280 blocks")
-    assert_close(h, hr, BF16, what="general h_last, 1280 blocks")
+    assert_close(y, yr, BF16, out_bf16=True, what=f"general y {case}")
+    assert_close(h, hr, BF16, what=f"general h_last {case}")
 
 
 def test_general_withheld_hand_over_times_out():
