@@ -149,6 +149,45 @@ def random_scan_inputs(batch, seqlen, dim, dstate, in_dtype="f32", seed=0, delta
     return x
 
 
+S_SYMTAB = 15  # symbol-table inputs: tables, then symbols, per tensor
+
+
+def symbol_scan_inputs(batch, seqlen, dim, dstate=16, nsym=16, seed=5):
+    """Inputs too large to draw value by value (more than 2^32 elements per
+    [batch, seqlen, dim] tensor), in the style of the DNA workload's alphabet:
+    u, delta_raw and z are each a table of `nsym` rows ~ N(0,1) over the
+    channels, bf16, indexed by a symbol per (b, t) drawn uniformly from
+    {0 .. nsym-1}; tensor[b, t, d] = table[sym[b, t], d]. B and C [batch,
+    seqlen, dstate] ~ N(0,1) bf16 are drawn in full. A, D and delta_bias follow
+    the layer recipe (A_log = log(n + 1), dt log-uniform in [1e-3, 1e-1]).
+    Returns {"tables": {k: [nsym, dim]}, "symbols": {k: [batch, seqlen] int64}
+    for k in u, delta_raw, z; "B", "C", "A", "D", "delta_bias"}; expand a
+    tensor with gather_symbols."""
+    w = ScanWorkload("symbols", batch, seqlen, dim, dstate, "bf16", seed, 1.0, 0.0)
+    A, Dskip, bias = make_params(w)
+    tables, symbols = {}, {}
+    for i, k in enumerate(("u", "delta_raw", "z")):
+        tables[k] = _store(randn_blocks(nsym * dim, seed, S_SYMTAB + 2 * i).view(nsym, dim), "bf16").contiguous()
+        g = torch.Generator().manual_seed(_block_seed(seed, S_SYMTAB + 2 * i + 1, 0))
+        symbols[k] = torch.randint(0, nsym, (batch, seqlen), generator=g)
+    n = batch * seqlen * dstate
+    return {
+        "tables": tables,
+        "symbols": symbols,
+        "B": _store(randn_blocks(n, seed, S_B).view(batch, seqlen, dstate), "bf16").contiguous(),
+        "C": _store(randn_blocks(n, seed, S_C).view(batch, seqlen, dstate), "bf16").contiguous(),
+        "A": A,
+        "D": Dskip,
+        "delta_bias": bias,
+    }
+
+
+def gather_symbols(table: torch.Tensor, symbols: torch.Tensor) -> torch.Tensor:
+    """table[symbols]: [*symbols.shape, table.shape[1]], contiguous, on the
+    tensors' device (a plain index copy, no arithmetic on the values)."""
+    return table[symbols].contiguous()
+
+
 def random_conv_inputs(batch, seqlen, dim, width, in_dtype="bf16", seed=0, with_state=False, has_bias=True):
     """Inputs of the causal depthwise convolution front-end:
     x [batch, seqlen, dim] ~ N(0,1) in `in_dtype`; weight [dim, width] ~
