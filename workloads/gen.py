@@ -149,27 +149,37 @@ def random_scan_inputs(batch, seqlen, dim, dstate, in_dtype="f32", seed=0, delta
     return x
 
 
-S_SYMTAB = 15  # symbol-table inputs: tables, then symbols, per tensor
+S_SYMTAB = 15  # symbol-table inputs: stream S_SYMTAB + 2 i (table) and + 2 i + 1 (symbols) for tensor i
+
+
+def symbol_tensor(index_shape, row_shape, seed, slot, nsym=16, dtype="bf16", scale=1.0):
+    """A tensor too large to draw value by value, as a table and its symbols:
+    table [nsym, *row_shape] ~ scale * N(0,1) in `dtype`, symbols [*index_shape]
+    uniform over {0 .. nsym-1}; the tensor is gather_symbols(table, symbols)
+    [*index_shape, *row_shape]. `slot` picks the tensor's pair of streams."""
+    rows = 1
+    for r in row_shape:
+        rows *= r
+    table = _store(scale * randn_blocks(nsym * rows, seed, S_SYMTAB + 2 * slot).view(nsym, *row_shape), dtype)
+    g = torch.Generator().manual_seed(_block_seed(seed, S_SYMTAB + 2 * slot + 1, 0))
+    symbols = torch.randint(0, nsym, tuple(index_shape), generator=g)
+    return table.contiguous(), symbols
 
 
 def symbol_scan_inputs(batch, seqlen, dim, dstate=16, nsym=16, seed=5):
     """Inputs too large to draw value by value (more than 2^32 elements per
     [batch, seqlen, dim] tensor), in the style of the DNA workload's alphabet:
     u, delta_raw and z are each a table of `nsym` rows ~ N(0,1) over the
-    channels, bf16, indexed by a symbol per (b, t) drawn uniformly from
-    {0 .. nsym-1}; tensor[b, t, d] = table[sym[b, t], d]. B and C [batch,
-    seqlen, dstate] ~ N(0,1) bf16 are drawn in full. A, D and delta_bias follow
-    the layer recipe (A_log = log(n + 1), dt log-uniform in [1e-3, 1e-1]).
-    Returns {"tables": {k: [nsym, dim]}, "symbols": {k: [batch, seqlen] int64}
-    for k in u, delta_raw, z; "B", "C", "A", "D", "delta_bias"}; expand a
-    tensor with gather_symbols."""
+    channels, bf16, indexed by a symbol per (b, t) (symbol_tensor). B and C
+    [batch, seqlen, dstate] ~ N(0,1) bf16 are drawn in full. A, D and
+    delta_bias follow the layer recipe (A_log = log(n + 1), dt log-uniform in
+    [1e-3, 1e-1]). Returns {"tables": {k: [nsym, dim]}, "symbols": {k: [batch,
+    seqlen] int64} for k in u, delta_raw, z; "B", "C", "A", "D", "delta_bias"}."""
     w = ScanWorkload("symbols", batch, seqlen, dim, dstate, "bf16", seed, 1.0, 0.0)
     A, Dskip, bias = make_params(w)
     tables, symbols = {}, {}
     for i, k in enumerate(("u", "delta_raw", "z")):
-        tables[k] = _store(randn_blocks(nsym * dim, seed, S_SYMTAB + 2 * i).view(nsym, dim), "bf16").contiguous()
-        g = torch.Generator().manual_seed(_block_seed(seed, S_SYMTAB + 2 * i + 1, 0))
-        symbols[k] = torch.randint(0, nsym, (batch, seqlen), generator=g)
+        tables[k], symbols[k] = symbol_tensor((batch, seqlen), (dim,), seed, i, nsym)
     n = batch * seqlen * dstate
     return {
         "tables": tables,
