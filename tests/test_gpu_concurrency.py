@@ -6,10 +6,9 @@ one another (stream-K and look-back hand-overs, persistent shares with tickets)
 running beside each other on the same SMs. Every such wait is on a CTA that has
 already started, so the kernels make progress whatever else is resident.
 
-The backward pass is left out: its cooperative launch needs all its CTAs
-resident at once, which a concurrent kernel on another stream can prevent (it
-then falls back to a launch without shares, which is correct but is a
-different split)."""
+The backward pass is left out: its cooperative launch needs all of its CTAs
+resident at once, so it does not share the SMs with kernels on other streams
+the way these do."""
 
 import threading
 
