@@ -106,7 +106,7 @@ def test_threads_on_separate_streams_match_serial_calls():
     reps = 3
     results = [None] * len(probs)
     errors = []
-    barrier = threading.Barrier(len(probs))
+    barrier = threading.Barrier(len(probs), timeout=60)
 
     def worker(i):
         try:
@@ -123,7 +123,7 @@ def test_threads_on_separate_streams_match_serial_calls():
         except Exception as e:  # reported below, with the problem's name
             errors.append(f"{probs[i][0]}: {e!r}")
 
-    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(probs))]
+    threads = [threading.Thread(target=worker, args=(i,), daemon=True) for i in range(len(probs))]
     for t in threads:
         t.start()
     for t in threads:
