@@ -220,13 +220,32 @@ def bench_scan(ss, w, x, steps, warmup, out_dtype, dev, nsets=None):
                 launches_per_step=1)
 
 
-def prime_queue():
-    """Open a timed region behind a short device-side spin (2 M cycles, about
-    1 ms). While it runs the host queues the first timed launches, so their
+def prime_queue(cycles=2_000_000):
+    """Open a timed region behind a device-side spin (by default 2 M cycles,
+    about 1 ms). While it runs the host queues the timed launches, so their
     launch latency is not counted as GPU time; every timed step's work still
     runs inside the region. (With the GPU idle at the start event, the first
     call of a batch measured 420-510 us against 224 us for the rest.)"""
-    torch.cuda._sleep(2_000_000)
+    torch.cuda._sleep(int(cycles))
+
+
+def spin_for(call, reps, probe=5):
+    """Spin cycles that cover the host's submission of `reps` timed calls: the
+    host time of one call with its two event records, measured on `probe`
+    calls queued behind a spin, times reps, with margin. A kernel shorter than
+    its host call (the convolution front-end: about 35 us on the device
+    against 50-90 us on the host) would otherwise drain the queue after the
+    default spin, and the later intervals would hold host time."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(probe)]
+    torch.cuda._sleep(20_000_000)
+    t = time.perf_counter()
+    for i in range(probe):
+        ev[i][0].record()
+        call(i)
+        ev[i][1].record()
+    host_s = (time.perf_counter() - t) / probe
+    torch.cuda.synchronize()
+    return max(2_000_000, min(int(1.5 * reps * host_s * 2.1e9), 400_000_000))
 
 
 def run_timed(ss, st, steps):
@@ -391,8 +410,9 @@ def bench_conv1d(ss, dev, hbm_peak, Bt=4, L=2048, Dm=5120, K=4, reps=20):
     for i in range(3):
         call(i)
     torch.cuda.synchronize()
+    spin = spin_for(call, reps)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    prime_queue()
+    prime_queue(spin)
     for i in range(reps):
         ev[i][0].record()
         call(i)
@@ -562,8 +582,9 @@ def bench_ssd(ss, dev, hbm_peak, tensor_peak, Bt=4, L=2048, H=80, N=128, G=1, re
     for _ in range(3):
         call()
     torch.cuda.synchronize()
+    spin = spin_for(lambda i: call(), reps)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    prime_queue()
+    prime_queue(spin)
     for i in range(reps):
         ev[i][0].record()
         call()
