@@ -237,7 +237,7 @@ def spin_for(call, reps, probe=5):
     against 50-90 us on the host) would otherwise drain the queue after the
     default spin, and the later intervals would hold host time."""
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(probe)]
-    torch.cuda._sleep(20_000_000)
+    torch.cuda._sleep(4_000_000)  # about 2 ms: the probe calls queue behind it
     t = time.perf_counter()
     for i in range(probe):
         ev[i][0].record()
