@@ -67,33 +67,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
-// NS consecutive elements as float (this lane's part of a B or C row in shared
-// memory; 16-byte aligned)
-template <typename T, int NS>
-__device__ __forceinline__ void row_part(const uint8_t* p, float (&o)[NS]) {
-  if constexpr (sizeof(T) == 4) {
-#pragma unroll
-    for (int q = 0; q < NS / 4; q++) {
-      const float4 v = reinterpret_cast<const float4*>(p)[q];
-      o[4 * q] = v.x;
-      o[4 * q + 1] = v.y;
-      o[4 * q + 2] = v.z;
-      o[4 * q + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < NS / 8; q++) {
-      const uint4 v = reinterpret_cast<const uint4*>(p)[q];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; k++) {
-        o[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
-        o[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-      }
-    }
-  }
-}
-
 template <typename T>
 __device__ __forceinline__ float sm_elem(const uint8_t* row, int i) {
   return to_f32(reinterpret_cast<const T*>(row)[i]);
@@ -129,16 +102,6 @@ __device__ __forceinline__ void stage_rows(uint8_t* dst, const void* base, int64
   }
 }
 
-// lo/hi of f2 pairs as a flat list of floats
-template <int NP>
-__device__ __forceinline__ void unpack(const f2 (&x)[NP], float* o) {
-#pragma unroll
-  for (int j = 0; j < NP; j++) {
-    o[2 * j] = f2lo(x[j]);
-    o[2 * j + 1] = f2hi(x[j]);
-  }
-}
-
 // Abar for a pair of states: 2^(delta * A2)
 __device__ __forceinline__ f2 abar2(f2 dl2, f2 a2) {
   const f2 e = mul2(dl2, a2);
@@ -162,6 +125,18 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
   const int ch = lane / SG;           // channel within the block
   const int soff = (lane % SG) * NS;  // first state of this lane
   const bool owner = (lane % SG) == 0;
+  // The lane's state pairs in a lane-dependent order: position j holds pair
+  // j ^ gp. gp is made of the lane bits over which the first stages of the
+  // dB/dC reduction below run (16 and 8, and 4 with one lane per channel), so
+  // that in those stages two partners hold the same element at positions e
+  // and e + w, and every lane keeps its lower half without a select.
+  constexpr int kPairBits = NP == 8 ? 3 : 2;
+  static_assert(NP == 8 || NP == 4, "one or two lanes per channel");
+  int gp = 0;
+#pragma unroll
+  for (int i = 0; i < kPairBits; i++) gp |= ((lane >> (4 - i)) & 1) << (kPairBits - 1 - i);
+  // first state of the pair at position j
+  auto sidx = [&](int j) { return soff + 2 * (j ^ gp); };
   const int64_t L = p.seqlen, Dm = p.dim, nsub = p.nsub;
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
 
@@ -218,8 +193,8 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
     nch = (int)min((int64_t)CW, Dm - c0);
 #pragma unroll
     for (int j = 0; j < NP; j++) {
-      const float a0 = dv ? __ldg(p.A + dc * kDState + soff + 2 * j) : 0.f;
-      const float a1 = dv ? __ldg(p.A + dc * kDState + soff + 2 * j + 1) : 0.f;
+      const float a0 = dv ? __ldg(p.A + dc * kDState + sidx(j)) : 0.f;
+      const float a1 = dv ? __ldg(p.A + dc * kDState + sidx(j) + 1) : 0.f;
       A2[j] = pk(a0 * kLog2e, a1 * kLog2e);
     }
     bias_d = (dv && p.delta_bias) ? __ldg(p.delta_bias + dc) : 0.f;
@@ -251,10 +226,14 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
   };
   // this lane's B or C pairs of step tt of a staged buffer
   auto row_pairs = [&](const uint8_t* buf, int off, int tt, f2 (&o)[NP]) {
-    float f[NS];
-    row_part<TIn, NS>(buf + off + tt * LY::BC_ROW + soff * (int)sizeof(TIn), f);
+    if constexpr (sizeof(TIn) == 4) {  // (bf16 rows are read widened, from wB and wC)
+      const float* r = reinterpret_cast<const float*>(buf + off + tt * LY::BC_ROW);
 #pragma unroll
-    for (int j = 0; j < NP; j++) o[j] = pk(f[2 * j], f[2 * j + 1]);
+      for (int j = 0; j < NP; j++) {
+        const float2 v = *reinterpret_cast<const float2*>(r + sidx(j));
+        o[j] = pk(v.x, v.y);
+      }
+    }
   };
   float* wB = reinterpret_cast<float*>(smem_raw + LY::OFF_WB);
   float* wC = reinterpret_cast<float*>(smem_raw + LY::OFF_WC);
@@ -284,10 +263,9 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
   auto rowB = [&](const uint8_t* buf, int tt, f2 (&o)[NP]) {
     if constexpr (LY::WIDEN) {
 #pragma unroll
-      for (int qq = 0; qq < NS / 4; qq++) {
-        const float4 v = reinterpret_cast<const float4*>(wB + tt * kDState + soff)[qq];
-        o[2 * qq] = pk(v.x, v.y);
-        o[2 * qq + 1] = pk(v.z, v.w);
+      for (int j = 0; j < NP; j++) {
+        const float2 v = *reinterpret_cast<const float2*>(wB + tt * kDState + sidx(j));
+        o[j] = pk(v.x, v.y);
       }
     } else {
       row_pairs(buf, LY::OFF_B, tt, o);
@@ -296,10 +274,9 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
   auto rowC = [&](const uint8_t* buf, int tt, f2 (&o)[NP]) {
     if constexpr (LY::WIDEN) {
 #pragma unroll
-      for (int qq = 0; qq < NS / 4; qq++) {
-        const float4 v = reinterpret_cast<const float4*>(wC + tt * kDState + soff)[qq];
-        o[2 * qq] = pk(v.x, v.y);
-        o[2 * qq + 1] = pk(v.z, v.w);
+      for (int j = 0; j < NP; j++) {
+        const float2 v = *reinterpret_cast<const float2*>(wC + tt * kDState + sidx(j));
+        o[j] = pk(v.x, v.y);
       }
     } else {
       row_pairs(buf, LY::OFF_C, tt, o);
@@ -312,7 +289,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
   // start of every sub-tile; the state leaving a head goes to the next share
   auto fwd_job = [&](const Seg& q) {
     f2 h[NP];
-    const int64_t hrow = (b * Dm + dc) * kDState + soff;
+    const int64_t hrow = (b * Dm + dc) * kDState;
     if (q.sb > 0) {
       if (!wait_flag(p.flags_h + q.u, (uint32_t)q.sb)) {
         aborted = true;
@@ -324,7 +301,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
     } else {
 #pragma unroll
       for (int j = 0; j < NP; j++)
-        h[j] = (dv && p.h0) ? pk(__ldg(p.h0 + hrow + 2 * j), __ldg(p.h0 + hrow + 2 * j + 1)) : pk(0.f, 0.f);
+        h[j] = (dv && p.h0) ? pk(__ldg(p.h0 + hrow + sidx(j)), __ldg(p.h0 + hrow + sidx(j) + 1)) : pk(0.f, 0.f);
     }
     ulonglong2* ck = reinterpret_cast<ulonglong2*>(p.ckpt) + (size_t)q.u * nsub * NQ * 32;
     stage(q.sb, false);
@@ -372,7 +349,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
   // goes back to the share that holds the block's start.
   auto rev_job = [&](const Seg& q) {
     f2 lam[NP], dAacc[NP];
-    const int64_t hrow = (b * Dm + dc) * kDState + soff;
+    const int64_t hrow = (b * Dm + dc) * kDState;
     if (q.se < nsub) {
       if (!wait_flag(p.flags_lam + q.u, (uint32_t)(nsub - q.se))) {
         aborted = true;
@@ -384,7 +361,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
     } else {
 #pragma unroll
       for (int j = 0; j < NP; j++)
-        lam[j] = (dv && p.dh_last) ? pk(__ldg(p.dh_last + hrow + 2 * j), __ldg(p.dh_last + hrow + 2 * j + 1))
+        lam[j] = (dv && p.dh_last) ? pk(__ldg(p.dh_last + hrow + sidx(j)), __ldg(p.dh_last + hrow + sidx(j) + 1))
                                    : pk(0.f, 0.f);
     }
 #pragma unroll
@@ -499,13 +476,29 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
         const int64_t i = (b * L + t) * Dm + dc;
         st_out(static_cast<TIn*>(p.du) + i, fmaf(dyv, D_d, dl * dub), dv && owner);
         st_out(static_cast<TIn*>(p.ddelta_raw) + i, dxr, dv && owner);
-        // sum over the warp's channels (lanes with the same lane % SG); after
-        // the stages lane l holds element (l / SG) of its v = [dB terms, dC terms]
+        // Sum over the warp's channels (lanes with the same lane % SG). Element
+        // 4 j + 2 k + c is the dB (c = 0) or dC (c = 1) term of state 2 j + k
+        // of the lane's pair j; position 4 j + 2 k + c of v holds the element
+        // of pair j ^ gp. At each stage (mask m, width w) a lane keeps w values
+        // and adds its partner's other w. In the stages over the pair bits the
+        // partners' orders differ exactly by w, so every lane keeps the lower
+        // half; the last two stages (the bits of k and c) select. After them
+        // lane l holds element l / SG.
         float v[2 * NS];
-        unpack<NP>(vB, v);
-        unpack<NP>(vC, v + NS);
 #pragma unroll
-        for (int m = 16, w = NS; m >= SG; m >>= 1, w >>= 1) {
+        for (int j = 0; j < NP; j++) {
+          v[4 * j] = f2lo(vB[j]);
+          v[4 * j + 1] = f2lo(vC[j]);
+          v[4 * j + 2] = f2hi(vB[j]);
+          v[4 * j + 3] = f2hi(vC[j]);
+        }
+#pragma unroll
+        for (int m = 16, w = NS; w >= 4; m >>= 1, w >>= 1) {
+#pragma unroll
+          for (int e = 0; e < w; e++) v[e] += __shfl_xor_sync(0xffffffffu, v[e + w], m);
+        }
+#pragma unroll
+        for (int m = 2 * SG, w = 2; m >= SG; m >>= 1, w >>= 1) {
           const bool up = (lane & m) != 0;
 #pragma unroll
           for (int e = 0; e < w; e++) {
@@ -515,8 +508,8 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
           }
         }
         const int e = ch;  // 0 .. 2NS-1
-        float* row = (e < NS ? p.dB : p.dC) + (b * L + t) * kDState + soff;
-        atomicAdd(row + (e < NS ? e : e - NS), v[0]);
+        float* row = ((e & 1) ? p.dC : p.dB) + (b * L + t) * kDState + soff;
+        atomicAdd(row + (e >> 1), v[0]);
       }
       __syncwarp();  // buffer s & 1 is refilled next iteration
     }
@@ -526,8 +519,8 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
       if (dv && p.dh0) {
 #pragma unroll
         for (int j = 0; j < NP; j++) {
-          p.dh0[(b * Dm + d) * kDState + soff + 2 * j] = f2lo(lam[j]);
-          p.dh0[(b * Dm + d) * kDState + soff + 2 * j + 1] = f2hi(lam[j]);
+          p.dh0[(b * Dm + d) * kDState + sidx(j)] = f2lo(lam[j]);
+          p.dh0[(b * Dm + d) * kDState + sidx(j) + 1] = f2hi(lam[j]);
         }
       }
     } else {
@@ -544,8 +537,8 @@ __global__ void __launch_bounds__(32 * kBwdWarps) scan_bwd_kernel(const __grid_c
     if (dv) {
 #pragma unroll
       for (int j = 0; j < NP; j++) {
-        atomicAdd(p.dA + d * kDState + soff + 2 * j, f2lo(dAacc[j]));
-        atomicAdd(p.dA + d * kDState + soff + 2 * j + 1, f2hi(dAacc[j]));
+        atomicAdd(p.dA + d * kDState + sidx(j), f2lo(dAacc[j]));
+        atomicAdd(p.dA + d * kDState + sidx(j) + 1, f2hi(dAacc[j]));
       }
       if (owner) {
         if (p.dD) atomicAdd(p.dD + d, dDacc);
