@@ -245,7 +245,7 @@ def spin_for(call, reps, probe=5):
         ev[i][1].record()
     host_s = (time.perf_counter() - t) / probe
     torch.cuda.synchronize()
-    return max(2_000_000, min(int(1.5 * reps * host_s * 2.1e9), 400_000_000))
+    return max(2_000_000, min(int(1.5 * reps * host_s * 2.1e9), 40_000_000))
 
 
 def run_timed(ss, st, steps):
