@@ -423,14 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1) scan_fwd_kernel(const __grid_cons
         // software-pipelined groups of eight tokens: the loop body computes
         // the next group's scalars (a long softplus -> ex2 chain) next to the
         // current group's state updates, so the two overlap in one basic
-        // block; the last group recomputes its own scalars instead of reading
-        // past the tile
+        // block; the last group, with no next group in the tile, runs after
+        // the loop on its own
         PairScalars cur0 = scalars_pair(0), cur1 = scalars_pair(2), cur2 = scalars_pair(4), cur3 = scalars_pair(6);
 #pragma unroll 1
-        for (int tt = 0; tt < TILE; tt += 8) {
-          const int tn = min(tt + 8, TILE - 8);
-          const PairScalars nx0 = scalars_pair(tn), nx1 = scalars_pair(tn + 2), nx2 = scalars_pair(tn + 4),
-                            nx3 = scalars_pair(tn + 6);
+        for (int tt = 0; tt < TILE - 8; tt += 8) {
+          const PairScalars nx0 = scalars_pair(tt + 8), nx1 = scalars_pair(tt + 10), nx2 = scalars_pair(tt + 12),
+                            nx3 = scalars_pair(tt + 14);
           update_pair(tt, cur0);
           update_pair(tt + 2, cur1);
           update_pair(tt + 4, cur2);
@@ -440,6 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1) scan_fwd_kernel(const __grid_cons
           cur2 = nx2;
           cur3 = nx3;
         }
+        update_pair(TILE - 8, cur0);
+        update_pair(TILE - 6, cur1);
+        update_pair(TILE - 4, cur2);
+        update_pair(TILE - 2, cur3);
       } else {
 #pragma unroll 1
         for (int tt = 0; tt < tlen; tt++) token(tt);
