@@ -481,16 +481,19 @@ __global__ void __launch_bounds__(kThreads, 1) scan_fwd_kernel(const __grid_cons
         if constexpr (MODE == kModeChunked) ssum += dl;
       };
       if (tlen == TILE) {
+        // as with one lane per channel: the tile's last eight tokens run after
+        // the pipelined loop, which computes scalars only for a group that follows
         PairScalars cur0 = scalars_pair(2 * s), cur1 = scalars_pair(4 + 2 * s);
 #pragma unroll 1
-        for (int tt = 0; tt < TILE; tt += 8) {
-          const int tn = min(tt + 8, TILE - 8);
-          const PairScalars nx0 = scalars_pair(tn + 2 * s), nx1 = scalars_pair(tn + 4 + 2 * s);
+        for (int tt = 0; tt < TILE - 8; tt += 8) {
+          const PairScalars nx0 = scalars_pair(tt + 8 + 2 * s), nx1 = scalars_pair(tt + 12 + 2 * s);
           group(tt, cur0);
           group(tt + 4, cur1);
           cur0 = nx0;
           cur1 = nx1;
         }
+        group(TILE - 8, cur0);
+        group(TILE - 4, cur1);
       } else {
 #pragma unroll 1
         for (int tt = 0; tt < tlen; tt++) token(tt);
