@@ -249,44 +249,18 @@ __device__ __forceinline__ float bits_f32(uint32_t bits) {
   return sizeof(T) == 4 ? __uint_as_float(bits) : __uint_as_float(bits << 16);
 }
 
-template <typename TIn, typename TOut, int K, int V, bool SILU>
+template <typename TIn, typename TOut, int K, int V, bool SILU, int BS>
 __global__ void __launch_bounds__(kConvThreads) conv1d_update_kernel(const __grid_constant__ ConvParams p) {
-  // V consecutive channels per thread: their states (V x H elements) are
-  // contiguous, so state, x and y move as whole 16-byte vectors when V > 1
+  // V consecutive channels of BS consecutive streams per thread: the V
+  // channels' states (V x H elements) are contiguous, so state, x and y move
+  // as whole 16-byte vectors when V > 1; the taps and biases, loaded once, serve
+  // all BS streams. (With V > 1, dim is a multiple of V.)
   constexpr int H = K - 1;
   const int64_t g = (int64_t)blockIdx.x * kConvThreads + threadIdx.x;
-  const int64_t c0 = g * V;  // first channel (flattened over batch x dim)
-  if (c0 >= p.batch * p.dim) return;
-  const int64_t d0 = c0 % p.dim;
-  TIn* st = static_cast<TIn*>(p.state_out) + c0 * H;
-  const TIn* gx = static_cast<const TIn*>(p.x) + c0;
-  constexpr int SW = (int)((V * H * sizeof(TIn) + 3) / 4), XW = (int)((V * sizeof(TIn) + 3) / 4);
-  uint32_t sw[SW], xw[XW];
-  if constexpr (V > 1) {
-#pragma unroll
-    for (int i = 0; i < SW / 4; i++) {
-      const uint4 q = reinterpret_cast<const uint4*>(st)[i];
-      sw[4 * i] = q.x;
-      sw[4 * i + 1] = q.y;
-      sw[4 * i + 2] = q.z;
-      sw[4 * i + 3] = q.w;
-    }
-#pragma unroll
-    for (int i = 0; i < XW / 4; i++) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(gx) + i);
-      xw[4 * i] = q.x;
-      xw[4 * i + 1] = q.y;
-      xw[4 * i + 2] = q.z;
-      xw[4 * i + 3] = q.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < SW; i++) sw[i] = 0u;
-    xw[0] = 0u;
-#pragma unroll
-    for (int k = 0; k < H; k++) set_word_elem<TIn>(sw, k, sizeof(TIn) == 4 ? __float_as_uint(to_f32(st[k])) : (uint32_t)__bfloat16_as_ushort(*reinterpret_cast<const __nv_bfloat16*>(st + k)));
-    set_word_elem<TIn>(xw, 0, sizeof(TIn) == 4 ? __float_as_uint(to_f32(gx[0])) : (uint32_t)__bfloat16_as_ushort(*reinterpret_cast<const __nv_bfloat16*>(gx)));
-  }
+  const int64_t ncg = (p.dim + V - 1) / V;  // channel groups per stream
+  const int64_t d0 = (g % ncg) * V;          // first channel of the group
+  const int64_t b0 = (g / ncg) * BS;         // first stream
+  if (b0 >= p.batch) return;
   // taps and biases of the V channels: contiguous, 16-byte vectors when V > 1
   float w[V * K], bias[V];
   if constexpr (V > 1) {
@@ -311,35 +285,69 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_update_kernel(const __gri
     for (int k = 0; k < K; k++) w[k] = __ldg(p.w + d0 * K + k);
     bias[0] = p.bias ? __ldg(p.bias + d0) : 0.f;
   }
-  float o[V];
+  constexpr int SW = (int)((V * H * sizeof(TIn) + 3) / 4), XW = (int)((V * sizeof(TIn) + 3) / 4);
 #pragma unroll
-  for (int v = 0; v < V; v++) {
-    float acc = bias[v];
+  for (int bs = 0; bs < BS; bs++) {
+    if (b0 + bs >= p.batch) break;
+    const int64_t c0 = (b0 + bs) * p.dim + d0;  // first channel, flattened over batch x dim
+    TIn* st = static_cast<TIn*>(p.state_out) + c0 * H;
+    const TIn* gx = static_cast<const TIn*>(p.x) + c0;
+    uint32_t sw[SW], xw[XW];
+    if constexpr (V > 1) {
 #pragma unroll
-    for (int k = 0; k < H; k++) acc = fmaf(w[v * K + k], bits_f32<TIn>(word_elem<TIn>(sw, v * H + k)), acc);
-    acc = fmaf(w[v * K + H], bits_f32<TIn>(word_elem<TIn>(xw, v)), acc);
-    o[v] = SILU ? silu(acc) : acc;
-  }
-  store_out<TOut, V>(static_cast<TOut*>(p.y) + c0, o);
-  // drop each channel's oldest input, append the new one
-  uint32_t nw[SW];
+      for (int i = 0; i < SW / 4; i++) {
+        const uint4 q = reinterpret_cast<const uint4*>(st)[i];
+        sw[4 * i] = q.x;
+        sw[4 * i + 1] = q.y;
+        sw[4 * i + 2] = q.z;
+        sw[4 * i + 3] = q.w;
+      }
 #pragma unroll
-  for (int i = 0; i < SW; i++) nw[i] = 0u;
+      for (int i = 0; i < XW / 4; i++) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(gx) + i);
+        xw[4 * i] = q.x;
+        xw[4 * i + 1] = q.y;
+        xw[4 * i + 2] = q.z;
+        xw[4 * i + 3] = q.w;
+      }
+    } else {
 #pragma unroll
-  for (int v = 0; v < V; v++) {
+      for (int i = 0; i < SW; i++) sw[i] = 0u;
+      xw[0] = 0u;
 #pragma unroll
-    for (int k = 0; k + 1 < H; k++) set_word_elem<TIn>(nw, v * H + k, word_elem<TIn>(sw, v * H + k + 1));
-    set_word_elem<TIn>(nw, v * H + H - 1, word_elem<TIn>(xw, v));
-  }
-  if constexpr (V > 1) {
+      for (int k = 0; k < H; k++) set_word_elem<TIn>(sw, k, sizeof(TIn) == 4 ? __float_as_uint(to_f32(st[k])) : (uint32_t)__bfloat16_as_ushort(*reinterpret_cast<const __nv_bfloat16*>(st + k)));
+      set_word_elem<TIn>(xw, 0, sizeof(TIn) == 4 ? __float_as_uint(to_f32(gx[0])) : (uint32_t)__bfloat16_as_ushort(*reinterpret_cast<const __nv_bfloat16*>(gx)));
+    }
+    float o[V];
 #pragma unroll
-    for (int i = 0; i < SW / 4; i++) reinterpret_cast<uint4*>(st)[i] = make_uint4(nw[4 * i], nw[4 * i + 1], nw[4 * i + 2], nw[4 * i + 3]);
-  } else {
+    for (int v = 0; v < V; v++) {
+      float acc = bias[v];
 #pragma unroll
-    for (int k = 0; k < H; k++) {
-      const uint32_t bits = word_elem<TIn>(nw, k);
-      if constexpr (sizeof(TIn) == 4) reinterpret_cast<float*>(st)[k] = __uint_as_float(bits);
-      else reinterpret_cast<__nv_bfloat16*>(st)[k] = __ushort_as_bfloat16((unsigned short)bits);
+      for (int k = 0; k < H; k++) acc = fmaf(w[v * K + k], bits_f32<TIn>(word_elem<TIn>(sw, v * H + k)), acc);
+      acc = fmaf(w[v * K + H], bits_f32<TIn>(word_elem<TIn>(xw, v)), acc);
+      o[v] = SILU ? silu(acc) : acc;
+    }
+    store_out<TOut, V>(static_cast<TOut*>(p.y) + c0, o);
+    // drop each channel's oldest input, append the new one
+    uint32_t nw[SW];
+#pragma unroll
+    for (int i = 0; i < SW; i++) nw[i] = 0u;
+#pragma unroll
+    for (int v = 0; v < V; v++) {
+#pragma unroll
+      for (int k = 0; k + 1 < H; k++) set_word_elem<TIn>(nw, v * H + k, word_elem<TIn>(sw, v * H + k + 1));
+      set_word_elem<TIn>(nw, v * H + H - 1, word_elem<TIn>(xw, v));
+    }
+    if constexpr (V > 1) {
+#pragma unroll
+      for (int i = 0; i < SW / 4; i++) reinterpret_cast<uint4*>(st)[i] = make_uint4(nw[4 * i], nw[4 * i + 1], nw[4 * i + 2], nw[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < H; k++) {
+        const uint32_t bits = word_elem<TIn>(nw, k);
+        if constexpr (sizeof(TIn) == 4) reinterpret_cast<float*>(st)[k] = __uint_as_float(bits);
+        else reinterpret_cast<__nv_bfloat16*>(st)[k] = __ushort_as_bfloat16((unsigned short)bits);
+      }
     }
   }
 }
@@ -681,10 +689,11 @@ cudaError_t launch_fwd_io(const ConvParams& p, bool vec, cudaStream_t s) {
 
 template <typename TIn, typename TOut, int K, int V>
 cudaError_t launch_upd_kv(const ConvParams& p, cudaStream_t s) {
-  const int64_t threads = (p.batch * p.dim + V - 1) / V;
+  constexpr int BS = V > 1 ? 4 : 1;  // streams per thread, sharing the loaded taps
+  const int64_t threads = (p.batch + BS - 1) / BS * ((p.dim + V - 1) / V);
   const int64_t blocks = (threads + kConvThreads - 1) / kConvThreads;
-  if (p.silu) conv1d_update_kernel<TIn, TOut, K, V, true><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
-  else conv1d_update_kernel<TIn, TOut, K, V, false><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
+  if (p.silu) conv1d_update_kernel<TIn, TOut, K, V, true, BS><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
+  else conv1d_update_kernel<TIn, TOut, K, V, false, BS><<<(unsigned)blocks, kConvThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
